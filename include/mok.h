@@ -1,0 +1,184 @@
+/*
+ * mok.h — C ABI of a single-GPU, deterministic mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * One call of the layer routes T tokens of width H to k of E experts, runs each expert
+ * (a SwiGLU FFN of intermediate width I) on its tokens, and merges the k expert outputs
+ * of each token with the router's gate weights.  The steps and their order follow the
+ * pages on Mixture-of-Kittens (MoK):
+ *   - "把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源 GPU 内核 MoK" (aientropygate.com),
+ *     §02: router decision -> dispatch -> grouped GEMM -> combine; the schedule step
+ *     counts each expert's tokens, places them and keeps an expert's tokens together;
+ *     §03 ①: the dispatch is a pull (the expert side reads the rows it needs);
+ *     §03 ③: MXFP8 activation quantisation sits on the dispatch / GEMM / SwiGLU path;
+ *     §04: the measured layer ends in a weighted merge.
+ *   - "Mixture-of-Kittens (MoK)" (sd114.wiki), pull-dispatch section: one schedule table
+ *     serves all four transfers; benchmark section: BF16 and MXFP8, router-weight
+ *     gradient computed inside the SwiGLU backward; introduction: fully deterministic.
+ *   - "Cursor Open-Sources Mixture-of-Kittens (MoK) ..." (aitrending.vip),
+ *     "Technical Details": the same, plus the ring token buffer.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current device; the caller owns and
+ *     allocates all memory (inputs, outputs, ctx, ws).  The library never allocates,
+ *     frees or synchronises inside the compute calls; everything is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *   - Row-major layouts, bf16 = IEEE bfloat16 bit patterns (uint16), f32 = IEEE float.
+ *   - Return values report host-side validation only (shapes, alignment, sizes) plus
+ *     launch errors.  Errors found on the device (a bounded wait that ran out, an expert
+ *     index out of range) go to a status word inside `ws`; read it with mok_read_status.
+ *   - Outputs are overwritten, never accumulated.  Results are bitwise reproducible for
+ *     the same inputs, descriptor and device: every reduction runs in a fixed order and
+ *     no floating-point atomics are used.
+ *   - No C++ exception crosses this boundary.  No global mutable state besides a per-device
+ *     cache of the SM count and the driver entry point used to encode TMA descriptors.
+ */
+#ifndef MOK_H_
+#define MOK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = 1,          /* null pointer, bad shape, misaligned pointer */
+  MOK_ERR_UNSUPPORTED = 2,          /* shape outside what the kernels tile (see mok_layer_desc) */
+  MOK_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws/ctx smaller than mok_workspace_size reports */
+  MOK_ERR_CUDA = 4,                 /* a CUDA runtime/driver call or kernel launch failed */
+  MOK_ERR_TIMEOUT = 5,              /* device: a bounded wait ran out (status word only) */
+  MOK_ERR_INVALID_ROUTING = 6       /* device: an expert index outside [0, E) or repeated */
+} mok_status;
+
+typedef enum { MOK_ROUTER_SOFTMAX = 0, MOK_ROUTER_SIGMOID = 1 } mok_router_kind;
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
+
+/* Layer descriptor.
+ *   T       tokens of this call, 1 <= T
+ *   H       hidden width; multiple of 256
+ *   I       expert intermediate width; multiple of 256
+ *   E       routed experts, 1 <= E <= 1024
+ *   k       experts per token, 1 <= k <= min(E, 16)
+ *   router  mok_router_kind: softmax over E logits, or elementwise sigmoid
+ *   renorm  nonzero: the k selected gates are divided by their sum
+ *   route_scale  factor on every gate (1.0 for the workloads here)
+ *   precision    mok_precision of the expert GEMMs
+ *   minibatch    ring forward only: rows per minibatch (0 = the whole call)
+ *   ring_bytes   ring forward only: bytes of the fixed token ring (0 = no ring)
+ *   flags        bit 0: MOK_FLAG_TEST_STUCK_WAIT (tests only, see mok_test_bounded_wait)
+ * T*k*max(H, 2I) must stay below 2^31 elements. */
+typedef struct {
+  int32_t T, H, I, E, k;
+  int32_t router;
+  int32_t renorm;
+  float route_scale;
+  int32_t precision;
+  int32_t minibatch;
+  int64_t ring_bytes;
+  int32_t flags;
+  int32_t reserved;
+} mok_layer_desc;
+
+/* Byte offsets (from the base pointer) of the tensors inside ctx and ws.  ctx holds what
+ * the forward saves for the backward; ws holds temporaries.  An offset of -1 means the
+ * tensor is absent for this descriptor.  Every offset is a multiple of 256. */
+typedef struct {
+  /* ctx */
+  int64_t topk_idx;   /* i32 [T][k]   selected experts, best first (ties -> lower index) */
+  int64_t gates;      /* f32 [T][k]   gate weights */
+  int64_t scores;     /* f32 [T][E]   router scores (softmax probabilities or sigmoids) */
+  int64_t counts;     /* i32 [E]      rows per expert */
+  int64_t offsets;    /* i32 [E+1]    exclusive prefix sum of counts */
+  int64_t row_of;     /* i32 [T*k]    sorted row of assignment a = t*k + j */
+  int64_t src_of;     /* i32 [T*k]    assignment held by sorted row r */
+  int64_t tile_off;   /* i32 [E+1]    prefix sum of ceil(counts/128) (GEMM m-tiles) */
+  int64_t gate_row;   /* f32 [T*k]    gate of each sorted row */
+  int64_t x_g;        /* bf16 [T*k][H]  dispatched (expert-sorted) token rows */
+  int64_t hu;         /* bf16 [T*k][2I] gate and up projections h | u */
+  int64_t ctx_bytes;
+  /* ws */
+  int64_t status;     /* i32 [4]      device status word: code, site */
+  int64_t logits;     /* f32 [T][E]   router logits */
+  int64_t act;        /* bf16 [T*k][I]  SwiGLU output a = silu(h) * u */
+  int64_t expert_out; /* bf16 [T*k][H]  expert outputs o (unweighted) */
+  int64_t dy_g;       /* bf16 [T*k][H]  dispatched upstream gradient (backward) */
+  int64_t dhu;        /* bf16 [T*k][2I] gradient of h | u (backward) */
+  int64_t gact;       /* bf16 [T*k][I]  gate * a, operand of dW2 (backward) */
+  int64_t dx_g;       /* bf16 [T*k][H]  per-row input gradient (backward) */
+  int64_t dg_part;    /* f32 [T*k][I/256] partial gate gradients per GEMM column tile */
+  int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
+  int64_t ws_bytes;
+} mok_layout;
+
+/* Fills *layout (and so the ctx and ws sizes) for a descriptor.  Host only. */
+mok_status mok_get_layout(const mok_layer_desc* desc, mok_layout* layout);
+
+/* Router + schedule table (the "unified schedule table" of the pull-dispatch section of
+ * "Mixture-of-Kittens (MoK)", sd114.wiki; fields and reading as in the layout above).
+ *   x [T][H] bf16, w_router [E][H] bf16, router_bias f32 [E] or NULL (added to the
+ *   selection score only).  given_topk i32 [T][k] or NULL: when non-NULL the selection is
+ *   taken from it (each row k distinct experts in [0, E); a violation is reported as
+ *   MOK_ERR_INVALID_ROUTING in the status word) and the gates are the router scores at
+ *   those experts; x and w_router may then be NULL only if gates are not needed (pass
+ *   gates = NULL too).
+ *   Outputs (i32 unless noted): topk_idx [T][k], gates f32 [T][k] (nullable), counts [E],
+ *   offsets [E+1], row_of [T*k], src_of [T*k].  ws: at least layout.ws_bytes.
+ * The table is exact integer work: rows of an expert are in ascending assignment order. */
+mok_status mok_schedule(const mok_layer_desc* desc, const void* x, const void* w_router,
+                        const float* router_bias, const int32_t* given_topk, int32_t* topk_idx,
+                        float* gates, int32_t* counts, int32_t* offsets, int32_t* row_of,
+                        int32_t* src_of, void* ws, size_t ws_bytes, void* stream);
+
+/* Layer forward: y [T][H] bf16 = sum over the k selected experts of gate * SwiGLU-FFN(x).
+ *   w13 [E][2I][H] bf16 (rows 0..I-1 gate projection, I..2I-1 up projection),
+ *   w2 [E][H][I] bf16, router_bias and given_topk as in mok_schedule.
+ *   ctx (layout.ctx_bytes) receives what the backward needs; ws (layout.ws_bytes) is
+ *   scratch and also holds the status word.  Pointers to x, weights, y, ctx and ws must be
+ *   16-byte aligned (TMA).  MXFP8 is not accepted here (MOK_ERR_UNSUPPORTED). */
+mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void* w_router,
+                           const float* router_bias, const int32_t* given_topk, const void* w13,
+                           const void* w2, void* y, void* ctx, size_t ctx_bytes, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Layer backward for upstream gradient dy [T][H] bf16, using the ctx written by the
+ * matching mok_moe_forward (same desc, inputs and weights).  Outputs:
+ *   dx [T][H] bf16, dw_router [E][H] f32, dw13 [E][2I][H] bf16, dw2 [E][H][I] bf16,
+ *   dgates [T][k] f32 (nullable): gradient w.r.t. each selected gate.
+ * The selection is held fixed; the router bias gets no gradient.  The gate gradient
+ * <dA', a> of each row is formed in the SwiGLU-backward epilogue (the router-weight
+ * gradient "fused into the SwiGLU backward" of the pages' benchmark section). */
+mok_status mok_moe_backward(const mok_layer_desc* desc, const void* dy, const void* x,
+                            const void* w_router, const void* w13, const void* w2,
+                            const void* ctx, size_t ctx_bytes, void* dx, float* dw_router,
+                            void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* Synchronises `stream`, copies the device status word out of ws into
+ * device_status[0] (code, a mok_status value) and device_status[1] (site), then clears it.
+ * Host-blocking; not for use inside captured graphs. */
+mok_status mok_read_status(void* ws, size_t ws_bytes, void* stream, int32_t* device_status);
+
+/* Test hook for the bounded waits (no counterpart on the pages): launches one kernel
+ * whose single thread waits on an mbarrier that nothing will complete, with the given
+ * limit in milliseconds; the wait gives up, records MOK_ERR_TIMEOUT in the status word
+ * of ws and the kernel returns normally.  Used to show that a stuck wait ends cleanly. */
+mok_status mok_test_bounded_wait(void* ws, size_t ws_bytes, int32_t limit_ms, void* stream);
+
+/* Human-readable name of a status code. */
+const char* mok_status_string(mok_status s);
+
+/* Number of SMs of the current device and the minimum minibatch (rows) whose expert-
+ * grouped GEMM1 fills two full SM waves of 128x256 output tiles: ceil(2*n_sm*128*256/(2I)).
+ * The pages state the two-wave rule and its result, 2,368 tokens, for hidden 7168 and
+ * intermediate 2048 ("Mixture-of-Kittens (MoK)", sd114.wiki, overlap-granularity section;
+ * aientropygate.com, §03 ②) but no formula; this is the reading that reproduces it for
+ * 148 SMs.  n_sm <= 0 means: query the current device. */
+int32_t mok_min_minibatch(int32_t n_sm, int32_t I);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H_ */

@@ -1,0 +1,8 @@
+"""Single-GPU deterministic mixture-of-experts layer for GB300 (sm_103a).
+
+The compute path is libmok.so (C ABI in include/mok.h, CUDA kernels under
+csrc/); this package only binds it (``_native``) and draws seeded synthetic
+workloads (``workloads``).
+"""
+from ._native import (LayerDesc, MoELayer, MokError, desc_from_shape, get_layout, load, make_desc,  # noqa: F401
+                      min_minibatch, moe_backward, moe_forward, read_status, schedule, status_string)

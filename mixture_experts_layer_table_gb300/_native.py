@@ -1,0 +1,218 @@
+"""ctypes binding of libmok.so (include/mok.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Device memory comes from PyTorch (caller tensors, or torch.empty for
+ctx / ws in MoELayer); the stream is PyTorch's current stream unless given.
+There is no fallback: if libmok.so is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmok.so")
+
+MOK_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace too small", 4: "CUDA error",
+                5: "timeout", 6: "invalid routing"}
+
+
+class MokError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(code, code)} ({code})")
+        self.code = code
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("router", ctypes.c_int32), ("renorm", ctypes.c_int32),
+                ("route_scale", ctypes.c_float), ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32),
+                ("ring_bytes", ctypes.c_int64), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
+                 "x_g", "hu", "ctx_bytes", "status", "logits", "act", "expert_out", "dy_g", "dhu", "gact", "dx_g",
+                 "dg_part", "dlogits", "ws_bytes"]
+CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
+WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in LAYOUT_FIELDS]
+
+
+EXPORTS = ["mok_get_layout", "mok_schedule", "mok_moe_forward", "mok_moe_backward", "mok_read_status",
+           "mok_test_bounded_wait", "mok_status_string", "mok_min_minibatch"]
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libmok.so once (raises OSError when it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} not found: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    D = ctypes.POINTER(LayerDesc)
+    lib.mok_get_layout.argtypes = [D, ctypes.POINTER(Layout)]
+    lib.mok_schedule.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    lib.mok_moe_forward.argtypes = [D, P, P, P, P, P, P, P, P, SZ, P, SZ, P]
+    lib.mok_moe_backward.argtypes = [D, P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
+    lib.mok_read_status.argtypes = [P, SZ, P, ctypes.POINTER(I32)]
+    lib.mok_test_bounded_wait.argtypes = [P, SZ, I32, P]
+    lib.mok_status_string.argtypes = [I32]
+    lib.mok_status_string.restype = ctypes.c_char_p
+    lib.mok_min_minibatch.argtypes = [I32, I32]
+    lib.mok_min_minibatch.restype = I32
+    for name in EXPORTS:
+        if name != "mok_status_string" and name != "mok_min_minibatch":
+            getattr(lib, name).restype = I32
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libmok must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn: str, code: int):
+    if code != MOK_OK:
+        raise MokError(fn, code)
+
+
+def make_desc(T, H, I, E, k, router, renorm, route_scale=1.0, precision=0, minibatch=0, ring_bytes=0,
+              flags=0) -> LayerDesc:
+    return LayerDesc(T, H, I, E, k, router, int(bool(renorm)), route_scale, precision, minibatch, ring_bytes,
+                     flags, 0)
+
+
+def desc_from_shape(shape, **kw) -> LayerDesc:
+    return make_desc(shape.T, shape.H, shape.I, shape.E, shape.k, shape.router, shape.renorm,
+                     precision=1 if shape.mxfp8 else 0, **kw)
+
+
+def get_layout(desc: LayerDesc) -> Dict[str, int]:
+    lay = Layout()
+    _check("mok_get_layout", load().mok_get_layout(ctypes.byref(desc), ctypes.byref(lay)))
+    return {n: getattr(lay, n) for n in LAYOUT_FIELDS}
+
+
+def min_minibatch(n_sm: int, I: int) -> int:
+    return int(load().mok_min_minibatch(n_sm, I))
+
+
+def status_string(code: int) -> str:
+    return load().mok_status_string(code).decode()
+
+
+def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts, offsets, row_of, src_of, ws,
+             stream=None):
+    _check("mok_schedule", load().mok_schedule(
+        ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(topk_idx),
+        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_forward(desc, x, w_router, router_bias, given_topk, w13, w2, y, ctx, ws, stream=None):
+    _check("mok_moe_forward", load().mok_moe_forward(
+        ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(w13), _ptr(w2),
+        _ptr(y), _ptr(ctx), ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_backward(desc, dy, x, w_router, w13, w2, ctx, dx, dw_router, dw13, dw2, dgates, ws, stream=None):
+    _check("mok_moe_backward", load().mok_moe_backward(
+        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(w13), _ptr(w2), _ptr(ctx),
+        ctx.numel() * ctx.element_size(), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def read_status(ws, stream=None):
+    """Synchronises the stream and returns (code, site) of the first device-side error, then clears it."""
+    out = (ctypes.c_int32 * 2)()
+    _check("mok_read_status", load().mok_read_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream), out))
+    return int(out[0]), int(out[1])
+
+
+def test_bounded_wait(ws, limit_ms: int, stream=None):
+    _check("mok_test_bounded_wait",
+           load().mok_test_bounded_wait(_ptr(ws), ws.numel() * ws.element_size(), limit_ms, _stream(stream)))
+
+
+_CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.float32, "counts": torch.int32,
+               "offsets": torch.int32, "row_of": torch.int32, "src_of": torch.int32, "tile_off": torch.int32,
+               "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.bfloat16, "status": torch.int32,
+               "logits": torch.float32, "act": torch.bfloat16, "expert_out": torch.bfloat16,
+               "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "gact": torch.bfloat16, "dx_g": torch.bfloat16,
+               "dg_part": torch.float32, "dlogits": torch.float32}
+
+
+class MoELayer:
+    """One layer descriptor with its ctx and ws buffers (torch-allocated device memory)."""
+
+    def __init__(self, desc: LayerDesc, device="cuda"):
+        self.desc = desc
+        self.layout = get_layout(desc)
+        self.ctx = torch.empty(self.layout["ctx_bytes"], dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(self.layout["ws_bytes"], dtype=torch.uint8, device=device)
+
+    def _shape(self, name):
+        d = self.desc
+        R = d.T * d.k
+        return {"topk_idx": (d.T, d.k), "gates": (d.T, d.k), "scores": (d.T, d.E), "counts": (d.E,),
+                "offsets": (d.E + 1,), "row_of": (R,), "src_of": (R,), "tile_off": (d.E + 1,), "gate_row": (R,),
+                "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "act": (R, d.I),
+                "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I), "gact": (R, d.I),
+                "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E)}[name]
+
+    def view(self, name: str) -> torch.Tensor:
+        """A typed view of one saved tensor (ctx) or temporary (ws)."""
+        buf = self.ctx if name in CTX_FIELDS else self.ws
+        off = self.layout[name]
+        dt = _CTX_DTYPES[name]
+        shape = self._shape(name)
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.empty((), dtype=dt).element_size()
+        return buf[off:off + nbytes].view(dt).view(shape)
+
+    def forward(self, x, w_router, w13, w2, router_bias=None, given_topk=None, y=None, stream=None):
+        if y is None:
+            y = torch.empty((self.desc.T, self.desc.H), dtype=torch.bfloat16, device=x.device)
+        moe_forward(self.desc, x, w_router, router_bias, given_topk, w13, w2, y, self.ctx, self.ws, stream)
+        return y
+
+    def backward(self, dy, x, w_router, w13, w2, out=None, stream=None):
+        d = self.desc
+        dev = dy.device
+        if out is None:
+            out = {"dx": torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev),
+                   "dw_router": torch.empty((d.E, d.H), dtype=torch.float32, device=dev),
+                   "dw13": torch.empty((d.E, 2 * d.I, d.H), dtype=torch.bfloat16, device=dev),
+                   "dw2": torch.empty((d.E, d.H, d.I), dtype=torch.bfloat16, device=dev),
+                   "dgates": torch.empty((d.T, d.k), dtype=torch.float32, device=dev)}
+        moe_backward(d, dy, x, w_router, w13, w2, self.ctx, out["dx"], out["dw_router"], out["dw13"], out["dw2"],
+                     out["dgates"], self.ws, stream)
+        return out
+
+    def status(self, stream=None):
+        return read_status(self.ws, stream)

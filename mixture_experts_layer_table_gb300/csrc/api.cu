@@ -1,0 +1,283 @@
+// C ABI of the layer (include/mok.h): argument checks, ctx / ws layout, and the launch
+// sequences of the forward and backward passes.  No allocation, no host synchronisation
+// in the compute calls; every kernel is enqueued on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "mok.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int sm_count() {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mok_status check_desc(const mok_layer_desc* d) {
+  if (d == nullptr) return MOK_ERR_INVALID_ARG;
+  if (d->T < 1 || d->H < 1 || d->I < 1 || d->E < 1 || d->k < 1) return MOK_ERR_INVALID_ARG;
+  if (d->k > d->E) return MOK_ERR_INVALID_ARG;
+  if (d->router != MOK_ROUTER_SOFTMAX && d->router != MOK_ROUTER_SIGMOID) return MOK_ERR_INVALID_ARG;
+  if (d->precision != MOK_BF16 && d->precision != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+  if (!std::isfinite(d->route_scale)) return MOK_ERR_INVALID_ARG;
+  if (d->minibatch < 0 || d->ring_bytes < 0) return MOK_ERR_INVALID_ARG;
+  if (d->H % 256 != 0 || d->I % 256 != 0) return MOK_ERR_UNSUPPORTED;
+  if (d->E > 1024 || d->k > 16) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = int64_t(d->T) * d->k;
+  const int64_t width = d->H > 2 * d->I ? d->H : 2 * int64_t(d->I);
+  if (R * width >= (int64_t(1) << 31)) return MOK_ERR_UNSUPPORTED;
+  return MOK_OK;
+}
+
+mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
+  const int64_t T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L->topk_idx = take(T * k * 4);
+  L->gates = take(T * k * 4);
+  L->scores = take(T * E * 4);
+  L->counts = take(E * 4);
+  L->offsets = take((E + 1) * 4);
+  L->row_of = take(R * 4);
+  L->src_of = take(R * 4);
+  L->tile_off = take((E + 1) * 4);
+  L->gate_row = take(R * 4);
+  L->x_g = take(R * H * 2);
+  L->hu = take(R * 2 * I * 2);
+  L->ctx_bytes = off;
+  off = 0;
+  L->status = take(16);
+  L->logits = take(T * E * 4);
+  L->act = take(R * I * 2);
+  L->expert_out = take(R * H * 2);
+  L->dy_g = take(R * H * 2);
+  L->dhu = take(R * 2 * I * 2);
+  L->gact = take(R * I * 2);
+  L->dx_g = take(R * H * 2);
+  L->dg_part = take(R * (I / 256) * 4);
+  L->dlogits = take(T * E * 4);
+  L->ws_bytes = off;
+  return MOK_OK;
+}
+
+template <typename T>
+T* at(void* base, int64_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+template <typename T>
+const T* at(const void* base, int64_t off) {
+  return reinterpret_cast<const T*>(static_cast<const char*>(base) + off);
+}
+
+#define MOK_CUDA(call)                       \
+  do {                                       \
+    if ((call) != cudaSuccess) return MOK_ERR_CUDA; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* mok_status_string(mok_status s) {
+  switch (s) {
+    case MOK_OK: return "ok";
+    case MOK_ERR_INVALID_ARG: return "invalid argument";
+    case MOK_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case MOK_ERR_WORKSPACE_TOO_SMALL: return "workspace or ctx too small";
+    case MOK_ERR_CUDA: return "CUDA error";
+    case MOK_ERR_TIMEOUT: return "device wait timed out";
+    case MOK_ERR_INVALID_ROUTING: return "invalid routing (expert index out of range or repeated)";
+  }
+  return "unknown status";
+}
+
+mok_status mok_get_layout(const mok_layer_desc* desc, mok_layout* layout) {
+  if (layout == nullptr) return MOK_ERR_INVALID_ARG;
+  const mok_status s = check_desc(desc);
+  if (s != MOK_OK) return s;
+  return fill_layout(desc, layout);
+}
+
+int32_t mok_min_minibatch(int32_t n_sm, int32_t I) {
+  if (I <= 0) return 0;
+  if (n_sm <= 0) n_sm = sm_count();
+  const int64_t rows = (2LL * n_sm * 128 * 256 + 2LL * I - 1) / (2LL * I);
+  return static_cast<int32_t>(rows);
+}
+
+mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_router, const float* router_bias,
+                        const int32_t* given_topk, int32_t* topk_idx, float* gates, int32_t* counts,
+                        int32_t* offsets, int32_t* row_of, int32_t* src_of, void* ws, size_t ws_bytes,
+                        void* stream) {
+  mok_status s = check_desc(d);
+  if (s != MOK_OK) return s;
+  mok_layout L;
+  fill_layout(d, &L);
+  if (!topk_idx || !counts || !offsets || !row_of || !src_of || !ws) return MOK_ERR_INVALID_ARG;
+  if ((int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const bool have_router = x != nullptr && w_router != nullptr;
+  if (!have_router && (given_topk == nullptr || gates != nullptr)) return MOK_ERR_INVALID_ARG;
+  if (have_router && (!aligned16(x) || !aligned16(w_router))) return MOK_ERR_INVALID_ARG;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  float* logits = at<float>(ws, L.logits);
+  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  if (have_router) MOK_CUDA(mok::launch_router_gemm(x, w_router, d->T, d->H, d->E, logits, status, n_sm, st));
+  MOK_CUDA(mok::launch_topk(have_router ? logits : nullptr, router_bias, given_topk, d->T, d->E, d->k, d->router,
+                            d->renorm, d->route_scale, topk_idx, gates, nullptr, status, st));
+  MOK_CUDA(mok::launch_schedule(topk_idx, nullptr, d->T * d->k, d->E, counts, offsets, row_of, src_of, nullptr,
+                                nullptr, status, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w_router, const float* router_bias,
+                           const int32_t* given_topk, const void* w13, const void* w2, void* y, void* ctx,
+                           size_t ctx_bytes, void* ws, size_t ws_bytes, void* stream) {
+  mok_status s = check_desc(d);
+  if (s != MOK_OK) return s;
+  if (d->precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (!x || !w_router || !w13 || !w2 || !y || !ctx || !ws) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_router) || !aligned16(w13) || !aligned16(w2) || !aligned16(y) ||
+      !aligned16(ctx) || !aligned16(ws))
+    return MOK_ERR_INVALID_ARG;
+  mok_layout L;
+  fill_layout(d, &L);
+  if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
+  int* status = at<int>(ws, L.status);
+  int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
+  float* gates = at<float>(ctx, L.gates);
+  int32_t* offsets = at<int32_t>(ctx, L.offsets);
+  int32_t* tile_off = at<int32_t>(ctx, L.tile_off);
+  int32_t* row_of = at<int32_t>(ctx, L.row_of);
+  int32_t* src_of = at<int32_t>(ctx, L.src_of);
+  void* x_g = at<char>(ctx, L.x_g);
+  void* hu = at<char>(ctx, L.hu);
+  void* act = at<char>(ws, L.act);
+  void* o = at<char>(ws, L.expert_out);
+  float* logits = at<float>(ws, L.logits);
+
+  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  // 1. router logits x W_r^T (tensor cores, fp32 accumulate)
+  MOK_CUDA(mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
+  // 2. scores, top-k and gates
+  MOK_CUDA(mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm, d->route_scale,
+                            topk_idx, gates, at<float>(ctx, L.scores), status, st));
+  // 3. schedule table
+  MOK_CUDA(mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of, src_of,
+                                tile_off, at<float>(ctx, L.gate_row), status, st));
+  // 4. pull dispatch into expert-contiguous rows
+  MOK_CUDA(mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
+  // 5. grouped GEMM1 with the SwiGLU epilogue
+  MOK_CUDA(mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, status, n_sm, st));
+  // 6. grouped GEMM2
+  MOK_CUDA(mok::launch_gemm2(act, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
+  // 7. weighted merge in fixed order
+  MOK_CUDA(mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void* x, const void* w_router,
+                            const void* w13, const void* w2, const void* ctx, size_t ctx_bytes, void* dx,
+                            float* dw_router, void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,
+                            void* stream) {
+  mok_status s = check_desc(d);
+  if (s != MOK_OK) return s;
+  if (d->precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (!dy || !x || !w_router || !w13 || !w2 || !ctx || !dx || !dw_router || !dw13 || !dw2 || !ws)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(w_router) || !aligned16(w13) || !aligned16(w2) ||
+      !aligned16(ctx) || !aligned16(dx) || !aligned16(dw_router) || !aligned16(dw13) || !aligned16(dw2) ||
+      !aligned16(ws))
+    return MOK_ERR_INVALID_ARG;
+  mok_layout L;
+  fill_layout(d, &L);
+  if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
+  int* status = at<int>(ws, L.status);
+  const int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
+  const float* gates = at<float>(ctx, L.gates);
+  const float* scores = at<float>(ctx, L.scores);
+  const int32_t* offsets = at<int32_t>(ctx, L.offsets);
+  const int32_t* tile_off = at<int32_t>(ctx, L.tile_off);
+  const int32_t* row_of = at<int32_t>(ctx, L.row_of);
+  const int32_t* src_of = at<int32_t>(ctx, L.src_of);
+  const float* gate_row = at<float>(ctx, L.gate_row);
+  const void* x_g = at<char>(ctx, L.x_g);
+  const void* hu = at<char>(ctx, L.hu);
+  void* dy_g = at<char>(ws, L.dy_g);
+  void* dhu = at<char>(ws, L.dhu);
+  void* gact = at<char>(ws, L.gact);
+  void* dx_g = at<char>(ws, L.dx_g);
+  float* dg_part = at<float>(ws, L.dg_part);
+  float* dl = at<float>(ws, L.dlogits);
+
+  // 1. reverse combine: pull the upstream gradient rows into expert order
+  MOK_CUDA(mok::launch_gather_rows(dy, src_of, k, R, H, dy_g, n_sm, st));
+  // 2. dA' = dY_g W2[e]; epilogue: SwiGLU backward, g * a, and per-tile <dA', a>
+  MOK_CUDA(mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu, gact, dg_part,
+                                    status, n_sm, st));
+  // 3. dX_g = [dh | du] W13[e]
+  MOK_CUDA(mok::launch_dgrad_x(dhu, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
+  // 4. dW2[e] = dY_g^T (g a), 5. dW13[e] = [dh | du]^T x_g, reduced over the expert's rows
+  MOK_CUDA(mok::launch_wgrad(dy_g, H, gact, I, R, E, offsets, dw2, status, n_sm, st));
+  MOK_CUDA(mok::launch_wgrad(dhu, 2 * I, x_g, H, R, E, offsets, dw13, status, n_sm, st));
+  // 6. gate and router-logit gradients, 7. router weight gradient
+  MOK_CUDA(mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
+                                      d->renorm, d->route_scale, dgates, dl, st));
+  MOK_CUDA(mok::launch_router_wgrad(dl, x, offsets, src_of, T, H, E, k, d->router == MOK_ROUTER_SIGMOID ? 1 : 0,
+                                    dw_router, st));
+  // 8. reverse dispatch: dX[t] = sum_j dX_g[row_of[t,j]] + dl[t] W_r
+  MOK_CUDA(mok::launch_combine(dx_g, nullptr, row_of, T, k, H, dl, w_router, topk_idx, E,
+                               d->router == MOK_ROUTER_SOFTMAX ? 1 : 0, dx, n_sm, st));
+  return MOK_OK;
+}
+
+mok_status mok_read_status(void* ws, size_t ws_bytes, void* stream, int32_t* device_status) {
+  if (!ws || !device_status || ws_bytes < 16) return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the status word is the first tensor of ws
+  MOK_CUDA(cudaMemcpyAsync(device_status, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  MOK_CUDA(cudaStreamSynchronize(st));
+  MOK_CUDA(cudaMemsetAsync(ws, 0, 16, st));
+  MOK_CUDA(cudaStreamSynchronize(st));
+  return MOK_OK;
+}
+
+mok_status mok_test_bounded_wait(void* ws, size_t ws_bytes, int32_t limit_ms, void* stream) {
+  if (!ws || ws_bytes < 16 || limit_ms < 1 || limit_ms > 10000) return MOK_ERR_INVALID_ARG;
+  MOK_CUDA(mok::launch_test_wait(static_cast<int*>(ws), (long long)limit_ms * 1000000LL,
+                                 static_cast<cudaStream_t>(stream)));
+  return MOK_OK;
+}
+
+}  // extern "C"

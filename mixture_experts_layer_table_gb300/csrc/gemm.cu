@@ -1,0 +1,204 @@
+// Host launchers of the tcgen05 GEMMs: TMA descriptor encoding and the kernel
+// instantiations used by the forward and backward of the layer.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+namespace mok {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tensor, innermost dimension first; strides in bytes for dims 1..rank-1; 128B swizzle,
+// out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+               const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) s[i] = strides_bytes[i];
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+             uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return make_tmap(m, base, 2, dims, strides, box);
+}
+
+bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const uint32_t box[3] = {b0, b1, 1};
+  return make_tmap(m, base, 3, dims, strides, box);
+}
+
+template <int MODE, int EPI>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid, cudaStream_t st) {
+  if (grid <= 0) return cudaSuccess;
+  auto kern = gemm_kernel<MODE, EPI>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem_bytes(1024));
+  if (err != cudaSuccess) return err;
+  kern<<<grid, GEMM_THREADS, gemm_smem_bytes(args.E), st>>>(a, b, args);
+  return cudaGetLastError();
+}
+
+GemmArgs base_args(int E, const int32_t* offsets, const int32_t* tile_off, int* status) {
+  GemmArgs g{};
+  g.E = E;
+  g.offsets = offsets;
+  g.tile_off = tile_off;
+  g.total_tiles = -1;
+  g.status = status;
+  return g;
+}
+
+// Upper bound of the 128-row tiles of R expert-sorted rows split into E segments.
+int row_tiles_bound(int R, int E) { return (R + BM - 1) / BM + E; }
+
+}  // namespace
+
+cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
+                               int* status, int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!tmap_2d(&ta, x, H, T, BK, BM) || !tmap_2d(&tb, w_router, H, E, BK, BN)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(1, nullptr, nullptr, status);
+  g.M = T;
+  g.N = E;
+  g.K = H;
+  g.out0 = logits;
+  g.ld0 = E;
+  const int tiles = ((T + BM - 1) / BM) * ((E + BN - 1) / BN);
+  g.total_tiles = tiles;
+  return launch<MODE_DENSE, EPI_F32>(ta, tb, g, std::min(tiles, n_sm), st);
+}
+
+cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
+                                const int32_t* offsets, const int32_t* tile_off, void* hu, void* act,
+                                int* status, int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!tmap_2d(&ta, x_g, H, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, BK, 128)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(E, offsets, tile_off, status);
+  g.N = I;
+  g.K = H;
+  g.I = I;
+  g.out0 = hu;
+  g.ld0 = 2LL * I;
+  g.out1 = act;
+  g.ld1 = I;
+  const int bound = row_tiles_bound(R, E) * (I / 128);
+  return launch<MODE_ROWS, EPI_SWIGLU>(ta, tb, g, std::min(bound, n_sm), st);
+}
+
+cudaError_t launch_gemm2(const void* act, const void* w2, int R, int H, int I, int E, const int32_t* offsets,
+                         const int32_t* tile_off, void* out, int* status, int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!tmap_2d(&ta, act, I, R, BK, BM) || !tmap_3d(&tb, w2, I, H, E, BK, BN)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(E, offsets, tile_off, status);
+  g.N = H;
+  g.K = I;
+  g.out0 = out;
+  g.ld0 = H;
+  const int bound = row_tiles_bound(R, E) * (H / BN);
+  return launch<MODE_ROWS, EPI_BF16>(ta, tb, g, std::min(bound, n_sm), st);
+}
+
+cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
+                                const int32_t* offsets, const int32_t* tile_off, const void* hu,
+                                const float* gate_row, void* dhu, void* gact, float* dg_part, int* status,
+                                int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  // A = dY_g [R][H] (K = H, K-major); B = W2[e] [H][I] seen as [K][N] (N contiguous)
+  if (!tmap_2d(&ta, dy_g, H, R, BK, BM) || !tmap_3d(&tb, w2, I, H, E, 64, BK)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(E, offsets, tile_off, status);
+  g.N = I;
+  g.K = H;
+  g.I = I;
+  g.out0 = dhu;
+  g.ld0 = 2LL * I;
+  g.out1 = gact;
+  g.ld1 = I;
+  g.out2 = dg_part;
+  g.ld2 = I / BN;
+  g.hu = reinterpret_cast<const __nv_bfloat16*>(hu);
+  g.gate_row = gate_row;
+  const int bound = row_tiles_bound(R, E) * (I / BN);
+  return launch<MODE_DGRAD, EPI_SWIGLU_BWD>(ta, tb, g, std::min(bound, n_sm), st);
+}
+
+cudaError_t launch_dgrad_x(const void* dhu, const void* w13, int R, int H, int I, int E, const int32_t* offsets,
+                           const int32_t* tile_off, void* dx_g, int* status, int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  // A = dHU [R][2I] (K = 2I); B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)
+  if (!tmap_2d(&ta, dhu, 2 * I, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, 64, BK)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(E, offsets, tile_off, status);
+  g.N = H;
+  g.K = 2 * I;
+  g.out0 = dx_g;
+  g.ld0 = H;
+  const int bound = row_tiles_bound(R, E) * (H / BN);
+  return launch<MODE_DGRAD, EPI_BF16>(ta, tb, g, std::min(bound, n_sm), st);
+}
+
+cudaError_t launch_wgrad(const void* a_rows, int M, const void* b_rows, int N, int R, int E,
+                         const int32_t* offsets, void* dw, int* status, int n_sm, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!tmap_2d(&ta, a_rows, M, R, 64, BK) || !tmap_2d(&tb, b_rows, N, R, 64, BK)) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(E, offsets, nullptr, status);
+  g.M = M;
+  g.N = N;
+  g.out0 = dw;
+  const int tiles = E * (M / BM) * (N / BN);
+  g.total_tiles = tiles;
+  return launch<MODE_WGRAD, EPI_BF16>(ta, tb, g, std::min(tiles, n_sm), st);
+}
+
+// ----------------------------------------------------------------------------- wait test
+__global__ void test_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    // nothing ever arrives on `bar`: the wait must give up and report
+    mbar_wait(smem_u32(&bar), 0, &abort_flag, status, SITE_TEST_WAIT, limit_ns);
+  }
+}
+
+cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st) {
+  test_wait_kernel<<<1, 32, 0, st>>>(status, (unsigned long long)limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace mok

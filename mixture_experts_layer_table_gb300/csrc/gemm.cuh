@@ -1,0 +1,533 @@
+// Persistent tcgen05 GEMM for the expert-grouped products of one MoE layer (sm_103a).
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer: loads A and B tiles of 64 K-elements into a 4-stage ring
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32) into TMEM, 128 x 256 tile
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused elementwise work, stores
+// The accumulator is double-buffered in TMEM (2 x 256 of the 512 columns), so the epilogue
+// of tile i overlaps the main loop of tile i+1.  Tiles are dealt round-robin over the CTAs
+// in a fixed order, so the result does not depend on timing (each output element is owned
+// by exactly one tile and reduced over K in a fixed order).
+//
+// Modes (how A, B and the tiles are laid out):
+//   MODE_DENSE  A [M][K], B [N][K], both K-major                  (router logits)
+//   MODE_ROWS   A = expert-sorted rows [R][K] (K-major), B [E][N][K] K-major
+//               (GEMM1 x_g W13^T with SwiGLU, GEMM2 a W2^T)
+//   MODE_DGRAD  A = rows [R][K] K-major, B [E][K][N] (N contiguous: MN-major)
+//               (dA' = dY_g W2[e], dX_g = dHU W13[e])
+//   MODE_WGRAD  A = rows [R][M] and B = rows [R][N], both MN-major; K runs over the rows of
+//               one expert (dW2[e] = dY_g^T (g a), dW13[e] = dHU^T x_g)
+// Rows of one expert are contiguous (the schedule table); a 128-row tile that runs past its
+// expert reads the next expert's rows (discarded at the store) or TMA zero fill past R.
+// In MODE_WGRAD the rows past the expert's end inside the last K block are zeroed in shared
+// memory before the MMA reads them.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace mok {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int GEMM_THREADS = 192;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = 512;
+constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom column: 64 K rows x 128 B
+
+// Leading / stride byte offsets of the MN-major 128B-swizzled operand layout:
+// LBO = distance between 64-element MN atom columns, SBO = distance between 8-row K groups.
+#ifndef MOK_MN_LBO
+#define MOK_MN_LBO MN_ATOM_BYTES
+#endif
+#ifndef MOK_MN_SBO
+#define MOK_MN_SBO 1024
+#endif
+
+enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
+enum GemmEpi { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3 };
+
+struct GemmArgs {
+  int M;            // DENSE: rows of A; WGRAD: output rows per expert
+  int N;            // output columns (per expert); SWIGLU: I (the tile pairs gate and up)
+  int K;            // reduction length (DENSE / ROWS / DGRAD)
+  int E;            // experts (groups)
+  int I;            // SWIGLU / SWIGLU_BWD: intermediate width
+  int total_tiles;  // host-known tile count, or -1: tile_off[E] * n_tiles (grouped rows)
+  const int* offsets;   // [E+1] expert row offsets
+  const int* tile_off;  // [E+1] prefix of ceil(rows/128)
+  void* out0;
+  void* out1;
+  void* out2;
+  long long ld0, ld1, ld2;
+  const __nv_bfloat16* hu;  // SWIGLU_BWD: saved h | u
+  const float* gate_row;    // SWIGLU_BWD: gate of each row
+  int* status;
+};
+
+struct TileInfo {
+  int e, m, n;
+  int row0;   // first A row (ROWS/DGRAD/DENSE) or first K row (WGRAD)
+  int rows;   // valid output rows (ROWS/DGRAD/DENSE) or K rows (WGRAD)
+  int nkb;    // K blocks
+};
+
+template <int MODE, int EPI>
+struct GemmTraits {
+  static constexpr bool kAmn = (MODE == MODE_WGRAD);
+  static constexpr bool kBmn = (MODE == MODE_DGRAD || MODE == MODE_WGRAD);
+  static __host__ __device__ int n_tiles(const GemmArgs& a) {
+    return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + BN - 1) / BN;
+  }
+};
+
+__host__ __device__ inline size_t gemm_smem_bytes(int E) {
+  return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+}
+
+template <int MODE, int EPI>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const int* s_off,
+                                                const int* s_toff) {
+  TileInfo t;
+  const int NT = GemmTraits<MODE, EPI>::n_tiles(a);
+  if (MODE == MODE_DENSE) {
+    const int MT = (a.M + BM - 1) / BM;
+    t.e = 0;
+    t.m = g % MT;
+    t.n = g / MT;
+    t.row0 = t.m * BM;
+    t.rows = min(BM, a.M - t.row0);
+    t.nkb = a.K / BK;
+  } else if (MODE == MODE_WGRAD) {
+    const int MT = a.M / BM;
+    const int per_e = MT * NT;
+    t.e = g / per_e;
+    const int rem = g - t.e * per_e;
+    t.m = rem / NT;
+    t.n = rem - t.m * NT;
+    t.row0 = s_off[t.e];
+    t.rows = s_off[t.e + 1] - t.row0;
+    t.nkb = (t.rows + BK - 1) / BK;
+  } else {
+    // expert e owns tiles [tile_off[e]*NT, tile_off[e+1]*NT); inside, m runs fastest so the
+    // m-tiles of one expert that share a weight tile are dealt to neighbouring CTAs.
+    int lo = 0, hi = a.E;  // find largest e with s_toff[e]*NT <= g
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_toff[mid] * NT <= g) lo = mid; else hi = mid;
+    }
+    // skip experts with no tiles that share the same start
+    t.e = lo;
+    const int Me = s_toff[lo + 1] - s_toff[lo];
+    const int local = g - s_toff[lo] * NT;
+    t.n = local / Me;
+    t.m = local - t.n * Me;
+    t.row0 = s_off[lo] + t.m * BM;
+    t.rows = min(BM, s_off[lo + 1] - t.row0);
+    t.nkb = a.K / BK;
+  }
+  return t;
+}
+
+template <int MODE, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs args) {
+  using Tr = GemmTraits<MODE, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_toff = s_off + (args.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (MODE != MODE_DENSE) {
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
+      s_off[i] = args.offsets[i];
+      s_toff[i] = (MODE == MODE_WGRAD) ? 0 : args.tile_off[i];
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int NT = Tr::n_tiles(args);
+  const int total = args.total_tiles >= 0 ? args.total_tiles : s_toff[args.E] * NT;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      const uint64_t pol_act = l2_policy_evict_last();
+      const uint64_t pol_w = (MODE == MODE_WGRAD) ? pol_act : l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+        const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (MODE == MODE_DENSE) {
+            tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
+            tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
+          } else if (MODE == MODE_ROWS) {
+            tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
+            if (EPI == EPI_SWIGLU) {
+              tma_load_3d(sb, &tmB, fb, k0, t.n * 128, t.e, pol_w);
+              tma_load_3d(sb + B_BYTES / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
+            } else {
+              tma_load_3d(sb, &tmB, fb, k0, t.n * BN, t.e, pol_w);
+            }
+          } else if (MODE == MODE_DGRAD) {
+            tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tma_load_3d(sb + q * MN_ATOM_BYTES, &tmB, fb, t.n * BN + q * 64, k0, t.e, pol_w);
+          } else {  // WGRAD
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              tma_load_2d(sa + q * MN_ATOM_BYTES, &tmA, fb, t.m * BM + q * 64, t.row0 + k0, pol_act);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              tma_load_2d(sb + q * MN_ATOM_BYTES, &tmB, fb, t.n * BN + q * 64, t.row0 + k0, pol_act);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborted: let the copies already in flight land before the CTA exits.
+        const int outstanding = min(issued, STAGES);
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < outstanding; ++i) {
+          if (--s < 0) {
+            s = STAGES - 1;
+            ph ^= 1;
+          }
+          volatile int no_abort = 0;
+          mbar_wait(full_bar(s), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, Tr::kAmn, Tr::kBmn);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool any_mma = false;
+    for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+      const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+      if (t.nkb == 0) continue;
+      int w_ok = 1;
+      if (lane == 0)
+        w_ok = mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        int f_ok = 1;
+        if (lane == 0)
+          f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t* sa_ptr = smem + stage * STAGE_BYTES;
+        const uint32_t sa = smem_u32(sa_ptr);
+        const uint32_t sb = sa + A_BYTES;
+        int kvalid = BK;
+        if (MODE == MODE_WGRAD) {
+          kvalid = min(BK, t.rows - kb * BK);
+          const int kend = (kvalid + 15) & ~15;
+          if (kvalid < kend) {
+            // zero the K rows [kvalid, kend) of the 2 A and 4 B atom columns
+            const int nl = kend - kvalid;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int idx = lane; idx < nl * 6 * 8; idx += 32) {
+              const int chunk = idx & 7;
+              const int li = idx >> 3;
+              const int atom = li / nl;
+              const int line = kvalid + (li - atom * nl);
+              uint8_t* p = sa_ptr + atom * MN_ATOM_BYTES + line * 128 + chunk * 16;
+              *reinterpret_cast<uint4*>(p) = z;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const int nk16 = (kvalid + 15) >> 4;
+          for (int k16 = 0; k16 < nk16; ++k16) {
+            uint64_t adesc, bdesc;
+            if (Tr::kAmn) adesc = smem_desc_sw128(sa + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
+            else adesc = smem_desc_sw128(sa + k16 * 32, 16, 1024);
+            if (Tr::kBmn) bdesc = smem_desc_sw128(sb + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
+            else bdesc = smem_desc_sw128(sb + k16 * 32, 16, 1024);
+            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | k16) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+        }
+        any_mma = true;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(tfull_bar(acc));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    // Wait for every MMA this CTA issued before TMEM is released.
+    if (any_mma) {
+      if (lane == 0) {
+        umma_commit(drain_bar);
+        volatile int no_abort = 0;
+        mbar_wait(drain_bar, 0, &no_abort, args.status, SITE_GEMM_DRAIN);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are reachable by this warp
+    const int r_local = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+      const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+      if (MODE == MODE_WGRAD && t.nkb == 0) {
+        // an expert without rows: its weight gradient is zero
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out0) +
+                             (size_t)t.e * args.M * args.N + (size_t)(t.m * BM + r_local) * args.N + t.n * BN;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll 4
+        for (int c = 0; c < BN / 8; ++c) reinterpret_cast<uint4*>(out)[c] = z;
+        continue;
+      }
+      int w_ok = 1;
+      if (lane == 0)
+        w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
+      const bool valid = (MODE == MODE_WGRAD) ? true : (r_local < t.rows);
+      const long long row = (MODE == MODE_WGRAD) ? 0 : (long long)(t.row0 + r_local);
+
+      if (EPI == EPI_F32) {
+        float* out = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+          const int col0 = t.n * BN + c * 32;
+          if (valid) {
+            if (col0 + 32 <= args.N) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(out + col0 + j) =
+                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                __uint_as_float(v[j + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j < args.N) out[col0 + j] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      } else if (EPI == EPI_BF16) {
+        __nv_bfloat16* out;
+        if (MODE == MODE_WGRAD)
+          out = reinterpret_cast<__nv_bfloat16*>(args.out0) + (size_t)t.e * args.M * args.N +
+                (size_t)(t.m * BM + r_local) * args.N + t.n * BN;
+        else
+          out = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0 + t.n * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              p[j] = *reinterpret_cast<uint32_t*>(&b);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+          }
+        }
+      } else if (EPI == EPI_SWIGLU) {
+        // columns 0..127 of the accumulator are gate (h), 128..255 up (u), for
+        // intermediate indices n*128 .. n*128+127
+        __nv_bfloat16* hu = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
+        __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t vh[32], vu[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, vh);
+          tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
+          tmem_wait_ld();
+          if (valid) {
+            const int col = t.n * 128 + c * 32;
+            uint32_t ph[16], pu[16], pa[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = __uint_as_float(vh[2 * j]), h1 = __uint_as_float(vh[2 * j + 1]);
+              const float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
+              const float a0 = h0 / (1.0f + __expf(-h0)) * u0;
+              const float a1 = h1 / (1.0f + __expf(-h1)) * u1;
+              __nv_bfloat162 bh = __floats2bfloat162_rn(h0, h1);
+              __nv_bfloat162 bu = __floats2bfloat162_rn(u0, u1);
+              __nv_bfloat162 ba = __floats2bfloat162_rn(a0, a1);
+              ph[j] = *reinterpret_cast<uint32_t*>(&bh);
+              pu[j] = *reinterpret_cast<uint32_t*>(&bu);
+              pa[j] = *reinterpret_cast<uint32_t*>(&ba);
+            }
+            uint4* dh = reinterpret_cast<uint4*>(hu + col);
+            uint4* du = reinterpret_cast<uint4*>(hu + args.I + col);
+            uint4* da = reinterpret_cast<uint4*>(act + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              dh[j] = make_uint4(ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
+              du[j] = make_uint4(pu[4 * j], pu[4 * j + 1], pu[4 * j + 2], pu[4 * j + 3]);
+              da[j] = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
+            }
+          }
+        }
+      } else {  // EPI_SWIGLU_BWD
+        // accumulator = dA' = dY_g W2[e] for intermediate columns n*256 .. n*256+255
+        const float g = valid ? args.gate_row[row] : 0.0f;
+        const __nv_bfloat16* hu_row = args.hu + row * (long long)(2 * args.I);
+        __nv_bfloat16* dhu = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
+        __nv_bfloat16* gact = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+        float dg = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+          if (valid) {
+            const int col = t.n * BN + c * 32;
+            uint4 hq[4], uq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              hq[j] = reinterpret_cast<const uint4*>(hu_row + col)[j];
+              uq[j] = reinterpret_cast<const uint4*>(hu_row + args.I + col)[j];
+            }
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(hq);
+            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(uq);
+            uint32_t pdh[16], pdu[16], pga[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 hh = __bfloat1622float2(h2[j]);
+              const float2 uu = __bfloat1622float2(u2[j]);
+              float r_dh[2], r_du[2], r_ga[2];
+              const float hv[2] = {hh.x, hh.y};
+              const float uv[2] = {uu.x, uu.y};
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const float dap = __uint_as_float(v[2 * j + q]);
+                const float sg = 1.0f / (1.0f + __expf(-hv[q]));
+                const float sl = hv[q] * sg;
+                const float a = sl * uv[q];
+                dg = fmaf(dap, a, dg);
+                const float dA = g * dap;
+                r_dh[q] = dA * uv[q] * sg * (1.0f + hv[q] * (1.0f - sg));
+                r_du[q] = dA * sl;
+                r_ga[q] = g * a;
+              }
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(r_dh[0], r_dh[1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(r_du[0], r_du[1]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(r_ga[0], r_ga[1]);
+              pdh[j] = *reinterpret_cast<uint32_t*>(&b0);
+              pdu[j] = *reinterpret_cast<uint32_t*>(&b1);
+              pga[j] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            uint4* o_dh = reinterpret_cast<uint4*>(dhu + col);
+            uint4* o_du = reinterpret_cast<uint4*>(dhu + args.I + col);
+            uint4* o_ga = reinterpret_cast<uint4*>(gact + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              o_dh[j] = make_uint4(pdh[4 * j], pdh[4 * j + 1], pdh[4 * j + 2], pdh[4 * j + 3]);
+              o_du[j] = make_uint4(pdu[4 * j], pdu[4 * j + 1], pdu[4 * j + 2], pdu[4 * j + 3]);
+              o_ga[j] = make_uint4(pga[4 * j], pga[4 * j + 1], pga[4 * j + 2], pga[4 * j + 3]);
+            }
+          }
+        }
+        if (valid) reinterpret_cast<float*>(args.out2)[row * args.ld2 + t.n] = dg;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace mok

@@ -1,0 +1,48 @@
+// Host-side launchers of the layer's kernels (internal to the library).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mok {
+
+// route.cu
+cudaError_t launch_topk(const float* logits, const float* bias, const int32_t* given, int T, int E, int k,
+                        int router, int renorm, float route_scale, int32_t* topk_idx, float* gates,
+                        float* scores, int* status, cudaStream_t st);
+cudaError_t launch_schedule(const int32_t* topk_idx, const float* gates, int R, int E, int32_t* counts,
+                            int32_t* offsets, int32_t* row_of, int32_t* src_of, int32_t* tile_off,
+                            float* gate_row, int* status, cudaStream_t st);
+cudaError_t launch_router_dlogits(const float* dg_part, int n_part, const int32_t* row_of,
+                                  const int32_t* topk_idx, const float* gates, const float* scores, int T,
+                                  int E, int k, int router, int renorm, float route_scale, float* dgates,
+                                  float* dl, cudaStream_t st);
+cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* offsets, const int32_t* src_of,
+                                int T, int H, int E, int k, int sparse, float* dw, cudaStream_t st);
+
+// rows.cu
+cudaError_t launch_gather_rows(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
+                               cudaStream_t st);
+cudaError_t launch_combine(const void* rows, const float* w, const int32_t* row_of, int T, int k, int H,
+                           const float* dl, const void* w_router, const int32_t* topk_idx, int E,
+                           int dense_router, void* out, int n_sm, cudaStream_t st);
+
+// gemm.cu
+cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
+                               int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
+                                const int32_t* offsets, const int32_t* tile_off, void* hu, void* act,
+                                int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_gemm2(const void* act, const void* w2, int R, int H, int I, int E, const int32_t* offsets,
+                         const int32_t* tile_off, void* out, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
+                                const int32_t* offsets, const int32_t* tile_off, const void* hu,
+                                const float* gate_row, void* dhu, void* gact, float* dg_part, int* status,
+                                int n_sm, cudaStream_t st);
+cudaError_t launch_dgrad_x(const void* dhu, const void* w13, int R, int H, int I, int E, const int32_t* offsets,
+                           const int32_t* tile_off, void* dx_g, int* status, int n_sm, cudaStream_t st);
+// dW[e] [M][N] = sum over rows r of expert e of A[r][0..M) (x) B[r][0..N)
+cudaError_t launch_wgrad(const void* a_rows, int M, const void* b_rows, int N, int R, int E,
+                         const int32_t* offsets, void* dw, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
+
+}  // namespace mok

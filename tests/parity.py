@@ -1,0 +1,61 @@
+"""Shared helpers of the GPU parity tests: tolerance checks and oracle runs on the inputs
+handed to the CUDA path (the oracle only ever sees generator draws, never GPU output)."""
+import numpy as np
+import torch
+
+from oracle import moe_oracle as O
+
+# bf16 outputs and gradients: max|err| <= 2e-2 * RMS(reference), relative Frobenius <= 1e-2
+BF16_MAX_REL_RMS = 2e-2
+BF16_FRO = 1e-2
+
+
+def to_f64(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def err_stats(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    diff = got - want
+    rms = np.sqrt(np.mean(want ** 2)) if want.size else 0.0
+    fro = np.linalg.norm(diff) / max(np.linalg.norm(want), 1e-300)
+    return float(np.abs(diff).max() if diff.size else 0.0), float(rms), float(fro)
+
+
+def assert_bf16_close(got, want, name, max_rel_rms=BF16_MAX_REL_RMS, fro_tol=BF16_FRO):
+    mx, rms, fro = err_stats(got, want)
+    assert mx <= max_rel_rms * rms and fro <= fro_tol, (
+        f"{name}: max|err| {mx:.3e} vs {max_rel_rms}*rms {max_rel_rms * rms:.3e}, rel fro {fro:.3e}")
+
+
+def inputs_f64(inp):
+    return {k: (to_f64(v) if v is not None else None) for k, v in inp.items()}
+
+
+def oracle_layer(shape, f64, topk_idx=None, backward=True):
+    fwd = O.forward(f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router, k=shape.k,
+                    renorm=shape.renorm, router_bias=f64.get("router_bias"), topk_idx=topk_idx)
+    bwd = None
+    if backward:
+        bwd = O.backward(fwd, f64["dy"], f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router,
+                         k=shape.k, renorm=shape.renorm)
+    return fwd, bwd
+
+
+def selection_is_valid(sel_scores, gpu_idx, k, rel_margin=1e-5):
+    """GPU top-k against the oracle's selection scores: every chosen expert must score at least
+    as high as every unchosen one, up to a relative margin (near-ties may break either way).
+    Returns the number of tokens whose chosen set differs from the oracle's exact top-k."""
+    T, E = sel_scores.shape
+    n_diff = 0
+    exact = O.select_topk(sel_scores, k)
+    for t in range(T):
+        chosen = set(int(e) for e in gpu_idx[t])
+        assert len(chosen) == k, f"token {t}: repeated experts {gpu_idx[t]}"
+        if chosen != set(int(e) for e in exact[t]):
+            n_diff += 1
+            lo = min(sel_scores[t, e] for e in chosen)
+            hi = max(sel_scores[t, e] for e in range(E) if e not in chosen)
+            assert lo >= hi - rel_margin * max(abs(hi), 1.0), f"token {t}: {lo} < {hi}"
+    return n_diff

@@ -1,0 +1,72 @@
+"""The C ABI library: loads, exports every declared entry point, host-side checks (CPU only)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_table_gb300 as mok
+from mixture_experts_layer_table_gb300 import _native as N
+from mixture_experts_layer_table_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_table_gb300 import build
+    build.build()
+    return N.load()
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(mok_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert {"mok_schedule", "mok_moe_forward", "mok_moe_backward"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_layout_sizes_and_alignment(lib):
+    lay = mok.get_layout(mok.desc_from_shape(W.DSV3))
+    R, H, I = W.DSV3.R, W.DSV3.H, W.DSV3.I
+    for name, off in lay.items():
+        assert off % 256 == 0, name
+    assert lay["ctx_bytes"] >= lay["hu"] + R * 2 * I * 2
+    assert lay["ws_bytes"] >= lay["dlogits"] + W.DSV3.T * W.DSV3.E * 4
+    assert lay["status"] == 0
+    assert lay["x_g"] < lay["hu"] and lay["hu"] - lay["x_g"] >= R * H * 2
+
+
+@pytest.mark.parametrize("field,value,code", [("H", 300, 2), ("I", 100, 2), ("k", 9, 1), ("E", 2000, 2),
+                                              ("T", 0, 1), ("router", 3, 1), ("k", 17, 1)])
+def test_desc_validation(lib, field, value, code):
+    d = mok.desc_from_shape(W.TINY)
+    setattr(d, field, value)
+    if field == "k" and value == 17:
+        d.E = 32
+        code = 2
+    lay = N.Layout()
+    assert lib.mok_get_layout(ctypes.byref(d), ctypes.byref(lay)) == code
+
+
+def test_min_minibatch_reproduces_page_number(lib):
+    with open(os.path.join(ROOT, "tests", "golden", "pages_numbers.json")) as f:
+        g = json.load(f)["min_minibatch_tokens"]
+    assert mok.min_minibatch(148, g["intermediate"]) == g["value"]
+    assert mok.min_minibatch(160, 2048) == 2560      # the other minibatch the pages time
+
+
+def test_status_strings(lib):
+    assert mok.status_string(0) == "ok"
+    assert "timed out" in mok.status_string(5)
