@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE layer (router -> schedule -> pull dispatch -> grouped SwiGLU FFN ->
+weighted combine, and its backward) on GB300.
+
+One step = one forward + one backward of the DeepSeek-V3-shaped layer (T=4096 tokens,
+hidden 7168, 256 experts of intermediate 2048, top-8 sigmoid router with renormalised
+gates) on seeded synthetic bf16 data, inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mok|reference]
+
+--impl reference times the float64 CPU oracle (the deliberately slow, obviously correct
+restatement of the layer) on a bounded sample of the same workload on the host cores.
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU and batch
+(weak scaling, no collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s, fwd+bwd, 1xGB300 (grouped-GEMM % of tensor peak reported alongside)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CPU_SAMPLE = {"T": 512, "E": 16}        # cpu_baseline: 512 tokens of the DSV3 shape over 16 experts
+REF_SAMPLE = {"T": 256, "E": 16}        # --impl reference: per step
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_bytes(s):
+    """Algorithmic HBM bytes of one launch of each kernel (reads + writes of distinct data)."""
+    T, H, I, E, k = s.T, s.H, s.I, s.E, s.k
+    R = T * k
+    return {
+        "router_gemm": T * H * 2 + E * H * 2 + T * E * 4,
+        "topk": T * E * 4 * 2 + T * k * 8,
+        "schedule": R * 4 * 5 + E * 8,
+        "gather_x": T * H * 2 + R * H * 2 + R * 4,
+        "gemm1_swiglu": E * 2 * I * H * 2 + R * H * 2 + R * 2 * I * 2 + R * I * 2,
+        "gemm2": E * H * I * 2 + R * I * 2 + R * H * 2,
+        "combine": R * H * 2 + T * H * 2 + R * 8,
+        "gather_dy": T * H * 2 + R * H * 2 + R * 4,
+        "dgrad_swiglu": E * H * I * 2 + R * H * 2 + R * 2 * I * 2 * 2 + R * I * 2 + R * (I // 256) * 4,
+        "dgrad_x": E * 2 * I * H * 2 + R * 2 * I * 2 + R * H * 2,
+        "wgrad_w2": R * H * 2 + R * I * 2 + E * H * I * 2,
+        "wgrad_w13": R * 2 * I * 2 + R * H * 2 + E * 2 * I * H * 2,
+        "router_dlogits": R * (I // 256) * 4 + R * 12 + T * E * 8,
+        "router_wgrad": T * H * 2 + E * H * 4 + T * E * 4,
+        "combine_dx": R * H * 2 + E * H * 2 + T * H * 2 + T * E * 4,
+    }
+
+
+def kernel_flops(s):
+    """Dense tensor-core FLOPs of one launch of each GEMM kernel."""
+    T, H, I, E, k = s.T, s.H, s.I, s.E, s.k
+    R = T * k
+    return {"router_gemm": 2 * T * E * H, "gemm1_swiglu": 2 * R * 2 * I * H, "gemm2": 2 * R * H * I,
+            "dgrad_swiglu": 2 * R * H * I, "dgrad_x": 2 * R * 2 * I * H, "wgrad_w2": 2 * R * H * I,
+            "wgrad_w13": 2 * R * 2 * I * H}
+
+
+def load_traffic():
+    """Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from the committed
+    ncu summary, keyed by kernel; only entries marked current for the present kernels."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_dsv3.txt")
+    out = {}
+    if os.path.exists(path):
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[2] == "current":
+                    out[parts[0]] = float(parts[1])
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+
+    FIELDS = "index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_sample_run(T, E, repeats=1):
+    """Times the float64 oracle (forward + backward) on T tokens of the DSV3 shape over E experts."""
+    import numpy as np
+    from mixture_experts_layer_table_gb300 import workloads as W
+    from oracle import moe_oracle as O
+    shp = W.DSV3.scaled(T=T, E=E)
+    inp = W.make_inputs(shp, seed=0, device="cpu")
+    f = {k: (v.double().numpy() if v is not None else None) for k, v in inp.items()}
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        fwd = O.forward(f["x"], f["w_router"], f["w13"], f["w2"], kind=shp.router, k=shp.k, renorm=shp.renorm)
+        O.backward(fwd, f["dy"], f["x"], f["w_router"], f["w13"], f["w2"], kind=shp.router, k=shp.k,
+                   renorm=shp.renorm)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_sample_subprocess(T, E, repeats=1):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores), MKL_NUM_THREADS=str(cores),
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(T), str(E), str(repeats)],
+                       env=env, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    times = json.loads(r.stdout.strip().splitlines()[-1])
+    return times, cores
+
+
+def sample_desc(T, E):
+    return (f"float64 oracle forward+backward on {T} tokens of the same layer shape (hidden 7168, "
+            f"intermediate 2048, top-8 sigmoid router, renormalised) restricted to {E} experts, "
+            f"seeded CPU draws; tokens/s = {T} / seconds")
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    T, E = REF_SAMPLE["T"], REF_SAMPLE["E"]
+    times, cores = cpu_sample_subprocess(T, E, repeats=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    sec = sum(timed)
+    value = T * len(timed) / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(timed),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Gaussian activations and weights)",
+            "config": {"workload": "dsv3_T4096_H7168_E256_I2048_top8_sigmoid (sampled: %d tokens, %d experts)" % (T, E),
+                       "passes": "fwd+bwd"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample_desc(T, E)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_mok(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import _native as N
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    mok.load()
+    shp = W.DSV3
+    T, H, I, E, k = shp.T, shp.H, shp.I, shp.E, shp.k
+    inp = W.make_inputs(shp, seed=1000 * rank, device=str(dev))
+    layer = mok.MoELayer(mok.desc_from_shape(shp), device=dev)
+    grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+             "dw_router": torch.empty((E, H), dtype=torch.float32, device=dev),
+             "dw13": torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev),
+             "dw2": torch.empty((E, H, I), dtype=torch.bfloat16, device=dev),
+             "dgates": torch.empty((T, k), dtype=torch.float32, device=dev)}
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    x, wr, w13, w2, dy = inp["x"], inp["w_router"], inp["w13"], inp["w2"], inp["dy"]
+
+    def fwd():
+        layer.forward(x, wr, w13, w2, y=y)
+
+    def step():
+        layer.forward(x, wr, w13, w2, y=y)
+        layer.backward(dy, x, wr, w13, w2, out=grads)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world > 1:
+            t = torch.tensor([v], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return v
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, site = layer.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site} during warm-up")
+    counts = layer.view("counts").cpu()
+
+    # ---- timed region: K steps of forward + backward, per-kernel events on the launching stream
+    sampler = ClockSampler(torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    N.trace_start(40 * args.steps + 16)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    trace = N.trace_stop()
+    clocks = sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+    code, site = layer.status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} at site {site}")
+
+    # ---- forward only
+    for _ in range(2):
+        fwd()
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fwd()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    x_h = x.cpu().pin_memory()
+    dy_h = dy.cpu().pin_memory()
+    y_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    dx_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    dy_d = torch.empty_like(dy)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        dy_d.copy_(dy_h, non_blocking=True)
+        layer.forward(x_d, wr, w13, w2, y=y)
+        layer.backward(dy_d, x_d, wr, w13, w2, out=grads)
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(grads["dx"], non_blocking=True)
+
+    e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    kb = kernel_bytes(shp)
+    kf = kernel_flops(shp)
+    per_kernel = {}
+    for name, t in trace.items():
+        avg = t["total_ms"] / t["launches"]
+        e = {"launches": t["launches"], "avg_ms": round(avg, 4), "share": None}
+        if name in kb:
+            e["GBps"] = round(kb[name] / (avg * 1e-3) / 1e9, 1)
+        if name in kf:
+            e["TFLOPs"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+        per_kernel[name] = e
+    tot = sum(t["total_ms"] for t in trace.values())
+    for name, t in trace.items():
+        per_kernel[name]["share"] = round(t["total_ms"] / tot, 4)
+    dom = max(trace, key=lambda n: trace[n]["total_ms"])
+    dom_avg_s = trace[dom]["total_ms"] / trace[dom]["launches"] * 1e-3
+    achieved = kb[dom] / dom_avg_s / 1e9
+    traffic = load_traffic().get(dom)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": dom,
+                "peak_source": peak_kind}
+    gemm_names = [n for n in kf if n in trace]
+    gemm_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in gemm_names)
+    gemm_flop = sum(kf[n] for n in gemm_names)
+    gemm_tflops = gemm_flop / (gemm_ms * 1e-3) / 1e12
+    fwd_gemm = [n for n in ("router_gemm", "gemm1_swiglu", "gemm2") if n in trace]
+    fwd_gemm_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in fwd_gemm)
+    fwd_gemm_tflops = sum(kf[n] for n in fwd_gemm) / (fwd_gemm_ms * 1e-3) / 1e12
+    launches = sum(t["launches"] for t in trace.values())
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        times, cores = cpu_sample_subprocess(CPU_SAMPLE["T"], CPU_SAMPLE["E"], repeats=1)
+        cpu = {"value": CPU_SAMPLE["T"] / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample_desc(CPU_SAMPLE["T"], CPU_SAMPLE["E"]), "seconds": round(times[0], 2)}
+
+    step_bytes = 2 * T * H * 2
+    line = {
+        "metric": METRIC, "value": round(T * world / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
+        "config": {"workload": shp.name, "T": T, "hidden": H, "experts": E, "intermediate": I, "top_k": k,
+                   "router": "sigmoid+renorm", "passes": "fwd+bwd",
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass)",
+                   "expert_rows_min_max": [int(counts.min()), int(counts.max())]},
+        "fwd_tokens_per_s": round(T * world / (fwd_ms * 1e-3), 1), "fwd_ms": round(fwd_ms, 4),
+        "tflops_fwd_bwd": round(W.algorithmic_flops(shp, "fwd+bwd") / (ms * 1e-3) / 1e12, 1),
+        "grouped_gemm": {"tflops_fwd_bwd": round(gemm_tflops, 1),
+                         "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
+                         "tflops_fwd": round(fwd_gemm_tflops, 1),
+                         "frac_bf16_peak_fwd": round(fwd_gemm_tflops / peaks["bf16_tflops_sustained"], 4),
+                         "peak": peaks["bf16_tflops_sustained"], "peak_source": peak_kind + " (sustained)"},
+        "roofline": roofline,
+        "kernels": per_kernel,
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": step_bytes,
+                "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
+                "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step"},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-sample":
+        T, E, rep = int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4])
+        print(json.dumps(cpu_sample_run(T, E, rep)))
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_mok(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -30,7 +30,8 @@
  *     the same inputs, descriptor and device: every reduction runs in a fixed order and
  *     no floating-point atomics are used.
  *   - No C++ exception crosses this boundary.  No global mutable state besides a per-device
- *     cache of the SM count and the driver entry point used to encode TMA descriptors.
+ *     cache of the SM count, the driver entry point used to encode TMA descriptors and the
+ *     optional per-kernel trace (mok_trace_start / mok_trace_stop).
  */
 #ifndef MOK_H_
 #define MOK_H_
@@ -165,6 +166,22 @@ mok_status mok_read_status(void* ws, size_t ws_bytes, void* stream, int32_t* dev
  * limit in milliseconds; the wait gives up, records MOK_ERR_TIMEOUT in the status word
  * of ws and the kernel returns normally.  Used to show that a stuck wait ends cleanly. */
 mok_status mok_test_bounded_wait(void* ws, size_t ws_bytes, int32_t limit_ms, void* stream);
+
+/* Per-kernel timing (tracing; no counterpart on the pages).  mok_trace_start enables it
+ * for the whole process: every kernel the library launches from then on is bracketed by
+ * two CUDA events recorded on the stream it is launched on, up to max_launches launches.
+ * mok_trace_stop synchronises those events, sums the elapsed time per kernel name into
+ * out[0..cap) (names in launch order of first appearance), stores the number of entries in
+ * *n_out, frees the events and disables tracing.  Host-side state only; not thread-safe;
+ * do not start it while a stream capture is active. */
+typedef struct {
+  char name[32];
+  int32_t launches;
+  float total_ms;
+} mok_trace_entry;
+
+mok_status mok_trace_start(int32_t max_launches);
+mok_status mok_trace_stop(mok_trace_entry* out, int32_t cap, int32_t* n_out);
 
 /* Human-readable name of a status code. */
 const char* mok_status_string(mok_status s);

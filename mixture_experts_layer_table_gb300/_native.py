@@ -46,8 +46,12 @@ class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in LAYOUT_FIELDS]
 
 
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_float)]
+
+
 EXPORTS = ["mok_get_layout", "mok_schedule", "mok_moe_forward", "mok_moe_backward", "mok_read_status",
-           "mok_test_bounded_wait", "mok_status_string", "mok_min_minibatch"]
+           "mok_test_bounded_wait", "mok_status_string", "mok_min_minibatch", "mok_trace_start", "mok_trace_stop"]
 
 _lib = None
 
@@ -72,6 +76,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mok_status_string.restype = ctypes.c_char_p
     lib.mok_min_minibatch.argtypes = [I32, I32]
     lib.mok_min_minibatch.restype = I32
+    lib.mok_trace_start.argtypes = [I32]
+    lib.mok_trace_stop.argtypes = [ctypes.POINTER(TraceEntry), I32, ctypes.POINTER(I32)]
     for name in EXPORTS:
         if name != "mok_status_string" and name != "mok_min_minibatch":
             getattr(lib, name).restype = I32
@@ -150,6 +156,21 @@ def read_status(ws, stream=None):
     out = (ctypes.c_int32 * 2)()
     _check("mok_read_status", load().mok_read_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream), out))
     return int(out[0]), int(out[1])
+
+
+def trace_start(max_launches: int = 4096):
+    """Starts per-kernel CUDA-event timing of every launch the library makes."""
+    _check("mok_trace_start", load().mok_trace_start(max_launches))
+
+
+def trace_stop() -> Dict[str, Dict[str, float]]:
+    """Stops timing; returns {kernel: {"launches": n, "total_ms": t}} in first-launch order."""
+    cap = 64
+    arr = (TraceEntry * cap)()
+    n = ctypes.c_int32(0)
+    _check("mok_trace_stop", load().mok_trace_stop(arr, cap, ctypes.byref(n)))
+    return {arr[i].name.decode(): {"launches": int(arr[i].launches), "total_ms": float(arr[i].total_ms)}
+            for i in range(n.value)}
 
 
 def test_bounded_wait(ws, limit_ms: int, stream=None):

@@ -5,7 +5,9 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
+#include <new>
 
 #include "kernels.cuh"
 #include "mok.h"
@@ -95,6 +97,39 @@ const T* at(const void* base, int64_t off) {
     if ((call) != cudaSuccess) return MOK_ERR_CUDA; \
   } while (0)
 
+// ------------------------------------------------------------------ per-kernel trace
+struct TraceRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+
+struct Trace {
+  std::mutex mu;
+  bool on = false;
+  int cap = 0;
+  int used = 0;
+  TraceRec* recs = nullptr;
+} g_trace;
+
+// Records a start event before and a stop event after the launch `call` on stream `st`.
+template <typename F>
+cudaError_t traced(const char* name, cudaStream_t st, F&& call) {
+  TraceRec* rec = nullptr;
+  if (g_trace.on) {
+    std::lock_guard<std::mutex> lock(g_trace.mu);
+    if (g_trace.on && g_trace.used < g_trace.cap) {
+      rec = &g_trace.recs[g_trace.used++];
+      rec->name = name;
+    }
+  }
+  if (rec) cudaEventRecord(rec->start, st);
+  const cudaError_t err = call();
+  if (rec) cudaEventRecord(rec->stop, st);
+  return err;
+}
+
+#define MOK_LAUNCH(name, st, expr) MOK_CUDA(traced(name, st, [&] { return (expr); }))
+
 }  // namespace
 
 extern "C" {
@@ -145,10 +180,10 @@ mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_ro
   int* status = at<int>(ws, L.status);
   float* logits = at<float>(ws, L.logits);
   MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
-  if (have_router) MOK_CUDA(mok::launch_router_gemm(x, w_router, d->T, d->H, d->E, logits, status, n_sm, st));
-  MOK_CUDA(mok::launch_topk(have_router ? logits : nullptr, router_bias, given_topk, d->T, d->E, d->k, d->router,
+  if (have_router) MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, d->T, d->H, d->E, logits, status, n_sm, st));
+  MOK_LAUNCH("topk", st, mok::launch_topk(have_router ? logits : nullptr, router_bias, given_topk, d->T, d->E, d->k, d->router,
                             d->renorm, d->route_scale, topk_idx, gates, nullptr, status, st));
-  MOK_CUDA(mok::launch_schedule(topk_idx, nullptr, d->T * d->k, d->E, counts, offsets, row_of, src_of, nullptr,
+  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, nullptr, d->T * d->k, d->E, counts, offsets, row_of, src_of, nullptr,
                                 nullptr, status, st));
   return MOK_OK;
 }
@@ -185,21 +220,21 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
 
   MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
   // 1. router logits x W_r^T (tensor cores, fp32 accumulate)
-  MOK_CUDA(mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
+  MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
   // 2. scores, top-k and gates
-  MOK_CUDA(mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm, d->route_scale,
+  MOK_LAUNCH("topk", st, mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm, d->route_scale,
                             topk_idx, gates, at<float>(ctx, L.scores), status, st));
   // 3. schedule table
-  MOK_CUDA(mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of, src_of,
+  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of, src_of,
                                 tile_off, at<float>(ctx, L.gate_row), status, st));
   // 4. pull dispatch into expert-contiguous rows
-  MOK_CUDA(mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
+  MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
   // 5. grouped GEMM1 with the SwiGLU epilogue
-  MOK_CUDA(mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, status, n_sm, st));
+  MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, status, n_sm, st));
   // 6. grouped GEMM2
-  MOK_CUDA(mok::launch_gemm2(act, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
+  MOK_LAUNCH("gemm2", st, mok::launch_gemm2(act, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
   // 7. weighted merge in fixed order
-  MOK_CUDA(mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
+  MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
 }
 
@@ -242,22 +277,22 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   float* dl = at<float>(ws, L.dlogits);
 
   // 1. reverse combine: pull the upstream gradient rows into expert order
-  MOK_CUDA(mok::launch_gather_rows(dy, src_of, k, R, H, dy_g, n_sm, st));
+  MOK_LAUNCH("gather_dy", st, mok::launch_gather_rows(dy, src_of, k, R, H, dy_g, n_sm, st));
   // 2. dA' = dY_g W2[e]; epilogue: SwiGLU backward, g * a, and per-tile <dA', a>
-  MOK_CUDA(mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu, gact, dg_part,
+  MOK_LAUNCH("dgrad_swiglu", st, mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu, gact, dg_part,
                                     status, n_sm, st));
   // 3. dX_g = [dh | du] W13[e]
-  MOK_CUDA(mok::launch_dgrad_x(dhu, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
+  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
   // 4. dW2[e] = dY_g^T (g a), 5. dW13[e] = [dh | du]^T x_g, reduced over the expert's rows
-  MOK_CUDA(mok::launch_wgrad(dy_g, H, gact, I, R, E, offsets, dw2, status, n_sm, st));
-  MOK_CUDA(mok::launch_wgrad(dhu, 2 * I, x_g, H, R, E, offsets, dw13, status, n_sm, st));
+  MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(dy_g, H, gact, I, R, E, offsets, dw2, status, n_sm, st));
+  MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(dhu, 2 * I, x_g, H, R, E, offsets, dw13, status, n_sm, st));
   // 6. gate and router-logit gradients, 7. router weight gradient
-  MOK_CUDA(mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
+  MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
                                       d->renorm, d->route_scale, dgates, dl, st));
-  MOK_CUDA(mok::launch_router_wgrad(dl, x, offsets, src_of, T, H, E, k, d->router == MOK_ROUTER_SIGMOID ? 1 : 0,
+  MOK_LAUNCH("router_wgrad", st, mok::launch_router_wgrad(dl, x, offsets, src_of, T, H, E, k, d->router == MOK_ROUTER_SIGMOID ? 1 : 0,
                                     dw_router, st));
   // 8. reverse dispatch: dX[t] = sum_j dX_g[row_of[t,j]] + dl[t] W_r
-  MOK_CUDA(mok::launch_combine(dx_g, nullptr, row_of, T, k, H, dl, w_router, topk_idx, E,
+  MOK_LAUNCH("combine_dx", st, mok::launch_combine(dx_g, nullptr, row_of, T, k, H, dl, w_router, topk_idx, E,
                                d->router == MOK_ROUTER_SOFTMAX ? 1 : 0, dx, n_sm, st));
   return MOK_OK;
 }
@@ -275,9 +310,71 @@ mok_status mok_read_status(void* ws, size_t ws_bytes, void* stream, int32_t* dev
 
 mok_status mok_test_bounded_wait(void* ws, size_t ws_bytes, int32_t limit_ms, void* stream) {
   if (!ws || ws_bytes < 16 || limit_ms < 1 || limit_ms > 10000) return MOK_ERR_INVALID_ARG;
-  MOK_CUDA(mok::launch_test_wait(static_cast<int*>(ws), (long long)limit_ms * 1000000LL,
+  MOK_LAUNCH("test_wait", static_cast<cudaStream_t>(stream), mok::launch_test_wait(static_cast<int*>(ws), (long long)limit_ms * 1000000LL,
                                  static_cast<cudaStream_t>(stream)));
   return MOK_OK;
+}
+
+mok_status mok_trace_start(int32_t max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20)) return MOK_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_trace.mu);
+  if (g_trace.on) return MOK_ERR_INVALID_ARG;
+  g_trace.recs = new (std::nothrow) TraceRec[max_launches];
+  if (!g_trace.recs) return MOK_ERR_INVALID_ARG;
+  for (int i = 0; i < max_launches; ++i) {
+    if (cudaEventCreate(&g_trace.recs[i].start) != cudaSuccess ||
+        cudaEventCreate(&g_trace.recs[i].stop) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) {
+        cudaEventDestroy(g_trace.recs[j].start);
+        cudaEventDestroy(g_trace.recs[j].stop);
+      }
+      delete[] g_trace.recs;
+      g_trace.recs = nullptr;
+      return MOK_ERR_CUDA;
+    }
+  }
+  g_trace.cap = max_launches;
+  g_trace.used = 0;
+  g_trace.on = true;
+  return MOK_OK;
+}
+
+mok_status mok_trace_stop(mok_trace_entry* out, int32_t cap, int32_t* n_out) {
+  std::lock_guard<std::mutex> lock(g_trace.mu);
+  if (!g_trace.on) return MOK_ERR_INVALID_ARG;
+  g_trace.on = false;
+  mok_status st = MOK_OK;
+  int n = 0;
+  for (int i = 0; i < g_trace.used; ++i) {
+    TraceRec& r = g_trace.recs[i];
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+      st = MOK_ERR_CUDA;
+      continue;
+    }
+    int slot = -1;
+    for (int j = 0; j < n; ++j)
+      if (std::strncmp(out[j].name, r.name, sizeof(out[j].name)) == 0) slot = j;
+    if (slot < 0) {
+      if (out == nullptr || n >= cap) continue;
+      slot = n++;
+      std::memset(out[slot].name, 0, sizeof(out[slot].name));
+      std::strncpy(out[slot].name, r.name, sizeof(out[slot].name) - 1);
+      out[slot].launches = 0;
+      out[slot].total_ms = 0.0f;
+    }
+    out[slot].launches += 1;
+    out[slot].total_ms += ms;
+  }
+  for (int i = 0; i < g_trace.cap; ++i) {
+    cudaEventDestroy(g_trace.recs[i].start);
+    cudaEventDestroy(g_trace.recs[i].stop);
+  }
+  delete[] g_trace.recs;
+  g_trace.recs = nullptr;
+  g_trace.cap = g_trace.used = 0;
+  if (n_out) *n_out = n;
+  return st;
 }
 
 }  // extern "C"
