@@ -68,8 +68,10 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *   precision    mok_precision of the expert GEMMs
  *   minibatch    ring forward only: rows per minibatch (0 = the whole call)
  *   ring_bytes   ring forward only: bytes of the fixed token ring (0 = no ring)
- *   flags        bit 0: MOK_FLAG_TEST_STUCK_WAIT (tests only, see mok_test_bounded_wait)
+ *   flags        MOK_FLAG_WGRAD_BF16: the expert weight gradients dw13 / dw2 of
+ *                mok_moe_backward are bf16 instead of the default f32
  * T*k*max(H, 2I) must stay below 2^31 elements. */
+#define MOK_FLAG_WGRAD_BF16 1
 typedef struct {
   int32_t T, H, I, E, k;
   int32_t router;
@@ -97,17 +99,21 @@ typedef struct {
   int64_t tile_off;   /* i32 [E+1]    prefix sum of ceil(counts/128) (GEMM m-tiles) */
   int64_t gate_row;   /* f32 [T*k]    gate of each sorted row */
   int64_t x_g;        /* bf16 [T*k][H]  dispatched (expert-sorted) token rows */
-  int64_t hu;         /* bf16 [T*k][2I] gate and up projections h | u */
+  int64_t hu;         /* f32 [T*k][2I]  gate and up projections h | u */
   int64_t ctx_bytes;
-  /* ws */
+  /* ws.  "hi/lo" pairs hold v as bf16 hi = bf16(v) plus bf16 lo = bf16(v - hi), so that a
+   * GEMM operand produced inside the layer keeps about 16 significant bits. */
   int64_t status;     /* i32 [4]      device status word: code, site */
   int64_t logits;     /* f32 [T][E]   router logits */
-  int64_t act;        /* bf16 [T*k][I]  SwiGLU output a = silu(h) * u */
-  int64_t expert_out; /* bf16 [T*k][H]  expert outputs o (unweighted) */
+  int64_t act;        /* bf16 [T*k][I]  SwiGLU output a = silu(h) * u, hi part */
+  int64_t act_lo;     /* bf16 [T*k][I]  lo part */
+  int64_t expert_out; /* f32 [T*k][H]   expert outputs o (unweighted) */
   int64_t dy_g;       /* bf16 [T*k][H]  dispatched upstream gradient (backward) */
-  int64_t dhu;        /* bf16 [T*k][2I] gradient of h | u (backward) */
-  int64_t gact;       /* bf16 [T*k][I]  gate * a, operand of dW2 (backward) */
-  int64_t dx_g;       /* bf16 [T*k][H]  per-row input gradient (backward) */
+  int64_t dhu;        /* bf16 [T*k][2I] gradient of h | u, hi part (backward) */
+  int64_t dhu_lo;     /* bf16 [T*k][2I] lo part */
+  int64_t gact;       /* bf16 [T*k][I]  gate * a, operand of dW2, hi part (backward) */
+  int64_t gact_lo;    /* bf16 [T*k][I]  lo part */
+  int64_t dx_g;       /* f32 [T*k][H]   per-row input gradient (backward) */
   int64_t dg_part;    /* f32 [T*k][I/256] partial gate gradients per GEMM column tile */
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
   int64_t ws_bytes;
@@ -145,8 +151,9 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
 
 /* Layer backward for upstream gradient dy [T][H] bf16, using the ctx written by the
  * matching mok_moe_forward (same desc, inputs and weights).  Outputs:
- *   dx [T][H] bf16, dw_router [E][H] f32, dw13 [E][2I][H] bf16, dw2 [E][H][I] bf16,
- *   dgates [T][k] f32 (nullable): gradient w.r.t. each selected gate.
+ *   dx [T][H] bf16, dw_router [E][H] f32, dw13 [E][2I][H] and dw2 [E][H][I] in f32 (bf16
+ *   with MOK_FLAG_WGRAD_BF16), dgates [T][k] f32 (nullable): gradient w.r.t. each gate.
+ *   An expert that received no rows gets an all-zero weight gradient.
  * The selection is held fixed; the router bias gets no gradient.  The gate gradient
  * <dA', a> of each row is formed in the SwiGLU-backward epilogue (the router-weight
  * gradient "fused into the SwiGLU backward" of the pages' benchmark section). */

@@ -36,8 +36,9 @@ class LayerDesc(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
-                 "x_g", "hu", "ctx_bytes", "status", "logits", "act", "expert_out", "dy_g", "dhu", "gact", "dx_g",
-                 "dg_part", "dlogits", "ws_bytes"]
+                 "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
+                 "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ws_bytes"]
+FLAG_WGRAD_BF16 = 1
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
 
@@ -180,9 +181,10 @@ def test_bounded_wait(ws, limit_ms: int, stream=None):
 
 _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.float32, "counts": torch.int32,
                "offsets": torch.int32, "row_of": torch.int32, "src_of": torch.int32, "tile_off": torch.int32,
-               "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.bfloat16, "status": torch.int32,
-               "logits": torch.float32, "act": torch.bfloat16, "expert_out": torch.bfloat16,
-               "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "gact": torch.bfloat16, "dx_g": torch.bfloat16,
+               "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.float32, "status": torch.int32,
+               "logits": torch.float32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
+               "expert_out": torch.float32, "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "dhu_lo": torch.bfloat16,
+               "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
                "dg_part": torch.float32, "dlogits": torch.float32}
 
 
@@ -201,8 +203,13 @@ class MoELayer:
         return {"topk_idx": (d.T, d.k), "gates": (d.T, d.k), "scores": (d.T, d.E), "counts": (d.E,),
                 "offsets": (d.E + 1,), "row_of": (R,), "src_of": (R,), "tile_off": (d.E + 1,), "gate_row": (R,),
                 "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "act": (R, d.I),
-                "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I), "gact": (R, d.I),
+                "act_lo": (R, d.I), "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I),
+                "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
                 "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E)}[name]
+
+    def view_split(self, name: str) -> torch.Tensor:
+        """hi + lo of a split operand ("act", "dhu", "gact") as one float32 tensor."""
+        return self.view(name).float() + self.view(name + "_lo").float()
 
     def view(self, name: str) -> torch.Tensor:
         """A typed view of one saved tensor (ctx) or temporary (ws)."""
@@ -226,10 +233,11 @@ class MoELayer:
         d = self.desc
         dev = dy.device
         if out is None:
+            wdt = torch.bfloat16 if (d.flags & FLAG_WGRAD_BF16) else torch.float32
             out = {"dx": torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev),
                    "dw_router": torch.empty((d.E, d.H), dtype=torch.float32, device=dev),
-                   "dw13": torch.empty((d.E, 2 * d.I, d.H), dtype=torch.bfloat16, device=dev),
-                   "dw2": torch.empty((d.E, d.H, d.I), dtype=torch.bfloat16, device=dev),
+                   "dw13": torch.empty((d.E, 2 * d.I, d.H), dtype=wdt, device=dev),
+                   "dw2": torch.empty((d.E, d.H, d.I), dtype=wdt, device=dev),
                    "dgates": torch.empty((d.T, d.k), dtype=torch.float32, device=dev)}
         moe_backward(d, dy, x, w_router, w13, w2, self.ctx, out["dx"], out["dw_router"], out["dw13"], out["dw2"],
                      out["dgates"], self.ws, stream)

@@ -66,17 +66,20 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->tile_off = take((E + 1) * 4);
   L->gate_row = take(R * 4);
   L->x_g = take(R * H * 2);
-  L->hu = take(R * 2 * I * 2);
+  L->hu = take(R * 2 * I * 4);
   L->ctx_bytes = off;
   off = 0;
   L->status = take(16);
   L->logits = take(T * E * 4);
   L->act = take(R * I * 2);
-  L->expert_out = take(R * H * 2);
+  L->act_lo = take(R * I * 2);
+  L->expert_out = take(R * H * 4);
   L->dy_g = take(R * H * 2);
   L->dhu = take(R * 2 * I * 2);
+  L->dhu_lo = take(R * 2 * I * 2);
   L->gact = take(R * I * 2);
-  L->dx_g = take(R * H * 2);
+  L->gact_lo = take(R * I * 2);
+  L->dx_g = take(R * H * 4);
   L->dg_part = take(R * (I / 256) * 4);
   L->dlogits = take(T * E * 4);
   L->ws_bytes = off;
@@ -213,9 +216,10 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   int32_t* row_of = at<int32_t>(ctx, L.row_of);
   int32_t* src_of = at<int32_t>(ctx, L.src_of);
   void* x_g = at<char>(ctx, L.x_g);
-  void* hu = at<char>(ctx, L.hu);
+  float* hu = at<float>(ctx, L.hu);
   void* act = at<char>(ws, L.act);
-  void* o = at<char>(ws, L.expert_out);
+  void* act_lo = at<char>(ws, L.act_lo);
+  float* o = at<float>(ws, L.expert_out);
   float* logits = at<float>(ws, L.logits);
 
   MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
@@ -230,9 +234,10 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   // 4. pull dispatch into expert-contiguous rows
   MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
   // 5. grouped GEMM1 with the SwiGLU epilogue
-  MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, status, n_sm, st));
-  // 6. grouped GEMM2
-  MOK_LAUNCH("gemm2", st, mok::launch_gemm2(act, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
+  MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
+                                                          status, n_sm, st));
+  // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
+  MOK_LAUNCH("gemm2", st, mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
   // 7. weighted merge in fixed order
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
@@ -268,24 +273,30 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   const int32_t* src_of = at<int32_t>(ctx, L.src_of);
   const float* gate_row = at<float>(ctx, L.gate_row);
   const void* x_g = at<char>(ctx, L.x_g);
-  const void* hu = at<char>(ctx, L.hu);
+  const float* hu = at<float>(ctx, L.hu);
   void* dy_g = at<char>(ws, L.dy_g);
   void* dhu = at<char>(ws, L.dhu);
+  void* dhu_lo = at<char>(ws, L.dhu_lo);
   void* gact = at<char>(ws, L.gact);
-  void* dx_g = at<char>(ws, L.dx_g);
+  void* gact_lo = at<char>(ws, L.gact_lo);
+  float* dx_g = at<float>(ws, L.dx_g);
   float* dg_part = at<float>(ws, L.dg_part);
   float* dl = at<float>(ws, L.dlogits);
+  const int wgrad_f32 = (d->flags & MOK_FLAG_WGRAD_BF16) ? 0 : 1;
 
   // 1. reverse combine: pull the upstream gradient rows into expert order
   MOK_LAUNCH("gather_dy", st, mok::launch_gather_rows(dy, src_of, k, R, H, dy_g, n_sm, st));
   // 2. dA' = dY_g W2[e]; epilogue: SwiGLU backward, g * a, and per-tile <dA', a>
-  MOK_LAUNCH("dgrad_swiglu", st, mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu, gact, dg_part,
-                                    status, n_sm, st));
+  MOK_LAUNCH("dgrad_swiglu", st, mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu,
+                                                          dhu_lo, gact, gact_lo, dg_part, status, n_sm, st));
   // 3. dX_g = [dh | du] W13[e]
-  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
-  // 4. dW2[e] = dY_g^T (g a), 5. dW13[e] = [dh | du]^T x_g, reduced over the expert's rows
-  MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(dy_g, H, gact, I, R, E, offsets, dw2, status, n_sm, st));
-  MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(dhu, 2 * I, x_g, H, R, E, offsets, dw13, status, n_sm, st));
+  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, dhu_lo, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
+  // 4. dW2[e] = (g a)^T dY_g stored as [H][I]; 5. dW13[e] = x_g^T [dh | du] stored as [2I][H];
+  //    both reduced over the expert's rows, the contiguous output dimension on the TMEM lanes
+  MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(gact, gact_lo, I, dy_g, nullptr, H, R, E, offsets, dw2, wgrad_f32,
+                                               status, n_sm, st));
+  MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(x_g, nullptr, H, dhu, dhu_lo, 2 * I, R, E, offsets, dw13, wgrad_f32,
+                                                status, n_sm, st));
   // 6. gate and router-logit gradients, 7. router weight gradient
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
                                       d->renorm, d->route_scale, dgates, dl, st));

@@ -62,14 +62,15 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
   return make_tmap(m, base, 3, dims, strides, box);
 }
 
-template <int MODE, int EPI>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid, cudaStream_t st) {
+template <int MODE, int EPI, int SPLIT, int BN>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& b2,
+                   const GemmArgs& args, int grid, cudaStream_t st) {
+  using C = GemmCfg<MODE, EPI, SPLIT, BN>;
   if (grid <= 0) return cudaSuccess;
-  auto kern = gemm_kernel<MODE, EPI>;
-  cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemm_smem_bytes(1024));
+  auto kern = gemm_kernel<MODE, EPI, SPLIT, BN>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
-  kern<<<grid, GEMM_THREADS, gemm_smem_bytes(args.E), st>>>(a, b, args);
+  kern<<<grid, GEMM_THREADS, C::smem_bytes(args.E), st>>>(a, a2, b, b2, args);
   return cudaGetLastError();
 }
 
@@ -91,21 +92,21 @@ int row_tiles_bound(int R, int E) { return (R + BM - 1) / BM + E; }
 cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
                                int* status, int n_sm, cudaStream_t st) {
   CUtensorMap ta, tb;
-  if (!tmap_2d(&ta, x, H, T, BK, BM) || !tmap_2d(&tb, w_router, H, E, BK, BN)) return cudaErrorInvalidValue;
+  if (!tmap_2d(&ta, x, H, T, BK, BM) || !tmap_2d(&tb, w_router, H, E, BK, 256)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(1, nullptr, nullptr, status);
   g.M = T;
   g.N = E;
   g.K = H;
   g.out0 = logits;
   g.ld0 = E;
-  const int tiles = ((T + BM - 1) / BM) * ((E + BN - 1) / BN);
+  const int tiles = ((T + BM - 1) / BM) * ((E + 255) / 256);
   g.total_tiles = tiles;
-  return launch<MODE_DENSE, EPI_F32>(ta, tb, g, std::min(tiles, n_sm), st);
+  return launch<MODE_DENSE, EPI_F32, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(tiles, n_sm), st);
 }
 
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
-                                const int32_t* offsets, const int32_t* tile_off, void* hu, void* act,
-                                int* status, int n_sm, cudaStream_t st) {
+                                const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
+                                void* act_lo, int* status, int n_sm, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!tmap_2d(&ta, x_g, H, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, BK, 128)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
@@ -114,29 +115,33 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
   g.I = I;
   g.out0 = hu;
   g.ld0 = 2LL * I;
-  g.out1 = act;
+  g.out1 = act_hi;
+  g.out2 = act_lo;
   g.ld1 = I;
   const int bound = row_tiles_bound(R, E) * (I / 128);
-  return launch<MODE_ROWS, EPI_SWIGLU>(ta, tb, g, std::min(bound, n_sm), st);
+  return launch<MODE_ROWS, EPI_SWIGLU, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st);
 }
 
-cudaError_t launch_gemm2(const void* act, const void* w2, int R, int H, int I, int E, const int32_t* offsets,
-                         const int32_t* tile_off, void* out, int* status, int n_sm, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  if (!tmap_2d(&ta, act, I, R, BK, BM) || !tmap_3d(&tb, w2, I, H, E, BK, BN)) return cudaErrorInvalidValue;
+cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
+                         const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
+                         cudaStream_t st) {
+  CUtensorMap ta, ta2, tb;
+  if (!tmap_2d(&ta, act_hi, I, R, BK, BM) || !tmap_2d(&ta2, act_lo, I, R, BK, BM) ||
+      !tmap_3d(&tb, w2, I, H, E, BK, 256))
+    return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
   g.N = H;
   g.K = I;
   g.out0 = out;
   g.ld0 = H;
-  const int bound = row_tiles_bound(R, E) * (H / BN);
-  return launch<MODE_ROWS, EPI_BF16>(ta, tb, g, std::min(bound, n_sm), st);
+  const int bound = row_tiles_bound(R, E) * (H / 256);
+  return launch<MODE_ROWS, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st);
 }
 
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
-                                const int32_t* offsets, const int32_t* tile_off, const void* hu,
-                                const float* gate_row, void* dhu, void* gact, float* dg_part, int* status,
-                                int n_sm, cudaStream_t st) {
+                                const int32_t* offsets, const int32_t* tile_off, const float* hu,
+                                const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,
+                                float* dg_part, int* status, int n_sm, cudaStream_t st) {
   CUtensorMap ta, tb;
   // A = dY_g [R][H] (K = H, K-major); B = W2[e] [H][I] seen as [K][N] (N contiguous)
   if (!tmap_2d(&ta, dy_g, H, R, BK, BM) || !tmap_3d(&tb, w2, I, H, E, 64, BK)) return cudaErrorInvalidValue;
@@ -144,43 +149,65 @@ cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, 
   g.N = I;
   g.K = H;
   g.I = I;
-  g.out0 = dhu;
+  g.out0 = dhu_hi;
+  g.out1 = dhu_lo;
   g.ld0 = 2LL * I;
-  g.out1 = gact;
+  g.out2 = gact_hi;
+  g.out3 = gact_lo;
   g.ld1 = I;
-  g.out2 = dg_part;
-  g.ld2 = I / BN;
-  g.hu = reinterpret_cast<const __nv_bfloat16*>(hu);
+  g.out4 = dg_part;
+  g.ld2 = I / 256;
+  g.hu = hu;
   g.gate_row = gate_row;
-  const int bound = row_tiles_bound(R, E) * (I / BN);
-  return launch<MODE_DGRAD, EPI_SWIGLU_BWD>(ta, tb, g, std::min(bound, n_sm), st);
+  const int bound = row_tiles_bound(R, E) * (I / 256);
+  return launch<MODE_DGRAD, EPI_SWIGLU_BWD, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st);
 }
 
-cudaError_t launch_dgrad_x(const void* dhu, const void* w13, int R, int H, int I, int E, const int32_t* offsets,
-                           const int32_t* tile_off, void* dx_g, int* status, int n_sm, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  // A = dHU [R][2I] (K = 2I); B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)
-  if (!tmap_2d(&ta, dhu, 2 * I, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, 64, BK)) return cudaErrorInvalidValue;
+cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w13, int R, int H, int I, int E,
+                           const int32_t* offsets, const int32_t* tile_off, float* dx_g, int* status, int n_sm,
+                           cudaStream_t st) {
+  CUtensorMap ta, ta2, tb;
+  // A = dHU [R][2I] (K = 2I) as hi + lo; B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)
+  if (!tmap_2d(&ta, dhu_hi, 2 * I, R, BK, BM) || !tmap_2d(&ta2, dhu_lo, 2 * I, R, BK, BM) ||
+      !tmap_3d(&tb, w13, H, 2 * I, E, 64, BK))
+    return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
   g.N = H;
   g.K = 2 * I;
   g.out0 = dx_g;
   g.ld0 = H;
-  const int bound = row_tiles_bound(R, E) * (H / BN);
-  return launch<MODE_DGRAD, EPI_BF16>(ta, tb, g, std::min(bound, n_sm), st);
+  const int bound = row_tiles_bound(R, E) * (H / 256);
+  return launch<MODE_DGRAD, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st);
 }
 
-cudaError_t launch_wgrad(const void* a_rows, int M, const void* b_rows, int N, int R, int E,
-                         const int32_t* offsets, void* dw, int* status, int n_sm, cudaStream_t st) {
-  CUtensorMap ta, tb;
-  if (!tmap_2d(&ta, a_rows, M, R, 64, BK) || !tmap_2d(&tb, b_rows, N, R, 64, BK)) return cudaErrorInvalidValue;
+cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
+                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int n_sm,
+                         cudaStream_t st) {
+  constexpr int WBN = 128;
+  CUtensorMap ta, ta2, tb, tb2;
+  if (!tmap_2d(&ta, a_hi, M, R, 64, BK) || !tmap_2d(&tb, b_hi, N, R, 64, BK)) return cudaErrorInvalidValue;
+  ta2 = ta;
+  tb2 = tb;
+  if (a_lo && !tmap_2d(&ta2, a_lo, M, R, 64, BK)) return cudaErrorInvalidValue;
+  if (b_lo && !tmap_2d(&tb2, b_lo, N, R, 64, BK)) return cudaErrorInvalidValue;
+  if (a_lo && b_lo) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, nullptr, status);
   g.M = M;
   g.N = N;
   g.out0 = dw;
-  const int tiles = E * (M / BM) * (N / BN);
+  const int tiles = E * (M / BM) * (N / WBN);
   g.total_tiles = tiles;
-  return launch<MODE_WGRAD, EPI_BF16>(ta, tb, g, std::min(tiles, n_sm), st);
+  const int grid = std::min(tiles, n_sm);
+  if (a_lo) {
+    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st)
+                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st);
+  }
+  if (b_lo) {
+    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st)
+                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st);
+  }
+  return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st)
+                 : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st);
 }
 
 // ----------------------------------------------------------------------------- wait test

@@ -1,13 +1,18 @@
 // Persistent tcgen05 GEMM for the expert-grouped products of one MoE layer (sm_103a).
 //
 // One CTA per SM, 6 warps:
-//   warp 0      TMA producer: loads A and B tiles of 64 K-elements into a 4-stage ring
-//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32) into TMEM, 128 x 256 tile
+//   warp 0      TMA producer: loads A and B tiles of 64 K-elements into a ring of stages
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> f32) into TMEM, 128 x BN tile
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused elementwise work, stores
-// The accumulator is double-buffered in TMEM (2 x 256 of the 512 columns), so the epilogue
-// of tile i overlaps the main loop of tile i+1.  Tiles are dealt round-robin over the CTAs
-// in a fixed order, so the result does not depend on timing (each output element is owned
-// by exactly one tile and reduced over K in a fixed order).
+// The accumulator is double-buffered in TMEM (2 x BN columns), so the epilogue of tile i
+// overlaps the main loop of tile i+1.  Tiles are dealt round-robin over the CTAs in a fixed
+// order; every output element is owned by one tile and reduced over K in a fixed order, so
+// results do not depend on timing.
+//
+// Split operands: an operand produced by this layer (SwiGLU output, its gradient) is kept as
+// a pair of bf16 tensors hi + lo with lo = bf16(v - hi), about 16 significant bits.  The MMA
+// warp issues hi and lo products into the same fp32 accumulator, so the GEMM sees the operand
+// at nearly fp32 precision while the tensor cores stay on the bf16 path.
 //
 // Modes (how A, B and the tiles are laid out):
 //   MODE_DENSE  A [M][K], B [N][K], both K-major                  (router logits)
@@ -16,7 +21,8 @@
 //   MODE_DGRAD  A = rows [R][K] K-major, B [E][K][N] (N contiguous: MN-major)
 //               (dA' = dY_g W2[e], dX_g = dHU W13[e])
 //   MODE_WGRAD  A = rows [R][M] and B = rows [R][N], both MN-major; K runs over the rows of
-//               one expert (dW2[e] = dY_g^T (g a), dW13[e] = dHU^T x_g)
+//               one expert; output stored transposed, out[e][n][m], so that the 32 lanes of a
+//               warp (32 consecutive m) write 32 consecutive elements
 // Rows of one expert are contiguous (the schedule table); a 128-row tile that runs past its
 // expert reads the next expert's rows (discarded at the store) or TMA zero fill past R.
 // In MODE_WGRAD the rows past the expert's end inside the last K block are zeroed in shared
@@ -29,15 +35,10 @@
 namespace mok {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
 constexpr int GEMM_THREADS = 192;
-constexpr int ACC_COLS = 256;
-constexpr int TMEM_COLS = 512;
+constexpr int A_TILE = BM * BK * 2;      // 16 KB
+constexpr int SMEM_RING = 192 * 1024;    // bytes for the stage ring
 constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom column: 64 K rows x 128 B
 
 // Leading / stride byte offsets of the MN-major 128B-swizzled operand layout:
@@ -50,10 +51,11 @@ constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom colum
 #endif
 
 enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
-enum GemmEpi { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3 };
+enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5 };
+enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 
 struct GemmArgs {
-  int M;            // DENSE: rows of A; WGRAD: output rows per expert
+  int M;            // DENSE: rows of A; WGRAD: output rows per expert (the contiguous output dim)
   int N;            // output columns (per expert); SWIGLU: I (the tile pairs gate and up)
   int K;            // reduction length (DENSE / ROWS / DGRAD)
   int E;            // experts (groups)
@@ -64,8 +66,10 @@ struct GemmArgs {
   void* out0;
   void* out1;
   void* out2;
+  void* out3;
+  void* out4;
   long long ld0, ld1, ld2;
-  const __nv_bfloat16* hu;  // SWIGLU_BWD: saved h | u
+  const float* hu;          // SWIGLU_BWD: saved h | u (fp32)
   const float* gate_row;    // SWIGLU_BWD: gate of each row
   int* status;
 };
@@ -77,24 +81,32 @@ struct TileInfo {
   int nkb;    // K blocks
 };
 
-template <int MODE, int EPI>
-struct GemmTraits {
+template <int MODE, int EPI, int SPLIT, int BN_>
+struct GemmCfg {
+  static constexpr int BN = BN_;
   static constexpr bool kAmn = (MODE == MODE_WGRAD);
   static constexpr bool kBmn = (MODE == MODE_DGRAD || MODE == MODE_WGRAD);
+  static constexpr int B_TILE = BN * BK * 2;
+  static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
+  static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
+  static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES;
+  static constexpr int STAGES = (SMEM_RING / STAGE_BYTES) < 4 ? (SMEM_RING / STAGE_BYTES) : 4;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
   static __host__ __device__ int n_tiles(const GemmArgs& a) {
     return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + BN - 1) / BN;
   }
+  static __host__ __device__ size_t smem_bytes(int E) {
+    return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+  }
 };
 
-__host__ __device__ inline size_t gemm_smem_bytes(int E) {
-  return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
-}
-
-template <int MODE, int EPI>
-__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const int* s_off,
-                                                const int* s_toff) {
+template <int MODE, int EPI, int SPLIT, int BN_>
+__device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const int* s_off, const int* s_toff) {
+  using C = GemmCfg<MODE, EPI, SPLIT, BN_>;
   TileInfo t;
-  const int NT = GemmTraits<MODE, EPI>::n_tiles(a);
+  const int NT = C::n_tiles(a);
   if (MODE == MODE_DENSE) {
     const int MT = (a.M + BM - 1) / BM;
     t.e = 0;
@@ -108,20 +120,19 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
     const int per_e = MT * NT;
     t.e = g / per_e;
     const int rem = g - t.e * per_e;
-    t.m = rem / NT;
-    t.n = rem - t.m * NT;
+    t.n = rem / MT;  // m fastest: neighbouring CTAs share the B (N) columns of the expert
+    t.m = rem - t.n * MT;
     t.row0 = s_off[t.e];
     t.rows = s_off[t.e + 1] - t.row0;
     t.nkb = (t.rows + BK - 1) / BK;
   } else {
     // expert e owns tiles [tile_off[e]*NT, tile_off[e+1]*NT); inside, m runs fastest so the
     // m-tiles of one expert that share a weight tile are dealt to neighbouring CTAs.
-    int lo = 0, hi = a.E;  // find largest e with s_toff[e]*NT <= g
+    int lo = 0, hi = a.E;  // largest e with s_toff[e]*NT <= g (the last of equal starts owns tiles)
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (s_toff[mid] * NT <= g) lo = mid; else hi = mid;
     }
-    // skip experts with no tiles that share the same start
     t.e = lo;
     const int Me = s_toff[lo + 1] - s_toff[lo];
     const int local = g - s_toff[lo] * NT;
@@ -134,11 +145,35 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
   return t;
 }
 
-template <int MODE, int EPI>
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// hi = bf16(v), lo = bf16(v - hi) for a pair of values.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+__device__ __forceinline__ void store_u32x16(void* dst, const uint32_t (&p)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+}
+
+template <int MODE, int EPI, int SPLIT, int BN_>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                 const GemmArgs args) {
-  using Tr = GemmTraits<MODE, EPI>;
+  using C = GemmCfg<MODE, EPI, SPLIT, BN_>;
+  constexpr int BN = C::BN;
+  constexpr int STAGES = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -176,7 +211,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -184,7 +219,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int NT = Tr::n_tiles(args);
+  const int NT = C::n_tiles(args);
   const int total = args.total_tiles >= 0 ? args.total_tiles : s_toff[args.E] * NT;
 
   if (warp == 0) {
@@ -192,6 +227,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if (SPLIT == SPLIT_A) tma_prefetch_desc(&tmA2);
+      if (SPLIT == SPLIT_B) tma_prefetch_desc(&tmB2);
       const uint64_t pol_act = l2_policy_evict_last();
       const uint64_t pol_w = (MODE == MODE_WGRAD) ? pol_act : l2_policy_evict_first();
       int stage = 0;
@@ -199,7 +236,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int issued = 0;
       bool ok = true;
       for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-        const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+        const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY)) {
             ok = false;
@@ -207,7 +244,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           const uint32_t fb = full_bar(stage);
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sa2 = sa + A_TILE;                 // A lo (SPLIT_A)
+          const uint32_t sb = sa + A_TILE * C::A_TILES;
+          const uint32_t sb2 = sb + C::B_TILE;              // B lo (SPLIT_B)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const int k0 = kb * BK;
           if (MODE == MODE_DENSE) {
@@ -215,24 +254,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
           } else if (MODE == MODE_ROWS) {
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
+            if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, t.row0, pol_act);
             if (EPI == EPI_SWIGLU) {
               tma_load_3d(sb, &tmB, fb, k0, t.n * 128, t.e, pol_w);
-              tma_load_3d(sb + B_BYTES / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
+              tma_load_3d(sb + C::B_TILE / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
             } else {
               tma_load_3d(sb, &tmB, fb, k0, t.n * BN, t.e, pol_w);
             }
           } else if (MODE == MODE_DGRAD) {
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
+            if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, t.row0, pol_act);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < BN / 64; ++q)
               tma_load_3d(sb + q * MN_ATOM_BYTES, &tmB, fb, t.n * BN + q * 64, k0, t.e, pol_w);
           } else {  // WGRAD
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
+            for (int q = 0; q < 2; ++q) {
               tma_load_2d(sa + q * MN_ATOM_BYTES, &tmA, fb, t.m * BM + q * 64, t.row0 + k0, pol_act);
+              if (SPLIT == SPLIT_A)
+                tma_load_2d(sa2 + q * MN_ATOM_BYTES, &tmA2, fb, t.m * BM + q * 64, t.row0 + k0, pol_act);
+            }
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < BN / 64; ++q) {
               tma_load_2d(sb + q * MN_ATOM_BYTES, &tmB, fb, t.n * BN + q * 64, t.row0 + k0, pol_act);
+              if (SPLIT == SPLIT_B)
+                tma_load_2d(sb2 + q * MN_ATOM_BYTES, &tmB2, fb, t.n * BN + q * 64, t.row0 + k0, pol_act);
+            }
           }
           ++issued;
           if (++stage == STAGES) {
@@ -258,7 +305,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, Tr::kAmn, Tr::kBmn);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -266,7 +312,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bool ok = true;
     bool any_mma = false;
     for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
-      const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+      const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (t.nkb == 0) continue;
       int w_ok = 1;
       if (lane == 0)
@@ -276,11 +322,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+      const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0)
-          f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (lane == 0) f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
@@ -288,22 +333,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_after();
         uint8_t* sa_ptr = smem + stage * STAGE_BYTES;
         const uint32_t sa = smem_u32(sa_ptr);
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t sa2 = sa + A_TILE;
+        const uint32_t sb = sa + A_TILE * C::A_TILES;
+        const uint32_t sb2 = sb + C::B_TILE;
         int kvalid = BK;
         if (MODE == MODE_WGRAD) {
           kvalid = min(BK, t.rows - kb * BK);
           const int kend = (kvalid + 15) & ~15;
           if (kvalid < kend) {
-            // zero the K rows [kvalid, kend) of the 2 A and 4 B atom columns
+            // zero the K rows [kvalid, kend) of every MN-major atom column of the stage
+            constexpr int ATOMS = STAGE_BYTES / MN_ATOM_BYTES;
             const int nl = kend - kvalid;
             const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int idx = lane; idx < nl * 6 * 8; idx += 32) {
+            for (int idx = lane; idx < nl * ATOMS * 8; idx += 32) {
               const int chunk = idx & 7;
               const int li = idx >> 3;
               const int atom = li / nl;
               const int line = kvalid + (li - atom * nl);
-              uint8_t* p = sa_ptr + atom * MN_ATOM_BYTES + line * 128 + chunk * 16;
-              *reinterpret_cast<uint4*>(p) = z;
+              *reinterpret_cast<uint4*>(sa_ptr + atom * MN_ATOM_BYTES + line * 128 + chunk * 16) = z;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -312,12 +359,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         if (lane == 0) {
           const int nk16 = (kvalid + 15) >> 4;
           for (int k16 = 0; k16 < nk16; ++k16) {
-            uint64_t adesc, bdesc;
-            if (Tr::kAmn) adesc = smem_desc_sw128(sa + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
-            else adesc = smem_desc_sw128(sa + k16 * 32, 16, 1024);
-            if (Tr::kBmn) bdesc = smem_desc_sw128(sb + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
-            else bdesc = smem_desc_sw128(sb + k16 * 32, 16, 1024);
-            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | k16) != 0 ? 1u : 0u);
+            const uint32_t a_off = C::kAmn ? k16 * 2048 : k16 * 32;
+            const uint32_t b_off = C::kBmn ? k16 * 2048 : k16 * 32;
+            const uint32_t a_lbo = C::kAmn ? MOK_MN_LBO : 16, a_sbo = C::kAmn ? MOK_MN_SBO : 1024;
+            const uint32_t b_lbo = C::kBmn ? MOK_MN_LBO : 16, b_sbo = C::kBmn ? MOK_MN_SBO : 1024;
+            const uint64_t adesc = smem_desc_sw128(sa + a_off, a_lbo, a_sbo);
+            const uint64_t bdesc = smem_desc_sw128(sb + b_off, b_lbo, b_sbo);
+            umma_f16(d_tmem, adesc, bdesc, C::IDESC, (kb | k16) != 0 ? 1u : 0u);
+            if (SPLIT == SPLIT_A) umma_f16(d_tmem, smem_desc_sw128(sa2 + a_off, a_lbo, a_sbo), bdesc, C::IDESC, 1u);
+            if (SPLIT == SPLIT_B) umma_f16(d_tmem, adesc, smem_desc_sw128(sb2 + b_off, b_lbo, b_sbo), C::IDESC, 1u);
           }
           umma_commit(empty_bar(stage));
         }
@@ -350,27 +400,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
-      const TileInfo t = decode_tile<MODE, EPI>(args, g, s_off, s_toff);
+      const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (MODE == MODE_WGRAD && t.nkb == 0) {
-        // an expert without rows: its weight gradient is zero
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out0) +
-                             (size_t)t.e * args.M * args.N + (size_t)(t.m * BM + r_local) * args.N + t.n * BN;
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-        for (int c = 0; c < BN / 8; ++c) reinterpret_cast<uint4*>(out)[c] = z;
+        // an expert without rows: its weight gradient is zero (transposed layout out[e][n][m])
+        const size_t base = (size_t)t.e * args.M * args.N + (size_t)(t.n * BN) * args.M + t.m * BM + r_local;
+        if (EPI == EPI_T_F32) {
+          float* out = reinterpret_cast<float*>(args.out0) + base;
+          for (int j = 0; j < BN; ++j) out[(size_t)j * args.M] = 0.0f;
+        } else {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out0) + base;
+          for (int j = 0; j < BN; ++j) out[(size_t)j * args.M] = __float2bfloat16_rn(0.0f);
+        }
         continue;
       }
       int w_ok = 1;
-      if (lane == 0)
-        w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL);
+      if (lane == 0) w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
       tc_fence_after();
-      const uint32_t tacc = tmem_base + acc * ACC_COLS + (uint32_t(quarter * 32) << 16);
+      const uint32_t tacc = tmem_base + acc * C::ACC_COLS + (uint32_t(quarter * 32) << 16);
       const bool valid = (MODE == MODE_WGRAD) ? true : (r_local < t.rows);
       const long long row = (MODE == MODE_WGRAD) ? 0 : (long long)(t.row0 + r_local);
 
       if (EPI == EPI_F32) {
         float* out = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+#pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + c * 32, v);
@@ -390,35 +443,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
           }
         }
-      } else if (EPI == EPI_BF16) {
-        __nv_bfloat16* out;
-        if (MODE == MODE_WGRAD)
-          out = reinterpret_cast<__nv_bfloat16*>(args.out0) + (size_t)t.e * args.M * args.N +
-                (size_t)(t.m * BM + r_local) * args.N + t.n * BN;
-        else
-          out = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0 + t.n * BN;
+      } else if (EPI == EPI_T_F32 || EPI == EPI_T_BF16) {
+        // out[e][n][m]: lane = m, so each store instruction covers 32 consecutive elements
+        const size_t base = (size_t)t.e * args.M * args.N + (size_t)(t.n * BN) * args.M + t.m * BM + r_local;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + c * 32, v);
           tmem_wait_ld();
-          if (valid) {
-            uint32_t p[16];
+          if (EPI == EPI_T_F32) {
+            float* out = reinterpret_cast<float*>(args.out0) + base + (size_t)(c * 32) * args.M;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-              p[j] = *reinterpret_cast<uint32_t*>(&b);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+            for (int j = 0; j < 32; ++j) out[(size_t)j * args.M] = __uint_as_float(v[j]);
+          } else {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out0) + base + (size_t)(c * 32) * args.M;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            for (int j = 0; j < 32; ++j) out[(size_t)j * args.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
         }
       } else if (EPI == EPI_SWIGLU) {
-        // columns 0..127 of the accumulator are gate (h), 128..255 up (u), for
-        // intermediate indices n*128 .. n*128+127
-        __nv_bfloat16* hu = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
-        __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+        // accumulator columns 0..127 are the gate projection h, 128..255 the up projection u,
+        // for intermediate indices n*128 .. n*128+127.  Stores h | u in fp32, a = silu(h) u as
+        // a bf16 hi / lo pair.
+        float* hu = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+        __nv_bfloat16* act_hi = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+        __nv_bfloat16* act_lo = reinterpret_cast<__nv_bfloat16*>(args.out2) + row * args.ld1;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t vh[32], vu[32];
@@ -427,37 +476,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tmem_wait_ld();
           if (valid) {
             const int col = t.n * 128 + c * 32;
-            uint32_t ph[16], pu[16], pa[16];
+            uint32_t phi[16], plo[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float h0 = __uint_as_float(vh[2 * j]), h1 = __uint_as_float(vh[2 * j + 1]);
               const float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
               const float a0 = h0 / (1.0f + __expf(-h0)) * u0;
               const float a1 = h1 / (1.0f + __expf(-h1)) * u1;
-              __nv_bfloat162 bh = __floats2bfloat162_rn(h0, h1);
-              __nv_bfloat162 bu = __floats2bfloat162_rn(u0, u1);
-              __nv_bfloat162 ba = __floats2bfloat162_rn(a0, a1);
-              ph[j] = *reinterpret_cast<uint32_t*>(&bh);
-              pu[j] = *reinterpret_cast<uint32_t*>(&bu);
-              pa[j] = *reinterpret_cast<uint32_t*>(&ba);
+              split_bf16x2(a0, a1, phi[j], plo[j]);
             }
-            uint4* dh = reinterpret_cast<uint4*>(hu + col);
-            uint4* du = reinterpret_cast<uint4*>(hu + args.I + col);
-            uint4* da = reinterpret_cast<uint4*>(act + col);
+            float4* dh = reinterpret_cast<float4*>(hu + col);
+            float4* du = reinterpret_cast<float4*>(hu + args.I + col);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              dh[j] = make_uint4(ph[4 * j], ph[4 * j + 1], ph[4 * j + 2], ph[4 * j + 3]);
-              du[j] = make_uint4(pu[4 * j], pu[4 * j + 1], pu[4 * j + 2], pu[4 * j + 3]);
-              da[j] = make_uint4(pa[4 * j], pa[4 * j + 1], pa[4 * j + 2], pa[4 * j + 3]);
+            for (int j = 0; j < 8; ++j) {
+              dh[j] = make_float4(__uint_as_float(vh[4 * j]), __uint_as_float(vh[4 * j + 1]),
+                                  __uint_as_float(vh[4 * j + 2]), __uint_as_float(vh[4 * j + 3]));
+              du[j] = make_float4(__uint_as_float(vu[4 * j]), __uint_as_float(vu[4 * j + 1]),
+                                  __uint_as_float(vu[4 * j + 2]), __uint_as_float(vu[4 * j + 3]));
             }
+            store_u32x16(act_hi + col, phi);
+            store_u32x16(act_lo + col, plo);
           }
         }
       } else {  // EPI_SWIGLU_BWD
-        // accumulator = dA' = dY_g W2[e] for intermediate columns n*256 .. n*256+255
+        // accumulator = dA' = dY_g W2[e] for intermediate columns n*BN .. n*BN+BN-1.
+        // out0/out1: dh|du hi/lo [R][2I]; out2/out3: g*a hi/lo [R][I]; out4: dg partials.
         const float g = valid ? args.gate_row[row] : 0.0f;
-        const __nv_bfloat16* hu_row = args.hu + row * (long long)(2 * args.I);
-        __nv_bfloat16* dhu = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
-        __nv_bfloat16* gact = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+        const float* hu_row = args.hu + row * (long long)(2 * args.I);
+        __nv_bfloat16* dhu_hi = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
+        __nv_bfloat16* dhu_lo = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld0;
+        __nv_bfloat16* ga_hi = reinterpret_cast<__nv_bfloat16*>(args.out2) + row * args.ld1;
+        __nv_bfloat16* ga_lo = reinterpret_cast<__nv_bfloat16*>(args.out3) + row * args.ld1;
         float dg = 0.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -466,53 +515,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tmem_wait_ld();
           if (valid) {
             const int col = t.n * BN + c * 32;
-            uint4 hq[4], uq[4];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              float hv[16], uv[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              hq[j] = reinterpret_cast<const uint4*>(hu_row + col)[j];
-              uq[j] = reinterpret_cast<const uint4*>(hu_row + args.I + col)[j];
-            }
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(hq);
-            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(uq);
-            uint32_t pdh[16], pdu[16], pga[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 hh = __bfloat1622float2(h2[j]);
-              const float2 uu = __bfloat1622float2(u2[j]);
-              float r_dh[2], r_du[2], r_ga[2];
-              const float hv[2] = {hh.x, hh.y};
-              const float uv[2] = {uu.x, uu.y};
-#pragma unroll
-              for (int q = 0; q < 2; ++q) {
-                const float dap = __uint_as_float(v[2 * j + q]);
-                const float sg = 1.0f / (1.0f + __expf(-hv[q]));
-                const float sl = hv[q] * sg;
-                const float a = sl * uv[q];
-                dg = fmaf(dap, a, dg);
-                const float dA = g * dap;
-                r_dh[q] = dA * uv[q] * sg * (1.0f + hv[q] * (1.0f - sg));
-                r_du[q] = dA * sl;
-                r_ga[q] = g * a;
+              for (int j = 0; j < 4; ++j) {
+                const float4 h4 = reinterpret_cast<const float4*>(hu_row + col + half * 16)[j];
+                const float4 u4 = reinterpret_cast<const float4*>(hu_row + args.I + col + half * 16)[j];
+                hv[4 * j] = h4.x; hv[4 * j + 1] = h4.y; hv[4 * j + 2] = h4.z; hv[4 * j + 3] = h4.w;
+                uv[4 * j] = u4.x; uv[4 * j + 1] = u4.y; uv[4 * j + 2] = u4.z; uv[4 * j + 3] = u4.w;
               }
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(r_dh[0], r_dh[1]);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(r_du[0], r_du[1]);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(r_ga[0], r_ga[1]);
-              pdh[j] = *reinterpret_cast<uint32_t*>(&b0);
-              pdu[j] = *reinterpret_cast<uint32_t*>(&b1);
-              pga[j] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            uint4* o_dh = reinterpret_cast<uint4*>(dhu + col);
-            uint4* o_du = reinterpret_cast<uint4*>(dhu + args.I + col);
-            uint4* o_ga = reinterpret_cast<uint4*>(gact + col);
+              uint32_t pdh_hi[8], pdh_lo[8], pdu_hi[8], pdu_lo[8], pga_hi[8], pga_lo[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              o_dh[j] = make_uint4(pdh[4 * j], pdh[4 * j + 1], pdh[4 * j + 2], pdh[4 * j + 3]);
-              o_du[j] = make_uint4(pdu[4 * j], pdu[4 * j + 1], pdu[4 * j + 2], pdu[4 * j + 3]);
-              o_ga[j] = make_uint4(pga[4 * j], pga[4 * j + 1], pga[4 * j + 2], pga[4 * j + 3]);
+              for (int j = 0; j < 8; ++j) {
+                float r_dh[2], r_du[2], r_ga[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int idx = 2 * j + q;
+                  const float dap = __uint_as_float(v[half * 16 + idx]);
+                  const float sg = 1.0f / (1.0f + __expf(-hv[idx]));
+                  const float sl = hv[idx] * sg;
+                  const float a = sl * uv[idx];
+                  dg = fmaf(dap, a, dg);
+                  const float dA = g * dap;
+                  r_dh[q] = dA * uv[idx] * sg * (1.0f + hv[idx] * (1.0f - sg));
+                  r_du[q] = dA * sl;
+                  r_ga[q] = g * a;
+                }
+                split_bf16x2(r_dh[0], r_dh[1], pdh_hi[j], pdh_lo[j]);
+                split_bf16x2(r_du[0], r_du[1], pdu_hi[j], pdu_lo[j]);
+                split_bf16x2(r_ga[0], r_ga[1], pga_hi[j], pga_lo[j]);
+              }
+              const int cc = col + half * 16;
+              uint4* o;
+              o = reinterpret_cast<uint4*>(dhu_hi + cc);
+              o[0] = make_uint4(pdh_hi[0], pdh_hi[1], pdh_hi[2], pdh_hi[3]);
+              o[1] = make_uint4(pdh_hi[4], pdh_hi[5], pdh_hi[6], pdh_hi[7]);
+              o = reinterpret_cast<uint4*>(dhu_lo + cc);
+              o[0] = make_uint4(pdh_lo[0], pdh_lo[1], pdh_lo[2], pdh_lo[3]);
+              o[1] = make_uint4(pdh_lo[4], pdh_lo[5], pdh_lo[6], pdh_lo[7]);
+              o = reinterpret_cast<uint4*>(dhu_hi + args.I + cc);
+              o[0] = make_uint4(pdu_hi[0], pdu_hi[1], pdu_hi[2], pdu_hi[3]);
+              o[1] = make_uint4(pdu_hi[4], pdu_hi[5], pdu_hi[6], pdu_hi[7]);
+              o = reinterpret_cast<uint4*>(dhu_lo + args.I + cc);
+              o[0] = make_uint4(pdu_lo[0], pdu_lo[1], pdu_lo[2], pdu_lo[3]);
+              o[1] = make_uint4(pdu_lo[4], pdu_lo[5], pdu_lo[6], pdu_lo[7]);
+              o = reinterpret_cast<uint4*>(ga_hi + cc);
+              o[0] = make_uint4(pga_hi[0], pga_hi[1], pga_hi[2], pga_hi[3]);
+              o[1] = make_uint4(pga_hi[4], pga_hi[5], pga_hi[6], pga_hi[7]);
+              o = reinterpret_cast<uint4*>(ga_lo + cc);
+              o[0] = make_uint4(pga_lo[0], pga_lo[1], pga_lo[2], pga_lo[3]);
+              o[1] = make_uint4(pga_lo[4], pga_lo[5], pga_lo[6], pga_lo[7]);
             }
           }
         }
-        if (valid) reinterpret_cast<float*>(args.out2)[row * args.ld2 + t.n] = dg;
+        if (valid) reinterpret_cast<float*>(args.out4)[row * args.ld2 + t.n] = dg;
       }
       tc_fence_before();
       __syncwarp();
@@ -526,7 +583,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 

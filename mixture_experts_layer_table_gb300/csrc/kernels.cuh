@@ -22,7 +22,8 @@ cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* o
 // rows.cu
 cudaError_t launch_gather_rows(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
                                cudaStream_t st);
-cudaError_t launch_combine(const void* rows, const float* w, const int32_t* row_of, int T, int k, int H,
+// out[t] = sum_j w[t][j] * rows[row_of[t*k+j]] (+ router term), rows fp32, out bf16
+cudaError_t launch_combine(const float* rows, const float* w, const int32_t* row_of, int T, int k, int H,
                            const float* dl, const void* w_router, const int32_t* topk_idx, int E,
                            int dense_router, void* out, int n_sm, cudaStream_t st);
 
@@ -30,19 +31,23 @@ cudaError_t launch_combine(const void* rows, const float* w, const int32_t* row_
 cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
                                int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
-                                const int32_t* offsets, const int32_t* tile_off, void* hu, void* act,
-                                int* status, int n_sm, cudaStream_t st);
-cudaError_t launch_gemm2(const void* act, const void* w2, int R, int H, int I, int E, const int32_t* offsets,
-                         const int32_t* tile_off, void* out, int* status, int n_sm, cudaStream_t st);
+                                const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
+                                void* act_lo, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
+                         const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
+                         cudaStream_t st);
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
-                                const int32_t* offsets, const int32_t* tile_off, const void* hu,
-                                const float* gate_row, void* dhu, void* gact, float* dg_part, int* status,
-                                int n_sm, cudaStream_t st);
-cudaError_t launch_dgrad_x(const void* dhu, const void* w13, int R, int H, int I, int E, const int32_t* offsets,
-                           const int32_t* tile_off, void* dx_g, int* status, int n_sm, cudaStream_t st);
-// dW[e] [M][N] = sum over rows r of expert e of A[r][0..M) (x) B[r][0..N)
-cudaError_t launch_wgrad(const void* a_rows, int M, const void* b_rows, int N, int R, int E,
-                         const int32_t* offsets, void* dw, int* status, int n_sm, cudaStream_t st);
+                                const int32_t* offsets, const int32_t* tile_off, const float* hu,
+                                const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,
+                                float* dg_part, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w13, int R, int H, int I, int E,
+                           const int32_t* offsets, const int32_t* tile_off, float* dx_g, int* status, int n_sm,
+                           cudaStream_t st);
+// dW[e] stored transposed as out[e][n][m] (m = the output's contiguous dimension):
+// out[e][n][m] = sum over rows r of expert e of A[r][m] * B[r][n]; A or B may be a hi/lo pair.
+cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
+                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int n_sm,
+                         cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

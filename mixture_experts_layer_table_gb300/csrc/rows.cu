@@ -70,14 +70,26 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&acc)[8]) {
   return o;
 }
 
+__device__ __forceinline__ void acc_f32x8(float (&acc)[8], uint4 a, uint4 b, float w) {
+  acc[0] = fmaf(w, __uint_as_float(a.x), acc[0]);
+  acc[1] = fmaf(w, __uint_as_float(a.y), acc[1]);
+  acc[2] = fmaf(w, __uint_as_float(a.z), acc[2]);
+  acc[3] = fmaf(w, __uint_as_float(a.w), acc[3]);
+  acc[4] = fmaf(w, __uint_as_float(b.x), acc[4]);
+  acc[5] = fmaf(w, __uint_as_float(b.y), acc[5]);
+  acc[6] = fmaf(w, __uint_as_float(b.z), acc[6]);
+  acc[7] = fmaf(w, __uint_as_float(b.w), acc[7]);
+}
+
 // y[t] = sum_{j=0..k-1} w[t][j] * rows[row_of[t*k+j]]  (+ sum over the router support of
-// dl[t][e] * w_router[e] when dl != nullptr), fp32 in the fixed order, rounded to bf16.
+// dl[t][e] * w_router[e] when dl != nullptr), fp32 in the fixed order, rounded to bf16 once.
+// rows are fp32 (expert outputs o, or per-row input gradients dX_g).
 // `w` null means weight 1 (the backward's reverse dispatch of dX rows).
 // Router support: the k selected experts (sparse) or all E experts (dense).
-// One warp per token; each lane handles 8-column chunks.
+// One warp per token; each lane handles 8-column chunks (vec_per_row = H / 8).
 template <int KMAX>
 __global__ void __launch_bounds__(256)
-    combine_kernel(const __nv_bfloat16* __restrict__ rows, const float* __restrict__ w,
+    combine_kernel(const float* __restrict__ rows, const float* __restrict__ w,
                    const int32_t* __restrict__ row_of, int T, int k, int vec_per_row,
                    const float* __restrict__ dl, const __nv_bfloat16* __restrict__ w_router,
                    const int32_t* __restrict__ topk_idx, int E, int dense_router,
@@ -98,13 +110,17 @@ __global__ void __launch_bounds__(256)
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-      uint4 v[KMAX];
+      uint4 va[KMAX], vb[KMAX];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) v[j] = ld_nc_v4(reinterpret_cast<const uint4*>(rows) + (size_t)rj[j] * vec_per_row + i);
+        if (j < k) {
+          const uint4* p = reinterpret_cast<const uint4*>(rows) + ((size_t)rj[j] * vec_per_row + i) * 2;
+          va[j] = ld_nc_v4(p);
+          vb[j] = ld_nc_v4(p + 1);
+        }
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) acc_bf16x8(acc, v[j], wj[j]);
+        if (j < k) acc_f32x8(acc, va[j], vb[j], wj[j]);
       if (dl != nullptr) {
         const int n_sup = dense_router ? E : k;
         for (int s = 0; s < n_sup; ++s) {
@@ -130,14 +146,14 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* src_of, int k, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const void* rows, const float* w, const int32_t* row_of, int T, int k, int H,
+cudaError_t launch_combine(const float* rows, const float* w, const int32_t* row_of, int T, int k, int H,
                            const float* dl, const void* w_router, const int32_t* topk_idx, int E,
                            int dense_router, void* out, int n_sm, cudaStream_t st) {
   const int vec = H / 8;
   const int warps = 8;
   int blocks = (T + warps - 1) / warps;
   blocks = min(blocks, n_sm * 8);
-  auto r = reinterpret_cast<const __nv_bfloat16*>(rows);
+  const float* r = rows;
   auto wr = reinterpret_cast<const __nv_bfloat16*>(w_router);
   auto o = reinterpret_cast<__nv_bfloat16*>(out);
   if (k <= 2)
