@@ -34,6 +34,14 @@ CPU_SAMPLE = {"T": 512, "E": 16}        # cpu_baseline: 512 tokens of the DSV3 s
 REF_SAMPLE = {"T": 256, "E": 16}        # --impl reference: per step
 
 
+def _workloads():
+    from mixture_experts_layer_table_gb300 import workloads as W
+    return {"dsv3": W.DSV3, "dsv3_e16_t256": W.DSV3.scaled(name="dsv3_e16_t256", T=256, E=16)}
+
+
+WORKLOADS = _workloads()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -209,14 +217,14 @@ def run_mok(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     mok.load()
-    shp = W.DSV3
+    shp = WORKLOADS[args.workload]
     T, H, I, E, k = shp.T, shp.H, shp.I, shp.E, shp.k
     inp = W.make_inputs(shp, seed=1000 * rank, device=str(dev))
     layer = mok.MoELayer(mok.desc_from_shape(shp), device=dev)
     grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
              "dw_router": torch.empty((E, H), dtype=torch.float32, device=dev),
-             "dw13": torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev),
-             "dw2": torch.empty((E, H, I), dtype=torch.bfloat16, device=dev),
+             "dw13": torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev),
+             "dw2": torch.empty((E, H, I), dtype=torch.float32, device=dev),
              "dgates": torch.empty((T, k), dtype=torch.float32, device=dev)}
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     x, wr, w13, w2, dy = inp["x"], inp["w_router"], inp["w13"], inp["w2"], inp["dy"]
@@ -386,6 +394,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
+                    help="dsv3: the benchmarked layer; dsv3_e16_t256: the same per-expert shape on "
+                         "16 experts and 256 tokens (a few GB, for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -130,8 +130,41 @@ def status_string(code: int) -> str:
     return load().mok_status_string(code).decode()
 
 
+def _expect(t, shape, dtype, name, nullable=False):
+    """The C ABI takes bare pointers, so buffer sizes and dtypes are checked here, on the host."""
+    if t is None:
+        if nullable:
+            return
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _check_layer_inputs(desc, x, w_router, router_bias, w13, w2):
+    bf = torch.bfloat16
+    _expect(x, (desc.T, desc.H), bf, "x")
+    _expect(w_router, (desc.E, desc.H), bf, "w_router")
+    _expect(router_bias, (desc.E,), torch.float32, "router_bias", nullable=True)
+    _expect(w13, (desc.E, 2 * desc.I, desc.H), bf, "w13")
+    _expect(w2, (desc.E, desc.H, desc.I), bf, "w2")
+
+
 def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts, offsets, row_of, src_of, ws,
              stream=None):
+    R = desc.T * desc.k
+    if x is not None:
+        _expect(x, (desc.T, desc.H), torch.bfloat16, "x")
+        _expect(w_router, (desc.E, desc.H), torch.bfloat16, "w_router")
+    _expect(router_bias, (desc.E,), torch.float32, "router_bias", nullable=True)
+    _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
+    _expect(topk_idx, (desc.T, desc.k), torch.int32, "topk_idx")
+    _expect(gates, (desc.T, desc.k), torch.float32, "gates", nullable=True)
+    _expect(counts, (desc.E,), torch.int32, "counts")
+    _expect(offsets, (desc.E + 1,), torch.int32, "offsets")
+    _expect(row_of, (R,), torch.int32, "row_of")
+    _expect(src_of, (R,), torch.int32, "src_of")
     _check("mok_schedule", load().mok_schedule(
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(topk_idx),
         _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(ws), ws.numel() * ws.element_size(),
@@ -139,6 +172,9 @@ def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts
 
 
 def moe_forward(desc, x, w_router, router_bias, given_topk, w13, w2, y, ctx, ws, stream=None):
+    _check_layer_inputs(desc, x, w_router, router_bias, w13, w2)
+    _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
+    _expect(y, (desc.T, desc.H), torch.bfloat16, "y")
     _check("mok_moe_forward", load().mok_moe_forward(
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(w13), _ptr(w2),
         _ptr(y), _ptr(ctx), ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(),
@@ -146,6 +182,14 @@ def moe_forward(desc, x, w_router, router_bias, given_topk, w13, w2, y, ctx, ws,
 
 
 def moe_backward(desc, dy, x, w_router, w13, w2, ctx, dx, dw_router, dw13, dw2, dgates, ws, stream=None):
+    _check_layer_inputs(desc, x, w_router, None, w13, w2)
+    wdt = torch.bfloat16 if (desc.flags & FLAG_WGRAD_BF16) else torch.float32
+    _expect(dy, (desc.T, desc.H), torch.bfloat16, "dy")
+    _expect(dx, (desc.T, desc.H), torch.bfloat16, "dx")
+    _expect(dw_router, (desc.E, desc.H), torch.float32, "dw_router")
+    _expect(dw13, (desc.E, 2 * desc.I, desc.H), wdt, "dw13")
+    _expect(dw2, (desc.E, desc.H, desc.I), wdt, "dw2")
+    _expect(dgates, (desc.T, desc.k), torch.float32, "dgates", nullable=True)
     _check("mok_moe_backward", load().mok_moe_backward(
         ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(w13), _ptr(w2), _ptr(ctx),
         ctx.numel() * ctx.element_size(), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), _ptr(ws),

@@ -149,24 +149,27 @@ def test_forward_backward_parity(shape, mode):
 
 
 @pytest.mark.parametrize("shape", [MID, MID_SKEW], ids=lambda s: s.name)
-def test_bf16_weight_gradients(shape):
-    """MOK_FLAG_WGRAD_BF16: dW13 / dW2 stored in bf16.  Each expert's weight gradient is its own
-    output tensor, so the max-error bar is taken against that expert's RMS."""
+def test_bf16_weight_gradients_are_rounded_fp32_ones(shape):
+    """MOK_FLAG_WGRAD_BF16 stores dW13 / dW2 in bf16.  The kernels and reduction order are the
+    same as the default fp32 output, so the result must be that fp32 result rounded to nearest
+    even, bit for bit (the fp32 result itself meets the bar against the oracle above).  Pure
+    bf16 rounding of an exact gradient alone moves its largest elements by up to 2^-8 of
+    their size, about 2% of the RMS at 5 sigma, so the max-error bar is not asked of bf16."""
     inp = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp)
     given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
-    _, bwd = oracle_layer(shape, f64, topk_idx=given)
+    _, g32 = _run(shape, inp, given=given)[1:]
     dev = _gpu_inputs(inp)
     layer = mok.MoELayer(mok.desc_from_shape(shape, flags=1))
     layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"],
                   given_topk=torch.tensor(given, device="cuda"))
     g = layer.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
     assert g["dw13"].dtype == torch.bfloat16 and layer.status() == (0, 0)
     for name in ("dw13", "dw2"):
-        got = to_f64(g[name])
-        for e in range(shape.E):
-            if np.any(bwd[name][e] != 0):
-                assert_bf16_close(got[e], bwd[name][e], f"{name}[{e}]")
+        assert torch.equal(g[name], g32[name].to(torch.bfloat16)), name
+    for name in ("dx", "dw_router", "dgates"):
+        assert torch.equal(g[name], g32[name]), name
 
 
 def test_empty_experts_get_zero_weight_gradient():
