@@ -51,8 +51,10 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def kernel_bytes(s):
-    """Algorithmic HBM bytes of one launch of each kernel (reads + writes of distinct data)."""
+def kernel_bytes(s, wgrad_bytes=4):
+    """Algorithmic HBM bytes of one launch of each kernel: reads + writes of distinct data in the
+    layouts the kernels use (bf16 inputs and weights; h|u, expert outputs and dX rows in fp32;
+    a, dh|du and g*a as bf16 hi + lo pairs; weight gradients in fp32 by default)."""
     T, H, I, E, k = s.T, s.H, s.I, s.E, s.k
     R = T * k
     return {
@@ -60,17 +62,17 @@ def kernel_bytes(s):
         "topk": T * E * 4 * 2 + T * k * 8,
         "schedule": R * 4 * 5 + E * 8,
         "gather_x": T * H * 2 + R * H * 2 + R * 4,
-        "gemm1_swiglu": E * 2 * I * H * 2 + R * H * 2 + R * 2 * I * 2 + R * I * 2,
-        "gemm2": E * H * I * 2 + R * I * 2 + R * H * 2,
-        "combine": R * H * 2 + T * H * 2 + R * 8,
+        "gemm1_swiglu": E * 2 * I * H * 2 + R * H * 2 + R * 2 * I * 4 + R * I * 4,
+        "gemm2": E * H * I * 2 + R * I * 4 + R * H * 4,
+        "combine": R * H * 4 + T * H * 2 + R * 8,
         "gather_dy": T * H * 2 + R * H * 2 + R * 4,
-        "dgrad_swiglu": E * H * I * 2 + R * H * 2 + R * 2 * I * 2 * 2 + R * I * 2 + R * (I // 256) * 4,
-        "dgrad_x": E * 2 * I * H * 2 + R * 2 * I * 2 + R * H * 2,
-        "wgrad_w2": R * H * 2 + R * I * 2 + E * H * I * 2,
-        "wgrad_w13": R * 2 * I * 2 + R * H * 2 + E * 2 * I * H * 2,
+        "dgrad_swiglu": E * H * I * 2 + R * H * 2 + R * 2 * I * 4 + R * 2 * I * 4 + R * I * 4 + R * (I // 256) * 4,
+        "dgrad_x": E * 2 * I * H * 2 + R * 2 * I * 4 + R * H * 4,
+        "wgrad_w2": R * H * 2 + R * I * 4 + E * H * I * wgrad_bytes,
+        "wgrad_w13": R * 2 * I * 4 + R * H * 2 + E * 2 * I * H * wgrad_bytes,
         "router_dlogits": R * (I // 256) * 4 + R * 12 + T * E * 8,
         "router_wgrad": T * H * 2 + E * H * 4 + T * E * 4,
-        "combine_dx": R * H * 2 + E * H * 2 + T * H * 2 + T * E * 4,
+        "combine_dx": R * H * 4 + E * H * 2 + T * H * 2 + T * E * 4,
     }
 
 

@@ -32,7 +32,8 @@ EncodeTiledFn encode_fn() {
 // bf16 tensor, innermost dimension first; strides in bytes for dims 1..rank-1; 128B swizzle,
 // out-of-bounds elements read as zero.
 bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-               const uint32_t* box) {
+               const uint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t d[3], s[2];
@@ -42,9 +43,19 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     b[i] = box[i];
   }
   for (int i = 0; i + 1 < rank; ++i) s[i] = strides_bytes[i];
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dtype, rank, const_cast<void*>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output map of a weight gradient stored as out[E][N][M] (M contiguous), 32 x 32 boxes, no swizzle.
+bool tmap_wgrad_out(CUtensorMap* m, void* base, uint64_t M, uint64_t N, uint64_t E, bool f32) {
+  const uint64_t es = f32 ? 4 : 2;
+  const uint64_t dims[3] = {M, N, E};
+  const uint64_t strides[2] = {M * es, M * N * es};
+  const uint32_t box[3] = {32, 32, 1};
+  return make_tmap(m, base, 3, dims, strides, box,
+                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -64,13 +75,14 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
 
 template <int MODE, int EPI, int SPLIT, int BN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& b2,
-                   const GemmArgs& args, int grid, cudaStream_t st) {
+                   const GemmArgs& args, int grid, cudaStream_t st, const CUtensorMap* out_map = nullptr) {
   using C = GemmCfg<MODE, EPI, SPLIT, BN>;
+  static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
   if (grid <= 0) return cudaSuccess;
   auto kern = gemm_kernel<MODE, EPI, SPLIT, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
-  kern<<<grid, GEMM_THREADS, C::smem_bytes(args.E), st>>>(a, a2, b, b2, args);
+  kern<<<grid, GEMM_THREADS, C::smem_bytes(args.E), st>>>(a, a2, b, b2, out_map ? *out_map : a, args);
   return cudaGetLastError();
 }
 
@@ -191,6 +203,8 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   if (a_lo && !tmap_2d(&ta2, a_lo, M, R, 64, BK)) return cudaErrorInvalidValue;
   if (b_lo && !tmap_2d(&tb2, b_lo, N, R, 64, BK)) return cudaErrorInvalidValue;
   if (a_lo && b_lo) return cudaErrorInvalidValue;
+  CUtensorMap to;
+  if (!tmap_wgrad_out(&to, dw, M, N, E, out_f32 != 0)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, nullptr, status);
   g.M = M;
   g.N = N;
@@ -199,15 +213,15 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   g.total_tiles = tiles;
   const int grid = std::min(tiles, n_sm);
   if (a_lo) {
-    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st)
-                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st);
+    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
+                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
   }
   if (b_lo) {
-    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st)
-                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st);
+    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
+                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
   }
-  return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st)
-                 : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st);
+  return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
+                 : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
 }
 
 // ----------------------------------------------------------------------------- wait test

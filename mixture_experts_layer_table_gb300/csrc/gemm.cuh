@@ -79,6 +79,7 @@ struct TileInfo {
   int row0;   // first A row (ROWS/DGRAD/DENSE) or first K row (WGRAD)
   int rows;   // valid output rows (ROWS/DGRAD/DENSE) or K rows (WGRAD)
   int nkb;    // K blocks
+  int mt;     // ROWS/DGRAD: number of 128-row tiles of this expert (they share each weight tile)
 };
 
 template <int MODE, int EPI, int SPLIT, int BN_>
@@ -90,15 +91,19 @@ struct GemmCfg {
   static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
   static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
   static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES;
-  static constexpr int STAGES = (SMEM_RING / STAGE_BYTES) < 4 ? (SMEM_RING / STAGE_BYTES) : 4;
+  // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: 2 buffers per
+  // epilogue warp of up to 32 x 32 fp32.
+  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * 2 * 4096 : 0;
+  static constexpr int RING = SMEM_RING - STG_BYTES;
+  static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
   static __host__ __device__ int n_tiles(const GemmArgs& a) {
     return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + BN - 1) / BN;
   }
-  static __host__ __device__ size_t smem_bytes(int E) {
-    return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+  static __host__ __device__ constexpr size_t smem_bytes(int E) {
+    return size_t(STAGES) * STAGE_BYTES + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
   }
 };
 
@@ -115,6 +120,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
     t.row0 = t.m * BM;
     t.rows = min(BM, a.M - t.row0);
     t.nkb = a.K / BK;
+    t.mt = MT;
   } else if (MODE == MODE_WGRAD) {
     const int MT = a.M / BM;
     const int per_e = MT * NT;
@@ -125,6 +131,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
     t.row0 = s_off[t.e];
     t.rows = s_off[t.e + 1] - t.row0;
     t.nkb = (t.rows + BK - 1) / BK;
+    t.mt = MT;
   } else {
     // expert e owns tiles [tile_off[e]*NT, tile_off[e+1]*NT); inside, m runs fastest so the
     // m-tiles of one expert that share a weight tile are dealt to neighbouring CTAs.
@@ -141,6 +148,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
     t.row0 = s_off[lo] + t.m * BM;
     t.rows = min(BM, s_off[lo + 1] - t.row0);
     t.nkb = a.K / BK;
+    t.mt = Me;
   }
   return t;
 }
@@ -169,18 +177,19 @@ template <int MODE, int EPI, int SPLIT, int BN_>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmO, const GemmArgs args) {
   using C = GemmCfg<MODE, EPI, SPLIT, BN_>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // WGRAD output staging (C::STG_BYTES)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STG_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_off = reinterpret_cast<int*>(staging + C::STG_BYTES + 256);
   int* s_toff = s_off + (args.E + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -230,13 +239,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (SPLIT == SPLIT_A) tma_prefetch_desc(&tmA2);
       if (SPLIT == SPLIT_B) tma_prefetch_desc(&tmB2);
       const uint64_t pol_act = l2_policy_evict_last();
-      const uint64_t pol_w = (MODE == MODE_WGRAD) ? pol_act : l2_policy_evict_first();
+      const uint64_t pol_once = l2_policy_evict_first();
+      const uint64_t pol_shared = l2_policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
       for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
         const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
+        // a weight tile is read once when its expert has a single m-tile; otherwise the
+        // neighbouring CTAs that run the expert's other m-tiles read it again from L2
+        const uint64_t pol_w = (MODE == MODE_WGRAD) ? pol_act : (t.mt > 1 ? pol_shared : pol_once);
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY)) {
             ok = false;
@@ -399,6 +412,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int r_local = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int stg_buf = 0;  // WGRAD: staging buffer alternation
     for (int g = blockIdx.x; g < total; g += gridDim.x) {
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (MODE == MODE_WGRAD && t.nkb == 0) {
@@ -444,22 +458,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       } else if (EPI == EPI_T_F32 || EPI == EPI_T_BF16) {
-        // out[e][n][m]: lane = m, so each store instruction covers 32 consecutive elements
-        const size_t base = (size_t)t.e * args.M * args.N + (size_t)(t.n * BN) * args.M + t.m * BM + r_local;
+        // out[e][n][m]: each 32 (m) x 32 (n) block of this warp is written to shared memory with
+        // m contiguous (lane = m: conflict-free) and stored by one TMA bulk tensor store.
+        uint8_t* stg = staging + (warp - 2) * 8192;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + c * 32, v);
           tmem_wait_ld();
+          uint8_t* buf = stg + (stg_buf & 1) * 4096;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
+          __syncwarp();
           if (EPI == EPI_T_F32) {
-            float* out = reinterpret_cast<float*>(args.out0) + base + (size_t)(c * 32) * args.M;
+            float* sb = reinterpret_cast<float*>(buf);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) out[(size_t)j * args.M] = __uint_as_float(v[j]);
+            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __uint_as_float(v[j]);
           } else {
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out0) + base + (size_t)(c * 32) * args.M;
+            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(buf);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) out[(size_t)j * args.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmO, smem_u32(buf), t.m * BM + quarter * 32, t.n * BN + c * 32, t.e);
+            bulk_commit_group();
+          }
+          ++stg_buf;
         }
       } else if (EPI == EPI_SWIGLU) {
         // accumulator columns 0..127 are the gate projection h, 128..255 the up projection u,
@@ -577,6 +602,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    // TMA stores of this warp must finish reading shared memory (and land) before exit
+    if (MODE == MODE_WGRAD && lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before();
