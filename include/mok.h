@@ -138,6 +138,31 @@ mok_status mok_schedule(const mok_layer_desc* desc, const void* x, const void* w
                         float* gates, int32_t* counts, int32_t* offsets, int32_t* row_of,
                         int32_t* src_of, void* ws, size_t ws_bytes, void* stream);
 
+/* mok_schedule without a workspace (the pages have no counterpart of this entry point).
+ * For callers that cannot allocate device memory when they route tokens: code running under
+ * an allocator that forbids new allocations (a step whose memory plan is fixed), a runtime
+ * that only hands out its own pre-sized buffers, or a plain C caller without a CUDA
+ * allocator.  Same arguments, outputs and results as mok_schedule, minus ws / ws_bytes; the
+ * scratch (status word and router logits) is one array compiled into the library:
+ * MOK_NOALLOC_MAX_LOGITS floats plus 256 bytes (about 4 MiB), held in the memory of every
+ * GPU that loads the library until the process exits.
+ *   - Rejects T * E > MOK_NOALLOC_MAX_LOGITS with MOK_ERR_WORKSPACE_TOO_SMALL when the router
+ *     runs (x and w_router given); the given_topk-only path has no size limit beyond
+ *     mok_layer_desc's.
+ *   - device_status: NULL, or a DEVICE buffer of 2 int32 that receives (code, site) of the
+ *     first device-side error of this call, as mok_read_status would report it.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the array and it keeps the last call's contents (the
+ *     status word is cleared at the start of each call).  Calls whose work overlaps on the
+ *     GPU (other streams, other host threads) race on it: order them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine. */
+#define MOK_NOALLOC_MAX_LOGITS (1 << 20)
+mok_status mok_schedule_noalloc(const mok_layer_desc* desc, const void* x, const void* w_router,
+                                const float* router_bias, const int32_t* given_topk, int32_t* topk_idx,
+                                float* gates, int32_t* counts, int32_t* offsets, int32_t* row_of,
+                                int32_t* src_of, int32_t* device_status, void* stream);
+
 /* Layer forward: y [T][H] bf16 = sum over the k selected experts of gate * SwiGLU-FFN(x).
  *   w13 [E][2I][H] bf16 (rows 0..I-1 gate projection, I..2I-1 up projection),
  *   w2 [E][H][I] bf16, router_bias and given_topk as in mok_schedule.

@@ -289,3 +289,33 @@ class MoELayer:
 
     def status(self, stream=None):
         return read_status(self.ws, stream)
+
+
+def schedule_noalloc(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts, offsets, row_of, src_of,
+                     device_status=None, stream=None):
+    """mok_schedule_noalloc: the router and schedule table with the library's own fixed scratch,
+    for callers that cannot allocate a workspace.  Same outputs as ``schedule``;
+    ``device_status`` (optional int32 [2] CUDA tensor) receives (code, site) of a device error."""
+    lib = load()
+    fn = lib.mok_schedule_noalloc
+    if fn.argtypes is None:
+        P = ctypes.c_void_p
+        fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, P, P, P, P, P, P]
+        fn.restype = ctypes.c_int32
+    R = desc.T * desc.k
+    if x is not None:
+        _expect(x, (desc.T, desc.H), torch.bfloat16, "x")
+        _expect(w_router, (desc.E, desc.H), torch.bfloat16, "w_router")
+    _expect(router_bias, (desc.E,), torch.float32, "router_bias", nullable=True)
+    _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
+    _expect(topk_idx, (desc.T, desc.k), torch.int32, "topk_idx")
+    _expect(gates, (desc.T, desc.k), torch.float32, "gates", nullable=True)
+    _expect(counts, (desc.E,), torch.int32, "counts")
+    _expect(offsets, (desc.E + 1,), torch.int32, "offsets")
+    _expect(row_of, (R,), torch.int32, "row_of")
+    _expect(src_of, (R,), torch.int32, "src_of")
+    _expect(device_status, (2,), torch.int32, "device_status", nullable=True)
+    _check("mok_schedule_noalloc", fn(
+        ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(topk_idx),
+        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(device_status),
+        _stream(stream)))
