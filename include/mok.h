@@ -66,10 +66,17 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *   renorm  nonzero: the k selected gates are divided by their sum
  *   route_scale  factor on every gate (1.0 for the workloads here)
  *   precision    mok_precision of the expert GEMMs
- *   minibatch    ring forward only: rows per minibatch (0 = the whole call)
- *   ring_bytes   ring forward only: bytes of the fixed token ring (0 = no ring)
+ *   ring_bytes   0: the forward gathers all T*k rows at once.  > 0: ring forward — the
+ *                gathered (dispatched) rows pass through a fixed ring of this many bytes in
+ *                minibatches, gathered by comm_sms CTAs while the other SMs run GEMM1 on
+ *                earlier minibatches, in one persistent launch that signals through device
+ *                counters ("Mixture-of-Kittens (MoK)", sd114.wiki, ring-buffer section;
+ *                aientropygate.com §03 ② and ③).  The ring must hold one minibatch.
+ *   minibatch    ring forward: rows per minibatch, consecutive rows of the expert-sorted
+ *                order (0 = mok_min_minibatch(0, I), two full SM waves of GEMM1 tiles)
  *   flags        MOK_FLAG_WGRAD_BF16: the expert weight gradients dw13 / dw2 of
  *                mok_moe_backward are bf16 instead of the default f32
+ *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1
 typedef struct {
@@ -81,7 +88,7 @@ typedef struct {
   int32_t minibatch;
   int64_t ring_bytes;
   int32_t flags;
-  int32_t reserved;
+  int32_t comm_sms;
 } mok_layer_desc;
 
 /* Byte offsets (from the base pointer) of the tensors inside ctx and ws.  ctx holds what
@@ -116,6 +123,10 @@ typedef struct {
   int64_t dx_g;       /* f32 [T*k][H]   per-row input gradient (backward) */
   int64_t dg_part;    /* f32 [T*k][I/256] partial gate gradients per GEMM column tile */
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
+  /* ring forward only (-1 otherwise) */
+  int64_t ring;       /* bf16 [slots * minibatch][H]  the token ring */
+  int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb+1] tile starts */
+  int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch */
   int64_t ws_bytes;
 } mok_layout;
 
@@ -168,7 +179,10 @@ mok_status mok_schedule_noalloc(const mok_layer_desc* desc, const void* x, const
  *   w2 [E][H][I] bf16, router_bias and given_topk as in mok_schedule.
  *   ctx (layout.ctx_bytes) receives what the backward needs; ws (layout.ws_bytes) is
  *   scratch and also holds the status word.  Pointers to x, weights, y, ctx and ws must be
- *   16-byte aligned (TMA).  MXFP8 is not accepted here (MOK_ERR_UNSUPPORTED). */
+ *   16-byte aligned (TMA).  MXFP8 is not accepted here (MOK_ERR_UNSUPPORTED).
+ *   With ring_bytes > 0 the dispatched rows live only in the ring (ctx x_g is not written;
+ *   mok_moe_backward gathers them again) and y is bitwise the same as without the ring.  The
+ *   ring launch is cooperative: all of its CTAs must be resident at once (one per SM). */
 mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void* w_router,
                            const float* router_bias, const int32_t* given_topk, const void* w13,
                            const void* w2, void* y, void* ctx, size_t ctx_bytes, void* ws,

@@ -32,12 +32,12 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("router", ctypes.c_int32), ("renorm", ctypes.c_int32),
                 ("route_scale", ctypes.c_float), ("precision", ctypes.c_int32), ("minibatch", ctypes.c_int32),
-                ("ring_bytes", ctypes.c_int64), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("ring_bytes", ctypes.c_int64), ("flags", ctypes.c_int32), ("comm_sms", ctypes.c_int32)]
 
 
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
                  "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
-                 "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ws_bytes"]
+                 "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
@@ -106,9 +106,9 @@ def _check(fn: str, code: int):
 
 
 def make_desc(T, H, I, E, k, router, renorm, route_scale=1.0, precision=0, minibatch=0, ring_bytes=0,
-              flags=0) -> LayerDesc:
+              flags=0, comm_sms=0) -> LayerDesc:
     return LayerDesc(T, H, I, E, k, router, int(bool(renorm)), route_scale, precision, minibatch, ring_bytes,
-                     flags, 0)
+                     flags, comm_sms)
 
 
 def desc_from_shape(shape, **kw) -> LayerDesc:

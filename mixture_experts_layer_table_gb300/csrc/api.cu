@@ -48,6 +48,36 @@ mok_status check_desc(const mok_layer_desc* d) {
   return MOK_OK;
 }
 
+// Two full waves of 128 x 256 GEMM1 output tiles over n_sm SMs, in rows: GEMM1 has 2I columns.
+int32_t min_minibatch_rows(int n_sm, int I) {
+  if (n_sm <= 0 || I <= 0) return 0;
+  return static_cast<int32_t>((2LL * n_sm * 128 * 256 + 2LL * I - 1) / (2LL * I));
+}
+
+// Ring forward geometry: rows per minibatch m, minibatches n_mb, ring slots (minibatches the
+// ring holds, at most n_mb).
+struct RingGeom {
+  int m = 0, n_mb = 0, slots = 0;
+};
+
+mok_status ring_geometry(const mok_layer_desc* d, RingGeom* g) {
+  const int64_t R = int64_t(d->T) * d->k;
+  int64_t m = d->minibatch;
+  if (m == 0) {
+    m = min_minibatch_rows(sm_count(), d->I);
+    if (m <= 0) return MOK_ERR_INVALID_ARG;  // no device to size the default minibatch
+  }
+  if (m > R) m = R;
+  const int64_t n_mb = (R + m - 1) / m;
+  int64_t slots = d->ring_bytes / (m * d->H * 2);
+  if (slots < 1) return MOK_ERR_UNSUPPORTED;  // the ring must hold one minibatch
+  if (slots > n_mb) slots = n_mb;
+  g->m = (int)m;
+  g->n_mb = (int)n_mb;
+  g->slots = (int)slots;
+  return MOK_OK;
+}
+
 mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   const int64_t T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
   int64_t off = 0;
@@ -82,6 +112,16 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->dx_g = take(R * H * 4);
   L->dg_part = take(R * (I / 256) * 4);
   L->dlogits = take(T * E * 4);
+  L->ring = L->mb_tables = L->mb_counters = -1;
+  if (d->ring_bytes > 0) {
+    RingGeom g;
+    const mok_status s = ring_geometry(d, &g);
+    if (s != MOK_OK) return s;
+    L->ring = take(int64_t(g.slots) * g.m * H * 2);
+    // mb_off [n_mb][E+1], mb_toff [n_mb][E+1], mb_tiles [n_mb], mb_start [n_mb+1]
+    L->mb_tables = take((int64_t(2) * g.n_mb * (E + 1) + 2 * int64_t(g.n_mb) + 1) * 4);
+    L->mb_counters = take(int64_t(2) * g.n_mb * 4);
+  }
   L->ws_bytes = off;
   return MOK_OK;
 }
@@ -158,10 +198,8 @@ mok_status mok_get_layout(const mok_layer_desc* desc, mok_layout* layout) {
 }
 
 int32_t mok_min_minibatch(int32_t n_sm, int32_t I) {
-  if (I <= 0) return 0;
   if (n_sm <= 0) n_sm = sm_count();
-  const int64_t rows = (2LL * n_sm * 128 * 256 + 2LL * I - 1) / (2LL * I);
-  return static_cast<int32_t>(rows);
+  return min_minibatch_rows(n_sm, I);
 }
 
 mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_router, const float* router_bias,
@@ -171,7 +209,8 @@ mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_ro
   mok_status s = check_desc(d);
   if (s != MOK_OK) return s;
   mok_layout L;
-  fill_layout(d, &L);
+  s = fill_layout(d, &L);
+  if (s != MOK_OK) return s;
   if (!topk_idx || !counts || !offsets || !row_of || !src_of || !ws) return MOK_ERR_INVALID_ARG;
   if ((int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
   const bool have_router = x != nullptr && w_router != nullptr;
@@ -202,10 +241,18 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
       !aligned16(ctx) || !aligned16(ws))
     return MOK_ERR_INVALID_ARG;
   mok_layout L;
-  fill_layout(d, &L);
+  s = fill_layout(d, &L);
+  if (s != MOK_OK) return s;
   if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
   const int n_sm = sm_count();
   if (n_sm <= 0) return MOK_ERR_CUDA;
+  RingGeom rg;
+  const int comm = d->comm_sms > 0 ? d->comm_sms : 8;
+  if (d->ring_bytes > 0) {
+    s = ring_geometry(d, &rg);
+    if (s != MOK_OK) return s;
+    if (comm >= n_sm) return MOK_ERR_INVALID_ARG;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
   int* status = at<int>(ws, L.status);
@@ -231,11 +278,44 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   // 3. schedule table
   MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of, src_of,
                                 tile_off, at<float>(ctx, L.gate_row), status, st));
-  // 4. pull dispatch into expert-contiguous rows
-  MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
-  // 5. grouped GEMM1 with the SwiGLU epilogue
-  MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
-                                                          status, n_sm, st));
+  if (d->ring_bytes == 0) {
+    // 4. pull dispatch into expert-contiguous rows
+    MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
+    // 5. grouped GEMM1 with the SwiGLU epilogue
+    MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
+                                                            status, n_sm, st));
+  } else {
+    // 4-5. ring forward: per-minibatch tables, then one persistent launch in which `comm`
+    //      CTAs gather minibatches into the ring while the others run GEMM1 on them
+    int32_t* tab = at<int32_t>(ws, L.mb_tables);
+    int32_t* mb_off = tab;
+    int32_t* mb_toff = mb_off + (size_t)rg.n_mb * (E + 1);
+    int32_t* mb_tiles = mb_toff + (size_t)rg.n_mb * (E + 1);
+    int32_t* mb_start = mb_tiles + rg.n_mb;
+    int32_t* counters = at<int32_t>(ws, L.mb_counters);
+    MOK_LAUNCH("ring_tables", st,
+               mok::launch_mb_tables(offsets, E, R, rg.m, rg.n_mb, I / 128, mb_off, mb_toff, mb_tiles, mb_start, st));
+    MOK_CUDA(cudaMemsetAsync(counters, 0, sizeof(int32_t) * 2 * rg.n_mb, st));
+    mok::RingArgs ra;
+    ra.x = x;
+    ra.src_of = src_of;
+    ra.k = k;
+    ra.R = R;
+    ra.H = H;
+    ra.I = I;
+    ra.E = E;
+    ra.mb_rows = rg.m;
+    ra.n_mb = rg.n_mb;
+    ra.ring_slots = rg.slots;
+    ra.comm_ctas = comm;
+    ra.ring = at<char>(ws, L.ring);
+    ra.mb_off = mb_off;
+    ra.mb_toff = mb_toff;
+    ra.mb_start = mb_start;
+    ra.gathered = counters;
+    ra.consumed = counters + rg.n_mb;
+    MOK_LAUNCH("ring_gemm1_swiglu", st, mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, st));
+  }
   // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
   MOK_LAUNCH("gemm2", st, mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
   // 7. weighted merge in fixed order
@@ -257,13 +337,20 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
       !aligned16(ws))
     return MOK_ERR_INVALID_ARG;
   mok_layout L;
-  fill_layout(d, &L);
+  s = fill_layout(d, &L);
+  if (s != MOK_OK) return s;
   if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
   const int n_sm = sm_count();
   if (n_sm <= 0) return MOK_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
   int* status = at<int>(ws, L.status);
+  if (d->ring_bytes > 0) {
+    // the ring forward kept the dispatched rows only in the ring: dispatch them again, into
+    // the expert-output scratch, which the backward does not otherwise use
+    MOK_LAUNCH("gather_x_replay", st,
+               mok::launch_gather_rows(x, at<int32_t>(ctx, L.src_of), k, R, H, at<char>(ws, L.expert_out), n_sm, st));
+  }
   const int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
   const float* gates = at<float>(ctx, L.gates);
   const float* scores = at<float>(ctx, L.scores);
@@ -272,7 +359,8 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   const int32_t* row_of = at<int32_t>(ctx, L.row_of);
   const int32_t* src_of = at<int32_t>(ctx, L.src_of);
   const float* gate_row = at<float>(ctx, L.gate_row);
-  const void* x_g = at<char>(ctx, L.x_g);
+  const void* x_g = d->ring_bytes > 0 ? static_cast<const void*>(at<char>(ws, L.expert_out))
+                                      : static_cast<const void*>(at<char>(ctx, L.x_g));
   const float* hu = at<float>(ctx, L.hu);
   void* dy_g = at<char>(ws, L.dy_g);
   void* dhu = at<char>(ws, L.dhu);

@@ -224,6 +224,47 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
                  : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
 }
 
+cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
+                              int* status, int n_sm, cudaStream_t st) {
+  using C = GemmCfg<MODE_RING, EPI_SWIGLU, SPLIT_NONE, 256>;
+  CUtensorMap ta, tb;
+  const uint64_t ring_rows = (uint64_t)ra.ring_slots * ra.mb_rows;
+  if (!tmap_2d(&ta, ra.ring, ra.H, ring_rows, BK, BM) || !tmap_3d(&tb, w13, ra.H, 2 * ra.I, ra.E, BK, 128))
+    return cudaErrorInvalidValue;
+  if (ra.comm_ctas < 1 || ra.comm_ctas >= n_sm) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(ra.E, nullptr, nullptr, status);
+  g.N = ra.I;
+  g.K = ra.H;
+  g.I = ra.I;
+  g.out0 = hu;
+  g.ld0 = 2LL * ra.I;
+  g.out1 = act_hi;
+  g.out2 = act_lo;
+  g.ld1 = ra.I;
+  g.comm_ctas = ra.comm_ctas;
+  g.n_mb = ra.n_mb;
+  g.mb_rows = ra.mb_rows;
+  g.ring_slots = ra.ring_slots;
+  g.R = ra.R;
+  g.k_top = ra.k;
+  g.H = ra.H;
+  g.mb_off = ra.mb_off;
+  g.mb_toff = ra.mb_toff;
+  g.mb_start = ra.mb_start;
+  g.gathered = ra.gathered;
+  g.consumed = ra.consumed;
+  g.x = reinterpret_cast<const __nv_bfloat16*>(ra.x);
+  g.src_of = ra.src_of;
+  g.ring = reinterpret_cast<__nv_bfloat16*>(ra.ring);
+  auto kern = gemm_kernel<MODE_RING, EPI_SWIGLU, SPLIT_NONE, 256>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
+  if (err != cudaSuccess) return err;
+  // gathering and GEMM CTAs wait on each other: all of them must be resident at once
+  void* params[] = {(void*)&ta, (void*)&ta, (void*)&tb, (void*)&tb, (void*)&ta, (void*)&g};
+  return cudaLaunchCooperativeKernel((const void*)kern, dim3(n_sm), dim3(GEMM_THREADS), params,
+                                     C::smem_bytes(ra.E), st);
+}
+
 // ----------------------------------------------------------------------------- wait test
 __global__ void test_wait_kernel(int* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;

@@ -50,7 +50,12 @@ constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom colum
 #define MOK_MN_SBO 1024
 #endif
 
-enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3 };
+// MODE_RING: GEMM1 of the ring forward.  A = the token ring (bf16 [slots * mb_rows][H]);
+// CTAs [0, comm_ctas) gather expert-sorted rows into ring slots minibatch by minibatch, the
+// other CTAs run the minibatches' grouped-GEMM tiles in minibatch order.  A minibatch's
+// tiles wait until its rows are gathered (counter `gathered`); a slot is refilled only after
+// every tile of the minibatch it held has finished (counter `consumed`).
+enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, MODE_RING = 4 };
 enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5 };
 enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 
@@ -72,6 +77,22 @@ struct GemmArgs {
   const float* hu;          // SWIGLU_BWD: saved h | u (fp32)
   const float* gate_row;    // SWIGLU_BWD: gate of each row
   int* status;
+  // MODE_RING
+  int comm_ctas;            // gathering CTAs (the first ones of the grid)
+  int n_mb;                 // minibatches
+  int mb_rows;              // rows per minibatch (the last one may be shorter)
+  int ring_slots;           // minibatches the ring holds
+  int R;                    // all rows
+  int k_top;                // experts per token (row r holds token src_of[r] / k_top)
+  int H;
+  const int* mb_off;        // [n_mb][E+1] expert row offsets inside each minibatch
+  const int* mb_toff;       // [n_mb][E+1] prefix of m-tiles inside each minibatch
+  const int* mb_start;      // [n_mb+1] first tile of each minibatch
+  int* gathered;            // [n_mb] rows gathered
+  int* consumed;            // [n_mb] epilogue warps finished (4 per tile)
+  const __nv_bfloat16* x;   // [T][H] tokens
+  const int* src_of;        // [R]
+  __nv_bfloat16* ring;      // [ring_slots * mb_rows][H]
 };
 
 struct TileInfo {
@@ -80,6 +101,7 @@ struct TileInfo {
   int rows;   // valid output rows (ROWS/DGRAD/DENSE) or K rows (WGRAD)
   int nkb;    // K blocks
   int mt;     // ROWS/DGRAD: number of 128-row tiles of this expert (they share each weight tile)
+  int mb;     // RING: minibatch of the tile (row0 / rows are inside the minibatch)
 };
 
 template <int MODE, int EPI, int SPLIT, int BN_>
@@ -132,6 +154,31 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmArgs& a, int g, const 
     t.rows = s_off[t.e + 1] - t.row0;
     t.nkb = (t.rows + BK - 1) / BK;
     t.mt = MT;
+  } else if (MODE == MODE_RING) {
+    // minibatch: largest mb with mb_start[mb] <= g; then the grouped decode inside it
+    int lo = 0, hi = a.n_mb;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(&a.mb_start[mid]) <= g) lo = mid; else hi = mid;
+    }
+    t.mb = lo;
+    const int* toff = a.mb_toff + (size_t)lo * (a.E + 1);
+    const int* off = a.mb_off + (size_t)lo * (a.E + 1);
+    const int gl = g - __ldg(&a.mb_start[lo]);
+    int el = 0, eh = a.E;
+    while (eh - el > 1) {
+      const int mid = (el + eh) >> 1;
+      if (__ldg(&toff[mid]) * NT <= gl) el = mid; else eh = mid;
+    }
+    t.e = el;
+    const int Me = __ldg(&toff[el + 1]) - __ldg(&toff[el]);
+    const int local = gl - __ldg(&toff[el]) * NT;
+    t.n = local / Me;
+    t.m = local - t.n * Me;
+    t.row0 = __ldg(&off[el]) + t.m * BM;
+    t.rows = min(BM, __ldg(&off[el + 1]) - t.row0);
+    t.nkb = a.K / BK;
+    t.mt = Me;
   } else {
     // expert e owns tiles [tile_off[e]*NT, tile_off[e+1]*NT); inside, m runs fastest so the
     // m-tiles of one expert that share a weight tile are dealt to neighbouring CTAs.
@@ -173,6 +220,67 @@ __device__ __forceinline__ void store_u32x16(void* dst, const uint32_t (&p)[16])
   for (int j = 0; j < 4; ++j) d[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits (one thread) until *p >= target; bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_counter(const int* p, int target, int* status, int site) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (ld_acquire_gpu(p) >= target) return true;
+    __nanosleep(64);
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      report_status(status, MOK_DEV_TIMEOUT, site);
+      return false;
+    }
+  }
+}
+
+// Gathering role of the ring forward: warps of the first comm_ctas CTAs copy the rows of each
+// minibatch, in order, into its ring slot (the pull dispatch), then publish how many rows they
+// copied.  A slot is overwritten only after every tile of the minibatch that held it finished.
+__device__ void ring_gather(const GemmArgs& a) {
+  const int warps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * warps + warp;
+  const int nw = a.comm_ctas * warps;
+  const int vec = a.H / 8;
+  for (int mb = 0; mb < a.n_mb; ++mb) {
+    const int slot = mb % a.ring_slots;
+    const int r0 = mb * a.mb_rows;
+    const int rows = min(a.mb_rows, a.R - r0);
+    if (mb >= a.ring_slots) {
+      const int old = mb - a.ring_slots;
+      int ok = 1;
+      if (lane == 0)
+        ok = wait_counter(&a.consumed[old], 4 * (a.mb_start[old + 1] - a.mb_start[old]), a.status, SITE_RING_WAIT);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+    int mine = 0;
+    for (int i = gw; i < rows; i += nw) {
+      const int tok = a.src_of[r0 + i] / a.k_top;
+      const uint4* s = reinterpret_cast<const uint4*>(a.x) + (size_t)tok * vec;
+      uint4* d = reinterpret_cast<uint4*>(a.ring) + ((size_t)slot * a.mb_rows + i) * vec;
+      for (int c = lane; c < vec; c += 32) d[c] = s[c];
+      ++mine;
+    }
+    __threadfence();
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0 && mine > 0) atomicAdd(&a.gathered[mb], mine);
+  }
+}
+
 template <int MODE, int EPI, int SPLIT, int BN_>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
@@ -200,6 +308,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
 
+  if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
+    ring_gather(args);
+    return;
+  }
+  // the GEMM CTAs of this launch (all of them, except the gathering ones of MODE_RING)
+  const int cta0 = (MODE == MODE_RING) ? (int)blockIdx.x - args.comm_ctas : (int)blockIdx.x;
+  const int ncta = (MODE == MODE_RING) ? (int)gridDim.x - args.comm_ctas : (int)gridDim.x;
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
@@ -213,7 +329,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (MODE != MODE_DENSE) {
+  if (MODE != MODE_DENSE && MODE != MODE_RING) {
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
       s_off[i] = args.offsets[i];
       s_toff[i] = (MODE == MODE_WGRAD) ? 0 : args.tile_off[i];
@@ -229,7 +345,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int NT = C::n_tiles(args);
-  const int total = args.total_tiles >= 0 ? args.total_tiles : s_toff[args.E] * NT;
+  const int total = (MODE == MODE_RING)       ? args.mb_start[args.n_mb]
+                    : args.total_tiles >= 0 ? args.total_tiles
+                                            : s_toff[args.E] * NT;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -245,11 +363,27 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+      int ring_ready = -1;  // MODE_RING: last minibatch known to be gathered
+      for (int g = cta0; g < total && ok; g += ncta) {
         const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
         // a weight tile is read once when its expert has a single m-tile; otherwise the
         // neighbouring CTAs that run the expert's other m-tiles read it again from L2
         const uint64_t pol_w = (MODE == MODE_WGRAD) ? pol_act : (t.mt > 1 ? pol_shared : pol_once);
+        int a_row = t.row0;
+        if (MODE == MODE_RING) {
+          // rows of this minibatch must be in the ring before the first load of its tiles
+          if (t.mb > ring_ready) {
+            const int rows_mb = min(args.mb_rows, args.R - t.mb * args.mb_rows);
+            if (!wait_counter(&args.gathered[t.mb], rows_mb, args.status, SITE_RING_WAIT)) {
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();
+            ring_ready = t.mb;
+          }
+          a_row = (t.mb % args.ring_slots) * args.mb_rows + t.row0;
+        }
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY)) {
             ok = false;
@@ -265,9 +399,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (MODE == MODE_DENSE) {
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
             tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
-          } else if (MODE == MODE_ROWS) {
-            tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
-            if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, t.row0, pol_act);
+          } else if (MODE == MODE_ROWS || MODE == MODE_RING) {
+            tma_load_2d(sa, &tmA, fb, k0, a_row, pol_act);
+            if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, a_row, pol_act);
             if (EPI == EPI_SWIGLU) {
               tma_load_3d(sb, &tmB, fb, k0, t.n * 128, t.e, pol_w);
               tma_load_3d(sb + C::B_TILE / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
@@ -324,7 +458,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     bool any_mma = false;
-    for (int g = blockIdx.x; g < total && ok; g += gridDim.x) {
+    for (int g = cta0; g < total && ok; g += ncta) {
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (t.nkb == 0) continue;
       int w_ok = 1;
@@ -413,7 +547,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int stg_buf = 0;  // WGRAD: staging buffer alternation
-    for (int g = blockIdx.x; g < total; g += gridDim.x) {
+    for (int g = cta0; g < total; g += ncta) {
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (MODE == MODE_WGRAD && t.nkb == 0) {
         // an expert without rows: its weight gradient is zero (transposed layout out[e][n][m])
@@ -433,7 +567,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * C::ACC_COLS + (uint32_t(quarter * 32) << 16);
       const bool valid = (MODE == MODE_WGRAD) ? true : (r_local < t.rows);
-      const long long row = (MODE == MODE_WGRAD) ? 0 : (long long)(t.row0 + r_local);
+      const long long row = (MODE == MODE_WGRAD)  ? 0
+                            : (MODE == MODE_RING) ? (long long)t.mb * args.mb_rows + t.row0 + r_local
+                                                  : (long long)(t.row0 + r_local);
 
       if (EPI == EPI_F32) {
         float* out = reinterpret_cast<float*>(args.out0) + row * args.ld0;
@@ -599,6 +735,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (MODE == MODE_RING && lane == 0) {
+        // this warp is done with the tile: its minibatch's ring slot may be refilled once
+        // every epilogue warp of every tile of the minibatch has counted in
+        __threadfence();
+        atomicAdd(&args.consumed[t.mb], 1);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -16,6 +16,8 @@ cudaError_t launch_router_dlogits(const float* dg_part, int n_part, const int32_
                                   const int32_t* topk_idx, const float* gates, const float* scores, int T,
                                   int E, int k, int router, int renorm, float route_scale, float* dgates,
                                   float* dl, cudaStream_t st);
+cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int32_t* mb_off,
+                             int32_t* mb_toff, int32_t* mb_tiles, int32_t* mb_start, cudaStream_t st);
 cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* offsets, const int32_t* src_of,
                                 int T, int H, int E, int k, int sparse, float* dw, cudaStream_t st);
 
@@ -48,6 +50,22 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
                          int E, const int32_t* offsets, void* dw, int out_f32, int* status, int n_sm,
                          cudaStream_t st);
+// Ring forward GEMM1: comm_ctas CTAs gather minibatches into the ring, the rest run GEMM1
+// (SwiGLU epilogue, rows written at their global position).  Cooperative launch, grid = n_sm.
+struct RingArgs {
+  const void* x;
+  const int32_t* src_of;
+  int k, R, H, I, E;
+  int mb_rows, n_mb, ring_slots, comm_ctas;
+  void* ring;
+  const int32_t* mb_off;
+  const int32_t* mb_toff;
+  const int32_t* mb_start;
+  int32_t* gathered;
+  int32_t* consumed;
+};
+cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
+                              int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

@@ -386,7 +386,77 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ----------------------------------------------------------------------------- ring tables
+// Minibatch mb holds the sorted rows [mb*m, mb*m + rows_mb).  One CTA per minibatch (threads
+// over experts) cuts the expert segments at its edges: mb_off[mb][e] = clamp(offsets[e] - r0,
+// 0, rows_mb), and scans the 128-row tiles of each cut segment into mb_toff[mb][e];
+// mb_tiles[mb] = total tiles * n_tiles (the column tiles of GEMM1).
+__global__ void __launch_bounds__(1024)
+    mb_tables_kernel(const int32_t* __restrict__ offsets, int E, int R, int m, int n_tiles,
+                     int32_t* __restrict__ mb_off, int32_t* __restrict__ mb_toff, int32_t* __restrict__ mb_tiles) {
+  __shared__ int warp_tot[32];
+  const int mb = blockIdx.x;
+  const int r0 = mb * m;
+  const int rows = min(m, R - r0);
+  const int e = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int tiles = 0;
+  if (e < E) {
+    const int lo = min(max(offsets[e] - r0, 0), rows);
+    const int hi = min(max(offsets[e + 1] - r0, 0), rows);
+    tiles = (hi - lo + 127) / 128;
+    mb_off[(size_t)mb * (E + 1) + e] = lo;
+  }
+  if (e == 0) mb_off[(size_t)mb * (E + 1) + E] = min(max(offsets[E] - r0, 0), rows);
+  int inc = tiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = warp_tot[lane];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    warp_tot[lane] = x - v;
+  }
+  __syncthreads();
+  const int excl = warp_tot[warp] + inc - tiles;
+  if (e < E) mb_toff[(size_t)mb * (E + 1) + e] = excl;
+  if (e == E - 1) {
+    mb_toff[(size_t)mb * (E + 1) + E] = excl + tiles;
+    mb_tiles[mb] = (excl + tiles) * n_tiles;
+  }
+}
+
+// mb_start = exclusive prefix of mb_tiles (n_mb + 1 entries), one thread, fixed order.
+__global__ void mb_start_kernel(const int32_t* __restrict__ mb_tiles, int n_mb, int32_t* __restrict__ mb_start) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < n_mb; ++i) {
+      mb_start[i] = run;
+      run += mb_tiles[i];
+    }
+    mb_start[n_mb] = run;
+  }
+}
+
 // ----------------------------------------------------------------------------- launchers
+cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int32_t* mb_off,
+                             int32_t* mb_toff, int32_t* mb_tiles, int32_t* mb_start, cudaStream_t st) {
+  mb_tables_kernel<<<n_mb, 1024, 0, st>>>(offsets, E, R, m, n_tiles, mb_off, mb_toff, mb_tiles);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  mb_start_kernel<<<1, 32, 0, st>>>(mb_tiles, n_mb, mb_start);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float* logits, const float* bias, const int32_t* given, int T, int E,
                         int k, int router, int renorm, float route_scale, int32_t* topk_idx,
                         float* gates, float* scores, int* status, cudaStream_t st) {

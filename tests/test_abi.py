@@ -41,7 +41,7 @@ def test_layout_sizes_and_alignment(lib):
     lay = mok.get_layout(mok.desc_from_shape(W.DSV3))
     R, H, I = W.DSV3.R, W.DSV3.H, W.DSV3.I
     for name, off in lay.items():
-        assert off % 256 == 0, name
+        assert off % 256 == 0 or (off == -1 and name in ("ring", "mb_tables", "mb_counters")), name
     assert lay["ctx_bytes"] >= lay["hu"] + R * 2 * I * 2
     assert lay["ws_bytes"] >= lay["dlogits"] + W.DSV3.T * W.DSV3.E * 4
     assert lay["status"] == 0
@@ -58,6 +58,22 @@ def test_desc_validation(lib, field, value, code):
         code = 2
     lay = N.Layout()
     assert lib.mok_get_layout(ctypes.byref(d), ctypes.byref(lay)) == code
+
+
+def test_ring_layout(lib):
+    """Ring forward: the ring holds whole minibatches (at most as many as there are)."""
+    shp = W.RING
+    m = 2368
+    d = mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES)
+    lay = mok.get_layout(d)
+    slots = W.RING_BYTES // (m * shp.H * 2)
+    n_mb = -(-shp.R // m)
+    assert lay["mb_tables"] - lay["ring"] >= slots * m * shp.H * 2
+    assert lay["mb_counters"] - lay["mb_tables"] >= (2 * n_mb * (shp.E + 1) + 2 * n_mb + 1) * 4
+    # a ring below one minibatch is refused
+    d.ring_bytes = m * shp.H * 2 - 1
+    lay_ = N.Layout()
+    assert lib.mok_get_layout(ctypes.byref(d), ctypes.byref(lay_)) == 2
 
 
 def test_min_minibatch_reproduces_page_number(lib):

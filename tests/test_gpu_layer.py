@@ -206,3 +206,45 @@ def test_stuck_wait_times_out_and_context_survives():
     # the context is still usable afterwards
     inp = W.make_inputs(TINY, seed=0, device="cpu")
     _run(TINY, inp)
+
+
+# ----------------------------------------------------------------------------- ring forward
+
+@pytest.mark.parametrize("shape,minibatch,slots,comm", [
+    (MID, 300, 2, 4),        # ragged minibatches (not a multiple of 128), the ring wraps 4 times
+    (MID, 1024, 1, 8),       # one slot: gathering and GEMM1 alternate
+    (MID_SKEW, 700, 3, 2),   # skewed experts cut at minibatch edges
+    (TINY, 96, 2, 3),        # tiny layer, softmax router
+], ids=lambda v: getattr(v, "name", str(v)))
+def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm):
+    """The ring forward (persistent launch: gathering CTAs fill ring slots while GEMM CTAs run
+    GEMM1 on earlier minibatches) computes every row exactly as the plain forward does, so y,
+    h|u and a must be bitwise equal; the backward after a ring forward must match too."""
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    dev = _gpu_inputs(inp)
+    plain = mok.MoELayer(mok.desc_from_shape(shape))
+    y0 = plain.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"])
+    g0 = plain.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+    ring_bytes = slots * minibatch * shape.H * 2
+    ring = mok.MoELayer(mok.desc_from_shape(shape, minibatch=minibatch, ring_bytes=ring_bytes, comm_sms=comm))
+    assert ring.layout["ring"] >= 0
+    for _ in range(2):  # the second call reuses the ring and the counters
+        y1 = ring.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"])
+        torch.cuda.synchronize()
+        assert ring.status() == (0, 0)
+        assert torch.equal(y1, y0)
+        assert torch.equal(ring.view("hu"), plain.view("hu"))
+        assert torch.equal(ring.view("act"), plain.view("act"))
+    g1 = ring.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    assert ring.status() == (0, 0)
+    for name in ("dx", "dw_router", "dw13", "dw2", "dgates"):
+        assert torch.equal(g1[name], g0[name]), name
+
+
+def test_ring_rejects_a_ring_smaller_than_one_minibatch():
+    shape = MID
+    desc = mok.desc_from_shape(shape, minibatch=512, ring_bytes=511 * shape.H * 2)
+    with pytest.raises(mok.MokError) as info:
+        mok.get_layout(desc)
+    assert info.value.code == 2
