@@ -385,6 +385,60 @@ def run_mok(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def run_ring_sweep(args):
+    """Ring forward at T=16384 (256 experts, top-8, hidden 7168): a fixed 512 MiB token ring
+    and the minibatch sizes 512 / 1024 / 2368 / 2560 / 4096, each timed over K forwards after
+    W warm-ups, against the same forward without the ring.  One JSON line."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    mok.load()
+    shp = W.RING
+    inp = W.make_inputs(shp, seed=0, device="cuda", with_dy=False)
+    y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def time_forward(layer):
+        for _ in range(args.warmup):
+            layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
+        torch.cuda.synchronize()
+        if layer.status() != (0, 0):
+            raise RuntimeError("device status set during warm-up")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if layer.status() != (0, 0):
+            raise RuntimeError("device status set")
+        return e0.elapsed_time(e1) / args.steps
+
+    plain = mok.MoELayer(mok.desc_from_shape(shp))
+    plain_ms = time_forward(plain)
+    y_plain = y.clone()
+    del plain
+    sweep = {}
+    for m in W.RING_MINIBATCHES:
+        layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES))
+        ms = time_forward(layer)
+        sweep[str(m)] = {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
+                         "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
+                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain))}
+        del layer
+    best = min(sweep.values(), key=lambda v: v["fwd_ms"])
+    line = {"metric": "ring forward tokens/s (fixed 512 MiB token ring, minibatch sweep)",
+            "value": best["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": best["fwd_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
+            "config": {"workload": shp.name, "ring_bytes": W.RING_BYTES, "comm_sms": 8, "passes": "fwd",
+                       "min_minibatch_two_waves": mok.min_minibatch(0, shp.I)},
+            "plain_forward_ms": round(plain_ms, 4), "sweep": sweep}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-sample":
         T, E, rep = int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4])
@@ -396,6 +450,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring-sweep", action="store_true",
+                    help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
                     help="dsv3: the benchmarked layer; dsv3_e16_t256: the same per-expert shape on "
                          "16 experts and 256 tokens (a few GB, for profiler captures)")
@@ -407,6 +463,10 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.ring_sweep:
+        if rank == 0:
+            run_ring_sweep(args)
         return
     if world > 1:
         import torch
