@@ -245,39 +245,57 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, int* stat
   }
 }
 
-// Gathering role of the ring forward: warps of the first comm_ctas CTAs copy the rows of each
-// minibatch, in order, into its ring slot (the pull dispatch), then publish how many rows they
-// copied.  A slot is overwritten only after every tile of the minibatch that held it finished.
-__device__ void ring_gather(const GemmArgs& a) {
-  const int warps = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * warps + warp;
-  const int nw = a.comm_ctas * warps;
-  const int vec = a.H / 8;
+// Gathering role of the ring forward (the pull dispatch): one thread of each of the first
+// comm_ctas CTAs moves its share of each minibatch's rows (row i of the minibatch goes to CTA
+// i % comm_ctas) from the token matrix into the minibatch's ring slot with bulk async copies
+// through shared memory: up to `ns` rows are in flight, a row's staging buffer is refilled as
+// soon as the store of the row before it has left shared memory.  When the CTA's rows of a
+// minibatch are in the ring it publishes their count.  A ring slot is overwritten only after
+// every GEMM tile of the minibatch that held it has finished.
+__device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint64_t* bars) {
+  if (threadIdx.x != 0) return;
+  const uint32_t row_bytes = (uint32_t)a.H * 2;
+  int ns = buf_bytes / (int)row_bytes;
+  if (ns > 16) ns = 16;
+  for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&bars[j]), 1);
+  fence_mbar_init();
+  volatile int no_abort = 0;
+  long long gcount = 0;  // rows this CTA has staged so far (slot = gcount % ns, parity = gcount / ns)
+  auto issue_load = [&](long long g, int r) {
+    const int j = (int)(g % ns);
+    const int tok = a.src_of[r] / a.k_top;
+    mbar_arrive_expect_tx(smem_u32(&bars[j]), row_bytes);
+    bulk_load_g2s(smem_u32(buf + (size_t)j * row_bytes), a.x + (size_t)tok * a.H, row_bytes, smem_u32(&bars[j]));
+  };
   for (int mb = 0; mb < a.n_mb; ++mb) {
     const int slot = mb % a.ring_slots;
     const int r0 = mb * a.mb_rows;
     const int rows = min(a.mb_rows, a.R - r0);
     if (mb >= a.ring_slots) {
       const int old = mb - a.ring_slots;
-      int ok = 1;
-      if (lane == 0)
-        ok = wait_counter(&a.consumed[old], 4 * (a.mb_start[old + 1] - a.mb_start[old]), a.status, SITE_RING_WAIT);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+      if (!wait_counter(&a.consumed[old], 4 * (a.mb_start[old + 1] - a.mb_start[old]), a.status, SITE_RING_WAIT))
+        return;
     }
-    int mine = 0;
-    for (int i = gw; i < rows; i += nw) {
-      const int tok = a.src_of[r0 + i] / a.k_top;
-      const uint4* s = reinterpret_cast<const uint4*>(a.x) + (size_t)tok * vec;
-      uint4* d = reinterpret_cast<uint4*>(a.ring) + ((size_t)slot * a.mb_rows + i) * vec;
-      for (int c = lane; c < vec; c += 32) d[c] = s[c];
-      ++mine;
+    const int cnt = rows > (int)blockIdx.x ? (rows - (int)blockIdx.x + a.comm_ctas - 1) / a.comm_ctas : 0;
+    for (int t = 0; t < cnt && t < ns; ++t) issue_load(gcount + t, r0 + (int)blockIdx.x + t * a.comm_ctas);
+    for (int t = 0; t < cnt; ++t) {
+      const long long g = gcount + t;
+      const int j = (int)(g % ns);
+      if (!mbar_wait(smem_u32(&bars[j]), (uint32_t)((g / ns) & 1), &no_abort, a.status, SITE_RING_WAIT)) return;
+      const int i = (int)blockIdx.x + t * a.comm_ctas;
+      bulk_store_s2g(a.ring + ((size_t)slot * a.mb_rows + i) * a.H, smem_u32(buf + (size_t)j * row_bytes), row_bytes);
+      bulk_commit_group();
+      // the staging buffer of row t-1 takes row t-1+ns once that row's store has read it
+      if (t >= 1 && t - 1 + ns < cnt) {
+        bulk_wait_group_read<1>();
+        issue_load(g - 1 + ns, r0 + (int)blockIdx.x + (t - 1 + ns) * a.comm_ctas);
+      }
     }
-    __threadfence();
+    gcount += cnt;
+    bulk_wait_group_all();  // this CTA's rows of the minibatch are in the ring
     fence_proxy_async_global();
-    __syncwarp();
-    if (lane == 0 && mine > 0) atomicAdd(&a.gathered[mb], mine);
+    __threadfence();
+    if (cnt > 0) atomicAdd(&a.gathered[mb], cnt);
   }
 }
 
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
 
   if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
-    ring_gather(args);
+    ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
     return;
   }
   // the GEMM CTAs of this launch (all of them, except the gathering ones of MODE_RING)
