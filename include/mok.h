@@ -188,6 +188,33 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
                            const void* w2, void* y, void* ctx, size_t ctx_bytes, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* MXFP8 weights for mok_moe_forward_mxfp8.  MXFP8 is one of the two precisions of the pages'
+ * kernel ("Mixture-of-Kittens (MoK)", sd114.wiki, benchmark section); the format is read as OCP
+ * Microscaling v1.0: E4M3 elements, one E8M0 scale per 32 consecutive elements along the GEMM's
+ * reduction dimension, X = clamp(floor(log2 amax) - 8, -127, 127), elements RNE(v / 2^X)
+ * saturated at +-448, scale byte X + 127.
+ *   w13 [E][2I][H] bf16 -> w13_q [E][2I][H] E4M3 bytes, w13_scale [E][H/32][2I] bytes
+ *   w2  [E][H][I]  bf16 -> w2_q  [E][H][I]  E4M3 bytes, w2_scale  [E][I/32][H]  bytes
+ * (scales are stored k-block-major so that one load brings a tile's scales).  All device
+ * pointers, 16-byte aligned. */
+mok_status mok_quantize_weights(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_q,
+                                void* w13_scale, void* w2_q, void* w2_scale, void* stream);
+
+/* Layer forward with MXFP8 expert GEMMs (desc->precision must be MOK_MXFP8, no ring).  As
+ * mok_moe_forward, with the expert weights given as mok_quantize_weights output.  The MXFP8
+ * activation quantisation sits on the data path ("把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源
+ * GPU 内核 MoK", aientropygate.com, §03 ③): the gather quantises each dispatched row in
+ * 32-element blocks along H and the GEMM1 epilogue quantises a = silu(h) * u along I; both keep
+ * the quantised values as bf16 (E4M3 * 2^X is exact in bf16).  The GEMMs stream E4M3 weights,
+ * expand them exactly to bf16 in shared memory and accumulate in fp32, so each product equals
+ * the MXFP8 product.  The router stays in bf16.  ctx / ws as for mok_moe_forward (ctx x_g holds
+ * the quantised rows).  There is no MXFP8 backward: mok_moe_backward returns
+ * MOK_ERR_UNSUPPORTED for an MXFP8 descriptor. */
+mok_status mok_moe_forward_mxfp8(const mok_layer_desc* desc, const void* x, const void* w_router,
+                                 const float* router_bias, const int32_t* given_topk, const void* w13_q,
+                                 const void* w13_scale, const void* w2_q, const void* w2_scale, void* y,
+                                 void* ctx, size_t ctx_bytes, void* ws, size_t ws_bytes, void* stream);
+
 /* Layer backward for upstream gradient dy [T][H] bf16, using the ctx written by the
  * matching mok_moe_forward (same desc, inputs and weights).  Outputs:
  *   dx [T][H] bf16, dw_router [E][H] f32, dw13 [E][2I][H] and dw2 [E][H][I] in f32 (bf16

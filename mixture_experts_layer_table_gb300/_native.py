@@ -319,3 +319,54 @@ def schedule_noalloc(desc, x, w_router, router_bias, given_topk, topk_idx, gates
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(topk_idx),
         _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(device_status),
         _stream(stream)))
+
+
+def _mx_fn(name, nargs):
+    fn = getattr(load(), name)
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.POINTER(LayerDesc)] + [ctypes.c_void_p] * nargs
+        fn.restype = ctypes.c_int32
+    return fn
+
+
+def quantize_weights(desc, w13, w2, stream=None):
+    """mok_quantize_weights: MXFP8 (E4M3 + E8M0 per 32 along K) copies of the expert weights.
+    Returns {"w13_q", "w13_scale", "w2_q", "w2_scale"} as uint8 CUDA tensors."""
+    _expect(w13, (desc.E, 2 * desc.I, desc.H), torch.bfloat16, "w13")
+    _expect(w2, (desc.E, desc.H, desc.I), torch.bfloat16, "w2")
+    dev = w13.device
+    E, H, I = desc.E, desc.H, desc.I
+    out = {"w13_q": torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev),
+           "w13_scale": torch.empty((E, H // 32, 2 * I), dtype=torch.uint8, device=dev),
+           "w2_q": torch.empty((E, H, I), dtype=torch.uint8, device=dev),
+           "w2_scale": torch.empty((E, I // 32, H), dtype=torch.uint8, device=dev)}
+    fn = load().mok_quantize_weights
+    fn.argtypes = [ctypes.POINTER(LayerDesc)] + [ctypes.c_void_p] * 7
+    fn.restype = ctypes.c_int32
+    _check("mok_quantize_weights", fn(ctypes.byref(desc), _ptr(w13), _ptr(w2), _ptr(out["w13_q"]),
+                                      _ptr(out["w13_scale"]), _ptr(out["w2_q"]), _ptr(out["w2_scale"]),
+                                      _stream(stream)))
+    return out
+
+
+def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws, stream=None):
+    """mok_moe_forward_mxfp8 with the weights of ``quantize_weights``."""
+    E, H, I = desc.E, desc.H, desc.I
+    _expect(x, (desc.T, H), torch.bfloat16, "x")
+    _expect(w_router, (E, H), torch.bfloat16, "w_router")
+    _expect(router_bias, (E,), torch.float32, "router_bias", nullable=True)
+    _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
+    _expect(wq["w13_q"], (E, 2 * I, H), torch.uint8, "w13_q")
+    _expect(wq["w13_scale"], (E, H // 32, 2 * I), torch.uint8, "w13_scale")
+    _expect(wq["w2_q"], (E, H, I), torch.uint8, "w2_q")
+    _expect(wq["w2_scale"], (E, I // 32, H), torch.uint8, "w2_scale")
+    _expect(y, (desc.T, H), torch.bfloat16, "y")
+    fn = load().mok_moe_forward_mxfp8
+    P, SZ = ctypes.c_void_p, ctypes.c_size_t
+    fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, P, P, P, P, SZ, P, SZ, P]
+    fn.restype = ctypes.c_int32
+    _check("mok_moe_forward_mxfp8", fn(
+        ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(wq["w13_q"]),
+        _ptr(wq["w13_scale"]), _ptr(wq["w2_q"]), _ptr(wq["w2_scale"]), _ptr(y), _ptr(ctx),
+        ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+    return y

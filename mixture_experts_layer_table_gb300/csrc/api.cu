@@ -323,6 +323,69 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   return MOK_OK;
 }
 
+mok_status mok_quantize_weights(const mok_layer_desc* d, const void* w13, const void* w2, void* w13_q, void* w13_scale,
+                                void* w2_q, void* w2_scale, void* stream) {
+  mok_status s = check_desc(d);
+  if (s != MOK_OK) return s;
+  const void* ptrs[] = {w13, w2, w13_q, w13_scale, w2_q, w2_scale};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MOK_ERR_INVALID_ARG;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOK_LAUNCH("quantize_w13", st, mok::launch_quantize_weights(w13, w13_q, w13_scale, d->E, 2 * d->I, d->H, n_sm, st));
+  MOK_LAUNCH("quantize_w2", st, mok::launch_quantize_weights(w2, w2_q, w2_scale, d->E, d->H, d->I, n_sm, st));
+  return MOK_OK;
+}
+
+mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const void* w_router,
+                                 const float* router_bias, const int32_t* given_topk, const void* w13_q,
+                                 const void* w13_scale, const void* w2_q, const void* w2_scale, void* y, void* ctx,
+                                 size_t ctx_bytes, void* ws, size_t ws_bytes, void* stream) {
+  mok_status s = check_desc(d);
+  if (s != MOK_OK) return s;
+  if (d->precision != MOK_MXFP8 || d->ring_bytes != 0) return MOK_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, w_router, w13_q, w13_scale, w2_q, w2_scale, y, ctx, ws};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return MOK_ERR_INVALID_ARG;
+  mok_layout L;
+  s = fill_layout(d, &L);
+  if (s != MOK_OK) return s;
+  if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
+  int* status = at<int>(ws, L.status);
+  int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
+  float* gates = at<float>(ctx, L.gates);
+  int32_t* offsets = at<int32_t>(ctx, L.offsets);
+  int32_t* tile_off = at<int32_t>(ctx, L.tile_off);
+  int32_t* row_of = at<int32_t>(ctx, L.row_of);
+  int32_t* src_of = at<int32_t>(ctx, L.src_of);
+  void* x_g = at<char>(ctx, L.x_g);
+  float* hu = at<float>(ctx, L.hu);
+  void* act = at<char>(ws, L.act);
+  float* o = at<float>(ws, L.expert_out);
+  float* logits = at<float>(ws, L.logits);
+
+  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
+  MOK_LAUNCH("topk", st, mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm,
+                                          d->route_scale, topk_idx, gates, at<float>(ctx, L.scores), status, st));
+  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of,
+                                                  src_of, tile_off, at<float>(ctx, L.gate_row), status, st));
+  // pull dispatch with the MXFP8 quantisation of each row along H
+  MOK_LAUNCH("gather_x_mx", st, mok::launch_gather_rows_mx(x, src_of, k, R, H, x_g, n_sm, st));
+  // GEMM1 on E4M3 weights, SwiGLU, a quantised along I
+  MOK_LAUNCH("gemm1_swiglu_mx", st, mok::launch_gemm1_swiglu_mx(x_g, w13_q, w13_scale, R, H, I, E, offsets, tile_off,
+                                                                hu, act, status, n_sm, st));
+  MOK_LAUNCH("gemm2_mx", st, mok::launch_gemm2_mx(act, w2_q, w2_scale, R, H, I, E, offsets, tile_off, o, status, n_sm,
+                                                  st));
+  MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
+  return MOK_OK;
+}
+
 mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void* x, const void* w_router,
                             const void* w13, const void* w2, const void* ctx, size_t ctx_bytes, void* dx,
                             float* dw_router, void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,

@@ -30,6 +30,7 @@
 #pragma once
 #include <cuda_bf16.h>
 
+#include "mx.cuh"
 #include "ptx.cuh"
 
 namespace mok {
@@ -56,8 +57,13 @@ constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom colum
 // tiles wait until its rows are gathered (counter `gathered`); a slot is refilled only after
 // every tile of the minibatch it held has finished (counter `consumed`).
 enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, MODE_RING = 4 };
-enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5 };
-enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
+// EPI_SWIGLU_MX: SwiGLU with a quantised to MXFP8 along I (32-column blocks) and stored as bf16
+// (E4M3 * 2^X is exact in bf16), the A operand of the MXFP8 GEMM2.
+enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5, EPI_SWIGLU_MX = 6 };
+// SPLIT_BMX: B is MXFP8 (E4M3 bytes + one E8M0 scale per 32 along K); TMA brings the bytes and
+// scales, four converter warps write the exact bf16 values into the stage for the MMA.
+enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_BMX = 3 };
+constexpr int GEMM_MAX_THREADS = 320;
 
 struct GemmArgs {
   int M;            // DENSE: rows of A; WGRAD: output rows per expert (the contiguous output dim)
@@ -112,17 +118,24 @@ struct GemmCfg {
   static constexpr int B_TILE = BN * BK * 2;
   static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
   static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
-  static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES;
+  static constexpr bool kBmx = (SPLIT == SPLIT_BMX);
+  // MXFP8 B: E4M3 bytes [BN][64] and scales [2][BN] after the converted bf16 B tile
+  static constexpr int BQ_BYTES = kBmx ? BN * BK : 0;
+  static constexpr int BS_BYTES = kBmx ? 1024 : 0;
+  static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES + BQ_BYTES + BS_BYTES;
+  // bytes TMA delivers into one stage
+  static constexpr int TX_BYTES = kBmx ? A_TILE + BQ_BYTES + 2 * BN : STAGE_BYTES;
+  static constexpr int THREADS = kBmx ? 320 : 192;
   // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: 2 buffers per
   // epilogue warp of up to 32 x 32 fp32.
   static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * 2 * 4096 : 0;
-  static constexpr int RING = SMEM_RING - STG_BYTES;
+  static constexpr int RING = (kBmx ? 3 * STAGE_BYTES : SMEM_RING) - STG_BYTES;
   static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
   static __host__ __device__ int n_tiles(const GemmArgs& a) {
-    return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + BN - 1) / BN;
+    return (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? a.I / 128 : (a.N + BN - 1) / BN;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
     return size_t(STAGES) * STAGE_BYTES + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
@@ -300,7 +313,7 @@ __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint
 }
 
 template <int MODE, int EPI, int SPLIT, int BN_>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmO, const GemmArgs args) {
@@ -313,7 +326,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* staging = smem + STAGES * STAGE_BYTES;  // WGRAD output staging (C::STG_BYTES)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STG_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  // bars + 2*STAGES+5: conv[STAGES] (MXFP8 B converted), used with SPLIT_BMX
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(staging + C::STG_BYTES + 256);
   int* s_toff = s_off + (args.E + 1);
@@ -325,6 +339,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+  auto conv_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + 5 + s]); };
 
   if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
     ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
@@ -344,6 +359,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
+    if (C::kBmx)
+      for (int s = 0; s < STAGES; ++s) mbar_init(conv_bar(s), 4);  // one arrival per converter warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -412,11 +429,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t sa2 = sa + A_TILE;                 // A lo (SPLIT_A)
           const uint32_t sb = sa + A_TILE * C::A_TILES;
           const uint32_t sb2 = sb + C::B_TILE;              // B lo (SPLIT_B)
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          mbar_arrive_expect_tx(fb, C::TX_BYTES);
           const int k0 = kb * BK;
           if (MODE == MODE_DENSE) {
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
             tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
+          } else if ((MODE == MODE_ROWS || MODE == MODE_RING) && C::kBmx) {
+            // MXFP8 weights: E4M3 bytes (tmB) and E8M0 scales (tmB2, [E][K/32][N]) of the B rows
+            const uint32_t sbq = sb + C::B_TILE;
+            const uint32_t sbs = sbq + C::BQ_BYTES;
+            tma_load_2d(sa, &tmA, fb, k0, a_row, pol_act);
+            if (EPI == EPI_SWIGLU_MX) {
+              tma_load_3d(sbq, &tmB, fb, k0, t.n * 128, t.e, pol_w);
+              tma_load_3d(sbq + C::BQ_BYTES / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
+              tma_load_3d(sbs, &tmB2, fb, t.n * 128, kb * 2, t.e, pol_w);
+              tma_load_3d(sbs + BN, &tmB2, fb, args.I + t.n * 128, kb * 2, t.e, pol_w);
+            } else {
+              tma_load_3d(sbq, &tmB, fb, k0, t.n * BN, t.e, pol_w);
+              tma_load_3d(sbs, &tmB2, fb, t.n * BN, kb * 2, t.e, pol_w);
+            }
           } else if (MODE == MODE_ROWS || MODE == MODE_RING) {
             tma_load_2d(sa, &tmA, fb, k0, a_row, pol_act);
             if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, a_row, pol_act);
@@ -490,7 +521,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0) f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (lane == 0)
+          f_ok = mbar_wait(C::kBmx ? conv_bar(stage) : full_bar(stage), phase, abort_flag, args.status,
+                           SITE_GEMM_MMA_FULL);
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
@@ -557,6 +590,57 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_wait(drain_bar, 0, &no_abort, args.status, SITE_GEMM_DRAIN);
       }
       __syncwarp();
+    }
+  } else if (C::kBmx && warp >= 6) {
+    // ------------------------------------------------------------------ MXFP8 B converters
+    // For every stage the producer fills: E4M3 bytes of B ([BN][64], row-major) and their E8M0
+    // scales -> exact bf16 values in the 128B-swizzled K-major layout the MMA reads.  Thread
+    // t of the 128 converts 16-byte chunks t, t+128, ... (chunk c = row c/4, elements
+    // 16*(c%4) .. +15, scale block (c%4)/2).
+    const int ct = threadIdx.x - 6 * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int g = cta0; g < total && ok; g += ncta) {
+      const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        int f_ok = 1;
+        if (lane == 0) f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st_base = smem + stage * STAGE_BYTES;
+        uint8_t* b16 = st_base + A_TILE;                    // converted bf16 B
+        const uint8_t* bq = b16 + C::B_TILE;               // E4M3 bytes
+        const uint8_t* bs = bq + C::BQ_BYTES;              // E8M0 scales
+#pragma unroll 2
+        for (int c = ct; c < BN * 4; c += 128) {
+          const int r = c >> 2;
+          const int q = c & 3;
+          const int kk = q >> 1;
+          const int sidx = (EPI == EPI_SWIGLU_MX) ? ((r >> 7) * 256 + kk * 128 + (r & 127)) : (kk * BN + r);
+          const float sc = exp2_int((int)bs[sidx] - 127);
+          const uint4 raw = *reinterpret_cast<const uint4*>(bq + r * 64 + q * 16);
+          const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
+          uint32_t o[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 f = f32x2_from_e4m3x2(pairs[j]);
+            o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+          }
+          uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
+          *reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(row_base + (((2 * q + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(conv_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -675,6 +759,41 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             store_u32x16(act_hi + col, phi);
             store_u32x16(act_lo + col, plo);
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_MX) {
+        // as EPI_SWIGLU, but a is quantised to MXFP8 in 32-column blocks (one block per chunk of
+        // this thread's row) and stored as the exact bf16 values of the MX grid.
+        float* hu = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+        __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t vh[32], vu[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, vh);
+          tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
+          tmem_wait_ld();
+          if (valid) {
+            const int col = t.n * 128 + c * 32;
+            float a[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float h = __uint_as_float(vh[j]), u = __uint_as_float(vu[j]);
+              a[j] = h / (1.0f + __expf(-h)) * u;
+            }
+            mx_quantize32(a, nullptr);
+            uint32_t pa[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pa[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+            float4* dh = reinterpret_cast<float4*>(hu + col);
+            float4* du = reinterpret_cast<float4*>(hu + args.I + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              dh[j] = make_float4(__uint_as_float(vh[4 * j]), __uint_as_float(vh[4 * j + 1]),
+                                  __uint_as_float(vh[4 * j + 2]), __uint_as_float(vh[4 * j + 3]));
+              du[j] = make_float4(__uint_as_float(vu[4 * j]), __uint_as_float(vu[4 * j + 1]),
+                                  __uint_as_float(vu[4 * j + 2]), __uint_as_float(vu[4 * j + 3]));
+            }
+            store_u32x16(act + col, pa);
           }
         }
       } else {  // EPI_SWIGLU_BWD

@@ -66,6 +66,16 @@ struct RingArgs {
 };
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, cudaStream_t st);
+// MXFP8 (mx.cu, gemm.cu)
+cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm, cudaStream_t st);
+cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
+                                  cudaStream_t st);
+cudaError_t launch_gemm1_swiglu_mx(const void* x_g, const void* w13_q, const void* w13_s, int R, int H, int I, int E,
+                                   const int32_t* offsets, const int32_t* tile_off, float* hu, void* act, int* status,
+                                   int n_sm, cudaStream_t st);
+cudaError_t launch_gemm2_mx(const void* act, const void* w2_q, const void* w2_s, int R, int H, int I, int E,
+                            const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
+                            cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

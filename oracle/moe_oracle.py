@@ -440,23 +440,29 @@ def _expert_ffn_quant(x_g, offsets, w13, w2, q):
 # ---------------------------------------------------------------------------
 
 def token_forward(x_t, w_router, router_bias, expert_weights, *, kind, k, renorm,
-                  route_scale=1.0, topk_idx=None):
+                  route_scale=1.0, topk_idx=None, quant=None):
     """Output of one token, computed on its own (for sampled checks at full size).
 
     ``expert_weights(e)`` returns (W13[e], W2[e]) as float64, so a caller can fetch
-    only the experts this token uses.  Returns (y_t, topk_idx_t, gates_t, o rows).
+    only the experts this token uses.  ``quant`` as in ``forward`` (each GEMM operand
+    quantised along that GEMM's reduction axis).  Returns (y_t, topk_idx_t, gates_t,
+    o rows, scores_t).
     """
     r = route(x_t[None, :], w_router, router_bias, kind, k, renorm, route_scale)
     idx = r["topk_idx"][0] if topk_idx is None else np.asarray(topk_idx, dtype=np.int32)
     g = gate_values(r["scores"], idx[None, :], renorm, route_scale)[0]
+    q = quant if quant is not None else (lambda v, axis: v)
+    xq = q(x_t[None, :], 1)[0]
     y = np.zeros_like(x_t)
     outs = []
     for j in range(k):
         w13_e, w2_e = expert_weights(int(idx[j]))
         I = w13_e.shape[0] // 2
-        h = w13_e[:I] @ x_t
-        u = w13_e[I:] @ x_t
-        o = w2_e @ (silu(h) * u)
+        w13_q = q(w13_e, 1)
+        h = w13_q[:I] @ xq
+        u = w13_q[I:] @ xq
+        a = q((silu(h) * u)[None, :], 1)[0]
+        o = q(w2_e, 1) @ a
         outs.append(o)
         y += g[j] * o
     return y, idx, g, outs, r["scores"][0]

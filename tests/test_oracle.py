@@ -398,3 +398,14 @@ def test_token_forward_matches_layer():
                                           kind=O.SIGMOID, k=3, renorm=True)
         assert np.array_equal(idx, fwd["topk_idx"][t])
         assert np.allclose(y, fwd["y"][t], rtol=1e-13, atol=1e-13)
+
+
+def test_token_forward_quantized_matches_layer():
+    rng = np.random.default_rng(14)
+    x, w_r, w13, w2 = _rand_layer(rng, 10, 64, 4, 64, scale=0.2)
+    q = O.mx_quantize_dequantize
+    fwd = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=2, renorm=True, quant=q)
+    for t in (0, 7):
+        y, *_ = O.token_forward(x[t], w_r, None, lambda e: (w13[e], w2[e]), kind=O.SIGMOID, k=2, renorm=True,
+                                quant=q)
+        assert np.allclose(y, fwd["y"][t], rtol=1e-12, atol=1e-14)
