@@ -316,6 +316,32 @@ def run_mok(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
 
+    # ---- MXFP8 forward (weights quantised once, outside the timed region)
+    mx = None
+    if not args.no_mxfp8:
+        wq = mok.quantize_weights(layer.desc, w13, w2)
+        mx_desc = mok.desc_from_shape(shp.scaled(mxfp8=True))
+        mx_layer = mok.MoELayer(mx_desc, device=dev)
+        for _ in range(2):
+            mok.moe_forward_mxfp8(mx_desc, x, wr, None, None, wq, y, mx_layer.ctx, mx_layer.ws)
+        barrier()
+        torch.cuda.synchronize()
+        N.trace_start(16 * args.steps + 16)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            mok.moe_forward_mxfp8(mx_desc, x, wr, None, None, wq, y, mx_layer.ctx, mx_layer.ws)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        mx_trace = N.trace_stop()
+        mx_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+        if mx_layer.status() != (0, 0):
+            raise RuntimeError("device status set in the MXFP8 forward")
+        mx = {"fwd_ms": round(mx_ms, 4), "tokens_per_s": round(T * world / (mx_ms * 1e-3), 1),
+              "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mx_trace.items()},
+              "weights": "E4M3 + E8M0 per 32 along K (11.3 GB), activations quantised in the gather and "
+                         "the SwiGLU epilogue"}
+        del mx_layer, wq
+
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
@@ -378,6 +404,7 @@ def run_mok(args, rank, world, local_rank):
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": step_bytes,
                 "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step"},
+        "mxfp8_fwd": mx,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -450,6 +477,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
