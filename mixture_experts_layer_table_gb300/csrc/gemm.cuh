@@ -620,14 +620,21 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
           const int q = c & 3;
           const int kk = q >> 1;
           const int sidx = (EPI == EPI_SWIGLU_MX) ? ((r >> 7) * 256 + kk * 128 + (r & 127)) : (kk * BN + r);
-          const float sc = exp2_int((int)bs[sidx] - 127);
+          const int X = (int)bs[sidx] - 127;
           const uint4 raw = *reinterpret_cast<const uint4*>(bq + r * 64 + q * 16);
-          const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t o[8];
+          bool fast = true;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float2 f = f32x2_from_e4m3x2(pairs[j]);
-            o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+          for (int j = 0; j < 4; ++j) fast &= e4m3x4_to_bf16x4_fast(wv[j], X, o[2 * j], o[2 * j + 1]);
+          if (!fast) {  // a zero or subnormal element, or an extreme scale
+            const float sc = exp2_int(X);
+            const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float2 f = f32x2_from_e4m3x2(pairs[j]);
+              o[j] = pack_bf16x2(f.x * sc, f.y * sc);
+            }
           }
           uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
           *reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);

@@ -38,6 +38,23 @@ __device__ __forceinline__ float2 f32x2_from_e4m3x2(uint16_t v) {
   return __half22float2(hh);
 }
 
+// Four E4M3 bytes w (byte i = element i) times 2^X -> four bf16 values as two bf16x2 words
+// (lo = elements 0, 1; hi = elements 2, 3), with integer operations only: the sign, 4 exponent
+// and 3 mantissa bits of each byte are moved to the bf16 positions and (120 + X) is added to
+// the exponent (E4M3 bias 7 -> bf16 bias 127).  Valid when no byte has a zero exponent field
+// (zero or subnormal) and -120 <= X <= 119; returns false otherwise (the caller converts the
+// slow way).
+__device__ __forceinline__ bool e4m3x4_to_bf16x4_fast(uint32_t w, int X, uint32_t& lo, uint32_t& hi) {
+  if (__vcmpeq4(w & 0x78787878u, 0u) != 0u || X < -120 || X > 119) return false;
+  const uint32_t bias = (uint32_t)(120 + X) << 7;
+  const uint32_t bias2 = bias | (bias << 16);
+  const uint32_t x01 = __byte_perm(w, 0u, 0x4140);  // [b0, 0, b1, 0]
+  const uint32_t x23 = __byte_perm(w, 0u, 0x4342);  // [b2, 0, b3, 0]
+  lo = (((x01 & 0x007f007fu) << 4) | ((x01 & 0x00800080u) << 8)) + bias2;
+  hi = (((x23 & 0x007f007fu) << 4) | ((x23 & 0x00800080u) << 8)) + bias2;
+  return true;
+}
+
 // Quantises 32 fp32 values in place to the MX grid (values become e4m3 * 2^X, exactly
 // representable in bf16) and returns X.  `q` receives the 32 E4M3 bytes when non-null.
 __device__ __forceinline__ int mx_quantize32(float (&v)[32], uint8_t* q) {
