@@ -61,9 +61,10 @@ enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, M
 // (E4M3 * 2^X is exact in bf16), the A operand of the MXFP8 GEMM2.
 enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5, EPI_SWIGLU_MX = 6 };
 // SPLIT_BMX: B is MXFP8 (E4M3 bytes + one E8M0 scale per 32 along K); TMA brings the bytes and
-// scales, four converter warps write the exact bf16 values into the stage for the MMA.
+// scales, eight converter warps write the exact bf16 values into the stage for the MMA.
 enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_BMX = 3 };
-constexpr int GEMM_MAX_THREADS = 320;
+constexpr int GEMM_MAX_THREADS = 448;
+constexpr int CONVERTER_WARPS = 8;  // SPLIT_BMX: warps 6 .. 13
 
 struct GemmArgs {
   int M;            // DENSE: rows of A; WGRAD: output rows per expert (the contiguous output dim)
@@ -125,7 +126,7 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES + BQ_BYTES + BS_BYTES;
   // bytes TMA delivers into one stage
   static constexpr int TX_BYTES = kBmx ? A_TILE + BQ_BYTES + 2 * BN : STAGE_BYTES;
-  static constexpr int THREADS = kBmx ? 320 : 192;
+  static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS : 192;
   // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: 2 buffers per
   // epilogue warp of up to 32 x 32 fp32.
   static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * 2 * 4096 : 0;
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     if (C::kBmx)
-      for (int s = 0; s < STAGES; ++s) mbar_init(conv_bar(s), 4);  // one arrival per converter warp
+      for (int s = 0; s < STAGES; ++s) mbar_init(conv_bar(s), CONVERTER_WARPS);  // one arrival per converter warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
     // ------------------------------------------------------------------ MXFP8 B converters
     // For every stage the producer fills: E4M3 bytes of B ([BN][64], row-major) and their E8M0
     // scales -> exact bf16 values in the 128B-swizzled K-major layout the MMA reads.  Thread
-    // t of the 128 converts 16-byte chunks t, t+128, ... (chunk c = row c/4, elements
+    // t of the 256 converts 16-byte chunks t, t+256, ... (chunk c = row c/4, elements
     // 16*(c%4) .. +15, scale block (c%4)/2).
     const int ct = threadIdx.x - 6 * 32;
     int stage = 0;
@@ -615,26 +616,24 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
         const uint8_t* bq = b16 + C::B_TILE;               // E4M3 bytes
         const uint8_t* bs = bq + C::BQ_BYTES;              // E8M0 scales
 #pragma unroll 2
-        for (int c = ct; c < BN * 4; c += 128) {
+        for (int c = ct; c < BN * 4; c += 32 * CONVERTER_WARPS) {
           const int r = c >> 2;
           const int q = c & 3;
           const int kk = q >> 1;
           const int sidx = (EPI == EPI_SWIGLU_MX) ? ((r >> 7) * 256 + kk * 128 + (r & 127)) : (kk * BN + r);
           const int X = (int)bs[sidx] - 127;
           const uint4 raw = *reinterpret_cast<const uint4*>(bq + r * 64 + q * 16);
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t o[8];
-          bool fast = true;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) fast &= e4m3x4_to_bf16x4_fast(wv[j], X, o[2 * j], o[2 * j + 1]);
-          if (!fast) {  // a zero or subnormal element, or an extreme scale
-            const float sc = exp2_int(X);
-            const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 f = f32x2_from_e4m3x2(pairs[j]);
-              o[j] = pack_bf16x2(f.x * sc, f.y * sc);
-            }
+          const uint32_t zero = e4m3_zero_exponent_bytes(raw.x) | e4m3_zero_exponent_bytes(raw.y) |
+                                e4m3_zero_exponent_bytes(raw.z) | e4m3_zero_exponent_bytes(raw.w);
+          if (zero == 0u && (unsigned)(X + 120) <= 239u) {
+            const uint32_t bias2 = (uint32_t)(120 + X) * 0x00800080u;  // (120 + X) << 7 in both halves
+            e4m3x4_to_bf16x4(raw.x, bias2, o[0], o[1]);
+            e4m3x4_to_bf16x4(raw.y, bias2, o[2], o[3]);
+            e4m3x4_to_bf16x4(raw.z, bias2, o[4], o[5]);
+            e4m3x4_to_bf16x4(raw.w, bias2, o[6], o[7]);
+          } else {
+            e4m3x16_to_bf16x16_slow(raw, X, o);
           }
           uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
           *reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
