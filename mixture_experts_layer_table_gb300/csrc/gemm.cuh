@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
           a_row = (t.mb % args.ring_slots) * args.mb_rows + t.row0;
         }
         for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY)) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
+                         kWaitLimitNs, 32)) {
             ok = false;
             break;
           }
@@ -606,7 +607,8 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0) f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (lane == 0)
+          f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL, kWaitLimitNs, 32);
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
@@ -670,7 +672,9 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
         continue;
       }
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL);
+      if (lane == 0)
+        w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL, kWaitLimitNs,
+                         256);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * C::ACC_COLS + (uint32_t(quarter * 32) << 16);

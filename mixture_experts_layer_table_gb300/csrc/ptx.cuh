@@ -56,13 +56,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // role of the CTA has already aborted.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// `sleep_ns` > 0 makes a waiting thread sleep between polls, so that warps idling in long
+// waits leave the issue slots of their SM sub-partition to warps that have work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int site, uint64_t limit_ns = kWaitLimitNs) {
+                                          int* status, int site, uint64_t limit_ns = kWaitLimitNs,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
     if ((++spins & 255u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
