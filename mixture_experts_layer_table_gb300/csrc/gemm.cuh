@@ -127,10 +127,10 @@ struct GemmCfg {
   // bytes TMA delivers into one stage
   static constexpr int TX_BYTES = kBmx ? A_TILE + BQ_BYTES + 2 * BN : STAGE_BYTES;
   static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS : 192;
-  // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: 2 buffers per
-  // epilogue warp of up to 32 x 32 fp32.
-  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * 2 * 4096 : 0;
-  static constexpr int RING = (kBmx ? 3 * STAGE_BYTES : SMEM_RING) - STG_BYTES;
+  // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: one buffer of up
+  // to 32 x 32 fp32 per block of a tile, per epilogue warp.
+  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * (BN / 32) * 4096 : 0;
+  static constexpr int RING = (kBmx || MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
   static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -314,7 +314,7 @@ __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint
 }
 
 template <int MODE, int EPI, int SPLIT, int BN_>
-__global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
+__global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmO, const GemmArgs args) {
@@ -656,7 +656,6 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
     const int r_local = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    int stg_buf = 0;  // WGRAD: staging buffer alternation
     for (int g = cta0; g < total; g += ncta) {
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       if (MODE == MODE_WGRAD && t.nkb == 0) {
@@ -706,33 +705,36 @@ __global__ void __launch_bounds__(GEMM_MAX_THREADS, 1)
           }
         }
       } else if (EPI == EPI_T_F32 || EPI == EPI_T_BF16) {
-        // out[e][n][m]: each 32 (m) x 32 (n) block of this warp is written to shared memory with
-        // m contiguous (lane = m: conflict-free) and stored by one TMA bulk tensor store.
-        uint8_t* stg = staging + (warp - 2) * 8192;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, v);
-          tmem_wait_ld();
-          uint8_t* buf = stg + (stg_buf & 1) * 4096;
-          if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
-          __syncwarp();
+        // out[e][n][m]: this warp's BN/32 blocks of 32 (m) x 32 (n).  All TMEM loads are issued
+        // before one wait; each block goes to its own shared-memory buffer (m contiguous, lane =
+        // m: conflict-free) and leaves through one TMA bulk tensor store.
+        constexpr int NC = BN / 32;
+        uint8_t* stg = staging + (warp - 2) * (NC * 4096);
+        uint32_t v[NC][32];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) tmem_ld_32x32b_x32(tacc + c * 32, v[c]);
+        tmem_wait_ld();
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores have read their buffers
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
           if (EPI == EPI_T_F32) {
-            float* sb = reinterpret_cast<float*>(buf);
+            float* sb = reinterpret_cast<float*>(stg + c * 4096);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __uint_as_float(v[j]);
+            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __uint_as_float(v[c][j]);
           } else {
-            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(buf);
+            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg + c * 4096);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[c][j]));
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmO, smem_u32(buf), t.m * BM + quarter * 32, t.n * BN + c * 32, t.e);
-            bulk_commit_group();
-          }
-          ++stg_buf;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            tma_store_3d(&tmO, smem_u32(stg + c * 4096), t.m * BM + quarter * 32, t.n * BN + c * 32, t.e);
+          bulk_commit_group();
         }
       } else if (EPI == EPI_SWIGLU) {
         // accumulator columns 0..127 are the gate projection h, 128..255 the up projection u,
