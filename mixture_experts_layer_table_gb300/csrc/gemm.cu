@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "wgrad.cuh"
 #include "kernels.cuh"
 
 namespace mok {
@@ -202,26 +203,31 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   tb2 = tb;
   if (a_lo && !tmap_2d(&ta2, a_lo, M, R, 64, BK)) return cudaErrorInvalidValue;
   if (b_lo && !tmap_2d(&tb2, b_lo, N, R, 64, BK)) return cudaErrorInvalidValue;
-  if (a_lo && b_lo) return cudaErrorInvalidValue;
+  // exactly one operand is a hi/lo pair: it is the stationary one
+  if ((a_lo != nullptr) == (b_lo != nullptr)) return cudaErrorInvalidValue;
+  (void)WBN;
   CUtensorMap to;
   if (!tmap_wgrad_out(&to, dw, M, N, E, out_f32 != 0)) return cudaErrorInvalidValue;
-  GemmArgs g = base_args(E, offsets, nullptr, status);
+  WgradArgs g;
   g.M = M;
   g.N = N;
-  g.out0 = dw;
-  const int tiles = E * (M / BM) * (N / WBN);
-  g.total_tiles = tiles;
-  const int grid = std::min(tiles, n_sm);
-  if (a_lo) {
-    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
-                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_A, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
-  }
-  if (b_lo) {
-    return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
-                   : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_B, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
-  }
-  return out_f32 ? launch<MODE_WGRAD, EPI_T_F32, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st, &to)
-                 : launch<MODE_WGRAD, EPI_T_BF16, SPLIT_NONE, WBN>(ta, ta2, tb, tb2, g, grid, st, &to);
+  g.E = E;
+  g.offsets = offsets;
+  g.out = dw;
+  g.status = status;
+  const int strips = E * (a_lo ? M / 128 : N / 128);
+  const int grid = std::min(strips, n_sm);
+  if (grid <= 0) return cudaSuccess;
+  const size_t smem = wgrad_smem_bytes(E);
+  auto run = [&](auto kern) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_smem_bytes(1024));
+    if (err != cudaSuccess) return err;
+    kern<<<grid, WG_THREADS, smem, st>>>(ta, ta2, tb, tb2, to, g);
+    return cudaGetLastError();
+  };
+  static_assert(wgrad_smem_bytes(1024) <= 232448, "shared memory budget");
+  if (a_lo) return out_f32 ? run(wgrad_kernel<true, true>) : run(wgrad_kernel<true, false>);
+  return out_f32 ? run(wgrad_kernel<false, true>) : run(wgrad_kernel<false, false>);
 }
 
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
