@@ -36,10 +36,13 @@ REF_SAMPLE = {"T": 256, "E": 16}        # --impl reference: per step
 
 def _workloads():
     from mixture_experts_layer_table_gb300 import workloads as W
-    return {"dsv3": W.DSV3, "dsv3_e16_t256": W.DSV3.scaled(name="dsv3_e16_t256", T=256, E=16)}
+    return {"dsv3": W.DSV3, "dsv3_e16_t256": W.DSV3.scaled(name="dsv3_e16_t256", T=256, E=16),
+            "dsv3_e16_t1024": W.DSV3.scaled(name="dsv3_e16_t1024", T=1024, E=16)}
 
 
 WORKLOADS = _workloads()
+# forward expert GEMMs: library choice, CTA pairs (256-row tiles) or single CTAs (128-row tiles)
+GEMM_FLAGS = {"auto": 0, "pair": 2, "single": 4}
 
 
 def load_peaks():
@@ -222,7 +225,7 @@ def run_mok(args, rank, world, local_rank):
     shp = WORKLOADS[args.workload]
     T, H, I, E, k = shp.T, shp.H, shp.I, shp.E, shp.k
     inp = W.make_inputs(shp, seed=1000 * rank, device=str(dev))
-    layer = mok.MoELayer(mok.desc_from_shape(shp), device=dev)
+    layer = mok.MoELayer(mok.desc_from_shape(shp, flags=GEMM_FLAGS[args.gemm]), device=dev)
     grads = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
              "dw_router": torch.empty((E, H), dtype=torch.float32, device=dev),
              "dw13": torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev),
@@ -388,6 +391,7 @@ def run_mok(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
         "config": {"workload": shp.name, "T": T, "hidden": H, "experts": E, "intermediate": I, "top_k": k,
+                   "forward_gemm": args.gemm,
                    "router": "sigmoid+renorm", "passes": "fwd+bwd",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass)",
@@ -443,10 +447,40 @@ def run_ring_sweep(args):
             raise RuntimeError("device status set")
         return e0.elapsed_time(e1) / args.steps
 
-    plain = mok.MoELayer(mok.desc_from_shape(shp))
+    plain = mok.MoELayer(mok.desc_from_shape(shp, flags=GEMM_FLAGS[args.gemm]))
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
     plain_ms = time_forward(plain)
     y_plain = y.clone()
+    # Per-kernel times of the plain forward (CUDA events around each launch, one more pass of
+    # K forwards) and the tensor-core fraction of its grouped GEMMs.
+    from mixture_experts_layer_table_gb300 import _native as N
+    N.trace_start(16 * args.steps + 16)
+    for _ in range(args.steps):
+        plain.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
+    torch.cuda.synchronize()
+    trace = N.trace_stop()
+    clocks = sampler.stop()
     del plain
+    peaks, peak_kind = load_peaks()
+    kf = kernel_flops(shp)
+    kernels = {}
+    for name, t in trace.items():
+        avg = t["total_ms"] / t["launches"]
+        kernels[name] = {"avg_ms": round(avg, 4)}
+        if name in kf:
+            kernels[name]["TFLOPs"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+            kernels[name]["frac_bf16_peak"] = round(kf[name] / (avg * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
+    fwd_gemm = [n for n in ("gemm1_swiglu", "gemm2") if n in trace]
+    g_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in fwd_gemm)
+    g_tf = sum(kf[n] for n in fwd_gemm) / (g_ms * 1e-3) / 1e12
+    # the GEMMs run inside back-to-back 13 ms forwards: both the burst and the sustained
+    # (power-capped) measured peaks are given, with the SM clocks seen meanwhile
+    grouped = {"kernels": fwd_gemm, "ms": round(g_ms, 4), "tflops": round(g_tf, 1),
+               "frac_bf16_peak": round(g_tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
+               "peak_source": peak_kind + " (burst)",
+               "frac_bf16_peak_sustained": round(g_tf / peaks["bf16_tflops_sustained"], 4),
+               "peak_sustained": peaks["bf16_tflops_sustained"], "clocks": clocks}
     sweep = {}
     for m in W.RING_MINIBATCHES:
         layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES))
@@ -461,8 +495,10 @@ def run_ring_sweep(args):
             "ms_per_step": best["fwd_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
             "config": {"workload": shp.name, "ring_bytes": W.RING_BYTES, "comm_sms": 8, "passes": "fwd",
+                       "forward_gemm": args.gemm,
                        "min_minibatch_two_waves": mok.min_minibatch(0, shp.I)},
-            "plain_forward_ms": round(plain_ms, 4), "sweep": sweep}
+            "plain_forward_ms": round(plain_ms, 4), "plain_forward_kernels": kernels,
+            "grouped_gemm_fwd": grouped, "sweep": sweep}
     print(json.dumps(line), flush=True)
 
 
@@ -480,9 +516,12 @@ def main():
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
+    ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",
+                    help="forward expert GEMMs on CTA pairs or single CTAs (default: the library's choice)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
-                    help="dsv3: the benchmarked layer; dsv3_e16_t256: the same per-expert shape on "
-                         "16 experts and 256 tokens (a few GB, for profiler captures)")
+                    help="dsv3: the benchmarked layer; dsv3_e16_t256 / dsv3_e16_t1024: the same "
+                         "layer on 16 experts and 256 / 1024 tokens (128 / 512 rows per expert, a few "
+                         "GB, for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -75,10 +75,17 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *   minibatch    ring forward: rows per minibatch, consecutive rows of the expert-sorted
  *                order (0 = mok_min_minibatch(0, I), two full SM waves of GEMM1 tiles)
  *   flags        MOK_FLAG_WGRAD_BF16: the expert weight gradients dw13 / dw2 of
- *                mok_moe_backward are bf16 instead of the default f32
+ *                mok_moe_backward are bf16 instead of the default f32.
+ *                MOK_FLAG_GEMM_PAIR: run the forward expert GEMMs on CTA pairs
+ *                (tcgen05 cta_group::2, two SMs per 256-row tile) instead of single CTAs
+ *                (128-row tiles, the default; MOK_FLAG_GEMM_SINGLE asks for it
+ *                explicitly).  Results are bitwise the same either way.  Setting both
+ *                is an invalid argument.
  *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1
+#define MOK_FLAG_GEMM_PAIR 2
+#define MOK_FLAG_GEMM_SINGLE 4
 typedef struct {
   int32_t T, H, I, E, k;
   int32_t router;

@@ -39,6 +39,8 @@ LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "
                  "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
+FLAG_GEMM_PAIR = 2     # forward expert GEMMs on CTA pairs (256-row tiles)
+FLAG_GEMM_SINGLE = 4   # forward expert GEMMs on single CTAs (128-row tiles)
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
 

@@ -40,6 +40,7 @@ mok_status check_desc(const mok_layer_desc* d) {
   if (d->precision != MOK_BF16 && d->precision != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
   if (!std::isfinite(d->route_scale)) return MOK_ERR_INVALID_ARG;
   if (d->minibatch < 0 || d->ring_bytes < 0) return MOK_ERR_INVALID_ARG;
+  if ((d->flags & MOK_FLAG_GEMM_PAIR) && (d->flags & MOK_FLAG_GEMM_SINGLE)) return MOK_ERR_INVALID_ARG;
   if (d->H % 256 != 0 || d->I % 256 != 0) return MOK_ERR_UNSUPPORTED;
   if (d->E > 1024 || d->k > 16) return MOK_ERR_UNSUPPORTED;
   const int64_t R = int64_t(d->T) * d->k;
@@ -47,6 +48,11 @@ mok_status check_desc(const mok_layer_desc* d) {
   if (R * width >= (int64_t(1) << 31)) return MOK_ERR_UNSUPPORTED;
   return MOK_OK;
 }
+
+// Forward expert GEMMs on CTA pairs (256-row tiles) only on request: measured on GB300 at 128
+// and at 512 rows per expert, the single-CTA GEMMs (128-row tiles) are as fast or faster, since
+// a 256-row tile pads each expert's ragged tail twice as much.
+bool gemm_pairs(const mok_layer_desc* d) { return (d->flags & MOK_FLAG_GEMM_PAIR) != 0; }
 
 // Two full waves of 128 x 256 GEMM1 output tiles over n_sm SMs, in rows: GEMM1 has 2I columns.
 int32_t min_minibatch_rows(int n_sm, int I) {
@@ -283,7 +289,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
     // 5. grouped GEMM1 with the SwiGLU epilogue
     MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
-                                                            status, n_sm, st));
+                                                            status, n_sm, gemm_pairs(d), st));
   } else {
     // 4-5. ring forward: per-minibatch tables, then one persistent launch in which `comm`
     //      CTAs gather minibatches into the ring while the others run GEMM1 on them
@@ -317,7 +323,8 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     MOK_LAUNCH("ring_gemm1_swiglu", st, mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, st));
   }
   // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
-  MOK_LAUNCH("gemm2", st, mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, st));
+  MOK_LAUNCH("gemm2", st,
+             mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, gemm_pairs(d), st));
   // 7. weighted merge in fixed order
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;

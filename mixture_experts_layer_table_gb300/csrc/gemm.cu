@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "wgrad.cuh"
 #include "kernels.cuh"
 
@@ -59,6 +60,18 @@ bool tmap_wgrad_out(CUtensorMap* m, void* base, uint64_t M, uint64_t N, uint64_t
                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Store map of a row-major output [rows][cols]: 32 x 32 boxes, fp32 with 128B swizzle (128-byte
+// box rows) or bf16 with 64B swizzle (64-byte box rows), as the epilogue stages them.
+bool tmap_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool f32) {
+  const uint64_t es = f32 ? 4 : 2;
+  const uint64_t dims[2] = {cols, rows};
+  const uint64_t strides[1] = {cols * es};
+  const uint32_t box[2] = {32, 32};
+  return make_tmap(m, base, 2, dims, strides, box,
+                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
              uint32_t box_outer) {
   const uint64_t dims[2] = {inner, outer};
@@ -74,16 +87,21 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
   return make_tmap(m, base, 3, dims, strides, box);
 }
 
+// out_map / out1 / out2: store maps of the outputs for epilogues that use TMA stores.
 template <int MODE, int EPI, int SPLIT, int BN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& b2,
-                   const GemmArgs& args, int grid, cudaStream_t st, const CUtensorMap* out_map = nullptr) {
+                   const GemmArgs& args, int grid, cudaStream_t st, const CUtensorMap* out_map = nullptr,
+                   const CUtensorMap* out1 = nullptr, const CUtensorMap* out2 = nullptr) {
   using C = GemmCfg<MODE, EPI, SPLIT, BN>;
   static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
   if (grid <= 0) return cudaSuccess;
   auto kern = gemm_kernel<MODE, EPI, SPLIT, BN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
-  kern<<<grid, C::THREADS, C::smem_bytes(args.E), st>>>(a, a2, b, b2, out_map ? *out_map : a, args);
+  if (C::kTmaEpi && out_map == nullptr) return cudaErrorInvalidValue;
+  if (EPI == EPI_SWIGLU && C::kTmaEpi && (out1 == nullptr || out2 == nullptr)) return cudaErrorInvalidValue;
+  kern<<<grid, C::THREADS, C::smem_bytes(args.E), st>>>(a, a2, b, b2, out_map ? *out_map : a, out1 ? *out1 : a,
+                                                        out2 ? *out2 : a, args);
   return cudaGetLastError();
 }
 
@@ -99,6 +117,49 @@ GemmArgs base_args(int E, const int32_t* offsets, const int32_t* tile_off, int* 
 
 // Upper bound of the 128-row tiles of R expert-sorted rows split into E segments.
 int row_tiles_bound(int R, int E) { return (R + BM - 1) / BM + E; }
+
+// CTA-pair GEMM: clusters of 2 CTAs, one pair per two SMs (as many as can be co-resident).
+template <int EPI, int SPLIT>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& o0,
+                        const CUtensorMap& o1, const CUtensorMap& o2, const GemmArgs& args, int pair_tiles_bound,
+                        int n_sm, cudaStream_t st) {
+  using C = PairCfg<EPI, SPLIT>;
+  static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
+  if (pair_tiles_bound <= 0) return cudaSuccess;
+  auto kern = gemm_pair_kernel<EPI, SPLIT>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::smem_bytes(args.E);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // co-resident pairs of this kernel on this device (cached per device)
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    cfg.gridDim = dim3(2 * std::max(1, n_sm / 2), 1, 1);
+    int clusters = 0;
+    if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
+    max_pairs[dev] = std::max(1, clusters);
+  }
+  const int pairs = std::min(pair_tiles_bound, max_pairs[dev]);
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, a, a2, b, o0, o1, o2, args);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+// Upper bound of the 256-row pair tiles of R expert-sorted rows split into E segments.
+int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
 
 }  // namespace
 
@@ -119,7 +180,7 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
 
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, cudaStream_t st) {
+                                void* act_lo, int* status, int n_sm, bool pair, cudaStream_t st) {
   CUtensorMap ta, tb;
   if (!tmap_2d(&ta, x_g, H, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, BK, 128)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
@@ -131,24 +192,38 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
   g.out1 = act_hi;
   g.out2 = act_lo;
   g.ld1 = I;
+  // TMA store maps of the outputs: h | u fp32 [R][2I] (SW128), a hi / lo bf16 [R][I] (SW64)
+  CUtensorMap thu, tah, tal;
+  if (!tmap_out(&thu, hu, 2ULL * I, R, true) || !tmap_out(&tah, act_hi, I, R, false) ||
+      !tmap_out(&tal, act_lo, I, R, false))
+    return cudaErrorInvalidValue;
+  if (pair)
+    return launch_pair<EPI_SWIGLU, SPLIT_NONE>(ta, ta, tb, thu, tah, tal, g, pair_tiles_bound(R, E) * (I / 128), n_sm,
+                                               st);
   const int bound = row_tiles_bound(R, E) * (I / 128);
-  return launch<MODE_ROWS, EPI_SWIGLU, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st);
+  return launch<MODE_ROWS, EPI_SWIGLU, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st, &thu, &tah,
+                                                        &tal);
 }
 
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         cudaStream_t st) {
+                         bool pair, cudaStream_t st) {
   CUtensorMap ta, ta2, tb;
   if (!tmap_2d(&ta, act_hi, I, R, BK, BM) || !tmap_2d(&ta2, act_lo, I, R, BK, BM) ||
-      !tmap_3d(&tb, w2, I, H, E, BK, 256))
+      !tmap_3d(&tb, w2, I, H, E, BK, pair ? 128 : 256))
     return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
   g.N = H;
   g.K = I;
   g.out0 = out;
   g.ld0 = H;
+  CUtensorMap to;
+  if (!tmap_out(&to, out, H, R, true)) return cudaErrorInvalidValue;
+  if (pair)
+    return launch_pair<EPI_F32, SPLIT_A>(ta, ta2, tb, to, to, to, g, pair_tiles_bound(R, E) * ((H + 255) / 256), n_sm,
+                                         st);
   const int bound = row_tiles_bound(R, E) * (H / 256);
-  return launch<MODE_ROWS, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st);
+  return launch<MODE_ROWS, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st, &to);
 }
 
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
@@ -190,7 +265,9 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
   g.out0 = dx_g;
   g.ld0 = H;
   const int bound = row_tiles_bound(R, E) * (H / 256);
-  return launch<MODE_DGRAD, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st);
+  CUtensorMap to;
+  if (!tmap_out(&to, dx_g, H, R, true)) return cudaErrorInvalidValue;
+  return launch<MODE_DGRAD, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st, &to);
 }
 
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
@@ -266,7 +343,8 @@ cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, vo
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
   // gathering and GEMM CTAs wait on each other: all of them must be resident at once
-  void* params[] = {(void*)&ta, (void*)&ta, (void*)&tb, (void*)&tb, (void*)&ta, (void*)&g};
+  // one pointer per kernel parameter: tmA, tmA2, tmB, tmB2, tmO, tmO1, tmO2, args
+  void* params[] = {(void*)&ta, (void*)&ta, (void*)&tb, (void*)&tb, (void*)&ta, (void*)&ta, (void*)&ta, (void*)&g};
   return cudaLaunchCooperativeKernel((const void*)kern, dim3(n_sm), dim3(C::THREADS), params,
                                      C::smem_bytes(ra.E), st);
 }
@@ -319,8 +397,10 @@ cudaError_t launch_gemm2_mx(const void* act, const void* w2_q, const void* w2_s,
   g.K = I;
   g.out0 = out;
   g.ld0 = H;
+  CUtensorMap to;
+  if (!tmap_out(&to, out, H, R, true)) return cudaErrorInvalidValue;
   const int bound = row_tiles_bound(R, E) * (H / 256);
-  return launch<MODE_ROWS, EPI_F32, SPLIT_BMX, 256>(ta, ta, tq, ts, g, std::min(bound, n_sm), st);
+  return launch<MODE_ROWS, EPI_F32, SPLIT_BMX, 256>(ta, ta, tq, ts, g, std::min(bound, n_sm), st, &to);
 }
 
 // ----------------------------------------------------------------------------- wait test

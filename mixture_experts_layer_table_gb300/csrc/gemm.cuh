@@ -129,7 +129,10 @@ struct GemmCfg {
   static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS : 192;
   // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: one buffer of up
   // to 32 x 32 fp32 per block of a tile, per epilogue warp.
-  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * (BN / 32) * 4096 : 0;
+  // ROWS / DGRAD fp32 and SwiGLU outputs leave through TMA stores from one 4 KB buffer per
+  // epilogue warp
+  static constexpr bool kTmaEpi = (MODE == MODE_ROWS || MODE == MODE_DGRAD) && (EPI == EPI_F32 || EPI == EPI_SWIGLU);
+  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * (BN / 32) * 4096 : kTmaEpi ? 4 * 4096 : 0;
   static constexpr int RING = (kBmx || MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
   static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
   static constexpr int ACC_COLS = BN;
@@ -259,6 +262,190 @@ __device__ __forceinline__ bool wait_counter(const int* p, int target, int* stat
   }
 }
 
+// Epilogue of one accumulator row (this thread's TMEM lane) of a 128 x BN tile: fp32 output
+// row, columns n*BN .. n*BN+BN-1 (clipped at args.N).
+template <int BN>
+__device__ __forceinline__ void epi_f32_row(uint32_t tacc, bool valid, long long row, int n, const GemmArgs& args) {
+  float* out = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    tmem_wait_ld();
+    const int col0 = n * BN + c * 32;
+    if (valid) {
+      if (col0 + 32 <= args.N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(out + col0 + j) = make_float4(
+              __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + j < args.N) out[col0 + j] = __uint_as_float(v[j]);
+      }
+    }
+  }
+}
+
+// SwiGLU epilogue of one accumulator row: columns 0..127 are the gate projection h, 128..255
+// the up projection u, for intermediate indices n*128 .. n*128+127.  Stores h | u in fp32 and
+// a = silu(h) u as a bf16 hi / lo pair.
+__device__ __forceinline__ void epi_swiglu_row(uint32_t tacc, bool valid, long long row, int n,
+                                               const GemmArgs& args) {
+  float* hu = reinterpret_cast<float*>(args.out0) + row * args.ld0;
+  __nv_bfloat16* act_hi = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
+  __nv_bfloat16* act_lo = reinterpret_cast<__nv_bfloat16*>(args.out2) + row * args.ld1;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t vh[32], vu[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, vh);
+    tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
+    tmem_wait_ld();
+    if (valid) {
+      const int col = n * 128 + c * 32;
+      uint32_t phi[16], plo[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float h0 = __uint_as_float(vh[2 * j]), h1 = __uint_as_float(vh[2 * j + 1]);
+        const float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
+        const float a0 = h0 / (1.0f + __expf(-h0)) * u0;
+        const float a1 = h1 / (1.0f + __expf(-h1)) * u1;
+        split_bf16x2(a0, a1, phi[j], plo[j]);
+      }
+      float4* dh = reinterpret_cast<float4*>(hu + col);
+      float4* du = reinterpret_cast<float4*>(hu + args.I + col);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        dh[j] = make_float4(__uint_as_float(vh[4 * j]), __uint_as_float(vh[4 * j + 1]), __uint_as_float(vh[4 * j + 2]),
+                            __uint_as_float(vh[4 * j + 3]));
+        du[j] = make_float4(__uint_as_float(vu[4 * j]), __uint_as_float(vu[4 * j + 1]), __uint_as_float(vu[4 * j + 2]),
+                            __uint_as_float(vu[4 * j + 3]));
+      }
+      store_u32x16(act_hi + col, phi);
+      store_u32x16(act_lo + col, plo);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- epilogues through TMA stores
+// A warp owns 32 accumulator rows (its TMEM lane quarter).  When all 32 rows are valid, a
+// 32 x 32 block leaves through shared memory and one TMA tile store (full lines, no per-thread
+// scattered stores competing with the operand traffic of the main loop); a warp whose rows
+// cross the end of the expert's segment stores its valid rows directly, so that no row of
+// another expert is touched.
+
+// fp32 block (thread = row r, v = its 32 columns) into a 128B-swizzled 32 x 128 B buffer
+// (1024-byte aligned): 16-byte chunk c of row r sits at r*128 + ((c ^ (r % 8)) * 16).
+__device__ __forceinline__ void stage_f32_sw128(uint8_t* stg, const uint32_t (&v)[32], int lane) {
+  uint8_t* row = stg + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// bf16 block (thread = row r, p = its 16 packed pairs) into a 64B-swizzled 32 x 64 B buffer
+// (512-byte aligned): 16-byte chunk c of row r sits at r*64 + ((c ^ ((r / 2) % 4)) * 16).
+__device__ __forceinline__ void stage_bf16_sw64(uint8_t* stg, const uint32_t (&p)[16], int lane) {
+  uint8_t* row = stg + lane * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ ((lane >> 1) & 3)) << 4)) = make_uint4(p[4 * c], p[4 * c + 1], p[4 * c + 2], p[4 * c + 3]);
+}
+
+// fp32 output rows through TMA stores.  `stg`: this warp's 4 KB buffer; `row0`: first row of
+// the warp's 32; `nvalid`: how many of them are valid; tmO: [rows][N] fp32, box 32 x 32, SW128.
+template <int BN>
+__device__ __forceinline__ void epi_f32_tma(uint32_t tacc, long long row0, int nvalid, int n, const GemmArgs& args,
+                                            const CUtensorMap* tmO, uint8_t* stg, int lane) {
+  if (nvalid < 32) {
+    epi_f32_row<BN>(tacc, lane < nvalid, row0 + lane, n, args);
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    tmem_wait_ld();
+    const int col0 = n * BN + c * 32;
+    if (col0 >= args.N) continue;
+    if (lane == 0) bulk_wait_group_read<0>();  // the previous block has left the buffer
+    __syncwarp();
+    stage_f32_sw128(stg, v, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmO, smem_u32(stg), col0, (int)row0);
+      bulk_commit_group();
+    }
+  }
+}
+
+// SwiGLU epilogue through TMA stores: h | u fp32 (tmHU: [rows][2I], box 32 x 32, SW128) and
+// a as hi / lo bf16 (tmAh, tmAl: [rows][I], box 32 x 32, SW64).  `stg`: this warp's buffer,
+// 1024-byte aligned: 12 KB (h 4 KB, u 4 KB, a hi 2 KB, a lo 2 KB, all four in flight) when
+// SEPARATE, else 4 KB that the four blocks pass through one after another.
+template <bool SEPARATE>
+__device__ __forceinline__ void epi_swiglu_tma(uint32_t tacc, long long row0, int nvalid, int n, const GemmArgs& args,
+                                               const CUtensorMap* tmHU, const CUtensorMap* tmAh,
+                                               const CUtensorMap* tmAl, uint8_t* stg, int lane) {
+  if (nvalid < 32) {
+    epi_swiglu_row(tacc, lane < nvalid, row0 + lane, n, args);
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t vh[32], vu[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, vh);
+    tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
+    tmem_wait_ld();
+    uint32_t phi[16], plo[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float h0 = __uint_as_float(vh[2 * j]), h1 = __uint_as_float(vh[2 * j + 1]);
+      const float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
+      const float a0 = h0 / (1.0f + __expf(-h0)) * u0;
+      const float a1 = h1 / (1.0f + __expf(-h1)) * u1;
+      split_bf16x2(a0, a1, phi[j], plo[j]);
+    }
+    const int col = n * 128 + c * 32;
+    if (SEPARATE) {
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+      stage_f32_sw128(stg, vh, lane);
+      stage_f32_sw128(stg + 4096, vu, lane);
+      stage_bf16_sw64(stg + 8192, phi, lane);
+      stage_bf16_sw64(stg + 10240, plo, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmHU, smem_u32(stg), col, (int)row0);
+        tma_store_2d(tmHU, smem_u32(stg + 4096), args.I + col, (int)row0);
+        tma_store_2d(tmAh, smem_u32(stg + 8192), col, (int)row0);
+        tma_store_2d(tmAl, smem_u32(stg + 10240), col, (int)row0);
+        bulk_commit_group();
+      }
+    } else {
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        if (piece == 0) stage_f32_sw128(stg, vh, lane);
+        else if (piece == 1) stage_f32_sw128(stg, vu, lane);
+        else stage_bf16_sw64(stg, piece == 2 ? phi : plo, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (piece == 0) tma_store_2d(tmHU, smem_u32(stg), col, (int)row0);
+          else if (piece == 1) tma_store_2d(tmHU, smem_u32(stg), args.I + col, (int)row0);
+          else tma_store_2d(piece == 2 ? tmAh : tmAl, smem_u32(stg), col, (int)row0);
+          bulk_commit_group();
+        }
+      }
+    }
+  }
+}
+
 // Gathering role of the ring forward (the pull dispatch): one thread of each of the first
 // comm_ctas CTAs moves its share of each minibatch's rows (row i of the minibatch goes to CTA
 // i % comm_ctas) from the token matrix into the minibatch's ring slot with bulk async copies
@@ -317,7 +504,8 @@ template <int MODE, int EPI, int SPLIT, int BN_>
 __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
-                const __grid_constant__ CUtensorMap tmO, const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO1,
+                const __grid_constant__ CUtensorMap tmO2, const GemmArgs args) {
   using C = GemmCfg<MODE, EPI, SPLIT, BN_>;
   constexpr int BN = C::BN;
   constexpr int STAGES = C::STAGES;
@@ -682,28 +870,15 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
                             : (MODE == MODE_RING) ? (long long)t.mb * args.mb_rows + t.row0 + r_local
                                                   : (long long)(t.row0 + r_local);
 
-      if (EPI == EPI_F32) {
-        float* out = reinterpret_cast<float*>(args.out0) + row * args.ld0;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, v);
-          tmem_wait_ld();
-          const int col0 = t.n * BN + c * 32;
-          if (valid) {
-            if (col0 + 32 <= args.N) {
-#pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(out + col0 + j) =
-                    make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                                __uint_as_float(v[j + 3]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + j < args.N) out[col0 + j] = __uint_as_float(v[j]);
-            }
-          }
-        }
+      const int nvalid = max(0, min(32, t.rows - quarter * 32));  // valid rows of this warp (ROWS / DGRAD)
+      if (EPI == EPI_F32 && C::kTmaEpi) {
+        epi_f32_tma<BN>(tacc, (long long)t.row0 + quarter * 32, nvalid, t.n, args, &tmO,
+                        staging + (warp - 2) * 4096, lane);
+      } else if (EPI == EPI_F32) {
+        epi_f32_row<BN>(tacc, valid, row, t.n, args);
+      } else if (EPI == EPI_SWIGLU && C::kTmaEpi) {
+        epi_swiglu_tma<false>(tacc, (long long)t.row0 + quarter * 32, nvalid, t.n, args, &tmO, &tmO1, &tmO2,
+                              staging + (warp - 2) * 4096, lane);
       } else if (EPI == EPI_T_F32 || EPI == EPI_T_BF16) {
         // out[e][n][m]: this warp's BN/32 blocks of 32 (m) x 32 (n).  All TMEM loads are issued
         // before one wait; each block goes to its own shared-memory buffer (m contiguous, lane =
@@ -737,42 +912,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
           bulk_commit_group();
         }
       } else if (EPI == EPI_SWIGLU) {
-        // accumulator columns 0..127 are the gate projection h, 128..255 the up projection u,
-        // for intermediate indices n*128 .. n*128+127.  Stores h | u in fp32, a = silu(h) u as
-        // a bf16 hi / lo pair.
-        float* hu = reinterpret_cast<float*>(args.out0) + row * args.ld0;
-        __nv_bfloat16* act_hi = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
-        __nv_bfloat16* act_lo = reinterpret_cast<__nv_bfloat16*>(args.out2) + row * args.ld1;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t vh[32], vu[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, vh);
-          tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
-          tmem_wait_ld();
-          if (valid) {
-            const int col = t.n * 128 + c * 32;
-            uint32_t phi[16], plo[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h0 = __uint_as_float(vh[2 * j]), h1 = __uint_as_float(vh[2 * j + 1]);
-              const float u0 = __uint_as_float(vu[2 * j]), u1 = __uint_as_float(vu[2 * j + 1]);
-              const float a0 = h0 / (1.0f + __expf(-h0)) * u0;
-              const float a1 = h1 / (1.0f + __expf(-h1)) * u1;
-              split_bf16x2(a0, a1, phi[j], plo[j]);
-            }
-            float4* dh = reinterpret_cast<float4*>(hu + col);
-            float4* du = reinterpret_cast<float4*>(hu + args.I + col);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              dh[j] = make_float4(__uint_as_float(vh[4 * j]), __uint_as_float(vh[4 * j + 1]),
-                                  __uint_as_float(vh[4 * j + 2]), __uint_as_float(vh[4 * j + 3]));
-              du[j] = make_float4(__uint_as_float(vu[4 * j]), __uint_as_float(vu[4 * j + 1]),
-                                  __uint_as_float(vu[4 * j + 2]), __uint_as_float(vu[4 * j + 3]));
-            }
-            store_u32x16(act_hi + col, phi);
-            store_u32x16(act_lo + col, plo);
-          }
-        }
+        epi_swiglu_row(tacc, valid, row, t.n, args);
       } else if (EPI == EPI_SWIGLU_MX) {
         // as EPI_SWIGLU, but a is quantised to MXFP8 in 32-column blocks (one block per chunk of
         // this thread's row) and stored as the exact bf16 values of the MX grid.
@@ -894,7 +1034,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
       if (acc == 0) acc_phase ^= 1;
     }
     // TMA stores of this warp must finish reading shared memory (and land) before exit
-    if (MODE == MODE_WGRAD && lane == 0) bulk_wait_group_all();
+    if ((MODE == MODE_WGRAD || C::kTmaEpi) && lane == 0) bulk_wait_group_all();
     __syncwarp();
   }
 

@@ -32,12 +32,14 @@ cudaError_t launch_combine(const float* rows, const float* w, const int32_t* row
 // gemm.cu
 cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
                                int* status, int n_sm, cudaStream_t st);
+// `pair`: run the GEMM on CTA pairs (tcgen05 cta_group::2, 256-row tiles) instead of single CTAs
+// (128-row tiles); same results bit for bit.
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, cudaStream_t st);
+                                void* act_lo, int* status, int n_sm, bool pair, cudaStream_t st);
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         cudaStream_t st);
+                         bool pair, cudaStream_t st);
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, const float* hu,
                                 const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,

@@ -49,7 +49,8 @@ def test_layout_sizes_and_alignment(lib):
 
 
 @pytest.mark.parametrize("field,value,code", [("H", 300, 2), ("I", 100, 2), ("k", 9, 1), ("E", 2000, 2),
-                                              ("T", 0, 1), ("router", 3, 1), ("k", 17, 1)])
+                                              ("T", 0, 1), ("router", 3, 1), ("k", 17, 1),
+                                              ("flags", N.FLAG_GEMM_PAIR | N.FLAG_GEMM_SINGLE, 1)])
 def test_desc_validation(lib, field, value, code):
     d = mok.desc_from_shape(W.TINY)
     setattr(d, field, value)

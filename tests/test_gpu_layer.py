@@ -194,6 +194,48 @@ def test_bitwise_deterministic():
         assert torch.equal(a, b)
 
 
+# ----------------------------------------------------------------------------- CTA-pair GEMMs
+
+# long expert segments (~750 rows: several 256-row pair tiles and a ragged one per expert)
+LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=768, k=4,
+                  router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
+PAIR_CASES = [(LONG, None), (MID, None), (MID, "skewed_given"), (TINY, None), (ONE, None)]
+
+
+@pytest.mark.parametrize("shape,mode", PAIR_CASES, ids=lambda c: getattr(c, "name", str(c)))
+def test_pair_gemm_forward(shape, mode):
+    """Forward expert GEMMs on CTA pairs (tcgen05 cta_group::2, 256-row tiles split over two
+    SMs): h|u, a, o and y against the oracle, and bitwise equal to the single-CTA GEMMs."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    if mode == "skewed_given":
+        given = _skewed_topk(shape.T, shape.E, shape.k, seed=5)
+    else:
+        given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
+    fwd, _ = oracle_layer(shape, f64, topk_idx=given)
+    dev = _gpu_inputs(inp)
+    given_t = torch.tensor(given, dtype=torch.int32, device="cuda")
+    outs = {}
+    for name, flag in (("pair", N.FLAG_GEMM_PAIR), ("single", N.FLAG_GEMM_SINGLE)):
+        layer = mok.MoELayer(mok.desc_from_shape(shape, flags=flag))
+        y = layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"],
+                          given_topk=given_t)
+        torch.cuda.synchronize()
+        assert layer.status() == (0, 0)
+        outs[name] = {"y": y.clone(), "hu": layer.view("hu").clone(), "act": layer.view_split("act").clone(),
+                      "o": layer.view("expert_out").clone()}
+    p = outs["pair"]
+    hu = to_f64(p["hu"])
+    assert_intermediate_close(hu[:, :shape.I], fwd["h"], "h", rel=1e-4)
+    assert_intermediate_close(hu[:, shape.I:], fwd["u"], "u", rel=1e-4)
+    assert_intermediate_close(to_f64(p["act"]), fwd["a"], "a", rel=1e-3)
+    assert_intermediate_close(to_f64(p["o"]), fwd["o"], "o", rel=1e-3)
+    assert_bf16_close(to_f64(p["y"]), fwd["y"], "y")
+    for name in ("hu", "act", "o", "y"):
+        assert torch.equal(p[name], outs["single"][name]), name
+
+
 # ----------------------------------------------------------------------------- bounded waits
 
 def test_stuck_wait_times_out_and_context_survives():
