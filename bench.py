@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s, fwd+bwd, 1xGB300 (grouped-GEMM % of tensor peak reported alongside)"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-CPU_SAMPLE = {"T": 512, "E": 16}        # cpu_baseline: 512 tokens of the DSV3 shape over 16 experts
+CPU_SAMPLE = {"T": 1536, "E": 16}       # cpu_baseline: 1536 tokens of the DSV3 shape over 16 experts (~10 s)
 REF_SAMPLE = {"T": 256, "E": 16}        # --impl reference: per step
 
 
