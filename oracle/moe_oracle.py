@@ -284,7 +284,7 @@ def backward(fwd: Dict[str, np.ndarray], dy, x, w_router, w13, w2, *, kind, k, r
     [aitrending] "Technical Details").  The arithmetic is the calculus of
     ``forward``:
 
-    * dg[t][j]  = <dY[t], o[row]>            (= <dA'_row, a_row>, with dA' = dY[t] W2[e])
+    * dg[t][j]  = <dA'_row, a_row>, dA' = dY[t] W2[e]   (= <dY[t], o[row]>)
     * dO_row    = g[t][j] * dY[t]
     * dW2[e]    = sum over the expert's rows of dO_row (x) a_row
     * dA_row    = dO_row W2[e]
@@ -304,9 +304,10 @@ def backward(fwd: Dict[str, np.ndarray], dy, x, w_router, w13, w2, *, kind, k, r
     dy_g = dy[tok]
 
     q = quant if quant is not None else (lambda v, axis: v)
-    # d(gate) of each row: <dY[t], o[row]>; written as <dA', a> it is the quantity the
-    # SwiGLU backward produces alongside dA.
-    dg_row = np.einsum("rh,rh->r", dy_g, o)
+    # d(gate) of each row, computed where the pages put it, inside the SwiGLU backward:
+    # <dA'_row, a_row> with dA' = dY_g W2[e] (the product the SwiGLU backward receives).  It
+    # equals <dY[t], o[row]>; under MX emulation dA' is the quantised product.
+    dg_row = np.zeros(R)
     dA = np.zeros((R, I))
     dw2 = np.zeros((E, H, I))
     for e in range(E):
@@ -314,6 +315,7 @@ def backward(fwd: Dict[str, np.ndarray], dy, x, w_router, w13, w2, *, kind, k, r
         if hi == lo:
             continue
         dA_prime = q(dy_g[lo:hi], 1) @ q(w2[e], 0)               # [n][I], reduction over H
+        dg_row[lo:hi] = np.einsum("ri,ri->r", dA_prime, a[lo:hi])
         dA[lo:hi] = g_row[lo:hi, None] * dA_prime
         dO = g_row[lo:hi, None] * dy_g[lo:hi]
         dw2[e] = q(dO, 0).T @ q(a[lo:hi], 0)                      # reduction over rows

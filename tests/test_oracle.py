@@ -409,3 +409,50 @@ def test_token_forward_quantized_matches_layer():
         y, *_ = O.token_forward(x[t], w_r, None, lambda e: (w13[e], w2[e]), kind=O.SIGMOID, k=2, renorm=True,
                                 quant=q)
         assert np.allclose(y, fwd["y"][t], rtol=1e-12, atol=1e-14)
+
+
+def test_quantized_backward_quantises_each_operand_along_its_reduction():
+    """MX emulation of the backward: every GEMM operand goes through q exactly once, along the
+    reduction dimension of its GEMM: dY_g rows and W2[e] along H for dA' = dY_g W2[e]; dHU rows
+    and W13[e] along 2I for dX_g = dHU W13[e]; the expert's rows for both weight gradients
+    (dO and a for dW2, dHU and x_g for dW13).  With q the identity the result is unchanged."""
+    rng = np.random.default_rng(15)
+    T, H, E, I, k = 12, 96, 3, 32, 2   # H, I, 2I and every expert's row count all differ
+    x, w_r, w13, w2 = _rand_layer(rng, T, H, E, I, scale=0.2)
+    dy = rng.normal(0, 1, (T, H))
+    fwd = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True)
+    calls = []
+
+    def rec(v, axis):
+        calls.append((tuple(np.asarray(v).shape), axis))
+        return v
+
+    ref = O.backward(fwd, dy, x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True)
+    got = O.backward(fwd, dy, x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True, quant=rec)
+    for name in ("dx", "dw13", "dw2", "dgates", "dw_router"):
+        assert np.allclose(got[name], ref[name], rtol=1e-12, atol=1e-12), name
+    expected = []
+    for e in range(E):
+        n = int(fwd["offsets"][e + 1] - fwd["offsets"][e])
+        if n == 0:
+            continue
+        assert n not in (H, I, 2 * I)
+        expected += [((n, H), 1), ((H, I), 0),          # dA' = dY_g W2[e]
+                     ((n, H), 0), ((n, I), 0),          # dW2 = dO^T a
+                     ((n, 2 * I), 0), ((n, H), 0),      # dW13 = dHU^T x_g
+                     ((n, 2 * I), 1), ((2 * I, H), 0)]  # dX_g = dHU W13[e]
+    assert sorted(calls) == sorted(expected)
+
+
+def test_quantized_backward_close_to_exact():
+    rng = np.random.default_rng(16)
+    x, w_r, w13, w2 = _rand_layer(rng, 32, 64, 4, 64, scale=0.2)
+    dy = rng.normal(0, 1, (32, 64))
+    q = O.mx_quantize_dequantize
+    f_ref = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=2, renorm=True)
+    f_q = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=2, renorm=True, quant=q)
+    ref = O.backward(f_ref, dy, x, w_r, w13, w2, kind=O.SIGMOID, k=2, renorm=True)
+    got = O.backward(f_q, dy, x, w_r, w13, w2, kind=O.SIGMOID, k=2, renorm=True, quant=q)
+    for name in ("dx", "dw13", "dw2", "dgates"):
+        rel = np.linalg.norm(got[name] - ref[name]) / np.linalg.norm(ref[name])
+        assert 1e-3 < rel < 0.2, (name, rel)
