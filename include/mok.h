@@ -134,6 +134,14 @@ typedef struct {
   int64_t ring;       /* bf16 [slots * minibatch][H]  the token ring */
   int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb+1] tile starts */
   int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch */
+  /* MXFP8 backward only (-1 otherwise): operands quantised along their GEMM's reduction
+   * dimension, as exact bf16 values */
+  int64_t mx_dhu_c;   /* bf16 [T*k][2I] dh | du in 32-column blocks (A of dX_g = dHU W13[e]) */
+  int64_t mx_dhu_r;   /* bf16 [T*k][2I] dh | du in 32-row blocks of each expert (dW13) */
+  int64_t mx_xg_r;    /* bf16 [T*k][H]  dispatched x in 32-row blocks (dW13) */
+  int64_t mx_do_r;    /* bf16 [T*k][H]  gate * dY rows in 32-row blocks (dW2) */
+  int64_t mx_a_r;     /* bf16 [T*k][I]  a = silu(h) * u in 32-row blocks (dW2) */
+  int64_t mx_blk_off; /* i32 [E+1]      32-row blocks before each expert */
   int64_t ws_bytes;
 } mok_layout;
 
@@ -207,6 +215,29 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
 mok_status mok_quantize_weights(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_q,
                                 void* w13_scale, void* w2_q, void* w2_scale, void* stream);
 
+/* Backward-direction MXFP8 weights for mok_moe_backward_mxfp8: each GEMM of the backward
+ * quantises its operands along its own reduction dimension, so the weights are quantised again
+ * along the other axis: W2[e] [H][I] along H (for dA' = dY_g W2[e]) and W13[e] [2I][H] along 2I
+ * (for dX_g = dHU W13[e]), 32-row blocks, same rule as mok_quantize_weights.  The results are
+ * stored as their exact bf16 values in the nn.Linear layouts (w13_b [E][2I][H], w2_b [E][H][I]):
+ * the backward GEMMs read them with the bf16 kernels.  All device pointers, 16-byte aligned. */
+mok_status mok_quantize_weights_backward(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_b,
+                                         void* w2_b, void* stream);
+
+/* Layer backward with MXFP8 expert GEMMs (desc->precision must be MOK_MXFP8), after
+ * mok_moe_forward_mxfp8 with the same ctx.  Every expert GEMM operand is quantised in 32-element
+ * blocks along that GEMM's reduction dimension: dY_g (gathered, along H) and W2 along H for dA';
+ * dh|du along 2I and W13 along 2I for dX_g; for the weight gradients both operands along the
+ * expert's rows (gate * dY and a for dW2, dh|du and the dispatched x for dW13), in 32-row blocks
+ * that start at the expert's first row.  The gate gradient is <dA', a> in the SwiGLU backward
+ * epilogue, with dA' the quantised product; the router backward and the reverse dispatch are the
+ * bf16 path's.  w13_b / w2_b come from mok_quantize_weights_backward.  Outputs and ws as for
+ * mok_moe_backward (ws layout from an MXFP8 descriptor). */
+mok_status mok_moe_backward_mxfp8(const mok_layer_desc* desc, const void* dy, const void* x, const void* w_router,
+                                  const void* w13_b, const void* w2_b, const void* ctx, size_t ctx_bytes, void* dx,
+                                  float* dw_router, void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* Layer forward with MXFP8 expert GEMMs (desc->precision must be MOK_MXFP8, no ring).  As
  * mok_moe_forward, with the expert weights given as mok_quantize_weights output.  The MXFP8
  * activation quantisation sits on the data path ("把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源
@@ -215,7 +246,7 @@ mok_status mok_quantize_weights(const mok_layer_desc* desc, const void* w13, con
  * the quantised values as bf16 (E4M3 * 2^X is exact in bf16).  The GEMMs stream E4M3 weights,
  * expand them exactly to bf16 in shared memory and accumulate in fp32, so each product equals
  * the MXFP8 product.  The router stays in bf16.  ctx / ws as for mok_moe_forward (ctx x_g holds
- * the quantised rows).  There is no MXFP8 backward: mok_moe_backward returns
+ * the quantised rows).  The MXFP8 backward is mok_moe_backward_mxfp8; mok_moe_backward returns
  * MOK_ERR_UNSUPPORTED for an MXFP8 descriptor. */
 mok_status mok_moe_forward_mxfp8(const mok_layer_desc* desc, const void* x, const void* w_router,
                                  const float* router_bias, const int32_t* given_topk, const void* w13_q,

@@ -37,7 +37,8 @@ class LayerDesc(ctypes.Structure):
 
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
                  "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
-                 "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters", "ws_bytes"]
+                 "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
+                 "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # forward expert GEMMs on CTA pairs (256-row tiles)
 FLAG_GEMM_SINGLE = 4   # forward expert GEMMs on single CTAs (128-row tiles)
@@ -231,7 +232,9 @@ _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.
                "logits": torch.float32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
                "expert_out": torch.float32, "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "dhu_lo": torch.bfloat16,
                "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
-               "dg_part": torch.float32, "dlogits": torch.float32}
+               "dg_part": torch.float32, "dlogits": torch.float32, "mx_dhu_c": torch.bfloat16,
+               "mx_dhu_r": torch.bfloat16, "mx_xg_r": torch.bfloat16, "mx_do_r": torch.bfloat16,
+               "mx_a_r": torch.bfloat16, "mx_blk_off": torch.int32}
 
 
 class MoELayer:
@@ -251,7 +254,9 @@ class MoELayer:
                 "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "act": (R, d.I),
                 "act_lo": (R, d.I), "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I),
                 "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
-                "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E)}[name]
+                "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E), "mx_dhu_c": (R, 2 * d.I),
+                "mx_dhu_r": (R, 2 * d.I), "mx_xg_r": (R, d.H), "mx_do_r": (R, d.H), "mx_a_r": (R, d.I),
+                "mx_blk_off": (d.E + 1,)}[name]
 
     def view_split(self, name: str) -> torch.Tensor:
         """hi + lo of a split operand ("act", "dhu", "gact") as one float32 tensor."""
@@ -287,6 +292,21 @@ class MoELayer:
                    "dgates": torch.empty((d.T, d.k), dtype=torch.float32, device=dev)}
         moe_backward(d, dy, x, w_router, w13, w2, self.ctx, out["dx"], out["dw_router"], out["dw13"], out["dw2"],
                      out["dgates"], self.ws, stream)
+        return out
+
+    def backward_mxfp8(self, dy, x, w_router, wb, out=None, stream=None):
+        """mok_moe_backward_mxfp8 after forward_mxfp8; ``wb`` from quantize_weights_backward."""
+        d = self.desc
+        dev = dy.device
+        if out is None:
+            wdt = torch.bfloat16 if (d.flags & FLAG_WGRAD_BF16) else torch.float32
+            out = {"dx": torch.empty((d.T, d.H), dtype=torch.bfloat16, device=dev),
+                   "dw_router": torch.empty((d.E, d.H), dtype=torch.float32, device=dev),
+                   "dw13": torch.empty((d.E, 2 * d.I, d.H), dtype=wdt, device=dev),
+                   "dw2": torch.empty((d.E, d.H, d.I), dtype=wdt, device=dev),
+                   "dgates": torch.empty((d.T, d.k), dtype=torch.float32, device=dev)}
+        moe_backward_mxfp8(d, dy, x, w_router, wb, self.ctx, out["dx"], out["dw_router"], out["dw13"], out["dw2"],
+                           out["dgates"], self.ws, stream)
         return out
 
     def status(self, stream=None):
@@ -372,3 +392,39 @@ def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws
         _ptr(wq["w13_scale"]), _ptr(wq["w2_q"]), _ptr(wq["w2_scale"]), _ptr(y), _ptr(ctx),
         ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
     return y
+
+
+def quantize_weights_backward(desc, w13, w2, stream=None):
+    """mok_quantize_weights_backward: W13 quantised along 2I and W2 along H (32-row blocks), as
+    their exact bf16 values.  Returns {"w13_b", "w2_b"}."""
+    _expect(w13, (desc.E, 2 * desc.I, desc.H), torch.bfloat16, "w13")
+    _expect(w2, (desc.E, desc.H, desc.I), torch.bfloat16, "w2")
+    out = {"w13_b": torch.empty_like(w13), "w2_b": torch.empty_like(w2)}
+    fn = _mx_fn("mok_quantize_weights_backward", 5)
+    _check("mok_quantize_weights_backward", fn(ctypes.byref(desc), _ptr(w13), _ptr(w2), _ptr(out["w13_b"]),
+                                               _ptr(out["w2_b"]), _stream(stream)))
+    return out
+
+
+def moe_backward_mxfp8(desc, dy, x, w_router, wb, ctx, dx, dw_router, dw13, dw2, dgates, ws, stream=None):
+    """mok_moe_backward_mxfp8 with the weights of ``quantize_weights_backward``."""
+    E, H, I = desc.E, desc.H, desc.I
+    wdt = torch.bfloat16 if (desc.flags & FLAG_WGRAD_BF16) else torch.float32
+    _expect(x, (desc.T, H), torch.bfloat16, "x")
+    _expect(w_router, (E, H), torch.bfloat16, "w_router")
+    _expect(wb["w13_b"], (E, 2 * I, H), torch.bfloat16, "w13_b")
+    _expect(wb["w2_b"], (E, H, I), torch.bfloat16, "w2_b")
+    _expect(dy, (desc.T, H), torch.bfloat16, "dy")
+    _expect(dx, (desc.T, H), torch.bfloat16, "dx")
+    _expect(dw_router, (E, H), torch.float32, "dw_router")
+    _expect(dw13, (E, 2 * I, H), wdt, "dw13")
+    _expect(dw2, (E, H, I), wdt, "dw2")
+    _expect(dgates, (desc.T, desc.k), torch.float32, "dgates", nullable=True)
+    fn = load().mok_moe_backward_mxfp8
+    P, SZ = ctypes.c_void_p, ctypes.c_size_t
+    fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
+    fn.restype = ctypes.c_int32
+    _check("mok_moe_backward_mxfp8", fn(
+        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(wb["w13_b"]), _ptr(wb["w2_b"]), _ptr(ctx),
+        ctx.numel() * ctx.element_size(), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))

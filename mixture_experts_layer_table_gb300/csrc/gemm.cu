@@ -255,10 +255,11 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
                            const int32_t* offsets, const int32_t* tile_off, float* dx_g, int* status, int n_sm,
                            cudaStream_t st) {
   CUtensorMap ta, ta2, tb;
-  // A = dHU [R][2I] (K = 2I) as hi + lo; B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)
-  if (!tmap_2d(&ta, dhu_hi, 2 * I, R, BK, BM) || !tmap_2d(&ta2, dhu_lo, 2 * I, R, BK, BM) ||
-      !tmap_3d(&tb, w13, H, 2 * I, E, 64, BK))
-    return cudaErrorInvalidValue;
+  // A = dHU [R][2I] (K = 2I) as hi + lo (or a single bf16 tensor when dhu_lo is null);
+  // B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)
+  if (!tmap_2d(&ta, dhu_hi, 2 * I, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, 64, BK)) return cudaErrorInvalidValue;
+  ta2 = ta;
+  if (dhu_lo != nullptr && !tmap_2d(&ta2, dhu_lo, 2 * I, R, BK, BM)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);
   g.N = H;
   g.K = 2 * I;
@@ -267,6 +268,8 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
   const int bound = row_tiles_bound(R, E) * (H / 256);
   CUtensorMap to;
   if (!tmap_out(&to, dx_g, H, R, true)) return cudaErrorInvalidValue;
+  if (dhu_lo == nullptr)
+    return launch<MODE_DGRAD, EPI_F32, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st, &to);
   return launch<MODE_DGRAD, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st, &to);
 }
 
@@ -280,8 +283,10 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   tb2 = tb;
   if (a_lo && !tmap_2d(&ta2, a_lo, M, R, 64, BK)) return cudaErrorInvalidValue;
   if (b_lo && !tmap_2d(&tb2, b_lo, N, R, 64, BK)) return cudaErrorInvalidValue;
-  // exactly one operand is a hi/lo pair: it is the stationary one
-  if ((a_lo != nullptr) == (b_lo != nullptr)) return cudaErrorInvalidValue;
+  // at most one operand is a hi/lo pair: it is the stationary one (A when neither is)
+  if (a_lo != nullptr && b_lo != nullptr) return cudaErrorInvalidValue;
+  const bool split = a_lo != nullptr || b_lo != nullptr;
+  const bool stat_a = a_lo != nullptr || !split;
   (void)WBN;
   CUtensorMap to;
   if (!tmap_wgrad_out(&to, dw, M, N, E, out_f32 != 0)) return cudaErrorInvalidValue;
@@ -292,7 +297,7 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   g.offsets = offsets;
   g.out = dw;
   g.status = status;
-  const int strips = E * (a_lo ? M / 128 : N / 128);
+  const int strips = E * (stat_a ? M / 128 : N / 128);
   const int grid = std::min(strips, n_sm);
   if (grid <= 0) return cudaSuccess;
   const size_t smem = wgrad_smem_bytes(E);
@@ -303,6 +308,7 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
     return cudaGetLastError();
   };
   static_assert(wgrad_smem_bytes(1024) <= 232448, "shared memory budget");
+  if (!split) return out_f32 ? run(wgrad_kernel<true, true, false>) : run(wgrad_kernel<true, false, false>);
   if (a_lo) return out_f32 ? run(wgrad_kernel<true, true>) : run(wgrad_kernel<true, false>);
   return out_f32 ? run(wgrad_kernel<false, true>) : run(wgrad_kernel<false, false>);
 }

@@ -70,6 +70,16 @@ cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, vo
                               int* status, int n_sm, cudaStream_t st);
 // MXFP8 (mx.cu, gemm.cu)
 cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm, cudaStream_t st);
+// MXFP8 backward operands (mx.cu).  src of launch_mx_quant_rows: 0 plain rows (in0, fixed
+// segments of seg_len rows), 1 hi + lo rows, 2 a = silu(h) u from h | u, 3 token rows gathered by
+// src_of, 4 gate_row * gathered token rows; segments from offsets / blk_off unless seg_len > 0.
+cudaError_t launch_mx_block_offsets(const int32_t* offsets, int E, int32_t* blk_off, cudaStream_t st);
+cudaError_t launch_mx_quant_rows(int src, int rows_bound, int C, int E, int seg_len, const int32_t* offsets,
+                                 const int32_t* blk_off, const void* in0, const void* in1, const float* hu,
+                                 const float* gate_row, const int32_t* src_of, int k, void* out, int n_sm,
+                                 cudaStream_t st);
+cudaError_t launch_mx_quant_cols(const void* hi, const void* lo, long long R, int C, void* out, int n_sm,
+                                 cudaStream_t st);
 cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
                                   cudaStream_t st);
 cudaError_t launch_gemm1_swiglu_mx(const void* x_g, const void* w13_q, const void* w13_s, int R, int H, int I, int E,

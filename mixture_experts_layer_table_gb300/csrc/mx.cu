@@ -4,6 +4,8 @@
 // on the dispatch / grouped GEMM / SwiGLU path instead of in a separate kernel).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "mx.cuh"
 
@@ -84,6 +86,185 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
+}
+
+// ---------------------------------------------------------------- MXFP8 backward operands
+// In the backward every GEMM operand is quantised along that GEMM's reduction dimension: for
+// the weight gradients that is the row (token) axis inside each expert's segment, in blocks of 32
+// rows that start at the segment's first row (a ragged last block is padded with zeros), for the
+// transposed weights the row axis of W2[e] (H) and W13[e] (2I).  Quantised values are stored as
+// their exact bf16 values.
+
+// blk_off[e] = number of 32-row blocks of the segments before e (blk_off[E] = total).
+__global__ void __launch_bounds__(1024) mx_block_offsets_kernel(const int32_t* __restrict__ offsets, int E,
+                                                                 int32_t* __restrict__ blk_off) {
+  __shared__ int32_t sc[1024];
+  const int t = threadIdx.x;
+  sc[t] = t < E ? (offsets[t + 1] - offsets[t] + 31) / 32 : 0;
+  __syncthreads();
+  for (int d = 1; d < 1024; d <<= 1) {  // inclusive scan
+    const int32_t v = t >= d ? sc[t - d] : 0;
+    __syncthreads();
+    sc[t] += v;
+    __syncthreads();
+  }
+  if (t < E) blk_off[t + 1] = sc[t];
+  if (t == 0) blk_off[0] = 0;
+}
+
+enum MxRowSrc { MXR_PLAIN = 0, MXR_SPLIT = 1, MXR_SWIGLU = 2, MXR_GATHER = 3, MXR_GATHER_GATE = 4 };
+
+struct MxRowsArgs {
+  int C;                          // columns (output row length)
+  int E;
+  int seg_len;                    // > 0: E segments of seg_len rows; 0: segments from offsets
+  const int32_t* offsets;         // [E+1]
+  const int32_t* blk_off;         // [E+1] from mx_block_offsets_kernel
+  const __nv_bfloat16* in0;       // PLAIN / SPLIT hi [rows][C]; GATHER*: token rows [T][C]
+  const __nv_bfloat16* in1;       // SPLIT lo
+  const float* hu;                // SWIGLU: h | u [rows][2C]
+  const float* gate_row;          // GATHER_GATE: gate of each row
+  const int32_t* src_of;          // GATHER*: row -> assignment (token = src_of / k)
+  int k;
+  __nv_bfloat16* out;             // [rows][C]
+};
+
+template <int SRC>
+__device__ __forceinline__ float mx_row_value(const MxRowsArgs& a, int r, int c) {
+  if (SRC == MXR_PLAIN) return __bfloat162float(a.in0[(size_t)r * a.C + c]);
+  if (SRC == MXR_SPLIT)
+    return __bfloat162float(a.in0[(size_t)r * a.C + c]) + __bfloat162float(a.in1[(size_t)r * a.C + c]);
+  if (SRC == MXR_SWIGLU) {
+    const float h = a.hu[(size_t)r * 2 * a.C + c], u = a.hu[(size_t)r * 2 * a.C + a.C + c];
+    return h / (1.0f + __expf(-h)) * u;
+  }
+  const int tok = a.src_of[r] / a.k;
+  const float v = __bfloat162float(a.in0[(size_t)tok * a.C + c]);
+  return SRC == MXR_GATHER_GATE ? a.gate_row[r] * v : v;
+}
+
+// One thread per (32-row block, column): reads the block's 32 values of its column, quantises
+// them as one MX block, writes the valid rows.  Threads of a CTA take consecutive columns.
+template <int SRC>
+__global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) {
+  const int nchunk = (a.C + 255) / 256;
+  const int nblk = a.seg_len > 0 ? a.E * (a.seg_len / 32) : a.blk_off[a.E];
+  const long long items = (long long)nblk * nchunk;
+  for (long long w = blockIdx.x; w < items; w += gridDim.x) {
+    const int b = (int)(w / nchunk);
+    const int c = (int)(w - (long long)b * nchunk) * 256 + threadIdx.x;
+    int r0, nrows;
+    if (a.seg_len > 0) {
+      r0 = b * 32;
+      nrows = 32;
+    } else {
+      int lo = 0, hi = a.E;  // largest e with blk_off[e] <= b (the last of equal starts owns blocks)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(&a.blk_off[mid]) <= b) lo = mid; else hi = mid;
+      }
+      r0 = __ldg(&a.offsets[lo]) + 32 * (b - __ldg(&a.blk_off[lo]));
+      nrows = min(32, __ldg(&a.offsets[lo + 1]) - r0);
+    }
+    if (c >= a.C) continue;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < nrows ? mx_row_value<SRC>(a, r0 + j, c) : 0.0f;
+    mx_quantize32(v, nullptr);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nrows) a.out[(size_t)(r0 + j) * a.C + c] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+// out[r] = MX(hi[r] + lo[r]) along the row, blocks of 32 columns.  One thread per block.
+__global__ void __launch_bounds__(256)
+    mx_quant_cols_kernel(const __nv_bfloat16* __restrict__ hi, const __nv_bfloat16* __restrict__ lo, long long R,
+                         int C, __nv_bfloat16* __restrict__ out) {
+  const int nb = C / 32;
+  const long long total = R * nb;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const size_t base = (size_t)i * 32;  // row-major: block i covers elements 32i .. 32i+31
+    const uint4* h4 = reinterpret_cast<const uint4*>(hi + base);
+    const uint4* l4 = reinterpret_cast<const uint4*>(lo + base);
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 uh = h4[c], ul = l4[c];
+      const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&uh);
+      const __nv_bfloat162* bl = reinterpret_cast<const __nv_bfloat162*>(&ul);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 fh = __bfloat1622float2(bh[j]), fl = __bfloat1622float2(bl[j]);
+        v[c * 8 + 2 * j] = fh.x + fl.x;
+        v[c * 8 + 2 * j + 1] = fh.y + fl.y;
+      }
+    }
+    mx_quantize32(v, nullptr);
+    uint4* d = reinterpret_cast<uint4*>(out + base);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 u;
+      uint32_t* p = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 bb = __floats2bfloat162_rn(v[c * 8 + 2 * j], v[c * 8 + 2 * j + 1]);
+        p[j] = *reinterpret_cast<uint32_t*>(&bb);
+      }
+      d[c] = u;
+    }
+  }
+}
+
+cudaError_t launch_mx_block_offsets(const int32_t* offsets, int E, int32_t* blk_off, cudaStream_t st) {
+  if (E > 1024) return cudaErrorInvalidValue;
+  mx_block_offsets_kernel<<<1, 1024, 0, st>>>(offsets, E, blk_off);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quant_rows(int src, int rows_bound, int C, int E, int seg_len, const int32_t* offsets,
+                                 const int32_t* blk_off, const void* in0, const void* in1, const float* hu,
+                                 const float* gate_row, const int32_t* src_of, int k, void* out, int n_sm,
+                                 cudaStream_t st) {
+  MxRowsArgs a;
+  a.C = C;
+  a.E = E;
+  a.seg_len = seg_len;
+  a.offsets = offsets;
+  a.blk_off = blk_off;
+  a.in0 = reinterpret_cast<const __nv_bfloat16*>(in0);
+  a.in1 = reinterpret_cast<const __nv_bfloat16*>(in1);
+  a.hu = hu;
+  a.gate_row = gate_row;
+  a.src_of = src_of;
+  a.k = k;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  if (seg_len > 0 && seg_len % 32 != 0) return cudaErrorInvalidValue;
+  // an upper bound of the work items sizes the grid; the kernel reads the exact count
+  const long long items = (long long)((rows_bound + 31) / 32 + E) * ((C + 255) / 256);
+  const int blocks = (int)std::min<long long>(std::max<long long>(items, 1), (long long)n_sm * 8);
+  switch (src) {
+    case MXR_PLAIN: mx_quant_rows_kernel<MXR_PLAIN><<<blocks, 256, 0, st>>>(a); break;
+    case MXR_SPLIT: mx_quant_rows_kernel<MXR_SPLIT><<<blocks, 256, 0, st>>>(a); break;
+    case MXR_SWIGLU: mx_quant_rows_kernel<MXR_SWIGLU><<<blocks, 256, 0, st>>>(a); break;
+    case MXR_GATHER: mx_quant_rows_kernel<MXR_GATHER><<<blocks, 256, 0, st>>>(a); break;
+    case MXR_GATHER_GATE: mx_quant_rows_kernel<MXR_GATHER_GATE><<<blocks, 256, 0, st>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quant_cols(const void* hi, const void* lo, long long R, int C, void* out, int n_sm,
+                                 cudaStream_t st) {
+  if (C % 32 != 0) return cudaErrorInvalidValue;
+  const long long total = R * (C / 32);
+  if (total == 0) return cudaSuccess;
+  const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)n_sm * 16);
+  mx_quant_cols_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(hi),
+                                               reinterpret_cast<const __nv_bfloat16*>(lo), R, C,
+                                               reinterpret_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm,

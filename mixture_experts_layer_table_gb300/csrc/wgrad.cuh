@@ -42,8 +42,9 @@ __host__ __device__ constexpr size_t wgrad_smem_bytes(int E) {
 }
 
 // STAT_A: A is the stationary pair (tmA hi, tmA2 lo), strips walk n; otherwise B is (tmB, tmB2)
-// and strips walk m.  OUT_F32: fp32 output, else bf16.
-template <bool STAT_A, bool OUT_F32>
+// and strips walk m.  OUT_F32: fp32 output, else bf16.  STAT_SPLIT false: the stationary
+// operand is a single bf16 tensor (no lo half; the MXFP8 backward, whose operands are exact).
+template <bool STAT_A, bool OUT_F32, bool STAT_SPLIT = true>
 __global__ void __launch_bounds__(WG_THREADS, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                  const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
@@ -125,14 +126,14 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         if (!mbar_wait(stat_empty, sphase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs, 32))
           return false;
         sphase ^= 1;
-        mbar_arrive_expect_tx(stat_full, nk * WG_STAT_SLOT);
+        mbar_arrive_expect_tx(stat_full, nk * (STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2));
         for (int j = 0; j < nk; ++j) {
           const uint32_t slot = smem_u32(stat + j * WG_STAT_SLOT);
           const int r = row0 + (kb0 + j) * WG_BK;
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             tma_load_2d(slot + q * 8192, sh, stat_full, f * 128 + q * 64, r, pol);
-            tma_load_2d(slot + 16384 + q * 8192, sl, stat_full, f * 128 + q * 64, r, pol);
+            if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full, f * 128 + q * 64, r, pol);
           }
         }
         return true;
@@ -224,10 +225,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           const uint32_t accum = (first && k16 == 0) ? 0u : 1u;
           if (STAT_A) {
             umma_f16(d, dh, ds, idesc, accum);
-            umma_f16(d, dl, ds, idesc, 1u);
+            if (STAT_SPLIT) umma_f16(d, dl, ds, idesc, 1u);
           } else {
             umma_f16(d, ds, dh, idesc, accum);
-            umma_f16(d, ds, dl, idesc, 1u);
+            if (STAT_SPLIT) umma_f16(d, ds, dl, idesc, 1u);
           }
         }
         umma_commit(empty_bar(stage));

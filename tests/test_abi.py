@@ -41,7 +41,8 @@ def test_layout_sizes_and_alignment(lib):
     lay = mok.get_layout(mok.desc_from_shape(W.DSV3))
     R, H, I = W.DSV3.R, W.DSV3.H, W.DSV3.I
     for name, off in lay.items():
-        assert off % 256 == 0 or (off == -1 and name in ("ring", "mb_tables", "mb_counters")), name
+        assert off % 256 == 0 or (off == -1 and (name in ("ring", "mb_tables", "mb_counters") or
+                                                 name.startswith("mx_"))), name
     assert lay["ctx_bytes"] >= lay["hu"] + R * 2 * I * 2
     assert lay["ws_bytes"] >= lay["dlogits"] + W.DSV3.T * W.DSV3.E * 4
     assert lay["status"] == 0
@@ -59,6 +60,22 @@ def test_desc_validation(lib, field, value, code):
         code = 2
     lay = N.Layout()
     assert lib.mok_get_layout(ctypes.byref(d), ctypes.byref(lay)) == code
+
+
+def test_mxfp8_layout_has_the_backward_operands(lib):
+    bf = mok.get_layout(mok.desc_from_shape(W.DSV3))
+    mx = mok.get_layout(mok.desc_from_shape(W.DSV3_MXFP8))
+    R, H, I, E = W.DSV3.T * W.DSV3.k, W.DSV3.H, W.DSV3.I, W.DSV3.E
+    sizes = {"mx_dhu_c": R * 2 * I * 2, "mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2, "mx_do_r": R * H * 2,
+             "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4}
+    ends = []
+    for name, nbytes in sizes.items():
+        assert bf[name] == -1, name
+        assert mx[name] >= bf["dlogits"] and mx[name] % 256 == 0, name
+        ends.append((mx[name], mx[name] + nbytes))
+    ends.sort()
+    assert all(a[1] <= b[0] for a, b in zip(ends, ends[1:]))  # disjoint
+    assert ends[-1][1] <= mx["ws_bytes"]
 
 
 def test_ring_layout(lib):

@@ -1,4 +1,4 @@
-"""MXFP8 forward on the GPU against the oracle's MX emulation (quantise every GEMM operand in
+"""MXFP8 forward and backward on the GPU against the oracle's MX emulation (quantise every GEMM operand in
 32-element blocks along that GEMM's reduction axis, then multiply in float64).
 
 Bars: the quantised weights (E4M3 bytes and E8M0 scales) and the quantised dispatched rows are
@@ -116,3 +116,66 @@ def test_mx_forward_full_size_sampled_and_deterministic():
         want.append(y_t)
     _, _, fro = err_stats(np.array(got), np.array(want))
     assert fro <= MX_FRO, fro
+
+
+# ----------------------------------------------------------------------------- backward
+
+def test_backward_weights_bit_exact():
+    """W2 quantised along H and W13 along 2I (32-row blocks of each expert's matrix)."""
+    inp = W.make_inputs(MID, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    desc = mok.desc_from_shape(MID)
+    wb = mok.quantize_weights_backward(desc, inp["w13"].cuda(), inp["w2"].cuda())
+    torch.cuda.synchronize()
+    for name, w in (("w13", f64["w13"]), ("w2", f64["w2"])):
+        got = to_f64(wb[name + "_b"])
+        for e in range(MID.E):
+            want = q(w[e], 0)
+            assert np.array_equal(got[e], want), (name, e, int((got[e] != want).sum()))
+
+
+def _mx_fwd_bwd(shape, seed=0, given=None):
+    inp = W.make_inputs(shape, seed=seed, device="cpu")
+    dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    desc = mok.desc_from_shape(shape)
+    wq = mok.quantize_weights(desc, dev["w13"], dev["w2"])
+    wb = mok.quantize_weights_backward(desc, dev["w13"], dev["w2"])
+    layer = mok.MoELayer(desc)
+    y = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+    g = torch.tensor(given, dtype=torch.int32, device="cuda") if given is not None else None
+    mok.moe_forward_mxfp8(desc, dev["x"], dev["w_router"], dev["router_bias"], g, wq, y, layer.ctx, layer.ws)
+    grads = layer.backward_mxfp8(dev["dy"], dev["x"], dev["w_router"], wb)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    return inp, layer, y, grads
+
+
+@pytest.mark.parametrize("skew", [False, True])
+def test_mx_backward_matches_mx_oracle(skew):
+    """Every gradient within relative Frobenius 5e-2 of the oracle's MX-emulating backward (each
+    backward GEMM operand quantised along its reduction axis, float64 products)."""
+    shape = MID.scaled(skew=skew)
+    inp0 = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp0)
+    given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
+    inp, layer, y, g = _mx_fwd_bwd(shape, given=given)
+    fwd = O.forward(f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router, k=shape.k,
+                    renorm=shape.renorm, router_bias=f64["router_bias"], topk_idx=given, quant=q)
+    bwd = O.backward(fwd, f64["dy"], f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router,
+                     k=shape.k, renorm=shape.renorm, quant=q)
+    ref_fwd = O.forward(f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router, k=shape.k,
+                        renorm=shape.renorm, router_bias=f64["router_bias"], topk_idx=given)
+    ref = O.backward(ref_fwd, f64["dy"], f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router,
+                     k=shape.k, renorm=shape.renorm)
+    for name in ("dx", "dw13", "dw2", "dgates", "dw_router"):
+        _, _, fro = err_stats(to_f64(g[name]), bwd[name])
+        _, _, fro_ref = err_stats(to_f64(g[name]), ref[name])
+        print("%s: vs MX oracle %.3e, vs unquantised %.3e" % (name, fro, fro_ref))
+        assert fro <= MX_FRO, (name, fro)
+
+
+def test_mx_backward_deterministic():
+    shape = MID.scaled(skew=True)
+    runs = [_mx_fwd_bwd(shape, seed=4) for _ in range(2)]
+    for name in ("dx", "dw13", "dw2", "dgates", "dw_router"):
+        assert torch.equal(runs[0][3][name], runs[1][3][name]), name
