@@ -339,11 +339,35 @@ def run_mok(args, rank, world, local_rank):
         mx_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
         if mx_layer.status() != (0, 0):
             raise RuntimeError("device status set in the MXFP8 forward")
+        # MXFP8 forward + backward (backward-direction weights quantised once, outside the timing)
+        wb = mok.quantize_weights_backward(layer.desc, w13, w2)
+
+        def mx_step():
+            mok.moe_forward_mxfp8(mx_desc, x, wr, None, None, wq, y, mx_layer.ctx, mx_layer.ws)
+            mx_layer.backward_mxfp8(dy, x, wr, wb, out=grads)
+
+        for _ in range(2):
+            mx_step()
+        barrier()
+        torch.cuda.synchronize()
+        N.trace_start(40 * args.steps + 16)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            mx_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        mxb_trace = N.trace_stop()
+        mxb_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+        if mx_layer.status() != (0, 0):
+            raise RuntimeError("device status set in the MXFP8 backward")
         mx = {"fwd_ms": round(mx_ms, 4), "tokens_per_s": round(T * world / (mx_ms * 1e-3), 1),
               "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mx_trace.items()},
-              "weights": "E4M3 + E8M0 per 32 along K (11.3 GB), activations quantised in the gather and "
-                         "the SwiGLU epilogue"}
-        del mx_layer, wq
+              "fwd_bwd_ms": round(mxb_ms, 4), "fwd_bwd_tokens_per_s": round(T * world / (mxb_ms * 1e-3), 1),
+              "fwd_bwd_kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mxb_trace.items()},
+              "weights": "forward: E4M3 + E8M0 per 32 along K (11.3 GB); backward: W2 along H and W13 along "
+                         "2I, stored as exact bf16 values (22.5 GB); activations and gradients quantised "
+                         "along each GEMM's reduction"}
+        del mx_layer, wq, wb
 
     if rank != 0:
         return
@@ -513,7 +537,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward timing")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",

@@ -129,30 +129,60 @@ struct MxRowsArgs {
   __nv_bfloat16* out;             // [rows][C]
 };
 
-template <int SRC>
-__device__ __forceinline__ float mx_row_value(const MxRowsArgs& a, int r, int c) {
-  if (SRC == MXR_PLAIN) return __bfloat162float(a.in0[(size_t)r * a.C + c]);
-  if (SRC == MXR_SPLIT)
-    return __bfloat162float(a.in0[(size_t)r * a.C + c]) + __bfloat162float(a.in1[(size_t)r * a.C + c]);
-  if (SRC == MXR_SWIGLU) {
-    const float h = a.hu[(size_t)r * 2 * a.C + c], u = a.hu[(size_t)r * 2 * a.C + a.C + c];
-    return h / (1.0f + __expf(-h)) * u;
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float* f) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 t = __bfloat1622float2(b[q]);
+    f[2 * q] = t.x;
+    f[2 * q + 1] = t.y;
   }
-  const int tok = a.src_of[r] / a.k;
-  const float v = __bfloat162float(a.in0[(size_t)tok * a.C + c]);
-  return SRC == MXR_GATHER_GATE ? a.gate_row[r] * v : v;
 }
 
-// One thread per (32-row block, column): reads the block's 32 values of its column, quantises
-// them as one MX block, writes the valid rows.  Threads of a CTA take consecutive columns.
+// Values of row r, columns c .. c+7 (c a multiple of 8), from the source.
+template <int SRC>
+__device__ __forceinline__ void mx_row_values8(const MxRowsArgs& a, int r, int c, float* f) {
+  if (SRC == MXR_PLAIN || SRC == MXR_SPLIT) {
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.in0 + (size_t)r * a.C + c), f);
+    if (SRC == MXR_SPLIT) {
+      float l[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.in1 + (size_t)r * a.C + c), l);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] += l[q];
+    }
+  } else if (SRC == MXR_SWIGLU) {
+    const float4* hp = reinterpret_cast<const float4*>(a.hu + (size_t)r * 2 * a.C + c);
+    const float4* up = reinterpret_cast<const float4*>(a.hu + (size_t)r * 2 * a.C + a.C + c);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const float4 h4 = hp[q], u4 = up[q];
+      const float hv[4] = {h4.x, h4.y, h4.z, h4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+      for (int z = 0; z < 4; ++z) f[4 * q + z] = hv[z] / (1.0f + __expf(-hv[z])) * uv[z];
+    }
+  } else {
+    const int tok = a.src_of[r] / a.k;
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.in0 + (size_t)tok * a.C + c), f);
+    if (SRC == MXR_GATHER_GATE) {
+      const float g = a.gate_row[r];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) f[q] *= g;
+    }
+  }
+}
+
+// One CTA per (32-row block, 256 columns): the 32 x 256 values are staged in shared memory with
+// 16-byte loads along the rows, then thread c quantises column c as one MX block and writes its
+// valid rows (consecutive threads, consecutive columns).  C is a multiple of 256.
 template <int SRC>
 __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) {
-  const int nchunk = (a.C + 255) / 256;
+  __shared__ float tile[32][257];
+  const int nchunk = a.C / 256;
   const int nblk = a.seg_len > 0 ? a.E * (a.seg_len / 32) : a.blk_off[a.E];
   const long long items = (long long)nblk * nchunk;
   for (long long w = blockIdx.x; w < items; w += gridDim.x) {
     const int b = (int)(w / nchunk);
-    const int c = (int)(w - (long long)b * nchunk) * 256 + threadIdx.x;
+    const int c0 = (int)(w - (long long)b * nchunk) * 256;
     int r0, nrows;
     if (a.seg_len > 0) {
       r0 = b * 32;
@@ -166,11 +196,28 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) 
       r0 = __ldg(&a.offsets[lo]) + 32 * (b - __ldg(&a.blk_off[lo]));
       nrows = min(32, __ldg(&a.offsets[lo + 1]) - r0);
     }
-    if (c >= a.C) continue;
+    // stage: 32 rows x 32 chunks of 8 columns, 4 chunks per thread
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = threadIdx.x + 256 * i;
+      const int row = idx >> 5, ch = idx & 31;
+      float f[8];
+      if (row < nrows) {
+        mx_row_values8<SRC>(a, r0 + row, c0 + 8 * ch, f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = 0.0f;  // the ragged last block is padded with zeros
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tile[row][8 * ch + q] = f[q];
+    }
+    __syncthreads();
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < nrows ? mx_row_value<SRC>(a, r0 + j, c) : 0.0f;
+    for (int j = 0; j < 32; ++j) v[j] = tile[j][threadIdx.x];
+    __syncthreads();  // the tile is refilled by the next item
     mx_quantize32(v, nullptr);
+    const int c = c0 + threadIdx.x;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (j < nrows) a.out[(size_t)(r0 + j) * a.C + c] = __float2bfloat16_rn(v[j]);
@@ -240,9 +287,9 @@ cudaError_t launch_mx_quant_rows(int src, int rows_bound, int C, int E, int seg_
   a.src_of = src_of;
   a.k = k;
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
-  if (seg_len > 0 && seg_len % 32 != 0) return cudaErrorInvalidValue;
+  if ((seg_len > 0 && seg_len % 32 != 0) || C % 256 != 0) return cudaErrorInvalidValue;
   // an upper bound of the work items sizes the grid; the kernel reads the exact count
-  const long long items = (long long)((rows_bound + 31) / 32 + E) * ((C + 255) / 256);
+  const long long items = (long long)((rows_bound + 31) / 32 + E) * (C / 256);
   const int blocks = (int)std::min<long long>(std::max<long long>(items, 1), (long long)n_sm * 8);
   switch (src) {
     case MXR_PLAIN: mx_quant_rows_kernel<MXR_PLAIN><<<blocks, 256, 0, st>>>(a); break;

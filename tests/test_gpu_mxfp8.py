@@ -179,3 +179,58 @@ def test_mx_backward_deterministic():
     runs = [_mx_fwd_bwd(shape, seed=4) for _ in range(2)]
     for name in ("dx", "dw13", "dw2", "dgates", "dw_router"):
         assert torch.equal(runs[0][3][name], runs[1][3][name]), name
+
+
+def test_mx_backward_full_size_sampled_experts():
+    """DSV3 layer in MXFP8, forward + backward as the benchmark runs it; for the coldest and the
+    hottest expert the oracle recomputes that expert's rows on their own (rows in schedule order,
+    so that the 32-row quantisation blocks match): sampled rows of dW2 and dW13 and the gate
+    gradients of the expert's rows.  Plus bitwise determinism of every gradient."""
+    shape = W.DSV3_MXFP8
+    inp = W.make_inputs(shape, seed=0, device="cuda")
+    desc = mok.desc_from_shape(shape)
+    wq = mok.quantize_weights(desc, inp["w13"], inp["w2"])
+    wb = mok.quantize_weights_backward(desc, inp["w13"], inp["w2"])
+    outs = []
+    for _ in range(2):
+        layer = mok.MoELayer(desc)
+        y = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        mok.moe_forward_mxfp8(desc, inp["x"], inp["w_router"], None, None, wq, y, layer.ctx, layer.ws)
+        g = layer.backward_mxfp8(inp["dy"], inp["x"], inp["w_router"], wb)
+        torch.cuda.synchronize()
+        assert layer.status() == (0, 0)
+        outs.append(g)
+    for name in ("dx", "dw_router", "dw13", "dw2", "dgates"):
+        assert torch.equal(outs[0][name], outs[1][name]), name
+    g = outs[0]
+    r = O.route(to_f64(inp["x"]), to_f64(inp["w_router"]), None, shape.router, shape.k, shape.renorm)
+    assert np.array_equal(layer.view("topk_idx").cpu().numpy(), r["topk_idx"])
+    counts = np.bincount(r["topk_idx"].reshape(-1), minlength=shape.E)
+    I = shape.I
+    for e in (int(np.argmin(counts)), int(np.argmax(counts))):
+        toks, js = np.nonzero(r["topk_idx"] == e)          # ascending tokens = the expert's row order
+        sel = torch.tensor(toks, device="cuda")
+        x = to_f64(inp["x"][sel])
+        dy = to_f64(inp["dy"][sel])
+        gs = r["gates"][toks, js]
+        w13 = to_f64(inp["w13"][e])
+        w2 = to_f64(inp["w2"][e])
+        hu = q(x, 1) @ q(w13, 1).T
+        h, u = hu[:, :I], hu[:, I:]
+        a = O.silu(h) * u
+        dA_p = q(dy, 1) @ q(w2, 0)
+        dg = np.einsum("ri,ri->r", dA_p, a)
+        dA = gs[:, None] * dA_p
+        dhu = np.concatenate([dA * u * O.dsilu(h), dA * O.silu(h)], axis=1)
+        rng = np.random.default_rng(e)
+        rows2 = rng.choice(shape.H, size=32, replace=False)
+        rows13 = rng.choice(2 * I, size=32, replace=False)
+        dw2 = q(gs[:, None] * dy, 0)[:, rows2].T @ q(a, 0)          # [rows][I]
+        dw13 = q(dhu, 0)[:, rows13].T @ q(x, 0)                     # [rows][H]
+        got2 = to_f64(g["dw2"][e][torch.tensor(rows2, device="cuda")])
+        got13 = to_f64(g["dw13"][e][torch.tensor(rows13, device="cuda")])
+        gotg = g["dgates"].cpu().numpy()[toks, js]
+        for name, got, want in (("dw2", got2, dw2), ("dw13", got13, dw13), ("dgates", gotg, dg)):
+            _, _, fro = err_stats(got, want)
+            print("expert %d %s: rel fro %.3e" % (e, name, fro))
+            assert fro <= MX_FRO, (e, name, fro)
