@@ -191,6 +191,32 @@ def sample_desc(T, E):
             f"seeded CPU draws; tokens/s = {T} / seconds")
 
 
+# ---- replicas (bench.py --gpus N under torchrun): one independent layer per GPU, no collective
+# on the data path; the ranks only meet at barriers around the timed region and to take the
+# slowest rank's time, and the whole-job rate counts every rank's tokens.
+
+def replica_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def replica_max(value, world, device):
+    """The largest value over the ranks (every rank gets it)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank, world, ms_per_step):
+    """tokens/s of the whole job: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -242,15 +268,10 @@ def run_mok(args, rank, world, local_rank):
         layer.backward(dy, x, wr, w13, w2, out=grads)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        replica_barrier(world)
 
     def max_over_ranks(v):
-        if world > 1:
-            t = torch.tensor([v], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return v
+        return replica_max(v, world, dev)
 
     for _ in range(args.warmup):
         step()
@@ -360,9 +381,9 @@ def run_mok(args, rank, world, local_rank):
         mxb_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
         if mx_layer.status() != (0, 0):
             raise RuntimeError("device status set in the MXFP8 backward")
-        mx = {"fwd_ms": round(mx_ms, 4), "tokens_per_s": round(T * world / (mx_ms * 1e-3), 1),
+        mx = {"fwd_ms": round(mx_ms, 4), "tokens_per_s": round(whole_job_rate(T, world, mx_ms), 1),
               "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mx_trace.items()},
-              "fwd_bwd_ms": round(mxb_ms, 4), "fwd_bwd_tokens_per_s": round(T * world / (mxb_ms * 1e-3), 1),
+              "fwd_bwd_ms": round(mxb_ms, 4), "fwd_bwd_tokens_per_s": round(whole_job_rate(T, world, mxb_ms), 1),
               "fwd_bwd_kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mxb_trace.items()},
               "weights": "forward: E4M3 + E8M0 per 32 along K (11.3 GB); backward: W2 along H and W13 along "
                          "2I, stored as exact bf16 values (22.5 GB); activations and gradients quantised "
@@ -410,7 +431,7 @@ def run_mok(args, rank, world, local_rank):
 
     step_bytes = 2 * T * H * 2
     line = {
-        "metric": METRIC, "value": round(T * world / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(whole_job_rate(T, world, ms), 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
@@ -420,7 +441,7 @@ def run_mok(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass)",
                    "expert_rows_min_max": [int(counts.min()), int(counts.max())]},
-        "fwd_tokens_per_s": round(T * world / (fwd_ms * 1e-3), 1), "fwd_ms": round(fwd_ms, 4),
+        "fwd_tokens_per_s": round(whole_job_rate(T, world, fwd_ms), 1), "fwd_ms": round(fwd_ms, 4),
         "tflops_fwd_bwd": round(W.algorithmic_flops(shp, "fwd+bwd") / (ms * 1e-3) / 1e12, 1),
         "grouped_gemm": {"tflops_fwd_bwd": round(gemm_tflops, 1),
                          "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
@@ -429,7 +450,7 @@ def run_mok(args, rank, world, local_rank):
                          "peak": peaks["bf16_tflops_sustained"], "peak_source": peak_kind + " (sustained)"},
         "roofline": roofline,
         "kernels": per_kernel,
-        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": step_bytes,
+        "e2e": {"value": round(whole_job_rate(T, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": step_bytes,
                 "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step"},
         "mxfp8_fwd": mx,
