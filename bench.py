@@ -390,6 +390,21 @@ def run_mok(args, rank, world, local_rank):
                          "along each GEMM's reduction"}
         del mx_layer, wq, wb
 
+    # ---- the same weights at T=16384 (512 rows per expert): the forward GEMMs become
+    #      tensor-bound; their fraction of the measured bf16 peak is graded there
+    tb = None
+    if not args.no_tensor_bound:
+        shp_tb = W.RING
+        g = torch.Generator(device=dev).manual_seed(12345 + rank)
+        x_tb = torch.randn((shp_tb.T, H), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        tb_ms, tb_kernels, tb_grouped, tb_layer, _ = tensor_bound_forward(shp_tb, x_tb, wr, w13, w2, args.steps,
+                                                                         args.warmup, GEMM_FLAGS[args.gemm])
+        tb = {"workload": shp_tb.name + " (same weights, x ~ N(0, 1))", "fwd_ms": round(tb_ms, 4),
+              "tokens_per_s": round(whole_job_rate(shp_tb.T, world, tb_ms), 1),
+              "grouped_gemm": tb_grouped,
+              "kernels": {n: v for n, v in tb_kernels.items()}}
+        del tb_layer, x_tb
+
     if rank != 0:
         return
     peaks, peak_kind = load_peaks()
@@ -454,11 +469,68 @@ def run_mok(args, rank, world, local_rank):
                 "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step"},
         "mxfp8_fwd": mx,
+        "tensor_bound_fwd": tb,
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def tensor_bound_forward(shp, x, w_router, w13, w2, steps, warmup, flags=0):
+    """The plain forward at a tensor-bound shape (512 rows per expert): K forwards timed between
+    CUDA events after W warm-ups, then K more with the per-kernel trace, SM clocks sampled
+    throughout.  Returns (ms per forward, per-kernel dict, grouped-GEMM dict, layer, y)."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import _native as N
+
+    y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16, device=x.device)
+    stream = torch.cuda.current_stream()
+    layer = mok.MoELayer(mok.desc_from_shape(shp, flags=flags), device=x.device)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(warmup):
+        layer.forward(x, w_router, w13, w2, y=y)
+    torch.cuda.synchronize()
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set during warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        layer.forward(x, w_router, w13, w2, y=y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    N.trace_start(16 * steps + 16)
+    for _ in range(steps):
+        layer.forward(x, w_router, w13, w2, y=y)
+    torch.cuda.synchronize()
+    trace = N.trace_stop()
+    clocks = sampler.stop()
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set")
+    peaks, peak_kind = load_peaks()
+    kf = kernel_flops(shp)
+    kernels = {}
+    for name, t in trace.items():
+        avg = t["total_ms"] / t["launches"]
+        kernels[name] = {"avg_ms": round(avg, 4)}
+        if name in kf:
+            kernels[name]["TFLOPs"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
+    fwd_gemm = [n for n in ("gemm1_swiglu", "gemm2") if n in trace]
+    g_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in fwd_gemm)
+    g_tf = sum(kf[n] for n in fwd_gemm) / (g_ms * 1e-3) / 1e12
+    # the GEMMs run inside back-to-back forwards (a long step): the sustained (power-capped)
+    # measured peak is the denominator; the burst one is given too, with the SM clocks seen
+    grouped = {"kernels": fwd_gemm, "ms": round(g_ms, 4), "tflops": round(g_tf, 1),
+               "frac_bf16_peak_sustained": round(g_tf / peaks["bf16_tflops_sustained"], 4),
+               "peak_sustained": peaks["bf16_tflops_sustained"],
+               "frac_bf16_peak": round(g_tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
+               "peak_source": peak_kind, "flops": "algorithmic: 2*R*2I*H (GEMM1) + 2*R*H*I (GEMM2)",
+               "clocks": clocks}
+    return ms, kernels, grouped, layer, y
 
 
 def run_ring_sweep(args):
@@ -473,8 +545,11 @@ def run_ring_sweep(args):
     mok.load()
     shp = W.RING
     inp = W.make_inputs(shp, seed=0, device="cuda", with_dy=False)
-    y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
+    plain_ms, kernels, grouped, plain, y = tensor_bound_forward(shp, inp["x"], inp["w_router"], inp["w13"], inp["w2"],
+                                                                args.steps, args.warmup, GEMM_FLAGS[args.gemm])
+    y_plain = y.clone()
+    del plain
 
     def time_forward(layer):
         for _ in range(args.warmup):
@@ -492,40 +567,6 @@ def run_ring_sweep(args):
             raise RuntimeError("device status set")
         return e0.elapsed_time(e1) / args.steps
 
-    plain = mok.MoELayer(mok.desc_from_shape(shp, flags=GEMM_FLAGS[args.gemm]))
-    sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
-    plain_ms = time_forward(plain)
-    y_plain = y.clone()
-    # Per-kernel times of the plain forward (CUDA events around each launch, one more pass of
-    # K forwards) and the tensor-core fraction of its grouped GEMMs.
-    from mixture_experts_layer_table_gb300 import _native as N
-    N.trace_start(16 * args.steps + 16)
-    for _ in range(args.steps):
-        plain.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
-    torch.cuda.synchronize()
-    trace = N.trace_stop()
-    clocks = sampler.stop()
-    del plain
-    peaks, peak_kind = load_peaks()
-    kf = kernel_flops(shp)
-    kernels = {}
-    for name, t in trace.items():
-        avg = t["total_ms"] / t["launches"]
-        kernels[name] = {"avg_ms": round(avg, 4)}
-        if name in kf:
-            kernels[name]["TFLOPs"] = round(kf[name] / (avg * 1e-3) / 1e12, 1)
-            kernels[name]["frac_bf16_peak"] = round(kf[name] / (avg * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)
-    fwd_gemm = [n for n in ("gemm1_swiglu", "gemm2") if n in trace]
-    g_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in fwd_gemm)
-    g_tf = sum(kf[n] for n in fwd_gemm) / (g_ms * 1e-3) / 1e12
-    # the GEMMs run inside back-to-back 13 ms forwards: both the burst and the sustained
-    # (power-capped) measured peaks are given, with the SM clocks seen meanwhile
-    grouped = {"kernels": fwd_gemm, "ms": round(g_ms, 4), "tflops": round(g_tf, 1),
-               "frac_bf16_peak": round(g_tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
-               "peak_source": peak_kind + " (burst)",
-               "frac_bf16_peak_sustained": round(g_tf / peaks["bf16_tflops_sustained"], 4),
-               "peak_sustained": peaks["bf16_tflops_sustained"], "clocks": clocks}
     sweep = {}
     for m in W.RING_MINIBATCHES:
         layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES))
@@ -559,6 +600,8 @@ def main():
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")
+    ap.add_argument("--no-tensor-bound", action="store_true",
+                    help="skip the forward at T=16384 (tensor-bound grouped GEMMs)")
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",

@@ -24,6 +24,9 @@ ONE = W.MoEShape("T1_H256_E1_I256_top1_softmax", T=1, H=256, E=1, I=256, k=1, ro
                  renorm=False, x_std=1.0, w_std=0.05)
 DENSE = W.MoEShape("dense_T300_H256_E1_I512_top1", T=300, H=256, E=1, I=512, k=1, router=W.ROUTER_SOFTMAX,
                    renorm=False, x_std=1.0, w_std=0.05)
+# the largest expert count and top-k the ABI accepts: 1024 experts (most with 0-8 rows), top-16
+MAXES = W.MoEShape("max_T200_H256_E1024_I256_top16_sigmoid", T=200, H=256, E=1024, I=256, k=16,
+                   router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.05)
 
 
 def _skewed_topk(T, E, k, seed, empty=(3, 9)):
@@ -114,7 +117,8 @@ def test_router_topk_and_gates(shape):
 
 # ----------------------------------------------------------------------------- forward / backward
 
-CASES = [(TINY, None), (MID, None), (MID_SKEW, None), (MID, "skewed_given"), (ONE, None), (DENSE, None)]
+CASES = [(TINY, None), (MID, None), (MID_SKEW, None), (MID, "skewed_given"), (ONE, None), (DENSE, None),
+         (MAXES, None)]
 
 
 @pytest.mark.parametrize("shape,mode", CASES, ids=lambda c: getattr(c, "name", str(c)))
