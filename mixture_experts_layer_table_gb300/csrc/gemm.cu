@@ -49,17 +49,6 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Output map of a weight gradient stored as out[E][N][M] (M contiguous), 32 x 32 boxes, no swizzle.
-bool tmap_wgrad_out(CUtensorMap* m, void* base, uint64_t M, uint64_t N, uint64_t E, bool f32) {
-  const uint64_t es = f32 ? 4 : 2;
-  const uint64_t dims[3] = {M, N, E};
-  const uint64_t strides[2] = {M * es, M * N * es};
-  const uint32_t box[3] = {32, 32, 1};
-  return make_tmap(m, base, 3, dims, strides, box,
-                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
 // Store map of a row-major output [rows][cols]: 32 x 32 boxes, fp32 with 128B swizzle (128-byte
 // box rows) or bf16 with 64B swizzle (64-byte box rows), as the epilogue stages them.
 bool tmap_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool f32) {
@@ -288,8 +277,6 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   const bool split = a_lo != nullptr || b_lo != nullptr;
   const bool stat_a = a_lo != nullptr || !split;
   (void)WBN;
-  CUtensorMap to;
-  if (!tmap_wgrad_out(&to, dw, M, N, E, out_f32 != 0)) return cudaErrorInvalidValue;
   WgradArgs g;
   g.M = M;
   g.N = N;
@@ -304,7 +291,7 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   auto run = [&](auto kern) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_smem_bytes(1024));
     if (err != cudaSuccess) return err;
-    kern<<<grid, WG_THREADS, smem, st>>>(ta, ta2, tb, tb2, to, g);
+    kern<<<grid, WG_THREADS, smem, st>>>(ta, ta2, tb, tb2, g);
     return cudaGetLastError();
   };
   static_assert(wgrad_smem_bytes(1024) <= 232448, "shared memory budget");

@@ -10,10 +10,14 @@
 // 48 KB.  Experts with more rows than the stationary region holds (3 K blocks = 192 rows) are
 // done tile by tile with the stationary K blocks reloaded in chunks.
 //
-// Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (TMEM -> shared staging -> TMA store, the
-// output transposed so that m is contiguous).  All waits are bounded; the rows past an expert's
-// end inside its last K block are zeroed in the stationary operand before the MMAs read it
-// (the streaming operand's rows there then multiply zeros).
+// Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (TMEM -> registers, the accumulator released
+// at once, then coalesced stores: the output is transposed so that the 32 lanes of a warp, 32
+// consecutive m, write one 128-byte line per column).  The shared memory left by the stationary
+// operand goes to a deep ring for the streaming operand: with only a few small K blocks per
+// tile, the loads in flight, not the MMAs, bound the main loop (measured: 3 stages of 16 KB held
+// the dW13 main loop at 4.6 ms on its own at the DSV3 layer).  All waits are bounded; the rows
+// past an expert's end inside its last K block are zeroed in the stationary operand before the
+// MMAs read it (the streaming operand's rows there then multiply zeros).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -25,8 +29,7 @@ constexpr int WG_BK = 64;                    // rows per K block
 constexpr int WG_KSTAT = 3;                  // K blocks the stationary region holds
 constexpr int WG_STAT_SLOT = 4 * 8192;       // one K block of the stationary pair: hi (2 atoms), lo (2 atoms)
 constexpr int WG_STAGE = 2 * 8192;           // one K block of the streaming operand (2 atoms)
-constexpr int WG_STAGES = 3;
-constexpr int WG_STG = 4 * 4 * 4096;         // epilogue staging: 4 warps x 4 blocks of 32 x 32 fp32
+constexpr int WG_STAGES = 7;
 constexpr int WG_THREADS = 192;
 
 struct WgradArgs {
@@ -37,8 +40,7 @@ struct WgradArgs {
 };
 
 __host__ __device__ constexpr size_t wgrad_smem_bytes(int E) {
-  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(WG_STAGES) * WG_STAGE + WG_STG + 1024 + 256 +
-         size_t(E + 1) * 4;
+  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(WG_STAGES) * WG_STAGE + 1024 + 256 + size_t(E + 1) * 4;
 }
 
 // STAT_A: A is the stationary pair (tmA hi, tmA2 lo), strips walk n; otherwise B is (tmB, tmB2)
@@ -48,17 +50,16 @@ template <bool STAT_A, bool OUT_F32, bool STAT_SPLIT = true>
 __global__ void __launch_bounds__(WG_THREADS, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                  const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
-                 const __grid_constant__ CUtensorMap tmO, const WgradArgs args) {
+                 const WgradArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stat = smem;                                   // WG_KSTAT slots
   uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WG_STAGES stages
-  uint8_t* staging = ring + WG_STAGES * WG_STAGE;         // WG_STG
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + WG_STG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + WG_STAGES * WG_STAGE);
   // bars: full[S], empty[S], tfull[2], tempty[2], stat_full, stat_empty, drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WG_STAGES + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(staging + WG_STG + 256);
+  int* s_off = reinterpret_cast<int*>(ring + WG_STAGES * WG_STAGE + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -295,7 +296,6 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     const int quarter = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint8_t* stg = staging + (warp - 2) * (4 * 4096);
     bool ok = true;
     for (int s = blockIdx.x; s < total && ok; s += gridDim.x) {
       int e, f, row0, rows, nkb;
@@ -326,37 +326,24 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tacc + c * 32, v[c]);
         tmem_wait_ld();
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (OUT_F32) {
-            float* sb = reinterpret_cast<float*>(stg + c * 4096);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __uint_as_float(v[c][j]);
-          } else {
-            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg + c * 4096);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sb[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(v[c][j]));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_store_3d(&tmO, smem_u32(stg + c * 4096), m * 128 + quarter * 32, n * 128 + c * 32, e);
-          bulk_commit_group();
-        }
+        // the accumulator is in registers: hand it back to the MMA before storing
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+        // out[e][n*128 + col][m*128 + quarter*32 + lane]
+        const size_t base = (size_t)e * args.M * args.N + (size_t)(n * 128) * args.M + m * 128 + quarter * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const size_t idx = base + (size_t)(c * 32 + j) * args.M;
+            if (OUT_F32) reinterpret_cast<float*>(args.out)[idx] = __uint_as_float(v[c][j]);
+            else reinterpret_cast<__nv_bfloat16*>(args.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[c][j]));
+          }
       }
     }
-    if (lane == 0) bulk_wait_group_all();
-    __syncwarp();
   }
 
   tc_fence_before();
