@@ -132,7 +132,9 @@ struct GemmCfg {
   // ROWS / DGRAD fp32 and SwiGLU outputs leave through TMA stores from one 4 KB buffer per
   // epilogue warp
   static constexpr bool kTmaEpi = (MODE == MODE_ROWS || MODE == MODE_DGRAD) && (EPI == EPI_F32 || EPI == EPI_SWIGLU);
-  static constexpr int STG_BYTES = (MODE == MODE_WGRAD) ? 4 * (BN / 32) * 4096 : kTmaEpi ? 4 * 4096 : 0;
+  static constexpr int STG_BYTES = (MODE == MODE_WGRAD)                        ? 4 * (BN / 32) * 4096
+                                   : (kTmaEpi || EPI == EPI_SWIGLU_BWD) ? 4 * 4096
+                                                                        : 0;
   static constexpr int RING = (kBmx || MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
   static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
   static constexpr int ACC_COLS = BN;
@@ -443,6 +445,89 @@ __device__ __forceinline__ void epi_swiglu_tma(uint32_t tacc, long long row0, in
         }
       }
     }
+  }
+}
+
+// SwiGLU backward epilogue with the columns on the lanes.  The accumulator dA' = dY_g W2[e] comes
+// out of TMEM one row per thread; each 32 x 32 block goes through a 128B-swizzled 4 KB buffer and
+// is read back so that 8 lanes share a row and each lane takes 4 consecutive columns: the loads
+// of h | u (16 bytes a lane) and the six bf16 outputs (dh, du, g*a as hi / lo; 8 bytes a lane)
+// then touch 4 rows per instruction instead of 32.  out0/out1: dh|du hi/lo [R][2I]; out2/out3:
+// g*a hi/lo [R][I]; out4: the row's partial gate gradient <dA', a> over this tile's columns.
+__device__ __forceinline__ uint2 pack_bf16x4(const float (&v)[4]) {
+  return make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_bwd_cols(uint32_t tacc, long long row0, int nvalid, int n,
+                                                    const GemmArgs& args, uint8_t* stg, int lane) {
+  const int I = args.I;
+  const int sub = lane >> 3;   // row within each group of 4
+  const int q = lane & 7;      // 4-column group within the 32-column block
+  const float g_lane = lane < nvalid ? args.gate_row[row0 + lane] : 0.0f;  // gate of row `lane`
+  float dgacc[8];              // rows sub, sub+4, ..., sub+28
+#pragma unroll
+  for (int i = 0; i < 8; ++i) dgacc[i] = 0.0f;
+  __nv_bfloat16* dhu_hi = reinterpret_cast<__nv_bfloat16*>(args.out0);
+  __nv_bfloat16* dhu_lo = reinterpret_cast<__nv_bfloat16*>(args.out1);
+  __nv_bfloat16* ga_hi = reinterpret_cast<__nv_bfloat16*>(args.out2);
+  __nv_bfloat16* ga_lo = reinterpret_cast<__nv_bfloat16*>(args.out3);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tacc + c * 32, v);
+    tmem_wait_ld();
+    __syncwarp();  // the previous block has been read back
+    stage_f32_sw128(stg, v, lane);
+    __syncwarp();
+    const int col = n * BN + c * 32 + 4 * q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + sub;
+      const float g = __shfl_sync(0xffffffffu, g_lane, r);
+      if (r < nvalid) {
+        const float4 dap4 = *reinterpret_cast<const float4*>(stg + r * 128 + ((q ^ (r & 7)) << 4));
+        const long long row = row0 + r;
+        const float4 h4 = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + col);
+        const float4 u4 = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + I + col);
+        const float dap[4] = {dap4.x, dap4.y, dap4.z, dap4.w};
+        const float hv[4] = {h4.x, h4.y, h4.z, h4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+        float dh[4], du[4], ga[4], dh_l[4], du_l[4], ga_l[4];
+#pragma unroll
+        for (int z = 0; z < 4; ++z) {
+          const float sg = 1.0f / (1.0f + __expf(-hv[z]));
+          const float sl = hv[z] * sg;
+          const float a = sl * uv[z];
+          dgacc[i] = fmaf(dap[z], a, dgacc[i]);
+          const float dA = g * dap[z];
+          const float vdh = dA * uv[z] * sg * (1.0f + hv[z] * (1.0f - sg));
+          const float vdu = dA * sl;
+          const float vga = g * a;
+          dh[z] = __bfloat162float(__float2bfloat16_rn(vdh));
+          du[z] = __bfloat162float(__float2bfloat16_rn(vdu));
+          ga[z] = __bfloat162float(__float2bfloat16_rn(vga));
+          dh_l[z] = vdh - dh[z];
+          du_l[z] = vdu - du[z];
+          ga_l[z] = vga - ga[z];
+        }
+        *reinterpret_cast<uint2*>(dhu_hi + row * args.ld0 + col) = pack_bf16x4(dh);
+        *reinterpret_cast<uint2*>(dhu_lo + row * args.ld0 + col) = pack_bf16x4(dh_l);
+        *reinterpret_cast<uint2*>(dhu_hi + row * args.ld0 + I + col) = pack_bf16x4(du);
+        *reinterpret_cast<uint2*>(dhu_lo + row * args.ld0 + I + col) = pack_bf16x4(du_l);
+        *reinterpret_cast<uint2*>(ga_hi + row * args.ld1 + col) = pack_bf16x4(ga);
+        *reinterpret_cast<uint2*>(ga_lo + row * args.ld1 + col) = pack_bf16x4(ga_l);
+      }
+    }
+  }
+  // each row's sum over its 8 lanes (fixed butterfly order); lane q == 0 of the group writes
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float s = dgacc[i];
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    const int r = 4 * i + sub;
+    if (q == 0 && r < nvalid) reinterpret_cast<float*>(args.out4)[(row0 + r) * args.ld2 + n] = s;
   }
 }
 
@@ -949,77 +1034,8 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
           }
         }
       } else {  // EPI_SWIGLU_BWD
-        // accumulator = dA' = dY_g W2[e] for intermediate columns n*BN .. n*BN+BN-1.
-        // out0/out1: dh|du hi/lo [R][2I]; out2/out3: g*a hi/lo [R][I]; out4: dg partials.
-        const float g = valid ? args.gate_row[row] : 0.0f;
-        const float* hu_row = args.hu + row * (long long)(2 * args.I);
-        __nv_bfloat16* dhu_hi = reinterpret_cast<__nv_bfloat16*>(args.out0) + row * args.ld0;
-        __nv_bfloat16* dhu_lo = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld0;
-        __nv_bfloat16* ga_hi = reinterpret_cast<__nv_bfloat16*>(args.out2) + row * args.ld1;
-        __nv_bfloat16* ga_lo = reinterpret_cast<__nv_bfloat16*>(args.out3) + row * args.ld1;
-        float dg = 0.0f;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, v);
-          tmem_wait_ld();
-          if (valid) {
-            const int col = t.n * BN + c * 32;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              float hv[16], uv[16];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float4 h4 = reinterpret_cast<const float4*>(hu_row + col + half * 16)[j];
-                const float4 u4 = reinterpret_cast<const float4*>(hu_row + args.I + col + half * 16)[j];
-                hv[4 * j] = h4.x; hv[4 * j + 1] = h4.y; hv[4 * j + 2] = h4.z; hv[4 * j + 3] = h4.w;
-                uv[4 * j] = u4.x; uv[4 * j + 1] = u4.y; uv[4 * j + 2] = u4.z; uv[4 * j + 3] = u4.w;
-              }
-              uint32_t pdh_hi[8], pdh_lo[8], pdu_hi[8], pdu_lo[8], pga_hi[8], pga_lo[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float r_dh[2], r_du[2], r_ga[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const int idx = 2 * j + q;
-                  const float dap = __uint_as_float(v[half * 16 + idx]);
-                  const float sg = 1.0f / (1.0f + __expf(-hv[idx]));
-                  const float sl = hv[idx] * sg;
-                  const float a = sl * uv[idx];
-                  dg = fmaf(dap, a, dg);
-                  const float dA = g * dap;
-                  r_dh[q] = dA * uv[idx] * sg * (1.0f + hv[idx] * (1.0f - sg));
-                  r_du[q] = dA * sl;
-                  r_ga[q] = g * a;
-                }
-                split_bf16x2(r_dh[0], r_dh[1], pdh_hi[j], pdh_lo[j]);
-                split_bf16x2(r_du[0], r_du[1], pdu_hi[j], pdu_lo[j]);
-                split_bf16x2(r_ga[0], r_ga[1], pga_hi[j], pga_lo[j]);
-              }
-              const int cc = col + half * 16;
-              uint4* o;
-              o = reinterpret_cast<uint4*>(dhu_hi + cc);
-              o[0] = make_uint4(pdh_hi[0], pdh_hi[1], pdh_hi[2], pdh_hi[3]);
-              o[1] = make_uint4(pdh_hi[4], pdh_hi[5], pdh_hi[6], pdh_hi[7]);
-              o = reinterpret_cast<uint4*>(dhu_lo + cc);
-              o[0] = make_uint4(pdh_lo[0], pdh_lo[1], pdh_lo[2], pdh_lo[3]);
-              o[1] = make_uint4(pdh_lo[4], pdh_lo[5], pdh_lo[6], pdh_lo[7]);
-              o = reinterpret_cast<uint4*>(dhu_hi + args.I + cc);
-              o[0] = make_uint4(pdu_hi[0], pdu_hi[1], pdu_hi[2], pdu_hi[3]);
-              o[1] = make_uint4(pdu_hi[4], pdu_hi[5], pdu_hi[6], pdu_hi[7]);
-              o = reinterpret_cast<uint4*>(dhu_lo + args.I + cc);
-              o[0] = make_uint4(pdu_lo[0], pdu_lo[1], pdu_lo[2], pdu_lo[3]);
-              o[1] = make_uint4(pdu_lo[4], pdu_lo[5], pdu_lo[6], pdu_lo[7]);
-              o = reinterpret_cast<uint4*>(ga_hi + cc);
-              o[0] = make_uint4(pga_hi[0], pga_hi[1], pga_hi[2], pga_hi[3]);
-              o[1] = make_uint4(pga_hi[4], pga_hi[5], pga_hi[6], pga_hi[7]);
-              o = reinterpret_cast<uint4*>(ga_lo + cc);
-              o[0] = make_uint4(pga_lo[0], pga_lo[1], pga_lo[2], pga_lo[3]);
-              o[1] = make_uint4(pga_lo[4], pga_lo[5], pga_lo[6], pga_lo[7]);
-            }
-          }
-        }
-        if (valid) reinterpret_cast<float*>(args.out4)[row * args.ld2 + t.n] = dg;
+        epi_swiglu_bwd_cols<BN>(tacc, (long long)t.row0 + quarter * 32, nvalid, t.n, args, staging + (warp - 2) * 4096,
+                                lane);
       }
       tc_fence_before();
       __syncwarp();
