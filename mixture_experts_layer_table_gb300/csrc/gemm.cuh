@@ -474,13 +474,26 @@ __device__ __forceinline__ void epi_swiglu_bwd_cols(uint32_t tacc, long long row
   __nv_bfloat16* ga_lo = reinterpret_cast<__nv_bfloat16*>(args.out3);
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
+    const int col = n * BN + c * 32 + 4 * q;
+    // this block's h | u first: their latency overlaps the TMEM load and the transpose
+    float4 h4s[8], u4s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + sub;
+      if (r < nvalid) {
+        const long long row = row0 + r;
+        h4s[i] = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + col);
+        u4s[i] = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + I + col);
+      } else {
+        h4s[i] = u4s[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
     uint32_t v[32];
     tmem_ld_32x32b_x32(tacc + c * 32, v);
     tmem_wait_ld();
     __syncwarp();  // the previous block has been read back
     stage_f32_sw128(stg, v, lane);
     __syncwarp();
-    const int col = n * BN + c * 32 + 4 * q;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = 4 * i + sub;
@@ -488,14 +501,14 @@ __device__ __forceinline__ void epi_swiglu_bwd_cols(uint32_t tacc, long long row
       if (r < nvalid) {
         const float4 dap4 = *reinterpret_cast<const float4*>(stg + r * 128 + ((q ^ (r & 7)) << 4));
         const long long row = row0 + r;
-        const float4 h4 = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + col);
-        const float4 u4 = *reinterpret_cast<const float4*>(args.hu + row * 2 * I + I + col);
+        const float4 h4 = h4s[i];
+        const float4 u4 = u4s[i];
         const float dap[4] = {dap4.x, dap4.y, dap4.z, dap4.w};
         const float hv[4] = {h4.x, h4.y, h4.z, h4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
         float dh[4], du[4], ga[4], dh_l[4], du_l[4], ga_l[4];
 #pragma unroll
         for (int z = 0; z < 4; ++z) {
-          const float sg = 1.0f / (1.0f + __expf(-hv[z]));
+          const float sg = __fdividef(1.0f, 1.0f + __expf(-hv[z]));
           const float sl = hv[z] * sg;
           const float a = sl * uv[z];
           dgacc[i] = fmaf(dap[z], a, dgacc[i]);
