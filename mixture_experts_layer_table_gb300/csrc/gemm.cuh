@@ -123,10 +123,19 @@ struct GemmCfg {
   // MXFP8 B: E4M3 bytes [BN][64] and scales [2][BN] after the converted bf16 B tile
   static constexpr int BQ_BYTES = kBmx ? BN * BK : 0;
   static constexpr int BS_BYTES = kBmx ? 1024 : 0;
-  static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES + BQ_BYTES + BS_BYTES;
+  // MXFP8 B (three rings): the stage ring carries only the E4M3 bytes and scales of B (the HBM
+  // stream, 5 deep), released as soon as the converter warps have expanded them; the A tiles
+  // have their own 3-deep ring, filled by a second producer warp; the expanded bf16 B tiles a
+  // 2-deep ring between the converters and the MMA.  With one shared ring (A, E4M3, bf16 B in
+  // each stage, 3 deep) a stage was held from its load through the conversion to the MMA and the
+  // E4M3 stream ran at a fraction of HBM.
+  static constexpr int STAGES_A = kBmx ? 3 : 0;
+  static constexpr int STAGES_C = kBmx ? 2 : 0;
+  static constexpr int STAGE_BYTES = kBmx ? BQ_BYTES + BS_BYTES : A_TILE * A_TILES + B_TILE * B_TILES;
   // bytes TMA delivers into one stage
-  static constexpr int TX_BYTES = kBmx ? A_TILE + BQ_BYTES + 2 * BN : STAGE_BYTES;
-  static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS : 192;
+  static constexpr int TX_BYTES = kBmx ? BQ_BYTES + 2 * BN : STAGE_BYTES;
+  static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS + 32 : 192;
+  static constexpr int A_WARP = 6 + CONVERTER_WARPS;  // MXFP8: the A-tile producer
   // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: one buffer of up
   // to 32 x 32 fp32 per block of a tile, per epilogue warp.
   // ROWS / DGRAD fp32 and SwiGLU outputs leave through TMA stores from one 4 KB buffer per
@@ -135,8 +144,9 @@ struct GemmCfg {
   static constexpr int STG_BYTES = (MODE == MODE_WGRAD)                        ? 4 * (BN / 32) * 4096
                                    : (kTmaEpi || EPI == EPI_SWIGLU_BWD) ? 4 * 4096
                                                                         : 0;
-  static constexpr int RING = (kBmx || MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
-  static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
+  static constexpr int RING = kBmx ? 5 * STAGE_BYTES : (MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
+  static constexpr int STAGES = kBmx ? 5 : (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
+  static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES + STAGES_A * A_TILE + STAGES_C * B_TILE;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
@@ -144,7 +154,7 @@ struct GemmCfg {
     return (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? a.I / 128 : (a.N + BN - 1) / BN;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
-    return size_t(STAGES) * STAGE_BYTES + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+    return size_t(RINGS_BYTES) + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
   }
 };
 
@@ -610,11 +620,14 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // WGRAD output staging (C::STG_BYTES)
+  uint8_t* a_ring = smem + STAGES * STAGE_BYTES;          // MXFP8: A tiles (C::STAGES_A)
+  uint8_t* c_ring = a_ring + C::STAGES_A * A_TILE;        // MXFP8: expanded bf16 B tiles (C::STAGES_C)
+  uint8_t* staging = smem + C::RINGS_BYTES;               // epilogue output staging (C::STG_BYTES)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STG_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  // bars + 2*STAGES+5: conv[STAGES] (MXFP8 B converted), used with SPLIT_BMX
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  // bars + 2*STAGES+5: conv[STAGES] (MXFP8: an expanded B tile is ready, per C slot)
+  // bars + 3*STAGES+5: fullA[STAGES_A], emptyA[STAGES_A], cempty[STAGES_C] (MXFP8)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5 + 2 * C::STAGES_A + C::STAGES_C);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(staging + C::STG_BYTES + 256);
   int* s_toff = s_off + (args.E + 1);
@@ -627,6 +640,9 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
   auto conv_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + 5 + s]); };
+  auto fulla_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + s]); };
+  auto emptya_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + C::STAGES_A + s]); };
+  auto cempty_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + 2 * C::STAGES_A + s]); };
 
   if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
     ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
@@ -639,15 +655,23 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), C::kBmx ? CONVERTER_WARPS : 1);  // MXFP8: the converters release the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
-    if (C::kBmx)
-      for (int s = 0; s < STAGES; ++s) mbar_init(conv_bar(s), CONVERTER_WARPS);  // one arrival per converter warp
+    if (C::kBmx) {
+      for (int s = 0; s < C::STAGES_C; ++s) {
+        mbar_init(conv_bar(s), CONVERTER_WARPS);  // one arrival per converter warp
+        mbar_init(cempty_bar(s), 1);
+      }
+      for (int s = 0; s < C::STAGES_A; ++s) {
+        mbar_init(fulla_bar(s), 1);
+        mbar_init(emptya_bar(s), 1);
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -723,10 +747,11 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
             tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
           } else if ((MODE == MODE_ROWS || MODE == MODE_RING) && C::kBmx) {
-            // MXFP8 weights: E4M3 bytes (tmB) and E8M0 scales (tmB2, [E][K/32][N]) of the B rows
-            const uint32_t sbq = sb + C::B_TILE;
+            // MXFP8 weights: E4M3 bytes (tmB) and E8M0 scales (tmB2, [E][K/32][N]) of the B rows;
+            // the stage holds nothing else (A has its own ring and producer)
+            const uint32_t sbq = sa;
             const uint32_t sbs = sbq + C::BQ_BYTES;
-            tma_load_2d(sa, &tmA, fb, k0, a_row, pol_act);
+            (void)a_row;
             if (EPI == EPI_SWIGLU_MX) {
               tma_load_3d(sbq, &tmB, fb, k0, t.n * 128, t.e, pol_w);
               tma_load_3d(sbq + C::BQ_BYTES / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
@@ -791,6 +816,8 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer
     int stage = 0;
     uint32_t phase = 0;
+    int astage = 0, cstage = 0;  // MXFP8: A ring and expanded-B ring
+    uint32_t aphase = 0, cphase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -809,18 +836,23 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
       const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0)
-          f_ok = mbar_wait(C::kBmx ? conv_bar(stage) : full_bar(stage), phase, abort_flag, args.status,
-                           SITE_GEMM_MMA_FULL);
+        if (lane == 0) {
+          if (C::kBmx) {
+            f_ok = mbar_wait(conv_bar(cstage), cphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+            if (f_ok) f_ok = mbar_wait(fulla_bar(astage), aphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+          } else {
+            f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+          }
+        }
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t* sa_ptr = smem + stage * STAGE_BYTES;
+        uint8_t* sa_ptr = C::kBmx ? a_ring + astage * A_TILE : smem + stage * STAGE_BYTES;
         const uint32_t sa = smem_u32(sa_ptr);
         const uint32_t sa2 = sa + A_TILE;
-        const uint32_t sb = sa + A_TILE * C::A_TILES;
+        const uint32_t sb = C::kBmx ? smem_u32(c_ring + cstage * C::B_TILE) : sa + A_TILE * C::A_TILES;
         const uint32_t sb2 = sb + C::B_TILE;
         int kvalid = BK;
         if (MODE == MODE_WGRAD) {
@@ -855,11 +887,25 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
             if (SPLIT == SPLIT_A) umma_f16(d_tmem, smem_desc_sw128(sa2 + a_off, a_lbo, a_sbo), bdesc, C::IDESC, 1u);
             if (SPLIT == SPLIT_B) umma_f16(d_tmem, adesc, smem_desc_sw128(sb2 + b_off, b_lbo, b_sbo), C::IDESC, 1u);
           }
-          umma_commit(empty_bar(stage));
+          if (C::kBmx) {
+            umma_commit(emptya_bar(astage));
+            umma_commit(cempty_bar(cstage));
+          } else {
+            umma_commit(empty_bar(stage));
+          }
         }
         any_mma = true;
         __syncwarp();
-        if (++stage == STAGES) {
+        if (C::kBmx) {
+          if (++astage == C::STAGES_A) {
+            astage = 0;
+            aphase ^= 1;
+          }
+          if (++cstage == C::STAGES_C) {
+            cstage = 0;
+            cphase ^= 1;
+          }
+        } else if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
@@ -879,6 +925,46 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
       }
       __syncwarp();
     }
+  } else if (C::kBmx && warp == C::A_WARP) {
+    // ------------------------------------------------------------------ MXFP8: A-tile producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      const uint64_t pol_act = l2_policy_evict_last();
+      int st = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int g = cta0; g < total && ok; g += ncta) {
+        const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
+        for (int kb = 0; kb < t.nkb; ++kb) {
+          if (!mbar_wait(emptya_bar(st), ph ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs,
+                         32)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fa = fulla_bar(st);
+          mbar_arrive_expect_tx(fa, A_TILE);
+          tma_load_2d(smem_u32(a_ring + st * A_TILE), &tmA, fa, kb * BK, t.row0, pol_act);
+          ++issued;
+          if (++st == C::STAGES_A) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // Aborted: let the copies already in flight land before the CTA exits.
+        const int outstanding = min(issued, C::STAGES_A);
+        for (int i = 0; i < outstanding; ++i) {
+          if (--st < 0) {
+            st = C::STAGES_A - 1;
+            ph ^= 1;
+          }
+          volatile int no_abort = 0;
+          mbar_wait(fulla_bar(st), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
+        }
+      }
+    }
   } else if (C::kBmx && warp >= 6) {
     // ------------------------------------------------------------------ MXFP8 B converters
     // For every stage the producer fills: E4M3 bytes of B ([BN][64], row-major) and their E8M0
@@ -886,53 +972,69 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
     // t of the 256 converts 16-byte chunks t, t+256, ... (chunk c = row c/4, elements
     // 16*(c%4) .. +15, scale block (c%4)/2).
     const int ct = threadIdx.x - 6 * 32;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
     bool ok = true;
     for (int g = cta0; g < total && ok; g += ncta) {
       const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0)
+        if (lane == 0) {
           f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL, kWaitLimitNs, 32);
+          // the expanded-B slot must have been read by the MMAs of its previous use
+          if (f_ok)
+            f_ok = mbar_wait(cempty_bar(cstage), cphase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_FULL,
+                             kWaitLimitNs, 32);
+        }
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
         }
-        uint8_t* st_base = smem + stage * STAGE_BYTES;
-        uint8_t* b16 = st_base + A_TILE;                    // converted bf16 B
-        const uint8_t* bq = b16 + C::B_TILE;               // E4M3 bytes
-        const uint8_t* bs = bq + C::BQ_BYTES;              // E8M0 scales
-#pragma unroll 2
-        for (int c = ct; c < BN * 4; c += 32 * CONVERTER_WARPS) {
+        uint8_t* b16 = c_ring + cstage * C::B_TILE;                 // expanded bf16 B
+        const uint8_t* bq = smem + stage * STAGE_BYTES;            // E4M3 bytes
+        const uint8_t* bs = bq + C::BQ_BYTES;                      // E8M0 scales
+        // all chunks of this thread at once (loads first), so that their shared-memory latencies overlap
+        constexpr int CHUNKS = BN * 4 / (32 * CONVERTER_WARPS);
+#pragma unroll
+        for (int it = 0; it < CHUNKS; ++it) {
+          const int c = ct + it * 32 * CONVERTER_WARPS;
           const int r = c >> 2;
           const int q = c & 3;
           const int kk = q >> 1;
           const int sidx = (EPI == EPI_SWIGLU_MX) ? ((r >> 7) * 256 + kk * 128 + (r & 127)) : (kk * BN + r);
           const int X = (int)bs[sidx] - 127;
           const uint4 raw = *reinterpret_cast<const uint4*>(bq + r * 64 + q * 16);
-          uint32_t o[8];
+          uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
+          uint4* dst0 = reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4));
+          uint4* dst1 = reinterpret_cast<uint4*>(row_base + (((2 * q + 1) ^ (r & 7)) << 4));
           const uint32_t zero = e4m3_zero_exponent_bytes(raw.x) | e4m3_zero_exponent_bytes(raw.y) |
                                 e4m3_zero_exponent_bytes(raw.z) | e4m3_zero_exponent_bytes(raw.w);
           if (zero == 0u && (unsigned)(X + 120) <= 239u) {
             const uint32_t bias2 = (uint32_t)(120 + X) * 0x00800080u;  // (120 + X) << 7 in both halves
-            e4m3x4_to_bf16x4(raw.x, bias2, o[0], o[1]);
-            e4m3x4_to_bf16x4(raw.y, bias2, o[2], o[3]);
-            e4m3x4_to_bf16x4(raw.z, bias2, o[4], o[5]);
-            e4m3x4_to_bf16x4(raw.w, bias2, o[6], o[7]);
+            uint32_t o0, o1, o2, o3, o4, o5, o6, o7;
+            e4m3x4_to_bf16x4(raw.x, bias2, o0, o1);
+            e4m3x4_to_bf16x4(raw.y, bias2, o2, o3);
+            e4m3x4_to_bf16x4(raw.z, bias2, o4, o5);
+            e4m3x4_to_bf16x4(raw.w, bias2, o6, o7);
+            *dst0 = make_uint4(o0, o1, o2, o3);
+            *dst1 = make_uint4(o4, o5, o6, o7);
           } else {
-            e4m3x16_to_bf16x16_slow(raw, X, o);
+            e4m3x16_to_bf16x16_slow(raw, X, dst0, dst1);
           }
-          uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
-          *reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(row_base + (((2 * q + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(conv_bar(stage));
+        if (lane == 0) {
+          mbar_arrive(conv_bar(cstage));  // the expanded tile is ready for the MMA
+          mbar_arrive(empty_bar(stage));  // the E4M3 stage has been read: the producer may refill it
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++cstage == C::STAGES_C) {
+          cstage = 0;
+          cphase ^= 1;
         }
       }
     }

@@ -66,16 +66,21 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t bias2, uin
 }
 
 // Slow path for a 16-byte chunk that holds a zero / subnormal or has an extreme scale (kept
-// out of line so that the common path is a real branch, not a predicated copy of this one).
-static __device__ __noinline__ void e4m3x16_to_bf16x16_slow(uint4 raw, int X, uint32_t* o) {
+// out of line so that the common path is a real branch, not a predicated copy of this one): the
+// 16 values, times 2^X, as bf16 into dst0 (elements 0-7) and dst1 (elements 8-15).  It stores
+// them itself so that the common path keeps its values in registers.
+static __device__ __noinline__ void e4m3x16_to_bf16x16_slow(uint4 raw, int X, uint4* dst0, uint4* dst1) {
   const float sc = exp2_int(X);
   const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
+  uint32_t o[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float2 f = f32x2_from_e4m3x2(pairs[j]);
     __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
     o[j] = *reinterpret_cast<uint32_t*>(&b);
   }
+  *dst0 = make_uint4(o[0], o[1], o[2], o[3]);
+  *dst1 = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 // Quantises 32 fp32 values in place to the MX grid (values become e4m3 * 2^X, exactly
