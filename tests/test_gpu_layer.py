@@ -203,7 +203,10 @@ def test_bitwise_deterministic():
 # long expert segments (~750 rows: several 256-row pair tiles and a ragged one per expert)
 LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=768, k=4,
                   router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
-PAIR_CASES = [(LONG, None), (MID, None), (MID, "skewed_given"), (TINY, None), (ONE, None)]
+# skewed long segments: hot experts with several full 256-row blocks, cold ones with only a tail
+LONG_SKEW = LONG.scaled(name="long_skew", skew=True)
+PAIR_CASES = [(LONG, None), (LONG_SKEW, None), (LONG, "skewed_given"), (MID, None), (MID, "skewed_given"),
+              (TINY, None), (ONE, None)]
 
 
 @pytest.mark.parametrize("shape,mode", PAIR_CASES, ids=lambda c: getattr(c, "name", str(c)))
