@@ -479,7 +479,7 @@ def run_mok(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
         "config": {"workload": shp.name, "T": T, "hidden": H, "experts": E, "intermediate": I, "top_k": k,
-                   "forward_gemm": args.gemm,
+                   "expert_gemm": args.gemm,
                    "router": "sigmoid+renorm", "passes": "fwd+bwd",
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "inputs larger than L2 (22.5 GB of expert weights streamed per pass)",
@@ -610,7 +610,7 @@ def run_ring_sweep(args):
             "ms_per_step": best["fwd_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
             "config": {"workload": shp.name, "ring_bytes": W.RING_BYTES, "comm_sms": 8, "passes": "fwd",
-                       "forward_gemm": args.gemm,
+                       "expert_gemm": args.gemm,
                        "min_minibatch_two_waves": mok.min_minibatch(0, shp.I)},
             "plain_forward_ms": round(plain_ms, 4), "plain_forward_kernels": kernels,
             "grouped_gemm_fwd": grouped, "sweep": sweep}
@@ -634,7 +634,8 @@ def main():
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",
-                    help="forward expert GEMMs on CTA pairs or single CTAs (default: the library's choice)")
+                    help="expert GEMM kernels: pair / single = the row-tile kernels on CTA pairs / single "
+                         "CTAs; auto = the library's default (narrow-segment pair kernel for GEMM2 and dX_g)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
                     help="dsv3: the benchmarked layer; dsv3_e16_t256 / dsv3_e16_t1024: the same "
                          "layer on 16 experts and 256 / 1024 tokens (128 / 512 rows per expert, a few "

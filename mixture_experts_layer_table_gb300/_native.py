@@ -40,8 +40,9 @@ LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
                  "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
-FLAG_GEMM_PAIR = 2     # forward expert GEMMs on CTA pairs (256-row tiles)
-FLAG_GEMM_SINGLE = 4   # forward expert GEMMs on single CTAs (128-row tiles)
+FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
+FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
+# neither: GEMM1 on single CTAs, GEMM2 and dX_g on the narrow-segment pair kernel
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
 

@@ -54,6 +54,15 @@ mok_status check_desc(const mok_layer_desc* d) {
 // a 256-row tile pads each expert's ragged tail twice as much.
 bool gemm_pairs(const mok_layer_desc* d) { return (d->flags & MOK_FLAG_GEMM_PAIR) != 0; }
 
+// GEMM2 and dX_g: by default the narrow-segment pair kernel (the expert's rows are the MMA's N,
+// padded to 16 rows instead of a 128-row tile); MOK_FLAG_GEMM_SINGLE / MOK_FLAG_GEMM_PAIR ask
+// for the row-tile kernels (dX_g has no pair row-tile form and runs on single CTAs then).
+int gemm_variant(const mok_layer_desc* d, bool forward) {
+  if (d->flags & MOK_FLAG_GEMM_PAIR) return forward ? mok::GEMM_ROWS_PAIR : mok::GEMM_ROWS_SINGLE;
+  if (d->flags & MOK_FLAG_GEMM_SINGLE) return mok::GEMM_ROWS_SINGLE;
+  return mok::GEMM_NARROW;
+}
+
 // Two full waves of 128 x 256 GEMM1 output tiles over n_sm SMs, in rows: GEMM1 has 2I columns.
 int32_t min_minibatch_rows(int n_sm, int I) {
   if (n_sm <= 0 || I <= 0) return 0;
@@ -333,7 +342,8 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   }
   // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
-             mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm, gemm_pairs(d), st));
+             mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm,
+                               gemm_variant(d, true), st));
   // 7. weighted merge in fixed order
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
@@ -436,7 +446,7 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                         nullptr, k, a_r, n_sm, st));
   // 4. dX_g = dHU W13[e], W13 quantised along 2I
   MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu_c, nullptr, w13_b, R, H, I, E, offsets, tile_off, dx_g, status,
-                                                n_sm, st));
+                                                n_sm, gemm_variant(d, false), st));
   // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H]
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(a_r, nullptr, I, do_r, nullptr, H, R, E, offsets, dw2, wgrad_f32, status,
                                                n_sm, st));
@@ -555,7 +565,8 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   MOK_LAUNCH("dgrad_swiglu", st, mok::launch_dgrad_swiglu(dy_g, w2, R, H, I, E, offsets, tile_off, hu, gate_row, dhu,
                                                           dhu_lo, gact, gact_lo, dg_part, status, n_sm, st));
   // 3. dX_g = [dh | du] W13[e]
-  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, dhu_lo, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm, st));
+  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, dhu_lo, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm,
+                                                gemm_variant(d, false), st));
   // 4. dW2[e] = (g a)^T dY_g stored as [H][I]; 5. dW13[e] = x_g^T [dh | du] stored as [2I][H];
   //    both reduced over the expert's rows, the contiguous output dimension on the TMEM lanes
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(gact, gact_lo, I, dy_g, nullptr, H, R, E, offsets, dw2, wgrad_f32,

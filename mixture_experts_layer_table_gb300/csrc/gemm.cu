@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "gemm_narrow.cuh"
 #include "gemm_pair.cuh"
 #include "wgrad.cuh"
 #include "kernels.cuh"
@@ -147,8 +148,53 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUten
   return cudaGetLastError();
 }
 
-// Upper bound of the 256-row pair tiles of R expert-sorted rows split into E segments.
+// Upper bound of the 256-row pair tiles of R expert-sorted rows split into E segments (also of
+// the narrow kernel's row chunks).
 int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
+
+// Narrow-segment GEMM on CTA pairs: W (K-major [E][N][K] or, WMN, MN-major [E][K][N]) against
+// expert-sorted rows X [R][K] (hi, and lo when SPLIT; x_lo is ignored otherwise); fp32 out
+// [R][N] (row stride ld).
+template <bool WMN, bool SPLIT, int NMAX>
+cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_lo, int K, GemmArgs args, int R,
+                          int n_sm, cudaStream_t st) {
+  using C = NarrowCfg<WMN, SPLIT, NMAX>;
+  static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
+  CUtensorMap tx, tx2;
+  if (!tmap_2d(&tx, x_hi, K, R, BK, NARROW_XBOX)) return cudaErrorInvalidValue;
+  tx2 = tx;
+  if (SPLIT && !tmap_2d(&tx2, x_lo, K, R, BK, NARROW_XBOX)) return cudaErrorInvalidValue;
+  const int bound = ((R + NMAX - 1) / NMAX + args.E) * C::m_tiles(args);
+  if (R <= 0 || bound <= 0) return cudaSuccess;
+  auto kern = gemm_narrow_kernel<WMN, SPLIT, NMAX>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::smem_bytes(args.E);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs[64] = {0};  // co-resident pairs of this kernel, per device
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    cfg.gridDim = dim3(2 * std::max(1, n_sm / 2), 1, 1);
+    int clusters = 0;
+    if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
+    max_pairs[dev] = std::max(1, clusters);
+  }
+  cfg.gridDim = dim3(2 * std::min(bound, max_pairs[dev]), 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, w, tx, tx2, args);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -196,7 +242,19 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
 
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         bool pair, cudaStream_t st) {
+                         int variant, cudaStream_t st) {
+  const bool pair = variant == GEMM_ROWS_PAIR;
+  if (variant == GEMM_NARROW) {
+    // W2 [E][H][I] K-major, 128-row boxes (one CTA's half of a 256-row weight tile)
+    CUtensorMap tw;
+    if (!tmap_3d(&tw, w2, I, H, E, BK, 128)) return cudaErrorInvalidValue;
+    GemmArgs g = base_args(E, offsets, tile_off, status);
+    g.N = H;
+    g.K = I;
+    g.out0 = out;
+    g.ld0 = H;
+    return launch_narrow<false, true, 256>(tw, act_hi, act_lo, I, g, R, n_sm, st);
+  }
   CUtensorMap ta, ta2, tb;
   if (!tmap_2d(&ta, act_hi, I, R, BK, BM) || !tmap_2d(&ta2, act_lo, I, R, BK, BM) ||
       !tmap_3d(&tb, w2, I, H, E, BK, pair ? 128 : 256))
@@ -242,7 +300,19 @@ cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, 
 
 cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w13, int R, int H, int I, int E,
                            const int32_t* offsets, const int32_t* tile_off, float* dx_g, int* status, int n_sm,
-                           cudaStream_t st) {
+                           int variant, cudaStream_t st) {
+  if (variant == GEMM_NARROW) {
+    // W13[e] [2I][H] as an MN-major W (64 x 64 boxes)
+    CUtensorMap tw;
+    if (!tmap_3d(&tw, w13, H, 2 * I, E, 64, BK)) return cudaErrorInvalidValue;
+    GemmArgs g = base_args(E, offsets, tile_off, status);
+    g.N = H;
+    g.K = 2 * I;
+    g.out0 = dx_g;
+    g.ld0 = H;
+    if (dhu_lo == nullptr) return launch_narrow<true, false, 256>(tw, dhu_hi, nullptr, 2 * I, g, R, n_sm, st);
+    return launch_narrow<true, true, 256>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
+  }
   CUtensorMap ta, ta2, tb;
   // A = dHU [R][2I] (K = 2I) as hi + lo (or a single bf16 tensor when dhu_lo is null);
   // B = W13[e] [2I][H] seen as [K][N] (N = H contiguous)

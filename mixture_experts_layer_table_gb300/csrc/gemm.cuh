@@ -149,6 +149,8 @@ struct GemmCfg {
   static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES + STAGES_A * A_TILE + STAGES_C * B_TILE;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                "tcgen05.alloc takes a power of two from 32 to 512 columns");
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
   static __host__ __device__ int n_tiles(const GemmArgs& a) {
     return (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? a.I / 128 : (a.N + BN - 1) / BN;

@@ -1,0 +1,359 @@
+// Narrow-segment grouped GEMM on CTA pairs (sm_103a): out[r][j] = sum_k X[r][k] W[e][j][k] over
+// the expert-sorted rows r of each expert e, computed transposed: D[j][r] = W[e] X^T.
+//
+// The row-tile kernels (gemm.cuh, gemm_pair.cuh) put an expert's rows on the MMA's M side in
+// tiles of 128 (or 256) rows; with about 128 rows per expert, half the experts spill a few rows
+// into a second tile and the tensor cores spend a third of their work on padding, twice over
+// for a hi / lo operand.  Here the roles swap: 256 weight rows (output columns j) are the M of a
+// tcgen05.mma.cta_group::2 (128 per CTA of the pair) and the expert's rows are its N, a multiple
+// of 16 up to 256, so an expert pads to 16 rows.  An expert with more than 256 rows is cut into
+// equal chunks (multiples of 16).  Per SM and 64-deep K step the pair loads 16 KB of weights and
+// at most 16 KB of rows per operand, against 32 KB of weights + 16 KB per A operand for the
+// single-CTA row tile.  Results are bitwise equal to the row-tile kernels' (same K order, same
+// fp32 accumulation per element).
+//
+//   WMN = false  W K-major  [E][N][K]   (GEMM2: o = a W2[e]^T, K = I)
+//   WMN = true   W MN-major [E][K][N]   (dX_g = dHU W13[e], K = 2I)
+//   SPLIT        X is a bf16 hi / lo pair, two MMAs per K step into the same accumulator
+//
+// Roles (both CTAs): warp 0 TMA producer, warp 1 MMA issuer (even CTA only), warps 2..5 epilogue
+// (tcgen05.ld of 32 rows x 32 columns, then per row one 128-byte store of 32 consecutive
+// columns by the warp).  Barriers as in gemm_pair.cuh: full[s] in the even CTA (one arrival with
+// the bytes of both CTAs), empty[s] and tfull[a] in both CTAs (multicast commits), tempty[a] in
+// the even CTA (8 arrivals).  Tiles (expert e, weight tile m of 256 columns, row chunk c; c
+// fastest, then m, so the pairs running one expert at the same time share its rows and each
+// weight tile in L2) are dealt to the pairs round-robin in a fixed order; every output element
+// is one tile's accumulator, reduced over K in a fixed order.
+#pragma once
+#include "gemm.cuh"
+
+namespace mok {
+
+// One CTA's rows of X arrive as 32-row TMA boxes (4 KB; the last may run into the next expert's
+// rows, which only feed accumulator columns that are not stored).  With 16-row boxes (up to 17
+// boxes per stage) the per-box cost of the copies, not the bytes, bounded the kernel: GEMM2 and
+// dX_g at the DSV3 layer took 1.81 and 3.71 ms, with 32-row boxes 1.64 and 3.10 ms, with 64-row
+// boxes the same as 32, and with a 16-row box for an odd tail 1.68 and 3.31 ms.
+constexpr int NARROW_XBOX = 32;
+
+template <bool WMN, bool SPLIT, int NMAX_>
+struct NarrowCfg {
+  static constexpr int PM = 256;                // weight rows (output columns) of a pair tile
+  static constexpr int NMAX = NMAX_;            // rows of a pair tile at most
+  static_assert((NMAX / 2) % NARROW_XBOX == 0, "the boxes of one CTA's rows fit its X buffer");
+  static constexpr int X_OP = (NMAX / 2) * 128; // one CTA's rows of one X operand x 64 K
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int X_OPS = SPLIT ? 2 : 1;
+  static constexpr int STAGE_BYTES = A_BYTES + X_OPS * X_OP;
+  static constexpr int STAGES = (208 * 1024 / STAGE_BYTES) < 8 ? (208 * 1024 / STAGE_BYTES) : 8;
+  // two accumulators of NMAX columns; tcgen05.alloc takes a power of two from 32 to 512
+  static constexpr int TMEM_COLS = 2 * NMAX <= 256 ? 256 : 512;
+  static_assert(NMAX % 32 == 0 && NMAX >= 32 && 2 * NMAX <= 512, "accumulators must fit the TMEM allocation");
+  static constexpr int THREADS = 192;
+  static __host__ __device__ int m_tiles(const GemmArgs& a) { return (a.N + PM - 1) / PM; }
+  static __host__ __device__ constexpr size_t smem_bytes(int E) {
+    return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+  }
+};
+
+struct NarrowTile {
+  int e, c, m;
+  int nc;    // row chunks of this expert (they share each weight tile)
+  int row0;  // first row of the chunk
+  int rows;  // rows of the chunk (1..256)
+  int n;     // MMA N: rows rounded up to 16
+};
+
+// Rows per chunk of an expert with `cnt` rows cut into `nc` chunks of at most `nmax`: the equal
+// share rounded up to 16 (so only the last chunk pads), or nmax where that would leave the last
+// chunk empty.
+__host__ __device__ __forceinline__ int narrow_chunk(int cnt, int nc, int nmax) {
+  int ch = ((cnt + nc - 1) / nc + 15) & ~15;
+  if ((nc - 1) * ch >= cnt) ch = nmax;
+  return ch;
+}
+
+// Expert e owns tiles [s_coff[e]*MT, s_coff[e+1]*MT) with s_coff the prefix of ceil(rows/nmax);
+// inside an expert the chunks of one weight tile are neighbours, so the pairs that run them at
+// the same time read that weight tile from HBM once.
+__device__ __forceinline__ NarrowTile decode_narrow_tile(int g, int MT, int E, int nmax, const int* s_off,
+                                                         const int* s_coff) {
+  int lo = 0, hi = E;  // largest e with s_coff[e]*MT <= g (the last of equal starts owns tiles)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_coff[mid] * MT <= g) lo = mid; else hi = mid;
+  }
+  NarrowTile t;
+  t.e = lo;
+  const int nc = s_coff[lo + 1] - s_coff[lo];
+  const int cnt = s_off[lo + 1] - s_off[lo];
+  const int local = g - s_coff[lo] * MT;
+  t.nc = nc;
+  t.m = local / nc;
+  t.c = local - t.m * nc;
+  const int ch = narrow_chunk(cnt, nc, nmax);
+  t.row0 = s_off[lo] + t.c * ch;
+  t.rows = min(ch, cnt - t.c * ch);
+  t.n = (t.rows + 15) & ~15;
+  return t;
+}
+
+// tmX / tmX2: X hi / lo in 32-row boxes.
+template <bool WMN, bool SPLIT, int NMAX>
+__global__ void __launch_bounds__(192, 1)
+    gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmX2, const GemmArgs args) {
+  using C = NarrowCfg<WMN, SPLIT, NMAX>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_coff = s_off + (args.E + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int pair = (int)blockIdx.x >> 1;
+  const int npairs = (int)gridDim.x >> 1;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = args.offsets[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < args.E; ++e) {
+      s_coff[e] = acc;
+      acc += (s_off[e + 1] - s_off[e] + C::NMAX - 1) / C::NMAX;
+    }
+    s_coff[args.E] = acc;
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int MT = C::m_tiles(args);
+  const int total = s_coff[args.E] * MT;
+  const int nkb = args.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(&tmX);
+      if (SPLIT) tma_prefetch_desc(&tmX2);
+      const uint64_t pol_rows = l2_policy_evict_last();   // rows: read by every weight tile
+      const uint64_t pol_once = l2_policy_evict_first();  // a weight tile read by one chunk
+      const uint64_t pol_shared = l2_policy_evict_normal();
+      const uint32_t full0_cl = mapa_shared(full_bar(0), 0);  // the even CTA's full barriers
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int g = pair; g < total && ok; g += npairs) {
+        const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+        const int half = t.n >> 1;                      // rows of this CTA's half of N
+        const int nbox = (half + NARROW_XBOX - 1) / NARROW_XBOX;
+        const int xrows = nbox * NARROW_XBOX;           // <= NMAX / 2: fits the X buffer
+        const int x_row = t.row0 + (int)rank * half;
+        const int w_row = t.m * C::PM + 128 * (int)rank;
+        const uint32_t pair_tx = 2u * (C::A_BYTES + C::X_OPS * xrows * 128);
+        const uint64_t pol_w = t.nc > 1 ? pol_shared : pol_once;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait<true>(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
+                               kWaitLimitNs, 32)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0_cl + 8u * stage;
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sx = sa + C::A_BYTES;
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair_tx);
+          const int k0 = kb * BK;
+          if (WMN) {
+            tma_load_3d_pair(sa, &tmW, fb, w_row, k0, t.e, pol_w);
+            tma_load_3d_pair(sa + MN_ATOM_BYTES, &tmW, fb, w_row + 64, k0, t.e, pol_w);
+          } else {
+            tma_load_3d_pair(sa, &tmW, fb, k0, w_row, t.e, pol_w);
+          }
+          for (int b = 0; b < nbox; ++b) {
+            const int r = b * NARROW_XBOX;
+            tma_load_2d_pair(sx + r * 128, &tmX, fb, k0, x_row + r, pol_rows);
+            if (SPLIT) tma_load_2d_pair(sx + C::X_OP + r * 128, &tmX2, fb, k0, x_row + r, pol_rows);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        if (rank == 0) {
+          // Aborted: the even CTA's full barriers count both CTAs' bytes; wait for the stages
+          // it armed so that no copy is still landing when the pair exits.
+          const int outstanding = min(issued, STAGES);
+          int s = stage;
+          uint32_t ph = phase;
+          for (int i = 0; i < outstanding; ++i) {
+            if (--s < 0) {
+              s = STAGES - 1;
+              ph ^= 1;
+            }
+            volatile int no_abort = 0;
+            mbar_wait(full_bar(s), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
+          }
+        } else {
+          // the peer cannot observe its own copies: give those in flight time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 100000ull) __nanosleep(1000);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool any_mma = false;
+      const uint32_t a_lbo = WMN ? MOK_MN_LBO : 16, a_sbo = WMN ? MOK_MN_SBO : 1024;
+      for (int g = pair; g < total && ok; g += npairs) {
+        const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+        const uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = mbar_wait<true>(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * C::NMAX;
+        for (int kb = 0; kb < nkb; ++kb) {
+          int f_ok = 1;
+          if (lane == 0) f_ok = mbar_wait<true>(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+          if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t sx = sa + C::A_BYTES;
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t adesc = smem_desc_sw128(sa + (WMN ? k16 * 2048 : k16 * 32), a_lbo, a_sbo);
+              umma_f16_pair(d_tmem, adesc, smem_desc_sw128(sx + k16 * 32, 16, 1024), idesc,
+                            (kb | k16) != 0 ? 1u : 0u);
+              if (SPLIT) umma_f16_pair(d_tmem, adesc, smem_desc_sw128(sx + C::X_OP + k16 * 32, 16, 1024), idesc, 1u);
+            }
+            umma_commit_pair(empty_bar(stage), 0x3);
+          }
+          any_mma = true;
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit_pair(tfull_bar(acc), 0x3);
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (any_mma) {
+        if (lane == 0) {
+          umma_commit_pair(drain_bar, 0x1);
+          volatile int no_abort = 0;
+          mbar_wait(drain_bar, 0, &no_abort, args.status, SITE_GEMM_DRAIN);
+        }
+        __syncwarp();
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are reachable by this warp
+    const uint32_t tempty0_cl = mapa_shared(tempty_bar(0), 0);
+    float* out = reinterpret_cast<float*>(args.out0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int g = pair; g < total; g += npairs) {
+      const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+      int w_ok = 1;
+      if (lane == 0)
+        w_ok = mbar_wait<true>(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL,
+                               kWaitLimitNs, 256);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+      tc_fence_after();
+      // this thread's output column; the accumulator's columns are the chunk's rows
+      const int j = t.m * C::PM + 128 * (int)rank + 32 * quarter + lane;
+      const bool jv = j < args.N;
+      const uint32_t tacc = tmem_base + acc * C::NMAX + (uint32_t(quarter * 32) << 16);
+      float* o = out + (long long)t.row0 * args.ld0 + j;
+#pragma unroll 1
+      for (int c = 0; c * 32 < t.rows; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tacc + c * 32, v);
+        tmem_wait_ld();
+        const int nr = min(32, t.rows - c * 32);
+        if (jv) {
+          float* oc = o + (long long)(c * 32) * args.ld0;
+          if (nr == 32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nr) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0_cl + 8u * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace mok

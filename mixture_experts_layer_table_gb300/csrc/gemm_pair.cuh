@@ -41,6 +41,8 @@ struct PairCfg {
   // for the staging buffers; GEMM2 keeps 4 x 48 KB
   static constexpr int STAGES = EPI == EPI_SWIGLU ? 5 : 4;
   static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                "tcgen05.alloc takes a power of two from 32 to 512 columns");
   static constexpr uint32_t IDESC = idesc_bf16_f32(PM, BN, false, false);
   static constexpr int THREADS = 192;
   static __host__ __device__ int n_tiles(const GemmArgs& a) {

@@ -37,16 +37,19 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
                                 void* act_lo, int* status, int n_sm, bool pair, cudaStream_t st);
+// Expert GEMM kernels for GEMM2 and dX_g: 128-row tiles on single CTAs, 256-row tiles on CTA
+// pairs (GEMM2 only), or the narrow-segment pair kernel (expert rows as the MMA's N).
+enum GemmVariant { GEMM_ROWS_SINGLE = 0, GEMM_ROWS_PAIR = 1, GEMM_NARROW = 2 };
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         bool pair, cudaStream_t st);
+                         int variant, cudaStream_t st);
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, const float* hu,
                                 const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,
                                 float* dg_part, int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w13, int R, int H, int I, int E,
                            const int32_t* offsets, const int32_t* tile_off, float* dx_g, int* status, int n_sm,
-                           cudaStream_t st);
+                           int variant, cudaStream_t st);
 // dW[e] stored transposed as out[e][n][m] (m = the output's contiguous dimension):
 // out[e][n][m] = sum over rows r of expert e of A[r][m] * B[r][n]; A or B may be a hi/lo pair.
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,

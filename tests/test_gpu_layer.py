@@ -48,9 +48,9 @@ def _lib(cuda_ok):
     mok.load()
 
 
-def _run(shape, inp, given=None):
+def _run(shape, inp, given=None, flags=0):
     dev = _gpu_inputs(inp)
-    layer = mok.MoELayer(mok.desc_from_shape(shape))
+    layer = mok.MoELayer(mok.desc_from_shape(shape, flags=flags))
     given_t = torch.tensor(given, dtype=torch.int32, device="cuda") if given is not None else None
     y = layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"],
                       given_topk=given_t)
@@ -152,6 +152,26 @@ def test_forward_backward_parity(shape, mode):
     assert_bf16_close(to_f64(g["dx"]), bwd["dx"], "dx")
 
 
+@pytest.mark.parametrize("shape,mode", [(MID, None), (MID, "skewed_given"), (TINY, None)],
+                         ids=lambda c: getattr(c, "name", str(c)))
+def test_row_tile_gemms_forward_backward(shape, mode):
+    """MOK_FLAG_GEMM_SINGLE: GEMM2 and dX_g on the 128-row-tile single-CTA kernels instead of the
+    narrow-segment pair kernel; o, y, dX_g and dX against the oracle."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    if mode == "skewed_given":
+        given = _skewed_topk(shape.T, shape.E, shape.k, seed=5)
+    else:
+        given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
+    fwd, bwd = oracle_layer(shape, f64, topk_idx=given)
+    layer, y, g = _run(shape, inp, given=given, flags=N.FLAG_GEMM_SINGLE)
+    assert_intermediate_close(to_f64(layer.view("expert_out")), fwd["o"], "o", rel=1e-3)
+    assert_bf16_close(to_f64(y), fwd["y"], "y")
+    assert_intermediate_close(to_f64(layer.view("dx_g")), bwd["dx_g"], "dx_g", rel=1e-3)
+    assert_bf16_close(to_f64(g["dx"]), bwd["dx"], "dx")
+
+
 @pytest.mark.parametrize("shape", [MID, MID_SKEW], ids=lambda s: s.name)
 def test_bf16_weight_gradients_are_rounded_fp32_ones(shape):
     """MOK_FLAG_WGRAD_BF16 stores dW13 / dW2 in bf16.  The kernels and reduction order are the
@@ -224,7 +244,8 @@ def test_pair_gemm_forward(shape, mode):
     dev = _gpu_inputs(inp)
     given_t = torch.tensor(given, dtype=torch.int32, device="cuda")
     outs = {}
-    for name, flag in (("pair", N.FLAG_GEMM_PAIR), ("single", N.FLAG_GEMM_SINGLE)):
+    # default flags: GEMM2 on the narrow-segment pair kernel (expert rows as the MMA's N)
+    for name, flag in (("pair", N.FLAG_GEMM_PAIR), ("single", N.FLAG_GEMM_SINGLE), ("narrow", 0)):
         layer = mok.MoELayer(mok.desc_from_shape(shape, flags=flag))
         y = layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"],
                           given_topk=given_t)
@@ -241,6 +262,11 @@ def test_pair_gemm_forward(shape, mode):
     assert_bf16_close(to_f64(p["y"]), fwd["y"], "y")
     for name in ("hu", "act", "o", "y"):
         assert torch.equal(p[name], outs["single"][name]), name
+    nw = outs["narrow"]
+    assert_intermediate_close(to_f64(nw["o"]), fwd["o"], "o (narrow)", rel=1e-3)
+    assert_bf16_close(to_f64(nw["y"]), fwd["y"], "y (narrow)")
+    for name in ("hu", "act"):
+        assert torch.equal(nw[name], outs["single"][name]), name
 
 
 # ----------------------------------------------------------------------------- bounded waits
