@@ -635,7 +635,7 @@ def main():
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
     ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",
                     help="expert GEMM kernels: pair / single = the row-tile kernels on CTA pairs / single "
-                         "CTAs; auto = the library's default (narrow-segment pair kernel for GEMM2 and dX_g)")
+                         "CTAs; auto = the library's default (narrow-segment pair kernel: expert rows as the MMA's N)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dsv3",
                     help="dsv3: the benchmarked layer; dsv3_e16_t256 / dsv3_e16_t1024: the same "
                          "layer on 16 experts and 256 / 1024 tokens (128 / 512 rows per expert, a few "

@@ -76,14 +76,13 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                order (0 = mok_min_minibatch(0, I), two full SM waves of GEMM1 tiles)
  *   flags        MOK_FLAG_WGRAD_BF16: the expert weight gradients dw13 / dw2 of
  *                mok_moe_backward are bf16 instead of the default f32.
- *                Expert GEMM kernels.  Default: GEMM1 on single CTAs with 128-row tiles
- *                of an expert's rows; GEMM2 and dX_g on CTA pairs with the expert's rows
- *                as the MMA's N, padded to 16 rows (tcgen05 cta_group::2, 256 weight
- *                rows per pair).  MOK_FLAG_GEMM_PAIR: GEMM1 and GEMM2 on CTA pairs with
- *                256-row tiles of an expert's rows, dX_g on single CTAs with 128-row
- *                tiles.  MOK_FLAG_GEMM_SINGLE: all three on single CTAs with 128-row
- *                tiles.  Results are bitwise the same in every case.  Setting both
- *                flags is an invalid argument.
+ *                Expert GEMM kernels.  Default: GEMM1, GEMM2 and dX_g on CTA pairs with
+ *                the expert's rows as the MMA's N, padded to 16 rows (tcgen05
+ *                cta_group::2, 256 weight rows per pair).  MOK_FLAG_GEMM_PAIR: GEMM1 and
+ *                GEMM2 on CTA pairs with 256-row tiles of an expert's rows, dX_g on
+ *                single CTAs with 128-row tiles.  MOK_FLAG_GEMM_SINGLE: all three on
+ *                single CTAs with 128-row tiles.  Results are bitwise the same in every
+ *                case.  Setting both flags is an invalid argument.
  *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1

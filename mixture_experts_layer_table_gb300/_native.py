@@ -42,7 +42,7 @@ LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "
 FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
 FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
-# neither: GEMM1 on single CTAs, GEMM2 and dX_g on the narrow-segment pair kernel
+# neither: GEMM1, GEMM2 and dX_g on the narrow-segment pair kernel (expert rows as the MMA's N)
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
 

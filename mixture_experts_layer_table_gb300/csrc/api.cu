@@ -49,16 +49,12 @@ mok_status check_desc(const mok_layer_desc* d) {
   return MOK_OK;
 }
 
-// Forward expert GEMMs on CTA pairs (256-row tiles) only on request: measured on GB300 at 128
-// and at 512 rows per expert, the single-CTA GEMMs (128-row tiles) are as fast or faster, since
-// a 256-row tile pads each expert's ragged tail twice as much.
-bool gemm_pairs(const mok_layer_desc* d) { return (d->flags & MOK_FLAG_GEMM_PAIR) != 0; }
-
-// GEMM2 and dX_g: by default the narrow-segment pair kernel (the expert's rows are the MMA's N,
-// padded to 16 rows instead of a 128-row tile); MOK_FLAG_GEMM_SINGLE / MOK_FLAG_GEMM_PAIR ask
-// for the row-tile kernels (dX_g has no pair row-tile form and runs on single CTAs then).
-int gemm_variant(const mok_layer_desc* d, bool forward) {
-  if (d->flags & MOK_FLAG_GEMM_PAIR) return forward ? mok::GEMM_ROWS_PAIR : mok::GEMM_ROWS_SINGLE;
+// Expert GEMM kernels: by default the narrow-segment pair kernel (the expert's rows are the
+// MMA's N, padded to 16 rows instead of a 128-row tile); MOK_FLAG_GEMM_SINGLE / MOK_FLAG_GEMM_PAIR
+// ask for the row-tile kernels (dX_g has no pair row-tile form and runs on single CTAs then).
+enum ExpertGemm { GEMM1 = 0, GEMM2 = 1, DGRAD_X = 2 };
+int gemm_variant(const mok_layer_desc* d, int which) {
+  if (d->flags & MOK_FLAG_GEMM_PAIR) return which == DGRAD_X ? mok::GEMM_ROWS_SINGLE : mok::GEMM_ROWS_PAIR;
   if (d->flags & MOK_FLAG_GEMM_SINGLE) return mok::GEMM_ROWS_SINGLE;
   return mok::GEMM_NARROW;
 }
@@ -307,7 +303,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
     // 5. grouped GEMM1 with the SwiGLU epilogue
     MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
-                                                            status, n_sm, gemm_pairs(d), st));
+                                                            status, n_sm, gemm_variant(d, GEMM1), st));
   } else {
     // 4-5. ring forward: per-minibatch tables, then one persistent launch in which `comm`
     //      CTAs gather minibatches into the ring while the others run GEMM1 on them
@@ -343,7 +339,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
              mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm,
-                               gemm_variant(d, true), st));
+                               gemm_variant(d, GEMM2), st));
   // 7. weighted merge in fixed order
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
@@ -446,7 +442,7 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                         nullptr, k, a_r, n_sm, st));
   // 4. dX_g = dHU W13[e], W13 quantised along 2I
   MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu_c, nullptr, w13_b, R, H, I, E, offsets, tile_off, dx_g, status,
-                                                n_sm, gemm_variant(d, false), st));
+                                                n_sm, gemm_variant(d, DGRAD_X), st));
   // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H]
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(a_r, nullptr, I, do_r, nullptr, H, R, E, offsets, dw2, wgrad_f32, status,
                                                n_sm, st));
@@ -566,7 +562,7 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
                                                           dhu_lo, gact, gact_lo, dg_part, status, n_sm, st));
   // 3. dX_g = [dh | du] W13[e]
   MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu, dhu_lo, w13, R, H, I, E, offsets, tile_off, dx_g, status, n_sm,
-                                                gemm_variant(d, false), st));
+                                                gemm_variant(d, DGRAD_X), st));
   // 4. dW2[e] = (g a)^T dY_g stored as [H][I]; 5. dW13[e] = x_g^T [dh | du] stored as [2I][H];
   //    both reduced over the expert's rows, the contiguous output dimension on the TMEM lanes
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(gact, gact_lo, I, dy_g, nullptr, H, R, E, offsets, dw2, wgrad_f32,

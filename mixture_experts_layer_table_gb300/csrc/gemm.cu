@@ -39,8 +39,9 @@ bool make_tmap(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t d[3], s[2];
-  cuuint32_t b[3], es[3] = {1, 1, 1};
+  if (rank < 1 || rank > 4) return false;
+  cuuint64_t d[4], s[3];
+  cuuint32_t b[4], es[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];
@@ -75,6 +76,15 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
   const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
   const uint32_t box[3] = {b0, b1, 1};
   return make_tmap(m, base, 3, dims, strides, box);
+}
+
+// W13 [E][2I][H] seen as [E][2][I][H]: one box of 64 K x 64 rows x both halves brings 64 gate
+// rows followed by the 64 up rows of the same intermediate indices.
+bool tmap_w13_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t E) {
+  const uint64_t dims[4] = {H, I, 2, E};
+  const uint64_t strides[3] = {H * 2, I * H * 2, 2 * I * H * 2};
+  const uint32_t box[4] = {64, 64, 2, 1};
+  return make_tmap(m, w13, 4, dims, strides, box);
 }
 
 // out_map / out1 / out2: store maps of the outputs for epilogues that use TMA stores.
@@ -155,18 +165,21 @@ int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
 // Narrow-segment GEMM on CTA pairs: W (K-major [E][N][K] or, WMN, MN-major [E][K][N]) against
 // expert-sorted rows X [R][K] (hi, and lo when SPLIT; x_lo is ignored otherwise); fp32 out
 // [R][N] (row stride ld).
-template <bool WMN, bool SPLIT, int NMAX>
+template <bool WMN, bool SPLIT, int NMAX, int EPI = EPI_F32>
 cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_lo, int K, GemmArgs args, int R,
                           int n_sm, cudaStream_t st) {
-  using C = NarrowCfg<WMN, SPLIT, NMAX>;
+  using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
   static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
-  CUtensorMap tx, tx2;
-  if (!tmap_2d(&tx, x_hi, K, R, BK, NARROW_XBOX)) return cudaErrorInvalidValue;
+  CUtensorMap tx, tx2, txs, tx2s;
+  if (!tmap_2d(&tx, x_hi, K, R, BK, NARROW_XBOX) || !tmap_2d(&txs, x_hi, K, R, BK, NARROW_XBOX_S))
+    return cudaErrorInvalidValue;
   tx2 = tx;
-  if (SPLIT && !tmap_2d(&tx2, x_lo, K, R, BK, NARROW_XBOX)) return cudaErrorInvalidValue;
+  tx2s = txs;
+  if (SPLIT && (!tmap_2d(&tx2, x_lo, K, R, BK, NARROW_XBOX) || !tmap_2d(&tx2s, x_lo, K, R, BK, NARROW_XBOX_S)))
+    return cudaErrorInvalidValue;
   const int bound = ((R + NMAX - 1) / NMAX + args.E) * C::m_tiles(args);
   if (R <= 0 || bound <= 0) return cudaSuccess;
-  auto kern = gemm_narrow_kernel<WMN, SPLIT, NMAX>;
+  auto kern = gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
@@ -191,7 +204,7 @@ cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_
     max_pairs[dev] = std::max(1, clusters);
   }
   cfg.gridDim = dim3(2 * std::min(bound, max_pairs[dev]), 1, 1);
-  err = cudaLaunchKernelEx(&cfg, kern, w, tx, tx2, args);
+  err = cudaLaunchKernelEx(&cfg, kern, w, tx, tx2, txs, tx2s, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
@@ -215,7 +228,23 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
 
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, bool pair, cudaStream_t st) {
+                                void* act_lo, int* status, int n_sm, int variant, cudaStream_t st) {
+  if (variant == GEMM_NARROW) {
+    // W13[e] as [2][I][H]: each CTA takes 64 gate rows and their 64 up rows in one box
+    CUtensorMap tw;
+    if (!tmap_w13_gate_up(&tw, w13, H, I, E)) return cudaErrorInvalidValue;
+    GemmArgs g = base_args(E, offsets, tile_off, status);
+    g.N = I;
+    g.K = H;
+    g.I = I;
+    g.out0 = hu;
+    g.ld0 = 2LL * I;
+    g.out1 = act_hi;
+    g.out2 = act_lo;
+    g.ld1 = I;
+    return launch_narrow<false, false, 256, EPI_SWIGLU>(tw, x_g, nullptr, H, g, R, n_sm, st);
+  }
+  const bool pair = variant == GEMM_ROWS_PAIR;
   CUtensorMap ta, tb;
   if (!tmap_2d(&ta, x_g, H, R, BK, BM) || !tmap_3d(&tb, w13, H, 2 * I, E, BK, 128)) return cudaErrorInvalidValue;
   GemmArgs g = base_args(E, offsets, tile_off, status);

@@ -15,6 +15,10 @@
 //   WMN = false  W K-major  [E][N][K]   (GEMM2: o = a W2[e]^T, K = I)
 //   WMN = true   W MN-major [E][K][N]   (dX_g = dHU W13[e], K = 2I)
 //   SPLIT        X is a bf16 hi / lo pair, two MMAs per K step into the same accumulator
+//   EPI_SWIGLU   GEMM1 x_g W13[e]^T (K = H): each CTA's 128 weight rows are 64 gate rows and the
+//                64 up rows of the same intermediate indices, so h and u of one (row, i) sit on
+//                TMEM lane quarters q and q + 2; the gate warp hands h to the up warp through
+//                shared memory, which forms a = silu(h) u (stored as a bf16 hi / lo pair).
 //
 // Roles (both CTAs): warp 0 TMA producer, warp 1 MMA issuer (even CTA only), warps 2..5 epilogue
 // (tcgen05.ld of 32 rows x 32 columns, then per row one 128-byte store of 32 consecutive
@@ -29,15 +33,29 @@
 
 namespace mok {
 
-// One CTA's rows of X arrive as 32-row TMA boxes (4 KB; the last may run into the next expert's
-// rows, which only feed accumulator columns that are not stored).  With 16-row boxes (up to 17
-// boxes per stage) the per-box cost of the copies, not the bytes, bounded the kernel: GEMM2 and
-// dX_g at the DSV3 layer took 1.81 and 3.71 ms, with 32-row boxes 1.64 and 3.10 ms, with 64-row
-// boxes the same as 32, and with a 16-row box for an odd tail 1.68 and 3.31 ms.
-constexpr int NARROW_XBOX = 32;
+// One CTA's rows of X arrive as 64-row TMA boxes (8 KB) and at most one 32-row box (the last box
+// may run into the next expert's rows, which only feed accumulator columns that are not stored).
+// The copies cost per box, not only per byte: with 16-row boxes (up to 17 boxes per stage) GEMM2
+// and dX_g at the DSV3 layer took 1.81 and 3.71 ms, with 32-row boxes 1.64 and 3.10 ms, and a
+// 16-row box for an odd tail made them slower again (1.68 and 3.31 ms).
+constexpr int NARROW_XBOX = 64;
+constexpr int NARROW_XBOX_S = 32;
 
-template <bool WMN, bool SPLIT, int NMAX_>
+// Boxes for `half` rows: n64 boxes of 64 rows, then one of 32 if `with32`; returns the rows loaded.
+__host__ __device__ __forceinline__ int narrow_x_boxes(int half, int& n64, bool& with32) {
+  n64 = half >> 6;
+  int rem = half & 63;
+  if (rem > NARROW_XBOX_S) {
+    ++n64;
+    rem = 0;
+  }
+  with32 = rem > 0;
+  return n64 * NARROW_XBOX + (with32 ? NARROW_XBOX_S : 0);
+}
+
+template <bool WMN, bool SPLIT, int NMAX_, int EPI = EPI_F32>
 struct NarrowCfg {
+  static_assert(EPI == EPI_F32 || (EPI == EPI_SWIGLU && !WMN && !SPLIT), "narrow GEMM epilogues");
   static constexpr int PM = 256;                // weight rows (output columns) of a pair tile
   static constexpr int NMAX = NMAX_;            // rows of a pair tile at most
   static_assert((NMAX / 2) % NARROW_XBOX == 0, "the boxes of one CTA's rows fit its X buffer");
@@ -50,9 +68,14 @@ struct NarrowCfg {
   static constexpr int TMEM_COLS = 2 * NMAX <= 256 ? 256 : 512;
   static_assert(NMAX % 32 == 0 && NMAX >= 32 && 2 * NMAX <= 512, "accumulators must fit the TMEM allocation");
   static constexpr int THREADS = 192;
-  static __host__ __device__ int m_tiles(const GemmArgs& a) { return (a.N + PM - 1) / PM; }
+  // SwiGLU: one 32 x 32 fp32 block of h and one of u per pair of warps
+  static constexpr int XBUF_BYTES = EPI == EPI_SWIGLU ? 2 * 2 * 32 * 32 * 4 : 0;
+  // weight tiles: 256 output columns, or (SwiGLU) 128 intermediate indices (gate and up rows)
+  static __host__ __device__ int m_tiles(const GemmArgs& a) {
+    return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + PM - 1) / PM;
+  }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
-    return size_t(STAGES) * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+    return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
   }
 };
 
@@ -98,21 +121,24 @@ __device__ __forceinline__ NarrowTile decode_narrow_tile(int g, int MT, int E, i
   return t;
 }
 
-// tmX / tmX2: X hi / lo in 32-row boxes.
-template <bool WMN, bool SPLIT, int NMAX>
+// tmX / tmX2: X hi / lo in 64-row boxes; tmXs / tmX2s: the same in 32-row boxes.  tmW (SwiGLU):
+// W13 seen as [E][2][I][H], one box = 64 gate rows and their 64 up rows.
+template <bool WMN, bool SPLIT, int NMAX, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const __grid_constant__ CUtensorMap tmX2, const GemmArgs args) {
-  using C = NarrowCfg<WMN, SPLIT, NMAX>;
+                       const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
+                       const __grid_constant__ CUtensorMap tmX2s, const GemmArgs args) {
+  using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // C::XBUF_BYTES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + 256);
   int* s_coff = s_off + (args.E + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -168,7 +194,11 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
-      if (SPLIT) tma_prefetch_desc(&tmX2);
+      tma_prefetch_desc(&tmXs);
+      if (SPLIT) {
+        tma_prefetch_desc(&tmX2);
+        tma_prefetch_desc(&tmX2s);
+      }
       const uint64_t pol_rows = l2_policy_evict_last();   // rows: read by every weight tile
       const uint64_t pol_once = l2_policy_evict_first();  // a weight tile read by one chunk
       const uint64_t pol_shared = l2_policy_evict_normal();
@@ -180,8 +210,9 @@ __global__ void __launch_bounds__(192, 1)
       for (int g = pair; g < total && ok; g += npairs) {
         const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
         const int half = t.n >> 1;                      // rows of this CTA's half of N
-        const int nbox = (half + NARROW_XBOX - 1) / NARROW_XBOX;
-        const int xrows = nbox * NARROW_XBOX;           // <= NMAX / 2: fits the X buffer
+        int n64;
+        bool with32;
+        const int xrows = narrow_x_boxes(half, n64, with32);  // <= NMAX / 2: fits the X buffer
         const int x_row = t.row0 + (int)rank * half;
         const int w_row = t.m * C::PM + 128 * (int)rank;
         const uint32_t pair_tx = 2u * (C::A_BYTES + C::X_OPS * xrows * 128);
@@ -197,16 +228,24 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sx = sa + C::A_BYTES;
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair_tx);
           const int k0 = kb * BK;
-          if (WMN) {
+          if (EPI == EPI_SWIGLU) {
+            // 64 gate rows, then the 64 up rows of the same intermediate indices
+            tma_load_4d_pair(sa, &tmW, fb, k0, t.m * 128 + 64 * (int)rank, 0, t.e, pol_w);
+          } else if (WMN) {
             tma_load_3d_pair(sa, &tmW, fb, w_row, k0, t.e, pol_w);
             tma_load_3d_pair(sa + MN_ATOM_BYTES, &tmW, fb, w_row + 64, k0, t.e, pol_w);
           } else {
             tma_load_3d_pair(sa, &tmW, fb, k0, w_row, t.e, pol_w);
           }
-          for (int b = 0; b < nbox; ++b) {
+          for (int b = 0; b < n64; ++b) {
             const int r = b * NARROW_XBOX;
             tma_load_2d_pair(sx + r * 128, &tmX, fb, k0, x_row + r, pol_rows);
             if (SPLIT) tma_load_2d_pair(sx + C::X_OP + r * 128, &tmX2, fb, k0, x_row + r, pol_rows);
+          }
+          if (with32) {
+            const int r = n64 * NARROW_XBOX;
+            tma_load_2d_pair(sx + r * 128, &tmXs, fb, k0, x_row + r, pol_rows);
+            if (SPLIT) tma_load_2d_pair(sx + C::X_OP + r * 128, &tmX2s, fb, k0, x_row + r, pol_rows);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -314,28 +353,85 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0)
         w_ok = mbar_wait<true>(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL,
                                kWaitLimitNs, 256);
-      if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
-      tc_fence_after();
-      // this thread's output column; the accumulator's columns are the chunk's rows
-      const int j = t.m * C::PM + 128 * (int)rank + 32 * quarter + lane;
-      const bool jv = j < args.N;
       const uint32_t tacc = tmem_base + acc * C::NMAX + (uint32_t(quarter * 32) << 16);
-      float* o = out + (long long)t.row0 * args.ld0 + j;
+      if (EPI == EPI_SWIGLU) {
+        // the two warps that share intermediate indices agree on stopping (one of them may
+        // have given up waiting while the other saw the accumulator complete)
+        const int qp = quarter & 1;
+        const bool w_fail = !__shfl_sync(0xffffffffu, w_ok, 0);
+        if (named_bar_any(1 + qp, 64, w_fail)) break;
+        tc_fence_after();
+        const bool gate = quarter < 2;  // lanes of gate rows (h); quarter + 2 holds u
+        const int i = t.m * 128 + 64 * (int)rank + 32 * qp + lane;
+        float* hu = reinterpret_cast<float*>(args.out0) + (long long)t.row0 * args.ld0;
+        __nv_bfloat16* ahi = reinterpret_cast<__nv_bfloat16*>(args.out1) + (long long)t.row0 * args.ld1;
+        __nv_bfloat16* alo = reinterpret_cast<__nv_bfloat16*>(args.out2) + (long long)t.row0 * args.ld1;
+        float* xh = xbuf + qp * 2 * 32 * 32;  // [32 rows][32 lanes]: h, then u
+        float* xu = xh + 32 * 32;
 #pragma unroll 1
-      for (int c = 0; c * 32 < t.rows; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tacc + c * 32, v);
-        tmem_wait_ld();
-        const int nr = min(32, t.rows - c * 32);
-        if (jv) {
-          float* oc = o + (long long)(c * 32) * args.ld0;
-          if (nr == 32) {
+        for (int c = 0; c * 32 < t.rows; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+          const int nr = min(32, t.rows - c * 32);
+          const long long rb = c * 32;
+          // both warps park their block in shared memory ([row][lane]: conflict-free), so the up
+          // warp's SwiGLU loop needs no fully unrolled register block
+          float* mine = gate ? xh : xu;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
-          } else {
+          for (int j = 0; j < 32; ++j) mine[j * 32 + lane] = __uint_as_float(v[j]);
+          if (gate) {
+            float* hp = hu + rb * args.ld0 + i;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nr) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+            for (int j = 0; j < 32; ++j) {
+              if (j < nr) *hp = __uint_as_float(v[j]);
+              hp += args.ld0;
+            }
+          }
+          named_bar_sync(1 + qp, 64);  // h of this block is in shared memory
+          if (!gate) {
+            float* up = hu + rb * args.ld0 + args.I + i;
+            __nv_bfloat16* php = ahi + rb * args.ld1 + i;
+            __nv_bfloat16* plp = alo + rb * args.ld1 + i;
+#pragma unroll 4
+            for (int j = 0; j < nr; ++j) {
+              const float h = xh[j * 32 + lane];
+              const float u = xu[j * 32 + lane];
+              *up = u;
+              const float a = h / (1.0f + __expf(-h)) * u;
+              const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
+              *php = a_hi;
+              *plp = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+              up += args.ld0;
+              php += args.ld1;
+              plp += args.ld1;
+            }
+          }
+          named_bar_sync(1 + qp, 64);  // the up warp has read it
+        }
+      } else {
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+        tc_fence_after();
+        // this thread's output column; the accumulator's columns are the chunk's rows
+        const int j = t.m * C::PM + 128 * (int)rank + 32 * quarter + lane;
+        const bool jv = j < args.N;
+        float* o = out + (long long)t.row0 * args.ld0 + j;
+#pragma unroll 1
+        for (int c = 0; c * 32 < t.rows; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+          const int nr = min(32, t.rows - c * 32);
+          if (jv) {
+            float* oc = o + (long long)(c * 32) * args.ld0;
+            if (nr == 32) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nr) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+            }
           }
         }
       }

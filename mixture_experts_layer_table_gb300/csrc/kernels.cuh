@@ -34,12 +34,13 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
                                int* status, int n_sm, cudaStream_t st);
 // `pair`: run the GEMM on CTA pairs (tcgen05 cta_group::2, 256-row tiles) instead of single CTAs
 // (128-row tiles); same results bit for bit.
+// Expert GEMM kernels (GEMM1, GEMM2, dX_g): 128-row tiles of an expert's rows on single CTAs,
+// 256-row tiles on CTA pairs (GEMM1 / GEMM2), or the narrow-segment pair kernel (the expert's
+// rows as the MMA's N).
+enum GemmVariant { GEMM_ROWS_SINGLE = 0, GEMM_ROWS_PAIR = 1, GEMM_NARROW = 2 };
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, bool pair, cudaStream_t st);
-// Expert GEMM kernels for GEMM2 and dX_g: 128-row tiles on single CTAs, 256-row tiles on CTA
-// pairs (GEMM2 only), or the narrow-segment pair kernel (expert rows as the MMA's N).
-enum GemmVariant { GEMM_ROWS_SINGLE = 0, GEMM_ROWS_PAIR = 1, GEMM_NARROW = 2 };
+                                void* act_lo, int* status, int n_sm, int variant, cudaStream_t st);
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
                          int variant, cudaStream_t st);
