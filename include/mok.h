@@ -119,7 +119,7 @@ typedef struct {
   int64_t ctx_bytes;
   /* ws.  "hi/lo" pairs hold v as bf16 hi = bf16(v) plus bf16 lo = bf16(v - hi), so that a
    * GEMM operand produced inside the layer keeps about 16 significant bits. */
-  int64_t status;     /* i32 [4]      device status word: code, site */
+  int64_t status;     /* i32 [64]     device status word (code, site), then per-call work counters */
   int64_t logits;     /* f32 [T][E]   router logits */
   int64_t act;        /* bf16 [T*k][I]  SwiGLU output a = silu(h) * u, hi part */
   int64_t act_lo;     /* bf16 [T*k][I]  lo part */

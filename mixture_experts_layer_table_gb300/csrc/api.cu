@@ -110,7 +110,7 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->hu = take(R * 2 * I * 4);
   L->ctx_bytes = off;
   off = 0;
-  L->status = take(16);
+  L->status = take(mok::STATUS_BYTES);
   L->logits = take(T * E * 4);
   L->act = take(R * I * 2);
   L->act_lo = take(R * I * 2);
@@ -241,7 +241,7 @@ mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_ro
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = at<int>(ws, L.status);
   float* logits = at<float>(ws, L.logits);
-  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOK_CUDA(cudaMemsetAsync(status, 0, mok::STATUS_BYTES, st));
   if (have_router) MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, d->T, d->H, d->E, logits, status, n_sm, st));
   MOK_LAUNCH("topk", st, mok::launch_topk(have_router ? logits : nullptr, router_bias, given_topk, d->T, d->E, d->k, d->router,
                             d->renorm, d->route_scale, topk_idx, gates, nullptr, status, st));
@@ -289,7 +289,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   float* o = at<float>(ws, L.expert_out);
   float* logits = at<float>(ws, L.logits);
 
-  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOK_CUDA(cudaMemsetAsync(status, 0, mok::STATUS_BYTES, st));
   // 1. router logits x W_r^T (tensor cores, fp32 accumulate)
   MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
   // 2. scores, top-k and gates
@@ -398,6 +398,8 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
   int* status = at<int>(ws, L.status);
+  // the work counters of this call start at zero (the status word keeps what the forward left)
+  MOK_CUDA(cudaMemsetAsync(status + mok::STATUS_COUNTERS, 0, mok::STATUS_BYTES - 4 * mok::STATUS_COUNTERS, st));
   const int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
   const float* gates = at<float>(ctx, L.gates);
   const float* scores = at<float>(ctx, L.scores);
@@ -445,9 +447,10 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                 n_sm, gemm_variant(d, DGRAD_X), st));
   // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H]
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(a_r, nullptr, I, do_r, nullptr, H, R, E, offsets, dw2, wgrad_f32, status,
-                                               n_sm, st));
+                                               status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, n_sm, st));
   MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(xg_r, nullptr, H, dhu_r, nullptr, 2 * I, R, E, offsets, dw13,
-                                                wgrad_f32, status, n_sm, st));
+                                                wgrad_f32, status,
+                                                status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, n_sm, st));
   // 6-8. gate and router gradients, router weight gradient, reverse dispatch (as in bf16)
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k,
                                                               d->router, d->renorm, d->route_scale, dgates, dl, st));
@@ -489,7 +492,7 @@ mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const v
   float* o = at<float>(ws, L.expert_out);
   float* logits = at<float>(ws, L.logits);
 
-  MOK_CUDA(cudaMemsetAsync(status, 0, 16, st));
+  MOK_CUDA(cudaMemsetAsync(status, 0, mok::STATUS_BYTES, st));
   MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
   MOK_LAUNCH("topk", st, mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm,
                                           d->route_scale, topk_idx, gates, at<float>(ctx, L.scores), status, st));
@@ -528,6 +531,8 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
   int* status = at<int>(ws, L.status);
+  // the work counters of this call start at zero (the status word keeps what the forward left)
+  MOK_CUDA(cudaMemsetAsync(status + mok::STATUS_COUNTERS, 0, mok::STATUS_BYTES - 4 * mok::STATUS_COUNTERS, st));
   if (d->ring_bytes > 0) {
     // the ring forward kept the dispatched rows only in the ring: dispatch them again, into
     // the expert-output scratch, which the backward does not otherwise use
@@ -566,9 +571,10 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   // 4. dW2[e] = (g a)^T dY_g stored as [H][I]; 5. dW13[e] = x_g^T [dh | du] stored as [2I][H];
   //    both reduced over the expert's rows, the contiguous output dimension on the TMEM lanes
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(gact, gact_lo, I, dy_g, nullptr, H, R, E, offsets, dw2, wgrad_f32,
-                                               status, n_sm, st));
+                                               status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, n_sm, st));
   MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(x_g, nullptr, H, dhu, dhu_lo, 2 * I, R, E, offsets, dw13, wgrad_f32,
-                                                status, n_sm, st));
+                                                status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, n_sm,
+                                                st));
   // 6. gate and router-logit gradients, 7. router weight gradient
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
                                       d->renorm, d->route_scale, dgates, dl, st));

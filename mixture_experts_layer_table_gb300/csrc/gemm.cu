@@ -362,8 +362,8 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
 }
 
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
-                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int n_sm,
-                         cudaStream_t st) {
+                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int* strip_counter,
+                         int n_sm, cudaStream_t st) {
   constexpr int WBN = 128;
   CUtensorMap ta, ta2, tb, tb2;
   if (!tmap_2d(&ta, a_hi, M, R, 64, BK) || !tmap_2d(&tb, b_hi, N, R, 64, BK)) return cudaErrorInvalidValue;
@@ -383,6 +383,8 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   g.offsets = offsets;
   g.out = dw;
   g.status = status;
+  g.strip_counter = strip_counter;
+  if (strip_counter == nullptr) return cudaErrorInvalidValue;
   const int strips = E * (stat_a ? M / 128 : N / 128);
   const int grid = std::min(strips, n_sm);
   if (grid <= 0) return cudaSuccess;

@@ -53,9 +53,16 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
                            int variant, cudaStream_t st);
 // dW[e] stored transposed as out[e][n][m] (m = the output's contiguous dimension):
 // out[e][n][m] = sum over rows r of expert e of A[r][m] * B[r][n]; A or B may be a hi/lo pair.
+// strip_counter: a device int that is zero when the kernel starts (its strips are dealt from it).
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
-                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int n_sm,
-                         cudaStream_t st);
+                         int E, const int32_t* offsets, void* dw, int out_f32, int* status, int* strip_counter,
+                         int n_sm, cudaStream_t st);
+// Status region of the workspace (256 bytes, cleared at the start of every entry point): the
+// status word (code, site) in ints 0..1, the work counters of dynamically dealt launches from
+// int STATUS_COUNTERS on.
+constexpr int STATUS_BYTES = 256;
+constexpr int STATUS_COUNTERS = 16;
+enum WorkCounter { CNT_WGRAD_W2 = 0, CNT_WGRAD_W13 = 1 };
 // Ring forward GEMM1: comm_ctas CTAs gather minibatches into the ring, the rest run GEMM1
 // (SwiGLU epilogue, rows written at their global position).  Cooperative launch, grid = n_sm.
 struct RingArgs {

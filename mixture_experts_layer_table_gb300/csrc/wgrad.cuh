@@ -10,9 +10,16 @@
 // 48 KB.  Experts with more rows than the stationary region holds (3 K blocks = 192 rows) are
 // done tile by tile with the stationary K blocks reloaded in chunks.
 //
-// Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue (TMEM -> registers, the accumulator released
-// at once, then coalesced stores: the output is transposed so that the 32 lanes of a warp, 32
-// consecutive m, write one 128-byte line per column).  The shared memory left by the stationary
+// Strips are dealt dynamically: the producer warp takes the next strip index from a global
+// counter and hands it to the MMA and epilogue warps through a 2-deep queue in shared memory.  On
+// GB300 a static round-robin deal of this write-bound kernel ran at the pace of the slowest SMs
+// (a store pattern like its epilogue's reached 6.7 TB/s dealt statically, 7.4-7.7 TB/s dealt from
+// a counter).  Every strip is computed the same way whichever CTA takes it, so the results do not
+// depend on the deal.
+//
+// Warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue in two groups of four, one per TMEM
+// accumulator (TMEM -> registers 32 columns at a time, then coalesced stores: the output is
+// transposed so that the 32 lanes of a warp, 32 consecutive m, write one 128-byte line per column).  The shared memory left by the stationary
 // operand goes to a deep ring for the streaming operand: with only a few small K blocks per
 // tile, the loads in flight, not the MMAs, bound the main loop (measured: 3 stages of 16 KB held
 // the dW13 main loop at 4.6 ms on its own at the DSV3 layer).  All waits are bounded; the rows
@@ -30,13 +37,14 @@ constexpr int WG_KSTAT = 3;                  // K blocks the stationary region h
 constexpr int WG_STAT_SLOT = 4 * 8192;       // one K block of the stationary pair: hi (2 atoms), lo (2 atoms)
 constexpr int WG_STAGE = 2 * 8192;           // one K block of the streaming operand (2 atoms)
 constexpr int WG_STAGES = 7;
-constexpr int WG_THREADS = 192;
+constexpr int WG_THREADS = 320;  // producer, MMA, two groups of four epilogue warps
 
 struct WgradArgs {
   int M, N, E;              // output dims per expert (out[e][n][m]), experts
   const int* offsets;       // [E+1] expert row offsets
-  void* out;                // [E][N][M] (fp32 or bf16), written by TMA except for empty experts
+  void* out;                // [E][N][M] (fp32 or bf16)
   int* status;
+  int* strip_counter;       // zero at launch: next strip to deal
 };
 
 __host__ __device__ constexpr size_t wgrad_smem_bytes(int E) {
@@ -56,9 +64,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   uint8_t* stat = smem;                                   // WG_KSTAT slots
   uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WG_STAGES stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + WG_STAGES * WG_STAGE);
-  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full, stat_empty, drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WG_STAGES + 7);
+  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full, stat_empty, drain, sq_full[2], sq_empty[2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WG_STAGES + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* sq = reinterpret_cast<volatile int*>(tmem_slot + 2);  // strip queue [2]
   int* s_off = reinterpret_cast<int*>(ring + WG_STAGES * WG_STAGE + 256);
 
   const int warp = threadIdx.x >> 5;
@@ -70,6 +79,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   const uint32_t stat_full = smem_u32(&bars[2 * WG_STAGES + 4]);
   const uint32_t stat_empty = smem_u32(&bars[2 * WG_STAGES + 5]);
   const uint32_t drain_bar = smem_u32(&bars[2 * WG_STAGES + 6]);
+  auto sq_full = [&](int d) { return smem_u32(&bars[2 * WG_STAGES + 7 + d]); };
+  auto sq_empty = [&](int d) { return smem_u32(&bars[2 * WG_STAGES + 9 + d]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < WG_STAGES; ++s) {
@@ -83,6 +94,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     mbar_init(stat_full, 1);
     mbar_init(stat_empty, 1);
     mbar_init(drain_bar, 1);
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(sq_full(d), 1);
+      mbar_init(sq_empty(d), 9);  // the MMA warp and the 8 epilogue warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -107,6 +122,25 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     row0 = s_off[e];
     rows = s_off[e + 1] - row0;
     nkb = (rows + WG_BK - 1) / WG_BK;
+  };
+  // consumers (one warp): the next strip of the queue, -1 when none is left, -2 on abort
+  int qd = 0;
+  uint32_t qph = 0;
+  auto take_strip = [&](int site) {
+    int ok = 1, sv = -1;
+    if (lane == 0) {
+      ok = mbar_wait(sq_full(qd), qph, abort_flag, args.status, site, kWaitLimitNs, 64);
+      if (ok) sv = *(sq + qd);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    sv = __shfl_sync(0xffffffffu, sv, 0);
+    if (lane == 0 && ok) mbar_arrive(sq_empty(qd));
+    __syncwarp();
+    if (++qd == 2) {
+      qd = 0;
+      qph ^= 1;
+    }
+    return ok ? sv : -2;
   };
 
   if (warp == 0) {
@@ -153,7 +187,19 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         }
         return true;
       };
-      for (int s = blockIdx.x; s < total && ok; s += gridDim.x) {
+      while (ok) {
+        // deal the next strip: take it from the counter and queue it for the other warps
+        if (!mbar_wait(sq_empty(qd), qph ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs, 32))
+          break;
+        int s = atomicAdd(args.strip_counter, 1);
+        if (s >= total) s = -1;
+        *(sq + qd) = s;
+        mbar_arrive(sq_full(qd));
+        if (++qd == 2) {
+          qd = 0;
+          qph ^= 1;
+        }
+        if (s < 0) break;
         int e, f, row0, rows, nkb;
         strip(s, e, f, row0, rows, nkb);
         if (nkb == 0) continue;
@@ -256,7 +302,9 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     };
-    for (int s = blockIdx.x; s < total && ok; s += gridDim.x) {
+    while (ok) {
+      const int s = take_strip(SITE_GEMM_MMA_FULL);
+      if (s < 0) break;
       int e, f, row0, rows, nkb;
       strip(s, e, f, row0, rows, nkb);
       if (nkb == 0) continue;
@@ -293,25 +341,36 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    // Two groups of four warps; group g drains accumulator g (the MMA alternates the two over
+    // its tiles), keeping it until its stores are issued, so one group stores while the other
+    // waits for the next tile: the store stream has no gap between tiles.
+    const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;
-    int acc = 0;
     uint32_t acc_phase = 0;
+    int tcount = 0;  // tiles with MMAs seen so far (both groups count all of them)
     bool ok = true;
-    for (int s = blockIdx.x; s < total && ok; s += gridDim.x) {
+    while (ok) {
+      const int s = take_strip(SITE_GEMM_EPI_TMEM_FULL);
+      if (s < 0) break;
       int e, f, row0, rows, nkb;
       strip(s, e, f, row0, rows, nkb);
       for (int i = 0; i < strip_len; ++i) {
         const int m = STAT_A ? f : i;
         const int n = STAT_A ? i : f;
+        // out[e][n*128 + col][m*128 + quarter*32 + lane]
+        const size_t base = (size_t)e * args.M * args.N + (size_t)(n * 128) * args.M + m * 128 + quarter * 32 + lane;
         if (nkb == 0) {
-          // an expert without rows: its weight gradient is zero (lane = m, contiguous stores)
-          const size_t base = (size_t)e * args.M * args.N + (size_t)(n * 128) * args.M + m * 128 + quarter * 32 + lane;
+          // an expert without rows: its weight gradient is zero (the groups take alternate tiles)
+          if ((i & 1) != grp) continue;
           for (int j = 0; j < 128; ++j) {
             if (OUT_F32) reinterpret_cast<float*>(args.out)[base + (size_t)j * args.M] = 0.0f;
             else reinterpret_cast<__nv_bfloat16*>(args.out)[base + (size_t)j * args.M] = __float2bfloat16_rn(0.0f);
           }
           continue;
         }
+        const int acc = tcount & 1;
+        ++tcount;
+        if (acc != grp) continue;
         int w_ok = 1;
         if (lane == 0)
           w_ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL, kWaitLimitNs,
@@ -322,26 +381,22 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t tacc = tmem_base + acc * 128 + (uint32_t(quarter * 32) << 16);
-        uint32_t v[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tacc + c * 32, v[c]);
-        tmem_wait_ld();
-        // the accumulator is in registers: hand it back to the MMA before storing
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
-        // out[e][n*128 + col][m*128 + quarter*32 + lane]
-        const size_t base = (size_t)e * args.M * args.N + (size_t)(n * 128) * args.M + m * 128 + quarter * 32 + lane;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const size_t idx = base + (size_t)(c * 32 + j) * args.M;
-            if (OUT_F32) reinterpret_cast<float*>(args.out)[idx] = __uint_as_float(v[c][j]);
-            else reinterpret_cast<__nv_bfloat16*>(args.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[c][j]));
+            if (OUT_F32) reinterpret_cast<float*>(args.out)[idx] = __uint_as_float(v[j]);
+            else reinterpret_cast<__nv_bfloat16*>(args.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        acc_phase ^= 1;
       }
     }
   }
