@@ -58,7 +58,8 @@ struct NarrowCfg {
   static_assert(EPI == EPI_F32 || (EPI == EPI_SWIGLU && !WMN && !SPLIT), "narrow GEMM epilogues");
   static constexpr int PM = 256;                // weight rows (output columns) of a pair tile
   static constexpr int NMAX = NMAX_;            // rows of a pair tile at most
-  static_assert((NMAX / 2) % NARROW_XBOX == 0, "the boxes of one CTA's rows fit its X buffer");
+  // narrow_x_boxes(h) <= NMAX / 2 for every h <= NMAX / 2 when NMAX / 2 is a multiple of 32
+  static_assert((NMAX / 2) % NARROW_XBOX_S == 0, "the boxes of one CTA's rows fit its X buffer");
   static constexpr int X_OP = (NMAX / 2) * 128; // one CTA's rows of one X operand x 64 K
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int X_OPS = SPLIT ? 2 : 1;
