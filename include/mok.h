@@ -81,8 +81,10 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                cta_group::2, 256 weight rows per pair).  MOK_FLAG_GEMM_PAIR: GEMM1 and
  *                GEMM2 on CTA pairs with 256-row tiles of an expert's rows, dX_g on
  *                single CTAs with 128-row tiles.  MOK_FLAG_GEMM_SINGLE: all three on
- *                single CTAs with 128-row tiles.  Results are bitwise the same in every
- *                case.  Setting both flags is an invalid argument.
+ *                single CTAs with 128-row tiles.  The weight gradients run on CTA pairs
+ *                (256 x 256 tiles) by default and on single CTAs (128 x 128) with either
+ *                flag.  Results are bitwise the same in every case.  Setting both flags
+ *                is an invalid argument.
  *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1

@@ -53,6 +53,8 @@ mok_status check_desc(const mok_layer_desc* d) {
 // MMA's N, padded to 16 rows instead of a 128-row tile); MOK_FLAG_GEMM_SINGLE / MOK_FLAG_GEMM_PAIR
 // ask for the row-tile kernels (dX_g has no pair row-tile form and runs on single CTAs then).
 enum ExpertGemm { GEMM1 = 0, GEMM2 = 1, DGRAD_X = 2 };
+// Weight gradients on CTA pairs (256 x 256 tiles) unless the row-tile kernels are asked for.
+bool wgrad_pairs(const mok_layer_desc* d) { return (d->flags & (MOK_FLAG_GEMM_SINGLE | MOK_FLAG_GEMM_PAIR)) == 0; }
 int gemm_variant(const mok_layer_desc* d, int which) {
   if (d->flags & MOK_FLAG_GEMM_PAIR) return which == DGRAD_X ? mok::GEMM_ROWS_SINGLE : mok::GEMM_ROWS_PAIR;
   if (d->flags & MOK_FLAG_GEMM_SINGLE) return mok::GEMM_ROWS_SINGLE;
@@ -447,10 +449,12 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                 n_sm, gemm_variant(d, DGRAD_X), st));
   // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H]
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(a_r, nullptr, I, do_r, nullptr, H, R, E, offsets, dw2, wgrad_f32, status,
-                                               status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, n_sm, st));
+                                               status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, wgrad_pairs(d),
+                                               n_sm, st));
   MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(xg_r, nullptr, H, dhu_r, nullptr, 2 * I, R, E, offsets, dw13,
                                                 wgrad_f32, status,
-                                                status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, n_sm, st));
+                                                status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, wgrad_pairs(d),
+                                                n_sm, st));
   // 6-8. gate and router gradients, router weight gradient, reverse dispatch (as in bf16)
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k,
                                                               d->router, d->renorm, d->route_scale, dgates, dl, st));
@@ -571,9 +575,11 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   // 4. dW2[e] = (g a)^T dY_g stored as [H][I]; 5. dW13[e] = x_g^T [dh | du] stored as [2I][H];
   //    both reduced over the expert's rows, the contiguous output dimension on the TMEM lanes
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(gact, gact_lo, I, dy_g, nullptr, H, R, E, offsets, dw2, wgrad_f32,
-                                               status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, n_sm, st));
+                                               status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2,
+                                               wgrad_pairs(d), n_sm, st));
   MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(x_g, nullptr, H, dhu, dhu_lo, 2 * I, R, E, offsets, dw13, wgrad_f32,
-                                                status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, n_sm,
+                                                status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13,
+                                                wgrad_pairs(d), n_sm,
                                                 st));
   // 6. gate and router-logit gradients, 7. router weight gradient
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,

@@ -8,6 +8,7 @@
 #include "gemm_narrow.cuh"
 #include "gemm_pair.cuh"
 #include "wgrad.cuh"
+#include "wgrad_pair.cuh"
 #include "kernels.cuh"
 
 namespace mok {
@@ -371,7 +372,7 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
 
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
                          int E, const int32_t* offsets, void* dw, int out_f32, int* status, int* strip_counter,
-                         int n_sm, cudaStream_t st) {
+                         bool pair, int n_sm, cudaStream_t st) {
   constexpr int WBN = 128;
   CUtensorMap ta, ta2, tb, tb2;
   if (!tmap_2d(&ta, a_hi, M, R, 64, BK) || !tmap_2d(&tb, b_hi, N, R, 64, BK)) return cudaErrorInvalidValue;
@@ -393,10 +394,39 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   g.status = status;
   g.strip_counter = strip_counter;
   if (strip_counter == nullptr) return cudaErrorInvalidValue;
+  const size_t smem = wgrad_smem_bytes(E);
+  if (pair && M % 256 == 0 && N % 256 == 0) {
+    // CTA pairs: 256 x 256 output tiles, each CTA half of both operands
+    const int pstrips = E * (stat_a ? M / 256 : N / 256);
+    if (pstrips <= 0) return cudaSuccess;
+    auto run_pair = [&](auto kern) {
+      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_smem_bytes(1024));
+      if (err != cudaSuccess) return err;
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(WGP_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3(2 * std::max(1, n_sm / 2), 1, 1);
+      int clusters = 0;
+      if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
+      cfg.gridDim = dim3(2 * std::min(pstrips, std::max(1, clusters)), 1, 1);
+      if ((err = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, g)) != cudaSuccess) return err;
+      return cudaGetLastError();
+    };
+    if (!split) return out_f32 ? run_pair(wgrad_pair_kernel<true, true, false>) : run_pair(wgrad_pair_kernel<true, false, false>);
+    if (a_lo) return out_f32 ? run_pair(wgrad_pair_kernel<true, true>) : run_pair(wgrad_pair_kernel<true, false>);
+    return out_f32 ? run_pair(wgrad_pair_kernel<false, true>) : run_pair(wgrad_pair_kernel<false, false>);
+  }
   const int strips = E * (stat_a ? M / 128 : N / 128);
   const int grid = std::min(strips, n_sm);
   if (grid <= 0) return cudaSuccess;
-  const size_t smem = wgrad_smem_bytes(E);
   auto run = [&](auto kern) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_smem_bytes(1024));
     if (err != cudaSuccess) return err;

@@ -53,10 +53,11 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
                            int variant, cudaStream_t st);
 // dW[e] stored transposed as out[e][n][m] (m = the output's contiguous dimension):
 // out[e][n][m] = sum over rows r of expert e of A[r][m] * B[r][n]; A or B may be a hi/lo pair.
-// strip_counter: a device int that is zero when the kernel starts (its strips are dealt from it).
+// strip_counter: a device int that is zero when the kernel starts (the single-CTA kernel deals its
+// strips from it).  pair: 256 x 256 tiles on CTA pairs (M and N multiples of 256).
 cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* b_hi, const void* b_lo, int N, int R,
                          int E, const int32_t* offsets, void* dw, int out_f32, int* status, int* strip_counter,
-                         int n_sm, cudaStream_t st);
+                         bool pair, int n_sm, cudaStream_t st);
 // Status region of the workspace (256 bytes, cleared at the start of every entry point): the
 // status word (code, site) in ints 0..1, the work counters of dynamically dealt launches from
 // int STATUS_COUNTERS on.

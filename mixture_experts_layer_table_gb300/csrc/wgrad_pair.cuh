@@ -1,0 +1,393 @@
+// Weight-gradient GEMM on CTA pairs (sm_103a, tcgen05.mma.cta_group::2).
+//
+//   out[e][n][m] = sum over the rows r of expert e of A[r][m] * B[r][n]
+//
+// Same operands and roles as wgrad_kernel (wgrad.cuh): one operand (the bf16 hi + lo pair, or the
+// plain one when neither is split) stays in shared memory for a strip of output tiles, the other
+// streams through a 7-stage ring.  Here two CTAs on neighbouring SMs run 256 x 256 output tiles
+// together: each CTA holds 128 columns of the stationary operand and streams 128 columns of the
+// other, the even CTA issues M = 256, N = 256 MMAs that read both CTAs' halves, and each CTA's
+// TMEM receives its 128 rows x 256 columns.  Per output element this halves the operand bytes
+// each SM's tensor core reads from shared memory and the MMA instructions; at the DSV3 layer the
+// single-CTA kernel's time followed its MMA count (half the MMAs: 10% faster) while the MMAs
+// themselves run at the ideal rate in isolation.
+//
+// Warps (both CTAs): 0 TMA producer, 1 MMA issuer (even CTA) / stationary check (odd CTA), 2..9
+// epilogue in two groups of four, one per TMEM accumulator.  The stationary halves are loaded by
+// each CTA with plain TMA into its own barrier; its warp 1 zeroes the rows past the expert's end
+// and then reports to the even CTA (stat_ready, 2 arrivals) before the pair's MMAs read them.
+// Strips (expert, 256-wide stationary tile) are dealt to the pairs round-robin; each output
+// element is one tile's accumulator, reduced over the expert's rows in a fixed order, so results
+// are bitwise those of the single-CTA kernel.
+#pragma once
+#include "wgrad.cuh"
+
+namespace mok {
+
+constexpr int WGP_THREADS = 320;
+
+template <bool STAT_A, bool OUT_F32, bool STAT_SPLIT = true>
+__global__ void __launch_bounds__(WGP_THREADS, 1)
+    wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                      const WgradArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stat = smem;                                   // WG_KSTAT slots
+  uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WG_STAGES stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + WG_STAGES * WG_STAGE);
+  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full, stat_ready, stat_empty, drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WG_STAGES + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_off = reinterpret_cast<int*>(ring + WG_STAGES * WG_STAGE + 256);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int pair = (int)blockIdx.x >> 1;
+  const int npairs = (int)gridDim.x >> 1;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[WG_STAGES + s]); };
+  auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * WG_STAGES + a]); };
+  auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * WG_STAGES + 2 + a]); };
+  const uint32_t stat_full = smem_u32(&bars[2 * WG_STAGES + 4]);
+  const uint32_t stat_ready = smem_u32(&bars[2 * WG_STAGES + 5]);
+  const uint32_t stat_empty = smem_u32(&bars[2 * WG_STAGES + 6]);
+  const uint32_t drain_bar = smem_u32(&bars[2 * WG_STAGES + 7]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < WG_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);  // the 4 warps of group a in both CTAs
+    }
+    mbar_init(stat_full, 1);
+    mbar_init(stat_ready, 2);  // warp 1 of both CTAs
+    mbar_init(stat_empty, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = args.offsets[i];
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // 256-wide tiles of the pair; this CTA owns the 128 columns at +128*rank of each
+  const int MT = args.M / 256, NT = args.N / 256;
+  const int per_e = STAT_A ? MT : NT;   // strips per expert
+  const int strip_len = STAT_A ? NT : MT;
+  const int total = args.E * per_e;
+  auto strip = [&](int s, int& e, int& f, int& row0, int& rows, int& nkb) {
+    e = s / per_e;
+    f = s - e * per_e;
+    row0 = s_off[e];
+    rows = s_off[e + 1] - row0;
+    nkb = (rows + WG_BK - 1) / WG_BK;
+  };
+  const int half0 = 128 * (int)rank;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmB2);
+      const uint64_t pol = l2_policy_evict_last();
+      const CUtensorMap* sh = STAT_A ? &tmA : &tmB;
+      const CUtensorMap* sl = STAT_A ? &tmA2 : &tmB2;
+      const CUtensorMap* st_map = STAT_A ? &tmB : &tmA;
+      const uint32_t full0_cl = mapa_shared(full_bar(0), 0);  // the even CTA's full barriers
+      int stage = 0;
+      uint32_t phase = 0, sphase = 0;
+      int issued = 0;
+      bool stat_pending = false;  // a stationary load whose bytes may still be landing
+      bool ok = true;
+      auto load_stat = [&](int f, int row0, int kb0, int nk) {
+        if (!mbar_wait<true>(stat_empty, sphase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
+                             kWaitLimitNs, 32))
+          return false;
+        sphase ^= 1;
+        mbar_arrive_expect_tx(stat_full, nk * (STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2));
+        for (int j = 0; j < nk; ++j) {
+          const uint32_t slot = smem_u32(stat + j * WG_STAT_SLOT);
+          const int r = row0 + (kb0 + j) * WG_BK;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            tma_load_2d(slot + q * 8192, sh, stat_full, f * 256 + half0 + q * 64, r, pol);
+            if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full, f * 256 + half0 + q * 64, r, pol);
+          }
+        }
+        stat_pending = true;
+        return true;
+      };
+      auto load_stream = [&](int i, int row0, int kb) {
+        if (!mbar_wait<true>(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
+                             kWaitLimitNs, 32))
+          return false;
+        const uint32_t fb = full0_cl + 8u * stage;
+        const uint32_t sa = smem_u32(ring + stage * WG_STAGE);
+        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * WG_STAGE);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          tma_load_2d_pair(sa + q * 8192, st_map, fb, i * 256 + half0 + q * 64, row0 + kb * WG_BK, pol);
+        ++issued;
+        if (++stage == WG_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        return true;
+      };
+      for (int s = pair; s < total && ok; s += npairs) {
+        int e, f, row0, rows, nkb;
+        strip(s, e, f, row0, rows, nkb);
+        if (nkb == 0) continue;
+        if (nkb <= WG_KSTAT) {
+          ok = load_stat(f, row0, 0, nkb);
+          for (int i = 0; i < strip_len && ok; ++i)
+            for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stream(i, row0, kb);
+        } else {
+          for (int i = 0; i < strip_len && ok; ++i)
+            for (int kb0 = 0; kb0 < nkb && ok; kb0 += WG_KSTAT) {
+              const int nk = min(WG_KSTAT, nkb - kb0);
+              ok = load_stat(f, row0, kb0, nk);
+              for (int kb = kb0; kb < kb0 + nk && ok; ++kb) ok = load_stream(i, row0, kb);
+            }
+        }
+      }
+      if (!ok) {
+        // Aborted: let no copy land in shared memory after the CTA has left.  The even CTA's full
+        // barriers count both CTAs' stream bytes; the peer cannot observe its own and waits a while.
+        volatile int no_abort = 0;
+        if (stat_pending) mbar_wait(stat_full, sphase ^ 1, &no_abort, args.status, SITE_GEMM_DRAIN);
+        if (rank == 0) {
+          const int outstanding = min(issued, WG_STAGES);
+          int st = stage;
+          uint32_t ph = phase;
+          for (int n = 0; n < outstanding; ++n) {
+            if (--st < 0) {
+              st = WG_STAGES - 1;
+              ph ^= 1;
+            }
+            mbar_wait(full_bar(st), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
+          }
+        } else {
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 100000ull) __nanosleep(1000);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (even CTA)
+    constexpr uint32_t idesc = idesc_bf16_f32(256, 256, true, true);
+    const uint32_t stat_ready0_cl = mapa_shared(stat_ready, 0);
+    int stage = 0;
+    uint32_t phase = 0, sphase = 0, rphase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true, any = false;
+    // Both CTAs: wait for this CTA's stationary K blocks [kb0, kb0+nk), zero the rows past the
+    // expert's end, report to the even CTA; the even CTA then waits for both reports.
+    auto take_stat = [&](int rows, int kb0, int nk) {
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(stat_full, sphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
+      sphase ^= 1;
+      const int last = kb0 + nk - 1;
+      const int kvalid = rows - last * WG_BK;
+      const int kend = (kvalid + 15) & ~15;
+      if (kvalid < WG_BK && kvalid < kend) {
+        uint8_t* slot = stat + (nk - 1) * WG_STAT_SLOT;
+        const int nl = kend - kvalid;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int idx = lane; idx < nl * 4 * 8; idx += 32) {
+          const int chunk = idx & 7;
+          const int li = idx >> 3;
+          const int atom = li / nl;
+          const int line = kvalid + (li - atom * nl);
+          *reinterpret_cast<uint4*>(slot + atom * 8192 + line * 128 + chunk * 16) = z;
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(stat_ready0_cl);
+      if (rank == 0) {
+        if (lane == 0)
+          w_ok = mbar_wait<true>(stat_ready, rphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
+        rphase ^= 1;
+        tc_fence_after();
+      }
+      return true;
+    };
+    auto mma_kblock = [&](int j, int rows, int kb, bool first) {
+      int f_ok = 1;
+      if (lane == 0) f_ok = mbar_wait<true>(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+      if (!__shfl_sync(0xffffffffu, f_ok, 0)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const int kvalid = min(WG_BK, rows - kb * WG_BK);
+        const int nk16 = (kvalid + 15) >> 4;
+        const uint32_t shi = smem_u32(stat + j * WG_STAT_SLOT);
+        const uint32_t slo = shi + 16384;
+        const uint32_t sst = smem_u32(ring + stage * WG_STAGE);
+        const uint32_t d = tmem_base + acc * 256;
+        for (int k16 = 0; k16 < nk16; ++k16) {
+          const uint64_t dh = smem_desc_sw128(shi + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
+          const uint64_t dl = smem_desc_sw128(slo + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
+          const uint64_t ds = smem_desc_sw128(sst + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
+          const uint32_t accum = (first && k16 == 0) ? 0u : 1u;
+          if (STAT_A) {
+            umma_f16_pair(d, dh, ds, idesc, accum);
+            if (STAT_SPLIT) umma_f16_pair(d, dl, ds, idesc, 1u);
+          } else {
+            umma_f16_pair(d, ds, dh, idesc, accum);
+            if (STAT_SPLIT) umma_f16_pair(d, ds, dl, idesc, 1u);
+          }
+        }
+        umma_commit_pair(empty_bar(stage), 0x3);
+      }
+      __syncwarp();
+      any = true;
+      if (++stage == WG_STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+      return true;
+    };
+    auto begin_tile = [&]() {
+      int w_ok = 1;
+      if (lane == 0)
+        w_ok = mbar_wait<true>(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
+      tc_fence_after();
+      return true;
+    };
+    auto end_tile = [&]() {
+      if (lane == 0) umma_commit_pair(tfull_bar(acc), 0x3);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    };
+    auto release_stat = [&]() {
+      if (lane == 0) umma_commit_pair(stat_empty, 0x3);  // both CTAs' slots are free once these MMAs end
+      __syncwarp();
+    };
+    for (int s = pair; s < total && ok; s += npairs) {
+      int e, f, row0, rows, nkb;
+      strip(s, e, f, row0, rows, nkb);
+      if (nkb == 0) continue;
+      if (nkb <= WG_KSTAT) {
+        ok = take_stat(rows, 0, nkb);
+        if (rank == 0) {
+          for (int i = 0; i < strip_len && ok; ++i) {
+            ok = begin_tile();
+            for (int kb = 0; kb < nkb && ok; ++kb) ok = mma_kblock(kb, rows, kb, kb == 0);
+            if (ok) end_tile();
+          }
+          if (ok) release_stat();
+        }
+      } else {
+        for (int i = 0; i < strip_len && ok; ++i) {
+          if (rank == 0) ok = begin_tile();
+          for (int kb0 = 0; kb0 < nkb && ok; kb0 += WG_KSTAT) {
+            const int nk = min(WG_KSTAT, nkb - kb0);
+            ok = take_stat(rows, kb0, nk);
+            if (rank == 0) {
+              for (int kb = kb0; kb < kb0 + nk && ok; ++kb) ok = mma_kblock(kb - kb0, rows, kb, kb == 0);
+              if (ok) release_stat();
+            }
+          }
+          if (ok && rank == 0) end_tile();
+        }
+      }
+    }
+    if (rank == 0 && any) {
+      if (lane == 0) {
+        umma_commit_pair(drain_bar, 0x1);
+        volatile int no_abort = 0;
+        mbar_wait(drain_bar, 0, &no_abort, args.status, SITE_GEMM_DRAIN);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    // Two groups of four warps; group g drains accumulator g of this CTA (its 128 rows x 256
+    // columns) and then reports to the even CTA.
+    const int grp = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const uint32_t tempty0_cl = mapa_shared(tempty_bar(0), 0);
+    uint32_t acc_phase = 0;
+    int tcount = 0;  // tiles with MMAs seen so far (both groups count all of them)
+    bool ok = true;
+    for (int s = pair; s < total && ok; s += npairs) {
+      int e, f, row0, rows, nkb;
+      strip(s, e, f, row0, rows, nkb);
+      for (int i = 0; i < strip_len; ++i) {
+        // this CTA's rows m and the tile's columns n (256)
+        const int m0 = (STAT_A ? f : i) * 256 + half0;
+        const int n0 = (STAT_A ? i : f) * 256;
+        // out[e][n0 + col][m0 + quarter*32 + lane]
+        const size_t base = (size_t)e * args.M * args.N + (size_t)n0 * args.M + m0 + quarter * 32 + lane;
+        if (nkb == 0) {
+          // an expert without rows: its weight gradient is zero (the groups take alternate tiles)
+          if ((i & 1) != grp) continue;
+          for (int j = 0; j < 256; ++j) {
+            if (OUT_F32) reinterpret_cast<float*>(args.out)[base + (size_t)j * args.M] = 0.0f;
+            else reinterpret_cast<__nv_bfloat16*>(args.out)[base + (size_t)j * args.M] = __float2bfloat16_rn(0.0f);
+          }
+          continue;
+        }
+        const int acc = tcount & 1;
+        ++tcount;
+        if (acc != grp) continue;
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = mbar_wait<true>(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL,
+                                 kWaitLimitNs, 256);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tacc = tmem_base + acc * 256 + (uint32_t(quarter * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const size_t idx = base + (size_t)(c * 32 + j) * args.M;
+            if (OUT_F32) reinterpret_cast<float*>(args.out)[idx] = __uint_as_float(v[j]);
+            else reinterpret_cast<__nv_bfloat16*>(args.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0_cl + 8u * acc);
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+}  // namespace mok

@@ -155,8 +155,9 @@ def test_forward_backward_parity(shape, mode):
 @pytest.mark.parametrize("shape,mode", [(MID, None), (MID, "skewed_given"), (TINY, None)],
                          ids=lambda c: getattr(c, "name", str(c)))
 def test_row_tile_gemms_forward_backward(shape, mode):
-    """MOK_FLAG_GEMM_SINGLE: GEMM2 and dX_g on the 128-row-tile single-CTA kernels instead of the
-    narrow-segment pair kernel; o, y, dX_g and dX against the oracle."""
+    """MOK_FLAG_GEMM_SINGLE: the expert GEMMs on the 128-row-tile single-CTA kernels and the weight
+    gradients on single CTAs (128 x 128 tiles) instead of the CTA-pair kernels; o, y, dX_g, dX,
+    dW2 and dW13 against the oracle."""
     from mixture_experts_layer_table_gb300 import _native as N
     inp = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp)
@@ -170,6 +171,8 @@ def test_row_tile_gemms_forward_backward(shape, mode):
     assert_bf16_close(to_f64(y), fwd["y"], "y")
     assert_intermediate_close(to_f64(layer.view("dx_g")), bwd["dx_g"], "dx_g", rel=1e-3)
     assert_bf16_close(to_f64(g["dx"]), bwd["dx"], "dx")
+    assert_bf16_close(to_f64(g["dw2"]), bwd["dw2"], "dw2")
+    assert_bf16_close(to_f64(g["dw13"]), bwd["dw13"], "dw13")
 
 
 @pytest.mark.parametrize("shape", [MID, MID_SKEW], ids=lambda s: s.name)
