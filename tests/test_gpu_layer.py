@@ -221,6 +221,27 @@ def test_bitwise_deterministic():
         assert torch.equal(a, b)
 
 
+def test_repeated_backward_on_one_layer_single_cta_kernels():
+    """The single-CTA weight-gradient kernels deal their strips from counters in the workspace;
+    each backward call clears them, so repeated backward calls on one layer object (same
+    workspace) give the same gradients bit for bit, and the forward's status word survives."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    shape = MID_SKEW
+    inp = W.make_inputs(shape, seed=4, device="cpu")
+    dev = _gpu_inputs(inp)
+    layer = mok.MoELayer(mok.desc_from_shape(shape, flags=N.FLAG_GEMM_SINGLE))
+    layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"])
+    grads = []
+    for _ in range(3):
+        g = layer.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+        grads.append({n: g[n].clone() for n in ("dx", "dw13", "dw2")})
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    for g in grads[1:]:
+        for n in ("dx", "dw13", "dw2"):
+            assert torch.equal(g[n], grads[0][n]), n
+
+
 # ----------------------------------------------------------------------------- CTA-pair GEMMs
 
 # long expert segments (~750 rows: several 256-row pair tiles and a ragged one per expert)
