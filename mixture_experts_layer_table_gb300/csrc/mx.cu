@@ -8,6 +8,7 @@
 
 #include "kernels.cuh"
 #include "mx.cuh"
+#include "ptx.cuh"
 
 namespace mok {
 
@@ -48,41 +49,53 @@ __global__ void __launch_bounds__(256)
 }
 
 // x_g[r] = MX(x[src_of[r] / k]) along H: each 32-element block quantised and stored back as
-// bf16 (E4M3 * 2^X is exact in bf16).  One warp per row, one lane per 32-element block.
-__global__ void __launch_bounds__(256)
-    gather_rows_mx_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ src_of, int k, int R,
-                          int H, __nv_bfloat16* __restrict__ dst) {
-  const int warps = blockDim.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int nb = H / 32;
-  for (int r = blockIdx.x * warps + (threadIdx.x >> 5); r < R; r += gridDim.x * warps) {
-    const int tok = src_of[r] / k;
-    const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)tok * H);
-    uint4* d = reinterpret_cast<uint4*>(dst + (size_t)r * H);
-    for (int b = lane; b < nb; b += 32) {
-      float v[32];
+// bf16 (E4M3 * 2^X is exact in bf16).  One short-lived block of 128 threads per destination row
+// (as the bf16 gather): 16-byte coalesced loads and stores, 4 adjacent lanes per 32-element block
+// (mx_quantize8_x4), the source rows marked L2 evict-last (each is read k times).  A persistent
+// version with one lane per 32-element block (64-byte strided accesses) moved 3.6 TB/s.
+constexpr int GATHER_MX_THREADS = 128;
+__global__ void __launch_bounds__(GATHER_MX_THREADS)
+    gather_rows_mx_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ src_of, int k,
+                          int vec_per_row, __nv_bfloat16* __restrict__ dst) {
+  constexpr int V = 8;
+  const int r = blockIdx.x;
+  const int tok = src_of[r] / k;
+  const uint64_t keep = l2_policy_evict_last();
+  const uint4* s = reinterpret_cast<const uint4*>(src) + (size_t)tok * vec_per_row;
+  uint4* d = reinterpret_cast<uint4*>(dst) + (size_t)r * vec_per_row;
+  for (int base = threadIdx.x; base < vec_per_row; base += GATHER_MX_THREADS * V) {
+    uint4 u[V];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 u = s[b * 4 + c];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    for (int j = 0; j < V; ++j) {
+      const int i = base + j * GATHER_MX_THREADS;  // a warp's 32 lanes are all in range or none
+      if (i < vec_per_row)
+        asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                     : "=r"(u[j].x), "=r"(u[j].y), "=r"(u[j].z), "=r"(u[j].w)
+                     : "l"(s + i), "l"(keep));
+    }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(h[j]);
-          v[c * 8 + 2 * j] = f.x;
-          v[c * 8 + 2 * j + 1] = f.y;
+    for (int j = 0; j < V; ++j) {
+      const int i = base + j * GATHER_MX_THREADS;
+      if (i < vec_per_row) {
+        float v[8];
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[j]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(h[q]);
+          v[2 * q] = f.x;
+          v[2 * q + 1] = f.y;
         }
-      }
-      mx_quantize32(v, nullptr);
+        mx_quantize8_x4(v);
+        uint4 o;
+        uint32_t* p = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint4 u;
-        uint32_t* p = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          __nv_bfloat162 bb = __floats2bfloat162_rn(v[c * 8 + 2 * j], v[c * 8 + 2 * j + 1]);
-          p[j] = *reinterpret_cast<uint32_t*>(&bb);
+        for (int q = 0; q < 4; ++q) {
+          __nv_bfloat162 bb = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+          p[q] = *reinterpret_cast<uint32_t*>(&bb);
         }
-        d[b * 4 + c] = u;
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(d + i), "r"(o.x), "r"(o.y), "r"(o.z),
+                     "r"(o.w)
+                     : "memory");
       }
     }
   }
@@ -328,11 +341,9 @@ cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int 
 cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
                                   cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  const int warps = 8;
-  int blocks = (R + warps - 1) / warps;
-  blocks = min(blocks, n_sm * 8);
-  gather_rows_mx_kernel<<<blocks, warps * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), src_of, k, R, H,
-                                                       reinterpret_cast<__nv_bfloat16*>(dst));
+  (void)n_sm;
+  gather_rows_mx_kernel<<<R, GATHER_MX_THREADS, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), src_of, k, H / 8,
+                                                         reinterpret_cast<__nv_bfloat16*>(dst));
   return cudaGetLastError();
 }
 

@@ -106,4 +106,25 @@ __device__ __forceinline__ int mx_quantize32(float (&v)[32], uint8_t* q) {
   return X;
 }
 
+// The same quantisation with each 32-element block spread over 4 adjacent lanes of a warp (lane
+// 4m + q holds elements 8q .. 8q+7 of block m): the block maximum is combined with two
+// butterfly shuffles (a max is exact in any order), so the values are those of mx_quantize32.
+// All 32 lanes of the warp must call it.
+__device__ __forceinline__ void mx_quantize8_x4(float (&v)[8]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int X = mx_exponent(amax);
+  const float inv = exp2_int(-X);
+  const float sc = exp2_int(X);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 f = f32x2_from_e4m3x2(e4m3x2_from_f32(v[j] * inv, v[j + 1] * inv));
+    v[j] = f.x * sc;
+    v[j + 1] = f.y * sc;
+  }
+}
+
 }  // namespace mok
