@@ -81,10 +81,10 @@ bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_
 
 // W13 [E][2I][H] seen as [E][2][I][H]: one box of 64 K x 64 rows x both halves brings 64 gate
 // rows followed by the 64 up rows of the same intermediate indices.
-bool tmap_w13_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t E) {
+bool tmap_w13_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t E, uint32_t rows = 64) {
   const uint64_t dims[4] = {H, I, 2, E};
   const uint64_t strides[3] = {H * 2, I * H * 2, 2 * I * H * 2};
-  const uint32_t box[4] = {64, 64, 2, 1};
+  const uint32_t box[4] = {64, rows, 2, 1};
   return make_tmap(m, w13, 4, dims, strides, box);
 }
 
@@ -237,9 +237,11 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
                                 void* act_lo, int* status, int n_sm, int variant, cudaStream_t st) {
   if (variant == GEMM_NARROW) {
-    // W13[e] as [2][I][H]: each CTA takes 64 gate rows and their 64 up rows in one box
+    // W13[e] as [2][I][H]: each CTA takes 64 gate rows and their 64 up rows in one box (128 and
+    // 128 in the paired form, at >= 384 rows per expert)
+    const bool paired = (long long)R >= 384LL * E;
     CUtensorMap tw;
-    if (!tmap_w13_gate_up(&tw, w13, H, I, E)) return cudaErrorInvalidValue;
+    if (!tmap_w13_gate_up(&tw, w13, H, I, E, paired ? 128 : 64)) return cudaErrorInvalidValue;
     GemmArgs g = base_args(E, offsets, tile_off, status);
     g.N = I;
     g.K = H;
@@ -249,6 +251,7 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
     g.out1 = act_hi;
     g.out2 = act_lo;
     g.ld1 = I;
+    if (paired) return launch_narrow<false, false, 256, EPI_SWIGLU_PAIRED>(tw, x_g, nullptr, H, g, R, n_sm, st);
     return launch_narrow<false, false, 256, EPI_SWIGLU>(tw, x_g, nullptr, H, g, R, n_sm, st);
   }
   const bool pair = variant == GEMM_ROWS_PAIR;

@@ -59,7 +59,17 @@ constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom colum
 enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, MODE_RING = 4 };
 // EPI_SWIGLU_MX: SwiGLU with a quantised to MXFP8 along I (32-column blocks) and stored as bf16
 // (E4M3 * 2^X is exact in bf16), the A operand of the MXFP8 GEMM2.
-enum GemmEpi { EPI_F32 = 0, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_T_F32 = 4, EPI_T_BF16 = 5, EPI_SWIGLU_MX = 6 };
+// EPI_SWIGLU_PAIRED (narrow kernel only): SwiGLU with the gate and up rows of the same
+// intermediate indices in two MMAs sharing the row operand, h and u in one thread's TMEM columns.
+enum GemmEpi {
+  EPI_F32 = 0,
+  EPI_SWIGLU = 2,
+  EPI_SWIGLU_BWD = 3,
+  EPI_T_F32 = 4,
+  EPI_T_BF16 = 5,
+  EPI_SWIGLU_MX = 6,
+  EPI_SWIGLU_PAIRED = 7
+};
 // SPLIT_BMX: B is MXFP8 (E4M3 bytes + one E8M0 scale per 32 along K); TMA brings the bytes and
 // scales, eight converter warps write the exact bf16 values into the stage for the MMA.
 enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_BMX = 3 };

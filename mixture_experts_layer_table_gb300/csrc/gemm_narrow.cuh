@@ -55,25 +55,33 @@ __host__ __device__ __forceinline__ int narrow_x_boxes(int half, int& n64, bool&
 
 template <bool WMN, bool SPLIT, int NMAX_, int EPI = EPI_F32>
 struct NarrowCfg {
-  static_assert(EPI == EPI_F32 || (EPI == EPI_SWIGLU && !WMN && !SPLIT), "narrow GEMM epilogues");
+  static_assert(EPI == EPI_F32 || ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_PAIRED) && !WMN && !SPLIT),
+                "narrow GEMM epilogues");
+  // EPI_SWIGLU_PAIRED: each CTA's A is 128 gate rows and the 128 up rows of the same intermediate
+  // indices, two MMAs per K step (gate, up) share the row operand, h and u accumulate in columns
+  // [0, N) and [256, 256 + N) of one accumulator (no second one: the epilogue is not overlapped).
+  static constexpr bool kPaired = EPI == EPI_SWIGLU_PAIRED;
+  static constexpr int ACCS = kPaired ? 1 : 2;  // accumulators in TMEM
   static constexpr int PM = 256;                // weight rows (output columns) of a pair tile
   static constexpr int NMAX = NMAX_;            // rows of a pair tile at most
   // narrow_x_boxes(h) <= NMAX / 2 for every h <= NMAX / 2 when NMAX / 2 is a multiple of 32
   static_assert((NMAX / 2) % NARROW_XBOX_S == 0, "the boxes of one CTA's rows fit its X buffer");
   static constexpr int X_OP = (NMAX / 2) * 128; // one CTA's rows of one X operand x 64 K
-  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int A_BYTES = (kPaired ? 2 : 1) * 128 * BK * 2;
   static constexpr int X_OPS = SPLIT ? 2 : 1;
   static constexpr int STAGE_BYTES = A_BYTES + X_OPS * X_OP;
   static constexpr int STAGES = (208 * 1024 / STAGE_BYTES) < 8 ? (208 * 1024 / STAGE_BYTES) : 8;
-  // two accumulators of NMAX columns; tcgen05.alloc takes a power of two from 32 to 512
-  static constexpr int TMEM_COLS = 2 * NMAX <= 256 ? 256 : 512;
+  // two accumulators of NMAX columns (paired: one of 256 + NMAX); tcgen05.alloc takes a power of
+  // two from 32 to 512
+  static constexpr int TMEM_COLS = (kPaired || 2 * NMAX > 256) ? 512 : 256;
   static_assert(NMAX % 32 == 0 && NMAX >= 32 && 2 * NMAX <= 512, "accumulators must fit the TMEM allocation");
   static constexpr int THREADS = 192;
   // SwiGLU: one 32 x 32 fp32 block of h and one of u per pair of warps
   static constexpr int XBUF_BYTES = EPI == EPI_SWIGLU ? 2 * 2 * 32 * 32 * 4 : 0;
-  // weight tiles: 256 output columns, or (SwiGLU) 128 intermediate indices (gate and up rows)
+  // weight tiles: 256 output columns, or (SwiGLU) 128 intermediate indices (gate and up rows),
+  // or (paired) 256 intermediate indices
   static __host__ __device__ int m_tiles(const GemmArgs& a) {
-    return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + PM - 1) / PM;
+    return kPaired ? a.I / 256 : EPI == EPI_SWIGLU ? a.I / 128 : (a.N + PM - 1) / PM;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
     return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
@@ -232,6 +240,9 @@ __global__ void __launch_bounds__(192, 1)
           if (EPI == EPI_SWIGLU) {
             // 64 gate rows, then the 64 up rows of the same intermediate indices
             tma_load_4d_pair(sa, &tmW, fb, k0, t.m * 128 + 64 * (int)rank, 0, t.e, pol_w);
+          } else if (C::kPaired) {
+            // 128 gate rows, then the 128 up rows of the same intermediate indices
+            tma_load_4d_pair(sa, &tmW, fb, k0, t.m * 256 + 128 * (int)rank, 0, t.e, pol_w);
           } else if (WMN) {
             tma_load_3d_pair(sa, &tmW, fb, w_row, k0, t.e, pol_w);
             tma_load_3d_pair(sa + MN_ATOM_BYTES, &tmW, fb, w_row + 64, k0, t.e, pol_w);
@@ -298,7 +309,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * C::NMAX;
+        const uint32_t d_tmem = tmem_base + acc * C::NMAX;  // paired: acc = 0, up rows at +256
         for (int kb = 0; kb < nkb; ++kb) {
           int f_ok = 1;
           if (lane == 0) f_ok = mbar_wait<true>(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
@@ -313,8 +324,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t adesc = smem_desc_sw128(sa + (WMN ? k16 * 2048 : k16 * 32), a_lbo, a_sbo);
-              umma_f16_pair(d_tmem, adesc, smem_desc_sw128(sx + k16 * 32, 16, 1024), idesc,
-                            (kb | k16) != 0 ? 1u : 0u);
+              const uint64_t bdesc = smem_desc_sw128(sx + k16 * 32, 16, 1024);
+              umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | k16) != 0 ? 1u : 0u);
+              if (C::kPaired)
+                umma_f16_pair(d_tmem + 256, smem_desc_sw128(sa + 128 * 128 + k16 * 32, 16, 1024), bdesc, idesc,
+                              (kb | k16) != 0 ? 1u : 0u);
               if (SPLIT) umma_f16_pair(d_tmem, adesc, smem_desc_sw128(sx + C::X_OP + k16 * 32, 16, 1024), idesc, 1u);
             }
             umma_commit_pair(empty_bar(stage), 0x3);
@@ -329,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
         if (lane == 0) umma_commit_pair(tfull_bar(acc), 0x3);
         __syncwarp();
-        acc ^= 1;
+        acc = (acc + 1) % C::ACCS;
         if (acc == 0) acc_phase ^= 1;
       }
       if (any_mma) {
@@ -410,6 +424,36 @@ __global__ void __launch_bounds__(192, 1)
           }
           named_bar_sync(1 + qp, 64);  // the up warp has read it
         }
+      } else if (C::kPaired) {
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+        tc_fence_after();
+        // this thread's intermediate index: h in column n, u in column 256 + n of its lane
+        const int i = t.m * 256 + 128 * (int)rank + 32 * quarter + lane;
+        float* hrow = reinterpret_cast<float*>(args.out0) + (long long)t.row0 * args.ld0 + i;
+        __nv_bfloat16* arow_hi = reinterpret_cast<__nv_bfloat16*>(args.out1) + (long long)t.row0 * args.ld1 + i;
+        __nv_bfloat16* arow_lo = reinterpret_cast<__nv_bfloat16*>(args.out2) + (long long)t.row0 * args.ld1 + i;
+#pragma unroll 1
+        for (int n0 = 0; n0 < t.rows; n0 += 8) {
+          uint32_t hv[8], uv[8];
+          tmem_ld_32x32b_x8(tacc + n0, hv);
+          tmem_ld_32x32b_x8(tacc + 256 + n0, uv);
+          tmem_wait_ld();
+          const int nr = min(8, t.rows - n0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j < nr) {
+              const float h = __uint_as_float(hv[j]);
+              const float u = __uint_as_float(uv[j]);
+              const long long r = n0 + j;
+              hrow[r * args.ld0] = h;
+              hrow[r * args.ld0 + args.I] = u;
+              const float a = h / (1.0f + __expf(-h)) * u;
+              const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
+              arow_hi[r * args.ld1] = a_hi;
+              arow_lo[r * args.ld1] = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+            }
+          }
+        }
       } else {
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
         tc_fence_after();
@@ -439,7 +483,7 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0_cl + 8u * acc);
-      acc ^= 1;
+      acc = (acc + 1) % C::ACCS;
       if (acc == 0) acc_phase ^= 1;
     }
   }
