@@ -163,10 +163,12 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUten
 // the narrow kernel's row chunks).
 int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
 
-// Split-operand narrow GEMMs (GEMM2, dX_g): chunks of at most 192 rows when experts average at
-// most 160 rows (a 24 KB row stage leaves room for 5 stages instead of 4: measured 3% / 1% faster
-// at 128 rows per expert), else 256 (192-row chunks cut 512-row experts into 3 and were 10%
-// slower there).
+// Split-operand narrow GEMMs (GEMM2, dX_g): when experts average at most 160 rows, chunks of at
+// most 192 rows and two 256-row weight tiles per pair tile sharing the row stages (EPI_F32_PAIRED:
+// 57% of each stage is weights instead of 40%, which these fill-bound GEMMs turn into weight
+// bandwidth; measured at 128 rows per expert dX_g 3.02 -> 2.76 ms, GEMM2 1.58 -> 1.57 ms); else
+// chunks of 256 rows, one weight tile (192-row chunks cut 512-row experts into 3 and were 10%
+// slower there, and at that shape GEMM2 is near its MMA rate, where pairing gained nothing).
 bool narrow_short_rows(int R, int E) { return (long long)R <= 160LL * E; }
 
 // Narrow-segment GEMM on CTA pairs: W (K-major [E][N][K] or, WMN, MN-major [E][K][N]) against
@@ -292,7 +294,8 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
     g.K = I;
     g.out0 = out;
     g.ld0 = H;
-    if (narrow_short_rows(R, E)) return launch_narrow<false, true, 192>(tw, act_hi, act_lo, I, g, R, n_sm, st);
+    if (narrow_short_rows(R, E))
+      return launch_narrow<false, true, 192, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
     return launch_narrow<false, true, 256>(tw, act_hi, act_lo, I, g, R, n_sm, st);
   }
   CUtensorMap ta, ta2, tb;
@@ -351,7 +354,8 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
     g.out0 = dx_g;
     g.ld0 = H;
     if (dhu_lo == nullptr) return launch_narrow<true, false, 256>(tw, dhu_hi, nullptr, 2 * I, g, R, n_sm, st);
-    if (narrow_short_rows(R, E)) return launch_narrow<true, true, 192>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
+    if (narrow_short_rows(R, E))
+      return launch_narrow<true, true, 192, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
     return launch_narrow<true, true, 256>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
   }
   CUtensorMap ta, ta2, tb;

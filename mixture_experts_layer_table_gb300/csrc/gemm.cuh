@@ -61,6 +61,8 @@ enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, M
 // (E4M3 * 2^X is exact in bf16), the A operand of the MXFP8 GEMM2.
 // EPI_SWIGLU_PAIRED (narrow kernel only): SwiGLU with the gate and up rows of the same
 // intermediate indices in two MMAs sharing the row operand, h and u in one thread's TMEM columns.
+// EPI_F32_PAIRED (narrow kernel only): two weight tiles 256 rows apart in two MMAs sharing the row
+// operand, accumulated in columns [0, N) and [256, 256 + N).
 enum GemmEpi {
   EPI_F32 = 0,
   EPI_SWIGLU = 2,
@@ -68,7 +70,8 @@ enum GemmEpi {
   EPI_T_F32 = 4,
   EPI_T_BF16 = 5,
   EPI_SWIGLU_MX = 6,
-  EPI_SWIGLU_PAIRED = 7
+  EPI_SWIGLU_PAIRED = 7,
+  EPI_F32_PAIRED = 8  // narrow kernel only: two 256-row weight tiles per pair tile, fp32 out
 };
 // SPLIT_BMX: B is MXFP8 (E4M3 bytes + one E8M0 scale per 32 along K); TMA brings the bytes and
 // scales, eight converter warps write the exact bf16 values into the stage for the MMA.

@@ -55,12 +55,15 @@ __host__ __device__ __forceinline__ int narrow_x_boxes(int half, int& n64, bool&
 
 template <bool WMN, bool SPLIT, int NMAX_, int EPI = EPI_F32>
 struct NarrowCfg {
-  static_assert(EPI == EPI_F32 || ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_PAIRED) && !WMN && !SPLIT),
+  static_assert(EPI == EPI_F32 || EPI == EPI_F32_PAIRED ||
+                    ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_PAIRED) && !WMN && !SPLIT),
                 "narrow GEMM epilogues");
   // EPI_SWIGLU_PAIRED: each CTA's A is 128 gate rows and the 128 up rows of the same intermediate
   // indices, two MMAs per K step (gate, up) share the row operand, h and u accumulate in columns
   // [0, N) and [256, 256 + N) of one accumulator (no second one: the epilogue is not overlapped).
-  static constexpr bool kPaired = EPI == EPI_SWIGLU_PAIRED;
+  // EPI_F32_PAIRED: each CTA's A is its 128 rows of two weight tiles 256 rows apart (a pair tile
+  // covers 512 output columns), the same two-MMA arrangement.
+  static constexpr bool kPaired = EPI == EPI_SWIGLU_PAIRED || EPI == EPI_F32_PAIRED;
   static constexpr int ACCS = kPaired ? 1 : 2;  // accumulators in TMEM
   static constexpr int PM = 256;                // weight rows (output columns) of a pair tile
   static constexpr int NMAX = NMAX_;            // rows of a pair tile at most
@@ -81,7 +84,10 @@ struct NarrowCfg {
   // weight tiles: 256 output columns, or (SwiGLU) 128 intermediate indices (gate and up rows),
   // or (paired) 256 intermediate indices
   static __host__ __device__ int m_tiles(const GemmArgs& a) {
-    return kPaired ? a.I / 256 : EPI == EPI_SWIGLU ? a.I / 128 : (a.N + PM - 1) / PM;
+    return EPI == EPI_SWIGLU_PAIRED ? a.I / 256
+           : EPI == EPI_SWIGLU     ? a.I / 128
+           : EPI == EPI_F32_PAIRED ? (a.N + 2 * PM - 1) / (2 * PM)
+                                   : (a.N + PM - 1) / PM;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
     return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
@@ -240,9 +246,22 @@ __global__ void __launch_bounds__(192, 1)
           if (EPI == EPI_SWIGLU) {
             // 64 gate rows, then the 64 up rows of the same intermediate indices
             tma_load_4d_pair(sa, &tmW, fb, k0, t.m * 128 + 64 * (int)rank, 0, t.e, pol_w);
-          } else if (C::kPaired) {
+          } else if (EPI == EPI_SWIGLU_PAIRED) {
             // 128 gate rows, then the 128 up rows of the same intermediate indices
             tma_load_4d_pair(sa, &tmW, fb, k0, t.m * 256 + 128 * (int)rank, 0, t.e, pol_w);
+          } else if (EPI == EPI_F32_PAIRED) {
+            // this CTA's 128 rows of each of the two weight tiles of a 512-row pair tile
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int wr = t.m * 2 * C::PM + h * C::PM + 128 * (int)rank;
+              const uint32_t sh = sa + h * (C::A_BYTES / 2);
+              if (WMN) {
+                tma_load_3d_pair(sh, &tmW, fb, wr, k0, t.e, pol_w);
+                tma_load_3d_pair(sh + MN_ATOM_BYTES, &tmW, fb, wr + 64, k0, t.e, pol_w);
+              } else {
+                tma_load_3d_pair(sh, &tmW, fb, k0, wr, t.e, pol_w);
+              }
+            }
           } else if (WMN) {
             tma_load_3d_pair(sa, &tmW, fb, w_row, k0, t.e, pol_w);
             tma_load_3d_pair(sa + MN_ATOM_BYTES, &tmW, fb, w_row + 64, k0, t.e, pol_w);
@@ -325,11 +344,17 @@ __global__ void __launch_bounds__(192, 1)
             for (int k16 = 0; k16 < BK / 16; ++k16) {
               const uint64_t adesc = smem_desc_sw128(sa + (WMN ? k16 * 2048 : k16 * 32), a_lbo, a_sbo);
               const uint64_t bdesc = smem_desc_sw128(sx + k16 * 32, 16, 1024);
-              umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | k16) != 0 ? 1u : 0u);
-              if (C::kPaired)
-                umma_f16_pair(d_tmem + 256, smem_desc_sw128(sa + 128 * 128 + k16 * 32, 16, 1024), bdesc, idesc,
-                              (kb | k16) != 0 ? 1u : 0u);
+              const uint32_t first = (kb | k16) != 0 ? 1u : 0u;
+              umma_f16_pair(d_tmem, adesc, bdesc, idesc, first);
               if (SPLIT) umma_f16_pair(d_tmem, adesc, smem_desc_sw128(sx + C::X_OP + k16 * 32, 16, 1024), idesc, 1u);
+              if (C::kPaired) {
+                // the second weight tile (or the up rows): the other half of this stage's A
+                const uint64_t adesc2 =
+                    smem_desc_sw128(sa + C::A_BYTES / 2 + (WMN ? k16 * 2048 : k16 * 32), a_lbo, a_sbo);
+                umma_f16_pair(d_tmem + 256, adesc2, bdesc, idesc, first);
+                if (SPLIT)
+                  umma_f16_pair(d_tmem + 256, adesc2, smem_desc_sw128(sx + C::X_OP + k16 * 32, 16, 1024), idesc, 1u);
+              }
             }
             umma_commit_pair(empty_bar(stage), 0x3);
           }
@@ -424,7 +449,7 @@ __global__ void __launch_bounds__(192, 1)
           }
           named_bar_sync(1 + qp, 64);  // the up warp has read it
         }
-      } else if (C::kPaired) {
+      } else if (EPI == EPI_SWIGLU_PAIRED) {
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
         tc_fence_after();
         // this thread's intermediate index: h in column n, u in column 256 + n of its lane
@@ -457,25 +482,30 @@ __global__ void __launch_bounds__(192, 1)
       } else {
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
         tc_fence_after();
-        // this thread's output column; the accumulator's columns are the chunk's rows
-        const int j = t.m * C::PM + 128 * (int)rank + 32 * quarter + lane;
-        const bool jv = j < args.N;
-        float* o = out + (long long)t.row0 * args.ld0 + j;
+        // this thread's output column; the accumulator's columns are the chunk's rows (paired:
+        // the second weight tile, 256 output columns further, in accumulator columns 256 + n)
 #pragma unroll 1
-        for (int c = 0; c * 32 < t.rows; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, v);
-          tmem_wait_ld();
-          const int nr = min(32, t.rows - c * 32);
-          if (jv) {
-            float* oc = o + (long long)(c * 32) * args.ld0;
-            if (nr == 32) {
+        for (int half = 0; half < (C::kPaired ? 2 : 1); ++half) {
+          const int j = t.m * (C::kPaired ? 2 : 1) * C::PM + half * C::PM + 128 * (int)rank + 32 * quarter + lane;
+          const bool jv = j < args.N;
+          float* o = out + (long long)t.row0 * args.ld0 + j;
+          const uint32_t th = tacc + half * 256;
+#pragma unroll 1
+          for (int c = 0; c * 32 < t.rows; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(th + c * 32, v);
+            tmem_wait_ld();
+            const int nr = min(32, t.rows - c * 32);
+            if (jv) {
+              float* oc = o + (long long)(c * 32) * args.ld0;
+              if (nr == 32) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
-            } else {
+                for (int i = 0; i < 32; ++i) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nr) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+                for (int i = 0; i < 32; ++i)
+                  if (i < nr) oc[(long long)i * args.ld0] = __uint_as_float(v[i]);
+              }
             }
           }
         }
