@@ -254,6 +254,10 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
     g.out2 = act_lo;
     g.ld1 = I;
     if (paired) return launch_narrow<false, false, 256, EPI_SWIGLU_PAIRED>(tw, x_g, nullptr, H, g, R, n_sm, st);
+    // at most 160 rows per expert on average: 192-row chunks (7 stages instead of 6; 1% faster at
+    // 128 rows per expert)
+    if (narrow_short_rows(R, E))
+      return launch_narrow<false, false, 192, EPI_SWIGLU>(tw, x_g, nullptr, H, g, R, n_sm, st);
     return launch_narrow<false, false, 256, EPI_SWIGLU>(tw, x_g, nullptr, H, g, R, n_sm, st);
   }
   const bool pair = variant == GEMM_ROWS_PAIR;
