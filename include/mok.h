@@ -136,7 +136,8 @@ typedef struct {
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
   /* ring forward only (-1 otherwise) */
   int64_t ring;       /* bf16 [slots * minibatch][H]  the token ring */
-  int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb+1] tile starts */
+  int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb] tiles,
+                          [n_mb+1] tile starts (exclusive prefix of the tiles) */
   int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch */
   /* MXFP8 backward only (-1 otherwise): operands quantised along their GEMM's reduction
    * dimension, as exact bf16 values */

@@ -104,3 +104,51 @@ def test_min_minibatch_reproduces_page_number(lib):
 def test_status_strings(lib):
     assert mok.status_string(0) == "ok"
     assert "timed out" in mok.status_string(5)
+
+
+def _region_sizes(shp, ring_slots=0, minibatch=0):
+    """Bytes of each tensor, as the comments of mok_layout in include/mok.h state them."""
+    T, H, I, E, k = shp.T, shp.H, shp.I, shp.E, shp.k
+    R = T * k
+    ctx = {"topk_idx": R * 4, "gates": R * 4, "scores": T * E * 4, "counts": E * 4, "offsets": (E + 1) * 4,
+           "row_of": R * 4, "src_of": R * 4, "tile_off": (E + 1) * 4, "gate_row": R * 4, "x_g": R * H * 2,
+           "hu": R * 2 * I * 4}
+    ws = {"status": 64 * 4, "logits": T * E * 4, "act": R * I * 2, "act_lo": R * I * 2, "expert_out": R * H * 4,
+          "dy_g": R * H * 2, "dhu": R * 2 * I * 2, "dhu_lo": R * 2 * I * 2, "gact": R * I * 2,
+          "gact_lo": R * I * 2, "dx_g": R * H * 4, "dg_part": R * (I // 256) * 4, "dlogits": T * E * 4}
+    if minibatch:
+        n_mb = -(-R // minibatch)
+        ws.update({"ring": ring_slots * minibatch * H * 2,
+                   "mb_tables": (2 * n_mb * (E + 1) + n_mb + (n_mb + 1)) * 4, "mb_counters": 2 * n_mb * 4})
+    if shp.mxfp8:
+        ws.update({"mx_dhu_c": R * 2 * I * 2, "mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
+                   "mx_do_r": R * H * 2, "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4})
+    return ctx, ws
+
+
+@pytest.mark.parametrize("case", ["tiny", "dsv3", "skew", "mxfp8", "ring"])
+def test_every_region_sized_aligned_and_disjoint(lib, case):
+    """Each tensor of ctx and ws gets at least the bytes the header states, on a 256-byte boundary,
+    without overlapping another; tensors a descriptor does not use are -1."""
+    shp = {"tiny": W.TINY, "dsv3": W.DSV3, "skew": W.DSV3_SKEW, "mxfp8": W.DSV3_MXFP8, "ring": W.RING}[case]
+    kw, slots, m = {}, 0, 0
+    if case == "ring":
+        m = 2368
+        kw = dict(minibatch=m, ring_bytes=W.RING_BYTES)
+        slots = W.RING_BYTES // (m * shp.H * 2)
+    lay = mok.get_layout(mok.desc_from_shape(shp, **kw))
+    ctx, ws = _region_sizes(shp, slots, m)
+    assert set(ctx) == set(N.CTX_FIELDS)
+    for fields, sizes, total in ((N.CTX_FIELDS, ctx, lay["ctx_bytes"]), (N.WS_FIELDS, ws, lay["ws_bytes"])):
+        spans = []
+        for name in fields:
+            if name not in sizes:
+                assert lay[name] == -1, name
+                continue
+            off = lay[name]
+            assert off >= 0 and off % 256 == 0, name
+            spans.append((off, off + sizes[name], name))
+        spans.sort()
+        for a, b in zip(spans, spans[1:]):
+            assert a[1] <= b[0], (a[2], b[2])
+        assert spans[-1][1] <= total
