@@ -117,8 +117,13 @@ def test_router_topk_and_gates(shape):
 
 # ----------------------------------------------------------------------------- forward / backward
 
+LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=768, k=4,
+                  router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
+# skewed long segments: hot experts with several full 256-row blocks, cold ones with only a tail
+LONG_SKEW = LONG.scaled(name="long_skew", skew=True)
+# LONG: 750 rows per expert, the expert GEMMs' 256-row chunks and GEMM1's paired form
 CASES = [(TINY, None), (MID, None), (MID_SKEW, None), (MID, "skewed_given"), (ONE, None), (DENSE, None),
-         (MAXES, None)]
+         (MAXES, None), (LONG, None), (LONG_SKEW, None)]
 
 
 @pytest.mark.parametrize("shape,mode", CASES, ids=lambda c: getattr(c, "name", str(c)))
@@ -245,10 +250,6 @@ def test_repeated_backward_on_one_layer_single_cta_kernels():
 # ----------------------------------------------------------------------------- CTA-pair GEMMs
 
 # long expert segments (~750 rows: several 256-row pair tiles and a ragged one per expert)
-LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=768, k=4,
-                  router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
-# skewed long segments: hot experts with several full 256-row blocks, cold ones with only a tail
-LONG_SKEW = LONG.scaled(name="long_skew", skew=True)
 PAIR_CASES = [(LONG, None), (LONG_SKEW, None), (LONG, "skewed_given"), (MID, None), (MID, "skewed_given"),
               (TINY, None), (ONE, None)]
 
