@@ -46,13 +46,14 @@ def inputs_f64(inp):
     return {k: (to_f64(v) if v is not None else None) for k, v in inp.items()}
 
 
-def oracle_layer(shape, f64, topk_idx=None, backward=True):
+def oracle_layer(shape, f64, topk_idx=None, backward=True, route_scale=1.0):
     fwd = O.forward(f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router, k=shape.k,
-                    renorm=shape.renorm, router_bias=f64.get("router_bias"), topk_idx=topk_idx)
+                    renorm=shape.renorm, router_bias=f64.get("router_bias"), topk_idx=topk_idx,
+                    route_scale=route_scale)
     bwd = None
     if backward:
         bwd = O.backward(fwd, f64["dy"], f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router,
-                         k=shape.k, renorm=shape.renorm)
+                         k=shape.k, renorm=shape.renorm, route_scale=route_scale)
     return fwd, bwd
 
 

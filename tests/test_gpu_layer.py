@@ -48,9 +48,9 @@ def _lib(cuda_ok):
     mok.load()
 
 
-def _run(shape, inp, given=None, flags=0):
+def _run(shape, inp, given=None, flags=0, route_scale=1.0):
     dev = _gpu_inputs(inp)
-    layer = mok.MoELayer(mok.desc_from_shape(shape, flags=flags))
+    layer = mok.MoELayer(mok.desc_from_shape(shape, flags=flags, route_scale=route_scale))
     given_t = torch.tensor(given, dtype=torch.int32, device="cuda") if given is not None else None
     y = layer.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"],
                       given_topk=given_t)
@@ -155,6 +155,21 @@ def test_forward_backward_parity(shape, mode):
     assert_bf16_close(to_f64(g["dw13"]), bwd["dw13"], "dw13")
     assert_bf16_close(to_f64(g["dw_router"]), bwd["dw_router"], "dw_router")
     assert_bf16_close(to_f64(g["dx"]), bwd["dx"], "dx")
+
+
+@pytest.mark.parametrize("shape,scale", [(MID_SKEW, 2.5), (TINY, 0.7)], ids=lambda c: getattr(c, "name", str(c)))
+def test_route_scale(shape, scale):
+    """A route scale other than 1 (the gates times a constant after any renormalisation): gates,
+    y and every gradient against the oracle with the same scale."""
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    fwd, bwd = oracle_layer(shape, f64, route_scale=scale)
+    layer, y, g = _run(shape, inp, route_scale=scale)
+    assert np.array_equal(layer.view("topk_idx").cpu().numpy(), fwd["topk_idx"])
+    assert np.allclose(layer.view("gates").cpu().numpy(), fwd["gates"], rtol=2e-5, atol=1e-7)
+    assert_bf16_close(to_f64(y), fwd["y"], "y")
+    for name in ("dgates", "dw_router", "dw2", "dw13", "dx"):
+        assert_bf16_close(to_f64(g[name]), bwd[name], name)
 
 
 @pytest.mark.parametrize("shape,mode", [(MID, None), (MID, "skewed_given"), (TINY, None)],

@@ -222,16 +222,20 @@ def _selection_margin(x, w_r, kind, k, bias=None):
     return (srt[:, k - 1] - srt[:, k]).min()
 
 
-@pytest.mark.parametrize("kind,renorm", [(O.SOFTMAX, False), (O.SIGMOID, True), (O.SOFTMAX, True)])
-def test_backward_matches_central_differences(kind, renorm):
+@pytest.mark.parametrize("kind,renorm,scale,use_bias", [(O.SOFTMAX, False, 1.0, False), (O.SIGMOID, True, 1.0, False),
+                                                        (O.SOFTMAX, True, 1.0, False), (O.SIGMOID, False, 1.0, False),
+                                                        (O.SIGMOID, True, 2.5, True), (O.SOFTMAX, False, 0.7, False)])
+def test_backward_matches_central_differences(kind, renorm, scale, use_bias):
     x, w_r, w13, w2, dy, k = _tiny_case(kind, renorm)
-    assert _selection_margin(x, w_r, kind, k) > 1e-4
-    fwd = O.forward(x, w_r, w13, w2, kind=kind, k=k, renorm=renorm)
-    grads = O.backward(fwd, dy, x, w_r, w13, w2, kind=kind, k=k, renorm=renorm)
+    E = w_r.shape[0]
+    bias = np.linspace(-0.05, 0.05, E) if use_bias else None
+    assert _selection_margin(x, w_r, kind, k, bias) > 1e-4
+    fwd = O.forward(x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, router_bias=bias, route_scale=scale)
+    grads = O.backward(fwd, dy, x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, route_scale=scale)
     idx = fwd["topk_idx"]
 
     def loss(x_, w_r_, w13_, w2_):
-        f = O.forward(x_, w_r_, w13_, w2_, kind=kind, k=k, renorm=renorm, topk_idx=idx)
+        f = O.forward(x_, w_r_, w13_, w2_, kind=kind, k=k, renorm=renorm, topk_idx=idx, route_scale=scale)
         return float((dy * f["y"]).sum())
 
     eps = 1e-6
@@ -248,6 +252,25 @@ def test_backward_matches_central_differences(kind, renorm):
             minus[ai][ip] -= eps
             fd = (loss(*plus) - loss(*minus)) / (2 * eps)
             assert abs(fd - grads[name][ip]) <= 1e-6 * max(1.0, abs(fd)), (name, ip, fd, grads[name][ip])
+
+
+@pytest.mark.parametrize("kind,renorm", [(O.SOFTMAX, False), (O.SIGMOID, True)])
+def test_route_scale_is_linear(kind, renorm):
+    """For a fixed selection y is linear in the gates, and the gates in the route scale s: y and
+    every gradient at scale s are s times those at scale 1; the selection does not move."""
+    x, w_r, w13, w2, dy, k = _tiny_case(kind, renorm, seed=6)
+    f1 = O.forward(x, w_r, w13, w2, kind=kind, k=k, renorm=renorm)
+    g1 = O.backward(f1, dy, x, w_r, w13, w2, kind=kind, k=k, renorm=renorm)
+    s = 2.5
+    fs = O.forward(x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, route_scale=s)
+    gs = O.backward(fs, dy, x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, route_scale=s)
+    assert np.array_equal(fs["topk_idx"], f1["topk_idx"])
+    assert np.allclose(fs["gates"], s * f1["gates"], rtol=1e-14, atol=0)
+    assert np.allclose(fs["y"], s * f1["y"], rtol=1e-12, atol=1e-15)
+    for name in ("dx", "dw_router", "dw13", "dw2"):
+        assert np.allclose(gs[name], s * g1[name], rtol=1e-12, atol=1e-15), name
+    # d loss / d gate is <dY, o>, which does not depend on the gates
+    assert np.allclose(gs["dgates"], g1["dgates"], rtol=1e-12, atol=1e-15)
 
 
 def test_dgates_is_derivative_of_merge():
