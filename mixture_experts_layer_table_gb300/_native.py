@@ -98,6 +98,14 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _buf(t: torch.Tensor, name: str):
+    """Pointer and byte size of a ctx / ws buffer: device memory, contiguous (the library checks
+    the size against the layout)."""
+    if t is None or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return _ptr(t), t.numel() * t.element_size()
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -171,7 +179,7 @@ def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts
     _expect(src_of, (R,), torch.int32, "src_of")
     _check("mok_schedule", load().mok_schedule(
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(topk_idx),
-        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(gates), _ptr(counts), _ptr(offsets), _ptr(row_of), _ptr(src_of), *_buf(ws, "ws"),
         _stream(stream)))
 
 
@@ -181,8 +189,7 @@ def moe_forward(desc, x, w_router, router_bias, given_topk, w13, w2, y, ctx, ws,
     _expect(y, (desc.T, desc.H), torch.bfloat16, "y")
     _check("mok_moe_forward", load().mok_moe_forward(
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(w13), _ptr(w2),
-        _ptr(y), _ptr(ctx), ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(),
-        _stream(stream)))
+        _ptr(y), *_buf(ctx, "ctx"), *_buf(ws, "ws"), _stream(stream)))
 
 
 def moe_backward(desc, dy, x, w_router, w13, w2, ctx, dx, dw_router, dw13, dw2, dgates, ws, stream=None):
@@ -195,15 +202,14 @@ def moe_backward(desc, dy, x, w_router, w13, w2, ctx, dx, dw_router, dw13, dw2, 
     _expect(dw2, (desc.E, desc.H, desc.I), wdt, "dw2")
     _expect(dgates, (desc.T, desc.k), torch.float32, "dgates", nullable=True)
     _check("mok_moe_backward", load().mok_moe_backward(
-        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(w13), _ptr(w2), _ptr(ctx),
-        ctx.numel() * ctx.element_size(), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), _ptr(ws),
-        ws.numel() * ws.element_size(), _stream(stream)))
+        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(w13), _ptr(w2), *_buf(ctx, "ctx"),
+        _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), *_buf(ws, "ws"), _stream(stream)))
 
 
 def read_status(ws, stream=None):
     """Synchronises the stream and returns (code, site) of the first device-side error, then clears it."""
     out = (ctypes.c_int32 * 2)()
-    _check("mok_read_status", load().mok_read_status(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream), out))
+    _check("mok_read_status", load().mok_read_status(*_buf(ws, "ws"), _stream(stream), out))
     return int(out[0]), int(out[1])
 
 
@@ -224,7 +230,7 @@ def trace_stop() -> Dict[str, Dict[str, float]]:
 
 def test_bounded_wait(ws, limit_ms: int, stream=None):
     _check("mok_test_bounded_wait",
-           load().mok_test_bounded_wait(_ptr(ws), ws.numel() * ws.element_size(), limit_ms, _stream(stream)))
+           load().mok_test_bounded_wait(*_buf(ws, "ws"), limit_ms, _stream(stream)))
 
 
 _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.float32, "counts": torch.int32,
@@ -390,8 +396,8 @@ def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws
     fn.restype = ctypes.c_int32
     _check("mok_moe_forward_mxfp8", fn(
         ctypes.byref(desc), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(given_topk), _ptr(wq["w13_q"]),
-        _ptr(wq["w13_scale"]), _ptr(wq["w2_q"]), _ptr(wq["w2_scale"]), _ptr(y), _ptr(ctx),
-        ctx.numel() * ctx.element_size(), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+        _ptr(wq["w13_scale"]), _ptr(wq["w2_q"]), _ptr(wq["w2_scale"]), _ptr(y), *_buf(ctx, "ctx"),
+        *_buf(ws, "ws"), _stream(stream)))
     return y
 
 
@@ -426,6 +432,6 @@ def moe_backward_mxfp8(desc, dy, x, w_router, wb, ctx, dx, dw_router, dw13, dw2,
     fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
     fn.restype = ctypes.c_int32
     _check("mok_moe_backward_mxfp8", fn(
-        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(wb["w13_b"]), _ptr(wb["w2_b"]), _ptr(ctx),
-        ctx.numel() * ctx.element_size(), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), _ptr(ws),
-        ws.numel() * ws.element_size(), _stream(stream)))
+        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(wb["w13_b"]), _ptr(wb["w2_b"]),
+        *_buf(ctx, "ctx"), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), *_buf(ws, "ws"),
+        _stream(stream)))

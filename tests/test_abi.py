@@ -152,3 +152,32 @@ def test_every_region_sized_aligned_and_disjoint(lib, case):
         for a, b in zip(spans, spans[1:]):
             assert a[1] <= b[0], (a[2], b[2])
         assert spans[-1][1] <= total
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: without libmok.so the binding raises instead of computing anything."""
+    import subprocess
+    import sys
+    code = ("from mixture_experts_layer_table_gb300 import _native as N\n"
+            f"N.load({str(tmp_path / 'libmok.so')!r})\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "OSError" in r.stderr and "not found" in r.stderr
+
+
+def test_host_tensors_are_refused(lib):
+    """Every tensor the library reads or writes must be device memory: host tensors are refused
+    by the binding before any library call (there is no CPU path)."""
+    import torch
+    shp = W.TINY
+    d = mok.desc_from_shape(shp)
+    layer = mok.MoELayer(d, device="cpu")
+    inp = W.make_inputs(shp, seed=0, device="cpu")
+    with pytest.raises(ValueError, match="CUDA"):
+        layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    with pytest.raises(ValueError, match="CUDA"):
+        N.read_status(layer.ws)
+    with pytest.raises(ValueError, match="CUDA"):
+        N.test_bounded_wait(layer.ws, 10)
+    y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        N.moe_forward(d, inp["x"], inp["w_router"], None, None, inp["w13"], inp["w2"], y, layer.ctx, layer.ws)
