@@ -181,3 +181,55 @@ def test_host_tensors_are_refused(lib):
     y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         N.moe_forward(d, inp["x"], inp["w_router"], None, None, inp["w13"], inp["w2"], y, layer.ctx, layer.ws)
+
+
+def test_entry_points_reject_bad_arguments_before_any_device_work(lib):
+    """The argument checks of the C ABI return their error codes before the library touches the
+    GPU, so they are exercised here with placeholder (never dereferenced) addresses: a null or
+    misaligned tensor is an invalid argument, a ctx / ws one byte short is too small, and a
+    descriptor of the other precision is unsupported.  Host-only: with a GPU present a regression
+    in the order of the checks could hand the placeholders to a kernel."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("placeholder addresses are for hosts without a GPU")
+    P, SZ = ctypes.c_void_p, ctypes.c_size_t
+    D = ctypes.POINTER(N.LayerDesc)
+    fwd_mx = lib.mok_moe_forward_mxfp8
+    fwd_mx.argtypes = [D] + [P] * 9 + [P, SZ, P, SZ, P]
+    bwd_mx = lib.mok_moe_backward_mxfp8
+    bwd_mx.argtypes = [D] + [P] * 6 + [SZ] + [P] * 6 + [SZ, P]
+    for f in (fwd_mx, bwd_mx):
+        f.restype = ctypes.c_int32
+    bf = mok.desc_from_shape(W.TINY)
+    mx = mok.desc_from_shape(W.TINY.scaled(mxfp8=True))
+    lay = mok.get_layout(bf)
+    lay_mx = mok.get_layout(mx)
+    a = [P(0x100000 * (i + 1)) for i in range(16)]   # 16-byte aligned placeholders
+    ctx_n, ws_n = lay["ctx_bytes"], lay["ws_bytes"]
+
+    def fwd(desc, x=a[0], ctx_n=ctx_n, ws_n=ws_n):
+        return lib.mok_moe_forward(ctypes.byref(desc), x, a[1], None, None, a[2], a[3], a[4], a[5], ctx_n, a[6],
+                                   ws_n, None)
+
+    def bwd(desc, dy=a[0], ctx_n=ctx_n, ws_n=ws_n):
+        return lib.mok_moe_backward(ctypes.byref(desc), dy, a[1], a[2], a[3], a[4], a[5], ctx_n, a[6], a[7],
+                                    a[8], a[9], None, a[10], ws_n, None)
+
+    for call in (fwd, bwd):
+        assert call(bf, ctx_n=ctx_n - 1) == 3
+        assert call(bf, ws_n=ws_n - 1) == 3
+        assert call(bf, P(0x100008), ctx_n=ctx_n - 1) == 1      # misaligned: checked first
+        assert call(bf, None, ctx_n=ctx_n - 1) == 1
+        assert call(mx) == 2                                    # MXFP8 has its own entry points
+    m_ctx, m_ws = lay_mx["ctx_bytes"], lay_mx["ws_bytes"]
+    assert fwd_mx(ctypes.byref(bf), *a[:9], a[9], m_ctx, a[10], m_ws, None) == 2
+    assert fwd_mx(ctypes.byref(mx), *a[:9], a[9], m_ctx, a[10], m_ws - 1, None) == 3
+    assert fwd_mx(ctypes.byref(mx), None, *a[1:9], a[9], m_ctx, a[10], m_ws - 1, None) == 1
+    assert bwd_mx(ctypes.byref(bf), *a[:6], m_ctx, *a[6:12], m_ws, None) == 2
+    assert bwd_mx(ctypes.byref(mx), *a[:6], m_ctx - 1, *a[6:12], m_ws, None) == 3
+    assert bwd_mx(ctypes.byref(mx), *a[:5], P(0x100004), m_ctx - 1, *a[6:12], m_ws, None) == 1
+    # schedule: ws one byte short, and a missing output
+    sch = lambda topk, ws_n: lib.mok_schedule(ctypes.byref(bf), a[0], a[1], None, None, topk, a[2], a[3], a[4], a[5],
+                                              a[6], a[7], ws_n, None)
+    assert sch(a[8], ws_n - 1) == 3
+    assert sch(None, ws_n) == 1
