@@ -273,6 +273,31 @@ def test_route_scale_is_linear(kind, renorm):
     assert np.allclose(gs["dgates"], g1["dgates"], rtol=1e-12, atol=1e-15)
 
 
+def test_unselected_experts_have_zero_gradient_and_no_influence():
+    """With a selection that never picks some experts: their dW13 / dW2 are exactly zero, and
+    changing their weights changes neither y nor any other gradient (an expert-index slip in the
+    grouped steps would move one of these)."""
+    rng = np.random.default_rng(11)
+    T, H, E, I, k = 9, 12, 6, 8, 2
+    x, w_r, w13, w2 = _rand_layer(rng, T, H, E, I, scale=0.3)
+    dy = rng.normal(0, 1, (T, H))
+    idx = np.array([[(t % 3) * 2, (t % 3) * 2 + 2 if t % 3 < 2 else 0] for t in range(T)], dtype=np.int32)
+    unused = sorted(set(range(E)) - set(idx.ravel().tolist()))
+    assert unused == [1, 3, 5]
+    kw = dict(kind=O.SIGMOID, k=k, renorm=True)
+    f = O.forward(x, w_r, w13, w2, topk_idx=idx, **kw)
+    g = O.backward(f, dy, x, w_r, w13, w2, **kw)
+    assert not g["dw13"][unused].any() and not g["dw2"][unused].any()
+    w13b, w2b = w13.copy(), w2.copy()
+    w13b[unused] = rng.normal(0, 5.0, w13b[unused].shape)
+    w2b[unused] = rng.normal(0, 5.0, w2b[unused].shape)
+    fb = O.forward(x, w_r, w13b, w2b, topk_idx=idx, **kw)
+    gb = O.backward(fb, dy, x, w_r, w13b, w2b, **kw)
+    assert np.array_equal(fb["y"], f["y"])
+    for name in ("dx", "dw_router", "dw13", "dw2", "dgates"):
+        assert np.array_equal(gb[name], g[name]), name
+
+
 def test_dgates_is_derivative_of_merge():
     x, w_r, w13, w2, dy, k = _tiny_case(O.SIGMOID, True, seed=4)
     fwd = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True)
