@@ -153,6 +153,11 @@ typedef struct {
 /* Fills *layout (and so the ctx and ws sizes) for a descriptor.  Host only. */
 mok_status mok_get_layout(const mok_layer_desc* desc, mok_layout* layout);
 
+/* The two sizes alone: *ws_bytes and *ctx_bytes are layout.ws_bytes and layout.ctx_bytes of
+ * mok_get_layout.  Host only; MOK_ERR_INVALID_ARG for a null output, otherwise the descriptor's
+ * validation status (outputs untouched on error). */
+mok_status mok_workspace_size(const mok_layer_desc* desc, size_t* ws_bytes, size_t* ctx_bytes);
+
 /* Router + schedule table (the "unified schedule table" of the pull-dispatch section of
  * "Mixture-of-Kittens (MoK)", sd114.wiki; fields and reading as in the layout above).
  *   x [T][H] bf16, w_router [E][H] bf16, router_bias f32 [E] or NULL (added to the

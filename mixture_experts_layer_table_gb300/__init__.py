@@ -6,4 +6,5 @@ workloads (``workloads``).
 """
 from ._native import (LayerDesc, MoELayer, MokError, desc_from_shape, get_layout, load, make_desc,  # noqa: F401
                       min_minibatch, moe_backward, moe_backward_mxfp8, moe_forward, moe_forward_mxfp8,
-                      quantize_weights, quantize_weights_backward, read_status, schedule, status_string)
+                      quantize_weights, quantize_weights_backward, read_status, schedule, status_string,
+                      workspace_size)

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Dict, Optional
+from typing import Dict, Optional, Tuple
 
 import torch
 
@@ -55,7 +55,7 @@ class TraceEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_float)]
 
 
-EXPORTS = ["mok_get_layout", "mok_schedule", "mok_moe_forward", "mok_moe_backward", "mok_read_status",
+EXPORTS = ["mok_get_layout", "mok_workspace_size", "mok_schedule", "mok_moe_forward", "mok_moe_backward", "mok_read_status",
            "mok_test_bounded_wait", "mok_status_string", "mok_min_minibatch", "mok_trace_start", "mok_trace_stop"]
 
 _lib = None
@@ -72,6 +72,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
     D = ctypes.POINTER(LayerDesc)
     lib.mok_get_layout.argtypes = [D, ctypes.POINTER(Layout)]
+    lib.mok_workspace_size.argtypes = [D, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
     lib.mok_schedule.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
     lib.mok_moe_forward.argtypes = [D, P, P, P, P, P, P, P, P, SZ, P, SZ, P]
     lib.mok_moe_backward.argtypes = [D, P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
@@ -132,6 +133,13 @@ def get_layout(desc: LayerDesc) -> Dict[str, int]:
     lay = Layout()
     _check("mok_get_layout", load().mok_get_layout(ctypes.byref(desc), ctypes.byref(lay)))
     return {n: getattr(lay, n) for n in LAYOUT_FIELDS}
+
+
+def workspace_size(desc: LayerDesc) -> Tuple[int, int]:
+    """(ws_bytes, ctx_bytes) for a descriptor (mok_workspace_size)."""
+    ws, ctx = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("mok_workspace_size", load().mok_workspace_size(ctypes.byref(desc), ctypes.byref(ws), ctypes.byref(ctx)))
+    return int(ws.value), int(ctx.value)
 
 
 def min_minibatch(n_sm: int, I: int) -> int:

@@ -219,6 +219,16 @@ mok_status mok_get_layout(const mok_layer_desc* desc, mok_layout* layout) {
   return fill_layout(desc, layout);
 }
 
+mok_status mok_workspace_size(const mok_layer_desc* desc, size_t* ws_bytes, size_t* ctx_bytes) {
+  if (ws_bytes == nullptr || ctx_bytes == nullptr) return MOK_ERR_INVALID_ARG;
+  mok_layout L;
+  const mok_status s = mok_get_layout(desc, &L);
+  if (s != MOK_OK) return s;
+  *ws_bytes = (size_t)L.ws_bytes;
+  *ctx_bytes = (size_t)L.ctx_bytes;
+  return MOK_OK;
+}
+
 int32_t mok_min_minibatch(int32_t n_sm, int32_t I) {
   if (n_sm <= 0) n_sm = sm_count();
   return min_minibatch_rows(n_sm, I);

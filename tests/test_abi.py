@@ -233,3 +233,17 @@ def test_entry_points_reject_bad_arguments_before_any_device_work(lib):
                                               a[6], a[7], ws_n, None)
     assert sch(a[8], ws_n - 1) == 3
     assert sch(None, ws_n) == 1
+
+
+@pytest.mark.parametrize("case", ["tiny", "dsv3", "mxfp8", "ring"])
+def test_workspace_size_matches_layout(lib, case):
+    shp = {"tiny": W.TINY, "dsv3": W.DSV3, "mxfp8": W.DSV3_MXFP8, "ring": W.RING}[case]
+    kw = dict(minibatch=2368, ring_bytes=W.RING_BYTES) if case == "ring" else {}
+    d = mok.desc_from_shape(shp, **kw)
+    lay = mok.get_layout(d)
+    assert mok.workspace_size(d) == (lay["ws_bytes"], lay["ctx_bytes"])
+    ws, ctx = ctypes.c_size_t(7), ctypes.c_size_t(7)
+    assert lib.mok_workspace_size(ctypes.byref(d), None, ctypes.byref(ctx)) == 1
+    d.k = d.E + 1                       # invalid descriptor: its status, outputs untouched
+    assert lib.mok_workspace_size(ctypes.byref(d), ctypes.byref(ws), ctypes.byref(ctx)) == 1
+    assert ws.value == 7 and ctx.value == 7
