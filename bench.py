@@ -185,6 +185,26 @@ def cpu_sample_subprocess(T, E, repeats=1):
     return times, cores
 
 
+def cpu_model():
+    """The host CPU's model name (/proc/cpuinfo, else lscpu, else the machine type)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
 def sample_desc(T, E):
     return (f"float64 oracle forward+backward on {T} tokens of the same layer shape (hidden 7168, "
             f"intermediate 2048, top-8 sigmoid router, renormalised) restricted to {E} experts, "
@@ -232,7 +252,7 @@ def run_reference(args, rank, world):
             "config": {"workload": "dsv3_T4096_H7168_E256_I2048_top8_sigmoid (sampled: %d tokens, %d experts)" % (T, E),
                        "passes": "fwd+bwd"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": sample_desc(T, E)},
+                             "sample": sample_desc(T, E), "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -470,7 +490,8 @@ def run_mok(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         times, cores = cpu_sample_subprocess(CPU_SAMPLE["T"], CPU_SAMPLE["E"], repeats=1)
         cpu = {"value": CPU_SAMPLE["T"] / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": sample_desc(CPU_SAMPLE["T"], CPU_SAMPLE["E"]), "seconds": round(times[0], 2)}
+               "sample": sample_desc(CPU_SAMPLE["T"], CPU_SAMPLE["E"]), "seconds": round(times[0], 2),
+               "cpu_model": cpu_model()}
 
     step_bytes = 2 * T * H * 2
     line = {
