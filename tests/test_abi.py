@@ -247,3 +247,17 @@ def test_workspace_size_matches_layout(lib, case):
     d.k = d.E + 1                       # invalid descriptor: its status, outputs untouched
     assert lib.mok_workspace_size(ctypes.byref(d), ctypes.byref(ws), ctypes.byref(ctx)) == 1
     assert ws.value == 7 and ctx.value == 7
+
+
+def test_trace_argument_checks(lib):
+    """mok_trace_start takes 1 .. 2^20 launches and refuses a second start; mok_trace_stop without
+    a trace running is an invalid argument (no device needed for these answers)."""
+    n = ctypes.c_int32(-1)
+    assert lib.mok_trace_start(0) == 1
+    assert lib.mok_trace_start((1 << 20) + 1) == 1
+    assert lib.mok_trace_stop(None, 0, ctypes.byref(n)) == 1
+    code = lib.mok_trace_start(4)
+    assert code in (0, 4)                  # 4 (a CUDA error) on a host without a GPU
+    if code == 0:
+        assert lib.mok_trace_start(4) == 1
+        assert lib.mok_trace_stop(None, 0, ctypes.byref(n)) == 0 and n.value == 0
