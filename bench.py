@@ -185,6 +185,14 @@ def cpu_sample_subprocess(T, E, repeats=1):
     return times, cores
 
 
+def tensor_sha256(t):
+    """SHA-256 of a tensor's bit pattern (row-major bytes), read back to the host."""
+    import hashlib
+    import torch
+    b = t.detach().contiguous().cpu().reshape(-1).view(torch.uint8)
+    return hashlib.sha256(b.numpy().tobytes()).hexdigest()
+
+
 def cpu_model():
     """The host CPU's model name (/proc/cpuinfo, else lscpu, else the machine type)."""
     try:
@@ -520,6 +528,9 @@ def run_mok(args, rank, world, local_rank):
                         "the copies of neighbouring steps overlap the compute on a second stream"},
         "mxfp8_fwd": mx,
         "tensor_bound_fwd": tb,
+        "inputs": {"seed": 1000 * rank, "generators": "x, W_r, W13, W2, dY from seeds seed+0..4 (fp32 draws "
+                   "rounded to bf16)", "sha256": {"x": tensor_sha256(x), "w_router": tensor_sha256(wr),
+                                                  "dy": tensor_sha256(dy)}},
         "gpu_launches": launches,
         "clocks": clocks,
         "cpu_baseline": cpu,

@@ -38,3 +38,18 @@ def test_reference_arm_prints_one_contract_line():
 def test_warmup_below_three_is_refused():
     r = _run("--impl", "reference", "--steps", "1", "--warmup", "1", timeout=300)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_tensor_sha256_is_the_bit_pattern_digest():
+    import hashlib
+
+    import numpy as np
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    t = torch.tensor([[1.0, -2.5], [3.0, 0.125]], dtype=torch.bfloat16)
+    raw = t.view(torch.int16).numpy().astype("<i2").tobytes()
+    assert bench.tensor_sha256(t) == hashlib.sha256(raw).hexdigest()
+    f = torch.arange(6, dtype=torch.float32).reshape(2, 3)
+    assert bench.tensor_sha256(f) == hashlib.sha256(np.arange(6, dtype="<f4").tobytes()).hexdigest()
+    assert bench.tensor_sha256(f.t()) != bench.tensor_sha256(f)     # row-major bytes of the view
