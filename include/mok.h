@@ -29,9 +29,11 @@
  *   - Outputs are overwritten, never accumulated.  Results are bitwise reproducible for
  *     the same inputs, descriptor and device: every reduction runs in a fixed order and
  *     no floating-point atomics are used.
- *   - No C++ exception crosses this boundary.  No global mutable state besides a per-device
- *     cache of the SM count, the driver entry point used to encode TMA descriptors and the
- *     optional per-kernel trace (mok_trace_start / mok_trace_stop).
+ *   - No C++ exception crosses this boundary.  No global mutable state besides per-device
+ *     caches of the SM count and of how many CTA pairs of each pair kernel fit at once, the
+ *     driver entry point used to encode TMA descriptors, the optional per-kernel trace
+ *     (mok_trace_start / mok_trace_stop) and the fixed device scratch of
+ *     mok_schedule_noalloc.  The caches are filled on first use with idempotent values.
  */
 #ifndef MOK_H_
 #define MOK_H_
