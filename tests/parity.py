@@ -73,3 +73,26 @@ def selection_is_valid(sel_scores, gpu_idx, k, rel_margin=1e-5):
             hi = max(sel_scores[t, e] for e in range(E) if e not in chosen)
             assert lo >= hi - rel_margin * max(abs(hi), 1.0), f"token {t}: {lo} < {hi}"
     return n_diff
+
+
+def clear_margin_tokens(sel_scores, k, n, seed, margin=1e-4):
+    """n tokens drawn (seeded) among those whose k-th and (k+1)-th selection scores differ by
+    more than `margin`, so that the GPU's fp32 router and the oracle must pick the same experts."""
+    srt = -np.sort(-sel_scores, axis=1)
+    ok = np.nonzero(srt[:, k - 1] - srt[:, k] > margin)[0]
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(ok, size=min(n, ok.size), replace=False))
+
+
+def check_sampled_token_outputs(tokens, x_rows, w_router, router_bias, expert_weights, shape, y_rows, idx_rows,
+                                name):
+    """Output rows of sampled tokens against the oracle computing each token on its own: the
+    GPU's experts for each token must be the oracle's, and the rows must meet the bf16 bar.
+    x_rows / y_rows / idx_rows hold the sampled tokens' rows (float64 / float64 / int)."""
+    want = []
+    for i, t in enumerate(tokens):
+        y_t, idx, _, _, _ = O.token_forward(x_rows[i], w_router, router_bias, expert_weights, kind=shape.router,
+                                            k=shape.k, renorm=shape.renorm)
+        assert list(idx) == list(idx_rows[i]), f"{name}: token {t} experts {list(idx_rows[i])} vs {list(idx)}"
+        want.append(y_t)
+    assert_bf16_close(np.asarray(y_rows), np.array(want), name)

@@ -1,0 +1,80 @@
+"""Full-size parity at the tensor-bound shape the benchmark times: T=16384 tokens of the DSV3
+layer (hidden 7168, 256 experts of intermediate 2048, top-8 sigmoid router with renormalised
+gates), 512 rows per expert, where GEMM1 takes its paired form and the expert GEMMs cut each
+expert into 256-row chunks; plain, and through the 512 MiB token ring at the minibatch of two
+GEMM1 waves (2368 rows).
+
+The oracle computes sampled tokens on their own (each needs only its k experts) and the ring
+forward must be bitwise the plain one.  Tokens are drawn among those whose k-th and (k+1)-th
+router scores differ clearly, so that the GPU's fp32 router and the float64 oracle pick the
+same experts.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_table_gb300 as mok
+from mixture_experts_layer_table_gb300 import workloads as W
+from oracle import moe_oracle as O
+from tests.parity import check_sampled_token_outputs, clear_margin_tokens, to_f64
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = W.RING
+MINIBATCH = 2368
+N_TOKENS = 6
+N_CANDIDATES = 64
+
+
+@pytest.fixture(scope="module")
+def run(cuda_ok):
+    from mixture_experts_layer_table_gb300 import build
+    build.build()
+    mok.load()
+    inp = W.make_inputs(SHAPE, seed=0, device="cuda", with_dy=False)
+    plain = mok.MoELayer(mok.desc_from_shape(SHAPE))
+    y_plain = plain.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    torch.cuda.synchronize()
+    assert plain.status() == (0, 0)
+    idx = plain.view("topk_idx").cpu().numpy()
+    del plain
+    torch.cuda.empty_cache()
+    ring = mok.MoELayer(mok.desc_from_shape(SHAPE, minibatch=MINIBATCH, ring_bytes=W.RING_BYTES))
+    assert ring.layout["ring"] >= 0
+    y_ring = ring.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    torch.cuda.synchronize()
+    assert ring.status() == (0, 0)
+    idx_ring = ring.view("topk_idx").cpu().numpy()
+    del ring
+    torch.cuda.empty_cache()
+    return inp, idx, y_plain, idx_ring, y_ring
+
+
+def test_ring_forward_is_bitwise_the_plain_forward(run):
+    _, idx, y_plain, idx_ring, y_ring = run
+    assert np.array_equal(idx, idx_ring)
+    assert torch.equal(y_plain, y_ring)
+
+
+def test_sampled_tokens_against_the_oracle(run):
+    inp, idx, y_plain, _, _ = run
+    rng = np.random.default_rng(1)
+    cand = np.sort(rng.choice(SHAPE.T, size=N_CANDIDATES, replace=False))
+    w_r = to_f64(inp["w_router"])
+    x_c = to_f64(inp["x"][torch.as_tensor(cand, device=inp["x"].device)])
+    _, scores = O.router_scores(x_c, w_r, SHAPE.router)
+    pick = clear_margin_tokens(scores, SHAPE.k, N_TOKENS, seed=2)
+    assert len(pick) == N_TOKENS
+    toks = cand[pick]
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            if len(cache) > 8:
+                cache.pop(next(iter(cache)))
+            cache[e] = (to_f64(inp["w13"][e]), to_f64(inp["w2"][e]))
+        return cache[e]
+
+    y_rows = to_f64(y_plain[torch.as_tensor(toks, device=y_plain.device)])
+    check_sampled_token_outputs(toks, x_c[pick], w_r, None, experts, SHAPE, y_rows, idx[toks],
+                                "y (T=16384, sampled tokens)")
