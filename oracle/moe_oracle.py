@@ -468,3 +468,98 @@ def token_forward(x_t, w_router, router_bias, expert_weights, *, kind, k, renorm
         outs.append(o)
         y += g[j] * o
     return y, idx, g, outs, r["scores"][0]
+
+
+def token_backward(x_t, dy_t, w_router, router_bias, expert_weights, *, kind, k, renorm,
+                   route_scale=1.0, topk_idx=None, quant=None):
+    """Input gradient and gate gradients of one token, computed on its own.
+
+    The per-token part of ``backward`` (for sampled checks at full size): each step
+    below is the step of ``backward`` restricted to the k rows of token t, in the same
+    order and with the same operands.  For the expert j = 0..k-1 of the token:
+
+    * h, u       = the forward's gate and up projections (``token_forward``)
+    * dA'_j      = dY[t] W2[e_j]                (reduction over H)
+    * dg_j       = <dA'_j, a_j>                 (the gate gradient, formed in the
+                                                 SwiGLU backward: [wiki] benchmark section)
+    * dA_j       = g_j dA'_j
+    * dh, du     = dA_j * u * silu'(h), dA_j * silu(h)
+    * dX_g row   = [dh | du] W13[e_j]           (reduction over 2I)
+
+    then dl = ``router_backward`` of the k gate gradients and
+    dX[t] = sum over j of the dX_g rows (j in order) + dl W_r.  ``quant`` as in
+    ``backward``: every operand of these row GEMMs is quantised along its reduction
+    axis (dY and W2[e] along H, [dh | du] and W13[e] along 2I; the forward's as in
+    ``token_forward``).  ``topk_idx`` fixes the token's experts.
+    Returns a dict: dx [H], dgates [k], dl [E], dhu [k][2I], dx_g [k][H], topk_idx,
+    gates, y.
+    """
+    r = route(x_t[None, :], w_router, router_bias, kind, k, renorm, route_scale)
+    idx = r["topk_idx"][0] if topk_idx is None else np.asarray(topk_idx, dtype=np.int32)
+    scores = r["scores"]
+    g = gate_values(scores, idx[None, :], renorm, route_scale)[0]
+    q = quant if quant is not None else (lambda v, axis: v)
+    xq = q(x_t[None, :], 1)[0]
+    dyq = q(dy_t[None, :], 1)[0]
+    y = np.zeros_like(x_t)
+    dgates = np.zeros(k)
+    dhu = []
+    dx_g = []
+    for j in range(k):
+        w13_e, w2_e = expert_weights(int(idx[j]))
+        I = w13_e.shape[0] // 2
+        w13_f = q(w13_e, 1)
+        h = w13_f[:I] @ xq
+        u = w13_f[I:] @ xq
+        a = silu(h) * u
+        y += g[j] * (q(w2_e, 1) @ q(a[None, :], 1)[0])
+        dA_prime = q(w2_e, 0).T @ dyq
+        dgates[j] = dA_prime @ a
+        dA = g[j] * dA_prime
+        dhu_j = np.concatenate([dA * u * dsilu(h), dA * silu(h)])
+        dhu.append(dhu_j)
+        dx_g.append(q(dhu_j[None, :], 1)[0] @ q(w13_e, 0))
+    dl = router_backward(dgates[None, :], scores, idx[None, :], kind, renorm, route_scale)[0]
+    dx = np.zeros_like(x_t)
+    for j in range(k):
+        dx += dx_g[j]
+    dx += dl @ w_router
+    return {"dx": dx, "dgates": dgates, "dl": dl, "dhu": np.array(dhu), "dx_g": np.array(dx_g),
+            "topk_idx": idx, "gates": g, "y": y}
+
+
+def expert_weight_grads(x_rows, dy_rows, g_rows, w13_e, w2_e, *, rows13=None, rows2=None, quant=None):
+    """Weight gradients of one expert from that expert's rows alone (sampled checks at full size).
+
+    ``x_rows`` [n][H] and ``dy_rows`` [n][H] are the expert's dispatched input and
+    upstream-gradient rows in schedule order (ascending assignment), ``g_rows`` [n] their
+    gates.  The steps are those of ``backward`` for one expert segment:
+
+    * h | u      = x W13[e]^T,  a = silu(h) * u
+    * dA'        = dY W2[e],  dg = <dA', a> per row,  dA = g * dA'
+    * dO         = g * dY,    dW2[e] = dO^T a       (reduction over the expert's rows)
+    * dh | du    = dA * u * silu'(h) | dA * silu(h)
+    * dW13[e]    = [dh | du]^T x                    (reduction over the expert's rows)
+
+    ``rows13`` / ``rows2`` (optional) select output rows of dW13[e] [2I][H] and dW2[e] [H][I];
+    a selected row is the same whether it is computed alone or with the rest (each output
+    row reduces over the expert's rows only, and ``quant`` along the rows treats every
+    column on its own).  ``quant`` as in ``backward`` (the weight-gradient operands in
+    32-row blocks from the expert's first row).
+    Returns a dict: dw13, dw2 (all rows or the selected ones), dg [n], dhu [n][2I].
+    """
+    q = quant if quant is not None else (lambda v, axis: v)
+    I = w13_e.shape[0] // 2
+    hu = q(x_rows, 1) @ q(w13_e, 1).T
+    h, u = hu[:, :I], hu[:, I:]
+    a = silu(h) * u
+    dA_prime = q(dy_rows, 1) @ q(w2_e, 0)
+    dg = np.einsum("ri,ri->r", dA_prime, a)
+    dA = g_rows[:, None] * dA_prime
+    dO = g_rows[:, None] * dy_rows
+    dhu = np.concatenate([dA * u * dsilu(h), dA * silu(h)], axis=1)
+    sel2 = slice(None) if rows2 is None else np.asarray(rows2, dtype=np.int64)
+    sel13 = slice(None) if rows13 is None else np.asarray(rows13, dtype=np.int64)
+    dw2 = q(dO[:, sel2], 0).T @ q(a, 0)
+    dw13 = q(dhu[:, sel13], 0).T @ q(x_rows, 0)
+    return {"dw13": dw13, "dw2": dw2, "dg": dg, "dhu": dhu}

@@ -96,3 +96,40 @@ def check_sampled_token_outputs(tokens, x_rows, w_router, router_bias, expert_we
         assert list(idx) == list(idx_rows[i]), f"{name}: token {t} experts {list(idx_rows[i])} vs {list(idx)}"
         want.append(y_t)
     assert_bf16_close(np.asarray(y_rows), np.array(want), name)
+
+
+def check_sampled_token_backward(tokens, x_rows, dy_rows, w_router, router_bias, expert_weights, shape, dx_rows,
+                                 dg_rows, idx_rows, name, quant=None, fro_tol=None):
+    """Input-gradient and gate-gradient rows of sampled tokens against the oracle's per-token
+    backward (oracle.token_backward, each token computed on its own): the GPU's experts for each
+    token must be the oracle's; dx and dgates must meet the bf16 bar (or, with `fro_tol`, the
+    relative Frobenius bar alone, as for MXFP8)."""
+    want_dx, want_dg = [], []
+    for i, t in enumerate(tokens):
+        r = O.token_backward(x_rows[i], dy_rows[i], w_router, router_bias, expert_weights, kind=shape.router,
+                             k=shape.k, renorm=shape.renorm, quant=quant)
+        assert list(r["topk_idx"]) == list(idx_rows[i]), f"{name}: token {t} experts {list(idx_rows[i])}"
+        want_dx.append(r["dx"])
+        want_dg.append(r["dgates"])
+    for what, got, want in (("dx", dx_rows, want_dx), ("dgates", dg_rows, want_dg)):
+        if fro_tol is None:
+            assert_bf16_close(np.asarray(got), np.array(want), f"{name} {what}")
+        else:
+            _, _, fro = err_stats(np.asarray(got), np.array(want))
+            assert fro <= fro_tol, f"{name} {what}: rel fro {fro:.3e}"
+
+
+def check_sampled_expert_wgrads(x_rows, dy_rows, g_rows, w13_e, w2_e, rows13, rows2, got13, got2, name,
+                                got_dg=None, quant=None, fro_tol=None):
+    """Sampled rows of one expert's weight gradients (and optionally the gate gradients of its
+    rows) against oracle.expert_weight_grads on that expert's rows in schedule order."""
+    r = O.expert_weight_grads(x_rows, dy_rows, g_rows, w13_e, w2_e, rows13=rows13, rows2=rows2, quant=quant)
+    pairs = [("dw13", got13, r["dw13"]), ("dw2", got2, r["dw2"])]
+    if got_dg is not None:
+        pairs.append(("dgates", got_dg, r["dg"]))
+    for what, got, want in pairs:
+        if fro_tol is None:
+            assert_bf16_close(np.asarray(got), want, f"{name} {what}")
+        else:
+            _, _, fro = err_stats(np.asarray(got), want)
+            assert fro <= fro_tol, f"{name} {what}: rel fro {fro:.3e}"

@@ -13,7 +13,8 @@ import torch
 import mixture_experts_layer_table_gb300 as mok
 from mixture_experts_layer_table_gb300 import workloads as W
 from oracle import moe_oracle as O
-from tests.parity import err_stats, inputs_f64, to_f64
+from tests.parity import (check_sampled_expert_wgrads, check_sampled_token_backward, clear_margin_tokens,
+                          err_stats, inputs_f64, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,6 +90,7 @@ def test_mx_forward_matches_mx_oracle(skew):
     print("MXFP8 vs unquantised: rel fro %.3e" % err_stats(to_f64(y), ref["y"])[2])
 
 
+@pytest.mark.slow
 def test_mx_forward_full_size_sampled_and_deterministic():
     shape = W.DSV3_MXFP8
     inp = W.make_inputs(shape, seed=0, device="cuda", with_dy=False)
@@ -181,11 +183,14 @@ def test_mx_backward_deterministic():
         assert torch.equal(runs[0][3][name], runs[1][3][name]), name
 
 
+@pytest.mark.slow
 def test_mx_backward_full_size_sampled_experts():
-    """DSV3 layer in MXFP8, forward + backward as the benchmark runs it; for the coldest and the
-    hottest expert the oracle recomputes that expert's rows on their own (rows in schedule order,
-    so that the 32-row quantisation blocks match): sampled rows of dW2 and dW13 and the gate
-    gradients of the expert's rows.  Plus bitwise determinism of every gradient."""
+    """DSV3 layer in MXFP8, forward + backward as the benchmark runs it.  For the coldest and the
+    hottest expert the oracle recomputes that expert's rows on their own (oracle.expert_weight_grads
+    on the rows in schedule order, so that the 32-row quantisation blocks match): sampled rows of
+    dW2 and dW13 and the gate gradients of the expert's rows.  For sampled tokens the oracle's
+    per-token backward (oracle.token_backward): dx and the gate gradients.  Plus bitwise
+    determinism of every gradient."""
     shape = W.DSV3_MXFP8
     inp = W.make_inputs(shape, seed=0, device="cuda")
     desc = mok.desc_from_shape(shape)
@@ -203,34 +208,37 @@ def test_mx_backward_full_size_sampled_experts():
     for name in ("dx", "dw_router", "dw13", "dw2", "dgates"):
         assert torch.equal(outs[0][name], outs[1][name]), name
     g = outs[0]
-    r = O.route(to_f64(inp["x"]), to_f64(inp["w_router"]), None, shape.router, shape.k, shape.renorm)
-    assert np.array_equal(layer.view("topk_idx").cpu().numpy(), r["topk_idx"])
-    counts = np.bincount(r["topk_idx"].reshape(-1), minlength=shape.E)
-    I = shape.I
+    w_r = to_f64(inp["w_router"])
+    r = O.route(to_f64(inp["x"]), w_r, None, shape.router, shape.k, shape.renorm)
+    gpu_idx = layer.view("topk_idx").cpu().numpy()
+    assert np.array_equal(gpu_idx, r["topk_idx"])
+    sched = O.schedule(gpu_idx, shape.E)
+    counts = sched["counts"]
+    dgates = g["dgates"].cpu().double().numpy().reshape(-1)
     for e in (int(np.argmin(counts)), int(np.argmax(counts))):
-        toks, js = np.nonzero(r["topk_idx"] == e)          # ascending tokens = the expert's row order
-        sel = torch.tensor(toks, device="cuda")
-        x = to_f64(inp["x"][sel])
-        dy = to_f64(inp["dy"][sel])
-        gs = r["gates"][toks, js]
-        w13 = to_f64(inp["w13"][e])
-        w2 = to_f64(inp["w2"][e])
-        hu = q(x, 1) @ q(w13, 1).T
-        h, u = hu[:, :I], hu[:, I:]
-        a = O.silu(h) * u
-        dA_p = q(dy, 1) @ q(w2, 0)
-        dg = np.einsum("ri,ri->r", dA_p, a)
-        dA = gs[:, None] * dA_p
-        dhu = np.concatenate([dA * u * O.dsilu(h), dA * O.silu(h)], axis=1)
+        lo, hi = int(sched["offsets"][e]), int(sched["offsets"][e + 1])
+        src = sched["src_of"][lo:hi].astype(np.int64)
+        sel = torch.as_tensor(src // shape.k, device="cuda")
         rng = np.random.default_rng(e)
         rows2 = rng.choice(shape.H, size=32, replace=False)
-        rows13 = rng.choice(2 * I, size=32, replace=False)
-        dw2 = q(gs[:, None] * dy, 0)[:, rows2].T @ q(a, 0)          # [rows][I]
-        dw13 = q(dhu, 0)[:, rows13].T @ q(x, 0)                     # [rows][H]
-        got2 = to_f64(g["dw2"][e][torch.tensor(rows2, device="cuda")])
-        got13 = to_f64(g["dw13"][e][torch.tensor(rows13, device="cuda")])
-        gotg = g["dgates"].cpu().numpy()[toks, js]
-        for name, got, want in (("dw2", got2, dw2), ("dw13", got13, dw13), ("dgates", gotg, dg)):
-            _, _, fro = err_stats(got, want)
-            print("expert %d %s: rel fro %.3e" % (e, name, fro))
-            assert fro <= MX_FRO, (e, name, fro)
+        rows13 = rng.choice(2 * shape.I, size=32, replace=False)
+        got2 = to_f64(g["dw2"][e][torch.as_tensor(rows2, device="cuda")])
+        got13 = to_f64(g["dw13"][e][torch.as_tensor(rows13, device="cuda")])
+        check_sampled_expert_wgrads(to_f64(inp["x"][sel]), to_f64(inp["dy"][sel]), r["gates"].reshape(-1)[src],
+                                    to_f64(inp["w13"][e]), to_f64(inp["w2"][e]), rows13, rows2, got13, got2,
+                                    f"MXFP8 expert {e} ({hi - lo} rows)", got_dg=dgates[src], quant=q,
+                                    fro_tol=MX_FRO)
+    toks = clear_margin_tokens(r["scores"], shape.k, 4, seed=3)
+    sel = torch.as_tensor(toks, device="cuda")
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            if len(cache) > 8:
+                cache.pop(next(iter(cache)))
+            cache[e] = (to_f64(inp["w13"][e]), to_f64(inp["w2"][e]))
+        return cache[e]
+
+    check_sampled_token_backward(toks, to_f64(inp["x"][sel]), to_f64(inp["dy"][sel]), w_r, None, experts, shape,
+                                 to_f64(g["dx"][sel]), to_f64(g["dgates"][sel]), gpu_idx[toks],
+                                 "MXFP8 (sampled tokens)", quant=q, fro_tol=MX_FRO)

@@ -18,7 +18,7 @@ from mixture_experts_layer_table_gb300 import workloads as W
 from oracle import moe_oracle as O
 from tests.parity import check_sampled_token_outputs, clear_margin_tokens, to_f64
 
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 SHAPE = W.RING
 MINIBATCH = 2368
@@ -37,6 +37,7 @@ def run(cuda_ok):
     torch.cuda.synchronize()
     assert plain.status() == (0, 0)
     idx = plain.view("topk_idx").cpu().numpy()
+    table = {name: plain.view(name).cpu().numpy() for name in ("counts", "offsets", "row_of", "src_of")}
     del plain
     torch.cuda.empty_cache()
     ring = mok.MoELayer(mok.desc_from_shape(SHAPE, minibatch=MINIBATCH, ring_bytes=W.RING_BYTES))
@@ -47,17 +48,17 @@ def run(cuda_ok):
     idx_ring = ring.view("topk_idx").cpu().numpy()
     del ring
     torch.cuda.empty_cache()
-    return inp, idx, y_plain, idx_ring, y_ring
+    return inp, idx, y_plain, idx_ring, y_ring, table
 
 
 def test_ring_forward_is_bitwise_the_plain_forward(run):
-    _, idx, y_plain, idx_ring, y_ring = run
+    _, idx, y_plain, idx_ring, y_ring, _ = run
     assert np.array_equal(idx, idx_ring)
     assert torch.equal(y_plain, y_ring)
 
 
 def test_sampled_tokens_against_the_oracle(run):
-    inp, idx, y_plain, _, _ = run
+    inp, idx, y_plain, _, _, _ = run
     rng = np.random.default_rng(1)
     cand = np.sort(rng.choice(SHAPE.T, size=N_CANDIDATES, replace=False))
     w_r = to_f64(inp["w_router"])
@@ -78,3 +79,12 @@ def test_sampled_tokens_against_the_oracle(run):
     y_rows = to_f64(y_plain[torch.as_tensor(toks, device=y_plain.device)])
     check_sampled_token_outputs(toks, x_c[pick], w_r, None, experts, SHAPE, y_rows, idx[toks],
                                 "y (T=16384, sampled tokens)")
+
+
+def test_schedule_table_bit_exact(run):
+    """The whole schedule table at T=16384 (131,072 assignments), bit-exact against the oracle's
+    stable counting sort of the same selection."""
+    _, idx, _, _, _, table = run
+    ref = O.schedule(idx, SHAPE.E)
+    for name in ("counts", "offsets", "row_of", "src_of"):
+        assert np.array_equal(table[name], ref[name]), name

@@ -504,3 +504,125 @@ def test_quantized_backward_close_to_exact():
     for name in ("dx", "dw13", "dw2", "dgates"):
         rel = np.linalg.norm(got[name] - ref[name]) / np.linalg.norm(ref[name])
         assert 1e-3 < rel < 0.2, (name, rel)
+
+
+# ---------------------------------------------------------------------------
+# Sampled evaluators (the full-size GPU checks use them one token / one expert at a time)
+# ---------------------------------------------------------------------------
+
+def test_quantized_forward_quantises_each_operand_along_its_reduction():
+    """MX emulation of the forward: x_g and W13[e] along H for h | u = x_g W13[e]^T, a and W2[e]
+    along I for o = a W2[e]^T; each operand exactly once per expert.  token_forward quantises
+    the same operands along the same axes.  With q the identity nothing changes."""
+    rng = np.random.default_rng(21)
+    T, H, E, I, k = 14, 96, 3, 40, 2      # H, I, 2I and the experts' row counts all differ
+    x, w_r, w13, w2 = _rand_layer(rng, T, H, E, I, scale=0.2)
+    calls = []
+
+    def rec(v, axis):
+        calls.append((tuple(np.asarray(v).shape), axis))
+        return v
+
+    ref = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True)
+    got = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True, quant=rec)
+    assert np.allclose(got["y"], ref["y"], rtol=1e-13, atol=1e-13)
+    expected = []
+    for e in range(E):
+        n = int(ref["offsets"][e + 1] - ref["offsets"][e])
+        if n == 0:
+            continue
+        assert n not in (H, I, 2 * I)
+        expected += [((n, H), 1), ((2 * I, H), 1),     # h | u = x_g W13[e]^T, reduction over H
+                     ((n, I), 1), ((H, I), 1)]         # o = a W2[e]^T, reduction over I
+    assert sorted(calls) == sorted(expected)
+    calls.clear()
+    O.token_forward(x[3], w_r, None, lambda e: (w13[e], w2[e]), kind=O.SIGMOID, k=k, renorm=True, quant=rec)
+    assert sorted(calls) == sorted([((1, H), 1)] + [((2 * I, H), 1), ((1, I), 1), ((H, I), 1)] * k)
+
+
+def _layer_case(kind, renorm, use_bias, scale, seed):
+    rng = np.random.default_rng(seed)
+    T, H, E, I, k = 20, 64, 6, 32, 3
+    x, w_r, w13, w2 = _rand_layer(rng, T, H, E, I, scale=0.3)
+    dy = rng.normal(0, 1, (T, H))
+    bias = rng.normal(0, 0.1, E) if use_bias else None
+    return x, w_r, w13, w2, dy, bias, k
+
+
+@pytest.mark.parametrize("kind,renorm,use_bias,scale,quant", [
+    (O.SIGMOID, True, False, 1.0, False), (O.SIGMOID, True, True, 2.5, False),
+    (O.SOFTMAX, False, False, 1.0, False), (O.SOFTMAX, True, True, 0.7, False),
+    (O.SIGMOID, True, True, 1.0, True)])
+def test_token_backward_matches_layer(kind, renorm, use_bias, scale, quant):
+    """token_backward equals the whole-layer backward on every token, element by element: dx,
+    the gate gradients, dl, and the token's k rows of dh | du and of the dX_g rows."""
+    x, w_r, w13, w2, dy, bias, k = _layer_case(kind, renorm, use_bias, scale, seed=22)
+    qf = O.mx_quantize_dequantize if quant else None
+    if quant:   # H and I multiples of 32 so that the row blocks are whole
+        assert x.shape[1] % 32 == 0 and w13.shape[1] % 64 == 0
+    fwd = O.forward(x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, router_bias=bias, route_scale=scale, quant=qf)
+    bwd = O.backward(fwd, dy, x, w_r, w13, w2, kind=kind, k=k, renorm=renorm, route_scale=scale, quant=qf)
+    rows = fwd["row_of"].reshape(-1, k)
+    for t in range(x.shape[0]):
+        got = O.token_backward(x[t], dy[t], w_r, bias, lambda e: (w13[e], w2[e]), kind=kind, k=k, renorm=renorm,
+                               route_scale=scale, quant=qf)
+        assert np.array_equal(got["topk_idx"], fwd["topk_idx"][t])
+        close = dict(rtol=1e-12, atol=1e-12)
+        assert np.allclose(got["y"], fwd["y"][t], **close)
+        assert np.allclose(got["dx"], bwd["dx"][t], **close)
+        assert np.allclose(got["dgates"], bwd["dgates"][t], **close)
+        assert np.allclose(got["dl"], bwd["dl"][t], **close)
+        assert np.allclose(got["dhu"], bwd["dhu"][rows[t]], **close)
+        assert np.allclose(got["dx_g"], bwd["dx_g"][rows[t]], **close)
+
+
+@pytest.mark.parametrize("quant", [False, True])
+def test_expert_weight_grads_match_layer(quant):
+    """expert_weight_grads on one expert's rows (schedule order) equals the whole-layer
+    backward's dW13[e], dW2[e], the rows' gate gradients and dh | du; selected output rows equal
+    the same rows of the full result."""
+    x, w_r, w13, w2, dy, bias, k = _layer_case(O.SIGMOID, True, True, 1.0, seed=23)
+    qf = O.mx_quantize_dequantize if quant else None
+    fwd = O.forward(x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True, router_bias=bias, quant=qf)
+    bwd = O.backward(fwd, dy, x, w_r, w13, w2, kind=O.SIGMOID, k=k, renorm=True, quant=qf)
+    E = w13.shape[0]
+    src = fwd["src_of"].astype(np.int64)
+    seen = 0
+    for e in range(E):
+        lo, hi = int(fwd["offsets"][e]), int(fwd["offsets"][e + 1])
+        if hi == lo:
+            continue
+        seen += 1
+        toks = src[lo:hi] // k
+        g_rows = fwd["gates"].reshape(-1)[src[lo:hi]]
+        got = O.expert_weight_grads(x[toks], dy[toks], g_rows, w13[e], w2[e], quant=qf)
+        close = dict(rtol=1e-12, atol=1e-12)
+        assert np.allclose(got["dw13"], bwd["dw13"][e], **close)
+        assert np.allclose(got["dw2"], bwd["dw2"][e], **close)
+        assert np.allclose(got["dg"], bwd["dgates"].reshape(-1)[src[lo:hi]], **close)
+        assert np.allclose(got["dhu"], bwd["dhu"][lo:hi], **close)
+        r13 = np.array([5, 0, 63, 17])
+        r2 = np.array([1, 40, 7])
+        sel = O.expert_weight_grads(x[toks], dy[toks], g_rows, w13[e], w2[e], rows13=r13, rows2=r2, quant=qf)
+        assert np.allclose(sel["dw13"], got["dw13"][r13], rtol=1e-13, atol=1e-13)
+        assert np.allclose(sel["dw2"], got["dw2"][r2], rtol=1e-13, atol=1e-13)
+    assert seen >= 3
+
+
+def test_expert_weight_grads_quantises_each_operand_along_its_reduction():
+    """The weight-gradient operands along the expert's rows (axis 0), the forward and dA'
+    operands along their own reductions, each once."""
+    x, w_r, w13, w2, dy, bias, k = _layer_case(O.SIGMOID, True, False, 1.0, seed=24)
+    n, H = 7, x.shape[1]
+    I = w13.shape[1] // 2
+    calls = []
+
+    def rec(v, axis):
+        calls.append((tuple(np.asarray(v).shape), axis))
+        return v
+
+    O.expert_weight_grads(x[:n], dy[:n], np.full(n, 0.3), w13[0], w2[0], quant=rec)
+    assert sorted(calls) == sorted([((n, H), 1), ((2 * I, H), 1),     # h | u
+                                    ((n, H), 1), ((H, I), 0),         # dA' = dY W2[e]
+                                    ((n, H), 0), ((n, I), 0),         # dW2 = dO^T a
+                                    ((n, 2 * I), 0), ((n, H), 0)])    # dW13 = dHU^T x
