@@ -11,6 +11,7 @@
 // The array lives in every GPU's memory that loads the library, until the process exits,
 // and every call on a device shares it.  Calls whose kernels overlap on the GPU (two
 // streams, or two host threads) race on it; callers must order them.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,20 +32,44 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
+CUcontext g_scratch_ctx[kMaxDevices] = {nullptr};
 int g_sm_count[kMaxDevices] = {0};
 
-// Looks up (once per device, with that device current) the device address of the scratch
-// array and the SM count.  Returns false when the lookup fails.
+// The driver's cuCtxGetCurrent, found through the runtime (the library does not link libcuda).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Looks up (once per device and context, with that device current) the device address of the
+// scratch array and the SM count.  The address is kept together with the context it was looked
+// up in: after a context is destroyed and created again (cudaDeviceReset) the module may load at
+// another address, so a new context means a new lookup.  Returns false when the lookup fails.
 bool setup_current_device(void** scratch, int* n_sm) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  // make the device's primary context current (cudaSetDevice initialises it) before asking which it is
+  if (cudaSetDevice(dev) != cudaSuccess) return false;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return false;
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return false;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
     g_sm_count[dev] = n;
   }
   *scratch = g_scratch_ptr[dev];
