@@ -148,7 +148,16 @@ typedef struct {
   int64_t mx_xg_r;    /* bf16 [T*k][H]  dispatched x in 32-row blocks (dW13) */
   int64_t mx_do_r;    /* bf16 [T*k][H]  gate * dY rows in 32-row blocks (dW2) */
   int64_t mx_a_r;     /* bf16 [T*k][I]  a = silu(h) * u in 32-row blocks (dW2) */
-  int64_t mx_blk_off; /* i32 [E+1]      32-row blocks before each expert */
+  int64_t mx_blk_off; /* i32 [E+1]      32-row blocks before each expert (forward and backward) */
+  /* MXFP8 forward only (-1 otherwise): E4M3 row operands of the FP8 GEMMs in a padded row space,
+   * expert e owning rows [32 mx_blk_off[e], 32 mx_blk_off[e+1]) (its rows in schedule order, then
+   * zero rows); RP = 32 (ceil(T*k / 32) + E) rows, G = RP / 32 + 4 row groups.  Scales: 512-byte
+   * blocks of 128 rows x 4 blocks of 32 along the row, row 32 j + l and block b at byte
+   * 16 l + 4 j + b; block (g, s) holds rows 32 g .. 32 g + 127 of 128-element stage s. */
+  int64_t mx_xq;      /* E4M3 [RP][H]            dispatched rows quantised along H */
+  int64_t mx_xsf;     /* E8M0 [G][H/128][512]    their scale blocks */
+  int64_t mx_aq;      /* E4M3 [RP][I]            a = silu(h) * u quantised along I */
+  int64_t mx_asf;     /* E8M0 [G][I/128][512]    its scale blocks */
   int64_t ws_bytes;
 } mok_layout;
 
@@ -220,10 +229,12 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
  * Microscaling v1.0: E4M3 elements, one E8M0 scale per 32 consecutive elements along the GEMM's
  * reduction dimension, X = clamp(floor(log2 amax) - 8, -127, 127), elements RNE(v / 2^X)
  * saturated at +-448, scale byte X + 127.
- *   w13 [E][2I][H] bf16 -> w13_q [E][2I][H] E4M3 bytes, w13_scale [E][H/32][2I] bytes
- *   w2  [E][H][I]  bf16 -> w2_q  [E][H][I]  E4M3 bytes, w2_scale  [E][I/32][H]  bytes
- * (scales are stored k-block-major so that one load brings a tile's scales).  All device
- * pointers, 16-byte aligned. */
+ *   w13 [E][2I][H] bf16 -> w13_q [E][2I][H] E4M3 bytes, w13_scale [E][2I/128][H/128][512] bytes
+ *   w2  [E][H][I]  bf16 -> w2_q  [E][H][I]  E4M3 bytes, w2_scale  [E][H/128][I/128][512]  bytes
+ * Scales come in 512-byte blocks, one per 128-row tile and 128-element stage of the reduction
+ * dimension, in the order the tensor cores read them from tensor memory: row 32 j + l (of the
+ * tile) and 32-element block b (of the stage) at byte 16 l + 4 j + b.  All device pointers,
+ * 16-byte aligned. */
 mok_status mok_quantize_weights(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_q,
                                 void* w13_scale, void* w2_q, void* w2_scale, void* stream);
 
@@ -254,12 +265,12 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* desc, const void* dy, co
  * mok_moe_forward, with the expert weights given as mok_quantize_weights output.  The MXFP8
  * activation quantisation sits on the data path ("把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源
  * GPU 内核 MoK", aientropygate.com, §03 ③): the gather quantises each dispatched row in
- * 32-element blocks along H and the GEMM1 epilogue quantises a = silu(h) * u along I; both keep
- * the quantised values as bf16 (E4M3 * 2^X is exact in bf16).  The GEMMs stream E4M3 weights,
- * expand them exactly to bf16 in shared memory and accumulate in fp32, so each product equals
- * the MXFP8 product.  The router stays in bf16.  ctx / ws as for mok_moe_forward (ctx x_g holds
- * the quantised rows).  The MXFP8 backward is mok_moe_backward_mxfp8; mok_moe_backward returns
- * MOK_ERR_UNSUPPORTED for an MXFP8 descriptor. */
+ * 32-element blocks along H and the GEMM1 epilogue quantises a = silu(h) * u along I, both into
+ * E4M3 bytes and scale blocks (layout.mx_xq / mx_xsf, mx_aq / mx_asf in ws).  The expert GEMMs
+ * run on the FP8 tensor path (block-scaled MMAs that apply the E8M0 scales themselves) and
+ * accumulate in fp32.  The router stays in bf16.  ctx as for mok_moe_forward except that ctx x_g
+ * is not written (the MXFP8 backward takes the dispatched rows from x).  The MXFP8 backward is
+ * mok_moe_backward_mxfp8; mok_moe_backward returns MOK_ERR_UNSUPPORTED for an MXFP8 descriptor. */
 mok_status mok_moe_forward_mxfp8(const mok_layer_desc* desc, const void* x, const void* w_router,
                                  const float* router_bias, const int32_t* given_topk, const void* w13_q,
                                  const void* w13_scale, const void* w2_q, const void* w2_scale, void* y,

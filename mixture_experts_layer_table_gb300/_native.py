@@ -38,7 +38,8 @@ class LayerDesc(ctypes.Structure):
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
                  "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
-                 "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "ws_bytes"]
+                 "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "mx_xq", "mx_xsf", "mx_aq",
+                 "mx_asf", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
 FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
@@ -249,7 +250,18 @@ _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.
                "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
                "dg_part": torch.float32, "dlogits": torch.float32, "mx_dhu_c": torch.bfloat16,
                "mx_dhu_r": torch.bfloat16, "mx_xg_r": torch.bfloat16, "mx_do_r": torch.bfloat16,
-               "mx_a_r": torch.bfloat16, "mx_blk_off": torch.int32}
+               "mx_a_r": torch.bfloat16, "mx_blk_off": torch.int32, "mx_xq": torch.uint8, "mx_xsf": torch.uint8,
+               "mx_aq": torch.uint8, "mx_asf": torch.uint8}
+
+
+def mx_rows_padded_bound(R: int, E: int) -> int:
+    """Rows of the MXFP8 padded row space (include/mok.h, mok_layout.mx_xq): 32 (ceil(R / 32) + E)."""
+    return 32 * ((R + 31) // 32 + E)
+
+
+def mx_row_groups(R: int, E: int) -> int:
+    """Row groups of the MXFP8 scale blocks: padded rows / 32 + 4."""
+    return mx_rows_padded_bound(R, E) // 32 + 4
 
 
 class MoELayer:
@@ -271,7 +283,9 @@ class MoELayer:
                 "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
                 "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E), "mx_dhu_c": (R, 2 * d.I),
                 "mx_dhu_r": (R, 2 * d.I), "mx_xg_r": (R, d.H), "mx_do_r": (R, d.H), "mx_a_r": (R, d.I),
-                "mx_blk_off": (d.E + 1,)}[name]
+                "mx_blk_off": (d.E + 1,), "mx_xq": (mx_rows_padded_bound(R, d.E), d.H),
+                "mx_xsf": (mx_row_groups(R, d.E), d.H // 128, 512), "mx_aq": (mx_rows_padded_bound(R, d.E), d.I),
+                "mx_asf": (mx_row_groups(R, d.E), d.I // 128, 512)}[name]
 
     def view_split(self, name: str) -> torch.Tensor:
         """hi + lo of a split operand ("act", "dhu", "gact") as one float32 tensor."""
@@ -374,9 +388,9 @@ def quantize_weights(desc, w13, w2, stream=None):
     dev = w13.device
     E, H, I = desc.E, desc.H, desc.I
     out = {"w13_q": torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev),
-           "w13_scale": torch.empty((E, H // 32, 2 * I), dtype=torch.uint8, device=dev),
+           "w13_scale": torch.empty((E, 2 * I // 128, H // 128, 512), dtype=torch.uint8, device=dev),
            "w2_q": torch.empty((E, H, I), dtype=torch.uint8, device=dev),
-           "w2_scale": torch.empty((E, I // 32, H), dtype=torch.uint8, device=dev)}
+           "w2_scale": torch.empty((E, H // 128, I // 128, 512), dtype=torch.uint8, device=dev)}
     fn = load().mok_quantize_weights
     fn.argtypes = [ctypes.POINTER(LayerDesc)] + [ctypes.c_void_p] * 7
     fn.restype = ctypes.c_int32
@@ -394,9 +408,9 @@ def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws
     _expect(router_bias, (E,), torch.float32, "router_bias", nullable=True)
     _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
     _expect(wq["w13_q"], (E, 2 * I, H), torch.uint8, "w13_q")
-    _expect(wq["w13_scale"], (E, H // 32, 2 * I), torch.uint8, "w13_scale")
+    _expect(wq["w13_scale"], (E, 2 * I // 128, H // 128, 512), torch.uint8, "w13_scale")
     _expect(wq["w2_q"], (E, H, I), torch.uint8, "w2_q")
-    _expect(wq["w2_scale"], (E, I // 32, H), torch.uint8, "w2_scale")
+    _expect(wq["w2_scale"], (E, H // 128, I // 128, 512), torch.uint8, "w2_scale")
     _expect(y, (desc.T, H), torch.bfloat16, "y")
     fn = load().mok_moe_forward_mxfp8
     P, SZ = ctypes.c_void_p, ctypes.c_size_t

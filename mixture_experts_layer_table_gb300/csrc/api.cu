@@ -11,6 +11,7 @@
 
 #include "kernels.cuh"
 #include "mok.h"
+#include "mx_tiles.h"
 
 namespace {
 
@@ -136,6 +137,7 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
     L->mb_counters = take(int64_t(2) * g.n_mb * 4);
   }
   L->mx_dhu_c = L->mx_dhu_r = L->mx_xg_r = L->mx_do_r = L->mx_a_r = L->mx_blk_off = -1;
+  L->mx_xq = L->mx_xsf = L->mx_aq = L->mx_asf = -1;
   if (d->precision == MOK_MXFP8) {
     L->mx_dhu_c = take(R * 2 * I * 2);
     L->mx_dhu_r = take(R * 2 * I * 2);
@@ -143,6 +145,11 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
     L->mx_do_r = take(R * H * 2);
     L->mx_a_r = take(R * I * 2);
     L->mx_blk_off = take((E + 1) * 4);
+    const int64_t RP = mok::mx_rows_padded_bound(R, (int)E), G = mok::mx_row_groups(R, (int)E);
+    L->mx_xq = take(RP * H);
+    L->mx_xsf = take(G * (H / mok::MX_BK) * mok::MX_SF_BLOCK);
+    L->mx_aq = take(RP * I);
+    L->mx_asf = take(G * (I / mok::MX_BK) * mok::MX_SF_BLOCK);
   }
   L->ws_bytes = off;
   return MOK_OK;
@@ -500,11 +507,15 @@ mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const v
   int32_t* tile_off = at<int32_t>(ctx, L.tile_off);
   int32_t* row_of = at<int32_t>(ctx, L.row_of);
   int32_t* src_of = at<int32_t>(ctx, L.src_of);
-  void* x_g = at<char>(ctx, L.x_g);
   float* hu = at<float>(ctx, L.hu);
-  void* act = at<char>(ws, L.act);
   float* o = at<float>(ws, L.expert_out);
   float* logits = at<float>(ws, L.logits);
+  int32_t* blk_off = at<int32_t>(ws, L.mx_blk_off);
+  void* xq = at<char>(ws, L.mx_xq);
+  void* xsf = at<char>(ws, L.mx_xsf);
+  void* aq = at<char>(ws, L.mx_aq);
+  void* asf = at<char>(ws, L.mx_asf);
+  const int RP = (int)mok::mx_rows_padded_bound(R, E), G = (int)mok::mx_row_groups(R, E);
 
   MOK_CUDA(cudaMemsetAsync(status, 0, mok::STATUS_BYTES, st));
   MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
@@ -512,13 +523,16 @@ mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const v
                                           d->route_scale, topk_idx, gates, at<float>(ctx, L.scores), status, st));
   MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of,
                                                   src_of, tile_off, at<float>(ctx, L.gate_row), status, st));
-  // pull dispatch with the MXFP8 quantisation of each row along H
-  MOK_LAUNCH("gather_x_mx", st, mok::launch_gather_rows_mx(x, src_of, k, R, H, x_g, n_sm, st));
-  // GEMM1 on E4M3 weights, SwiGLU, a quantised along I
-  MOK_LAUNCH("gemm1_swiglu_mx", st, mok::launch_gemm1_swiglu_mx(x_g, w13_q, w13_scale, R, H, I, E, offsets, tile_off,
-                                                                hu, act, status, n_sm, st));
-  MOK_LAUNCH("gemm2_mx", st, mok::launch_gemm2_mx(act, w2_q, w2_scale, R, H, I, E, offsets, tile_off, o, status, n_sm,
-                                                  st));
+  // each expert's rows padded to 32 in the E4M3 row space of the FP8 GEMMs
+  MOK_LAUNCH("mx_block_offsets", st, mok::launch_mx_block_offsets(offsets, E, blk_off, st));
+  // pull dispatch with the MXFP8 quantisation of each row along H (E4M3 bytes + scale blocks)
+  MOK_LAUNCH("gather_x_mx", st, mok::launch_gather_rows_mxf8(x, src_of, topk_idx, offsets, blk_off, k, R, H, E, xq,
+                                                             xsf, st));
+  // GEMM1 on the FP8 tensor path, SwiGLU, a quantised along I (E4M3 bytes + scale blocks)
+  MOK_LAUNCH("gemm1_swiglu_mx", st, mok::launch_gemm1_swiglu_mxf8(xq, xsf, w13_q, w13_scale, RP, G, H, I, E, offsets,
+                                                                  blk_off, hu, aq, asf, status, n_sm, st));
+  MOK_LAUNCH("gemm2_mx", st, mok::launch_gemm2_mxf8(aq, asf, w2_q, w2_scale, RP, G, H, I, E, offsets, blk_off, o,
+                                                    status, n_sm, st));
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
 }

@@ -100,6 +100,17 @@ cudaError_t launch_gemm1_swiglu_mx(const void* x_g, const void* w13_q, const voi
 cudaError_t launch_gemm2_mx(const void* act, const void* w2_q, const void* w2_s, int R, int H, int I, int E,
                             const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
                             cudaStream_t st);
+// MXFP8 forward on the FP8 tensor path (mx.cu, gemm_mx.cu): E4M3 row operands in the padded row
+// space of mx_tiles.h (blk_off from launch_mx_block_offsets), scale blocks of RP / 32 + 4 row groups.
+cudaError_t launch_gather_rows_mxf8(const void* x, const int32_t* src_of, const int32_t* topk_idx,
+                                    const int32_t* offsets, const int32_t* blk_off, int k, int R, int H, int E,
+                                    void* xq, void* xsf, cudaStream_t st);
+cudaError_t launch_gemm1_swiglu_mxf8(const void* xq, const void* xsf, const void* w13_q, const void* w13_sf, int RP,
+                                     int G, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off,
+                                     float* hu, void* aq, void* asf, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_gemm2_mxf8(const void* aq, const void* asf, const void* w2_q, const void* w2_sf, int RP, int G,
+                              int H, int I, int E, const int32_t* offsets, const int32_t* blk_off, float* o,
+                              int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

@@ -8,12 +8,14 @@
 
 #include "kernels.cuh"
 #include "mx.cuh"
+#include "mx_tiles.h"
 #include "ptx.cuh"
 
 namespace mok {
 
-// w [E][N][K] bf16 -> q [E][N][K] E4M3 bytes, s [E][K/32][N] E8M0 bytes.  One thread per
-// (e, k-block, n), n fastest so the scale stores are coalesced.
+// w [E][N][K] bf16 -> q [E][N][K] E4M3 bytes, s [E][N/128][K/128][512] E8M0 bytes: one 512-byte
+// block per 128-row tile and 128-element K stage, in the order tcgen05.cp puts it into TMEM
+// (mx_tiles.h).  One thread per (e, k-block, n), n fastest.
 __global__ void __launch_bounds__(256)
     quantize_weights_kernel(const __nv_bfloat16* __restrict__ w, uint8_t* __restrict__ q, uint8_t* __restrict__ s,
                             int E, int N, int K) {
@@ -44,7 +46,8 @@ __global__ void __launch_bounds__(256)
     uint4* dst = reinterpret_cast<uint4*>(q + base);
     dst[0] = *reinterpret_cast<uint4*>(bytes);
     dst[1] = *reinterpret_cast<uint4*>(bytes + 16);
-    s[((size_t)e * KB + kb) * N + n] = (uint8_t)(X + 127);
+    s[(((size_t)e * (N / 128) + n / 128) * (K / 128) + kb / 4) * MX_SF_BLOCK + mx_sf_byte(n & 127, kb & 3)] =
+        (uint8_t)(X + 127);
   }
 }
 
@@ -96,6 +99,85 @@ __global__ void __launch_bounds__(GATHER_MX_THREADS)
         asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(d + i), "r"(o.x), "r"(o.y), "r"(o.z),
                      "r"(o.w)
                      : "memory");
+      }
+    }
+  }
+}
+
+// The dispatch of the MXFP8 forward on the FP8 tensor path: x_q[p] = E4M3 bytes of
+// x[src_of[r] / k] along H, at padded row p = 32 blk_off[e] + (r - offsets[e]) of the row's expert
+// e, and the row's scales into the four row-group blocks that hold them (mx_tiles.h).  Blocks
+// [0, R) are rows, as gather_rows_mx_kernel: 128 threads, 16-byte loads, 4 adjacent lanes per
+// 32-element block (mx_quantize8_x4_e4m3), one 8-byte store per lane.  Block R + e zero-fills the
+// padding rows of expert e (their bytes and scales), so that the GEMM reads zeros there.
+__global__ void __launch_bounds__(GATHER_MX_THREADS)
+    gather_rows_mxf8_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ src_of,
+                            const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ offsets,
+                            const int32_t* __restrict__ blk_off, int k, int R, int H, uint8_t* __restrict__ xq,
+                            uint8_t* __restrict__ xsf) {
+  constexpr int V = 8;
+  const int vec_per_row = H / 8;
+  const int S = H / MX_BK;
+  if ((int)blockIdx.x < R) {
+    const int r = blockIdx.x;
+    const int a = src_of[r];
+    const int tok = a / k;
+    const int e = topk_idx[a];
+    const int p = MX_ROW_ALIGN * blk_off[e] + (r - offsets[e]);
+    const uint64_t keep = l2_policy_evict_last();
+    const uint4* s = reinterpret_cast<const uint4*>(src) + (size_t)tok * vec_per_row;
+    uint2* d = reinterpret_cast<uint2*>(xq + (size_t)p * H);
+    for (int base = threadIdx.x; base < vec_per_row; base += GATHER_MX_THREADS * V) {
+      uint4 u[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int i = base + j * GATHER_MX_THREADS;  // a warp's 32 lanes are all in range or none
+        if (i < vec_per_row)
+          asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                       : "=r"(u[j].x), "=r"(u[j].y), "=r"(u[j].z), "=r"(u[j].w)
+                       : "l"(s + i), "l"(keep));
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int i = base + j * GATHER_MX_THREADS;
+        if (i < vec_per_row) {
+          float v[8];
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[j]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(h[q]);
+            v[2 * q] = f.x;
+            v[2 * q + 1] = f.y;
+          }
+          uint2 bytes;
+          const int X = mx_quantize8_x4_e4m3(v, bytes);
+          d[i] = bytes;
+          if ((i & 3) == 0) {  // the first lane of the block stores its scale
+            const int kb = i >> 2;
+            const int g_top = p >> 5;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int g = g_top - jj;
+              if (g >= 0)
+                xsf[((size_t)g * S + (kb >> 2)) * MX_SF_BLOCK + (p & 31) * 16 + jj * 4 + (kb & 3)] = (uint8_t)(X + 127);
+            }
+          }
+        }
+      }
+    }
+  } else {
+    const int e = (int)blockIdx.x - R;
+    const int p_end = MX_ROW_ALIGN * blk_off[e + 1];
+    for (int p = MX_ROW_ALIGN * blk_off[e] + (offsets[e + 1] - offsets[e]); p < p_end; ++p) {
+      uint2* d = reinterpret_cast<uint2*>(xq + (size_t)p * H);
+      for (int i = threadIdx.x; i < vec_per_row; i += GATHER_MX_THREADS) d[i] = make_uint2(0u, 0u);
+      const int g_top = p >> 5;
+      for (int kb = threadIdx.x; kb < H / 32; kb += GATHER_MX_THREADS) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int g = g_top - jj;
+          if (g >= 0) xsf[((size_t)g * S + (kb >> 2)) * MX_SF_BLOCK + (p & 31) * 16 + jj * 4 + (kb & 3)] = 0;
+        }
       }
     }
   }
@@ -370,6 +452,16 @@ cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k,
   (void)n_sm;
   gather_rows_mx_kernel<<<R, GATHER_MX_THREADS, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), src_of, k, H / 8,
                                                          reinterpret_cast<__nv_bfloat16*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_mxf8(const void* x, const int32_t* src_of, const int32_t* topk_idx,
+                                    const int32_t* offsets, const int32_t* blk_off, int k, int R, int H, int E,
+                                    void* xq, void* xsf, cudaStream_t st) {
+  if (R + E == 0) return cudaSuccess;
+  gather_rows_mxf8_kernel<<<R + E, GATHER_MX_THREADS, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), src_of, topk_idx, offsets, blk_off, k, R, H,
+      reinterpret_cast<uint8_t*>(xq), reinterpret_cast<uint8_t*>(xsf));
   return cudaGetLastError();
 }
 

@@ -127,4 +127,26 @@ __device__ __forceinline__ void mx_quantize8_x4(float (&v)[8]) {
   }
 }
 
+// mx_quantize8_x4 returning the E4M3 bytes (byte j = element j of this lane's 8, little-endian
+// in `bytes`) and the block's exponent X instead of the dequantised values.  All 32 lanes of the
+// warp must call it.
+__device__ __forceinline__ int mx_quantize8_x4_e4m3(const float (&v)[8], uint2& bytes) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int X = mx_exponent(amax);
+  const float inv = exp2_int(-X);
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t lo = e4m3x2_from_f32(v[4 * h] * inv, v[4 * h + 1] * inv);
+    const uint32_t hi = e4m3x2_from_f32(v[4 * h + 2] * inv, v[4 * h + 3] * inv);
+    w[h] = lo | (hi << 16);
+  }
+  bytes = make_uint2(w[0], w[1]);
+  return X;
+}
+
 }  // namespace mok

@@ -373,4 +373,50 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+
+// ---------------------------------------------------------------- tcgen05 block-scaled MXFP8
+// Shared-memory matrix descriptor without swizzle (tcgen05 format, version 1): the source of a
+// tcgen05.cp of scale factors, 8-row core matrices of 16-byte rows `sbo_bytes` apart.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;  // version
+  return d;
+}
+
+// Copies a 32-row x 16-byte block of scale factors from shared memory into 4 TMEM columns at
+// `taddr`, the same 32 rows into each of the four 32-lane quarters (warpx4): lane l of every
+// quarter, column j receives bytes 16 l + 4 j .. +3 of the block.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * 2^SFA) (B * 2^SFB), kind::mxf8f6f4 with one E8M0 scale per 32 K-elements
+// (scale_vec::1X): A row m takes its scale from TMEM column sfa + m / 32, lane m % 32 (of any
+// quarter), byte `a_sf_id` of the instruction descriptor; B column n likewise from sfb.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (both K-major), E8M0 scales, f32
+// accumulate, M x N tile; the scale byte of each operand's TMEM word is sf_id (0..3): the K-block
+// of 32 inside a 128-byte K stage.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int a_sf_id, int b_sf_id) {
+  return (static_cast<uint32_t>(b_sf_id) << 4)      // B scale byte
+         | (0u << 7) | (0u << 10)                   // A, B format E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N
+         | (1u << 23)                               // scale format E8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)    // M
+         | (static_cast<uint32_t>(a_sf_id) << 29);  // A scale byte
+}
+
 }  // namespace mok

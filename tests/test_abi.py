@@ -123,6 +123,10 @@ def _region_sizes(shp, ring_slots=0, minibatch=0):
     if shp.mxfp8:
         ws.update({"mx_dhu_c": R * 2 * I * 2, "mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
                    "mx_do_r": R * H * 2, "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4})
+        RP = 32 * (-(-R // 32) + E)       # padded rows: every expert's rows rounded up to 32
+        G = RP // 32 + 4                  # row groups of the scale blocks
+        ws.update({"mx_xq": RP * H, "mx_xsf": G * (H // 128) * 512, "mx_aq": RP * I,
+                   "mx_asf": G * (I // 128) * 512})
     return ctx, ws
 
 

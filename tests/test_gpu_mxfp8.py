@@ -31,12 +31,50 @@ def _lib(cuda_ok):
     mok.load()
 
 
-def _decode(qb, sb, K):
-    """E4M3 bytes [.., N, K] and k-block-major scales [.., K/32, N] -> float64 values [.., N, K]."""
+def _sf_byte(r, kb):
+    """Byte of (row r, 32-element block kb) in a 512-byte scale block: 128 rows x 4 blocks, row
+    32 j + l and block b at byte 16 l + 4 j + b (the order the tensor cores read from TMEM)."""
+    return (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+
+
+def _decode_w(qb, sb, N, K):
+    """E4M3 bytes [E, N, K] and scale blocks [E, N/128, K/128, 512] -> (float64 values [E, N, K],
+    exponents [E, N, K/32])."""
     vals = qb.view(torch.float8_e4m3fn).double().cpu().numpy()
-    X = sb.cpu().numpy().astype(np.int64) - 127               # [.., K/32, N]
-    X = np.repeat(np.swapaxes(X, -1, -2), 32, axis=-1)[..., :K]
-    return np.ldexp(vals, X)                                   # exact powers of two
+    blocks = sb.cpu().numpy().astype(np.int64)
+    n = np.arange(N)[:, None]
+    kb = np.arange(K // 32)[None, :]
+    X = blocks[:, n // 128, kb // 4, _sf_byte(n, kb)] - 127               # [E, N, K/32]
+    return np.ldexp(vals, np.repeat(X, 32, axis=-1)), X
+
+
+def _decode_rows(layer, xq_name, sf_name, K, prows):
+    """Rows `prows` of an E4M3 row operand of the MXFP8 forward (padded row space) and their scales:
+    (float64 values [n, K], exponents [n, K/32]).  Every row's scales are stored in four blocks (row
+    groups p/32 - 3 .. p/32); all four copies must agree."""
+    vals = layer.view(xq_name)[torch.as_tensor(prows, device="cuda")].view(torch.float8_e4m3fn).double().cpu().numpy()
+    blocks = layer.view(sf_name).cpu().numpy().astype(np.int64)            # [G, K/128, 512]
+    p = np.asarray(prows)[:, None]
+    kb = np.arange(K // 32)[None, :]
+    X = blocks[p // 32, kb // 4, (p % 32) * 16 + kb % 4] - 127
+    for jj in (1, 2, 3):
+        ok = p // 32 - jj >= 0
+        Xj = blocks[np.maximum(p // 32 - jj, 0), kb // 4, (p % 32) * 16 + jj * 4 + kb % 4] - 127
+        assert np.all((Xj == X) | ~ok), f"scale copy {jj} disagrees"
+    return np.ldexp(vals, np.repeat(X, 32, axis=-1)), X
+
+
+def _padded_rows(layer, shape):
+    """Padded row of each schedule-order row, and the padding rows (expert rows padded to 32)."""
+    off = layer.view("offsets").cpu().numpy().astype(np.int64)
+    blk = layer.view("mx_blk_off").cpu().numpy().astype(np.int64)
+    assert np.array_equal(blk[1:] - blk[:-1], (off[1:] - off[:-1] + 31) // 32)
+    rows, pads = [], []
+    for e in range(shape.E):
+        n = off[e + 1] - off[e]
+        rows.append(32 * blk[e] + np.arange(n))
+        pads.append(32 * blk[e] + np.arange(n, 32 * (blk[e + 1] - blk[e])))
+    return np.concatenate(rows), np.concatenate(pads)
 
 
 def _run_mx(shape, inp, given=None):
@@ -56,15 +94,15 @@ def test_quantized_weights_bit_exact():
     inp = W.make_inputs(MID, seed=0, device="cpu")
     f64 = inputs_f64(inp)
     _, _, wq = _run_mx(MID, inp)
-    for name, w, K in (("w13", f64["w13"], MID.H), ("w2", f64["w2"], MID.I)):
-        got = _decode(wq[name + "_q"], wq[name + "_scale"], K)
+    for name, w, N, K in (("w13", f64["w13"], 2 * MID.I, MID.H), ("w2", f64["w2"], MID.H, MID.I)):
+        got, X_got = _decode_w(wq[name + "_q"], wq[name + "_scale"], N, K)
         for e in range(MID.E):
             want = q(w[e], 1)
             bad = np.argwhere(got[e] != want)
             assert bad.size == 0, (name, e, len(bad), [(tuple(b), got[e][tuple(b)], want[tuple(b)], w[e][tuple(b)])
                                                        for b in bad[:4]])
             _, X = O.mx_quantize(w[e], 1)
-            assert np.array_equal(wq[name + "_scale"][e].cpu().numpy().astype(np.int64) - 127, X.T), (name, e)
+            assert np.array_equal(X_got[e], X), (name, e)
 
 
 @pytest.mark.parametrize("skew", [False, True])
@@ -76,8 +114,26 @@ def test_mx_forward_matches_mx_oracle(skew):
     fwd = O.forward(f64["x"], f64["w_router"], f64["w13"], f64["w2"], kind=shape.router, k=shape.k,
                     renorm=shape.renorm, router_bias=f64["router_bias"], topk_idx=given, quant=q)
     layer, y, _ = _run_mx(shape, inp, given)
-    # the dispatched rows are quantised in the gather: bit-exact against the oracle's quantiser
-    assert np.array_equal(to_f64(layer.view("x_g")), q(fwd["x_g"], 1))
+    # the dispatched rows are quantised in the gather into E4M3 bytes and scale blocks at their
+    # padded rows: bit-exact against the oracle's quantiser (elements and exponents); the padding
+    # rows are zero
+    prows, pads = _padded_rows(layer, shape)
+    xg, Xg = _decode_rows(layer, "mx_xq", "mx_xsf", shape.H, prows)
+    assert np.array_equal(xg, q(fwd["x_g"], 1))
+    assert np.array_equal(Xg, O.mx_quantize(fwd["x_g"], 1)[1])
+    if len(pads):
+        zp, _ = _decode_rows(layer, "mx_xq", "mx_xsf", shape.H, pads)
+        assert not np.any(zp)
+    # a = silu(h) u quantised along I by the GEMM1 epilogue: against the oracle's quantiser applied
+    # to a computed from the GPU's own h | u (only a value on a rounding boundary can differ)
+    hu_gpu = to_f64(layer.view("hu"))
+    a_gpu = O.silu(hu_gpu[:, :shape.I]) * hu_gpu[:, shape.I:]
+    ag, _ = _decode_rows(layer, "mx_aq", "mx_asf", shape.I, prows)
+    _, _, fro_a = err_stats(ag, q(a_gpu, 1))
+    assert fro_a <= 1e-3, fro_a
+    if len(pads):
+        zp, _ = _decode_rows(layer, "mx_aq", "mx_asf", shape.I, pads)
+        assert not np.any(zp)
     _, _, fro = err_stats(to_f64(y), fwd["y"])
     assert fro <= MX_FRO, fro
     # h | u come from exact products of MX-grid operands: close to the oracle's
