@@ -456,60 +456,6 @@ cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, vo
                                      C::smem_bytes(ra.E), st);
 }
 
-// ----------------------------------------------------------------------------- MXFP8
-namespace {
-
-// E4M3 bytes w[E][N][K] (box 64 bytes of K x `rows`) and E8M0 scales s[E][K/32][N] (box `rows`
-// of N x 2 k-blocks), both without swizzle.
-bool tmaps_mx_weights(CUtensorMap* tq, CUtensorMap* ts, const void* q, const void* s, uint64_t E, uint64_t N,
-                      uint64_t K, uint32_t rows) {
-  const uint64_t dq[3] = {K, N, E};
-  const uint64_t sq[2] = {K, K * N};
-  const uint32_t bq[3] = {64, rows, 1};
-  const uint64_t ds[3] = {N, K / 32, E};
-  const uint64_t ss[2] = {N, N * (K / 32)};
-  const uint32_t bs[3] = {rows, 2, 1};
-  return make_tmap(tq, q, 3, dq, sq, bq, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_tmap(ts, s, 3, ds, ss, bs, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-}  // namespace
-
-cudaError_t launch_gemm1_swiglu_mx(const void* x_g, const void* w13_q, const void* w13_s, int R, int H, int I, int E,
-                                   const int32_t* offsets, const int32_t* tile_off, float* hu, void* act, int* status,
-                                   int n_sm, cudaStream_t st) {
-  CUtensorMap ta, tq, ts;
-  if (!tmap_2d(&ta, x_g, H, R, BK, BM) || !tmaps_mx_weights(&tq, &ts, w13_q, w13_s, E, 2 * I, H, 128))
-    return cudaErrorInvalidValue;
-  GemmArgs g = base_args(E, offsets, tile_off, status);
-  g.N = I;
-  g.K = H;
-  g.I = I;
-  g.out0 = hu;
-  g.ld0 = 2LL * I;
-  g.out1 = act;
-  g.ld1 = I;
-  const int bound = row_tiles_bound(R, E) * (I / 128);
-  return launch<MODE_ROWS, EPI_SWIGLU_MX, SPLIT_BMX, 256>(ta, ta, tq, ts, g, std::min(bound, n_sm), st);
-}
-
-cudaError_t launch_gemm2_mx(const void* act, const void* w2_q, const void* w2_s, int R, int H, int I, int E,
-                            const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                            cudaStream_t st) {
-  CUtensorMap ta, tq, ts;
-  if (!tmap_2d(&ta, act, I, R, BK, BM) || !tmaps_mx_weights(&tq, &ts, w2_q, w2_s, E, H, I, 256))
-    return cudaErrorInvalidValue;
-  GemmArgs g = base_args(E, offsets, tile_off, status);
-  g.N = H;
-  g.K = I;
-  g.out0 = out;
-  g.ld0 = H;
-  CUtensorMap to;
-  if (!tmap_out(&to, out, H, R, true)) return cudaErrorInvalidValue;
-  const int bound = row_tiles_bound(R, E) * (H / 256);
-  return launch<MODE_ROWS, EPI_F32, SPLIT_BMX, 256>(ta, ta, tq, ts, g, std::min(bound, n_sm), st, &to);
-}
-
 // ----------------------------------------------------------------------------- wait test
 __global__ void test_wait_kernel(int* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;

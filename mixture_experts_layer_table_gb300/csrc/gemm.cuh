@@ -57,8 +57,6 @@ constexpr int MN_ATOM_BYTES = 64 * 128;  // one MN-major 128B-swizzle atom colum
 // tiles wait until its rows are gathered (counter `gathered`); a slot is refilled only after
 // every tile of the minibatch it held has finished (counter `consumed`).
 enum GemmMode { MODE_DENSE = 0, MODE_ROWS = 1, MODE_DGRAD = 2, MODE_WGRAD = 3, MODE_RING = 4 };
-// EPI_SWIGLU_MX: SwiGLU with a quantised to MXFP8 along I (32-column blocks) and stored as bf16
-// (E4M3 * 2^X is exact in bf16), the A operand of the MXFP8 GEMM2.
 // EPI_SWIGLU_PAIRED (narrow kernel only): SwiGLU with the gate and up rows of the same
 // intermediate indices in two MMAs sharing the row operand, h and u in one thread's TMEM columns.
 // EPI_F32_PAIRED (narrow kernel only): two weight tiles 256 rows apart in two MMAs sharing the row
@@ -69,15 +67,10 @@ enum GemmEpi {
   EPI_SWIGLU_BWD = 3,
   EPI_T_F32 = 4,
   EPI_T_BF16 = 5,
-  EPI_SWIGLU_MX = 6,
   EPI_SWIGLU_PAIRED = 7,
   EPI_F32_PAIRED = 8  // narrow kernel only: two 256-row weight tiles per pair tile, fp32 out
 };
-// SPLIT_BMX: B is MXFP8 (E4M3 bytes + one E8M0 scale per 32 along K); TMA brings the bytes and
-// scales, eight converter warps write the exact bf16 values into the stage for the MMA.
-enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2, SPLIT_BMX = 3 };
-constexpr int GEMM_MAX_THREADS = 448;
-constexpr int CONVERTER_WARPS = 8;  // SPLIT_BMX: warps 6 .. 13
+enum GemmSplit { SPLIT_NONE = 0, SPLIT_A = 1, SPLIT_B = 2 };
 
 struct GemmArgs {
   int M;            // DENSE: rows of A; WGRAD: output rows per expert (the contiguous output dim)
@@ -132,23 +125,9 @@ struct GemmCfg {
   static constexpr int B_TILE = BN * BK * 2;
   static constexpr int A_TILES = SPLIT == SPLIT_A ? 2 : 1;
   static constexpr int B_TILES = SPLIT == SPLIT_B ? 2 : 1;
-  static constexpr bool kBmx = (SPLIT == SPLIT_BMX);
-  // MXFP8 B: E4M3 bytes [BN][64] and scales [2][BN] after the converted bf16 B tile
-  static constexpr int BQ_BYTES = kBmx ? BN * BK : 0;
-  static constexpr int BS_BYTES = kBmx ? 1024 : 0;
-  // MXFP8 B (three rings): the stage ring carries only the E4M3 bytes and scales of B (the HBM
-  // stream, 5 deep), released as soon as the converter warps have expanded them; the A tiles
-  // have their own 3-deep ring, filled by a second producer warp; the expanded bf16 B tiles a
-  // 2-deep ring between the converters and the MMA.  With one shared ring (A, E4M3, bf16 B in
-  // each stage, 3 deep) a stage was held from its load through the conversion to the MMA and the
-  // E4M3 stream ran at a fraction of HBM.
-  static constexpr int STAGES_A = kBmx ? 3 : 0;
-  static constexpr int STAGES_C = kBmx ? 2 : 0;
-  static constexpr int STAGE_BYTES = kBmx ? BQ_BYTES + BS_BYTES : A_TILE * A_TILES + B_TILE * B_TILES;
-  // bytes TMA delivers into one stage
-  static constexpr int TX_BYTES = kBmx ? BQ_BYTES + 2 * BN : STAGE_BYTES;
-  static constexpr int THREADS = kBmx ? 192 + 32 * CONVERTER_WARPS + 32 : 192;
-  static constexpr int A_WARP = 6 + CONVERTER_WARPS;  // MXFP8: the A-tile producer
+  static constexpr int STAGE_BYTES = A_TILE * A_TILES + B_TILE * B_TILES;
+  static constexpr int TX_BYTES = STAGE_BYTES;  // bytes TMA delivers into one stage
+  static constexpr int THREADS = 192;
   // WGRAD stages its 32 x 32 output blocks in shared memory for TMA stores: one buffer of up
   // to 32 x 32 fp32 per block of a tile, per epilogue warp.
   // ROWS / DGRAD fp32 and SwiGLU outputs leave through TMA stores from one 4 KB buffer per
@@ -157,16 +136,16 @@ struct GemmCfg {
   static constexpr int STG_BYTES = (MODE == MODE_WGRAD)                        ? 4 * (BN / 32) * 4096
                                    : (kTmaEpi || EPI == EPI_SWIGLU_BWD) ? 4 * 4096
                                                                         : 0;
-  static constexpr int RING = kBmx ? 5 * STAGE_BYTES : (MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
-  static constexpr int STAGES = kBmx ? 5 : (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
-  static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES + STAGES_A * A_TILE + STAGES_C * B_TILE;
+  static constexpr int RING = (MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
+  static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
+  static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
                 "tcgen05.alloc takes a power of two from 32 to 512 columns");
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, kAmn, kBmn);
   static __host__ __device__ int n_tiles(const GemmArgs& a) {
-    return (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_MX) ? a.I / 128 : (a.N + BN - 1) / BN;
+    return EPI == EPI_SWIGLU ? a.I / 128 : (a.N + BN - 1) / BN;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
     return size_t(RINGS_BYTES) + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
@@ -635,14 +614,10 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* a_ring = smem + STAGES * STAGE_BYTES;          // MXFP8: A tiles (C::STAGES_A)
-  uint8_t* c_ring = a_ring + C::STAGES_A * A_TILE;        // MXFP8: expanded bf16 B tiles (C::STAGES_C)
   uint8_t* staging = smem + C::RINGS_BYTES;               // epilogue output staging (C::STG_BYTES)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STG_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  // bars + 2*STAGES+5: conv[STAGES] (MXFP8: an expanded B tile is ready, per C slot)
-  // bars + 3*STAGES+5: fullA[STAGES_A], emptyA[STAGES_A], cempty[STAGES_C] (MXFP8)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5 + 2 * C::STAGES_A + C::STAGES_C);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(staging + C::STG_BYTES + 256);
   int* s_toff = s_off + (args.E + 1);
@@ -654,10 +629,6 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
-  auto conv_bar = [&](int s) { return smem_u32(&bars[2 * STAGES + 5 + s]); };
-  auto fulla_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + s]); };
-  auto emptya_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + C::STAGES_A + s]); };
-  auto cempty_bar = [&](int s) { return smem_u32(&bars[3 * STAGES + 5 + 2 * C::STAGES_A + s]); };
 
   if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
     ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
@@ -670,23 +641,13 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), C::kBmx ? CONVERTER_WARPS : 1);  // MXFP8: the converters release the stage
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
-    if (C::kBmx) {
-      for (int s = 0; s < C::STAGES_C; ++s) {
-        mbar_init(conv_bar(s), CONVERTER_WARPS);  // one arrival per converter warp
-        mbar_init(cempty_bar(s), 1);
-      }
-      for (int s = 0; s < C::STAGES_A; ++s) {
-        mbar_init(fulla_bar(s), 1);
-        mbar_init(emptya_bar(s), 1);
-      }
-    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -761,21 +722,6 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
           if (MODE == MODE_DENSE) {
             tma_load_2d(sa, &tmA, fb, k0, t.row0, pol_act);
             tma_load_2d(sb, &tmB, fb, k0, t.n * BN, pol_w);
-          } else if ((MODE == MODE_ROWS || MODE == MODE_RING) && C::kBmx) {
-            // MXFP8 weights: E4M3 bytes (tmB) and E8M0 scales (tmB2, [E][K/32][N]) of the B rows;
-            // the stage holds nothing else (A has its own ring and producer)
-            const uint32_t sbq = sa;
-            const uint32_t sbs = sbq + C::BQ_BYTES;
-            (void)a_row;
-            if (EPI == EPI_SWIGLU_MX) {
-              tma_load_3d(sbq, &tmB, fb, k0, t.n * 128, t.e, pol_w);
-              tma_load_3d(sbq + C::BQ_BYTES / 2, &tmB, fb, k0, args.I + t.n * 128, t.e, pol_w);
-              tma_load_3d(sbs, &tmB2, fb, t.n * 128, kb * 2, t.e, pol_w);
-              tma_load_3d(sbs + BN, &tmB2, fb, args.I + t.n * 128, kb * 2, t.e, pol_w);
-            } else {
-              tma_load_3d(sbq, &tmB, fb, k0, t.n * BN, t.e, pol_w);
-              tma_load_3d(sbs, &tmB2, fb, t.n * BN, kb * 2, t.e, pol_w);
-            }
           } else if (MODE == MODE_ROWS || MODE == MODE_RING) {
             tma_load_2d(sa, &tmA, fb, k0, a_row, pol_act);
             if (SPLIT == SPLIT_A) tma_load_2d(sa2, &tmA2, fb, k0, a_row, pol_act);
@@ -831,8 +777,6 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
     // ------------------------------------------------------------------ MMA issuer
     int stage = 0;
     uint32_t phase = 0;
-    int astage = 0, cstage = 0;  // MXFP8: A ring and expanded-B ring
-    uint32_t aphase = 0, cphase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -851,23 +795,16 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
       const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
       for (int kb = 0; kb < t.nkb; ++kb) {
         int f_ok = 1;
-        if (lane == 0) {
-          if (C::kBmx) {
-            f_ok = mbar_wait(conv_bar(cstage), cphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
-            if (f_ok) f_ok = mbar_wait(fulla_bar(astage), aphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
-          } else {
-            f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
-          }
-        }
+        if (lane == 0) f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
         if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t* sa_ptr = C::kBmx ? a_ring + astage * A_TILE : smem + stage * STAGE_BYTES;
+        uint8_t* sa_ptr = smem + stage * STAGE_BYTES;
         const uint32_t sa = smem_u32(sa_ptr);
         const uint32_t sa2 = sa + A_TILE;
-        const uint32_t sb = C::kBmx ? smem_u32(c_ring + cstage * C::B_TILE) : sa + A_TILE * C::A_TILES;
+        const uint32_t sb = sa + A_TILE * C::A_TILES;
         const uint32_t sb2 = sb + C::B_TILE;
         int kvalid = BK;
         if (MODE == MODE_WGRAD) {
@@ -902,25 +839,11 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
             if (SPLIT == SPLIT_A) umma_f16(d_tmem, smem_desc_sw128(sa2 + a_off, a_lbo, a_sbo), bdesc, C::IDESC, 1u);
             if (SPLIT == SPLIT_B) umma_f16(d_tmem, adesc, smem_desc_sw128(sb2 + b_off, b_lbo, b_sbo), C::IDESC, 1u);
           }
-          if (C::kBmx) {
-            umma_commit(emptya_bar(astage));
-            umma_commit(cempty_bar(cstage));
-          } else {
-            umma_commit(empty_bar(stage));
-          }
+          umma_commit(empty_bar(stage));
         }
         any_mma = true;
         __syncwarp();
-        if (C::kBmx) {
-          if (++astage == C::STAGES_A) {
-            astage = 0;
-            aphase ^= 1;
-          }
-          if (++cstage == C::STAGES_C) {
-            cstage = 0;
-            cphase ^= 1;
-          }
-        } else if (++stage == STAGES) {
+        if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
@@ -939,119 +862,6 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
         mbar_wait(drain_bar, 0, &no_abort, args.status, SITE_GEMM_DRAIN);
       }
       __syncwarp();
-    }
-  } else if (C::kBmx && warp == C::A_WARP) {
-    // ------------------------------------------------------------------ MXFP8: A-tile producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      const uint64_t pol_act = l2_policy_evict_last();
-      int st = 0;
-      uint32_t ph = 0;
-      int issued = 0;
-      bool ok = true;
-      for (int g = cta0; g < total && ok; g += ncta) {
-        const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
-        for (int kb = 0; kb < t.nkb; ++kb) {
-          if (!mbar_wait(emptya_bar(st), ph ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs,
-                         32)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fa = fulla_bar(st);
-          mbar_arrive_expect_tx(fa, A_TILE);
-          tma_load_2d(smem_u32(a_ring + st * A_TILE), &tmA, fa, kb * BK, t.row0, pol_act);
-          ++issued;
-          if (++st == C::STAGES_A) {
-            st = 0;
-            ph ^= 1;
-          }
-        }
-      }
-      if (!ok) {
-        // Aborted: let the copies already in flight land before the CTA exits.
-        const int outstanding = min(issued, C::STAGES_A);
-        for (int i = 0; i < outstanding; ++i) {
-          if (--st < 0) {
-            st = C::STAGES_A - 1;
-            ph ^= 1;
-          }
-          volatile int no_abort = 0;
-          mbar_wait(fulla_bar(st), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
-        }
-      }
-    }
-  } else if (C::kBmx && warp >= 6) {
-    // ------------------------------------------------------------------ MXFP8 B converters
-    // For every stage the producer fills: E4M3 bytes of B ([BN][64], row-major) and their E8M0
-    // scales -> exact bf16 values in the 128B-swizzled K-major layout the MMA reads.  Thread
-    // t of the 256 converts 16-byte chunks t, t+256, ... (chunk c = row c/4, elements
-    // 16*(c%4) .. +15, scale block (c%4)/2).
-    const int ct = threadIdx.x - 6 * 32;
-    int stage = 0, cstage = 0;
-    uint32_t phase = 0, cphase = 0;
-    bool ok = true;
-    for (int g = cta0; g < total && ok; g += ncta) {
-      const TileInfo t = decode_tile<MODE, EPI, SPLIT, BN_>(args, g, s_off, s_toff);
-      for (int kb = 0; kb < t.nkb; ++kb) {
-        int f_ok = 1;
-        if (lane == 0) {
-          f_ok = mbar_wait(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL, kWaitLimitNs, 32);
-          // the expanded-B slot must have been read by the MMAs of its previous use
-          if (f_ok)
-            f_ok = mbar_wait(cempty_bar(cstage), cphase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_FULL,
-                             kWaitLimitNs, 32);
-        }
-        if (!__shfl_sync(0xffffffffu, f_ok, 0)) {
-          ok = false;
-          break;
-        }
-        uint8_t* b16 = c_ring + cstage * C::B_TILE;                 // expanded bf16 B
-        const uint8_t* bq = smem + stage * STAGE_BYTES;            // E4M3 bytes
-        const uint8_t* bs = bq + C::BQ_BYTES;                      // E8M0 scales
-        // all chunks of this thread at once (loads first), so that their shared-memory latencies overlap
-        constexpr int CHUNKS = BN * 4 / (32 * CONVERTER_WARPS);
-#pragma unroll
-        for (int it = 0; it < CHUNKS; ++it) {
-          const int c = ct + it * 32 * CONVERTER_WARPS;
-          const int r = c >> 2;
-          const int q = c & 3;
-          const int kk = q >> 1;
-          const int sidx = (EPI == EPI_SWIGLU_MX) ? ((r >> 7) * 256 + kk * 128 + (r & 127)) : (kk * BN + r);
-          const int X = (int)bs[sidx] - 127;
-          const uint4 raw = *reinterpret_cast<const uint4*>(bq + r * 64 + q * 16);
-          uint8_t* row_base = b16 + (r >> 3) * 1024 + (r & 7) * 128;
-          uint4* dst0 = reinterpret_cast<uint4*>(row_base + (((2 * q) ^ (r & 7)) << 4));
-          uint4* dst1 = reinterpret_cast<uint4*>(row_base + (((2 * q + 1) ^ (r & 7)) << 4));
-          const uint32_t zero = e4m3_zero_exponent_bytes(raw.x) | e4m3_zero_exponent_bytes(raw.y) |
-                                e4m3_zero_exponent_bytes(raw.z) | e4m3_zero_exponent_bytes(raw.w);
-          if (zero == 0u && (unsigned)(X + 120) <= 239u) {
-            const uint32_t bias2 = (uint32_t)(120 + X) * 0x00800080u;  // (120 + X) << 7 in both halves
-            uint32_t o0, o1, o2, o3, o4, o5, o6, o7;
-            e4m3x4_to_bf16x4(raw.x, bias2, o0, o1);
-            e4m3x4_to_bf16x4(raw.y, bias2, o2, o3);
-            e4m3x4_to_bf16x4(raw.z, bias2, o4, o5);
-            e4m3x4_to_bf16x4(raw.w, bias2, o6, o7);
-            *dst0 = make_uint4(o0, o1, o2, o3);
-            *dst1 = make_uint4(o4, o5, o6, o7);
-          } else {
-            e4m3x16_to_bf16x16_slow(raw, X, dst0, dst1);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(conv_bar(cstage));  // the expanded tile is ready for the MMA
-          mbar_arrive(empty_bar(stage));  // the E4M3 stage has been read: the producer may refill it
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++cstage == C::STAGES_C) {
-          cstage = 0;
-          cphase ^= 1;
-        }
-      }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
@@ -1128,41 +938,6 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
         }
       } else if (EPI == EPI_SWIGLU) {
         epi_swiglu_row(tacc, valid, row, t.n, args);
-      } else if (EPI == EPI_SWIGLU_MX) {
-        // as EPI_SWIGLU, but a is quantised to MXFP8 in 32-column blocks (one block per chunk of
-        // this thread's row) and stored as the exact bf16 values of the MX grid.
-        float* hu = reinterpret_cast<float*>(args.out0) + row * args.ld0;
-        __nv_bfloat16* act = reinterpret_cast<__nv_bfloat16*>(args.out1) + row * args.ld1;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t vh[32], vu[32];
-          tmem_ld_32x32b_x32(tacc + c * 32, vh);
-          tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
-          tmem_wait_ld();
-          if (valid) {
-            const int col = t.n * 128 + c * 32;
-            float a[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float h = __uint_as_float(vh[j]), u = __uint_as_float(vu[j]);
-              a[j] = h / (1.0f + __expf(-h)) * u;
-            }
-            mx_quantize32(a, nullptr);
-            uint32_t pa[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) pa[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
-            float4* dh = reinterpret_cast<float4*>(hu + col);
-            float4* du = reinterpret_cast<float4*>(hu + args.I + col);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              dh[j] = make_float4(__uint_as_float(vh[4 * j]), __uint_as_float(vh[4 * j + 1]),
-                                  __uint_as_float(vh[4 * j + 2]), __uint_as_float(vh[4 * j + 3]));
-              du[j] = make_float4(__uint_as_float(vu[4 * j]), __uint_as_float(vu[4 * j + 1]),
-                                  __uint_as_float(vu[4 * j + 2]), __uint_as_float(vu[4 * j + 3]));
-            }
-            store_u32x16(act + col, pa);
-          }
-        }
       } else {  // EPI_SWIGLU_BWD
         epi_swiglu_bwd_cols<BN>(tacc, (long long)t.row0 + quarter * 32, nvalid, t.n, args, staging + (warp - 2) * 4096,
                                 lane);

@@ -80,7 +80,7 @@ struct RingArgs {
 };
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, cudaStream_t st);
-// MXFP8 (mx.cu, gemm.cu)
+// MXFP8 weights (mx.cu)
 cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm, cudaStream_t st);
 // MXFP8 backward operands (mx.cu).  src of launch_mx_quant_rows: 0 plain rows (in0, fixed
 // segments of seg_len rows), 1 hi + lo rows, 2 a = silu(h) u from h | u, 3 token rows gathered by
@@ -94,12 +94,6 @@ cudaError_t launch_mx_quant_cols(const void* hi, const void* lo, long long R, in
                                  cudaStream_t st);
 cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
                                   cudaStream_t st);
-cudaError_t launch_gemm1_swiglu_mx(const void* x_g, const void* w13_q, const void* w13_s, int R, int H, int I, int E,
-                                   const int32_t* offsets, const int32_t* tile_off, float* hu, void* act, int* status,
-                                   int n_sm, cudaStream_t st);
-cudaError_t launch_gemm2_mx(const void* act, const void* w2_q, const void* w2_s, int R, int H, int I, int E,
-                            const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                            cudaStream_t st);
 // MXFP8 forward on the FP8 tensor path (mx.cu, gemm_mx.cu): E4M3 row operands in the padded row
 // space of mx_tiles.h (blk_off from launch_mx_block_offsets), scale blocks of RP / 32 + 4 row groups.
 cudaError_t launch_gather_rows_mxf8(const void* x, const int32_t* src_of, const int32_t* topk_idx,

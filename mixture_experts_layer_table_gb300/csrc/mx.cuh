@@ -38,51 +38,6 @@ __device__ __forceinline__ float2 f32x2_from_e4m3x2(uint16_t v) {
   return __half22float2(hh);
 }
 
-// Four E4M3 bytes w (byte i = element i) times 2^X -> four bf16 values as two bf16x2 words
-// (lo = elements 0, 1; hi = elements 2, 3), with integer operations only: the sign, 4 exponent
-// and 3 mantissa bits of each byte are moved to the bf16 positions and (120 + X) is added to
-// the exponent (E4M3 bias 7 -> bf16 bias 127).  Valid when no byte has a zero exponent field
-// (zero or subnormal) and -120 <= X <= 119; returns false otherwise (the caller converts the
-// slow way).
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
-  return d;
-}
-
-// Nonzero when some byte of w has a zero exponent field (an E4M3 zero or subnormal).
-__device__ __forceinline__ uint32_t e4m3_zero_exponent_bytes(uint32_t w) {
-  const uint32_t t = w & 0x78787878u;
-  return (t - 0x01010101u) & ~t & 0x80808080u;
-}
-
-// Four E4M3 bytes with nonzero exponents, times 2^X for -120 <= X <= 119.  prmt with the
-// sign-replicate selector bit builds [sign(b1)][b1][sign(b0)][b0]; shifted left by 4 this puts
-// each byte's exponent and mantissa at bf16 bits 10..4 and its sign at bit 15 of its half,
-// the mask drops the rest, and adding (120 + X) << 7 rebiases the exponent.
-__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t bias2, uint32_t& lo, uint32_t& hi) {
-  lo = ((prmt(w, 0x9180u) << 4) & 0x87F087F0u) + bias2;
-  hi = ((prmt(w, 0xB3A2u) << 4) & 0x87F087F0u) + bias2;
-}
-
-// Slow path for a 16-byte chunk that holds a zero / subnormal or has an extreme scale (kept
-// out of line so that the common path is a real branch, not a predicated copy of this one): the
-// 16 values, times 2^X, as bf16 into dst0 (elements 0-7) and dst1 (elements 8-15).  It stores
-// them itself so that the common path keeps its values in registers.
-static __device__ __noinline__ void e4m3x16_to_bf16x16_slow(uint4 raw, int X, uint4* dst0, uint4* dst1) {
-  const float sc = exp2_int(X);
-  const uint16_t* pairs = reinterpret_cast<const uint16_t*>(&raw);
-  uint32_t o[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float2 f = f32x2_from_e4m3x2(pairs[j]);
-    __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
-    o[j] = *reinterpret_cast<uint32_t*>(&b);
-  }
-  *dst0 = make_uint4(o[0], o[1], o[2], o[3]);
-  *dst1 = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
 // Quantises 32 fp32 values in place to the MX grid (values become e4m3 * 2^X, exactly
 // representable in bf16) and returns X.  `q` receives the 32 E4M3 bytes when non-null.
 __device__ __forceinline__ int mx_quantize32(float (&v)[32], uint8_t* q) {
