@@ -185,6 +185,147 @@ def cpu_sample_subprocess(T, E, repeats=1):
     return times, cores
 
 
+class LazyExperts:
+    """[E][rows][cols] float64 view of a host bf16 tensor that widens one expert at a time, so
+    that the oracle can stream the experts of a full-size layer (45 GB in float64) through host
+    memory.  Indexing only: w[e], w[e, a:b]."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        if isinstance(idx, tuple):
+            return self.t[idx[0]].double().numpy()[idx[1:]]
+        return self.t[idx].double().numpy()
+
+
+def mem_available_gb():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 2**20
+    except OSError:
+        pass
+    return None
+
+
+def cpu_planned_timings(inp, shp):
+    """The float64 oracle, as it stands, at the full sizes of the workloads, on the host cores
+    after the GPU runs: the DSV3 layer forward (near-uniform routing) and the skewed DSV3 layer
+    forward + backward on all cores (numpy / OpenBLAS default threads, one per core), each
+    streaming one expert's weights in float64 at a time (LazyExperts), and the tiny layer forward
+    + backward on one thread.  The inputs are this run's (copied from the GPU).  The skewed
+    forward + backward holds the layer's float64 weight gradients (45 GB): it is skipped, with
+    the reason, when the host has less than 150 GB available."""
+    import numpy as np
+    from mixture_experts_layer_table_gb300 import workloads as W
+    from oracle import moe_oracle as O
+
+    cores = os.cpu_count() or 1
+    out = {"cores": cores, "threads": "OpenBLAS default (one per core); tiny: 1", "cpu_model": cpu_model()}
+    host = {k: v.cpu() for k, v in inp.items() if v is not None}
+    x, wr, dy = (host[n].double().numpy() for n in ("x", "w_router", "dy"))
+    w13, w2 = LazyExperts(host["w13"]), LazyExperts(host["w2"])
+    T = shp.T
+    t0 = time.perf_counter()
+    O.forward(x, wr, w13, w2, kind=shp.router, k=shp.k, renorm=shp.renorm)
+    sec = time.perf_counter() - t0
+    out["dsv3_fwd"] = {"seconds": round(sec, 2), "tokens_per_s": round(T / sec, 1),
+                       "workload": shp.name + ", forward, full size"}
+    avail = mem_available_gb()
+    skew = W.DSV3_SKEW
+    if avail is not None and avail < 150:
+        out["dsv3_skew_fwd_bwd"] = {"skipped": f"needs ~120 GB of host memory, {avail:.0f} GB available"}
+    else:
+        bias = W.skew_bias(skew.E).double().numpy()
+        t0 = time.perf_counter()
+        f = O.forward(x, wr, w13, w2, kind=skew.router, k=skew.k, renorm=skew.renorm, router_bias=bias)
+        O.backward(f, dy, x, wr, w13, w2, kind=skew.router, k=skew.k, renorm=skew.renorm)
+        sec = time.perf_counter() - t0
+        del f
+        out["dsv3_skew_fwd_bwd"] = {"seconds": round(sec, 2), "tokens_per_s": round(T / sec, 1),
+                                    "workload": skew.name + ", forward + backward, full size"}
+    del x, wr, dy, w13, w2, host
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-tiny"], env=env, capture_output=True,
+                       text=True, timeout=600)
+    if r.returncode == 0:
+        sec = json.loads(r.stdout.strip().splitlines()[-1])
+        out["tiny_fwd_bwd_1thread"] = {"seconds": round(sec, 4), "tokens_per_s": round(W.TINY.T / sec, 1),
+                                       "workload": W.TINY.name + ", forward + backward, one thread"}
+    else:
+        out["tiny_fwd_bwd_1thread"] = {"skipped": r.stderr[-300:]}
+    return out
+
+
+def cpu_tiny_run():
+    """Seconds of the float64 oracle's forward + backward of the tiny layer (one thread when the
+    caller sets the BLAS thread count to 1)."""
+    from mixture_experts_layer_table_gb300 import workloads as W
+    from oracle import moe_oracle as O
+    shp = W.TINY
+    inp = W.make_inputs(shp, seed=0, device="cpu")
+    f = {k: (v.double().numpy() if v is not None else None) for k, v in inp.items()}
+    best = None
+    for _ in range(3):
+        t0 = time.perf_counter()
+        fwd = O.forward(f["x"], f["w_router"], f["w13"], f["w2"], kind=shp.router, k=shp.k, renorm=shp.renorm)
+        O.backward(fwd, f["dy"], f["x"], f["w_router"], f["w13"], f["w2"], kind=shp.router, k=shp.k,
+                   renorm=shp.renorm)
+        sec = time.perf_counter() - t0
+        best = sec if best is None else min(best, sec)
+    return best
+
+
+def fwd_gemm_hbm(trace, kb, peaks):
+    """Forward expert GEMMs at the DSV3 layer against the measured HBM copy bandwidth: algorithmic
+    bytes (weights, rows in and out) over their traced time."""
+    names = [n for n in ("gemm1_swiglu", "gemm2") if n in trace and n in kb]
+    if not names:
+        return None
+    ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in names)
+    gbps = sum(kb[n] for n in names) / (ms * 1e-3) / 1e9
+    return {"kernels": names, "ms": round(ms, 4), "GBps": round(gbps, 1), "frac": round(gbps / peaks["hbm_gbs"], 4),
+            "peak": peaks["hbm_gbs"]}
+
+
+def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
+    """The ring forward at `shp` (a fixed 512 MiB token ring) for each minibatch of the sweep:
+    ms per forward over K forwards after W warm-ups, and whether y is bitwise the plain forward's."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream()
+    y = torch.empty_like(y_plain)
+    sweep = {}
+    for m in W.RING_MINIBATCHES:
+        layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES), device=x.device)
+        for _ in range(warmup):
+            layer.forward(x, w_router, w13, w2, y=y)
+        torch.cuda.synchronize()
+        if layer.status() != (0, 0):
+            raise RuntimeError("device status set during the ring warm-up")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            layer.forward(x, w_router, w13, w2, y=y)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if layer.status() != (0, 0):
+            raise RuntimeError("device status set in the ring forward")
+        ms = e0.elapsed_time(e1) / steps
+        sweep[str(m)] = {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
+                         "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
+                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain))}
+        del layer
+    return sweep
+
+
 def tensor_sha256(t):
     """SHA-256 of a tensor's bit pattern (row-major bytes), read back to the host."""
     import hashlib
@@ -342,6 +483,36 @@ def run_mok(args, rank, world, local_rank):
     torch.cuda.synchronize()
     fwd_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
 
+    # ---- the same step with bf16 weight gradients (MOK_FLAG_WGRAD_BF16): what the fp32 reading
+    #      of dW13 / dW2 costs (the bf16 result is the fp32 one rounded to nearest even)
+    wgrad_bf16_ms = None
+    if not args.no_wgrad_bf16:
+        layer16 = mok.MoELayer(mok.desc_from_shape(shp, flags=GEMM_FLAGS[args.gemm] | N.FLAG_WGRAD_BF16), device=dev)
+        g16 = dict(grads)
+        g16["dw13"] = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
+        g16["dw2"] = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            layer16.forward(x, wr, w13, w2, y=y)
+            layer16.backward(dy, x, wr, w13, w2, out=g16)
+        barrier()
+        torch.cuda.synchronize()
+        N.trace_start(40 * args.steps + 16)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            layer16.forward(x, wr, w13, w2, y=y)
+            layer16.backward(dy, x, wr, w13, w2, out=g16)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        trace16 = N.trace_stop()
+        wgrad_bf16_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+        if layer16.status() != (0, 0):
+            raise RuntimeError("device status set in the bf16 weight-gradient step")
+        wgrad_bf16 = {"fwd_bwd_ms": round(wgrad_bf16_ms, 4),
+                      "tokens_per_s": round(whole_job_rate(T, world, wgrad_bf16_ms), 1),
+                      "kernels": {n: round(trace16[n]["total_ms"] / trace16[n]["launches"], 4)
+                                  for n in ("wgrad_w2", "wgrad_w13") if n in trace16}}
+        del layer16, g16
+
     # ---- end to end through the public API with host buffers (pinned), copies timed.  Every
     #      step copies its own x and dY in and its y and dX out; a copy stream moves step i+1's
     #      inputs and step i-1's outputs while step i computes (two device buffer sets).
@@ -453,13 +624,16 @@ def run_mok(args, rank, world, local_rank):
         shp_tb = W.RING
         g = torch.Generator(device=dev).manual_seed(12345 + rank)
         x_tb = torch.randn((shp_tb.T, H), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
-        tb_ms, tb_kernels, tb_grouped, tb_layer, _ = tensor_bound_forward(shp_tb, x_tb, wr, w13, w2, args.steps,
-                                                                         args.warmup, GEMM_FLAGS[args.gemm])
+        tb_ms, tb_kernels, tb_grouped, tb_layer, y_tb = tensor_bound_forward(shp_tb, x_tb, wr, w13, w2, args.steps,
+                                                                            args.warmup, GEMM_FLAGS[args.gemm])
         tb = {"workload": shp_tb.name + " (same weights, x ~ N(0, 1))", "fwd_ms": round(tb_ms, 4),
               "tokens_per_s": round(whole_job_rate(shp_tb.T, world, tb_ms), 1),
               "grouped_gemm": tb_grouped,
               "kernels": {n: v for n, v in tb_kernels.items()}}
-        del tb_layer, x_tb
+        del tb_layer
+        if not args.no_ring_sweep:
+            tb["ring_sweep"] = ring_sweep(shp_tb, x_tb, wr, w13, w2, y_tb.clone(), args.steps, args.warmup)
+        del x_tb, y_tb
 
     if rank != 0:
         return
@@ -500,6 +674,8 @@ def run_mok(args, rank, world, local_rank):
         cpu = {"value": CPU_SAMPLE["T"] / times[0], "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": sample_desc(CPU_SAMPLE["T"], CPU_SAMPLE["E"]), "seconds": round(times[0], 2),
                "cpu_model": cpu_model()}
+        if not args.no_cpu_full:
+            cpu["planned"] = cpu_planned_timings(inp, shp)
 
     step_bytes = 2 * T * H * 2
     line = {
@@ -519,13 +695,19 @@ def run_mok(args, rank, world, local_rank):
                          "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4),
                          "tflops_fwd": round(fwd_gemm_tflops, 1),
                          "frac_bf16_peak_fwd": round(fwd_gemm_tflops / peaks["bf16_tflops_sustained"], 4),
-                         "peak": peaks["bf16_tflops_sustained"], "peak_source": peak_kind + " (sustained)"},
+                         "peak": peaks["bf16_tflops_sustained"], "peak_source": peak_kind + " (sustained)",
+                         "frac_bf16_peak_fwd_burst": round(fwd_gemm_tflops / peaks["bf16_tflops"], 4),
+                         "fwd_hbm": fwd_gemm_hbm(trace, kb, peaks),
+                         "note": "at this shape (128 rows per expert) the forward GEMMs stream 22.5 GB of "
+                                 "weights: HBM-bound, their HBM fraction is the one that applies"},
         "roofline": roofline,
         "kernels": per_kernel,
         "e2e": {"value": round(whole_job_rate(T, world, e2e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": step_bytes,
                 "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step; "
                         "the copies of neighbouring steps overlap the compute on a second stream"},
+        "wgrad_bf16": wgrad_bf16 if wgrad_bf16_ms is not None else None,
+        "fwd_bwd_ms_wgrad_bf16": round(wgrad_bf16_ms, 4) if wgrad_bf16_ms is not None else None,
         "mxfp8_fwd": mx,
         "tensor_bound_fwd": tb,
         "inputs": {"seed": 1000 * rank, "generators": "x, W_r, W13, W2, dY from seeds seed+0..4 (fp32 draws "
@@ -591,6 +773,11 @@ def tensor_bound_forward(shp, x, w_router, w13, w2, steps, warmup, flags=0):
                "frac_bf16_peak": round(g_tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
                "peak_source": peak_kind, "flops": "algorithmic: 2*R*2I*H (GEMM1) + 2*R*H*I (GEMM2)",
                "clocks": clocks}
+    if clocks and clocks.get("sm_mhz") and peaks.get("sm_max_mhz"):
+        # the burst peak scaled to this run's median SM clock (taking the burst figure as measured
+        # at the maximum clock): how close the kernels come at the clock the power cap allowed
+        scale = clocks["sm_mhz"] / peaks["sm_max_mhz"]
+        grouped["frac_bf16_peak_clock_normalised"] = round(g_tf / (peaks["bf16_tflops"] * scale), 4)
     return ms, kernels, grouped, layer, y
 
 
@@ -606,36 +793,11 @@ def run_ring_sweep(args):
     mok.load()
     shp = W.RING
     inp = W.make_inputs(shp, seed=0, device="cuda", with_dy=False)
-    stream = torch.cuda.current_stream()
     plain_ms, kernels, grouped, plain, y = tensor_bound_forward(shp, inp["x"], inp["w_router"], inp["w13"], inp["w2"],
                                                                 args.steps, args.warmup, GEMM_FLAGS[args.gemm])
     y_plain = y.clone()
     del plain
-
-    def time_forward(layer):
-        for _ in range(args.warmup):
-            layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
-        torch.cuda.synchronize()
-        if layer.status() != (0, 0):
-            raise RuntimeError("device status set during warm-up")
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if layer.status() != (0, 0):
-            raise RuntimeError("device status set")
-        return e0.elapsed_time(e1) / args.steps
-
-    sweep = {}
-    for m in W.RING_MINIBATCHES:
-        layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES))
-        ms = time_forward(layer)
-        sweep[str(m)] = {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
-                         "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
-                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain))}
-        del layer
+    sweep = ring_sweep(shp, inp["x"], inp["w_router"], inp["w13"], inp["w2"], y_plain, args.steps, args.warmup)
     best = min(sweep.values(), key=lambda v: v["fwd_ms"])
     line = {"metric": "ring forward tokens/s (fixed 512 MiB token ring, minibatch sweep)",
             "value": best["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -650,6 +812,9 @@ def run_ring_sweep(args):
 
 
 def main():
+    if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-tiny":
+        print(json.dumps(cpu_tiny_run()))
+        return
     if len(sys.argv) >= 2 and sys.argv[1] == "--cpu-sample":
         T, E, rep = int(sys.argv[2]), int(sys.argv[3]), int(sys.argv[4])
         print(json.dumps(cpu_sample_run(T, E, rep)))
@@ -660,6 +825,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mok", "reference"], default="mok")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-full", action="store_true",
+                    help="skip the full-size oracle timings (DSV3 forward, skewed DSV3 forward + backward; ~1 min)")
+    ap.add_argument("--no-wgrad-bf16", action="store_true", help="skip the step with bf16 weight gradients")
+    ap.add_argument("--no-ring-sweep", action="store_true",
+                    help="skip the ring-forward minibatch sweep at T=16384 in the default line")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")
     ap.add_argument("--no-tensor-bound", action="store_true",
                     help="skip the forward at T=16384 (tensor-bound grouped GEMMs)")

@@ -125,6 +125,7 @@ typedef struct {
    * GEMM operand produced inside the layer keeps about 16 significant bits. */
   int64_t status;     /* i32 [64]     device status word (code, site), then per-call work counters */
   int64_t logits;     /* f32 [T][E]   router logits */
+  int64_t sched;      /* i32 [ceil(T*k/1024)][E]  schedule-table scratch: per-block counts, then starts */
   int64_t act;        /* bf16 [T*k][I]  SwiGLU output a = silu(h) * u, hi part */
   int64_t act_lo;     /* bf16 [T*k][I]  lo part */
   int64_t expert_out; /* f32 [T*k][H]   expert outputs o (unweighted) */

@@ -36,7 +36,7 @@ class LayerDesc(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
-                 "x_g", "hu", "ctx_bytes", "status", "logits", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
+                 "x_g", "hu", "ctx_bytes", "status", "logits", "sched", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
                  "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "mx_xq", "mx_xsf", "mx_aq",
                  "mx_asf", "ws_bytes"]
@@ -245,7 +245,7 @@ def test_bounded_wait(ws, limit_ms: int, stream=None):
 _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.float32, "counts": torch.int32,
                "offsets": torch.int32, "row_of": torch.int32, "src_of": torch.int32, "tile_off": torch.int32,
                "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.float32, "status": torch.int32,
-               "logits": torch.float32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
+               "logits": torch.float32, "sched": torch.int32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
                "expert_out": torch.float32, "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "dhu_lo": torch.bfloat16,
                "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
                "dg_part": torch.float32, "dlogits": torch.float32, "mx_dhu_c": torch.bfloat16,
@@ -278,7 +278,7 @@ class MoELayer:
         R = d.T * d.k
         return {"topk_idx": (d.T, d.k), "gates": (d.T, d.k), "scores": (d.T, d.E), "counts": (d.E,),
                 "offsets": (d.E + 1,), "row_of": (R,), "src_of": (R,), "tile_off": (d.E + 1,), "gate_row": (R,),
-                "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "act": (R, d.I),
+                "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "sched": (-(-R // 1024), d.E), "act": (R, d.I),
                 "act_lo": (R, d.I), "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I),
                 "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
                 "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E), "mx_dhu_c": (R, 2 * d.I),

@@ -115,6 +115,7 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   off = 0;
   L->status = take(mok::STATUS_BYTES);
   L->logits = take(T * E * 4);
+  L->sched = take(int64_t(mok::schedule_blocks((int)R)) * E * 4);
   L->act = take(R * I * 2);
   L->act_lo = take(R * I * 2);
   L->expert_out = take(R * H * 4);
@@ -264,8 +265,8 @@ mok_status mok_schedule(const mok_layer_desc* d, const void* x, const void* w_ro
   if (have_router) MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, d->T, d->H, d->E, logits, status, n_sm, st));
   MOK_LAUNCH("topk", st, mok::launch_topk(have_router ? logits : nullptr, router_bias, given_topk, d->T, d->E, d->k, d->router,
                             d->renorm, d->route_scale, topk_idx, gates, nullptr, status, st));
-  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, nullptr, d->T * d->k, d->E, counts, offsets, row_of, src_of, nullptr,
-                                nullptr, status, st));
+  MOK_LAUNCH("schedule", st, mok::launch_schedule_multi(topk_idx, nullptr, d->T * d->k, d->E, counts, offsets, row_of,
+                                                        src_of, nullptr, nullptr, at<int32_t>(ws, L.sched), status, st));
   return MOK_OK;
 }
 
@@ -315,8 +316,9 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   MOK_LAUNCH("topk", st, mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm, d->route_scale,
                             topk_idx, gates, at<float>(ctx, L.scores), status, st));
   // 3. schedule table
-  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of, src_of,
-                                tile_off, at<float>(ctx, L.gate_row), status, st));
+  MOK_LAUNCH("schedule", st, mok::launch_schedule_multi(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of,
+                                                        src_of, tile_off, at<float>(ctx, L.gate_row),
+                                                        at<int32_t>(ws, L.sched), status, st));
   if (d->ring_bytes == 0) {
     // 4. pull dispatch into expert-contiguous rows
     MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
@@ -521,8 +523,9 @@ mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const v
   MOK_LAUNCH("router_gemm", st, mok::launch_router_gemm(x, w_router, T, H, E, logits, status, n_sm, st));
   MOK_LAUNCH("topk", st, mok::launch_topk(logits, router_bias, given_topk, T, E, k, d->router, d->renorm,
                                           d->route_scale, topk_idx, gates, at<float>(ctx, L.scores), status, st));
-  MOK_LAUNCH("schedule", st, mok::launch_schedule(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets, row_of,
-                                                  src_of, tile_off, at<float>(ctx, L.gate_row), status, st));
+  MOK_LAUNCH("schedule", st, mok::launch_schedule_multi(topk_idx, gates, R, E, at<int32_t>(ctx, L.counts), offsets,
+                                                        row_of, src_of, tile_off, at<float>(ctx, L.gate_row),
+                                                        at<int32_t>(ws, L.sched), status, st));
   // each expert's rows padded to 32 in the E4M3 row space of the FP8 GEMMs
   MOK_LAUNCH("mx_block_offsets", st, mok::launch_mx_block_offsets(offsets, E, blk_off, st));
   // pull dispatch with the MXFP8 quantisation of each row along H (E4M3 bytes + scale blocks)

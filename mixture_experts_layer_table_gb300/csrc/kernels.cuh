@@ -12,6 +12,12 @@ cudaError_t launch_topk(const float* logits, const float* bias, const int32_t* g
 cudaError_t launch_schedule(const int32_t* topk_idx, const float* gates, int R, int E, int32_t* counts,
                             int32_t* offsets, int32_t* row_of, int32_t* src_of, int32_t* tile_off,
                             float* gate_row, int* status, cudaStream_t st);
+// The schedule table from ceil(R / 1024) CTAs in three launches (hist: i32 [schedule_blocks(R)][E]
+// scratch); bitwise the same table as launch_schedule.
+int schedule_blocks(int R);
+cudaError_t launch_schedule_multi(const int32_t* topk_idx, const float* gates, int R, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* row_of, int32_t* src_of, int32_t* tile_off,
+                                  float* gate_row, int32_t* hist, int* status, cudaStream_t st);
 cudaError_t launch_router_dlogits(const float* dg_part, int n_part, const int32_t* row_of,
                                   const int32_t* topk_idx, const float* gates, const float* scores, int T,
                                   int E, int k, int router, int renorm, float route_scale, float* dgates,

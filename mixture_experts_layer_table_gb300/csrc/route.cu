@@ -271,6 +271,164 @@ __global__ void __launch_bounds__(1024, 1)
   }
 }
 
+// ----------------------------------------------------------------------------- schedule (multi-CTA)
+// The same table from many CTAs, in three launches, for large T*k: the single-CTA kernel above
+// walks all assignments with one CTA and grows linearly with T*k (0.35 ms at 131,072
+// assignments).  Block b owns assignments [b * SCHED_CHUNK, (b + 1) * SCHED_CHUNK) and its warp
+// w the 128 of them starting at w * 128:
+//   1. schedule_hist_kernel: per-block histogram hist[b][e] (per-warp counts by warp match,
+//      summed over the warps: integer sums, so the order of the adds does not matter);
+//   2. schedule_scan_kernel (one CTA, thread e): counts, the exclusive scans over experts (rows
+//      and 128-row tiles), and in place of hist[b][e] the first row of block b's share of e;
+//   3. schedule_place_kernel: each block recounts its warps' shares, adds them to its block's
+//      starts, and every warp walks its assignments in order as in the single-CTA kernel.
+// Rows of an expert are in ascending assignment order (blocks, then warps, then lanes), the
+// unique stable order, so the table is bitwise the single-CTA kernel's.
+constexpr int SCHED_CHUNK = 1024;
+constexpr int SCHED_THREADS = 256;
+constexpr int SCHED_WARP_SPAN = SCHED_CHUNK / (SCHED_THREADS / 32);  // 128 assignments per warp
+
+// Per-warp histogram of this block's assignments into sh[warp][E] (zeroed here).
+__device__ __forceinline__ void sched_block_counts(const int32_t* __restrict__ topk_idx, int R, int E, int* sh,
+                                                   int* status, bool report) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < (SCHED_THREADS / 32) * E; i += SCHED_THREADS) sh[i] = 0;
+  __syncthreads();
+  const int a_begin = min(R, (int)blockIdx.x * SCHED_CHUNK + warp * SCHED_WARP_SPAN);
+  const int a_end = min(R, a_begin + SCHED_WARP_SPAN);
+  int* my = sh + warp * E;
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < a_end;
+    int e = valid ? topk_idx[a] : -1;
+    if (valid && (e < 0 || e >= E)) {
+      if (report) report_status(status, MOK_DEV_INVALID_ROUTING, SITE_SCHEDULE_INDEX);
+      e = 0;
+    }
+    const unsigned mask = __match_any_sync(0xffffffffu, e);
+    if (valid && lane == __ffs(mask) - 1) my[e] += __popc(mask);
+    __syncwarp();
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(SCHED_THREADS)
+    schedule_hist_kernel(const int32_t* __restrict__ topk_idx, int R, int E, int32_t* __restrict__ hist,
+                         int* status) {
+  extern __shared__ int sh[];  // [8][E]
+  sched_block_counts(topk_idx, R, E, sh, status, true);
+  for (int e = threadIdx.x; e < E; e += SCHED_THREADS) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < SCHED_THREADS / 32; ++w) t += sh[w * E + e];
+    hist[(size_t)blockIdx.x * E + e] = t;
+  }
+}
+
+__global__ void __launch_bounds__(1024, 1)
+    schedule_scan_kernel(int32_t* __restrict__ hist, int NB, int E, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
+  __shared__ int warp_tot[32], warp_tot2[32];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int e = threadIdx.x;
+  int tot = 0, tiles = 0;
+  if (e < E) {
+    for (int b = 0; b < NB; ++b) tot += hist[(size_t)b * E + e];
+    tiles = (tot + 127) / 128;
+  }
+  int inc = tot, inc2 = tiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    const int v2 = __shfl_up_sync(0xffffffffu, inc2, o);
+    if (lane >= o) {
+      inc += v;
+      inc2 += v2;
+    }
+  }
+  if (lane == 31) {
+    warp_tot[warp] = inc;
+    warp_tot2[warp] = inc2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int v = warp_tot[lane], v2 = warp_tot2[lane];
+    int x = v, x2 = v2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+      if (lane >= o) {
+        x += y;
+        x2 += y2;
+      }
+    }
+    warp_tot[lane] = x - v;  // exclusive over warps
+    warp_tot2[lane] = x2 - v2;
+  }
+  __syncthreads();
+  if (e < E) {
+    const int excl = warp_tot[warp] + inc - tot;
+    const int excl2 = warp_tot2[warp] + inc2 - tiles;
+    counts[e] = tot;
+    offsets[e] = excl;
+    if (tile_off) tile_off[e] = excl2;
+    if (e == E - 1) {
+      offsets[E] = excl + tot;
+      if (tile_off) tile_off[E] = excl2 + tiles;
+    }
+    int run = excl;
+    for (int b = 0; b < NB; ++b) {
+      const int c = hist[(size_t)b * E + e];
+      hist[(size_t)b * E + e] = run;
+      run += c;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(SCHED_THREADS)
+    schedule_place_kernel(const int32_t* __restrict__ topk_idx, const float* __restrict__ gates, int R, int E,
+                          const int32_t* __restrict__ starts, int32_t* __restrict__ row_of,
+                          int32_t* __restrict__ src_of, float* __restrict__ gate_row) {
+  extern __shared__ int sh[];  // [8][E]
+  sched_block_counts(topk_idx, R, E, sh, nullptr, false);
+  for (int e = threadIdx.x; e < E; e += SCHED_THREADS) {
+    int run = starts[(size_t)blockIdx.x * E + e];
+#pragma unroll
+    for (int w = 0; w < SCHED_THREADS / 32; ++w) {
+      const int c = sh[w * E + e];
+      sh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int a_begin = min(R, (int)blockIdx.x * SCHED_CHUNK + warp * SCHED_WARP_SPAN);
+  const int a_end = min(R, a_begin + SCHED_WARP_SPAN);
+  int* my = sh + warp * E;
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < a_end;
+    int ex = valid ? topk_idx[a] : -1;
+    if (valid && (ex < 0 || ex >= E)) ex = 0;
+    const unsigned mask = __match_any_sync(0xffffffffu, ex);
+    const int leader = __ffs(mask) - 1;
+    if (valid) {
+      const int pos = my[ex] + __popc(mask & lt_mask);
+      row_of[a] = pos;
+      src_of[pos] = a;
+      if (gate_row) gate_row[pos] = gates[a];
+    }
+    __syncwarp();
+    if (valid && lane == leader) my[ex] += __popc(mask);
+    __syncwarp();
+  }
+}
+
 // ----------------------------------------------------------------------------- router bwd
 // One warp per token.  dg_j = sum over the column-tile partials of row_of[t*k+j] (fixed
 // order); then the chain rule through the gates (renormalisation) and the scores (softmax
@@ -493,6 +651,25 @@ cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* o
   dim3 grid(E, (H + 2047) / 2048);
   router_wgrad_kernel<<<grid, 256, 0, st>>>(dl, reinterpret_cast<const __nv_bfloat16*>(x), offsets, src_of, T,
                                             H, E, k, sparse, dw);
+  return cudaGetLastError();
+}
+
+int schedule_blocks(int R) { return (R + SCHED_CHUNK - 1) / SCHED_CHUNK; }
+
+cudaError_t launch_schedule_multi(const int32_t* topk_idx, const float* gates, int R, int E, int32_t* counts,
+                                  int32_t* offsets, int32_t* row_of, int32_t* src_of, int32_t* tile_off,
+                                  float* gate_row, int32_t* hist, int* status, cudaStream_t st) {
+  const int NB = schedule_blocks(R);
+  const size_t smem = (size_t)(SCHED_THREADS / 32) * E * sizeof(int);
+  if (NB > 0) {
+    schedule_hist_kernel<<<NB, SCHED_THREADS, smem, st>>>(topk_idx, R, E, hist, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  schedule_scan_kernel<<<1, 1024, 0, st>>>(hist, NB, E, counts, offsets, tile_off);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || NB == 0) return err;
+  schedule_place_kernel<<<NB, SCHED_THREADS, smem, st>>>(topk_idx, gates, R, E, hist, row_of, src_of, gate_row);
   return cudaGetLastError();
 }
 

@@ -113,7 +113,7 @@ def _region_sizes(shp, ring_slots=0, minibatch=0):
     ctx = {"topk_idx": R * 4, "gates": R * 4, "scores": T * E * 4, "counts": E * 4, "offsets": (E + 1) * 4,
            "row_of": R * 4, "src_of": R * 4, "tile_off": (E + 1) * 4, "gate_row": R * 4, "x_g": R * H * 2,
            "hu": R * 2 * I * 4}
-    ws = {"status": 64 * 4, "logits": T * E * 4, "act": R * I * 2, "act_lo": R * I * 2, "expert_out": R * H * 4,
+    ws = {"status": 64 * 4, "logits": T * E * 4, "sched": -(-R // 1024) * E * 4, "act": R * I * 2, "act_lo": R * I * 2, "expert_out": R * H * 4,
           "dy_g": R * H * 2, "dhu": R * 2 * I * 2, "dhu_lo": R * 2 * I * 2, "gact": R * I * 2,
           "gact_lo": R * I * 2, "dx_g": R * H * 4, "dg_part": R * (I // 256) * 4, "dlogits": T * E * 4}
     if minibatch:
