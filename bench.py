@@ -612,9 +612,11 @@ def run_mok(args, rank, world, local_rank):
               "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mx_trace.items()},
               "fwd_bwd_ms": round(mxb_ms, 4), "fwd_bwd_tokens_per_s": round(whole_job_rate(T, world, mxb_ms), 1),
               "fwd_bwd_kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mxb_trace.items()},
-              "weights": "forward: E4M3 + E8M0 per 32 along K (11.3 GB); backward: W2 along H and W13 along "
-                         "2I, stored as exact bf16 values (22.5 GB); activations and gradients quantised "
-                         "along each GEMM's reduction"}
+              "weights": "forward: E4M3 + E8M0 per 32 along K (11.3 GB + 0.35 GB of scales); backward: W2 "
+                         "and W13 transposed, E4M3 + E8M0 along H and 2I (11.3 GB + 0.35 GB); GEMM1, GEMM2, dA' "
+                         "and dX_g on the FP8 tensor path (block-scaled MMAs), the weight gradients on the "
+                         "exact values of their row-quantised operands (bf16 tensor path); activations and "
+                         "gradients quantised along each GEMM's reduction"}
         del mx_layer, wq, wb
 
     # ---- the same weights at T=16384 (512 rows per expert): the forward GEMMs become

@@ -135,7 +135,7 @@ typedef struct {
   int64_t gact;       /* bf16 [T*k][I]  gate * a, operand of dW2, hi part (backward) */
   int64_t gact_lo;    /* bf16 [T*k][I]  lo part */
   int64_t dx_g;       /* f32 [T*k][H]   per-row input gradient (backward) */
-  int64_t dg_part;    /* f32 [T*k][I/256] partial gate gradients per GEMM column tile */
+  int64_t dg_part;    /* f32 [T*k][I/128] partial gate gradients per GEMM column tile (bf16: I/256 used) */
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
   /* ring forward only (-1 otherwise) */
   int64_t ring;       /* bf16 [slots * minibatch][H]  the token ring */
@@ -144,7 +144,6 @@ typedef struct {
   int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch */
   /* MXFP8 backward only (-1 otherwise): operands quantised along their GEMM's reduction
    * dimension, as exact bf16 values */
-  int64_t mx_dhu_c;   /* bf16 [T*k][2I] dh | du in 32-column blocks (A of dX_g = dHU W13[e]) */
   int64_t mx_dhu_r;   /* bf16 [T*k][2I] dh | du in 32-row blocks of each expert (dW13) */
   int64_t mx_xg_r;    /* bf16 [T*k][H]  dispatched x in 32-row blocks (dW13) */
   int64_t mx_do_r;    /* bf16 [T*k][H]  gate * dY rows in 32-row blocks (dW2) */
@@ -159,6 +158,11 @@ typedef struct {
   int64_t mx_xsf;     /* E8M0 [G][H/128][512]    their scale blocks */
   int64_t mx_aq;      /* E4M3 [RP][I]            a = silu(h) * u quantised along I */
   int64_t mx_asf;     /* E8M0 [G][I/128][512]    its scale blocks */
+  /* MXFP8 backward, same padded row space */
+  int64_t mx_dyq;     /* E4M3 [RP][H]            dispatched dY rows quantised along H */
+  int64_t mx_dysf;    /* E8M0 [G][H/128][512]    their scale blocks */
+  int64_t mx_dhuq;    /* E4M3 [RP][2I]           dh | du quantised along 2I */
+  int64_t mx_dhusf;   /* E8M0 [G][2I/128][512]   its scale blocks */
   int64_t ws_bytes;
 } mok_layout;
 
@@ -230,37 +234,45 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
  * Microscaling v1.0: E4M3 elements, one E8M0 scale per 32 consecutive elements along the GEMM's
  * reduction dimension, X = clamp(floor(log2 amax) - 8, -127, 127), elements RNE(v / 2^X)
  * saturated at +-448, scale byte X + 127.
- *   w13 [E][2I][H] bf16 -> w13_q [E][2I][H] E4M3 bytes, w13_scale [E][2I/128][H/128][512] bytes
+ *   w13 [E][2I][H] bf16 -> w13_q [E][2I][H] E4M3 bytes, w13_scale [E][I/64][H/128][512] bytes
  *   w2  [E][H][I]  bf16 -> w2_q  [E][H][I]  E4M3 bytes, w2_scale  [E][H/128][I/128][512]  bytes
  * Scales come in 512-byte blocks, one per 128-row tile and 128-element stage of the reduction
  * dimension, in the order the tensor cores read them from tensor memory: row 32 j + l (of the
- * tile) and 32-element block b (of the stage) at byte 16 l + 4 j + b.  All device pointers,
+ * tile) and 32-element block b (of the stage) at byte 16 l + 4 j + b.  The 128-row tiles of W13
+ * pair the gate rows 64 t .. 64 t + 63 (tile rows 0..63) with the up rows I + 64 t .. I + 64 t + 63
+ * (tile rows 64..127): the rows one CTA of the SwiGLU GEMM multiplies.  All device pointers,
  * 16-byte aligned. */
 mok_status mok_quantize_weights(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_q,
                                 void* w13_scale, void* w2_q, void* w2_scale, void* stream);
 
 /* Backward-direction MXFP8 weights for mok_moe_backward_mxfp8: each GEMM of the backward
- * quantises its operands along its own reduction dimension, so the weights are quantised again
- * along the other axis: W2[e] [H][I] along H (for dA' = dY_g W2[e]) and W13[e] [2I][H] along 2I
- * (for dX_g = dHU W13[e]), 32-row blocks, same rule as mok_quantize_weights.  The results are
- * stored as their exact bf16 values in the nn.Linear layouts (w13_b [E][2I][H], w2_b [E][H][I]):
- * the backward GEMMs read them with the bf16 kernels.  All device pointers, 16-byte aligned. */
-mok_status mok_quantize_weights_backward(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13_b,
-                                         void* w2_b, void* stream);
+ * quantises its operands along its own reduction dimension, so the weights are quantised again,
+ * along the other axis, and stored transposed so that the reduction dimension is contiguous:
+ *   w2  [E][H][I]  -> w2t_q  [E][I][H]  E4M3, quantised along H (for dA' = dY_g W2[e]),
+ *                     w2t_scale [E][I/128][H/128][512]
+ *   w13 [E][2I][H] -> w13t_q [E][H][2I] E4M3, quantised along 2I (for dX_g = dHU W13[e]),
+ *                     w13t_scale [E][H/128][2I/128][512]
+ * Scale blocks as for mok_quantize_weights (row 32 j + l of a 128-row tile and 32-element block b
+ * of a 128-element stage at byte 16 l + 4 j + b).  Same rule as mok_quantize_weights.  All device
+ * pointers, 16-byte aligned. */
+mok_status mok_quantize_weights_backward(const mok_layer_desc* desc, const void* w13, const void* w2, void* w13t_q,
+                                         void* w13t_scale, void* w2t_q, void* w2t_scale, void* stream);
 
 /* Layer backward with MXFP8 expert GEMMs (desc->precision must be MOK_MXFP8), after
  * mok_moe_forward_mxfp8 with the same ctx.  Every expert GEMM operand is quantised in 32-element
  * blocks along that GEMM's reduction dimension: dY_g (gathered, along H) and W2 along H for dA';
  * dh|du along 2I and W13 along 2I for dX_g; for the weight gradients both operands along the
  * expert's rows (gate * dY and a for dW2, dh|du and the dispatched x for dW13), in 32-row blocks
- * that start at the expert's first row.  The gate gradient is <dA', a> in the SwiGLU backward
- * epilogue, with dA' the quantised product; the router backward and the reverse dispatch are the
- * bf16 path's.  w13_b / w2_b come from mok_quantize_weights_backward.  Outputs and ws as for
- * mok_moe_backward (ws layout from an MXFP8 descriptor). */
+ * that start at the expert's first row.  dA' and dX_g run on the FP8 tensor path (block-scaled MMAs
+ * on the E4M3 weights of mok_quantize_weights_backward); the weight gradients multiply the exact
+ * values of their quantised operands on the bf16 tensor path.  The gate gradient is <dA', a> in the
+ * SwiGLU backward epilogue, with dA' the quantised product; the router backward and the reverse
+ * dispatch are the bf16 path's.  Outputs and ws as for mok_moe_backward (ws layout from an MXFP8
+ * descriptor). */
 mok_status mok_moe_backward_mxfp8(const mok_layer_desc* desc, const void* dy, const void* x, const void* w_router,
-                                  const void* w13_b, const void* w2_b, const void* ctx, size_t ctx_bytes, void* dx,
-                                  float* dw_router, void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,
-                                  void* stream);
+                                  const void* w13t_q, const void* w13t_scale, const void* w2t_q, const void* w2t_scale,
+                                  const void* ctx, size_t ctx_bytes, void* dx, float* dw_router, void* dw13, void* dw2,
+                                  float* dgates, void* ws, size_t ws_bytes, void* stream);
 
 /* Layer forward with MXFP8 expert GEMMs (desc->precision must be MOK_MXFP8, no ring).  As
  * mok_moe_forward, with the expert weights given as mok_quantize_weights output.  The MXFP8

@@ -38,8 +38,8 @@ class LayerDesc(ctypes.Structure):
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
                  "x_g", "hu", "ctx_bytes", "status", "logits", "sched", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
-                 "mx_dhu_c", "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "mx_xq", "mx_xsf", "mx_aq",
-                 "mx_asf", "ws_bytes"]
+                 "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "mx_xq", "mx_xsf", "mx_aq",
+                 "mx_asf", "mx_dyq", "mx_dysf", "mx_dhuq", "mx_dhusf", "ws_bytes"]
 FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
 FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
@@ -248,10 +248,11 @@ _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.
                "logits": torch.float32, "sched": torch.int32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
                "expert_out": torch.float32, "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "dhu_lo": torch.bfloat16,
                "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
-               "dg_part": torch.float32, "dlogits": torch.float32, "mx_dhu_c": torch.bfloat16,
+               "dg_part": torch.float32, "dlogits": torch.float32,
                "mx_dhu_r": torch.bfloat16, "mx_xg_r": torch.bfloat16, "mx_do_r": torch.bfloat16,
                "mx_a_r": torch.bfloat16, "mx_blk_off": torch.int32, "mx_xq": torch.uint8, "mx_xsf": torch.uint8,
-               "mx_aq": torch.uint8, "mx_asf": torch.uint8}
+               "mx_aq": torch.uint8, "mx_asf": torch.uint8, "mx_dyq": torch.uint8, "mx_dysf": torch.uint8,
+               "mx_dhuq": torch.uint8, "mx_dhusf": torch.uint8}
 
 
 def mx_rows_padded_bound(R: int, E: int) -> int:
@@ -281,11 +282,13 @@ class MoELayer:
                 "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "sched": (-(-R // 1024), d.E), "act": (R, d.I),
                 "act_lo": (R, d.I), "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I),
                 "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
-                "dx_g": (R, d.H), "dg_part": (R, d.I // 256), "dlogits": (d.T, d.E), "mx_dhu_c": (R, 2 * d.I),
-                "mx_dhu_r": (R, 2 * d.I), "mx_xg_r": (R, d.H), "mx_do_r": (R, d.H), "mx_a_r": (R, d.I),
+                "dx_g": (R, d.H), "dg_part": (R, d.I // 128), "dlogits": (d.T, d.E), "mx_dhu_r": (R, 2 * d.I), "mx_xg_r": (R, d.H), "mx_do_r": (R, d.H), "mx_a_r": (R, d.I),
                 "mx_blk_off": (d.E + 1,), "mx_xq": (mx_rows_padded_bound(R, d.E), d.H),
                 "mx_xsf": (mx_row_groups(R, d.E), d.H // 128, 512), "mx_aq": (mx_rows_padded_bound(R, d.E), d.I),
-                "mx_asf": (mx_row_groups(R, d.E), d.I // 128, 512)}[name]
+                "mx_asf": (mx_row_groups(R, d.E), d.I // 128, 512), "mx_dyq": (mx_rows_padded_bound(R, d.E), d.H),
+                "mx_dysf": (mx_row_groups(R, d.E), d.H // 128, 512),
+                "mx_dhuq": (mx_rows_padded_bound(R, d.E), 2 * d.I),
+                "mx_dhusf": (mx_row_groups(R, d.E), 2 * d.I // 128, 512)}[name]
 
     def view_split(self, name: str) -> torch.Tensor:
         """hi + lo of a split operand ("act", "dhu", "gact") as one float32 tensor."""
@@ -388,7 +391,7 @@ def quantize_weights(desc, w13, w2, stream=None):
     dev = w13.device
     E, H, I = desc.E, desc.H, desc.I
     out = {"w13_q": torch.empty((E, 2 * I, H), dtype=torch.uint8, device=dev),
-           "w13_scale": torch.empty((E, 2 * I // 128, H // 128, 512), dtype=torch.uint8, device=dev),
+           "w13_scale": torch.empty((E, I // 64, H // 128, 512), dtype=torch.uint8, device=dev),
            "w2_q": torch.empty((E, H, I), dtype=torch.uint8, device=dev),
            "w2_scale": torch.empty((E, H // 128, I // 128, 512), dtype=torch.uint8, device=dev)}
     fn = load().mok_quantize_weights
@@ -408,7 +411,7 @@ def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws
     _expect(router_bias, (E,), torch.float32, "router_bias", nullable=True)
     _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
     _expect(wq["w13_q"], (E, 2 * I, H), torch.uint8, "w13_q")
-    _expect(wq["w13_scale"], (E, 2 * I // 128, H // 128, 512), torch.uint8, "w13_scale")
+    _expect(wq["w13_scale"], (E, I // 64, H // 128, 512), torch.uint8, "w13_scale")
     _expect(wq["w2_q"], (E, H, I), torch.uint8, "w2_q")
     _expect(wq["w2_scale"], (E, H // 128, I // 128, 512), torch.uint8, "w2_scale")
     _expect(y, (desc.T, H), torch.bfloat16, "y")
@@ -424,14 +427,21 @@ def moe_forward_mxfp8(desc, x, w_router, router_bias, given_topk, wq, y, ctx, ws
 
 
 def quantize_weights_backward(desc, w13, w2, stream=None):
-    """mok_quantize_weights_backward: W13 quantised along 2I and W2 along H (32-row blocks), as
-    their exact bf16 values.  Returns {"w13_b", "w2_b"}."""
+    """mok_quantize_weights_backward: W2 transposed to [E][I][H] and quantised along H, W13 transposed to
+    [E][H][2I] and quantised along 2I (E4M3 + scale blocks).  Returns {"w13t_q", "w13t_scale", "w2t_q",
+    "w2t_scale"} as uint8 CUDA tensors."""
     _expect(w13, (desc.E, 2 * desc.I, desc.H), torch.bfloat16, "w13")
     _expect(w2, (desc.E, desc.H, desc.I), torch.bfloat16, "w2")
-    out = {"w13_b": torch.empty_like(w13), "w2_b": torch.empty_like(w2)}
-    fn = _mx_fn("mok_quantize_weights_backward", 5)
-    _check("mok_quantize_weights_backward", fn(ctypes.byref(desc), _ptr(w13), _ptr(w2), _ptr(out["w13_b"]),
-                                               _ptr(out["w2_b"]), _stream(stream)))
+    dev = w13.device
+    E, H, I = desc.E, desc.H, desc.I
+    out = {"w13t_q": torch.empty((E, H, 2 * I), dtype=torch.uint8, device=dev),
+           "w13t_scale": torch.empty((E, H // 128, 2 * I // 128, 512), dtype=torch.uint8, device=dev),
+           "w2t_q": torch.empty((E, I, H), dtype=torch.uint8, device=dev),
+           "w2t_scale": torch.empty((E, I // 128, H // 128, 512), dtype=torch.uint8, device=dev)}
+    fn = _mx_fn("mok_quantize_weights_backward", 7)
+    _check("mok_quantize_weights_backward", fn(ctypes.byref(desc), _ptr(w13), _ptr(w2), _ptr(out["w13t_q"]),
+                                               _ptr(out["w13t_scale"]), _ptr(out["w2t_q"]), _ptr(out["w2t_scale"]),
+                                               _stream(stream)))
     return out
 
 
@@ -441,8 +451,10 @@ def moe_backward_mxfp8(desc, dy, x, w_router, wb, ctx, dx, dw_router, dw13, dw2,
     wdt = torch.bfloat16 if (desc.flags & FLAG_WGRAD_BF16) else torch.float32
     _expect(x, (desc.T, H), torch.bfloat16, "x")
     _expect(w_router, (E, H), torch.bfloat16, "w_router")
-    _expect(wb["w13_b"], (E, 2 * I, H), torch.bfloat16, "w13_b")
-    _expect(wb["w2_b"], (E, H, I), torch.bfloat16, "w2_b")
+    _expect(wb["w13t_q"], (E, H, 2 * I), torch.uint8, "w13t_q")
+    _expect(wb["w13t_scale"], (E, H // 128, 2 * I // 128, 512), torch.uint8, "w13t_scale")
+    _expect(wb["w2t_q"], (E, I, H), torch.uint8, "w2t_q")
+    _expect(wb["w2t_scale"], (E, I // 128, H // 128, 512), torch.uint8, "w2t_scale")
     _expect(dy, (desc.T, H), torch.bfloat16, "dy")
     _expect(dx, (desc.T, H), torch.bfloat16, "dx")
     _expect(dw_router, (E, H), torch.float32, "dw_router")
@@ -451,9 +463,9 @@ def moe_backward_mxfp8(desc, dy, x, w_router, wb, ctx, dx, dw_router, dw13, dw2,
     _expect(dgates, (desc.T, desc.k), torch.float32, "dgates", nullable=True)
     fn = load().mok_moe_backward_mxfp8
     P, SZ = ctypes.c_void_p, ctypes.c_size_t
-    fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
+    fn.argtypes = [ctypes.POINTER(LayerDesc), P, P, P, P, P, P, P, P, SZ, P, P, P, P, P, P, SZ, P]
     fn.restype = ctypes.c_int32
     _check("mok_moe_backward_mxfp8", fn(
-        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(wb["w13_b"]), _ptr(wb["w2_b"]),
-        *_buf(ctx, "ctx"), _ptr(dx), _ptr(dw_router), _ptr(dw13), _ptr(dw2), _ptr(dgates), *_buf(ws, "ws"),
-        _stream(stream)))
+        ctypes.byref(desc), _ptr(dy), _ptr(x), _ptr(w_router), _ptr(wb["w13t_q"]), _ptr(wb["w13t_scale"]),
+        _ptr(wb["w2t_q"]), _ptr(wb["w2t_scale"]), *_buf(ctx, "ctx"), _ptr(dx), _ptr(dw_router), _ptr(dw13),
+        _ptr(dw2), _ptr(dgates), *_buf(ws, "ws"), _stream(stream)))

@@ -125,7 +125,7 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->gact = take(R * I * 2);
   L->gact_lo = take(R * I * 2);
   L->dx_g = take(R * H * 4);
-  L->dg_part = take(R * (I / 256) * 4);
+  L->dg_part = take(R * (I / 128) * 4);
   L->dlogits = take(T * E * 4);
   L->ring = L->mb_tables = L->mb_counters = -1;
   if (d->ring_bytes > 0) {
@@ -137,10 +137,9 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
     L->mb_tables = take((int64_t(2) * g.n_mb * (E + 1) + 2 * int64_t(g.n_mb) + 1) * 4);
     L->mb_counters = take(int64_t(2) * g.n_mb * 4);
   }
-  L->mx_dhu_c = L->mx_dhu_r = L->mx_xg_r = L->mx_do_r = L->mx_a_r = L->mx_blk_off = -1;
-  L->mx_xq = L->mx_xsf = L->mx_aq = L->mx_asf = -1;
+  L->mx_dhu_r = L->mx_xg_r = L->mx_do_r = L->mx_a_r = L->mx_blk_off = -1;
+  L->mx_xq = L->mx_xsf = L->mx_aq = L->mx_asf = L->mx_dyq = L->mx_dysf = L->mx_dhuq = L->mx_dhusf = -1;
   if (d->precision == MOK_MXFP8) {
-    L->mx_dhu_c = take(R * 2 * I * 2);
     L->mx_dhu_r = take(R * 2 * I * 2);
     L->mx_xg_r = take(R * H * 2);
     L->mx_do_r = take(R * H * 2);
@@ -151,6 +150,10 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
     L->mx_xsf = take(G * (H / mok::MX_BK) * mok::MX_SF_BLOCK);
     L->mx_aq = take(RP * I);
     L->mx_asf = take(G * (I / mok::MX_BK) * mok::MX_SF_BLOCK);
+    L->mx_dyq = take(RP * H);
+    L->mx_dysf = take(G * (H / mok::MX_BK) * mok::MX_SF_BLOCK);
+    L->mx_dhuq = take(RP * 2 * I);
+    L->mx_dhusf = take(G * (2 * I / mok::MX_BK) * mok::MX_SF_BLOCK);
   }
   L->ws_bytes = off;
   return MOK_OK;
@@ -376,38 +379,37 @@ mok_status mok_quantize_weights(const mok_layer_desc* d, const void* w13, const 
   const int n_sm = sm_count();
   if (n_sm <= 0) return MOK_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOK_LAUNCH("quantize_w13", st, mok::launch_quantize_weights(w13, w13_q, w13_scale, d->E, 2 * d->I, d->H, n_sm, st));
-  MOK_LAUNCH("quantize_w2", st, mok::launch_quantize_weights(w2, w2_q, w2_scale, d->E, d->H, d->I, n_sm, st));
+  MOK_LAUNCH("quantize_w13", st,
+             mok::launch_quantize_weights(w13, w13_q, w13_scale, d->E, 2 * d->I, d->H, d->I, n_sm, st));
+  MOK_LAUNCH("quantize_w2", st, mok::launch_quantize_weights(w2, w2_q, w2_scale, d->E, d->H, d->I, 0, n_sm, st));
   return MOK_OK;
 }
 
-mok_status mok_quantize_weights_backward(const mok_layer_desc* d, const void* w13, const void* w2, void* w13_b,
-                                         void* w2_b, void* stream) {
+mok_status mok_quantize_weights_backward(const mok_layer_desc* d, const void* w13, const void* w2, void* w13t_q,
+                                         void* w13t_scale, void* w2t_q, void* w2t_scale, void* stream) {
   mok_status s = check_desc(d);
   if (s != MOK_OK) return s;
-  const void* ptrs[] = {w13, w2, w13_b, w2_b};
+  const void* ptrs[] = {w13, w2, w13t_q, w13t_scale, w2t_q, w2t_scale};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return MOK_ERR_INVALID_ARG;
   const int n_sm = sm_count();
   if (n_sm <= 0) return MOK_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int H = d->H, I = d->I, E = d->E;
-  // W2[e] [H][I] along H: E segments of H rows; W13[e] [2I][H] along 2I: E segments of 2I rows
-  MOK_LAUNCH("quantize_w2_bwd", st, mok::launch_mx_quant_rows(0, E * H, I, E, H, nullptr, nullptr, w2, nullptr, nullptr,
-                                                              nullptr, nullptr, 1, w2_b, n_sm, st));
-  MOK_LAUNCH("quantize_w13_bwd", st, mok::launch_mx_quant_rows(0, E * 2 * I, H, E, 2 * I, nullptr, nullptr, w13, nullptr,
-                                                               nullptr, nullptr, nullptr, 1, w13_b, n_sm, st));
+  // W2[e] [H][I] -> [I][H] quantised along H; W13[e] [2I][H] -> [H][2I] quantised along 2I
+  MOK_LAUNCH("quantize_w2_bwd", st, mok::launch_quantize_transpose(w2, w2t_q, w2t_scale, E, H, I, n_sm, st));
+  MOK_LAUNCH("quantize_w13_bwd", st, mok::launch_quantize_transpose(w13, w13t_q, w13t_scale, E, 2 * I, H, n_sm, st));
   return MOK_OK;
 }
 
 mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const void* x, const void* w_router,
-                                  const void* w13_b, const void* w2_b, const void* ctx, size_t ctx_bytes, void* dx,
-                                  float* dw_router, void* dw13, void* dw2, float* dgates, void* ws, size_t ws_bytes,
-                                  void* stream) {
+                                  const void* w13t_q, const void* w13t_scale, const void* w2t_q, const void* w2t_scale,
+                                  const void* ctx, size_t ctx_bytes, void* dx, float* dw_router, void* dw13, void* dw2,
+                                  float* dgates, void* ws, size_t ws_bytes, void* stream) {
   mok_status s = check_desc(d);
   if (s != MOK_OK) return s;
   if (d->precision != MOK_MXFP8 || d->ring_bytes != 0) return MOK_ERR_UNSUPPORTED;
-  const void* ptrs[] = {dy, x, w_router, w13_b, w2_b, ctx, dx, dw_router, dw13, dw2, ws};
+  const void* ptrs[] = {dy, x, w_router, w13t_q, w13t_scale, w2t_q, w2t_scale, ctx, dx, dw_router, dw13, dw2, ws};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return MOK_ERR_INVALID_ARG;
   mok_layout L;
@@ -418,6 +420,7 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
   if (n_sm <= 0) return MOK_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
+  const int RP = (int)mok::mx_rows_padded_bound(R, E), G = (int)mok::mx_row_groups(R, E);
   int* status = at<int>(ws, L.status);
   // the work counters of this call start at zero (the status word keeps what the forward left)
   MOK_CUDA(cudaMemsetAsync(status + mok::STATUS_COUNTERS, 0, mok::STATUS_BYTES - 4 * mok::STATUS_COUNTERS, st));
@@ -425,36 +428,38 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
   const float* gates = at<float>(ctx, L.gates);
   const float* scores = at<float>(ctx, L.scores);
   const int32_t* offsets = at<int32_t>(ctx, L.offsets);
-  const int32_t* tile_off = at<int32_t>(ctx, L.tile_off);
   const int32_t* row_of = at<int32_t>(ctx, L.row_of);
   const int32_t* src_of = at<int32_t>(ctx, L.src_of);
   const float* gate_row = at<float>(ctx, L.gate_row);
   const float* hu = at<float>(ctx, L.hu);
-  void* dy_g = at<char>(ws, L.dy_g);
   void* dhu = at<char>(ws, L.dhu);
   void* dhu_lo = at<char>(ws, L.dhu_lo);
-  void* gact = at<char>(ws, L.gact);
-  void* gact_lo = at<char>(ws, L.gact_lo);
   float* dx_g = at<float>(ws, L.dx_g);
   float* dg_part = at<float>(ws, L.dg_part);
   float* dl = at<float>(ws, L.dlogits);
-  void* dhu_c = at<char>(ws, L.mx_dhu_c);
   void* dhu_r = at<char>(ws, L.mx_dhu_r);
   void* xg_r = at<char>(ws, L.mx_xg_r);
   void* do_r = at<char>(ws, L.mx_do_r);
   void* a_r = at<char>(ws, L.mx_a_r);
   int32_t* blk_off = at<int32_t>(ws, L.mx_blk_off);
+  void* dyq = at<char>(ws, L.mx_dyq);
+  void* dysf = at<char>(ws, L.mx_dysf);
+  void* dhuq = at<char>(ws, L.mx_dhuq);
+  void* dhusf = at<char>(ws, L.mx_dhusf);
   const int wgrad_f32 = (d->flags & MOK_FLAG_WGRAD_BF16) ? 0 : 1;
 
-  // 1. reverse combine, with dY_g quantised along H (the reduction dimension of dA')
-  MOK_LAUNCH("gather_dy_mx", st, mok::launch_gather_rows_mx(dy, src_of, k, R, H, dy_g, n_sm, st));
-  // 2. dA' = dY_g W2[e] with W2 quantised along H; SwiGLU backward epilogue: dh|du (hi/lo) and
-  //    the partial gate gradients <dA', a>
-  MOK_LAUNCH("dgrad_swiglu", st, mok::launch_dgrad_swiglu(dy_g, w2_b, R, H, I, E, offsets, tile_off, hu, gate_row, dhu,
-                                                          dhu_lo, gact, gact_lo, dg_part, status, n_sm, st));
-  // 3. the other GEMMs' operands, each quantised along its GEMM's reduction dimension
+  // 1. reverse combine: dY rows gathered into the padded row space, quantised along H (the reduction
+  //    dimension of dA') into E4M3 bytes and scale blocks
   MOK_LAUNCH("mx_block_offsets", st, mok::launch_mx_block_offsets(offsets, E, blk_off, st));
-  MOK_LAUNCH("mx_dhu_cols", st, mok::launch_mx_quant_cols(dhu, dhu_lo, R, 2 * I, dhu_c, n_sm, st));
+  MOK_LAUNCH("gather_dy_mx", st, mok::launch_gather_rows_mxf8(dy, src_of, topk_idx, offsets, blk_off, k, R, H, E, dyq,
+                                                              dysf, st));
+  // 2. dA' = dY_g W2[e] on the FP8 tensor path (W2 stored [I][H], quantised along H); SwiGLU backward
+  //    epilogue: dh | du (bf16 hi / lo, and E4M3 along 2I for dX_g) and the partial gate gradients
+  //    <dA', a> per 128 intermediate indices
+  MOK_LAUNCH("dgrad_swiglu_mx", st,
+             mok::launch_dgrad_swiglu_mxf8(dyq, dysf, w2t_q, w2t_scale, RP, G, R, H, I, E, offsets, blk_off, hu,
+                                           gate_row, dhu, dhu_lo, dhuq, dhusf, dg_part, status, n_sm, st));
+  // 3. the weight-gradient operands, each quantised along the expert's rows (its reduction)
   MOK_LAUNCH("mx_dhu_rows", st, mok::launch_mx_quant_rows(1, R, 2 * I, E, 0, offsets, blk_off, dhu, dhu_lo, nullptr,
                                                           nullptr, nullptr, k, dhu_r, n_sm, st));
   MOK_LAUNCH("mx_xg_rows", st, mok::launch_mx_quant_rows(3, R, H, E, 0, offsets, blk_off, x, nullptr, nullptr, nullptr,
@@ -463,10 +468,11 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                          gate_row, src_of, k, do_r, n_sm, st));
   MOK_LAUNCH("mx_a_rows", st, mok::launch_mx_quant_rows(2, R, I, E, 0, offsets, blk_off, nullptr, nullptr, hu, nullptr,
                                                         nullptr, k, a_r, n_sm, st));
-  // 4. dX_g = dHU W13[e], W13 quantised along 2I
-  MOK_LAUNCH("dgrad_x", st, mok::launch_dgrad_x(dhu_c, nullptr, w13_b, R, H, I, E, offsets, tile_off, dx_g, status,
-                                                n_sm, gemm_variant(d, DGRAD_X), st));
-  // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H]
+  // 4. dX_g = dHU W13[e] on the FP8 tensor path (W13 stored [H][2I], quantised along 2I)
+  MOK_LAUNCH("dgrad_x_mx", st, mok::launch_dgrad_x_mxf8(dhuq, dhusf, w13t_q, w13t_scale, RP, G, R, H, I, E, offsets,
+                                                        blk_off, dx_g, status, n_sm, st));
+  // 5. dW2[e] = (g dY)^T a stored as [H][I]; dW13[e] = dHU^T x_g stored as [2I][H] (exact products of the
+  //    quantised values on the bf16 kernels)
   MOK_LAUNCH("wgrad_w2", st, mok::launch_wgrad(a_r, nullptr, I, do_r, nullptr, H, R, E, offsets, dw2, wgrad_f32, status,
                                                status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W2, wgrad_pairs(d),
                                                n_sm, st));
@@ -475,7 +481,7 @@ mok_status mok_moe_backward_mxfp8(const mok_layer_desc* d, const void* dy, const
                                                 status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13, wgrad_pairs(d),
                                                 n_sm, st));
   // 6-8. gate and router gradients, router weight gradient, reverse dispatch (as in bf16)
-  MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k,
+  MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 128, row_of, topk_idx, gates, scores, T, E, k,
                                                               d->router, d->renorm, d->route_scale, dgates, dl, st));
   MOK_LAUNCH("router_wgrad", st, mok::launch_router_wgrad(dl, x, offsets, src_of, T, H, E, k,
                                                           d->router == MOK_ROUTER_SIGMOID ? 1 : 0, dw_router, st));
@@ -532,9 +538,9 @@ mok_status mok_moe_forward_mxfp8(const mok_layer_desc* d, const void* x, const v
   MOK_LAUNCH("gather_x_mx", st, mok::launch_gather_rows_mxf8(x, src_of, topk_idx, offsets, blk_off, k, R, H, E, xq,
                                                              xsf, st));
   // GEMM1 on the FP8 tensor path, SwiGLU, a quantised along I (E4M3 bytes + scale blocks)
-  MOK_LAUNCH("gemm1_swiglu_mx", st, mok::launch_gemm1_swiglu_mxf8(xq, xsf, w13_q, w13_scale, RP, G, H, I, E, offsets,
+  MOK_LAUNCH("gemm1_swiglu_mx", st, mok::launch_gemm1_swiglu_mxf8(xq, xsf, w13_q, w13_scale, RP, G, R, H, I, E, offsets,
                                                                   blk_off, hu, aq, asf, status, n_sm, st));
-  MOK_LAUNCH("gemm2_mx", st, mok::launch_gemm2_mxf8(aq, asf, w2_q, w2_scale, RP, G, H, I, E, offsets, blk_off, o,
+  MOK_LAUNCH("gemm2_mx", st, mok::launch_gemm2_mxf8(aq, asf, w2_q, w2_scale, RP, G, R, H, I, E, offsets, blk_off, o,
                                                     status, n_sm, st));
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;

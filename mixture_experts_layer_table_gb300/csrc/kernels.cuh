@@ -87,7 +87,10 @@ struct RingArgs {
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, cudaStream_t st);
 // MXFP8 weights (mx.cu)
-cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm, cudaStream_t st);
+// w [E][N][K] bf16 -> q [E][N][K] E4M3 and 512-byte scale blocks; gate_up_I > 0 (W13, N = 2I):
+// the blocks of 128 rows pair 64 gate rows with the 64 up rows of the same intermediate indices.
+cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int gate_up_I, int n_sm,
+                                    cudaStream_t st);
 // MXFP8 backward operands (mx.cu).  src of launch_mx_quant_rows: 0 plain rows (in0, fixed
 // segments of seg_len rows), 1 hi + lo rows, 2 a = silu(h) u from h | u, 3 token rows gathered by
 // src_of, 4 gate_row * gathered token rows; segments from offsets / blk_off unless seg_len > 0.
@@ -106,11 +109,24 @@ cudaError_t launch_gather_rows_mxf8(const void* x, const int32_t* src_of, const 
                                     const int32_t* offsets, const int32_t* blk_off, int k, int R, int H, int E,
                                     void* xq, void* xsf, cudaStream_t st);
 cudaError_t launch_gemm1_swiglu_mxf8(const void* xq, const void* xsf, const void* w13_q, const void* w13_sf, int RP,
-                                     int G, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off,
+                                     int G, int R, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off,
                                      float* hu, void* aq, void* asf, int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_gemm2_mxf8(const void* aq, const void* asf, const void* w2_q, const void* w2_sf, int RP, int G,
-                              int H, int I, int E, const int32_t* offsets, const int32_t* blk_off, float* o,
+                              int R, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off, float* o,
                               int* status, int n_sm, cudaStream_t st);
+// MXFP8 backward on the FP8 tensor path: dA' = dY_g W2[e] with the SwiGLU backward (dh | du as bf16
+// hi / lo and as E4M3 along 2I, partial gate gradients per 128 intermediate indices), and
+// dX_g = dHU W13[e]; the weights transposed and quantised along their reduction (launch_quantize_transpose).
+cudaError_t launch_dgrad_swiglu_mxf8(const void* dyq, const void* dysf, const void* w2t_q, const void* w2t_sf, int RP,
+                                     int G, int R, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off,
+                                     const float* hu, const float* gate_row, void* dhu_hi, void* dhu_lo, void* dhuq,
+                                     void* dhusf, float* dg_part, int* status, int n_sm, cudaStream_t st);
+cudaError_t launch_dgrad_x_mxf8(const void* dhuq, const void* dhusf, const void* w13t_q, const void* w13t_sf, int RP,
+                                int G, int R, int H, int I, int E, const int32_t* offsets, const int32_t* blk_off,
+                                float* dx_g, int* status, int n_sm, cudaStream_t st);
+// w [E][N][K] bf16 -> wt [E][K][N] E4M3 quantised in 32-blocks along N, scales [E][K/128][N/128][512].
+cudaError_t launch_quantize_transpose(const void* w, void* wt_q, void* wt_s, int E, int N, int K, int n_sm,
+                                      cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

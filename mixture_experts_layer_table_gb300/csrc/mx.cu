@@ -15,10 +15,12 @@ namespace mok {
 
 // w [E][N][K] bf16 -> q [E][N][K] E4M3 bytes, s [E][N/128][K/128][512] E8M0 bytes: one 512-byte
 // block per 128-row tile and 128-element K stage, in the order tcgen05.cp puts it into TMEM
-// (mx_tiles.h).  One thread per (e, k-block, n), n fastest.
+// (mx_tiles.h).  With gate_up_I > 0 (W13, N = 2I) tile t holds the gate rows 64 t .. 64 t + 63 and
+// the up rows I + 64 t .. I + 64 t + 63 (the rows one CTA of the SwiGLU GEMM multiplies).  One
+// thread per (e, k-block, n), n fastest.
 __global__ void __launch_bounds__(256)
     quantize_weights_kernel(const __nv_bfloat16* __restrict__ w, uint8_t* __restrict__ q, uint8_t* __restrict__ s,
-                            int E, int N, int K) {
+                            int E, int N, int K, int gate_up_I) {
   const int KB = K / 32;
   const long long total = (long long)E * KB * N;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -46,7 +48,13 @@ __global__ void __launch_bounds__(256)
     uint4* dst = reinterpret_cast<uint4*>(q + base);
     dst[0] = *reinterpret_cast<uint4*>(bytes);
     dst[1] = *reinterpret_cast<uint4*>(bytes + 16);
-    s[(((size_t)e * (N / 128) + n / 128) * (K / 128) + kb / 4) * MX_SF_BLOCK + mx_sf_byte(n & 127, kb & 3)] =
+    int tile = n >> 7, local = n & 127;
+    if (gate_up_I > 0) {
+      const int half = n / gate_up_I, ii = n - half * gate_up_I;
+      tile = ii >> 6;
+      local = half * 64 + (ii & 63);
+    }
+    s[(((size_t)e * (N / 128) + tile) * (K / 128) + kb / 4) * MX_SF_BLOCK + mx_sf_byte(local, kb & 3)] =
         (uint8_t)(X + 127);
   }
 }
@@ -101,6 +109,36 @@ __global__ void __launch_bounds__(GATHER_MX_THREADS)
                      : "memory");
       }
     }
+  }
+}
+
+// Backward-direction MXFP8 weights: w [E][N][K] bf16 -> wt [E][K][N] E4M3, each row of wt (a column
+// of w) quantised in 32-element blocks along N, scales s [E][K/128][N/128][512] (the layout of
+// quantize_weights_kernel for the transposed matrix).  One thread per (e, k, 32-block of N), k
+// fastest: a warp reads 32 consecutive k of each of its 32 rows (64-byte segments) and writes 32
+// bytes of its own row of wt.
+__global__ void __launch_bounds__(256)
+    quantize_transpose_kernel(const __nv_bfloat16* __restrict__ w, uint8_t* __restrict__ wt, uint8_t* __restrict__ s,
+                              int E, int N, int K) {
+  const int NB = N / 32;
+  const long long total = (long long)E * NB * K;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(idx % K);
+    const long long rest = idx / K;
+    const int nb = (int)(rest % NB);
+    const int e = (int)(rest / NB);
+    const __nv_bfloat16* src = w + ((size_t)e * N + (size_t)nb * 32) * K + k;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __bfloat162float(src[(size_t)j * K]);
+    __align__(16) uint8_t bytes[32];
+    const int X = mx_quantize32(v, bytes);
+    uint4* dst = reinterpret_cast<uint4*>(wt + ((size_t)e * K + k) * N + (size_t)nb * 32);
+    dst[0] = *reinterpret_cast<uint4*>(bytes);
+    dst[1] = *reinterpret_cast<uint4*>(bytes + 16);
+    s[(((size_t)e * (K / 128) + k / 128) * (N / 128) + nb / 4) * MX_SF_BLOCK + mx_sf_byte(k & 127, nb & 3)] =
+        (uint8_t)(X + 127);
   }
 }
 
@@ -435,14 +473,14 @@ cudaError_t launch_mx_quant_cols(const void* hi, const void* lo, long long R, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int n_sm,
+cudaError_t launch_quantize_weights(const void* w, void* q, void* s, int E, int N, int K, int gate_up_I, int n_sm,
                                     cudaStream_t st) {
   const long long total = (long long)E * (K / 32) * N;
   long long blocks = (total + 255) / 256;
   if (blocks > (long long)n_sm * 64) blocks = (long long)n_sm * 64;
   quantize_weights_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w),
                                                        reinterpret_cast<uint8_t*>(q), reinterpret_cast<uint8_t*>(s),
-                                                       E, N, K);
+                                                       E, N, K, gate_up_I);
   return cudaGetLastError();
 }
 
@@ -452,6 +490,18 @@ cudaError_t launch_gather_rows_mx(const void* src, const int32_t* src_of, int k,
   (void)n_sm;
   gather_rows_mx_kernel<<<R, GATHER_MX_THREADS, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src), src_of, k, H / 8,
                                                          reinterpret_cast<__nv_bfloat16*>(dst));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_transpose(const void* w, void* wt_q, void* wt_s, int E, int N, int K, int n_sm,
+                                      cudaStream_t st) {
+  const long long total = (long long)E * (N / 32) * K;
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)n_sm * 64) blocks = (long long)n_sm * 64;
+  if (blocks <= 0) return cudaSuccess;
+  quantize_transpose_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w),
+                                                         reinterpret_cast<uint8_t*>(wt_q), reinterpret_cast<uint8_t*>(wt_s),
+                                                         E, N, K);
   return cudaGetLastError();
 }
 

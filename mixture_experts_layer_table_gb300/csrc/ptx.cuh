@@ -407,6 +407,25 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// CTA-pair forms (issued by one thread of the even CTA): tcgen05.cp copies each CTA's own shared
+// memory block into its own TMEM at the same address; the MMA's M is split across the pair (each
+// CTA's TMEM holds its 128 rows), A's scales come from each CTA's own TMEM, and each CTA's TMEM must
+// hold the scales of all N columns of B.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B (both K-major), E8M0 scales, f32
 // accumulate, M x N tile; the scale byte of each operand's TMEM word is sf_id (0..3): the K-block
 // of 32 inside a 128-byte K stage.

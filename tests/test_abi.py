@@ -66,8 +66,11 @@ def test_mxfp8_layout_has_the_backward_operands(lib):
     bf = mok.get_layout(mok.desc_from_shape(W.DSV3))
     mx = mok.get_layout(mok.desc_from_shape(W.DSV3_MXFP8))
     R, H, I, E = W.DSV3.T * W.DSV3.k, W.DSV3.H, W.DSV3.I, W.DSV3.E
-    sizes = {"mx_dhu_c": R * 2 * I * 2, "mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2, "mx_do_r": R * H * 2,
-             "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4}
+    RP = 32 * (-(-R // 32) + E)
+    G = RP // 32 + 4
+    sizes = {"mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2, "mx_do_r": R * H * 2,
+             "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4, "mx_dyq": RP * H, "mx_dysf": G * (H // 128) * 512,
+             "mx_dhuq": RP * 2 * I, "mx_dhusf": G * (2 * I // 128) * 512}
     ends = []
     for name, nbytes in sizes.items():
         assert bf[name] == -1, name
@@ -115,18 +118,19 @@ def _region_sizes(shp, ring_slots=0, minibatch=0):
            "hu": R * 2 * I * 4}
     ws = {"status": 64 * 4, "logits": T * E * 4, "sched": -(-R // 1024) * E * 4, "act": R * I * 2, "act_lo": R * I * 2, "expert_out": R * H * 4,
           "dy_g": R * H * 2, "dhu": R * 2 * I * 2, "dhu_lo": R * 2 * I * 2, "gact": R * I * 2,
-          "gact_lo": R * I * 2, "dx_g": R * H * 4, "dg_part": R * (I // 256) * 4, "dlogits": T * E * 4}
+          "gact_lo": R * I * 2, "dx_g": R * H * 4, "dg_part": R * (I // 128) * 4, "dlogits": T * E * 4}
     if minibatch:
         n_mb = -(-R // minibatch)
         ws.update({"ring": ring_slots * minibatch * H * 2,
                    "mb_tables": (2 * n_mb * (E + 1) + n_mb + (n_mb + 1)) * 4, "mb_counters": 2 * n_mb * 4})
     if shp.mxfp8:
-        ws.update({"mx_dhu_c": R * 2 * I * 2, "mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
+        ws.update({"mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
                    "mx_do_r": R * H * 2, "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4})
         RP = 32 * (-(-R // 32) + E)       # padded rows: every expert's rows rounded up to 32
         G = RP // 32 + 4                  # row groups of the scale blocks
         ws.update({"mx_xq": RP * H, "mx_xsf": G * (H // 128) * 512, "mx_aq": RP * I,
-                   "mx_asf": G * (I // 128) * 512})
+                   "mx_asf": G * (I // 128) * 512, "mx_dyq": RP * H, "mx_dysf": G * (H // 128) * 512,
+                   "mx_dhuq": RP * 2 * I, "mx_dhusf": G * (2 * I // 128) * 512})
     return ctx, ws
 
 
@@ -201,7 +205,7 @@ def test_entry_points_reject_bad_arguments_before_any_device_work(lib):
     fwd_mx = lib.mok_moe_forward_mxfp8
     fwd_mx.argtypes = [D] + [P] * 9 + [P, SZ, P, SZ, P]
     bwd_mx = lib.mok_moe_backward_mxfp8
-    bwd_mx.argtypes = [D] + [P] * 6 + [SZ] + [P] * 6 + [SZ, P]
+    bwd_mx.argtypes = [D] + [P] * 8 + [SZ] + [P] * 6 + [SZ, P]
     for f in (fwd_mx, bwd_mx):
         f.restype = ctypes.c_int32
     bf = mok.desc_from_shape(W.TINY)
@@ -229,9 +233,9 @@ def test_entry_points_reject_bad_arguments_before_any_device_work(lib):
     assert fwd_mx(ctypes.byref(bf), *a[:9], a[9], m_ctx, a[10], m_ws, None) == 2
     assert fwd_mx(ctypes.byref(mx), *a[:9], a[9], m_ctx, a[10], m_ws - 1, None) == 3
     assert fwd_mx(ctypes.byref(mx), None, *a[1:9], a[9], m_ctx, a[10], m_ws - 1, None) == 1
-    assert bwd_mx(ctypes.byref(bf), *a[:6], m_ctx, *a[6:12], m_ws, None) == 2
-    assert bwd_mx(ctypes.byref(mx), *a[:6], m_ctx - 1, *a[6:12], m_ws, None) == 3
-    assert bwd_mx(ctypes.byref(mx), *a[:5], P(0x100004), m_ctx - 1, *a[6:12], m_ws, None) == 1
+    assert bwd_mx(ctypes.byref(bf), *a[:8], m_ctx, *a[8:14], m_ws, None) == 2
+    assert bwd_mx(ctypes.byref(mx), *a[:8], m_ctx - 1, *a[8:14], m_ws, None) == 3
+    assert bwd_mx(ctypes.byref(mx), *a[:7], P(0x100004), m_ctx - 1, *a[8:14], m_ws, None) == 1
     # schedule: ws one byte short, and a missing output
     sch = lambda topk, ws_n: lib.mok_schedule(ctypes.byref(bf), a[0], a[1], None, None, topk, a[2], a[3], a[4], a[5],
                                               a[6], a[7], ws_n, None)

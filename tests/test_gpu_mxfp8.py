@@ -37,14 +37,19 @@ def _sf_byte(r, kb):
     return (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
 
 
-def _decode_w(qb, sb, N, K):
+def _decode_w(qb, sb, N, K, gate_up_I=0):
     """E4M3 bytes [E, N, K] and scale blocks [E, N/128, K/128, 512] -> (float64 values [E, N, K],
-    exponents [E, N, K/32])."""
+    exponents [E, N, K/32]).  gate_up_I > 0 (W13, N = 2I): block t holds the gate rows 64 t .. +63
+    (block rows 0..63) and the up rows I + 64 t .. +63 (block rows 64..127)."""
     vals = qb.view(torch.float8_e4m3fn).double().cpu().numpy()
-    blocks = sb.cpu().numpy().astype(np.int64)
+    blocks = sb.cpu().numpy().astype(np.int64).reshape(qb.shape[0], N // 128, K // 128, 512)
     n = np.arange(N)[:, None]
     kb = np.arange(K // 32)[None, :]
-    X = blocks[:, n // 128, kb // 4, _sf_byte(n, kb)] - 127               # [E, N, K/32]
+    if gate_up_I:
+        tile, local = (n % gate_up_I) // 64, (n // gate_up_I) * 64 + n % 64
+    else:
+        tile, local = n // 128, n % 128
+    X = blocks[:, tile, kb // 4, _sf_byte(local, kb)] - 127               # [E, N, K/32]
     return np.ldexp(vals, np.repeat(X, 32, axis=-1)), X
 
 
@@ -94,8 +99,8 @@ def test_quantized_weights_bit_exact():
     inp = W.make_inputs(MID, seed=0, device="cpu")
     f64 = inputs_f64(inp)
     _, _, wq = _run_mx(MID, inp)
-    for name, w, N, K in (("w13", f64["w13"], 2 * MID.I, MID.H), ("w2", f64["w2"], MID.H, MID.I)):
-        got, X_got = _decode_w(wq[name + "_q"], wq[name + "_scale"], N, K)
+    for name, w, N, K, gu in (("w13", f64["w13"], 2 * MID.I, MID.H, MID.I), ("w2", f64["w2"], MID.H, MID.I, 0)):
+        got, X_got = _decode_w(wq[name + "_q"], wq[name + "_scale"], N, K, gu)
         for e in range(MID.E):
             want = q(w[e], 1)
             bad = np.argwhere(got[e] != want)
@@ -179,17 +184,20 @@ def test_mx_forward_full_size_sampled_and_deterministic():
 # ----------------------------------------------------------------------------- backward
 
 def test_backward_weights_bit_exact():
-    """W2 quantised along H and W13 along 2I (32-row blocks of each expert's matrix)."""
+    """W2 quantised along H and W13 along 2I (32-row blocks of each expert's matrix), stored transposed
+    ([E][I][H] and [E][H][2I]) as E4M3 bytes and scale blocks."""
     inp = W.make_inputs(MID, seed=0, device="cpu")
     f64 = inputs_f64(inp)
     desc = mok.desc_from_shape(MID)
     wb = mok.quantize_weights_backward(desc, inp["w13"].cuda(), inp["w2"].cuda())
     torch.cuda.synchronize()
-    for name, w in (("w13", f64["w13"]), ("w2", f64["w2"])):
-        got = to_f64(wb[name + "_b"])
+    for name, w, N, K in (("w13", f64["w13"], MID.H, 2 * MID.I), ("w2", f64["w2"], MID.I, MID.H)):
+        got, X_got = _decode_w(wb[name + "t_q"], wb[name + "t_scale"], N, K)
         for e in range(MID.E):
-            want = q(w[e], 0)
+            want = q(w[e], 0).T
             assert np.array_equal(got[e], want), (name, e, int((got[e] != want).sum()))
+            _, X = O.mx_quantize(w[e], 0)
+            assert np.array_equal(X_got[e], X.T), (name, e)
 
 
 def _mx_fwd_bwd(shape, seed=0, given=None):
