@@ -633,6 +633,18 @@ def run_mok(args, rank, world, local_rank):
               "grouped_gemm": tb_grouped,
               "kernels": {n: v for n, v in tb_kernels.items()}}
         del tb_layer
+        if not args.no_fp16_w2:
+            # the same forward on an fp16 copy of W2 (converted once, outside the timing): a kept as
+            # one fp16 value, one GEMM2 MMA per K step instead of the bf16 hi / lo pair
+            w2_f16 = mok.convert_f16(w2)
+            f_ms, f_kernels, f_grouped, f_layer, _ = tensor_bound_forward(
+                shp_tb, x_tb, wr, w13, w2_f16, args.steps, args.warmup, GEMM_FLAGS[args.gemm] | N.FLAG_W2_F16)
+            tb["fp16_w2"] = {"fwd_ms": round(f_ms, 4), "tokens_per_s": round(whole_job_rate(shp_tb.T, world, f_ms), 1),
+                             "grouped_gemm": f_grouped, "kernels": f_kernels,
+                             "what": "MOK_FLAG_W2_F16: W2 as IEEE fp16 (exact for these bf16 weights), a as one "
+                                     "fp16 value (11 significant bits) instead of a bf16 hi / lo pair"}
+            del f_layer, w2_f16
+            torch.cuda.empty_cache()
         if not args.no_ring_sweep:
             tb["ring_sweep"] = ring_sweep(shp_tb, x_tb, wr, w13, w2, y_tb.clone(), args.steps, args.warmup)
         del x_tb, y_tb
@@ -830,6 +842,8 @@ def main():
     ap.add_argument("--no-cpu-full", action="store_true",
                     help="skip the full-size oracle timings (DSV3 forward, skewed DSV3 forward + backward; ~1 min)")
     ap.add_argument("--no-wgrad-bf16", action="store_true", help="skip the step with bf16 weight gradients")
+    ap.add_argument("--no-fp16-w2", action="store_true",
+                    help="skip the T=16384 forward on an fp16 copy of W2 (MOK_FLAG_W2_F16)")
     ap.add_argument("--no-ring-sweep", action="store_true",
                     help="skip the ring-forward minibatch sweep at T=16384 in the default line")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")

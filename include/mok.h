@@ -87,11 +87,19 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                (256 x 256 tiles) by default and on single CTAs (128 x 128) with either
  *                flag.  Results are bitwise the same in every case.  Setting both flags
  *                is an invalid argument.
+ *                MOK_FLAG_W2_F16: mok_moe_forward reads w2 as IEEE fp16 [E][H][I] (the
+ *                layer's bf16 W2 converted once with mok_convert_f16, exact for weights of
+ *                magnitude 2^-14 and above), keeps a = silu(h) * u as one fp16 value (11
+ *                significant bits) instead of a bf16 hi / lo pair, and runs GEMM2 on fp16
+ *                operands, one MMA per K step instead of two.  Default GEMM kernels and no
+ *                ring only (else MOK_ERR_UNSUPPORTED); mok_moe_backward ignores the flag and
+ *                takes w2 in bf16 (the backward does not read a).
  *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1
 #define MOK_FLAG_GEMM_PAIR 2
 #define MOK_FLAG_GEMM_SINGLE 4
+#define MOK_FLAG_W2_F16 8
 typedef struct {
   int32_t T, H, I, E, k;
   int32_t router;
@@ -228,6 +236,12 @@ mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void
                            const float* router_bias, const int32_t* given_topk, const void* w13,
                            const void* w2, void* y, void* ctx, size_t ctx_bytes, void* ws,
                            size_t ws_bytes, void* stream);
+
+/* IEEE fp16 copy of a bf16 tensor: dst [n] fp16 = src [n] bf16 rounded to nearest even (exact
+ * for magnitudes 2^-14 .. 65504; smaller values become fp16 subnormals, larger ones infinities).
+ * For the fp16 W2 of MOK_FLAG_W2_F16 (no counterpart on the pages: a precision choice of this
+ * library for the tensor-bound GEMM2).  Device pointers, 16-byte aligned; async on `stream`. */
+mok_status mok_convert_f16(const void* src, void* dst, int64_t n, void* stream);
 
 /* MXFP8 weights for mok_moe_forward_mxfp8.  MXFP8 is one of the two precisions of the pages'
  * kernel ("Mixture-of-Kittens (MoK)", sd114.wiki, benchmark section); the format is read as OCP

@@ -43,6 +43,7 @@ LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "
 FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
 FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
+FLAG_W2_F16 = 8        # forward: w2 is fp16 (convert_f16), a kept as fp16, GEMM2 on fp16 operands
 # neither: GEMM1, GEMM2 and dX_g on the narrow-segment pair kernel (expert rows as the MMA's N)
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]
@@ -163,13 +164,13 @@ def _expect(t, shape, dtype, name, nullable=False):
         raise ValueError(f"{name} must be a CUDA tensor")
 
 
-def _check_layer_inputs(desc, x, w_router, router_bias, w13, w2):
+def _check_layer_inputs(desc, x, w_router, router_bias, w13, w2, w2_f16=False):
     bf = torch.bfloat16
     _expect(x, (desc.T, desc.H), bf, "x")
     _expect(w_router, (desc.E, desc.H), bf, "w_router")
     _expect(router_bias, (desc.E,), torch.float32, "router_bias", nullable=True)
     _expect(w13, (desc.E, 2 * desc.I, desc.H), bf, "w13")
-    _expect(w2, (desc.E, desc.H, desc.I), bf, "w2")
+    _expect(w2, (desc.E, desc.H, desc.I), torch.float16 if w2_f16 else bf, "w2")
 
 
 def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts, offsets, row_of, src_of, ws,
@@ -193,7 +194,7 @@ def schedule(desc, x, w_router, router_bias, given_topk, topk_idx, gates, counts
 
 
 def moe_forward(desc, x, w_router, router_bias, given_topk, w13, w2, y, ctx, ws, stream=None):
-    _check_layer_inputs(desc, x, w_router, router_bias, w13, w2)
+    _check_layer_inputs(desc, x, w_router, router_bias, w13, w2, w2_f16=bool(desc.flags & FLAG_W2_F16))
     _expect(given_topk, (desc.T, desc.k), torch.int32, "given_topk", nullable=True)
     _expect(y, (desc.T, desc.H), torch.bfloat16, "y")
     _check("mok_moe_forward", load().mok_moe_forward(
@@ -381,6 +382,19 @@ def _mx_fn(name, nargs):
         fn.argtypes = [ctypes.POINTER(LayerDesc)] + [ctypes.c_void_p] * nargs
         fn.restype = ctypes.c_int32
     return fn
+
+
+def convert_f16(src, stream=None):
+    """mok_convert_f16: an fp16 copy of a bf16 CUDA tensor (round to nearest even), e.g. W2 for
+    MOK_FLAG_W2_F16."""
+    if src is None or src.device.type != "cuda" or src.dtype != torch.bfloat16:
+        raise ValueError("convert_f16 takes a bf16 CUDA tensor")
+    out = torch.empty(src.shape, dtype=torch.float16, device=src.device)
+    fn = load().mok_convert_f16
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
+    _check("mok_convert_f16", fn(_ptr(src), _ptr(out), src.numel(), _stream(stream)))
+    return out
 
 
 def quantize_weights(desc, w13, w2, stream=None):

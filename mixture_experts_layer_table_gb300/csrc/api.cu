@@ -289,6 +289,9 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   if ((int64_t)ctx_bytes < L.ctx_bytes || (int64_t)ws_bytes < L.ws_bytes) return MOK_ERR_WORKSPACE_TOO_SMALL;
   const int n_sm = sm_count();
   if (n_sm <= 0) return MOK_ERR_CUDA;
+  // fp16 W2 (MOK_FLAG_W2_F16): the narrow-segment GEMMs without the ring only
+  const bool w2_f16 = (d->flags & MOK_FLAG_W2_F16) != 0;
+  if (w2_f16 && (d->ring_bytes > 0 || gemm_variant(d, GEMM2) != mok::GEMM_NARROW)) return MOK_ERR_UNSUPPORTED;
   RingGeom rg;
   const int comm = d->comm_sms > 0 ? d->comm_sms : 8;
   if (d->ring_bytes > 0) {
@@ -327,7 +330,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     MOK_LAUNCH("gather_x", st, mok::launch_gather_rows(x, src_of, k, R, H, x_g, n_sm, st));
     // 5. grouped GEMM1 with the SwiGLU epilogue
     MOK_LAUNCH("gemm1_swiglu", st, mok::launch_gemm1_swiglu(x_g, w13, R, H, I, E, offsets, tile_off, hu, act, act_lo,
-                                                            status, n_sm, gemm_variant(d, GEMM1), st));
+                                                            status, n_sm, gemm_variant(d, GEMM1), w2_f16, st));
   } else {
     // 4-5. ring forward: per-minibatch tables, then one persistent launch in which `comm`
     //      CTAs gather minibatches into the ring while the others run GEMM1 on them
@@ -360,12 +363,22 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     ra.consumed = counters + rg.n_mb;
     MOK_LAUNCH("ring_gemm1_swiglu", st, mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, st));
   }
-  // 6. grouped GEMM2 (a as hi + lo), fp32 expert outputs
+  // 6. grouped GEMM2 (a as hi + lo, or as fp16 against the fp16 W2), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
              mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm,
-                               gemm_variant(d, GEMM2), st));
+                               gemm_variant(d, GEMM2), w2_f16, st));
   // 7. weighted merge in fixed order
   MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
+  return MOK_OK;
+}
+
+mok_status mok_convert_f16(const void* src, void* dst, int64_t n, void* stream) {
+  if (!src || !dst || n < 0 || !aligned16(src) || !aligned16(dst)) return MOK_ERR_INVALID_ARG;
+  if (n == 0) return MOK_OK;
+  const int n_sm = sm_count();
+  if (n_sm <= 0) return MOK_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOK_LAUNCH("convert_f16", st, mok::launch_bf16_to_f16(src, dst, n, n_sm, st));
   return MOK_OK;
 }
 

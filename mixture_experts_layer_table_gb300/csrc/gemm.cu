@@ -201,7 +201,8 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
 
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, int variant, cudaStream_t st) {
+                                void* act_lo, int* status, int n_sm, int variant, bool a_f16, cudaStream_t st) {
+  if (a_f16 && variant != GEMM_NARROW) return cudaErrorInvalidValue;
   if (variant == GEMM_NARROW) {
     // W13[e] as [2][I][H]: each CTA takes 64 gate rows and their 64 up rows in one box (128 and
     // 128 in the paired form, at >= 384 rows per expert)
@@ -217,6 +218,7 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
     g.out1 = act_hi;
     g.out2 = act_lo;
     g.ld1 = I;
+    g.a_f16 = a_f16 ? 1 : 0;
     if (paired) return launch_narrow<false, false, 256, EPI_SWIGLU_PAIRED>(tw, x_g, nullptr, H, g, R, n_sm, st);
     // at most 160 rows per expert on average: 192-row chunks (7 stages instead of 6; 1% faster at
     // 128 rows per expert)
@@ -251,8 +253,9 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
 
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         int variant, cudaStream_t st) {
+                         int variant, bool f16, cudaStream_t st) {
   const bool pair = variant == GEMM_ROWS_PAIR;
+  if (f16 && variant != GEMM_NARROW) return cudaErrorInvalidValue;
   if (variant == GEMM_NARROW) {
     // W2 [E][H][I] K-major, 128-row boxes (one CTA's half of a 256-row weight tile)
     CUtensorMap tw;
@@ -262,6 +265,14 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
     g.K = I;
     g.out0 = out;
     g.ld0 = H;
+    if (f16) {
+      // fp16 a (one value, 11 significant bits) against an fp16 copy of W2: one MMA per K step
+      // (the TMA copies are bitwise: the bf16 maps serve any 16-bit element)
+      g.f16 = 1;
+      if (narrow_short_rows(R, E))
+        return launch_narrow<false, false, 192, EPI_F32_PAIRED>(tw, act_hi, nullptr, I, g, R, n_sm, st);
+      return launch_narrow<false, false, 256>(tw, act_hi, nullptr, I, g, R, n_sm, st);
+    }
     if (narrow_short_rows(R, E))
       return launch_narrow<false, true, 192, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
     return launch_narrow<false, true, 256>(tw, act_hi, act_lo, I, g, R, n_sm, st);

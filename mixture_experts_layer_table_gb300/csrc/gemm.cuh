@@ -87,6 +87,9 @@ struct GemmArgs {
   void* out3;
   void* out4;
   long long ld0, ld1, ld2;
+  int f16;                  // narrow kernels: the MMA operands are fp16 (else bf16)
+  int a_f16;                // narrow SwiGLU epilogues: a = silu(h) u stored as one fp16 value in out1
+                            // (11 significant bits) instead of a bf16 hi / lo pair
   const float* hu;          // SWIGLU_BWD: saved h | u (fp32)
   const float* gate_row;    // SWIGLU_BWD: gate of each row
   int* status;

@@ -18,7 +18,9 @@
 //   EPI_SWIGLU   GEMM1 x_g W13[e]^T (K = H): each CTA's 128 weight rows are 64 gate rows and the
 //                64 up rows of the same intermediate indices, so h and u of one (row, i) sit on
 //                TMEM lane quarters q and q + 2; the gate warp hands h to the up warp through
-//                shared memory, which forms a = silu(h) u (stored as a bf16 hi / lo pair).
+//                shared memory, which forms a = silu(h) u (stored as a bf16 hi / lo pair, or with
+//                args.a_f16 as one fp16 value, for a GEMM2 on fp16 operands).
+//   args.f16     the MMA operands are fp16 (GEMM2 on an fp16 copy of W2 and fp16 a) instead of bf16.
 //
 // Roles (both CTAs): warp 0 TMA producer, warp 1 MMA issuer (even CTA only), warps 2..5 epilogue
 // (tcgen05.ld of 32 rows x 32 columns, then per row one 128-byte store of 32 consecutive
@@ -258,7 +260,8 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t a_lbo = WMN ? MOK_MN_LBO : 16, a_sbo = WMN ? MOK_MN_SBO : 1024;
       for (int g = pair; g < total && ok; g += npairs) {
         const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
-        const uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
+        uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
+        if (args.f16) idesc &= ~((1u << 7) | (1u << 10));  // A and B formats: fp16 instead of bf16
         int w_ok = 1;
         if (lane == 0)
           w_ok = mbar_wait<true>(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
@@ -378,9 +381,13 @@ __global__ void __launch_bounds__(192, 1)
               const float u = xu[j * 32 + lane];
               *up = u;
               const float a = h / (1.0f + __expf(-h)) * u;
-              const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
-              *php = a_hi;
-              *plp = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+              if (args.a_f16) {
+                *reinterpret_cast<__half*>(php) = __float2half_rn(a);
+              } else {
+                const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
+                *php = a_hi;
+                *plp = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+              }
               up += args.ld0;
               php += args.ld1;
               plp += args.ld1;
@@ -412,9 +419,13 @@ __global__ void __launch_bounds__(192, 1)
               hrow[r * args.ld0] = h;
               hrow[r * args.ld0 + args.I] = u;
               const float a = h / (1.0f + __expf(-h)) * u;
-              const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
-              arow_hi[r * args.ld1] = a_hi;
-              arow_lo[r * args.ld1] = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+              if (args.a_f16) {
+                reinterpret_cast<__half*>(arow_hi)[r * args.ld1] = __float2half_rn(a);
+              } else {
+                const __nv_bfloat16 a_hi = __float2bfloat16_rn(a);
+                arow_hi[r * args.ld1] = a_hi;
+                arow_lo[r * args.ld1] = __float2bfloat16_rn(a - __bfloat162float(a_hi));
+              }
             }
           }
         }

@@ -46,10 +46,10 @@ cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H
 enum GemmVariant { GEMM_ROWS_SINGLE = 0, GEMM_ROWS_PAIR = 1, GEMM_NARROW = 2 };
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, float* hu, void* act_hi,
-                                void* act_lo, int* status, int n_sm, int variant, cudaStream_t st);
+                                void* act_lo, int* status, int n_sm, int variant, bool a_f16, cudaStream_t st);
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         int variant, cudaStream_t st);
+                         int variant, bool f16, cudaStream_t st);
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, const float* hu,
                                 const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,
@@ -127,6 +127,8 @@ cudaError_t launch_dgrad_x_mxf8(const void* dhuq, const void* dhusf, const void*
 // w [E][N][K] bf16 -> wt [E][K][N] E4M3 quantised in 32-blocks along N, scales [E][K/128][N/128][512].
 cudaError_t launch_quantize_transpose(const void* w, void* wt_q, void* wt_s, int E, int N, int K, int n_sm,
                                       cudaStream_t st);
+// src [n] bf16 -> dst [n] fp16 (round to nearest even; exact for bf16 values of magnitude 2^-14 .. 65504)
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, int n_sm, cudaStream_t st);
 cudaError_t launch_test_wait(int* status, long long limit_ns, cudaStream_t st);
 
 }  // namespace mok

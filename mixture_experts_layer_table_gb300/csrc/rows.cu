@@ -7,6 +7,7 @@
 // the weighted merge (same page, §04); each token's k rows are summed in the fixed order
 // j = 0..k-1 in fp32, so the result is bitwise reproducible (no atomics).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -181,6 +182,32 @@ cudaError_t launch_combine(const float* rows, const float* w, const int32_t* row
     combine_kernel<8><<<blocks, warps * 32, 0, st>>>(r, w, row_of, T, k, vec, dl, wr, topk_idx, E, dense_router, o);
   else
     combine_kernel<16><<<blocks, warps * 32, 0, st>>>(r, w, row_of, T, k, vec, dl, wr, topk_idx, E, dense_router, o);
+  return cudaGetLastError();
+}
+
+// bf16 -> fp16, 8 elements per thread per step (16-byte loads and stores; a ragged tail element by
+// element).  Round to nearest even: exact for bf16 values of magnitude 2^-14 .. 65504 (fp16 normals
+// hold every 8-bit bf16 significand), smaller ones become fp16 subnormals (absolute error <= 2^-25).
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ src,
+                                                          __half* __restrict__ dst, long long n) {
+  const long long n8 = n / 8;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 u = reinterpret_cast<const uint4*>(src)[i];
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+    uint4 o;
+    __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = __float22half2_rn(__bfloat1622float2(b[q]));
+    reinterpret_cast<uint4*>(dst)[i] = o;
+  }
+  for (long long i = n8 * 8 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = __float2half_rn(__bfloat162float(src[i]));
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, int n_sm, cudaStream_t st) {
+  bf16_to_f16_kernel<<<n_sm * 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src),
+                                               reinterpret_cast<__half*>(dst), n);
   return cudaGetLastError();
 }
 

@@ -363,3 +363,50 @@ def test_ring_rejects_a_ring_smaller_than_one_minibatch():
     with pytest.raises(mok.MokError) as info:
         mok.get_layout(desc)
     assert info.value.code == 2
+
+
+# ----------------------------------------------------------------------------- fp16 W2 (MOK_FLAG_W2_F16)
+
+@pytest.mark.parametrize("shape", [MID, MID_SKEW, LONG, LONG_SKEW], ids=lambda c: c.name)
+def test_forward_with_fp16_w2(shape):
+    """The forward on an fp16 copy of W2 with a kept as one fp16 value (GEMM1's SwiGLU epilogue in
+    both forms: LONG has 750 rows per expert, the paired form): a is the fp16 rounding of the GPU's
+    own silu(h) u, the expert outputs and y meet the bars against the float64 oracle on the bf16
+    weights, and the backward (bf16 W2) is unchanged."""
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
+    fwd, bwd = oracle_layer(shape, f64, topk_idx=given)
+    dev = _gpu_inputs(inp)
+    w2_f16 = mok.convert_f16(dev["w2"])
+    w32, h32 = dev["w2"].float(), w2_f16.float()
+    big = w32.abs() >= 2.0 ** -14                                      # fp16 normals: exact
+    assert torch.equal(h32[big], w32[big])
+    assert float((h32 - w32).abs().max()) <= 2.0 ** -25                # subnormals: half a step
+    layer = mok.MoELayer(mok.desc_from_shape(shape, flags=mok.FLAG_W2_F16))
+    given_t = torch.tensor(given, dtype=torch.int32, device="cuda")
+    y = layer.forward(dev["x"], dev["w_router"], dev["w13"], w2_f16, router_bias=dev["router_bias"], given_topk=given_t)
+    grads = layer.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    hu = layer.view("hu").double()
+    a_gpu = (hu[:, :shape.I] / (1 + torch.exp(-hu[:, :shape.I])) * hu[:, shape.I:]).float()
+    a16 = layer.view("act").view(torch.float16)
+    assert torch.allclose(a16.float(), a_gpu.half().float(), rtol=2.0 ** -10, atol=1e-30)
+    assert_intermediate_close(to_f64(a16), fwd["a"], "a (fp16)", rel=2.0 ** -10)
+    assert_intermediate_close(to_f64(layer.view("expert_out")), fwd["o"], "o", rel=1e-3)
+    assert_bf16_close(to_f64(y), fwd["y"], "y")
+    for name in ("dx", "dw13", "dw2", "dgates", "dw_router"):
+        assert_bf16_close(to_f64(grads[name]), bwd[name], name)
+
+
+def test_fp16_w2_refused_with_ring_and_row_tiles():
+    d_ring = mok.desc_from_shape(MID, flags=mok.FLAG_W2_F16, minibatch=256, ring_bytes=8 << 20)
+    d_rows = mok.desc_from_shape(MID, flags=mok.FLAG_W2_F16 | mok.FLAG_GEMM_SINGLE)
+    inp = _gpu_inputs(W.make_inputs(MID, seed=0, device="cpu", with_dy=False))
+    w2_f16 = mok.convert_f16(inp["w2"])
+    for d in (d_ring, d_rows):
+        layer = mok.MoELayer(d)
+        with pytest.raises(mok.MokError) as err:
+            layer.forward(inp["x"], inp["w_router"], inp["w13"], w2_f16)
+        assert err.value.code == 2

@@ -88,3 +88,37 @@ def test_schedule_table_bit_exact(run):
     ref = O.schedule(idx, SHAPE.E)
     for name in ("counts", "offsets", "row_of", "src_of"):
         assert np.array_equal(table[name], ref[name]), name
+
+
+def test_fp16_w2_forward_sampled_tokens(run):
+    """The same T=16384 forward with MOK_FLAG_W2_F16 (fp16 copy of W2, a as one fp16 value, one GEMM2
+    MMA per K step): the same selection, and the sampled tokens against the oracle on the bf16
+    weights at the bf16 bar."""
+    inp, idx, y_plain, _, _, _ = run
+    w2_f16 = mok.convert_f16(inp["w2"])
+    layer = mok.MoELayer(mok.desc_from_shape(SHAPE, flags=mok.FLAG_W2_F16))
+    y = layer.forward(inp["x"], inp["w_router"], inp["w13"], w2_f16)
+    torch.cuda.synchronize()
+    assert layer.status() == (0, 0)
+    assert np.array_equal(layer.view("topk_idx").cpu().numpy(), idx)
+    del layer, w2_f16
+    torch.cuda.empty_cache()
+    rng = np.random.default_rng(3)
+    cand = np.sort(rng.choice(SHAPE.T, size=N_CANDIDATES, replace=False))
+    w_r = to_f64(inp["w_router"])
+    x_c = to_f64(inp["x"][torch.as_tensor(cand, device=inp["x"].device)])
+    _, scores = O.router_scores(x_c, w_r, SHAPE.router)
+    pick = clear_margin_tokens(scores, SHAPE.k, N_TOKENS, seed=4)
+    toks = cand[pick]
+    cache = {}
+
+    def experts(e):
+        if e not in cache:
+            if len(cache) > 8:
+                cache.pop(next(iter(cache)))
+            cache[e] = (to_f64(inp["w13"][e]), to_f64(inp["w2"][e]))
+        return cache[e]
+
+    y_rows = to_f64(y[torch.as_tensor(toks, device=y.device)])
+    check_sampled_token_outputs(toks, x_c[pick], w_r, None, experts, SHAPE, y_rows, idx[toks],
+                                "y (T=16384, fp16 W2, sampled tokens)")
