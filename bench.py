@@ -326,6 +326,59 @@ def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
     return sweep
 
 
+def ring_fwd_bwd(shp, x, w_router, w13, w2, steps, warmup, minibatch=2368):
+    """Forward + backward at `shp` with and without the 512 MiB ring (minibatch `minibatch`): ms per
+    step over K steps after W warm-ups, the backward's replay of the dispatched rows (the ring-based
+    backward gathers only the minibatches the ring overwrote), and whether every gradient is
+    bitwise the plain layer's."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import _native as N
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    g = torch.Generator(device=x.device).manual_seed(4)
+    dy = torch.empty((shp.T, shp.H), dtype=torch.float32, device=x.device).normal_(0.0, 1.0, generator=g)
+    dy = dy.to(torch.bfloat16)
+    stream = torch.cuda.current_stream()
+    out = {"minibatch": minibatch, "ring_bytes": W.RING_BYTES}
+    grads = {}
+    for name, kw in (("plain", {}), ("ring", {"minibatch": minibatch, "ring_bytes": W.RING_BYTES})):
+        layer = mok.MoELayer(mok.desc_from_shape(shp, **kw), device=x.device)
+        for _ in range(warmup):
+            layer.forward(x, w_router, w13, w2)
+            gr = layer.backward(dy, x, w_router, w13, w2)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        N.trace_start(40 * steps + 16)
+        e0.record(stream)
+        for _ in range(steps):
+            layer.forward(x, w_router, w13, w2)
+            layer.backward(dy, x, w_router, w13, w2, out=gr)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        trace = N.trace_stop()
+        if layer.status() != (0, 0):
+            raise RuntimeError(f"device status set in the {name} forward + backward")
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"fwd_bwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1)}
+        if "gather_x_replay" in trace:
+            t = trace["gather_x_replay"]
+            out[name]["replay_ms"] = round(t["total_ms"] / t["launches"], 4)
+        grads[name] = gr
+        del layer
+        torch.cuda.empty_cache()
+    out["bitwise_equal_gradients"] = all(torch.equal(grads["plain"][n], grads["ring"][n]) for n in grads["plain"])
+    R = shp.R
+    n_mb = -(-R // minibatch)
+    slots = min(W.RING_BYTES // (minibatch * shp.H * 2), n_mb)
+    out["rows_replayed"] = (n_mb - slots) * minibatch
+    out["rows_resident"] = R - out["rows_replayed"]
+    del grads, dy
+    torch.cuda.empty_cache()
+    return out
+
+
 def tensor_sha256(t):
     """SHA-256 of a tensor's bit pattern (row-major bytes), read back to the host."""
     import hashlib
@@ -647,6 +700,7 @@ def run_mok(args, rank, world, local_rank):
             torch.cuda.empty_cache()
         if not args.no_ring_sweep:
             tb["ring_sweep"] = ring_sweep(shp_tb, x_tb, wr, w13, w2, y_tb.clone(), args.steps, args.warmup)
+            tb["ring_fwd_bwd"] = ring_fwd_bwd(shp_tb, x_tb, wr, w13, w2, args.steps, args.warmup)
         del x_tb, y_tb
 
     if rank != 0:

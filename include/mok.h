@@ -128,6 +128,7 @@ typedef struct {
   int64_t gate_row;   /* f32 [T*k]    gate of each sorted row */
   int64_t x_g;        /* bf16 [T*k][H]  dispatched (expert-sorted) token rows */
   int64_t hu;         /* f32 [T*k][2I]  gate and up projections h | u */
+  int64_t ring_stamp; /* u64 [2]      ring forward only: a count of the ring forwards on this ctx */
   int64_t ctx_bytes;
   /* ws.  "hi/lo" pairs hold v as bf16 hi = bf16(v) plus bf16 lo = bf16(v - hi), so that a
    * GEMM operand produced inside the layer keeps about 16 significant bits. */
@@ -146,10 +147,16 @@ typedef struct {
   int64_t dg_part;    /* f32 [T*k][I/128] partial gate gradients per GEMM column tile (bf16: I/256 used) */
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
   /* ring forward only (-1 otherwise) */
-  int64_t ring;       /* bf16 [slots * minibatch][H]  the token ring */
+  int64_t ring;       /* bf16 [n_mb * minibatch][H]  the dispatched rows of every minibatch: the
+                          token ring is the last slots * minibatch rows, minibatch mb in slot
+                          (mb + n_mb * (slots - 1)) % slots, so that the minibatches the ring still
+                          holds after the forward sit at their own rows; the backward replays the
+                          rest in front of them */
   int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb] tiles,
                           [n_mb+1] tile starts (exclusive prefix of the tiles) */
-  int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch */
+  int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch; then
+                          (16-byte aligned) u64 [2] {ctx address, ctx ring_stamp} of the forward
+                          whose rows the ring holds */
   /* MXFP8 backward only (-1 otherwise): operands quantised along their GEMM's reduction
    * dimension, as exact bf16 values */
   int64_t mx_dhu_r;   /* bf16 [T*k][2I] dh | du in 32-row blocks of each expert (dW13) */
@@ -229,9 +236,12 @@ mok_status mok_schedule_noalloc(const mok_layer_desc* desc, const void* x, const
  *   ctx (layout.ctx_bytes) receives what the backward needs; ws (layout.ws_bytes) is
  *   scratch and also holds the status word.  Pointers to x, weights, y, ctx and ws must be
  *   16-byte aligned (TMA).  MXFP8 is not accepted here (MOK_ERR_UNSUPPORTED).
- *   With ring_bytes > 0 the dispatched rows live only in the ring (ctx x_g is not written;
- *   mok_moe_backward gathers them again) and y is bitwise the same as without the ring.  The
- *   ring launch is cooperative: all of its CTAs must be resident at once (one per SM). */
+ *   With ring_bytes > 0 the dispatched rows live only in the ring (ctx x_g is not written) and y
+ *   is bitwise the same as without the ring.  The ring-based backward (mok_moe_backward on the
+ *   same ctx and ws) reuses the minibatches the ring still holds and gathers again only those it
+ *   overwrote ("Mixture-of-Kittens (MoK)", sd114.wiki, ring-buffer section); given another ws it
+ *   gathers them all, with the same results.  The ring launch is cooperative: all of its CTAs
+ *   must be resident at once (one per SM). */
 mok_status mok_moe_forward(const mok_layer_desc* desc, const void* x, const void* w_router,
                            const float* router_bias, const int32_t* given_topk, const void* w13,
                            const void* w2, void* y, void* ctx, size_t ctx_bytes, void* ws,

@@ -36,7 +36,7 @@ class LayerDesc(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ["topk_idx", "gates", "scores", "counts", "offsets", "row_of", "src_of", "tile_off", "gate_row",
-                 "x_g", "hu", "ctx_bytes", "status", "logits", "sched", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
+                 "x_g", "hu", "ring_stamp", "ctx_bytes", "status", "logits", "sched", "act", "act_lo", "expert_out", "dy_g", "dhu", "dhu_lo",
                  "gact", "gact_lo", "dx_g", "dg_part", "dlogits", "ring", "mb_tables", "mb_counters",
                  "mx_dhu_r", "mx_xg_r", "mx_do_r", "mx_a_r", "mx_blk_off", "mx_xq", "mx_xsf", "mx_aq",
                  "mx_asf", "mx_dyq", "mx_dysf", "mx_dhuq", "mx_dhusf", "ws_bytes"]
@@ -245,7 +245,7 @@ def test_bounded_wait(ws, limit_ms: int, stream=None):
 
 _CTX_DTYPES = {"topk_idx": torch.int32, "gates": torch.float32, "scores": torch.float32, "counts": torch.int32,
                "offsets": torch.int32, "row_of": torch.int32, "src_of": torch.int32, "tile_off": torch.int32,
-               "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.float32, "status": torch.int32,
+               "gate_row": torch.float32, "x_g": torch.bfloat16, "hu": torch.float32, "ring_stamp": torch.int64, "ring": torch.bfloat16, "status": torch.int32,
                "logits": torch.float32, "sched": torch.int32, "act": torch.bfloat16, "act_lo": torch.bfloat16,
                "expert_out": torch.float32, "dy_g": torch.bfloat16, "dhu": torch.bfloat16, "dhu_lo": torch.bfloat16,
                "gact": torch.bfloat16, "gact_lo": torch.bfloat16, "dx_g": torch.float32,
@@ -275,12 +275,22 @@ class MoELayer:
         self.ctx = torch.empty(self.layout["ctx_bytes"], dtype=torch.uint8, device=device)
         self.ws = torch.zeros(self.layout["ws_bytes"], dtype=torch.uint8, device=device)
 
+    def ring_rows(self) -> int:
+        """Rows of the ring forward's dispatched-row region (whole minibatches)."""
+        d = self.desc
+        R = d.T * d.k
+        m = d.minibatch if d.minibatch > 0 else min_minibatch(0, d.I)
+        m = min(m, R)
+        return -(-R // m) * m
+
     def _shape(self, name):
         d = self.desc
         R = d.T * d.k
+        if name == "ring":
+            return (self.ring_rows(), d.H)
         return {"topk_idx": (d.T, d.k), "gates": (d.T, d.k), "scores": (d.T, d.E), "counts": (d.E,),
                 "offsets": (d.E + 1,), "row_of": (R,), "src_of": (R,), "tile_off": (d.E + 1,), "gate_row": (R,),
-                "x_g": (R, d.H), "hu": (R, 2 * d.I), "status": (4,), "logits": (d.T, d.E), "sched": (-(-R // 1024), d.E), "act": (R, d.I),
+                "x_g": (R, d.H), "hu": (R, 2 * d.I), "ring_stamp": (2,), "status": (4,), "logits": (d.T, d.E), "sched": (-(-R // 1024), d.E), "act": (R, d.I),
                 "act_lo": (R, d.I), "expert_out": (R, d.H), "dy_g": (R, d.H), "dhu": (R, 2 * d.I),
                 "dhu_lo": (R, 2 * d.I), "gact": (R, d.I), "gact_lo": (R, d.I),
                 "dx_g": (R, d.H), "dg_part": (R, d.I // 128), "dlogits": (d.T, d.E), "mx_dhu_r": (R, 2 * d.I), "mx_xg_r": (R, d.H), "mx_do_r": (R, d.H), "mx_a_r": (R, d.I),

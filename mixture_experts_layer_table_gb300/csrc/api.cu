@@ -74,6 +74,9 @@ struct RingGeom {
   int m = 0, n_mb = 0, slots = 0;
 };
 
+// Byte offset of the ring stamp (u64 [2]) after the [2][n_mb] i32 counters.
+int64_t ring_stamp_offset(int n_mb) { return (int64_t(2) * n_mb * 4 + 15) & ~int64_t(15); }
+
 mok_status ring_geometry(const mok_layer_desc* d, RingGeom* g) {
   const int64_t R = int64_t(d->T) * d->k;
   int64_t m = d->minibatch;
@@ -111,6 +114,12 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->gate_row = take(R * 4);
   L->x_g = take(R * H * 2);
   L->hu = take(R * 2 * I * 4);
+  RingGeom rgeom;
+  if (d->ring_bytes > 0) {
+    const mok_status s = ring_geometry(d, &rgeom);
+    if (s != MOK_OK) return s;
+  }
+  L->ring_stamp = d->ring_bytes > 0 ? take(16) : -1;
   L->ctx_bytes = off;
   off = 0;
   L->status = take(mok::STATUS_BYTES);
@@ -129,13 +138,13 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
   L->dlogits = take(T * E * 4);
   L->ring = L->mb_tables = L->mb_counters = -1;
   if (d->ring_bytes > 0) {
-    RingGeom g;
-    const mok_status s = ring_geometry(d, &g);
-    if (s != MOK_OK) return s;
-    L->ring = take(int64_t(g.slots) * g.m * H * 2);
+    const RingGeom& g = rgeom;
+    // the dispatched rows of every minibatch; the token ring is the last slots * m of them
+    L->ring = take(int64_t(g.n_mb) * g.m * H * 2);
     // mb_off [n_mb][E+1], mb_toff [n_mb][E+1], mb_tiles [n_mb], mb_start [n_mb+1]
     L->mb_tables = take((int64_t(2) * g.n_mb * (E + 1) + 2 * int64_t(g.n_mb) + 1) * 4);
-    L->mb_counters = take(int64_t(2) * g.n_mb * 4);
+    // counters [2][n_mb], then the u64 [2] stamp of the forward that filled the ring
+    L->mb_counters = take(ring_stamp_offset(g.n_mb) + 16);
   }
   L->mx_dhu_r = L->mx_xg_r = L->mx_do_r = L->mx_a_r = L->mx_blk_off = -1;
   L->mx_xq = L->mx_xsf = L->mx_aq = L->mx_asf = L->mx_dyq = L->mx_dysf = L->mx_dhuq = L->mx_dhusf = -1;
@@ -354,14 +363,23 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     ra.mb_rows = rg.m;
     ra.n_mb = rg.n_mb;
     ra.ring_slots = rg.slots;
+    // minibatch mb in slot (mb + shift) % slots: the last `slots` minibatches, which the ring still
+    // holds after the forward, then sit in slot order at their own rows of the dispatched-row region
+    ra.ring_shift = (rg.slots - rg.n_mb % rg.slots) % rg.slots;
     ra.comm_ctas = comm;
-    ra.ring = at<char>(ws, L.ring);
+    ra.ring = at<char>(ws, L.ring) + (int64_t)(rg.n_mb - rg.slots) * rg.m * H * 2;
     ra.mb_off = mb_off;
     ra.mb_toff = mb_toff;
     ra.mb_start = mb_start;
     ra.gathered = counters;
     ra.consumed = counters + rg.n_mb;
     MOK_LAUNCH("ring_gemm1_swiglu", st, mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, st));
+    // the ring rows are this forward's (the backward reuses them when it is given this ws)
+    MOK_LAUNCH("ring_stamp", st,
+               mok::launch_ring_stamp(at<unsigned long long>(ctx, L.ring_stamp),
+                                      reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(counters) +
+                                                                            ring_stamp_offset(rg.n_mb)),
+                                      (unsigned long long)reinterpret_cast<uintptr_t>(ctx), st));
   }
   // 6. grouped GEMM2 (a as hi + lo, or as fp16 against the fp16 W2), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
@@ -584,10 +602,20 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   // the work counters of this call start at zero (the status word keeps what the forward left)
   MOK_CUDA(cudaMemsetAsync(status + mok::STATUS_COUNTERS, 0, mok::STATUS_BYTES - 4 * mok::STATUS_COUNTERS, st));
   if (d->ring_bytes > 0) {
-    // the ring forward kept the dispatched rows only in the ring: dispatch them again, into
-    // the expert-output scratch, which the backward does not otherwise use
+    // Ring backward: the ring forward left the dispatched rows of its last `slots` minibatches in
+    // the ring, at their own rows of the dispatched-row region of ws; replay (gather again) only
+    // the minibatches it overwrote, in front of them.  If ws is not the one that forward filled
+    // (its stamp differs from ctx's), every row is replayed; the rows are the same either way.
+    RingGeom rg;
+    s = ring_geometry(d, &rg);
+    if (s != MOK_OK) return s;
+    const int32_t* cnt = at<int32_t>(ws, L.mb_counters);
     MOK_LAUNCH("gather_x_replay", st,
-               mok::launch_gather_rows(x, at<int32_t>(ctx, L.src_of), k, R, H, at<char>(ws, L.expert_out), n_sm, st));
+               mok::launch_ring_replay(
+                   x, at<int32_t>(ctx, L.src_of), k, R, H, at<char>(ws, L.ring), (rg.n_mb - rg.slots) * rg.m,
+                   reinterpret_cast<const unsigned long long*>(reinterpret_cast<const char*>(cnt) +
+                                                               ring_stamp_offset(rg.n_mb)),
+                   at<unsigned long long>(ctx, L.ring_stamp), (unsigned long long)reinterpret_cast<uintptr_t>(ctx), st));
   }
   const int32_t* topk_idx = at<int32_t>(ctx, L.topk_idx);
   const float* gates = at<float>(ctx, L.gates);
@@ -597,7 +625,7 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
   const int32_t* row_of = at<int32_t>(ctx, L.row_of);
   const int32_t* src_of = at<int32_t>(ctx, L.src_of);
   const float* gate_row = at<float>(ctx, L.gate_row);
-  const void* x_g = d->ring_bytes > 0 ? static_cast<const void*>(at<char>(ws, L.expert_out))
+  const void* x_g = d->ring_bytes > 0 ? static_cast<const void*>(at<char>(ws, L.ring))
                                       : static_cast<const void*>(at<char>(ctx, L.x_g));
   const float* hu = at<float>(ctx, L.hu);
   void* dy_g = at<char>(ws, L.dy_g);

@@ -446,6 +446,7 @@ cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, vo
   g.n_mb = ra.n_mb;
   g.mb_rows = ra.mb_rows;
   g.ring_slots = ra.ring_slots;
+  g.ring_shift = ra.ring_shift;
   g.R = ra.R;
   g.k_top = ra.k;
   g.H = ra.H;

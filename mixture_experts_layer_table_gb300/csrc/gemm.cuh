@@ -98,6 +98,7 @@ struct GemmArgs {
   int n_mb;                 // minibatches
   int mb_rows;              // rows per minibatch (the last one may be shorter)
   int ring_slots;           // minibatches the ring holds
+  int ring_shift;           // minibatch mb lives in slot (mb + ring_shift) % ring_slots
   int R;                    // all rows
   int k_top;                // experts per token (row r holds token src_of[r] / k_top)
   int H;
@@ -574,7 +575,7 @@ __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint
     bulk_load_g2s(smem_u32(buf + (size_t)j * row_bytes), a.x + (size_t)tok * a.H, row_bytes, smem_u32(&bars[j]));
   };
   for (int mb = 0; mb < a.n_mb; ++mb) {
-    const int slot = mb % a.ring_slots;
+    const int slot = (mb + a.ring_shift) % a.ring_slots;
     const int r0 = mb * a.mb_rows;
     const int rows = min(a.mb_rows, a.R - r0);
     if (mb >= a.ring_slots) {
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
             fence_proxy_async_global();
             ring_ready = t.mb;
           }
-          a_row = (t.mb % args.ring_slots) * args.mb_rows + t.row0;
+          a_row = ((t.mb + args.ring_shift) % args.ring_slots) * args.mb_rows + t.row0;
         }
         for (int kb = 0; kb < t.nkb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,

@@ -28,6 +28,15 @@ cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* o
                                 int T, int H, int E, int k, int sparse, float* dw, cudaStream_t st);
 
 // rows.cu
+// The backward's replay of the dispatched rows after a ring forward: x_rows[r] = x[src_of[r] / k]
+// for r < R, except the rows the ring still holds (r >= head_rows) when the workspace's ring stamp
+// is the forward's (ws_stamp == {ctx address, ctx_stamp[0]}); else every row is replayed.
+cudaError_t launch_ring_replay(const void* x, const int32_t* src_of, int k, int R, int H, void* x_rows, int head_rows,
+                               const unsigned long long* ws_stamp, const unsigned long long* ctx_stamp,
+                               unsigned long long ctx_addr, cudaStream_t st);
+// Marks the ring rows as the work of this forward: ctx_stamp[0] += 1, ws_stamp = {ctx address, ctx_stamp[0]}.
+cudaError_t launch_ring_stamp(unsigned long long* ctx_stamp, unsigned long long* ws_stamp, unsigned long long ctx_addr,
+                              cudaStream_t st);
 cudaError_t launch_gather_rows(const void* src, const int32_t* src_of, int k, int R, int H, void* dst, int n_sm,
                                cudaStream_t st);
 // out[t] = sum_j w[t][j] * rows[row_of[t*k+j]] (+ router term), rows fp32, out bf16
@@ -77,6 +86,7 @@ struct RingArgs {
   const int32_t* src_of;
   int k, R, H, I, E;
   int mb_rows, n_mb, ring_slots, comm_ctas;
+  int ring_shift;  // minibatch mb lives in slot (mb + ring_shift) % ring_slots
   void* ring;
   const int32_t* mb_off;
   const int32_t* mb_toff;

@@ -69,6 +69,31 @@ __global__ void __launch_bounds__(GATHER_THREADS) gather_rows_kernel(const __nv_
   }
 }
 
+// Ring backward: block r replays dispatched row r unless the ring still holds it.  Every block
+// reads the two stamps (L2-resident after the first) and decides the same way.
+__global__ void __launch_bounds__(GATHER_THREADS)
+    ring_replay_kernel(const __nv_bfloat16* __restrict__ src, const int32_t* __restrict__ src_of, int k,
+                       int vec_per_row, __nv_bfloat16* __restrict__ dst, int head_rows,
+                       const unsigned long long* __restrict__ ws_stamp, const unsigned long long* __restrict__ ctx_stamp,
+                       unsigned long long ctx_addr) {
+  const int r = blockIdx.x;
+  const bool resident = ws_stamp[0] == ctx_addr && ws_stamp[1] == ctx_stamp[0];
+  if (resident && r >= head_rows) return;
+  const int tok = src_of[r] / k;
+  const uint64_t keep = l2_policy_evict_last();
+  const uint4* s = reinterpret_cast<const uint4*>(src) + (size_t)tok * vec_per_row;
+  uint4* d = reinterpret_cast<uint4*>(dst) + (size_t)r * vec_per_row;
+  for (int i = threadIdx.x; i < vec_per_row; i += GATHER_THREADS) st_v4_stream(d + i, ld_nc_v4_keep(s + i, keep));
+}
+
+__global__ void ring_stamp_kernel(unsigned long long* ctx_stamp, unsigned long long* ws_stamp,
+                                  unsigned long long ctx_addr) {
+  const unsigned long long n = ctx_stamp[0] + 1;
+  ctx_stamp[0] = n;
+  ws_stamp[0] = ctx_addr;
+  ws_stamp[1] = n;
+}
+
 __device__ __forceinline__ void acc_bf16x8(float (&acc)[8], uint4 v, float w) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -208,6 +233,22 @@ __global__ void __launch_bounds__(256) bf16_to_f16_kernel(const __nv_bfloat16* _
 cudaError_t launch_bf16_to_f16(const void* src, void* dst, long long n, int n_sm, cudaStream_t st) {
   bf16_to_f16_kernel<<<n_sm * 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(src),
                                                reinterpret_cast<__half*>(dst), n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_replay(const void* x, const int32_t* src_of, int k, int R, int H, void* x_rows, int head_rows,
+                               const unsigned long long* ws_stamp, const unsigned long long* ctx_stamp,
+                               unsigned long long ctx_addr, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  ring_replay_kernel<<<R, GATHER_THREADS, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), src_of, k, H / 8,
+                                                   reinterpret_cast<__nv_bfloat16*>(x_rows), head_rows, ws_stamp,
+                                                   ctx_stamp, ctx_addr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_stamp(unsigned long long* ctx_stamp, unsigned long long* ws_stamp, unsigned long long ctx_addr,
+                              cudaStream_t st) {
+  ring_stamp_kernel<<<1, 1, 0, st>>>(ctx_stamp, ws_stamp, ctx_addr);
   return cudaGetLastError();
 }
 

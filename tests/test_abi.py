@@ -41,7 +41,7 @@ def test_layout_sizes_and_alignment(lib):
     lay = mok.get_layout(mok.desc_from_shape(W.DSV3))
     R, H, I = W.DSV3.R, W.DSV3.H, W.DSV3.I
     for name, off in lay.items():
-        assert off % 256 == 0 or (off == -1 and (name in ("ring", "mb_tables", "mb_counters") or
+        assert off % 256 == 0 or (off == -1 and (name in ("ring", "mb_tables", "mb_counters", "ring_stamp") or
                                                  name.startswith("mx_"))), name
     assert lay["ctx_bytes"] >= lay["hu"] + R * 2 * I * 2
     assert lay["ws_bytes"] >= lay["dlogits"] + W.DSV3.T * W.DSV3.E * 4
@@ -89,7 +89,9 @@ def test_ring_layout(lib):
     lay = mok.get_layout(d)
     slots = W.RING_BYTES // (m * shp.H * 2)
     n_mb = -(-shp.R // m)
-    assert lay["mb_tables"] - lay["ring"] >= slots * m * shp.H * 2
+    # the dispatched rows of every minibatch (the ring is their last `slots` minibatches)
+    assert lay["mb_tables"] - lay["ring"] >= n_mb * m * shp.H * 2 and slots < n_mb
+    assert lay["ring_stamp"] >= 0 and lay["ring_stamp"] + 16 <= lay["ctx_bytes"]
     assert lay["mb_counters"] - lay["mb_tables"] >= (2 * n_mb * (shp.E + 1) + 2 * n_mb + 1) * 4
     # a ring below one minibatch is refused
     d.ring_bytes = m * shp.H * 2 - 1
@@ -116,13 +118,16 @@ def _region_sizes(shp, ring_slots=0, minibatch=0):
     ctx = {"topk_idx": R * 4, "gates": R * 4, "scores": T * E * 4, "counts": E * 4, "offsets": (E + 1) * 4,
            "row_of": R * 4, "src_of": R * 4, "tile_off": (E + 1) * 4, "gate_row": R * 4, "x_g": R * H * 2,
            "hu": R * 2 * I * 4}
+    if minibatch:
+        ctx["ring_stamp"] = 16
     ws = {"status": 64 * 4, "logits": T * E * 4, "sched": -(-R // 1024) * E * 4, "act": R * I * 2, "act_lo": R * I * 2, "expert_out": R * H * 4,
           "dy_g": R * H * 2, "dhu": R * 2 * I * 2, "dhu_lo": R * 2 * I * 2, "gact": R * I * 2,
           "gact_lo": R * I * 2, "dx_g": R * H * 4, "dg_part": R * (I // 128) * 4, "dlogits": T * E * 4}
     if minibatch:
         n_mb = -(-R // minibatch)
-        ws.update({"ring": ring_slots * minibatch * H * 2,
-                   "mb_tables": (2 * n_mb * (E + 1) + n_mb + (n_mb + 1)) * 4, "mb_counters": 2 * n_mb * 4})
+        ws.update({"ring": n_mb * minibatch * H * 2,
+                   "mb_tables": (2 * n_mb * (E + 1) + n_mb + (n_mb + 1)) * 4,
+                   "mb_counters": ((2 * n_mb * 4 + 15) // 16) * 16 + 16})
     if shp.mxfp8:
         ws.update({"mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
                    "mx_do_r": R * H * 2, "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4})
@@ -146,7 +151,7 @@ def test_every_region_sized_aligned_and_disjoint(lib, case):
         slots = W.RING_BYTES // (m * shp.H * 2)
     lay = mok.get_layout(mok.desc_from_shape(shp, **kw))
     ctx, ws = _region_sizes(shp, slots, m)
-    assert set(ctx) == set(N.CTX_FIELDS)
+    assert set(ctx) | {"ring_stamp"} == set(N.CTX_FIELDS)   # ring_stamp: ring forward only
     for fields, sizes, total in ((N.CTX_FIELDS, ctx, lay["ctx_bytes"]), (N.WS_FIELDS, ws, lay["ws_bytes"])):
         spans = []
         for name in fields:

@@ -357,6 +357,44 @@ def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm
         assert torch.equal(g1[name], g0[name]), name
 
 
+def test_ring_backward_reuses_the_resident_minibatches():
+    """The ring-based backward: after a ring forward the ring still holds its last minibatches at
+    their own rows of the dispatched-row region, and the backward gathers again only the rows in
+    front of them.  Shown by handing the backward another x: the replayed rows come from it, the
+    resident ones are still the forward's.  With a fresh workspace (stamp mismatch) every row is
+    replayed.  The stamp in ws names the forward's ctx and its count of ring forwards."""
+    shape, minibatch, slots = MID, 300, 2
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    dev = _gpu_inputs(inp)
+    desc = mok.desc_from_shape(shape, minibatch=minibatch, ring_bytes=slots * minibatch * shape.H * 2, comm_sms=4)
+    ring = mok.MoELayer(desc)
+    ring.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    assert ring.status() == (0, 0)
+    R = shape.R
+    n_mb = -(-R // minibatch)
+    head = (n_mb - slots) * minibatch
+    stamp_ws = ring.ws[ring.layout["mb_counters"]:].view(torch.int32)
+    off = ((2 * n_mb * 4 + 15) // 16) * 4  # the u64 stamp after the counters, in int32 units
+    stamp = stamp_ws[off:off + 4].view(torch.int64).cpu().tolist()
+    assert stamp == [ring.ctx.data_ptr(), int(ring.view("ring_stamp")[0])]
+    src = ring.view("src_of").cpu().numpy().astype(np.int64) // shape.k
+    x2 = dev["x"] + 1.0                                            # another x for the backward
+    ring.backward(dev["dy"], x2, dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    rows = ring.view("ring")[:R].float().cpu()
+    x_cpu, x2_cpu = dev["x"].float().cpu(), x2.float().cpu()
+    assert torch.equal(rows[:head], x2_cpu[src[:head]])          # replayed from the backward's x
+    assert torch.equal(rows[head:], x_cpu[src[head:]])           # still the forward's rows
+    fresh = mok.MoELayer(desc)
+    fresh.ctx.copy_(ring.ctx)                                      # the forward's ctx, another ws
+    fresh_ctx_stamp = fresh.view("ring_stamp").clone()
+    fresh.backward(dev["dy"], x2, dev["w_router"], dev["w13"], dev["w2"])
+    torch.cuda.synchronize()
+    assert torch.equal(fresh.view("ring")[:R].float().cpu(), x2_cpu[src])
+    assert torch.equal(fresh.view("ring_stamp"), fresh_ctx_stamp)  # the backward does not touch ctx
+
+
 def test_ring_rejects_a_ring_smaller_than_one_minibatch():
     shape = MID
     desc = mok.desc_from_shape(shape, minibatch=512, ring_bytes=511 * shape.H * 2)

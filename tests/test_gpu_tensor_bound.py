@@ -122,3 +122,30 @@ def test_fp16_w2_forward_sampled_tokens(run):
     y_rows = to_f64(y[torch.as_tensor(toks, device=y.device)])
     check_sampled_token_outputs(toks, x_c[pick], w_r, None, experts, SHAPE, y_rows, idx[toks],
                                 "y (T=16384, fp16 W2, sampled tokens)")
+
+
+def test_ring_backward_full_size_bitwise(run):
+    """Forward + backward at T=16384 through the 512 MiB ring (minibatch 2368): the ring-based
+    backward reuses the minibatches the ring still holds and gathers the rest again; every
+    gradient is bitwise the plain layer's."""
+    inp = run[0]
+    g = torch.Generator(device="cuda").manual_seed(4)
+    dy = torch.empty((SHAPE.T, SHAPE.H), dtype=torch.float32, device="cuda").normal_(0.0, 1.0, generator=g)
+    dy = dy.to(torch.bfloat16)
+    args = (inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    plain = mok.MoELayer(mok.desc_from_shape(SHAPE))
+    plain.forward(*args)
+    g0 = plain.backward(dy, *args)
+    torch.cuda.synchronize()
+    assert plain.status() == (0, 0)
+    del plain
+    torch.cuda.empty_cache()
+    ring = mok.MoELayer(mok.desc_from_shape(SHAPE, minibatch=MINIBATCH, ring_bytes=W.RING_BYTES))
+    ring.forward(*args)
+    g1 = ring.backward(dy, *args)
+    torch.cuda.synchronize()
+    assert ring.status() == (0, 0)
+    for name in ("dx", "dw_router", "dw13", "dw2", "dgates"):
+        assert torch.equal(g1[name], g0[name]), name
+    del ring, g0, g1
+    torch.cuda.empty_cache()
