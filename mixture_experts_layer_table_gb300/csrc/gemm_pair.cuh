@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(192, 1)
       else epi_f32_tma<C::BN>(tacc, row0, nvalid, t.n, args, &tmO0, stg, lane);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty0_cl + 8u * acc);
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty0_cl + 8u * acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -115,6 +115,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+// Arrive with relaxed semantics at cluster scope: for an epilogue handing a TMEM accumulator back
+// to the MMA thread.  The warp's tcgen05.wait::ld has completed its TMEM reads and its
+// tcgen05.fence::before_thread_sync orders them before this arrive; the MMA thread's acquiring
+// wait and tcgen05.fence::after_thread_sync order its next MMAs after it.  Nothing else has to be
+// made visible, so the arrive need not wait, as a release would, for the warp's global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

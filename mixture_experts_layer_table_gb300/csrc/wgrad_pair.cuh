@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty0_cl + 8u * acc);
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty0_cl + 8u * acc);
         acc_phase ^= 1;
       }
     }
