@@ -536,32 +536,6 @@ def run_mok(args, rank, world, local_rank):
     torch.cuda.synchronize()
     fwd_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
 
-    # ---- the forward with the combine's weighting in GEMM2's epilogue (MOK_FLAG_COMBINE_IN_GEMM2)
-    combine_fused = None
-    if not args.no_combine_fused:
-        layer_cf = mok.MoELayer(mok.desc_from_shape(shp, flags=GEMM_FLAGS[args.gemm] | N.FLAG_COMBINE_IN_GEMM2),
-                                device=dev)
-        for _ in range(3):
-            layer_cf.forward(x, wr, w13, w2, y=y)
-        barrier()
-        torch.cuda.synchronize()
-        N.trace_start(16 * args.steps + 16)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            layer_cf.forward(x, wr, w13, w2, y=y)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        trace_cf = N.trace_stop()
-        cf_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
-        if layer_cf.status() != (0, 0):
-            raise RuntimeError("device status set in the fused-combine forward")
-        combine_fused = {"fwd_ms": round(cf_ms, 4), "fwd_ms_default": round(fwd_ms, 4),
-                         "kernels": {n: round(trace_cf[n]["total_ms"] / trace_cf[n]["launches"], 4)
-                                     for n in ("gemm2", "combine") if n in trace_cf},
-                         "kernels_default": {n: round(trace[n]["total_ms"] / trace[n]["launches"], 4)
-                                             for n in ("gemm2", "combine") if n in trace}}
-        del layer_cf
-
     # ---- the same step with bf16 weight gradients (MOK_FLAG_WGRAD_BF16): what the fp32 reading
     #      of dW13 / dW2 costs (the bf16 result is the fp32 one rounded to nearest even)
     wgrad_bf16_ms = None
@@ -800,7 +774,6 @@ def run_mok(args, rank, world, local_rank):
                 "d2h_bytes_per_step": step_bytes, "ms_per_step": round(e2e_ms, 4),
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step; "
                         "the copies of neighbouring steps overlap the compute on a second stream"},
-        "combine_in_gemm2": combine_fused,
         "wgrad_bf16": wgrad_bf16 if wgrad_bf16_ms is not None else None,
         "fwd_bwd_ms_wgrad_bf16": round(wgrad_bf16_ms, 4) if wgrad_bf16_ms is not None else None,
         "mxfp8_fwd": mx,
@@ -923,8 +896,6 @@ def main():
     ap.add_argument("--no-cpu-full", action="store_true",
                     help="skip the full-size oracle timings (DSV3 forward, skewed DSV3 forward + backward; ~1 min)")
     ap.add_argument("--no-wgrad-bf16", action="store_true", help="skip the step with bf16 weight gradients")
-    ap.add_argument("--no-combine-fused", action="store_true",
-                    help="skip the forward with the combine's weighting in GEMM2 (MOK_FLAG_COMBINE_IN_GEMM2)")
     ap.add_argument("--no-fp16-w2", action="store_true",
                     help="skip the T=16384 forward on an fp16 copy of W2 (MOK_FLAG_W2_F16)")
     ap.add_argument("--no-ring-sweep", action="store_true",

@@ -94,20 +94,12 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                operands, one MMA per K step instead of two.  Default GEMM kernels and no
  *                ring only (else MOK_ERR_UNSUPPORTED); mok_moe_backward ignores the flag and
  *                takes w2 in bf16 (the backward does not read a).
- *                MOK_FLAG_COMBINE_IN_GEMM2: the weighting of the combine moves into GEMM2's
- *                epilogue, which stores each expert row times its gate at its assignment's row
- *                (t*k + j), so that the merge sums k contiguous rows per token (the combine
- *                fused into the GEMM2 epilogue, "把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源 GPU
- *                内核 MoK", aientropygate.com §03 ③).  Deterministic; y differs from the default
- *                in the last bits (the product and the sum are rounded separately).  Default
- *                GEMM kernels only (else MOK_ERR_UNSUPPORTED).
  *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1
 #define MOK_FLAG_GEMM_PAIR 2
 #define MOK_FLAG_GEMM_SINGLE 4
 #define MOK_FLAG_W2_F16 8
-#define MOK_FLAG_COMBINE_IN_GEMM2 16
 typedef struct {
   int32_t T, H, I, E, k;
   int32_t router;

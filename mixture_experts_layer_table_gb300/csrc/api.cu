@@ -301,7 +301,6 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   // fp16 W2 (MOK_FLAG_W2_F16): the narrow-segment GEMMs without the ring only
   const bool w2_f16 = (d->flags & MOK_FLAG_W2_F16) != 0;
   if (w2_f16 && (d->ring_bytes > 0 || gemm_variant(d, GEMM2) != mok::GEMM_NARROW)) return MOK_ERR_UNSUPPORTED;
-  if ((d->flags & MOK_FLAG_COMBINE_IN_GEMM2) && gemm_variant(d, GEMM2) != mok::GEMM_NARROW) return MOK_ERR_UNSUPPORTED;
   RingGeom rg;
   const int comm = d->comm_sms > 0 ? d->comm_sms : 8;
   if (d->ring_bytes > 0) {
@@ -382,17 +381,12 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
                                                                             ring_stamp_offset(rg.n_mb)),
                                       (unsigned long long)reinterpret_cast<uintptr_t>(ctx), st));
   }
-  // 6. grouped GEMM2 (a as hi + lo, or as fp16 against the fp16 W2), fp32 expert outputs (with
-  //    MOK_FLAG_COMBINE_IN_GEMM2: gate-weighted, in assignment order)
-  const bool fused = (d->flags & MOK_FLAG_COMBINE_IN_GEMM2) != 0;
+  // 6. grouped GEMM2 (a as hi + lo, or as fp16 against the fp16 W2), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
              mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm,
-                               gemm_variant(d, GEMM2), w2_f16, fused ? src_of : nullptr,
-                               fused ? at<float>(ctx, L.gate_row) : nullptr, st));
-  // 7. weighted merge in fixed order (fused: the rows are weighted already and a token's k rows
-  //    are contiguous)
-  MOK_LAUNCH("combine", st, mok::launch_combine(o, fused ? nullptr : gates, fused ? nullptr : row_of, T, k, H, nullptr,
-                                                nullptr, nullptr, E, 0, y, n_sm, st));
+                               gemm_variant(d, GEMM2), w2_f16, st));
+  // 7. weighted merge in fixed order
+  MOK_LAUNCH("combine", st, mok::launch_combine(o, gates, row_of, T, k, H, nullptr, nullptr, nullptr, E, 0, y, n_sm, st));
   return MOK_OK;
 }
 

@@ -253,10 +253,9 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
 
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         int variant, bool f16, const int32_t* scatter_src_of, const float* scatter_gate,
-                         cudaStream_t st) {
+                         int variant, bool f16, cudaStream_t st) {
   const bool pair = variant == GEMM_ROWS_PAIR;
-  if ((f16 || scatter_src_of != nullptr) && variant != GEMM_NARROW) return cudaErrorInvalidValue;
+  if (f16 && variant != GEMM_NARROW) return cudaErrorInvalidValue;
   if (variant == GEMM_NARROW) {
     // W2 [E][H][I] K-major, 128-row boxes (one CTA's half of a 256-row weight tile)
     CUtensorMap tw;
@@ -266,11 +265,6 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
     g.K = I;
     g.out0 = out;
     g.ld0 = H;
-    if (scatter_src_of != nullptr) {
-      g.scatter_rows = 1;
-      g.src_of = scatter_src_of;
-      g.gate_row = scatter_gate;
-    }
     if (f16) {
       // fp16 a (one value, 11 significant bits) against an fp16 copy of W2: one MMA per K step
       // (the TMA copies are bitwise: the bf16 maps serve any 16-bit element)

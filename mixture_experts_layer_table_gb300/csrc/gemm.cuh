@@ -88,8 +88,6 @@ struct GemmArgs {
   void* out4;
   long long ld0, ld1, ld2;
   int f16;                  // narrow kernels: the MMA operands are fp16 (else bf16)
-  int scatter_rows;         // narrow fp32 epilogues: row r is stored gate-weighted at row src_of[r]
-                            // (assignment order; gate_row[r] the weight) instead of row r
   int a_f16;                // narrow SwiGLU epilogues: a = silu(h) u stored as one fp16 value in out1
                             // (11 significant bits) instead of a bf16 hi / lo pair
   const float* hu;          // SWIGLU_BWD: saved h | u (fp32)

@@ -446,20 +446,6 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld_32x32b_x32(th + c * 32, v);
             tmem_wait_ld();
             const int nr = min(32, t.rows - c * 32);
-            if (args.scatter_rows) {
-              // the combine's weighting here: row r goes, times its gate, to its assignment's row
-              const int rr = t.row0 + c * 32 + lane;
-              const int a_lane = lane < nr ? args.src_of[rr] : 0;
-              const float g_lane = lane < nr ? args.gate_row[rr] : 0.0f;
-              float* ob = out + j;
-#pragma unroll
-              for (int ii = 0; ii < 32; ++ii) {
-                const int a = __shfl_sync(0xffffffffu, a_lane, ii);
-                const float g = __shfl_sync(0xffffffffu, g_lane, ii);
-                if (jv && ii < nr) ob[(long long)a * args.ld0] = g * __uint_as_float(v[ii]);
-              }
-              continue;
-            }
             if (jv) {
               float* oc = o + (long long)(c * 32) * args.ld0;
               if (nr == 32) {

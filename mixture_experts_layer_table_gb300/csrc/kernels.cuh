@@ -58,8 +58,7 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
                                 void* act_lo, int* status, int n_sm, int variant, bool a_f16, cudaStream_t st);
 cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2, int R, int H, int I, int E,
                          const int32_t* offsets, const int32_t* tile_off, float* out, int* status, int n_sm,
-                         int variant, bool f16, const int32_t* scatter_src_of, const float* scatter_gate,
-                         cudaStream_t st);
+                         int variant, bool f16, cudaStream_t st);
 cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, int I, int E,
                                 const int32_t* offsets, const int32_t* tile_off, const float* hu,
                                 const float* gate_row, void* dhu_hi, void* dhu_lo, void* gact_hi, void* gact_lo,

@@ -129,8 +129,7 @@ __device__ __forceinline__ void acc_f32x8(float (&acc)[8], uint4 a, uint4 b, flo
 // y[t] = sum_{j=0..k-1} w[t][j] * rows[row_of[t*k+j]]  (+ sum over the router support of
 // dl[t][e] * w_router[e] when dl != nullptr), fp32 in the fixed order, rounded to bf16 once.
 // rows are fp32 (expert outputs o, or per-row input gradients dX_g).
-// `w` null means weight 1 (the backward's reverse dispatch of dX rows, or rows already weighted);
-// `row_of` null means the rows are in assignment order (row t*k + j).
+// `w` null means weight 1 (the backward's reverse dispatch of dX rows).
 // Router support: the k selected experts (sparse) or all E experts (dense).
 // One warp per token; each lane handles 8-column chunks (vec_per_row = H / 8).
 template <int KMAX>
@@ -148,7 +147,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
       if (j < k) {
-        rj[j] = row_of ? row_of[(size_t)t * k + j] : t * k + j;
+        rj[j] = row_of[(size_t)t * k + j];
         wj[j] = w ? w[(size_t)t * k + j] : 1.0f;
       }
     }

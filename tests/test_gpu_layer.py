@@ -448,33 +448,3 @@ def test_fp16_w2_refused_with_ring_and_row_tiles():
         with pytest.raises(mok.MokError) as err:
             layer.forward(inp["x"], inp["w_router"], inp["w13"], w2_f16)
         assert err.value.code == 2
-
-
-@pytest.mark.parametrize("shape", [MID, MID_SKEW, LONG], ids=lambda c: c.name)
-def test_combine_in_gemm2(shape):
-    """MOK_FLAG_COMBINE_IN_GEMM2: GEMM2's epilogue stores gate * o at each row's assignment and the
-    merge sums k contiguous rows.  y meets the bar against the oracle, agrees with the default path
-    to a few fp32 roundings, and is bitwise the same on a second run."""
-    inp = W.make_inputs(shape, seed=0, device="cpu")
-    f64 = inputs_f64(inp)
-    given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
-    fwd, _ = oracle_layer(shape, f64, topk_idx=given, backward=False)
-    dev = _gpu_inputs(inp)
-    given_t = torch.tensor(given, dtype=torch.int32, device="cuda")
-    args = (dev["x"], dev["w_router"], dev["w13"], dev["w2"])
-    plain = mok.MoELayer(mok.desc_from_shape(shape))
-    y0 = plain.forward(*args, router_bias=dev["router_bias"], given_topk=given_t)
-    ys = []
-    for _ in range(2):
-        fused = mok.MoELayer(mok.desc_from_shape(shape, flags=mok.FLAG_COMBINE_IN_GEMM2))
-        ys.append(fused.forward(*args, router_bias=dev["router_bias"], given_topk=given_t))
-        torch.cuda.synchronize()
-        assert fused.status() == (0, 0)
-    assert torch.equal(ys[0], ys[1])
-    # the weighted rows in assignment order: row t*k + j is g[t][j] * o[row_of[t*k + j]]
-    rows = to_f64(fused.view("expert_out"))
-    want = fwd["gates"].reshape(-1)[:, None] * fwd["o"][fwd["row_of"].astype(np.int64)]
-    assert_intermediate_close(rows, want, "g * o (assignment order)", rel=1e-3)
-    assert_bf16_close(to_f64(ys[0]), fwd["y"], "y")
-    d = (ys[0].float() - y0.float()).abs().max().item()
-    assert d <= 2.0 ** -6 * float(y0.float().abs().max()), d
