@@ -871,7 +871,7 @@ def run_ring_sweep(args):
             "value": best["tokens_per_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": best["fwd_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
-            "config": {"workload": shp.name, "ring_bytes": W.RING_BYTES, "comm_sms": 8, "passes": "fwd",
+            "config": {"workload": shp.name, "ring_bytes": W.RING_BYTES, "comm_sms": 12, "passes": "fwd",
                        "expert_gemm": args.gemm,
                        "min_minibatch_two_waves": mok.min_minibatch(0, shp.I)},
             "plain_forward_ms": round(plain_ms, 4), "plain_forward_kernels": kernels,

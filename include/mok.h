@@ -94,7 +94,9 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                operands, one MMA per K step instead of two.  Default GEMM kernels and no
  *                ring only (else MOK_ERR_UNSUPPORTED); mok_moe_backward ignores the flag and
  *                takes w2 in bf16 (the backward does not read a).
- *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 8)
+ *   comm_sms     ring forward: CTAs (one per SM) that gather rows (0 = 12); even when GEMM1
+ *                runs on the narrow-segment CTA-pair kernel (the default), since those
+ *                CTAs are launched in clusters of two
  * T*k*max(H, 2I) must stay below 2^31 elements. */
 #define MOK_FLAG_WGRAD_BF16 1
 #define MOK_FLAG_GEMM_PAIR 2

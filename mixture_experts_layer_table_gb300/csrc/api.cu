@@ -302,11 +302,13 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   const bool w2_f16 = (d->flags & MOK_FLAG_W2_F16) != 0;
   if (w2_f16 && (d->ring_bytes > 0 || gemm_variant(d, GEMM2) != mok::GEMM_NARROW)) return MOK_ERR_UNSUPPORTED;
   RingGeom rg;
-  const int comm = d->comm_sms > 0 ? d->comm_sms : 8;
+  const int comm = d->comm_sms > 0 ? d->comm_sms : 12;
   if (d->ring_bytes > 0) {
     s = ring_geometry(d, &rg);
     if (s != MOK_OK) return s;
     if (comm >= n_sm) return MOK_ERR_INVALID_ARG;
+    // the CTA-pair ring kernel takes its gathering CTAs in whole clusters of two
+    if (gemm_variant(d, GEMM1) == mok::GEMM_NARROW && comm % 2 != 0) return MOK_ERR_INVALID_ARG;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = d->T, H = d->H, I = d->I, E = d->E, k = d->k, R = T * k;
@@ -349,8 +351,10 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     int32_t* mb_tiles = mb_toff + (size_t)rg.n_mb * (E + 1);
     int32_t* mb_start = mb_tiles + rg.n_mb;
     int32_t* counters = at<int32_t>(ws, L.mb_counters);
+    const int ring_variant = gemm_variant(d, GEMM1);
     MOK_LAUNCH("ring_tables", st,
-               mok::launch_mb_tables(offsets, E, R, rg.m, rg.n_mb, I / 128, mb_off, mb_toff, mb_tiles, mb_start, st));
+               mok::launch_mb_tables(offsets, E, R, rg.m, rg.n_mb, I / 128, mok::ring_chunk_rows(ring_variant), mb_off,
+                                     mb_toff, mb_tiles, mb_start, st));
     MOK_CUDA(cudaMemsetAsync(counters, 0, sizeof(int32_t) * 2 * rg.n_mb, st));
     mok::RingArgs ra;
     ra.x = x;
@@ -373,7 +377,8 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     ra.mb_start = mb_start;
     ra.gathered = counters;
     ra.consumed = counters + rg.n_mb;
-    MOK_LAUNCH("ring_gemm1_swiglu", st, mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, st));
+    MOK_LAUNCH("ring_gemm1_swiglu", st,
+               mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, ring_variant, st));
     // the ring rows are this forward's (the backward reuses them when it is given this ws)
     MOK_LAUNCH("ring_stamp", st,
                mok::launch_ring_stamp(at<unsigned long long>(ctx, L.ring_stamp),

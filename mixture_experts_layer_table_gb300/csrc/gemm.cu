@@ -425,8 +425,92 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   return out_f32 ? run(wgrad_kernel<false, true>) : run(wgrad_kernel<false, false>);
 }
 
+// Ring GEMM1 on the narrow-segment CTA-pair kernel: chunks of at most 256 rows of each expert's
+// segment in a minibatch, 128 intermediate indices (64 gate + 64 up rows per CTA) per pair tile.
+constexpr int RING_NARROW_NMAX = 256;
+
+int ring_chunk_rows(int variant) { return variant == GEMM_NARROW ? RING_NARROW_NMAX : BM; }
+
+namespace {
+
+cudaError_t launch_ring_gemm1_narrow(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
+                                     int* status, int n_sm, cudaStream_t st) {
+  using C = NarrowCfg<false, false, RING_NARROW_NMAX, EPI_SWIGLU>;
+  static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
+  const uint64_t ring_rows = (uint64_t)ra.ring_slots * ra.mb_rows;
+  CUtensorMap tw, tx, txs;
+  if (!tmap_w13_gate_up(&tw, w13, ra.H, ra.I, ra.E, 64) || !tmap_2d(&tx, ra.ring, ra.H, ring_rows, BK, NARROW_XBOX) ||
+      !tmap_2d(&txs, ra.ring, ra.H, ring_rows, BK, NARROW_XBOX_S))
+    return cudaErrorInvalidValue;
+  // whole clusters of gathering CTAs, at least one pair of GEMM CTAs
+  if (ra.comm_ctas < 2 || ra.comm_ctas % 2 != 0 || ra.comm_ctas + 2 > n_sm) return cudaErrorInvalidValue;
+  GemmArgs g = base_args(ra.E, nullptr, nullptr, status);
+  g.N = ra.I;
+  g.K = ra.H;
+  g.I = ra.I;
+  g.out0 = hu;
+  g.ld0 = 2LL * ra.I;
+  g.out1 = act_hi;
+  g.out2 = act_lo;
+  g.ld1 = ra.I;
+  g.comm_ctas = ra.comm_ctas;
+  g.n_mb = ra.n_mb;
+  g.mb_rows = ra.mb_rows;
+  g.ring_slots = ra.ring_slots;
+  g.ring_shift = ra.ring_shift;
+  g.R = ra.R;
+  g.k_top = ra.k;
+  g.H = ra.H;
+  g.mb_off = ra.mb_off;
+  g.mb_toff = ra.mb_toff;
+  g.mb_start = ra.mb_start;
+  g.gathered = ra.gathered;
+  g.consumed = ra.consumed;
+  g.consume_per_tile = 8;  // four epilogue warps in each CTA of the pair
+  g.x = reinterpret_cast<const __nv_bfloat16*>(ra.x);
+  g.src_of = ra.src_of;
+  g.ring = reinterpret_cast<__nv_bfloat16*>(ra.ring);
+  auto kern = gemm_narrow_kernel<false, false, RING_NARROW_NMAX, EPI_SWIGLU, true>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
+  if (err != cudaSuccess) return err;
+  // gathering and GEMM CTAs wait on each other: the launch is cooperative (all CTAs resident at
+  // once), in clusters of two, one CTA per SM
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::smem_bytes(ra.E);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  static int max_clusters[64] = {0};  // co-resident clusters of this kernel, per device
+  int dev = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    cfg.gridDim = dim3(2 * std::max(1, n_sm / 2), 1, 1);
+    int clusters = 0;
+    if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
+    max_clusters[dev] = std::max(1, clusters);
+  }
+  const int pairs = max_clusters[dev] - ra.comm_ctas / 2;
+  if (pairs < 1) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3(ra.comm_ctas + 2 * pairs, 1, 1);
+  err = cudaLaunchKernelEx(&cfg, kern, tw, tx, tx, txs, txs, g);
+  if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
-                              int* status, int n_sm, cudaStream_t st) {
+                              int* status, int n_sm, int variant, cudaStream_t st) {
+  if (variant == GEMM_NARROW) return launch_ring_gemm1_narrow(ra, w13, hu, act_hi, act_lo, status, n_sm, st);
   using C = GemmCfg<MODE_RING, EPI_SWIGLU, SPLIT_NONE, 256>;
   CUtensorMap ta, tb;
   const uint64_t ring_rows = (uint64_t)ra.ring_slots * ra.mb_rows;
@@ -455,6 +539,7 @@ cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, vo
   g.mb_start = ra.mb_start;
   g.gathered = ra.gathered;
   g.consumed = ra.consumed;
+  g.consume_per_tile = 4;  // the four epilogue warps of the CTA
   g.x = reinterpret_cast<const __nv_bfloat16*>(ra.x);
   g.src_of = ra.src_of;
   g.ring = reinterpret_cast<__nv_bfloat16*>(ra.ring);

@@ -106,7 +106,8 @@ struct GemmArgs {
   const int* mb_toff;       // [n_mb][E+1] prefix of m-tiles inside each minibatch
   const int* mb_start;      // [n_mb+1] first tile of each minibatch
   int* gathered;            // [n_mb] rows gathered
-  int* consumed;            // [n_mb] epilogue warps finished (4 per tile)
+  int* consumed;            // [n_mb] epilogue warps finished (consume_per_tile per tile)
+  int consume_per_tile;     // epilogue warps counting out one tile (4, or 8 for a CTA pair)
   const __nv_bfloat16* x;   // [T][H] tokens
   const int* src_of;        // [R]
   __nv_bfloat16* ring;      // [ring_slots * mb_rows][H]
@@ -552,57 +553,151 @@ __device__ __forceinline__ void epi_swiglu_bwd_cols(uint32_t tacc, long long row
   }
 }
 
-// Gathering role of the ring forward (the pull dispatch): one thread of each of the first
-// comm_ctas CTAs moves its share of each minibatch's rows (row i of the minibatch goes to CTA
-// i % comm_ctas) from the token matrix into the minibatch's ring slot with bulk async copies
-// through shared memory: up to `ns` rows are in flight, a row's staging buffer is refilled as
-// soon as the store of the row before it has left shared memory.  When the CTA's rows of a
-// minibatch are in the ring it publishes their count.  A ring slot is overwritten only after
-// every GEMM tile of the minibatch that held it has finished.
+// Gathering role of the ring forward (the pull dispatch): each of the first comm_ctas CTAs moves
+// its share of each minibatch's rows (row i of the minibatch goes to CTA i % comm_ctas) from the
+// token matrix into the minibatch's ring slot.  One SM moves rows on two paths at once, each of
+// them bound by the latency of its copies in flight: warp 0 stages rows through shared memory
+// with bulk async copies (lane 0 issues them, up to `ns` rows in flight; a row's staging buffer is
+// refilled as soon as the store of the row before it has left it; the warp reads the rows' token
+// indices 32 at a time, one window ahead), and the other warps copy rows through registers, one
+// row per warp at a time, 16 bytes per lane and load.  Of every GATHER_PERIOD consecutive rows of
+// the CTA, the first GATHER_BULK take the bulk path.  When the CTA's rows of a minibatch are in
+// the ring it publishes their count.  A ring slot is overwritten only after every GEMM tile of the
+// minibatch that held it has finished.
+constexpr int GATHER_PERIOD = 9;
+constexpr int GATHER_BULK = 4;
+
+__device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src, uint4* __restrict__ dst, int vec,
+                                              int lane) {
+  constexpr int U = 16;
+  for (int c = lane; c < vec; c += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (c + u * 32 < vec) v[u] = __ldg(src + c + u * 32);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (c + u * 32 < vec) dst[c + u * 32] = v[u];
+  }
+}
+
 __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint64_t* bars) {
-  if (threadIdx.x != 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int copy_warps = (int)(blockDim.x >> 5) - 1;  // warps 1.. copy through registers
   const uint32_t row_bytes = (uint32_t)a.H * 2;
   int ns = buf_bytes / (int)row_bytes;
   if (ns > 16) ns = 16;
-  for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&bars[j]), 1);
-  fence_mbar_init();
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&bars[j]), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   volatile int no_abort = 0;
-  long long gcount = 0;  // rows this CTA has staged so far (slot = gcount % ns, parity = gcount / ns)
-  auto issue_load = [&](long long g, int r) {
-    const int j = (int)(g % ns);
-    const int tok = a.src_of[r] / a.k_top;
-    mbar_arrive_expect_tx(smem_u32(&bars[j]), row_bytes);
-    bulk_load_g2s(smem_u32(buf + (size_t)j * row_bytes), a.x + (size_t)tok * a.H, row_bytes, smem_u32(&bars[j]));
-  };
+  long long gcount = 0;  // bulk rows this CTA has staged so far (slot = gcount % ns, parity = gcount / ns)
+  long long issued = 0;  // bulk rows whose load has been issued
   for (int mb = 0; mb < a.n_mb; ++mb) {
     const int slot = (mb + a.ring_shift) % a.ring_slots;
     const int r0 = mb * a.mb_rows;
     const int rows = min(a.mb_rows, a.R - r0);
-    if (mb >= a.ring_slots) {
+    int ok = 1;
+    if (mb >= a.ring_slots && threadIdx.x == 0) {
       const int old = mb - a.ring_slots;
-      if (!wait_counter(&a.consumed[old], 4 * (a.mb_start[old + 1] - a.mb_start[old]), a.status, SITE_RING_WAIT))
-        return;
+      ok = wait_counter(&a.consumed[old], a.consume_per_tile * (a.mb_start[old + 1] - a.mb_start[old]), a.status,
+                        SITE_RING_WAIT);
     }
+    if (__syncthreads_or(!ok)) return;
     const int cnt = rows > (int)blockIdx.x ? (rows - (int)blockIdx.x + a.comm_ctas - 1) / a.comm_ctas : 0;
-    for (int t = 0; t < cnt && t < ns; ++t) issue_load(gcount + t, r0 + (int)blockIdx.x + t * a.comm_ctas);
-    for (int t = 0; t < cnt; ++t) {
-      const long long g = gcount + t;
-      const int j = (int)(g % ns);
-      if (!mbar_wait(smem_u32(&bars[j]), (uint32_t)((g / ns) & 1), &no_abort, a.status, SITE_RING_WAIT)) return;
-      const int i = (int)blockIdx.x + t * a.comm_ctas;
-      bulk_store_s2g(a.ring + ((size_t)slot * a.mb_rows + i) * a.H, smem_u32(buf + (size_t)j * row_bytes), row_bytes);
-      bulk_commit_group();
-      // the staging buffer of row t-1 takes row t-1+ns once that row's store has read it
-      if (t >= 1 && t - 1 + ns < cnt) {
-        bulk_wait_group_read<1>();
-        issue_load(g - 1 + ns, r0 + (int)blockIdx.x + (t - 1 + ns) * a.comm_ctas);
+    const int full = cnt / GATHER_PERIOD, rest = cnt % GATHER_PERIOD;
+    const int n_bulk = full * GATHER_BULK + min(rest, GATHER_BULK);
+    // the minibatch row of this CTA's q-th bulk / q-th register-copied row
+    auto bulk_row = [&](int q) {
+      return (int)blockIdx.x + ((q / GATHER_BULK) * GATHER_PERIOD + q % GATHER_BULK) * a.comm_ctas;
+    };
+    auto copy_row = [&](int q) {
+      constexpr int NC = GATHER_PERIOD - GATHER_BULK;
+      return (int)blockIdx.x + ((q / NC) * GATHER_PERIOD + GATHER_BULK + q % NC) * a.comm_ctas;
+    };
+    bool fail = false;
+    if (warp == 0) {
+      // token of the q-th bulk row: lane l holds rows base + l (cur) and base + 32 + l (nxt); q
+      // only grows within a minibatch
+      auto load_tok = [&](int q) {
+        const int qq = q + lane;
+        return qq < n_bulk ? a.src_of[r0 + bulk_row(qq)] / a.k_top : 0;
+      };
+      int base = 0;
+      int cur = load_tok(0), nxt = load_tok(32);
+      auto tok_at = [&](int q) {
+        while (q >= base + 32) {
+          base += 32;
+          cur = nxt;
+          nxt = load_tok(base + 32);
+        }
+        return __shfl_sync(0xffffffffu, cur, q - base);
+      };
+      auto issue_load = [&](long long g, int q) {
+        const int tok = tok_at(q);
+        if (lane == 0) {
+          const int j = (int)(g % ns);
+          mbar_arrive_expect_tx(smem_u32(&bars[j]), row_bytes);
+          bulk_load_g2s(smem_u32(buf + (size_t)j * row_bytes), a.x + (size_t)tok * a.H, row_bytes,
+                        smem_u32(&bars[j]));
+        }
+        issued = g + 1;
+      };
+      for (int q = 0; q < n_bulk && q < ns; ++q) issue_load(gcount + q, q);
+      for (int q = 0; q < n_bulk; ++q) {
+        const long long g = gcount + q;
+        const int j = (int)(g % ns);
+        int w_ok = 1;
+        if (lane == 0) {
+          w_ok = mbar_wait(smem_u32(&bars[j]), (uint32_t)((g / ns) & 1), &no_abort, a.status, SITE_RING_WAIT);
+          if (w_ok) {
+            bulk_store_s2g(a.ring + ((size_t)slot * a.mb_rows + bulk_row(q)) * a.H,
+                           smem_u32(buf + (size_t)j * row_bytes), row_bytes);
+            bulk_commit_group();
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          if (lane == 0) {
+            // gave up: let the copies in flight land before the CTA leaves (bounded waits)
+            bulk_wait_group_all();
+            for (long long r = g; r < issued; ++r)
+              mbar_wait(smem_u32(&bars[r % ns]), (uint32_t)((r / ns) & 1), &no_abort, a.status, SITE_RING_WAIT,
+                        1000000ull);
+          }
+          fail = true;
+          break;
+        }
+        // the staging buffer of row q-1 takes row q-1+ns once that row's store has read it
+        if (q >= 1 && q - 1 + ns < n_bulk) {
+          if (lane == 0) bulk_wait_group_read<1>();
+          __syncwarp();
+          issue_load(g - 1 + ns, q - 1 + ns);
+        }
       }
+      gcount += n_bulk;
+      if (!fail && lane == 0) {
+        bulk_wait_group_all();  // the bulk rows are in the ring
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+    } else {
+      const int vec = a.H / 8;  // 16-byte words of a row
+      for (int q = warp - 1; q < cnt - n_bulk; q += copy_warps) {
+        const int i = copy_row(q);
+        const int tok = a.src_of[r0 + i] / a.k_top;
+        copy_row_warp(reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H),
+                      reinterpret_cast<uint4*>(a.ring + ((size_t)slot * a.mb_rows + i) * a.H), vec, lane);
+      }
+      __threadfence();
     }
-    gcount += cnt;
-    bulk_wait_group_all();  // this CTA's rows of the minibatch are in the ring
-    fence_proxy_async_global();
-    __threadfence();
-    if (cnt > 0) atomicAdd(&a.gathered[mb], cnt);
+    if (__syncthreads_or(fail)) return;
+    if (threadIdx.x == 0) {
+      // every row of this CTA's share is in the ring: publish the count
+      __threadfence();
+      if (cnt > 0) atomicAdd(&a.gathered[mb], cnt);
+    }
   }
 }
 

@@ -79,7 +79,14 @@ struct NarrowCfg {
 
 // tmX / tmX2: X hi / lo in 64-row boxes; tmXs / tmX2s: the same in 32-row boxes.  tmW (SwiGLU):
 // W13 seen as [E][2][I][H], one box = 64 gate rows and their 64 up rows.
-template <bool WMN, bool SPLIT, int NMAX, int EPI>
+//
+// RING (GEMM1 of the ring forward): X is the token ring [slots * mb_rows][H].  The first
+// args.comm_ctas CTAs (an even number, whole clusters) gather minibatch after minibatch into the
+// ring (ring_gather, as in gemm.cuh); the CTA pairs run the narrow tiles of each minibatch's
+// expert segments (args.mb_off / mb_toff: row offsets and chunk prefixes per minibatch,
+// args.mb_start: the tiles before each minibatch), wait for a minibatch's rows before loading
+// them, and count each tile's epilogue warps out on args.consumed so that the slot can be refilled.
+template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
@@ -97,11 +104,16 @@ __global__ void __launch_bounds__(192, 1)
   int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + 256);
   int* s_coff = s_off + (args.E + 1);
 
+  if (RING && (int)blockIdx.x < args.comm_ctas) {
+    ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
+    return;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
-  const int pair = (int)blockIdx.x >> 1;
-  const int npairs = (int)gridDim.x >> 1;
+  const int cta0 = RING ? args.comm_ctas : 0;
+  const int pair = ((int)blockIdx.x - cta0) >> 1;
+  const int npairs = ((int)gridDim.x - cta0) >> 1;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
@@ -121,9 +133,11 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = args.offsets[i];
+  // the whole layer's segments and chunk prefixes (RING decodes through the minibatch tables)
+  if (!RING)
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = args.offsets[i];
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (!RING && threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < args.E; ++e) {
       s_coff[e] = acc;
@@ -142,8 +156,29 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int MT = C::m_tiles(args);
-  const int total = s_coff[args.E] * MT;
+  const int total = RING ? args.mb_start[args.n_mb] : s_coff[args.E] * MT;
   const int nkb = args.K / BK;
+  // Tile g.  RING: the minibatch mb holding it, the tile decoded inside it, its rows' position in the
+  // ring (ring_row0) and its rows' position in the outputs (t.row0, all rows of the layer).
+  auto decode = [&](int g, int& mb, int& ring_row0) -> NarrowTile {
+    if (!RING) {
+      mb = 0;
+      const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+      ring_row0 = t.row0;
+      return t;
+    }
+    int lo = 0, hi = args.n_mb;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (args.mb_start[mid] <= g) lo = mid; else hi = mid;
+    }
+    mb = lo;
+    NarrowTile t = decode_narrow_tile(g - args.mb_start[lo], MT, args.E, C::NMAX,
+                                      args.mb_off + (size_t)lo * (args.E + 1), args.mb_toff + (size_t)lo * (args.E + 1));
+    ring_row0 = ((lo + args.ring_shift) % args.ring_slots) * args.mb_rows + t.row0;
+    t.row0 += lo * args.mb_rows;
+    return t;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -163,13 +198,26 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
+      int ring_ready = -1;  // RING: last minibatch known to be gathered
       for (int g = pair; g < total && ok; g += npairs) {
-        const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+        int mb, ring_row0;
+        const NarrowTile t = decode(g, mb, ring_row0);
+        if (RING && mb > ring_ready) {
+          // the minibatch's rows must be in the ring before the first load of its tiles
+          const int rows_mb = min(args.mb_rows, args.R - mb * args.mb_rows);
+          if (!wait_counter(&args.gathered[mb], rows_mb, args.status, SITE_RING_WAIT)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          ring_ready = mb;
+        }
         const int half = t.n >> 1;                      // rows of this CTA's half of N
         int n64;
         bool with32;
         const int xrows = narrow_x_boxes(half, n64, with32);  // <= NMAX / 2: fits the X buffer
-        const int x_row = t.row0 + (int)rank * half;
+        const int x_row = ring_row0 + (int)rank * half;
         const int w_row = t.m * C::PM + 128 * (int)rank;
         const uint32_t pair_tx = 2u * (C::A_BYTES + C::X_OPS * xrows * 128);
         const uint64_t pol_w = t.nc > 1 ? pol_shared : pol_once;
@@ -259,7 +307,8 @@ __global__ void __launch_bounds__(192, 1)
       bool any_mma = false;
       const uint32_t a_lbo = WMN ? MOK_MN_LBO : 16, a_sbo = WMN ? MOK_MN_SBO : 1024;
       for (int g = pair; g < total && ok; g += npairs) {
-        const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+        int mb_unused, rr_unused;
+        const NarrowTile t = decode(g, mb_unused, rr_unused);
         uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
         if (args.f16) idesc &= ~((1u << 7) | (1u << 10));  // A and B formats: fp16 instead of bf16
         int w_ok = 1;
@@ -330,7 +379,8 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int g = pair; g < total; g += npairs) {
-      const NarrowTile t = decode_narrow_tile(g, MT, args.E, C::NMAX, s_off, s_coff);
+      int mb, rr_unused;
+      const NarrowTile t = decode(g, mb, rr_unused);
       int w_ok = 1;
       if (lane == 0)
         w_ok = mbar_wait<true>(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL,
@@ -463,6 +513,9 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty0_cl + 8u * acc);
+      // RING: this warp is done with the tile (its MMAs have read the rows): once every epilogue
+      // warp of every tile of the minibatch has counted in, its ring slot may be refilled
+      if (RING && lane == 0) atomicAdd(&args.consumed[mb], 1);
       acc = (acc + 1) % C::ACCS;
       if (acc == 0) acc_phase ^= 1;
     }

@@ -22,7 +22,7 @@ cudaError_t launch_router_dlogits(const float* dg_part, int n_part, const int32_
                                   const int32_t* topk_idx, const float* gates, const float* scores, int T,
                                   int E, int k, int router, int renorm, float route_scale, float* dgates,
                                   float* dl, cudaStream_t st);
-cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int32_t* mb_off,
+cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int tile_rows, int32_t* mb_off,
                              int32_t* mb_toff, int32_t* mb_tiles, int32_t* mb_start, cudaStream_t st);
 cudaError_t launch_router_wgrad(const float* dl, const void* x, const int32_t* offsets, const int32_t* src_of,
                                 int T, int H, int E, int k, int sparse, float* dw, cudaStream_t st);
@@ -94,8 +94,11 @@ struct RingArgs {
   int32_t* gathered;
   int32_t* consumed;
 };
+// variant GEMM_NARROW: the narrow-segment CTA-pair kernel (minibatch tables in chunks of
+// ring_chunk_rows() rows); else the row-tile kernel (128-row tiles)
+int ring_chunk_rows(int variant);
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
-                              int* status, int n_sm, cudaStream_t st);
+                              int* status, int n_sm, int variant, cudaStream_t st);
 // MXFP8 weights (mx.cu)
 // w [E][N][K] bf16 -> q [E][N][K] E4M3 and 512-byte scale blocks; gate_up_I > 0 (W13, N = 2I):
 // the blocks of 128 rows pair 64 gate rows with the 64 up rows of the same intermediate indices.

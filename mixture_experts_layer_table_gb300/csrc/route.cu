@@ -547,10 +547,10 @@ __global__ void __launch_bounds__(256)
 // ----------------------------------------------------------------------------- ring tables
 // Minibatch mb holds the sorted rows [mb*m, mb*m + rows_mb).  One CTA per minibatch (threads
 // over experts) cuts the expert segments at its edges: mb_off[mb][e] = clamp(offsets[e] - r0,
-// 0, rows_mb), and scans the 128-row tiles of each cut segment into mb_toff[mb][e];
-// mb_tiles[mb] = total tiles * n_tiles (the column tiles of GEMM1).
+// 0, rows_mb), and scans the chunks of at most tile_rows rows of each cut segment into mb_toff[mb][e];
+// mb_tiles[mb] = total chunks * n_tiles (the column tiles of GEMM1).
 __global__ void __launch_bounds__(1024)
-    mb_tables_kernel(const int32_t* __restrict__ offsets, int E, int R, int m, int n_tiles,
+    mb_tables_kernel(const int32_t* __restrict__ offsets, int E, int R, int m, int n_tiles, int tile_rows,
                      int32_t* __restrict__ mb_off, int32_t* __restrict__ mb_toff, int32_t* __restrict__ mb_tiles) {
   __shared__ int warp_tot[32];
   const int mb = blockIdx.x;
@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(1024)
   if (e < E) {
     const int lo = min(max(offsets[e] - r0, 0), rows);
     const int hi = min(max(offsets[e + 1] - r0, 0), rows);
-    tiles = (hi - lo + 127) / 128;
+    tiles = (hi - lo + tile_rows - 1) / tile_rows;
     mb_off[(size_t)mb * (E + 1) + e] = lo;
   }
   if (e == 0) mb_off[(size_t)mb * (E + 1) + E] = min(max(offsets[E] - r0, 0), rows);
@@ -606,9 +606,9 @@ __global__ void mb_start_kernel(const int32_t* __restrict__ mb_tiles, int n_mb, 
 }
 
 // ----------------------------------------------------------------------------- launchers
-cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int32_t* mb_off,
+cudaError_t launch_mb_tables(const int32_t* offsets, int E, int R, int m, int n_mb, int n_tiles, int tile_rows, int32_t* mb_off,
                              int32_t* mb_toff, int32_t* mb_tiles, int32_t* mb_start, cudaStream_t st) {
-  mb_tables_kernel<<<n_mb, 1024, 0, st>>>(offsets, E, R, m, n_tiles, mb_off, mb_toff, mb_tiles);
+  mb_tables_kernel<<<n_mb, 1024, 0, st>>>(offsets, E, R, m, n_tiles, tile_rows, mb_off, mb_toff, mb_tiles);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   mb_start_kernel<<<1, 32, 0, st>>>(mb_tiles, n_mb, mb_start);

@@ -325,23 +325,29 @@ def test_stuck_wait_times_out_and_context_survives():
 
 # ----------------------------------------------------------------------------- ring forward
 
-@pytest.mark.parametrize("shape,minibatch,slots,comm", [
-    (MID, 300, 2, 4),        # ragged minibatches (not a multiple of 128), the ring wraps 4 times
-    (MID, 1024, 1, 8),       # one slot: gathering and GEMM1 alternate
-    (MID_SKEW, 700, 3, 2),   # skewed experts cut at minibatch edges
-    (TINY, 96, 2, 3),        # tiny layer, softmax router
+@pytest.mark.parametrize("shape,minibatch,slots,comm,flags", [
+    (MID, 300, 2, 4, 0),        # ragged minibatches (not a multiple of 128), the ring wraps 4 times
+    (MID, 1024, 1, 8, 0),       # one slot: gathering and GEMM1 alternate
+    (MID_SKEW, 700, 3, 2, 0),   # skewed experts cut at minibatch edges
+    (TINY, 96, 2, 2, 0),        # tiny layer, softmax router
+    (LONG, 3000, 2, 6, 0),      # 750 rows per expert: chunks of up to 256 rows cut at minibatch edges
+    (MID, 300, 2, 3, "single"),  # the row-tile ring kernel (one CTA per 128-row tile), odd comm count
+    (MID_SKEW, 700, 2, 4, "pair"),  # the row-tile ring kernel under the CTA-pair flag
 ], ids=lambda v: getattr(v, "name", str(v)))
-def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm):
+def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm, flags):
     """The ring forward (persistent launch: gathering CTAs fill ring slots while GEMM CTAs run
-    GEMM1 on earlier minibatches) computes every row exactly as the plain forward does, so y,
-    h|u and a must be bitwise equal; the backward after a ring forward must match too."""
+    GEMM1 on earlier minibatches; GEMM1 on the narrow-segment CTA-pair kernel by default, on the
+    row-tile kernel under the row-tile flags) computes every row exactly as the plain forward does,
+    so y, h|u and a must be bitwise equal; the backward after a ring forward must match too."""
+    flags = {0: 0, "single": mok.FLAG_GEMM_SINGLE, "pair": mok.FLAG_GEMM_PAIR}[flags]
     inp = W.make_inputs(shape, seed=0, device="cpu")
     dev = _gpu_inputs(inp)
-    plain = mok.MoELayer(mok.desc_from_shape(shape))
+    plain = mok.MoELayer(mok.desc_from_shape(shape, flags=flags))
     y0 = plain.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"])
     g0 = plain.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
     ring_bytes = slots * minibatch * shape.H * 2
-    ring = mok.MoELayer(mok.desc_from_shape(shape, minibatch=minibatch, ring_bytes=ring_bytes, comm_sms=comm))
+    ring = mok.MoELayer(mok.desc_from_shape(shape, minibatch=minibatch, ring_bytes=ring_bytes, comm_sms=comm,
+                                            flags=flags))
     assert ring.layout["ring"] >= 0
     for _ in range(2):  # the second call reuses the ring and the counters
         y1 = ring.forward(dev["x"], dev["w_router"], dev["w13"], dev["w2"], router_bias=dev["router_bias"])
@@ -401,6 +407,17 @@ def test_ring_rejects_a_ring_smaller_than_one_minibatch():
     with pytest.raises(mok.MokError) as info:
         mok.get_layout(desc)
     assert info.value.code == 2
+
+
+def test_ring_rejects_an_odd_comm_count_on_the_pair_kernel():
+    """The narrow-segment ring kernel launches its gathering CTAs in clusters of two: an odd
+    comm_sms is an invalid argument there (and fine on the row-tile kernel, covered above)."""
+    shape = MID
+    inp = _gpu_inputs(W.make_inputs(shape, seed=0, device="cpu", with_dy=False))
+    layer = mok.MoELayer(mok.desc_from_shape(shape, minibatch=300, ring_bytes=600 * shape.H * 2, comm_sms=3))
+    with pytest.raises(mok.MokError) as info:
+        layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    assert info.value.code == 1
 
 
 # ----------------------------------------------------------------------------- fp16 W2 (MOK_FLAG_W2_F16)
