@@ -60,8 +60,11 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
 
 /* Layer descriptor.
  *   T       tokens of this call, 1 <= T
- *   H       hidden width; multiple of 256
- *   I       expert intermediate width; multiple of 256
+ *   H       hidden width; multiple of 128 (MOK_ERR_UNSUPPORTED otherwise)
+ *   I       expert intermediate width; multiple of 128 (MOK_ERR_UNSUPPORTED otherwise).
+ *           128 is one CTA's share of a CTA pair's 256-row weight tile and the K step of
+ *           the MXFP8 kernels; where H or I is an odd multiple of 128 the last pair tile
+ *           reads zeros past the end and stores nothing there
  *   E       routed experts, 1 <= E <= 1024
  *   k       experts per token, 1 <= k <= min(E, 16)
  *   router  mok_router_kind: softmax over E logits, or elementwise sigmoid
@@ -146,7 +149,7 @@ typedef struct {
   int64_t gact;       /* bf16 [T*k][I]  gate * a, operand of dW2, hi part (backward) */
   int64_t gact_lo;    /* bf16 [T*k][I]  lo part */
   int64_t dx_g;       /* f32 [T*k][H]   per-row input gradient (backward) */
-  int64_t dg_part;    /* f32 [T*k][I/128] partial gate gradients per GEMM column tile (bf16: I/256 used) */
+  int64_t dg_part;    /* f32 [T*k][I/128] partial gate gradients per GEMM column tile (bf16: ceil(I/256) used) */
   int64_t dlogits;    /* f32 [T][E]   router logit gradient (backward) */
   /* ring forward only (-1 otherwise) */
   int64_t ring;       /* bf16 [n_mb * minibatch][H]  the dispatched rows of every minibatch: the

@@ -42,7 +42,9 @@ mok_status check_desc(const mok_layer_desc* d) {
   if (!std::isfinite(d->route_scale)) return MOK_ERR_INVALID_ARG;
   if (d->minibatch < 0 || d->ring_bytes < 0) return MOK_ERR_INVALID_ARG;
   if ((d->flags & MOK_FLAG_GEMM_PAIR) && (d->flags & MOK_FLAG_GEMM_SINGLE)) return MOK_ERR_INVALID_ARG;
-  if (d->H % 256 != 0 || d->I % 256 != 0) return MOK_ERR_UNSUPPORTED;
+  // 128: one CTA's weight rows (half a CTA pair's 256-row tile) and the MXFP8 kernels' K step; a
+  // pair tile over H or I that reaches past the end reads zeros there and stores none of it
+  if (d->H % 128 != 0 || d->I % 128 != 0) return MOK_ERR_UNSUPPORTED;
   if (d->E > 1024 || d->k > 16) return MOK_ERR_UNSUPPORTED;
   const int64_t R = int64_t(d->T) * d->k;
   const int64_t width = d->H > 2 * d->I ? d->H : 2 * int64_t(d->I);
@@ -661,7 +663,7 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
                                                 wgrad_pairs(d), n_sm,
                                                 st));
   // 6. gate and router-logit gradients, 7. router weight gradient
-  MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, I / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
+  MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, (I + 255) / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
                                       d->renorm, d->route_scale, dgates, dl, st));
   MOK_LAUNCH("router_wgrad", st, mok::launch_router_wgrad(dl, x, offsets, src_of, T, H, E, k, d->router == MOK_ROUTER_SIGMOID ? 1 : 0,
                                     dw_router, st));

@@ -206,7 +206,7 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
   if (variant == GEMM_NARROW) {
     // W13[e] as [2][I][H]: each CTA takes 64 gate rows and their 64 up rows in one box (128 and
     // 128 in the paired form, at >= 384 rows per expert)
-    const bool paired = (long long)R >= 384LL * E;
+    const bool paired = (long long)R >= 384LL * E && I % 256 == 0;  // whole 256-index tiles
     CUtensorMap tw;
     if (!tmap_w13_gate_up(&tw, w13, H, I, E, paired ? 128 : 64)) return cudaErrorInvalidValue;
     GemmArgs g = base_args(E, offsets, tile_off, status);
@@ -291,7 +291,7 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
   if (pair)
     return launch_pair<EPI_F32, SPLIT_A>(ta, ta2, tb, to, to, to, g, pair_tiles_bound(R, E) * ((H + 255) / 256), n_sm,
                                          st);
-  const int bound = row_tiles_bound(R, E) * (H / 256);
+  const int bound = row_tiles_bound(R, E) * ((H + 255) / 256);
   return launch<MODE_ROWS, EPI_F32, SPLIT_A, 256>(ta, ta2, tb, tb, g, std::min(bound, n_sm), st, &to);
 }
 
@@ -313,10 +313,10 @@ cudaError_t launch_dgrad_swiglu(const void* dy_g, const void* w2, int R, int H, 
   g.out3 = gact_lo;
   g.ld1 = I;
   g.out4 = dg_part;
-  g.ld2 = I / 256;
+  g.ld2 = (I + 255) / 256;  // one partial per 256-column tile (the last may hold 128)
   g.hu = hu;
   g.gate_row = gate_row;
-  const int bound = row_tiles_bound(R, E) * (I / 256);
+  const int bound = row_tiles_bound(R, E) * ((I + 255) / 256);
   return launch<MODE_DGRAD, EPI_SWIGLU_BWD, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(bound, n_sm), st);
 }
 
@@ -348,7 +348,7 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
   g.K = 2 * I;
   g.out0 = dx_g;
   g.ld0 = H;
-  const int bound = row_tiles_bound(R, E) * (H / 256);
+  const int bound = row_tiles_bound(R, E) * ((H + 255) / 256);
   CUtensorMap to;
   if (!tmap_out(&to, dx_g, H, R, true)) return cudaErrorInvalidValue;
   if (dhu_lo == nullptr)

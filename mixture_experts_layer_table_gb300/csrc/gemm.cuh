@@ -483,6 +483,7 @@ __device__ __forceinline__ void epi_swiglu_bwd_cols(uint32_t tacc, long long row
   __nv_bfloat16* ga_lo = reinterpret_cast<__nv_bfloat16*>(args.out3);
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
+    if (n * BN + c * 32 >= I) break;  // the tile reaches past I (I a multiple of 128, not 256)
     const int col = n * BN + c * 32 + 4 * q;
     // this block's h | u first: their latency overlaps the TMEM load and the transpose
     float4 h4s[8], u4s[8];

@@ -122,7 +122,7 @@ cudaError_t launch_gemm2_mxf8(const void* aq, const void* asf, const void* w2_q,
       !tmap_sf_blocks(&tws, w2_sf, (uint64_t)E * (H / 128) * (I / MX_BK)) ||
       !tmap_sf_blocks(&txs, asf, (uint64_t)G * (I / MX_BK)))
     return cudaErrorInvalidValue;
-  MxGemmArgs a = mx_args(E, I, H / 256, H, I, H / 128, offsets, blk_off, status);
+  MxGemmArgs a = mx_args(E, I, (H + 255) / 256, H, I, H / 128, offsets, blk_off, status);
   a.N_out = H;
   a.out = o;
   a.ld = H;
@@ -138,7 +138,7 @@ cudaError_t launch_dgrad_swiglu_mxf8(const void* dyq, const void* dysf, const vo
       !tmap_sf_blocks(&tws, w2t_sf, (uint64_t)E * (I / 128) * (H / MX_BK)) ||
       !tmap_sf_blocks(&txs, dysf, (uint64_t)G * (H / MX_BK)))
     return cudaErrorInvalidValue;
-  MxGemmArgs a = mx_args(E, H, I / 256, I, I, I / 128, offsets, blk_off, status);
+  MxGemmArgs a = mx_args(E, H, (I + 255) / 256, I, I, I / 128, offsets, blk_off, status);
   a.hu = hu;
   a.gate_row = gate_row;
   a.dhu_hi = static_cast<__nv_bfloat16*>(dhu_hi);
@@ -157,7 +157,7 @@ cudaError_t launch_dgrad_x_mxf8(const void* dhuq, const void* dhusf, const void*
       !tmap_sf_blocks(&tws, w13t_sf, (uint64_t)E * (H / 128) * (2 * I / MX_BK)) ||
       !tmap_sf_blocks(&txs, dhusf, (uint64_t)G * (2 * I / MX_BK)))
     return cudaErrorInvalidValue;
-  MxGemmArgs a = mx_args(E, 2 * I, H / 256, H, I, H / 128, offsets, blk_off, status);
+  MxGemmArgs a = mx_args(E, 2 * I, (H + 255) / 256, H, I, H / 128, offsets, blk_off, status);
   a.N_out = H;
   a.out = dx_g;
   a.ld = H;

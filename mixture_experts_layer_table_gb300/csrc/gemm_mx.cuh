@@ -46,8 +46,8 @@ enum MxEpi { MXE_SWIGLU = 0, MXE_F32 = 1, MXE_SWIGLU_BWD = 2 };
 struct MxGemmArgs {
   int E;
   int K;                  // reduction length, a multiple of 128
-  int MT;                 // pair weight tiles per expert (GEMM1: I / 128; else Nw / 256)
-  int Nw;                 // rows of each expert's weight matrix (F32 / BWD: MT * 256)
+  int MT;                 // pair weight tiles per expert (GEMM1: I / 128; else ceil(Nw / 256))
+  int Nw;                 // rows of each expert's weight matrix (a multiple of 128)
   int I;                  // intermediate width (SwiGLU epilogues)
   int N_out;              // F32: output columns (the weight rows of an expert)
   int sfa_tiles;          // 128-row scale tiles per expert of the weight matrix
@@ -462,6 +462,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const int I = args.I;
         const int twoI = 2 * I;
+        // the pair tile reaches past I (a multiple of 128, not 256): this CTA's 128 indices lie
+        // beyond it and it has nothing to store (the same for all four warps of the CTA)
+        const bool cta_in = t.m * 256 + 128 * (int)rank < I;
         const int i = t.m * 256 + 128 * (int)rank + 32 * quarter + lane;  // this thread's intermediate index
         const int S = twoI / MX_BK;
         const int s_h = i >> 7, s_u = (I + i) >> 7;            // K stages of dX_g holding dh_i, du_i
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(192, 1)
         const int part = 2 * t.m + (int)rank;                   // this CTA's 128 intermediate indices
         const int nparts = I / 128;
 #pragma unroll 1
-        for (int c = 0; c * 32 < t.nload; ++c) {
+        for (int c = 0; cta_in && c * 32 < t.nload; ++c) {
           const int nr = min(32, t.rows - c * 32);
           const int p0 = t.prow0 + c * 32;
           const long long r0 = (long long)t.row0 + c * 32;

@@ -165,11 +165,16 @@ __global__ void __launch_bounds__(GATHER_MX_THREADS)
     const uint64_t keep = l2_policy_evict_last();
     const uint4* s = reinterpret_cast<const uint4*>(src) + (size_t)tok * vec_per_row;
     uint2* d = reinterpret_cast<uint2*>(xq + (size_t)p * H);
-    for (int base = threadIdx.x; base < vec_per_row; base += GATHER_MX_THREADS * V) {
+    // H a multiple of 128: a warp's 32 lanes (256 elements) may reach past the row by 16 lanes;
+    // those lanes quantise zeros alongside (the 4-lane shuffles of a block see every lane) and
+    // store nothing.  Blocks (4 lanes) are whole: in the row or past it.
+    const int lane = threadIdx.x & 31;
+    for (int base = threadIdx.x; base - lane < vec_per_row; base += GATHER_MX_THREADS * V) {
       uint4 u[V];
 #pragma unroll
       for (int j = 0; j < V; ++j) {
-        const int i = base + j * GATHER_MX_THREADS;  // a warp's 32 lanes are all in range or none
+        const int i = base + j * GATHER_MX_THREADS;
+        u[j] = make_uint4(0u, 0u, 0u, 0u);
         if (i < vec_per_row)
           asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                        : "=r"(u[j].x), "=r"(u[j].y), "=r"(u[j].z), "=r"(u[j].w)
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(GATHER_MX_THREADS)
 #pragma unroll
       for (int j = 0; j < V; ++j) {
         const int i = base + j * GATHER_MX_THREADS;
-        if (i < vec_per_row) {
+        if (base - lane + j * GATHER_MX_THREADS < vec_per_row) {  // the warp's first lane is in the row
           float v[8];
           const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[j]);
 #pragma unroll
@@ -189,8 +194,8 @@ __global__ void __launch_bounds__(GATHER_MX_THREADS)
           }
           uint2 bytes;
           const int X = mx_quantize8_x4_e4m3(v, bytes);
-          d[i] = bytes;
-          if ((i & 3) == 0) {  // the first lane of the block stores its scale
+          if (i < vec_per_row) d[i] = bytes;
+          if (i < vec_per_row && (i & 3) == 0) {  // the first lane of the block stores its scale
             const int kb = i >> 2;
             const int g_top = p >> 5;
 #pragma unroll
@@ -308,19 +313,21 @@ __device__ __forceinline__ void mx_row_values8(const MxRowsArgs& a, int r, int c
 // memory with 16-byte loads along the rows, thread c quantises column c as one MX block, the
 // quantised values go back into the tile and leave as 16-byte stores along the rows.  Staged rows
 // are 260 floats apart (16-byte aligned; the column reads hit 32 different banks).  C is a
-// multiple of 256.  (A persistent version that stored one bf16 per thread per row, with 8-way
+// multiple of 128: the last chunk of a row may hold 128 columns, the rest of its tile is zeros that
+// are quantised and not stored.  (A persistent version that stored one bf16 per thread per row, with 8-way
 // bank conflicts on the staging, ran the x_g and dY_g passes at 1.3 TB/s.)
 constexpr int MXQ_LD = 260;
 template <int SRC>
 __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) {
   __shared__ __align__(16) float tile[32 * MXQ_LD];
-  const int nchunk = a.C / 256;
+  const int nchunk = (a.C + 255) / 256;
   const int nblk = a.seg_len > 0 ? a.E * (a.seg_len / 32) : a.blk_off[a.E];
   const long long items = (long long)nblk * nchunk;
   const long long w = blockIdx.x;
   if (w >= items) return;  // the grid is an upper bound of the items
   const int b = (int)(w / nchunk);
   const int c0 = (int)(w - (long long)b * nchunk) * 256;
+  const int cols = min(256, a.C - c0);
   int r0, nrows;
   if (a.seg_len > 0) {
     r0 = b * 32;
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) 
     const int idx = threadIdx.x + 256 * i;
     const int row = idx >> 5, ch = idx & 31;
     float f[8];
-    if (row < nrows) {
+    if (row < nrows && 8 * ch < cols) {
       mx_row_values8<SRC>(a, r0 + row, c0 + 8 * ch, f);
     } else {
 #pragma unroll
@@ -363,7 +370,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const MxRowsArgs a) 
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + 256 * i;
     const int row = idx >> 5, ch = idx & 31;
-    if (row < nrows) {
+    if (row < nrows && 8 * ch < cols) {
       const float4* t4 = reinterpret_cast<const float4*>(&tile[row * MXQ_LD + 8 * ch]);
       const float4 x0 = t4[0], x1 = t4[1];
       uint4 o;
@@ -442,12 +449,12 @@ cudaError_t launch_mx_quant_rows(int src, int rows_bound, int C, int E, int seg_
   a.src_of = src_of;
   a.k = k;
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
-  if ((seg_len > 0 && seg_len % 32 != 0) || C % 256 != 0) return cudaErrorInvalidValue;
+  if ((seg_len > 0 && seg_len % 32 != 0) || C % 128 != 0) return cudaErrorInvalidValue;
   // an upper bound of the work items sizes the grid; the kernel reads the exact count
   // an upper bound of the work items sizes the grid (one item per CTA); the kernel reads the
   // exact count
   (void)n_sm;
-  const long long items = (long long)((rows_bound + 31) / 32 + E) * (C / 256);
+  const long long items = (long long)((rows_bound + 31) / 32 + E) * ((C + 255) / 256);
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int blocks = (int)std::max<long long>(items, 1);
   switch (src) {

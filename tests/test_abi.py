@@ -274,3 +274,17 @@ def test_trace_argument_checks(lib):
     if code == 0:
         assert lib.mok_trace_start(4) == 1
         assert lib.mok_trace_stop(None, 0, ctypes.byref(n)) == 0 and n.value == 0
+
+
+@pytest.mark.parametrize("H,I,ok", [(384, 640, True), (7168, 1408, True), (128, 128, True), (320, 512, False),
+                                    (512, 448, False), (256, 64, False)])
+def test_widths_are_multiples_of_128(lib, H, I, ok):
+    """H and I: any multiple of 128 (odd multiples included: the last 256-row pair tile reads zeros
+    past the end), anything else is unsupported (MOK_ERR_UNSUPPORTED = 2)."""
+    desc = N.make_desc(64, H, I, 8, 2, W.ROUTER_SIGMOID, True)
+    if ok:
+        assert N.get_layout(desc)["ws_bytes"] > 0
+    else:
+        with pytest.raises(mok.MokError) as info:
+            N.get_layout(desc)
+        assert info.value.code == 2

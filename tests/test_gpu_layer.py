@@ -122,8 +122,21 @@ LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=
 # skewed long segments: hot experts with several full 256-row blocks, cold ones with only a tail
 LONG_SKEW = LONG.scaled(name="long_skew", skew=True)
 # LONG: 750 rows per expert, the expert GEMMs' 256-row chunks and GEMM1's paired form
+# H and I odd multiples of 128: the last 256-row weight tile of GEMM2, dA' and dX_g reaches past the
+# end (zeros loaded, nothing stored); ODD_LONG has 1500 rows per expert, where GEMM1 keeps its
+# unpaired form (the paired one takes whole 256-index tiles); ODD_SHORT takes the paired GEMM2 /
+# dX_g form with one 512-row tile over H = 384; EDGE128 has one CTA of each pair past the end
+ODD = W.MoEShape("odd_T600_H384_E8_I640_top4_sigmoid", T=600, H=384, E=8, I=640, k=4,
+                 router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
+ODD_LONG = W.MoEShape("odd_long_T1500_H384_E4_I640_top4", T=1500, H=384, E=4, I=640, k=4,
+                      router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
+ODD_SHORT = W.MoEShape("odd_short_T256_H384_E16_I640_top4", T=256, H=384, E=16, I=640, k=4,
+                       router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03, skew=True)
+EDGE128 = W.MoEShape("edge_T100_H128_E4_I128_top2_softmax", T=100, H=128, E=4, I=128, k=2,
+                     router=W.ROUTER_SOFTMAX, renorm=False, x_std=1.0, w_std=0.05)
 CASES = [(TINY, None), (MID, None), (MID_SKEW, None), (MID, "skewed_given"), (ONE, None), (DENSE, None),
-         (MAXES, None), (LONG, None), (LONG_SKEW, None)]
+         (MAXES, None), (LONG, None), (LONG_SKEW, None), (ODD, None), (ODD_LONG, None), (ODD_SHORT, None),
+         (EDGE128, None)]
 
 
 @pytest.mark.parametrize("shape,mode", CASES, ids=lambda c: getattr(c, "name", str(c)))
@@ -172,7 +185,8 @@ def test_route_scale(shape, scale):
         assert_bf16_close(to_f64(g[name]), bwd[name], name)
 
 
-@pytest.mark.parametrize("shape,mode", [(MID, None), (MID, "skewed_given"), (TINY, None)],
+@pytest.mark.parametrize("shape,mode", [(MID, None), (MID, "skewed_given"), (TINY, None), (ODD, None),
+                                        (EDGE128, None)],
                          ids=lambda c: getattr(c, "name", str(c)))
 def test_row_tile_gemms_forward_backward(shape, mode):
     """MOK_FLAG_GEMM_SINGLE: the expert GEMMs on the 128-row-tile single-CTA kernels and the weight
@@ -266,7 +280,7 @@ def test_repeated_backward_on_one_layer_single_cta_kernels():
 
 # long expert segments (~750 rows: several 256-row pair tiles and a ragged one per expert)
 PAIR_CASES = [(LONG, None), (LONG_SKEW, None), (LONG, "skewed_given"), (MID, None), (MID, "skewed_given"),
-              (TINY, None), (ONE, None)]
+              (TINY, None), (ONE, None), (ODD_LONG, None), (EDGE128, None)]
 
 
 @pytest.mark.parametrize("shape,mode", PAIR_CASES, ids=lambda c: getattr(c, "name", str(c)))
@@ -333,6 +347,7 @@ def test_stuck_wait_times_out_and_context_survives():
     (LONG, 3000, 2, 6, 0),      # 750 rows per expert: chunks of up to 256 rows cut at minibatch edges
     (MID, 300, 2, 3, "single"),  # the row-tile ring kernel (one CTA per 128-row tile), odd comm count
     (MID_SKEW, 700, 2, 4, "pair"),  # the row-tile ring kernel under the CTA-pair flag
+    (ODD, 500, 2, 4, 0),        # H and I odd multiples of 128
 ], ids=lambda v: getattr(v, "name", str(v)))
 def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm, flags):
     """The ring forward (persistent launch: gathering CTAs fill ring slots while GEMM CTAs run
@@ -422,7 +437,7 @@ def test_ring_rejects_an_odd_comm_count_on_the_pair_kernel():
 
 # ----------------------------------------------------------------------------- fp16 W2 (MOK_FLAG_W2_F16)
 
-@pytest.mark.parametrize("shape", [MID, MID_SKEW, LONG, LONG_SKEW], ids=lambda c: c.name)
+@pytest.mark.parametrize("shape", [MID, MID_SKEW, LONG, LONG_SKEW, ODD, ODD_SHORT], ids=lambda c: c.name)
 def test_forward_with_fp16_w2(shape):
     """The forward on an fp16 copy of W2 with a kept as one fp16 value (GEMM1's SwiGLU epilogue in
     both forms: LONG has 750 rows per expert, the paired form): a is the fp16 rounding of the GPU's

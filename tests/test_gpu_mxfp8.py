@@ -21,6 +21,10 @@ pytestmark = pytest.mark.gpu
 MX_FRO = 5e-2
 MID = W.MoEShape("mid_mx_T600_H512_E16_I768_top4", T=600, H=512, E=16, I=768, k=4, router=W.ROUTER_SIGMOID,
                  renorm=True, x_std=1.0, w_std=0.03, mxfp8=True)
+# H and I odd multiples of 128: the last 256-row pair tile of GEMM2, dA' and dX_g reaches past the
+# end, the row quantisers see half-width chunks
+ODD = W.MoEShape("odd_mx_T600_H384_E8_I640_top4", T=600, H=384, E=8, I=640, k=4, router=W.ROUTER_SIGMOID,
+                 renorm=True, x_std=1.0, w_std=0.03, mxfp8=True)
 q = O.mx_quantize_dequantize
 
 
@@ -95,13 +99,15 @@ def _run_mx(shape, inp, given=None):
     return layer, y, wq
 
 
-def test_quantized_weights_bit_exact():
-    inp = W.make_inputs(MID, seed=0, device="cpu")
+@pytest.mark.parametrize("shape", [MID, ODD], ids=lambda s: s.name)
+def test_quantized_weights_bit_exact(shape):
+    inp = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp)
-    _, _, wq = _run_mx(MID, inp)
-    for name, w, N, K, gu in (("w13", f64["w13"], 2 * MID.I, MID.H, MID.I), ("w2", f64["w2"], MID.H, MID.I, 0)):
+    _, _, wq = _run_mx(shape, inp)
+    for name, w, N, K, gu in (("w13", f64["w13"], 2 * shape.I, shape.H, shape.I),
+                              ("w2", f64["w2"], shape.H, shape.I, 0)):
         got, X_got = _decode_w(wq[name + "_q"], wq[name + "_scale"], N, K, gu)
-        for e in range(MID.E):
+        for e in range(shape.E):
             want = q(w[e], 1)
             bad = np.argwhere(got[e] != want)
             assert bad.size == 0, (name, e, len(bad), [(tuple(b), got[e][tuple(b)], want[tuple(b)], w[e][tuple(b)])
@@ -110,9 +116,8 @@ def test_quantized_weights_bit_exact():
             assert np.array_equal(X_got[e], X), (name, e)
 
 
-@pytest.mark.parametrize("skew", [False, True])
-def test_mx_forward_matches_mx_oracle(skew):
-    shape = MID.scaled(skew=skew)
+@pytest.mark.parametrize("shape", [MID, MID.scaled(name="mid_mx_skew", skew=True), ODD], ids=lambda s: s.name)
+def test_mx_forward_matches_mx_oracle(shape):
     inp = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp)
     given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
@@ -183,17 +188,18 @@ def test_mx_forward_full_size_sampled_and_deterministic():
 
 # ----------------------------------------------------------------------------- backward
 
-def test_backward_weights_bit_exact():
+@pytest.mark.parametrize("shape", [MID, ODD], ids=lambda s: s.name)
+def test_backward_weights_bit_exact(shape):
     """W2 quantised along H and W13 along 2I (32-row blocks of each expert's matrix), stored transposed
     ([E][I][H] and [E][H][2I]) as E4M3 bytes and scale blocks."""
-    inp = W.make_inputs(MID, seed=0, device="cpu")
+    inp = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp)
-    desc = mok.desc_from_shape(MID)
+    desc = mok.desc_from_shape(shape)
     wb = mok.quantize_weights_backward(desc, inp["w13"].cuda(), inp["w2"].cuda())
     torch.cuda.synchronize()
-    for name, w, N, K in (("w13", f64["w13"], MID.H, 2 * MID.I), ("w2", f64["w2"], MID.I, MID.H)):
+    for name, w, N, K in (("w13", f64["w13"], shape.H, 2 * shape.I), ("w2", f64["w2"], shape.I, shape.H)):
         got, X_got = _decode_w(wb[name + "t_q"], wb[name + "t_scale"], N, K)
-        for e in range(MID.E):
+        for e in range(shape.E):
             want = q(w[e], 0).T
             assert np.array_equal(got[e], want), (name, e, int((got[e] != want).sum()))
             _, X = O.mx_quantize(w[e], 0)
@@ -216,11 +222,10 @@ def _mx_fwd_bwd(shape, seed=0, given=None):
     return inp, layer, y, grads
 
 
-@pytest.mark.parametrize("skew", [False, True])
-def test_mx_backward_matches_mx_oracle(skew):
+@pytest.mark.parametrize("shape", [MID, MID.scaled(name="mid_mx_skew", skew=True), ODD], ids=lambda s: s.name)
+def test_mx_backward_matches_mx_oracle(shape):
     """Every gradient within relative Frobenius 5e-2 of the oracle's MX-emulating backward (each
     backward GEMM operand quantised along its reduction axis, float64 products)."""
-    shape = MID.scaled(skew=skew)
     inp0 = W.make_inputs(shape, seed=0, device="cpu")
     f64 = inputs_f64(inp0)
     given = O.route(f64["x"], f64["w_router"], f64["router_bias"], shape.router, shape.k, shape.renorm)["topk_idx"]
