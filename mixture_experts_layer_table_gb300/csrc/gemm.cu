@@ -382,11 +382,24 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
   if (strip_counter == nullptr) return cudaErrorInvalidValue;
   const size_t smem = wgrad_smem_bytes(E);
   if (pair && M % 256 == 0 && N % 256 == 0) {
-    // CTA pairs: 256 x 256 output tiles, each CTA half of both operands
+    // CTA pairs: 256 x 256 output tiles, each CTA half of both operands; the output as
+    // [E*N rows][M] for the epilogue's 32 x 32 TMA stores
     const int pstrips = E * (stat_a ? M / 256 : N / 256);
     if (pstrips <= 0) return cudaSuccess;
+    CUtensorMap to;
+    {
+      const uint64_t dims[2] = {(uint64_t)M, (uint64_t)E * N};
+      const uint64_t strides[1] = {(uint64_t)M * (out_f32 ? 4 : 2)};
+      const uint32_t box[2] = {32, 32};
+      if (!make_tmap(&to, dw, 2, dims, strides, box,
+                     out_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    }
+    static_assert(wgrad_pair_smem_bytes(1024) <= 232448, "shared memory budget");
     auto run_pair = [&](auto kern) {
-      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_smem_bytes(1024));
+      cudaError_t err =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_pair_smem_bytes(1024));
       if (err != cudaSuccess) return err;
       cudaLaunchConfig_t cfg{};
       cudaLaunchAttribute attr[1];
@@ -395,7 +408,7 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
       attr[0].val.clusterDim.y = 1;
       attr[0].val.clusterDim.z = 1;
       cfg.blockDim = dim3(WGP_THREADS, 1, 1);
-      cfg.dynamicSmemBytes = smem;
+      cfg.dynamicSmemBytes = wgrad_pair_smem_bytes(E);
       cfg.stream = st;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
@@ -403,7 +416,7 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
       int clusters = 0;
       if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
       cfg.gridDim = dim3(2 * std::min(pstrips, std::max(1, clusters)), 1, 1);
-      if ((err = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, g)) != cudaSuccess) return err;
+      if ((err = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, to, g)) != cudaSuccess) return err;
       return cudaGetLastError();
     };
     if (!split) return out_f32 ? run_pair(wgrad_pair_kernel<true, true, false>) : run_pair(wgrad_pair_kernel<true, false, false>);
