@@ -61,7 +61,12 @@ struct NarrowCfg {
   // two from 32 to 512
   static constexpr int TMEM_COLS = (kPaired || 2 * NMAX > 256) ? 512 : 256;
   static_assert(NMAX % 32 == 0 && NMAX >= 32 && 2 * NMAX <= 512, "accumulators must fit the TMEM allocation");
-  static constexpr int THREADS = 192;
+  // epilogue warps: two per TMEM lane quarter in the paired SwiGLU form (taking alternate 8-row
+  // blocks), whose single accumulator is held while the epilogue stores h, u and a: more warps
+  // storing at once free it sooner (at T = 16384, 512 rows per expert, the stores of four warps
+  // held the MMAs 0.8 ms of 6.0)
+  static constexpr int EPI_WARPS = EPI == EPI_SWIGLU_PAIRED ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // SwiGLU: one 32 x 32 fp32 block of h and one of u per pair of warps
   static constexpr int XBUF_BYTES = EPI == EPI_SWIGLU ? 2 * 2 * 32 * 32 * 4 : 0;
   // weight tiles: 256 output columns, or (SwiGLU) 128 intermediate indices (gate and up rows),
@@ -87,7 +92,7 @@ struct NarrowCfg {
 // args.mb_start: the tiles before each minibatch), wait for a minibatch's rows before loading
 // them, and count each tile's epilogue warps out on args.consumed so that the slot can be refilled.
 template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
                        const __grid_constant__ CUtensorMap tmX2s, const GemmArgs args) {
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 8);
+      mbar_init(tempty_bar(a), 2 * C::EPI_WARPS);  // every epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -448,13 +453,15 @@ __global__ void __launch_bounds__(192, 1)
       } else if (EPI == EPI_SWIGLU_PAIRED) {
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
         tc_fence_after();
-        // this thread's intermediate index: h in column n, u in column 256 + n of its lane
+        // this thread's intermediate index: h in column n, u in column 256 + n of its lane; the
+        // warp's group takes every other 8-row block
         const int i = t.m * 256 + 128 * (int)rank + 32 * quarter + lane;
+        const int grp = (warp - 2) >> 2;
         float* hrow = reinterpret_cast<float*>(args.out0) + (long long)t.row0 * args.ld0 + i;
         __nv_bfloat16* arow_hi = reinterpret_cast<__nv_bfloat16*>(args.out1) + (long long)t.row0 * args.ld1 + i;
         __nv_bfloat16* arow_lo = reinterpret_cast<__nv_bfloat16*>(args.out2) + (long long)t.row0 * args.ld1 + i;
 #pragma unroll 1
-        for (int n0 = 0; n0 < t.rows; n0 += 8) {
+        for (int n0 = 8 * grp; n0 < t.rows; n0 += 8 * (C::EPI_WARPS / 4)) {
           uint32_t hv[8], uv[8];
           tmem_ld_32x32b_x8(tacc + n0, hv);
           tmem_ld_32x32b_x8(tacc + 256 + n0, uv);
