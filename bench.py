@@ -566,6 +566,36 @@ def run_mok(args, rank, world, local_rank):
                                   for n in ("wgrad_w2", "wgrad_w13") if n in trace16}}
         del layer16, g16
 
+    # ---- the skewed-routing layer: the same tokens and weights with the Zipf-Mandelbrot router
+    #      bias (hottest expert ~10x the mean load), forward + backward
+    skew = None
+    if not args.no_skew:
+        bias = W.skew_bias(E).to(dev)
+
+        def skew_step():
+            layer.forward(x, wr, w13, w2, router_bias=bias, y=y)
+            layer.backward(dy, x, wr, w13, w2, out=grads)
+
+        for _ in range(2):
+            skew_step()
+        barrier()
+        torch.cuda.synchronize()
+        N.trace_start(40 * args.steps + 16)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            skew_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        skew_trace = N.trace_stop()
+        skew_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+        if layer.status() != (0, 0):
+            raise RuntimeError("device status set in the skewed step")
+        sc = layer.view("counts").cpu()
+        skew = {"workload": W.DSV3_SKEW.name + " (same tokens and weights, Zipf-Mandelbrot router bias)",
+                "fwd_bwd_ms": round(skew_ms, 4), "tokens_per_s": round(whole_job_rate(T, world, skew_ms), 1),
+                "expert_rows_min_max": [int(sc.min()), int(sc.max())],
+                "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in skew_trace.items()}}
+
     # ---- end to end through the public API with host buffers (pinned), copies timed.  Every
     #      step copies its own x and dY in and its y and dX out; a copy stream moves step i+1's
     #      inputs and step i-1's outputs while step i computes (two device buffer sets).
@@ -775,6 +805,7 @@ def run_mok(args, rank, world, local_rank):
                 "what": "pinned host x and dY copied in, forward + backward, y and dX copied out, every step; "
                         "the copies of neighbouring steps overlap the compute on a second stream"},
         "wgrad_bf16": wgrad_bf16 if wgrad_bf16_ms is not None else None,
+        "skew_fwd_bwd": skew,
         "fwd_bwd_ms_wgrad_bf16": round(wgrad_bf16_ms, 4) if wgrad_bf16_ms is not None else None,
         "mxfp8_fwd": mx,
         "tensor_bound_fwd": tb,
@@ -849,6 +880,88 @@ def tensor_bound_forward(shp, x, w_router, w13, w2, steps, warmup, flags=0):
     return ms, kernels, grouped, layer, y
 
 
+def run_macrobatch_study(args):
+    """Macrobatch interleaving on one GPU: the T=16384 forward (256 experts, top-8, hidden 7168) as
+    one call, then as M = 2 and 4 macrobatches of T/M tokens each, (a) back to back on one stream
+    and (b) interleaved over two streams with a workspace each, so that the combine of macrobatch i
+    can run beside the router, schedule and dispatch of macrobatch i+1.  Each macrobatch streams
+    all expert weights again.  K forwards after W warm-ups, CUDA events around the whole loop.
+    One JSON line."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    mok.load()
+    shp = W.RING
+    inp = W.make_inputs(shp, seed=0, device="cuda", with_dy=False)
+    x, wr, w13, w2 = inp["x"], inp["w_router"], inp["w13"], inp["w2"]
+    y = torch.empty((shp.T, shp.H), dtype=torch.bfloat16, device="cuda")
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+
+    def timed(run):
+        for _ in range(args.warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(args.steps):
+            run()
+        main.wait_stream(side)
+        e1.record(main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    one = mok.MoELayer(mok.desc_from_shape(shp))
+    y_one = None
+
+    def run_one():
+        one.forward(x, wr, w13, w2, y=y)
+
+    out = {"one_call_ms": round(timed(run_one), 4)}
+    y_one = y.clone()
+    del one
+    torch.cuda.empty_cache()
+    for M in (2, 4):
+        tm = shp.T // M
+        sub = shp.scaled(T=tm)
+        layers = [mok.MoELayer(mok.desc_from_shape(sub)) for _ in range(2)]
+        streams = [main, side]
+
+        def run_seq():
+            for i in range(M):
+                sl = slice(i * tm, (i + 1) * tm)
+                layers[0].forward(x[sl], wr, w13, w2, y=y[sl])
+
+        def run_inter():
+            # macrobatch i on stream i % 2 with workspace i % 2; a stream waits for the other's
+            # previous macrobatch only through the workspace it reuses (two back)
+            for i in range(M):
+                st = streams[i % 2]
+                sl = slice(i * tm, (i + 1) * tm)
+                with torch.cuda.stream(st):
+                    layers[i % 2].forward(x[sl], wr, w13, w2, y=y[sl], stream=st)
+
+        seq_ms = timed(run_seq)
+        seq_equal = bool(torch.equal(y, y_one))
+        inter_ms = timed(run_inter)
+        inter_equal = bool(torch.equal(y, y_one))
+        ok = all(l.status() == (0, 0) for l in layers)
+        out[f"M{M}"] = {"macrobatch_tokens": tm, "back_to_back_ms": round(seq_ms, 4),
+                        "interleaved_two_streams_ms": round(inter_ms, 4),
+                        "y_bitwise_equal_to_one_call": [seq_equal, inter_equal], "status_ok": ok}
+        del layers
+        torch.cuda.empty_cache()
+    line = {"metric": "macrobatch study: forward ms at T=16384 (one call vs M macrobatches)",
+            "value": out["one_call_ms"], "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": False, "dtype": "bf16",
+            "data": "synthetic (seeded Gaussian bf16 activations and weights; no dataset)",
+            "config": {"workload": shp.name, "weights_bytes_per_pass": shp.E * 3 * shp.H * shp.I * 2},
+            "study": out}
+    print(json.dumps(line), flush=True)
+
+
 def run_ring_sweep(args):
     """Ring forward at T=16384 (256 experts, top-8, hidden 7168): a fixed 512 MiB token ring
     and the minibatch sizes 512 / 1024 / 2368 / 2560 / 4096, each timed over K forwards after
@@ -901,10 +1014,14 @@ def main():
     ap.add_argument("--no-ring-sweep", action="store_true",
                     help="skip the ring-forward minibatch sweep at T=16384 in the default line")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")
+    ap.add_argument("--no-skew", action="store_true", help="skip the skewed-routing forward+backward timing")
     ap.add_argument("--no-tensor-bound", action="store_true",
                     help="skip the forward at T=16384 (tensor-bound grouped GEMMs)")
     ap.add_argument("--ring-sweep", action="store_true",
                     help="time the ring forward at T=16384 over the minibatch sweep instead")
+    ap.add_argument("--macrobatch", action="store_true",
+                    help="time the T=16384 forward as one call against 2 and 4 macrobatches (back to back, "
+                         "and interleaved over two streams) instead")
     ap.add_argument("--gemm", choices=sorted(GEMM_FLAGS), default="auto",
                     help="expert GEMM kernels: pair / single = the row-tile kernels on CTA pairs / single "
                          "CTAs; auto = the library's default (narrow-segment pair kernel: expert rows as the MMA's N)")
@@ -924,6 +1041,10 @@ def main():
     if args.ring_sweep:
         if rank == 0:
             run_ring_sweep(args)
+        return
+    if args.macrobatch:
+        if rank == 0:
+            run_macrobatch_study(args)
         return
     if world > 1:
         import torch

@@ -660,8 +660,7 @@ mok_status mok_moe_backward(const mok_layer_desc* d, const void* dy, const void*
                                                wgrad_pairs(d), n_sm, st));
   MOK_LAUNCH("wgrad_w13", st, mok::launch_wgrad(x_g, nullptr, H, dhu, dhu_lo, 2 * I, R, E, offsets, dw13, wgrad_f32,
                                                 status, status + mok::STATUS_COUNTERS + mok::CNT_WGRAD_W13,
-                                                wgrad_pairs(d), n_sm,
-                                                st));
+                                                wgrad_pairs(d), n_sm, st));
   // 6. gate and router-logit gradients, 7. router weight gradient
   MOK_LAUNCH("router_dlogits", st, mok::launch_router_dlogits(dg_part, (I + 255) / 256, row_of, topk_idx, gates, scores, T, E, k, d->router,
                                       d->renorm, d->route_scale, dgates, dl, st));

@@ -233,6 +233,19 @@ def test_bf16_weight_gradients_are_rounded_fp32_ones(shape):
         assert torch.equal(g[name], g32[name]), name
 
 
+def test_weight_gradients_pair_and_single_bitwise_with_a_hot_expert():
+    """The pair kernel deals its strips back and forth over the pairs, the single-CTA kernel from a
+    counter: with a hot expert and an empty one the weight gradients are bitwise the same."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    shape = MID_SKEW
+    inp = W.make_inputs(shape, seed=2, device="cpu")
+    given = _skewed_topk(shape.T, shape.E, shape.k, seed=11, empty=(5,))
+    _, _, g = _run(shape, inp, given=given)
+    _, _, g1 = _run(shape, inp, given=given, flags=N.FLAG_GEMM_SINGLE)
+    for name in ("dw13", "dw2"):
+        assert torch.equal(g[name], g1[name]), name
+
+
 def test_empty_experts_get_zero_weight_gradient():
     shape = MID
     inp = W.make_inputs(shape, seed=1, device="cpu")
