@@ -13,12 +13,17 @@
 // themselves run at the ideal rate in isolation.
 //
 // Warps (both CTAs): 0 TMA producer, 1 MMA issuer (even CTA) / stationary check (odd CTA), 2..9
-// epilogue in two groups of four, one per TMEM accumulator.  The stationary halves are loaded by
-// each CTA with plain TMA into its own barrier; its warp 1 zeroes the rows past the expert's end
-// and then reports to the even CTA (stat_ready, 2 arrivals) before the pair's MMAs read them.
-// Strips (expert, 256-wide stationary tile) are dealt to the pairs round-robin; each output
-// element is one tile's accumulator, reduced over the expert's rows in a fixed order, so results
-// are bitwise those of the single-CTA kernel.
+// epilogue in two groups of four, one per TMEM accumulator.  The stationary region is a ring of
+// WG_KSTAT slots of one 64-row K block each, with a full, a ready and an empty barrier per slot:
+// each CTA loads its stationary halves with plain TMA into its own full barrier, its warp 1
+// zeroes the rows past the expert's end and reports to the even CTA (ready, 2 arrivals) before
+// the pair's MMAs read the slot.  An expert of at most WG_KSTAT K blocks keeps its stationary
+// blocks for the whole strip; a longer one streams them again for each tile, one block per slot,
+// up to WG_KSTAT blocks ahead of the MMAs.
+// Work items (single tiles of the long experts, then strips of the others; see the item list
+// below) are dealt to the pairs in a fixed order; each output element is one tile's accumulator,
+// reduced over the expert's rows in a fixed order, so results are bitwise those of the single-CTA
+// kernel.
 //
 // The output leaves through TMA stores: an epilogue warp reads 32 columns of its 32 accumulator
 // rows from TMEM, parks them in its 4 KB shared-memory block as 32 output rows of 32 elements
@@ -37,10 +42,12 @@ namespace mok {
 constexpr int WGP_THREADS = 320;
 constexpr int WGP_STAGES = 5;
 constexpr int WGP_STG = 4096;  // one epilogue warp's staging block (32 x 32 fp32)
+// the barriers, the TMEM address and the abort flag share 256 bytes
+static_assert((2 * WGP_STAGES + 5 + 3 * WG_KSTAT) * 8 + 8 <= 256, "wgrad pair barriers");
 
 __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
   return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(WGP_STAGES) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + 256 +
-         size_t(E + 1) * 4;
+         size_t(E + 1) * 4 * 2;
 }
 
 template <bool STAT_A, bool OUT_F32, bool STAT_SPLIT = true>
@@ -54,10 +61,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WGP_STAGES stages
   uint8_t* stg_all = ring + WGP_STAGES * WG_STAGE;        // 8 epilogue warps x WGP_STG
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 8 * WGP_STG);
-  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full, stat_ready, stat_empty, drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 8);
+  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full[K], stat_ready[K], stat_empty[K], drain
+  // (K = WG_KSTAT)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 3 * WG_KSTAT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(stg_all + 8 * WGP_STG + 256);
+  int* s_list = s_off + args.E + 1;  // experts with more than WG_KSTAT K blocks, then the others
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -68,10 +77,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   auto empty_bar = [&](int s) { return smem_u32(&bars[WGP_STAGES + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * WGP_STAGES + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * WGP_STAGES + 2 + a]); };
-  const uint32_t stat_full = smem_u32(&bars[2 * WGP_STAGES + 4]);
-  const uint32_t stat_ready = smem_u32(&bars[2 * WGP_STAGES + 5]);
-  const uint32_t stat_empty = smem_u32(&bars[2 * WGP_STAGES + 6]);
-  const uint32_t drain_bar = smem_u32(&bars[2 * WGP_STAGES + 7]);
+  auto stat_full = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 4 + j]); };
+  auto stat_ready = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 4 + WG_KSTAT + j]); };
+  auto stat_empty = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 4 + 2 * WG_KSTAT + j]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * WGP_STAGES + 4 + 3 * WG_KSTAT]);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < WGP_STAGES; ++s) {
@@ -82,14 +91,34 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 8);  // the 4 warps of group a in both CTAs
     }
-    mbar_init(stat_full, 1);
-    mbar_init(stat_ready, 2);  // warp 1 of both CTAs
-    mbar_init(stat_empty, 1);
+    for (int j = 0; j < WG_KSTAT; ++j) {
+      mbar_init(stat_full(j), 1);
+      mbar_init(stat_ready(j), 2);  // warp 1 of both CTAs
+      mbar_init(stat_empty(j), 1);
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i <= args.E; i += blockDim.x) s_off[i] = args.offsets[i];
+  if (warp == 2) {
+    // the expert list: first the experts whose rows exceed the stationary region (in expert
+    // order), then the others (in expert order); s_list[E] = how many are first
+    int n_long = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      int at = pass == 0 ? 0 : n_long;
+      for (int e0 = 0; e0 < args.E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool is_long = e < args.E && args.offsets[e + 1] - args.offsets[e] > WG_KSTAT * WG_BK;
+        const bool take = e < args.E && (pass == 0 ? is_long : !is_long);
+        const uint32_t m = __ballot_sync(0xffffffffu, take);
+        if (take) s_list[at + __popc(m & ((1u << lane) - 1u))] = e;
+        at += __popc(m);
+      }
+      if (pass == 0) n_long = at;
+    }
+    if (lane == 0) s_list[args.E] = n_long;
+  }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), 512);
     tmem_relinquish_pair();
@@ -104,23 +133,48 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   const int MT = args.M / 256, NT = args.N / 256;
   const int per_e = STAT_A ? MT : NT;   // strips per expert
   const int strip_len = STAT_A ? NT : MT;
-  const int total = args.E * per_e;
-  // Strips in expert order, each expert's strips in a row (neighbouring pairs write neighbouring
-  // output); pair p takes strip round * npairs + p in even rounds and round * npairs + npairs - 1 - p
-  // in odd ones: dealt back and forth, so that a pair that drew a costly strip (an expert with many
-  // rows) in one round draws from the other end in the next and the pairs' totals even out (at the
-  // DSV3 layer with Zipf-skewed routing, 2 to 1335 rows per expert: dW13 8.54 -> 8.25 ms, dW2
-  // 4.47 -> 4.07 ms; sorting the experts by rows instead was slower with uniform routing).  Every
-  // role of both CTAs walks the same list.
-  auto strip = [&](int s, int& e, int& f, int& row0, int& rows, int& nkb) {
-    e = s / per_e;
-    f = s - e * per_e;
+  // Work items, dealt to the pairs in one fixed order:
+  //  * first, one item per output tile of each expert with more than WG_KSTAT K blocks of rows
+  //    (expert by expert, in s_list order; tiles of one stationary strip f in a row).  Its
+  //    stationary blocks are streamed again for every tile anyway, so the pairs spread over the
+  //    tiles of one expert at a time and share its rows in L2 (one pair per strip of 28 tiles, as
+  //    the strips below are dealt, kept some five long experts in flight at once, more than L2
+  //    holds: at 16 experts of 1024 rows, 45% of the operand reads hit L2 and dW13 took 2.3 us
+  //    per 64-row K block of a pair tile);
+  //  * then one item per strip (expert, 256-wide stationary tile f, all strip_len tiles) of the
+  //    other experts, whose stationary blocks stay in shared memory for the whole strip (each
+  //    expert's strips in a row, so neighbouring pairs share its streaming rows in L2).
+  // Pair p takes item round * npairs + p in even rounds and round * npairs + npairs - 1 - p in odd
+  // ones: dealt back and forth, so that a pair that drew a costly item in one round draws from the
+  // other end in the next and the pairs' totals even out.  Every role of both CTAs walks the same
+  // list.
+  const int n_long = s_list[args.E];
+  const int tiles_e = per_e * strip_len;
+  const int n_tile_items = n_long * tiles_e;
+  const int total = n_tile_items + (args.E - n_long) * per_e;
+  // item -> expert e, stationary strip f, tiles [i0, i1) along the strip, its rows
+  auto item = [&](int n, int& e, int& f, int& i0, int& i1, int& row0, int& rows, int& nkb) {
+    if (n < n_tile_items) {
+      const int le = n / tiles_e;
+      const int local = n - le * tiles_e;
+      e = s_list[le];
+      f = local / strip_len;
+      i0 = local - f * strip_len;
+      i1 = i0 + 1;
+    } else {
+      const int b = n - n_tile_items;
+      const int se = b / per_e;
+      e = s_list[n_long + se];
+      f = b - se * per_e;
+      i0 = 0;
+      i1 = strip_len;
+    }
     row0 = s_off[e];
     rows = s_off[e + 1] - row0;
     nkb = (rows + WG_BK - 1) / WG_BK;
   };
   const int half0 = 128 * (int)rank;
-  auto strip_at = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
+  auto item_at = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -135,26 +189,25 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       const CUtensorMap* st_map = STAT_A ? &tmB : &tmA;
       const uint32_t full0_cl = mapa_shared(full_bar(0), 0);  // the even CTA's full barriers
       int stage = 0;
-      uint32_t phase = 0, sphase = 0;
+      uint32_t phase = 0;
       int issued = 0;
-      bool stat_pending = false;  // a stationary load whose bytes may still be landing
+      int sc = 0;  // stationary K blocks loaded so far: the next goes to slot sc % WG_KSTAT
       bool ok = true;
-      auto load_stat = [&](int f, int row0, int kb0, int nk) {
-        if (!mbar_wait<true>(stat_empty, sphase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
+      auto load_stat = [&](int f, int row0, int kb) {
+        const int j = sc % WG_KSTAT;
+        const uint32_t ph = (uint32_t)(sc / WG_KSTAT) & 1u;
+        if (!mbar_wait<true>(stat_empty(j), ph ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
                              kWaitLimitNs, 32))
           return false;
-        sphase ^= 1;
-        mbar_arrive_expect_tx(stat_full, nk * (STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2));
-        for (int j = 0; j < nk; ++j) {
-          const uint32_t slot = smem_u32(stat + j * WG_STAT_SLOT);
-          const int r = row0 + (kb0 + j) * WG_BK;
+        mbar_arrive_expect_tx(stat_full(j), STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2);
+        const uint32_t slot = smem_u32(stat + j * WG_STAT_SLOT);
+        const int r = row0 + kb * WG_BK;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tma_load_2d(slot + q * 8192, sh, stat_full, f * 256 + half0 + q * 64, r, pol);
-            if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full, f * 256 + half0 + q * 64, r, pol);
-          }
+        for (int q = 0; q < 2; ++q) {
+          tma_load_2d(slot + q * 8192, sh, stat_full(j), f * 256 + half0 + q * 64, r, pol);
+          if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full(j), f * 256 + half0 + q * 64, r, pol);
         }
-        stat_pending = true;
+        ++sc;
         return true;
       };
       auto load_stream = [&](int i, int row0, int kb) {
@@ -174,20 +227,19 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         }
         return true;
       };
-      for (int round = 0, s = pair; s < total && ok; s = strip_at(++round)) {
-        int e, f, row0, rows, nkb;
-        strip(s, e, f, row0, rows, nkb);
+      for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+        int e, f, i0, i1, row0, rows, nkb;
+        item(n, e, f, i0, i1, row0, rows, nkb);
         if (nkb == 0) continue;
         if (nkb <= WG_KSTAT) {
-          ok = load_stat(f, row0, 0, nkb);
-          for (int i = 0; i < strip_len && ok; ++i)
+          for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stat(f, row0, kb);
+          for (int i = i0; i < i1 && ok; ++i)
             for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stream(i, row0, kb);
         } else {
-          for (int i = 0; i < strip_len && ok; ++i)
-            for (int kb0 = 0; kb0 < nkb && ok; kb0 += WG_KSTAT) {
-              const int nk = min(WG_KSTAT, nkb - kb0);
-              ok = load_stat(f, row0, kb0, nk);
-              for (int kb = kb0; kb < kb0 + nk && ok; ++kb) ok = load_stream(i, row0, kb);
+          for (int i = i0; i < i1 && ok; ++i)
+            for (int kb = 0; kb < nkb && ok; ++kb) {
+              ok = load_stat(f, row0, kb);
+              if (ok) ok = load_stream(i, row0, kb);
             }
         }
       }
@@ -195,7 +247,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         // Aborted: let no copy land in shared memory after the CTA has left.  The even CTA's full
         // barriers count both CTAs' stream bytes; the peer cannot observe its own and waits a while.
         volatile int no_abort = 0;
-        if (stat_pending) mbar_wait(stat_full, sphase ^ 1, &no_abort, args.status, SITE_GEMM_DRAIN);
+        // this CTA's stationary loads complete on its own barriers: wait for the last of each slot
+        for (int n = 1; n <= min(sc, WG_KSTAT); ++n)
+          mbar_wait(stat_full((sc - n) % WG_KSTAT), (uint32_t)((sc - n) / WG_KSTAT) & 1u, &no_abort, args.status,
+                    SITE_GEMM_DRAIN);
         if (rank == 0) {
           const int outstanding = min(issued, WGP_STAGES);
           int st = stage;
@@ -216,24 +271,26 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer (even CTA)
     constexpr uint32_t idesc = idesc_bf16_f32(256, 256, true, true);
-    const uint32_t stat_ready0_cl = mapa_shared(stat_ready, 0);
     int stage = 0;
-    uint32_t phase = 0, sphase = 0, rphase = 0;
+    uint32_t phase = 0;
+    int sc = 0;  // stationary K blocks taken so far, in the producer's order
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true, any = false;
-    // Both CTAs: wait for this CTA's stationary K blocks [kb0, kb0+nk), zero the rows past the
-    // expert's end, report to the even CTA; the even CTA then waits for both reports.
-    auto take_stat = [&](int rows, int kb0, int nk) {
+    // Both CTAs: wait for this CTA's stationary K block kb of the strip (slot sc % WG_KSTAT), zero
+    // its rows past the expert's end, report to the even CTA; the even CTA then waits for both
+    // reports.  Returns the slot.
+    auto take_stat = [&](int rows, int kb, int& j) {
+      j = sc % WG_KSTAT;
+      const uint32_t ph = (uint32_t)(sc / WG_KSTAT) & 1u;
+      ++sc;
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(stat_full, sphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+      if (lane == 0) w_ok = mbar_wait(stat_full(j), ph, abort_flag, args.status, SITE_GEMM_MMA_FULL);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
-      sphase ^= 1;
-      const int last = kb0 + nk - 1;
-      const int kvalid = rows - last * WG_BK;
+      const int kvalid = rows - kb * WG_BK;
       const int kend = (kvalid + 15) & ~15;
       if (kvalid < WG_BK && kvalid < kend) {
-        uint8_t* slot = stat + (nk - 1) * WG_STAT_SLOT;
+        uint8_t* slot = stat + j * WG_STAT_SLOT;
         const int nl = kend - kvalid;
         const uint4 z = make_uint4(0, 0, 0, 0);
         for (int idx = lane; idx < nl * 4 * 8; idx += 32) {
@@ -246,12 +303,11 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(stat_ready0_cl);
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(stat_ready(j), 0));
       if (rank == 0) {
         if (lane == 0)
-          w_ok = mbar_wait<true>(stat_ready, rphase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+          w_ok = mbar_wait<true>(stat_ready(j), ph, abort_flag, args.status, SITE_GEMM_MMA_FULL);
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
-        rphase ^= 1;
         tc_fence_after();
       }
       return true;
@@ -305,33 +361,34 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     };
-    auto release_stat = [&]() {
-      if (lane == 0) umma_commit_pair(stat_empty, 0x3);  // both CTAs' slots are free once these MMAs end
+    auto release_stat = [&](int j) {
+      if (lane == 0) umma_commit_pair(stat_empty(j), 0x3);  // both CTAs' slots are free once these MMAs end
       __syncwarp();
     };
-    for (int round = 0, s = pair; s < total && ok; s = strip_at(++round)) {
-      int e, f, row0, rows, nkb;
-      strip(s, e, f, row0, rows, nkb);
+    for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+      int e, f, i0, i1, row0, rows, nkb;
+      item(n, e, f, i0, i1, row0, rows, nkb);
       if (nkb == 0) continue;
       if (nkb <= WG_KSTAT) {
-        ok = take_stat(rows, 0, nkb);
+        int js[WG_KSTAT];
+        for (int kb = 0; kb < nkb && ok; ++kb) ok = take_stat(rows, kb, js[kb]);
         if (rank == 0) {
-          for (int i = 0; i < strip_len && ok; ++i) {
+          for (int i = i0; i < i1 && ok; ++i) {
             ok = begin_tile();
-            for (int kb = 0; kb < nkb && ok; ++kb) ok = mma_kblock(kb, rows, kb, kb == 0);
+            for (int kb = 0; kb < nkb && ok; ++kb) ok = mma_kblock(js[kb], rows, kb, kb == 0);
             if (ok) end_tile();
           }
-          if (ok) release_stat();
+          for (int kb = 0; kb < nkb && ok; ++kb) release_stat(js[kb]);
         }
       } else {
-        for (int i = 0; i < strip_len && ok; ++i) {
+        for (int i = i0; i < i1 && ok; ++i) {
           if (rank == 0) ok = begin_tile();
-          for (int kb0 = 0; kb0 < nkb && ok; kb0 += WG_KSTAT) {
-            const int nk = min(WG_KSTAT, nkb - kb0);
-            ok = take_stat(rows, kb0, nk);
-            if (rank == 0) {
-              for (int kb = kb0; kb < kb0 + nk && ok; ++kb) ok = mma_kblock(kb - kb0, rows, kb, kb == 0);
-              if (ok) release_stat();
+          for (int kb = 0; kb < nkb && ok; ++kb) {
+            int j;
+            ok = take_stat(rows, kb, j);
+            if (ok && rank == 0) {
+              ok = mma_kblock(j, rows, kb, kb == 0);
+              if (ok) release_stat(j);
             }
           }
           if (ok && rank == 0) end_tile();
@@ -359,10 +416,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     uint32_t acc_phase = 0;
     int tcount = 0;  // tiles with MMAs seen so far (both groups count all of them)
     bool ok = true;
-    for (int round = 0, s = pair; s < total && ok; s = strip_at(++round)) {
-      int e, f, row0, rows, nkb;
-      strip(s, e, f, row0, rows, nkb);
-      for (int i = 0; i < strip_len; ++i) {
+    for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+      int e, f, i0, i1, row0, rows, nkb;
+      item(n, e, f, i0, i1, row0, rows, nkb);
+      for (int i = i0; i < i1; ++i) {
         // this CTA's rows m and the tile's columns n (256)
         const int m0 = (STAT_A ? f : i) * 256 + half0;
         const int n0 = (STAT_A ? i : f) * 256;
