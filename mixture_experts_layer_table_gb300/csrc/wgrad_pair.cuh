@@ -134,13 +134,16 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   const int per_e = STAT_A ? MT : NT;   // strips per expert
   const int strip_len = STAT_A ? NT : MT;
   // Work items, dealt to the pairs in one fixed order:
-  //  * first, one item per output tile of each expert with more than WG_KSTAT K blocks of rows
-  //    (expert by expert, in s_list order; tiles of one stationary strip f in a row).  Its
-  //    stationary blocks are streamed again for every tile anyway, so the pairs spread over the
-  //    tiles of one expert at a time and share its rows in L2 (one pair per strip of 28 tiles, as
+  //  * first, one item per two neighbouring output tiles (i, i + 1) of one stationary strip f of
+  //    each expert with more than WG_KSTAT K blocks of rows (expert by expert, in s_list order).
+  //    Their stationary blocks are streamed again for every item, so the pairs spread over the
+  //    items of one expert at a time and share its rows in L2 (one pair per strip of 28 tiles, as
   //    the strips below are dealt, kept some five long experts in flight at once, more than L2
   //    holds: at 16 experts of 1024 rows, 45% of the operand reads hit L2 and dW13 took 2.3 us
-  //    per 64-row K block of a pair tile);
+  //    per 64-row K block of a pair tile; tile by tile over one expert, 1.6 us).  Both tiles
+  //    accumulate at once, one in each TMEM accumulator, so each stationary block that arrives
+  //    feeds twice the MMAs (the epilogue of an item then no longer overlaps its MMAs; at 16
+  //    experts of 1024 rows dW13 2.59 -> 2.02 ms, 1.34 us per K block of a pair tile);
   //  * then one item per strip (expert, 256-wide stationary tile f, all strip_len tiles) of the
   //    other experts, whose stationary blocks stay in shared memory for the whole strip (each
   //    expert's strips in a row, so neighbouring pairs share its streaming rows in L2).
@@ -149,7 +152,8 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   // other end in the next and the pairs' totals even out.  Every role of both CTAs walks the same
   // list.
   const int n_long = s_list[args.E];
-  const int tiles_e = per_e * strip_len;
+  const int pairs_f = (strip_len + 1) / 2;  // two-tile items per strip
+  const int tiles_e = per_e * pairs_f;       // two-tile items per long expert
   const int n_tile_items = n_long * tiles_e;
   const int total = n_tile_items + (args.E - n_long) * per_e;
   // item -> expert e, stationary strip f, tiles [i0, i1) along the strip, its rows
@@ -158,9 +162,9 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       const int le = n / tiles_e;
       const int local = n - le * tiles_e;
       e = s_list[le];
-      f = local / strip_len;
-      i0 = local - f * strip_len;
-      i1 = i0 + 1;
+      f = local / pairs_f;
+      i0 = 2 * (local - f * pairs_f);
+      i1 = min(i0 + 2, strip_len);
     } else {
       const int b = n - n_tile_items;
       const int se = b / per_e;
@@ -236,11 +240,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
           for (int i = i0; i < i1 && ok; ++i)
             for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stream(i, row0, kb);
         } else {
-          for (int i = i0; i < i1 && ok; ++i)
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-              ok = load_stat(f, row0, kb);
-              if (ok) ok = load_stream(i, row0, kb);
-            }
+          for (int kb = 0; kb < nkb && ok; ++kb) {
+            ok = load_stat(f, row0, kb);
+            for (int i = i0; i < i1 && ok; ++i) ok = load_stream(i, row0, kb);
+          }
         }
       }
       if (!ok) {
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       }
       return true;
     };
-    auto mma_kblock = [&](int j, int rows, int kb, bool first) {
+    auto mma_kblock = [&](int j, int rows, int kb, bool first, int next = 0) {
       int f_ok = 1;
       if (lane == 0) f_ok = mbar_wait<true>(full_bar(stage), phase, abort_flag, args.status, SITE_GEMM_MMA_FULL);
       if (!__shfl_sync(0xffffffffu, f_ok, 0)) return false;
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         const uint32_t shi = smem_u32(stat + j * WG_STAT_SLOT);
         const uint32_t slo = shi + 16384;
         const uint32_t sst = smem_u32(ring + stage * WG_STAGE);
-        const uint32_t d = tmem_base + acc * 256;
+        const uint32_t d = tmem_base + (acc ^ next) * 256;
         for (int k16 = 0; k16 < nk16; ++k16) {
           const uint64_t dh = smem_desc_sw128(shi + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
           const uint64_t dl = smem_desc_sw128(slo + k16 * 2048, MOK_MN_LBO, MOK_MN_SBO);
@@ -347,10 +350,14 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       }
       return true;
     };
-    auto begin_tile = [&]() {
+    // next = 1: the tile after the current one (the other accumulator; its use count is one more
+    // when the current one is accumulator 1)
+    auto begin_tile = [&](int next = 0) {
+      const int a = acc ^ next;
+      const uint32_t ph = (next && acc == 1) ? acc_phase ^ 1 : acc_phase;
       int w_ok = 1;
       if (lane == 0)
-        w_ok = mbar_wait<true>(tempty_bar(acc), acc_phase ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
+        w_ok = mbar_wait<true>(tempty_bar(a), ph ^ 1, abort_flag, args.status, SITE_GEMM_MMA_TMEM_EMPTY);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
       tc_fence_after();
       return true;
@@ -381,17 +388,24 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
           for (int kb = 0; kb < nkb && ok; ++kb) release_stat(js[kb]);
         }
       } else {
-        for (int i = i0; i < i1 && ok; ++i) {
-          if (rank == 0) ok = begin_tile();
-          for (int kb = 0; kb < nkb && ok; ++kb) {
-            int j;
-            ok = take_stat(rows, kb, j);
-            if (ok && rank == 0) {
-              ok = mma_kblock(j, rows, kb, kb == 0);
-              if (ok) release_stat(j);
-            }
+        // tiles i0 and i0 + 1 (if any) in the accumulators acc and acc ^ 1, K block by K block
+        const int nt = i1 - i0;
+        if (rank == 0) {
+          ok = begin_tile();
+          if (ok && nt == 2) ok = begin_tile(1);
+        }
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          int j;
+          ok = take_stat(rows, kb, j);
+          if (ok && rank == 0) {
+            ok = mma_kblock(j, rows, kb, kb == 0);
+            if (ok && nt == 2) ok = mma_kblock(j, rows, kb, kb == 0, 1);
+            if (ok) release_stat(j);
           }
-          if (ok && rank == 0) end_tile();
+        }
+        if (ok && rank == 0) {
+          end_tile();
+          if (nt == 2) end_tile();
         }
       }
     }
