@@ -14,10 +14,13 @@
 //
 // Warps (both CTAs): 0 TMA producer, 1 MMA issuer (even CTA) / stationary check (odd CTA), 2..9
 // epilogue in two groups of four, one per TMEM accumulator.  The stationary region is a ring of
-// WG_KSTAT slots of one 64-row K block each, with a full, a ready and an empty barrier per slot:
-// each CTA loads its stationary halves with plain TMA into its own full barrier, its warp 1
-// zeroes the rows past the expert's end and reports to the even CTA (ready, 2 arrivals) before
-// the pair's MMAs read the slot.  An expert of at most WG_KSTAT K blocks keeps its stationary
+// WG_KSTAT slots of one 64-row K block each.  A block that ends inside an MMA K step (the last of
+// an expert whose rows are not a multiple of 16) is loaded by each CTA onto its own full barrier;
+// its warp 1 zeroes the rows past the expert's end and reports to the even CTA (ready, 2
+// arrivals) before the pair's MMAs read the slot.  Every other block is loaded by both CTAs onto
+// the even CTA's pfull barrier, as the streaming stages are, with no report (the report's round
+// trip in every block held a long expert's pipeline: 16 experts of 1024 rows, dW13 2.02 ->
+// 1.34 ms without it).  An expert of at most WG_KSTAT K blocks keeps its stationary
 // blocks for the whole strip; a longer one streams them again for each tile, one block per slot,
 // up to WG_KSTAT blocks ahead of the MMAs.
 // Work items (single tiles of the long experts, then strips of the others; see the item list
@@ -43,7 +46,7 @@ constexpr int WGP_THREADS = 320;
 constexpr int WGP_STAGES = 5;
 constexpr int WGP_STG = 4096;  // one epilogue warp's staging block (32 x 32 fp32)
 // the barriers, the TMEM address and the abort flag share 256 bytes
-static_assert((2 * WGP_STAGES + 5 + 3 * WG_KSTAT) * 8 + 8 <= 256, "wgrad pair barriers");
+static_assert((2 * WGP_STAGES + 5 + 4 * WG_KSTAT) * 8 + 8 <= 256, "wgrad pair barriers");
 
 __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
   return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(WGP_STAGES) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + 256 +
@@ -61,9 +64,9 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WGP_STAGES stages
   uint8_t* stg_all = ring + WGP_STAGES * WG_STAGE;        // 8 epilogue warps x WGP_STG
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 8 * WGP_STG);
-  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full[K], stat_ready[K], stat_empty[K], drain
-  // (K = WG_KSTAT)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 3 * WG_KSTAT);
+  // bars: full[S], empty[S], tfull[2], tempty[2], stat_full[K], stat_ready[K], stat_empty[K], drain,
+  // stat_pfull[K] (K = WG_KSTAT)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 4 * WG_KSTAT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(stg_all + 8 * WGP_STG + 256);
   int* s_list = s_off + args.E + 1;  // experts with more than WG_KSTAT K blocks, then the others
@@ -81,6 +84,8 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   auto stat_ready = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 4 + WG_KSTAT + j]); };
   auto stat_empty = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 4 + 2 * WG_KSTAT + j]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * WGP_STAGES + 4 + 3 * WG_KSTAT]);
+  // a stationary block loaded by both CTAs onto the even CTA's barrier (no rows to zero)
+  auto stat_pfull = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 5 + 3 * WG_KSTAT + j]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < WGP_STAGES; ++s) {
@@ -95,6 +100,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       mbar_init(stat_full(j), 1);
       mbar_init(stat_ready(j), 2);  // warp 1 of both CTAs
       mbar_init(stat_empty(j), 1);
+      mbar_init(stat_pfull(j), 1);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -178,6 +184,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     nkb = (rows + WG_BK - 1) / WG_BK;
   };
   const int half0 = 128 * (int)rank;
+  // K block kb of an expert with `rows` rows ends inside an MMA K step: the stationary rows past
+  // the expert's end must be zeroed before the MMAs read them (each CTA its own, then a report)
+  auto stat_ragged = [&](int rows, int kb) {
+    const int kvalid = rows - kb * WG_BK;
+    return kvalid < WG_BK && (kvalid & 15) != 0;
+  };
   auto item_at = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
 
   if (warp == 0) {
@@ -196,20 +208,43 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;
       int sc = 0;  // stationary K blocks loaded so far: the next goes to slot sc % WG_KSTAT
+      uint32_t hs_ph = 0, pf_ph = 0;  // per slot: phase bits of its full and its pfull barrier
+      uint32_t last_pair = 0, last_ph = 0;  // per slot: its latest load's barrier kind and phase
+      const uint32_t pfull0_cl = mapa_shared(stat_pfull(0), 0);
       bool ok = true;
-      auto load_stat = [&](int f, int row0, int kb) {
+      auto load_stat = [&](int f, int row0, int rows, int kb) {
         const int j = sc % WG_KSTAT;
         const uint32_t ph = (uint32_t)(sc / WG_KSTAT) & 1u;
         if (!mbar_wait<true>(stat_empty(j), ph ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
                              kWaitLimitNs, 32))
           return false;
-        mbar_arrive_expect_tx(stat_full(j), STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2);
+        const uint32_t bytes = STAT_SPLIT ? WG_STAT_SLOT : WG_STAT_SLOT / 2;
         const uint32_t slot = smem_u32(stat + j * WG_STAT_SLOT);
         const int r = row0 + kb * WG_BK;
+        const uint32_t bit = 1u << j;
+        if (stat_ragged(rows, kb)) {
+          // rows past the expert's end to zero: each CTA's bytes on its own barrier
+          mbar_arrive_expect_tx(stat_full(j), bytes);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          tma_load_2d(slot + q * 8192, sh, stat_full(j), f * 256 + half0 + q * 64, r, pol);
-          if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full(j), f * 256 + half0 + q * 64, r, pol);
+          for (int q = 0; q < 2; ++q) {
+            tma_load_2d(slot + q * 8192, sh, stat_full(j), f * 256 + half0 + q * 64, r, pol);
+            if (STAT_SPLIT) tma_load_2d(slot + 16384 + q * 8192, sl, stat_full(j), f * 256 + half0 + q * 64, r, pol);
+          }
+          last_pair &= ~bit;
+          last_ph = (last_ph & ~bit) | (hs_ph & bit);
+          hs_ph ^= bit;
+        } else {
+          // both CTAs' bytes on the even CTA's barrier, as the streaming stages
+          if (rank == 0) mbar_arrive_expect_tx(stat_pfull(j), 2 * bytes);
+          const uint32_t pb = pfull0_cl + 8u * j;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            tma_load_2d_pair(slot + q * 8192, sh, pb, f * 256 + half0 + q * 64, r, pol);
+            if (STAT_SPLIT) tma_load_2d_pair(slot + 16384 + q * 8192, sl, pb, f * 256 + half0 + q * 64, r, pol);
+          }
+          last_pair |= bit;
+          last_ph = (last_ph & ~bit) | (pf_ph & bit);
+          pf_ph ^= bit;
         }
         ++sc;
         return true;
@@ -236,12 +271,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         item(n, e, f, i0, i1, row0, rows, nkb);
         if (nkb == 0) continue;
         if (nkb <= WG_KSTAT) {
-          for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stat(f, row0, kb);
+          for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stat(f, row0, rows, kb);
           for (int i = i0; i < i1 && ok; ++i)
             for (int kb = 0; kb < nkb && ok; ++kb) ok = load_stream(i, row0, kb);
         } else {
           for (int kb = 0; kb < nkb && ok; ++kb) {
-            ok = load_stat(f, row0, kb);
+            ok = load_stat(f, row0, rows, kb);
             for (int i = i0; i < i1 && ok; ++i) ok = load_stream(i, row0, kb);
           }
         }
@@ -250,10 +285,14 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         // Aborted: let no copy land in shared memory after the CTA has left.  The even CTA's full
         // barriers count both CTAs' stream bytes; the peer cannot observe its own and waits a while.
         volatile int no_abort = 0;
-        // this CTA's stationary loads complete on its own barriers: wait for the last of each slot
-        for (int n = 1; n <= min(sc, WG_KSTAT); ++n)
-          mbar_wait(stat_full((sc - n) % WG_KSTAT), (uint32_t)((sc - n) / WG_KSTAT) & 1u, &no_abort, args.status,
-                    SITE_GEMM_DRAIN);
+        // the latest stationary load of each slot: on this CTA's own barrier, or (pair form) on the
+        // even CTA's, which counts both CTAs' bytes; the odd CTA waits a while below
+        for (int j = 0; j < min(sc, WG_KSTAT); ++j) {
+          const uint32_t bit = 1u << j;
+          const uint32_t lp = (last_ph >> j) & 1u;
+          if (!(last_pair & bit)) mbar_wait(stat_full(j), lp, &no_abort, args.status, SITE_GEMM_DRAIN);
+          else if (rank == 0) mbar_wait(stat_pfull(j), lp, &no_abort, args.status, SITE_GEMM_DRAIN);
+        }
         if (rank == 0) {
           const int outstanding = min(issued, WGP_STAGES);
           int st = stage;
@@ -277,22 +316,36 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     int sc = 0;  // stationary K blocks taken so far, in the producer's order
+    uint32_t hs_ph = 0, pf_ph = 0;  // per slot: phase bits of its full / ready and its pfull barrier
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true, any = false;
-    // Both CTAs: wait for this CTA's stationary K block kb of the strip (slot sc % WG_KSTAT), zero
-    // its rows past the expert's end, report to the even CTA; the even CTA then waits for both
-    // reports.  Returns the slot.
+    // Stationary K block kb of the item, in slot sc % WG_KSTAT (returned in j).  Pair form: the even
+    // CTA waits for both CTAs' bytes on its pfull barrier.  Ragged form: each CTA waits for its own
+    // bytes, zeroes its rows past the expert's end and reports to the even CTA, which waits for both
+    // reports.
     auto take_stat = [&](int rows, int kb, int& j) {
       j = sc % WG_KSTAT;
-      const uint32_t ph = (uint32_t)(sc / WG_KSTAT) & 1u;
       ++sc;
+      const uint32_t bit = 1u << j;
       int w_ok = 1;
+      if (!stat_ragged(rows, kb)) {
+        const uint32_t ph = (pf_ph >> j) & 1u;
+        pf_ph ^= bit;
+        if (rank == 0) {
+          if (lane == 0) w_ok = mbar_wait<true>(stat_pfull(j), ph, abort_flag, args.status, SITE_GEMM_MMA_FULL);
+          if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
+          tc_fence_after();
+        }
+        return true;
+      }
+      const uint32_t ph = (hs_ph >> j) & 1u;
+      hs_ph ^= bit;
       if (lane == 0) w_ok = mbar_wait(stat_full(j), ph, abort_flag, args.status, SITE_GEMM_MMA_FULL);
       if (!__shfl_sync(0xffffffffu, w_ok, 0)) return false;
-      const int kvalid = rows - kb * WG_BK;
-      const int kend = (kvalid + 15) & ~15;
-      if (kvalid < WG_BK && kvalid < kend) {
+      {
+        const int kvalid = rows - kb * WG_BK;
+        const int kend = (kvalid + 15) & ~15;
         uint8_t* slot = stat + j * WG_STAT_SLOT;
         const int nl = kend - kvalid;
         const uint4 z = make_uint4(0, 0, 0, 0);
