@@ -37,12 +37,16 @@ REF_SAMPLE = {"T": 256, "E": 16}        # --impl reference: per step
 def _workloads():
     from mixture_experts_layer_table_gb300 import workloads as W
     return {"dsv3": W.DSV3, "dsv3_e16_t256": W.DSV3.scaled(name="dsv3_e16_t256", T=256, E=16),
-            "dsv3_e16_t1024": W.DSV3.scaled(name="dsv3_e16_t1024", T=1024, E=16)}
+            "dsv3_e16_t1024": W.DSV3.scaled(name="dsv3_e16_t1024", T=1024, E=16),
+            "dsv3_skew": W.DSV3_SKEW}
 
 
 WORKLOADS = _workloads()
 # forward expert GEMMs: library choice, CTA pairs (256-row tiles) or single CTAs (128-row tiles)
 GEMM_FLAGS = {"auto": 0, "pair": 2, "single": 4}
+# Kernels per traced library call where one call launches several: the schedule table is a
+# histogram, a scan and a placement kernel.
+KERNELS_PER_CALL = {"schedule": 3}
 
 
 def load_peaks():
@@ -481,12 +485,13 @@ def run_mok(args, rank, world, local_rank):
              "dgates": torch.empty((T, k), dtype=torch.float32, device=dev)}
     y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     x, wr, w13, w2, dy = inp["x"], inp["w_router"], inp["w13"], inp["w2"], inp["dy"]
+    bias0 = inp["router_bias"]  # the skewed workload's selection bias, else None
 
     def fwd():
-        layer.forward(x, wr, w13, w2, y=y)
+        layer.forward(x, wr, w13, w2, router_bias=bias0, y=y)
 
     def step():
-        layer.forward(x, wr, w13, w2, y=y)
+        layer.forward(x, wr, w13, w2, router_bias=bias0, y=y)
         layer.backward(dy, x, wr, w13, w2, out=grads)
 
     def barrier():
@@ -629,7 +634,7 @@ def run_mok(args, rank, world, local_rank):
         for i in range(n):
             b = i % 2
             stream.wait_event(ready[b])
-            layer.forward(x_d[b], wr, w13, w2, y=y_d[b])
+            layer.forward(x_d[b], wr, w13, w2, router_bias=bias0, y=y_d[b])
             g_e2e["dx"] = dx_d[b]
             layer.backward(dy_d[b], x_d[b], wr, w13, w2, out=g_e2e)
             done[b].record(stream)
@@ -753,7 +758,8 @@ def run_mok(args, rank, world, local_rank):
     dom = max(trace, key=lambda n: trace[n]["total_ms"])
     dom_avg_s = trace[dom]["total_ms"] / trace[dom]["launches"] * 1e-3
     achieved = kb[dom] / dom_avg_s / 1e9
-    traffic = load_traffic().get(dom)
+    # the committed DRAM counters were taken on the DSV3 layer with near-uniform routing
+    traffic = load_traffic().get(dom) if args.workload == "dsv3" else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": dom,
                 "peak_source": peak_kind}
@@ -764,7 +770,7 @@ def run_mok(args, rank, world, local_rank):
     fwd_gemm = [n for n in ("router_gemm", "gemm1_swiglu", "gemm2") if n in trace]
     fwd_gemm_ms = sum(trace[n]["total_ms"] / trace[n]["launches"] for n in fwd_gemm)
     fwd_gemm_tflops = sum(kf[n] for n in fwd_gemm) / (fwd_gemm_ms * 1e-3) / 1e12
-    launches = sum(t["launches"] for t in trace.values())
+    launches = sum(t["launches"] * KERNELS_PER_CALL.get(n, 1) for n, t in trace.items())
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
