@@ -302,6 +302,7 @@ def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
     import torch
 
     import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import _native as N
     from mixture_experts_layer_table_gb300 import workloads as W
 
     stream = torch.cuda.current_stream()
@@ -315,17 +316,20 @@ def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
         if layer.status() != (0, 0):
             raise RuntimeError("device status set during the ring warm-up")
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        N.trace_start(16 * steps + 16)
         e0.record(stream)
         for _ in range(steps):
             layer.forward(x, w_router, w13, w2, y=y)
         e1.record(stream)
         torch.cuda.synchronize()
+        trace = N.trace_stop()
         if layer.status() != (0, 0):
             raise RuntimeError("device status set in the ring forward")
         ms = e0.elapsed_time(e1) / steps
         sweep[str(m)] = {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
                          "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
-                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain))}
+                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain)),
+                         "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in trace.items()}}
         del layer
     return sweep
 

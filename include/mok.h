@@ -159,9 +159,10 @@ typedef struct {
                           rest in front of them */
   int64_t mb_tables;  /* i32 [n_mb][E+1] row offsets, [n_mb][E+1] tile offsets, [n_mb] tiles,
                           [n_mb+1] tile starts (exclusive prefix of the tiles) */
-  int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch; then
-                          (16-byte aligned) u64 [2] {ctx address, ctx ring_stamp} of the forward
-                          whose rows the ring holds */
+  int64_t mb_counters;/* i32 [2][n_mb]  rows gathered, tile epilogues finished, per minibatch; i32
+                          the GEMM1 tile counter the CTA pairs take tiles from; then (16-byte
+                          aligned) u64 [2] {ctx address, ctx ring_stamp} of the forward whose rows
+                          the ring holds */
   /* MXFP8 backward only (-1 otherwise): operands quantised along their GEMM's reduction
    * dimension, as exact bf16 values */
   int64_t mx_dhu_r;   /* bf16 [T*k][2I] dh | du in 32-row blocks of each expert (dW13) */

@@ -77,7 +77,9 @@ struct RingGeom {
 };
 
 // Byte offset of the ring stamp (u64 [2]) after the [2][n_mb] i32 counters.
-int64_t ring_stamp_offset(int n_mb) { return (int64_t(2) * n_mb * 4 + 15) & ~int64_t(15); }
+// counters: gathered [n_mb], consumed [n_mb], the tile ticket; then the stamp, 16-byte aligned
+int64_t ring_counter_ints(int n_mb) { return int64_t(2) * n_mb + 1; }
+int64_t ring_stamp_offset(int n_mb) { return (ring_counter_ints(n_mb) * 4 + 15) & ~int64_t(15); }
 
 mok_status ring_geometry(const mok_layer_desc* d, RingGeom* g) {
   const int64_t R = int64_t(d->T) * d->k;
@@ -145,7 +147,7 @@ mok_status fill_layout(const mok_layer_desc* d, mok_layout* L) {
     L->ring = take(int64_t(g.n_mb) * g.m * H * 2);
     // mb_off [n_mb][E+1], mb_toff [n_mb][E+1], mb_tiles [n_mb], mb_start [n_mb+1]
     L->mb_tables = take((int64_t(2) * g.n_mb * (E + 1) + 2 * int64_t(g.n_mb) + 1) * 4);
-    // counters [2][n_mb], then the u64 [2] stamp of the forward that filled the ring
+    // counters [2][n_mb] and the tile ticket, then the u64 [2] stamp of the forward that filled the ring
     L->mb_counters = take(ring_stamp_offset(g.n_mb) + 16);
   }
   L->mx_dhu_r = L->mx_xg_r = L->mx_do_r = L->mx_a_r = L->mx_blk_off = -1;
@@ -355,9 +357,10 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     int32_t* counters = at<int32_t>(ws, L.mb_counters);
     const int ring_variant = gemm_variant(d, GEMM1);
     MOK_LAUNCH("ring_tables", st,
-               mok::launch_mb_tables(offsets, E, R, rg.m, rg.n_mb, I / 128, mok::ring_chunk_rows(ring_variant), mb_off,
+               mok::launch_mb_tables(offsets, E, R, rg.m, rg.n_mb, mok::ring_tiles_per_chunk(ring_variant, R, E, I),
+                                     mok::ring_chunk_rows(ring_variant), mb_off,
                                      mb_toff, mb_tiles, mb_start, st));
-    MOK_CUDA(cudaMemsetAsync(counters, 0, sizeof(int32_t) * 2 * rg.n_mb, st));
+    MOK_CUDA(cudaMemsetAsync(counters, 0, sizeof(int32_t) * ring_counter_ints(rg.n_mb), st));
     mok::RingArgs ra;
     ra.x = x;
     ra.src_of = src_of;
@@ -379,6 +382,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     ra.mb_start = mb_start;
     ra.gathered = counters;
     ra.consumed = counters + rg.n_mb;
+    ra.ticket = counters + 2 * rg.n_mb;
     MOK_LAUNCH("ring_gemm1_swiglu", st,
                mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, ring_variant, st));
     // the ring rows are this forward's (the backward reuses them when it is given this ws)

@@ -439,20 +439,32 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
 }
 
 // Ring GEMM1 on the narrow-segment CTA-pair kernel: chunks of at most 256 rows of each expert's
-// segment in a minibatch, 128 intermediate indices (64 gate + 64 up rows per CTA) per pair tile.
+// segment in a minibatch, 128 intermediate indices (64 gate + 64 up rows per CTA) per pair tile,
+// or, where the plain forward takes the paired SwiGLU form (>= 384 rows per expert, whole
+// 256-index tiles), 256 (128 gate + 128 up rows per CTA).
 constexpr int RING_NARROW_NMAX = 256;
 
 int ring_chunk_rows(int variant) { return variant == GEMM_NARROW ? RING_NARROW_NMAX : BM; }
 
+bool ring_gemm1_paired(int variant, int R, int E, int I) {
+  return variant == GEMM_NARROW && (long long)R >= 384LL * E && I % 256 == 0;
+}
+
+int ring_tiles_per_chunk(int variant, int R, int E, int I) {
+  return ring_gemm1_paired(variant, R, E, I) ? I / 256 : I / 128;
+}
+
 namespace {
 
+template <int EPI>
 cudaError_t launch_ring_gemm1_narrow(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                                      int* status, int n_sm, cudaStream_t st) {
-  using C = NarrowCfg<false, false, RING_NARROW_NMAX, EPI_SWIGLU>;
+  using C = NarrowCfg<false, false, RING_NARROW_NMAX, EPI>;
   static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
   const uint64_t ring_rows = (uint64_t)ra.ring_slots * ra.mb_rows;
   CUtensorMap tw, tx, txs;
-  if (!tmap_w13_gate_up(&tw, w13, ra.H, ra.I, ra.E, 64) || !tmap_2d(&tx, ra.ring, ra.H, ring_rows, BK, NARROW_XBOX) ||
+  if (!tmap_w13_gate_up(&tw, w13, ra.H, ra.I, ra.E, EPI == EPI_SWIGLU_PAIRED ? 128 : 64) ||
+      !tmap_2d(&tx, ra.ring, ra.H, ring_rows, BK, NARROW_XBOX) ||
       !tmap_2d(&txs, ra.ring, ra.H, ring_rows, BK, NARROW_XBOX_S))
     return cudaErrorInvalidValue;
   // whole clusters of gathering CTAs, at least one pair of GEMM CTAs
@@ -479,11 +491,12 @@ cudaError_t launch_ring_gemm1_narrow(const RingArgs& ra, const void* w13, float*
   g.mb_start = ra.mb_start;
   g.gathered = ra.gathered;
   g.consumed = ra.consumed;
-  g.consume_per_tile = 8;  // four epilogue warps in each CTA of the pair
+  g.consume_per_tile = 2 * C::EPI_WARPS;  // every epilogue warp of both CTAs of the pair
+  g.ticket = ra.ticket;
   g.x = reinterpret_cast<const __nv_bfloat16*>(ra.x);
   g.src_of = ra.src_of;
   g.ring = reinterpret_cast<__nv_bfloat16*>(ra.ring);
-  auto kern = gemm_narrow_kernel<false, false, RING_NARROW_NMAX, EPI_SWIGLU, true>;
+  auto kern = gemm_narrow_kernel<false, false, RING_NARROW_NMAX, EPI, true>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
   // gathering and GEMM CTAs wait on each other: the launch is cooperative (all CTAs resident at
@@ -523,7 +536,10 @@ cudaError_t launch_ring_gemm1_narrow(const RingArgs& ra, const void* w13, float*
 
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, int variant, cudaStream_t st) {
-  if (variant == GEMM_NARROW) return launch_ring_gemm1_narrow(ra, w13, hu, act_hi, act_lo, status, n_sm, st);
+  if (ring_gemm1_paired(variant, ra.R, ra.E, ra.I))
+    return launch_ring_gemm1_narrow<EPI_SWIGLU_PAIRED>(ra, w13, hu, act_hi, act_lo, status, n_sm, st);
+  if (variant == GEMM_NARROW)
+    return launch_ring_gemm1_narrow<EPI_SWIGLU>(ra, w13, hu, act_hi, act_lo, status, n_sm, st);
   using C = GemmCfg<MODE_RING, EPI_SWIGLU, SPLIT_NONE, 256>;
   CUtensorMap ta, tb;
   const uint64_t ring_rows = (uint64_t)ra.ring_slots * ra.mb_rows;

@@ -108,6 +108,7 @@ struct GemmArgs {
   int* gathered;            // [n_mb] rows gathered
   int* consumed;            // [n_mb] epilogue warps finished (consume_per_tile per tile)
   int consume_per_tile;     // epilogue warps counting out one tile (4, or 8 for a CTA pair)
+  int* ticket;              // narrow ring GEMM1: next tile to take (one counter for all pairs)
   const __nv_bfloat16* x;   // [T][H] tokens
   const int* src_of;        // [R]
   __nv_bfloat16* ring;      // [ring_slots * mb_rows][H]
@@ -582,12 +583,49 @@ __device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src, uin
   }
 }
 
+// Minibatch 0 of the ring, copied by every CTA of the launch before it takes its role (one row
+// per warp at a time, rows dealt over all warps of the grid), so that no GEMM CTA waits for the
+// gathering CTAs alone to fill the first slot: at T = 16384 with 2368-token minibatches the first
+// slot holds 271 MB, about half a millisecond for 12 gathering SMs.  The gathering CTAs go on from
+// minibatch 1.
+__device__ void ring_gather_first(const GemmArgs& a) {
+  const int warps = (int)(blockDim.x >> 5);
+  const int gw = (int)blockIdx.x * warps + (int)(threadIdx.x >> 5);
+  const int nw = (int)gridDim.x * warps;
+  const int rows = min(a.mb_rows, a.R);
+  const int slot = a.ring_shift % a.ring_slots;
+  const int vec = a.H / 8;  // 16-byte words of a row
+  int cnt = 0;
+  for (int i = gw; i < rows; i += nw, ++cnt) {
+    const int tok = a.src_of[i] / a.k_top;
+    copy_row_warp(reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H),
+                  reinterpret_cast<uint4*>(a.ring + ((size_t)slot * a.mb_rows + i) * a.H), vec, threadIdx.x & 31);
+  }
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0 && cnt > 0) atomicAdd(&a.gathered[0], cnt);
+}
+
+// staging barriers of ring_gather (one per row buffer of the CTA's shared memory, at most 16)
+__device__ __forceinline__ int ring_gather_slots(const GemmArgs& a, int buf_bytes) {
+  return min(16, buf_bytes / (a.H * 2));
+}
+
+// After ring_gather: its staging barriers are invalidated so that the CTA can set up other
+// barriers in the same shared memory (every copy that completes on them has landed).
+__device__ void ring_gather_retire(const GemmArgs& a, int buf_bytes, uint64_t* bars) {
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int j = 0; j < ring_gather_slots(a, buf_bytes); ++j)
+      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[j])) : "memory");
+  __syncthreads();
+}
+
 __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint64_t* bars) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int copy_warps = (int)(blockDim.x >> 5) - 1;  // warps 1.. copy through registers
   const uint32_t row_bytes = (uint32_t)a.H * 2;
-  int ns = buf_bytes / (int)row_bytes;
-  if (ns > 16) ns = 16;
+  const int ns = ring_gather_slots(a, buf_bytes);
   if (threadIdx.x == 0) {
     for (int j = 0; j < ns; ++j) mbar_init(smem_u32(&bars[j]), 1);
     fence_mbar_init();
@@ -596,7 +634,7 @@ __device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint
   volatile int no_abort = 0;
   long long gcount = 0;  // bulk rows this CTA has staged so far (slot = gcount % ns, parity = gcount / ns)
   long long issued = 0;  // bulk rows whose load has been issued
-  for (int mb = 0; mb < a.n_mb; ++mb) {
+  for (int mb = 1; mb < a.n_mb; ++mb) {  // minibatch 0: ring_gather_first, by every CTA
     const int slot = (mb + a.ring_shift) % a.ring_slots;
     const int r0 = mb * a.mb_rows;
     const int rows = min(a.mb_rows, a.R - r0);
@@ -730,6 +768,7 @@ __global__ void __launch_bounds__(GemmCfg<MODE, EPI, SPLIT, BN_>::THREADS, 1)
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
 
+  if (MODE == MODE_RING) ring_gather_first(args);
   if (MODE == MODE_RING && (int)blockIdx.x < args.comm_ctas) {
     ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
     return;

@@ -85,12 +85,19 @@ struct NarrowCfg {
 // tmX / tmX2: X hi / lo in 64-row boxes; tmXs / tmX2s: the same in 32-row boxes.  tmW (SwiGLU):
 // W13 seen as [E][2][I][H], one box = 64 gate rows and their 64 up rows.
 //
-// RING (GEMM1 of the ring forward): X is the token ring [slots * mb_rows][H].  The first
-// args.comm_ctas CTAs (an even number, whole clusters) gather minibatch after minibatch into the
-// ring (ring_gather, as in gemm.cuh); the CTA pairs run the narrow tiles of each minibatch's
-// expert segments (args.mb_off / mb_toff: row offsets and chunk prefixes per minibatch,
-// args.mb_start: the tiles before each minibatch), wait for a minibatch's rows before loading
-// them, and count each tile's epilogue warps out on args.consumed so that the slot can be refilled.
+// RING (GEMM1 of the ring forward): X is the token ring [slots * mb_rows][H].  Every CTA first
+// copies minibatch 0 into the ring (ring_gather_first); then the first args.comm_ctas CTAs (an
+// even number, whole clusters) gather the later minibatches (ring_gather, as in gemm.cuh) while
+// the CTA pairs run the narrow tiles of each minibatch's expert segments (args.mb_off / mb_toff:
+// row offsets and chunk prefixes per minibatch, args.mb_start: the tiles before each minibatch),
+// wait for a minibatch's rows before loading them, and count each tile's epilogue warps out on
+// args.consumed so that the slot can be refilled.  Once a gathering pair has gathered its share of
+// every minibatch it runs tiles too.  So the tiles are not dealt in a fixed order but taken from
+// one counter (args.ticket) in tile order: the even CTA's producer takes a tile and passes it to
+// the roles of both CTAs through a TQ-deep queue in shared memory (each entry with a full
+// barrier in both CTAs and an empty barrier in the even CTA); -1 ends the queue.  Which pair
+// computes a tile does not change its result: each output element is still one tile's
+// accumulator over K in a fixed order.
 template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
 __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
@@ -103,27 +110,32 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // C::XBUF_BYTES
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, tq_full[TQ], tq_empty[TQ]
+  constexpr int TQ = 4;  // RING: depth of the tile queue
+  static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= 256, "barriers, TMEM address and abort flag");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + 256);
   int* s_coff = s_off + (args.E + 1);
+  volatile int* tq = s_off;  // RING: the tile queue (the segment tables are not used there)
 
+  if (RING) ring_gather_first(args);
   if (RING && (int)blockIdx.x < args.comm_ctas) {
     ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
-    return;
+    ring_gather_retire(args, STAGES * STAGE_BYTES, bars);  // then this pair runs tiles as well
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
-  const int cta0 = RING ? args.comm_ctas : 0;
-  const int pair = ((int)blockIdx.x - cta0) >> 1;
-  const int npairs = ((int)gridDim.x - cta0) >> 1;
+  const int pair = (int)blockIdx.x >> 1;  // the fixed deal (not RING)
+  const int npairs = (int)gridDim.x >> 1;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + a]); };
   auto tempty_bar = [&](int a) { return smem_u32(&bars[2 * STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * STAGES + 4]);
+  auto tq_full = [&](int q) { return smem_u32(&bars[2 * STAGES + 5 + q]); };
+  auto tq_empty = [&](int q) { return smem_u32(&bars[2 * STAGES + 5 + TQ + q]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -133,6 +145,12 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       mbar_init(tempty_bar(a), 2 * C::EPI_WARPS);  // every epilogue warp of both CTAs
+    }
+    for (int q = 0; q < TQ; ++q) {
+      mbar_init(tq_full(q), 1);
+      // readers of a queue entry: the even CTA's MMA warp and the odd CTA's producer, and every
+      // epilogue warp of both CTAs
+      mbar_init(tq_empty(q), 2 + 2 * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -185,6 +203,34 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     return t;
   };
 
+  // RING: the n-th tile of this pair from the tile queue (-1: no more).  The even CTA's producer
+  // (one thread) waits until entry n % TQ has been read by everyone, takes the next ticket and
+  // writes it into both CTAs' queues; every other reader (one thread of a warp) waits for the
+  // entry, reads it and counts itself out on the even CTA's empty barrier.
+  auto publish_tile = [&](int n, int& g) -> bool {
+    const int q = n % TQ;
+    const uint32_t u = (uint32_t)(n / TQ) & 1u;
+    if (!mbar_wait<true>(tq_empty(q), u ^ 1, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, 32))
+      return false;
+    g = atomicAdd(args.ticket, 1);
+    if (g >= total) g = -1;
+    tq[q] = g;
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&tq[q])), 1), (uint32_t)g);
+    mbar_arrive(tq_full(q));
+    mbar_arrive_cluster(mapa_shared(tq_full(q), 1));  // release: the peer's copy is written
+    return true;
+  };
+  auto read_tile = [&](int n, int& g, uint32_t sleep_ns) -> bool {
+    const int q = n % TQ;
+    const uint32_t u = (uint32_t)(n / TQ) & 1u;
+    if (!mbar_wait<true>(tq_full(q), u, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, sleep_ns))
+      return false;
+    g = tq[q];
+    if (rank == 0) mbar_arrive(tq_empty(q));
+    else mbar_arrive_cluster(mapa_shared(tq_empty(q), 0));
+    return true;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -204,7 +250,13 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       int issued = 0;
       bool ok = true;
       int ring_ready = -1;  // RING: last minibatch known to be gathered
-      for (int g = pair; g < total && ok; g += npairs) {
+      for (int n = 0; ok; ++n) {
+        int g = pair + n * npairs;
+        if (RING && !(rank == 0 ? publish_tile(n, g) : read_tile(n, g, 32))) {
+          ok = false;
+          break;
+        }
+        if (g < 0 || g >= total) break;
         int mb, ring_row0;
         const NarrowTile t = decode(g, mb, ring_row0);
         if (RING && mb > ring_ready) {
@@ -311,7 +363,18 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       bool ok = true;
       bool any_mma = false;
       const uint32_t a_lbo = WMN ? MOK_MN_LBO : 16, a_sbo = WMN ? MOK_MN_SBO : 1024;
-      for (int g = pair; g < total && ok; g += npairs) {
+      for (int n = 0; ok; ++n) {
+        int g = pair + n * npairs;
+        if (RING) {
+          int r_ok = 1;
+          if (lane == 0) r_ok = read_tile(n, g, 32);
+          g = __shfl_sync(0xffffffffu, g, 0);
+          if (!__shfl_sync(0xffffffffu, r_ok, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (g < 0 || g >= total) break;
         int mb_unused, rr_unused;
         const NarrowTile t = decode(g, mb_unused, rr_unused);
         uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
@@ -383,7 +446,15 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     float* out = reinterpret_cast<float*>(args.out0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int g = pair; g < total; g += npairs) {
+    for (int n = 0;; ++n) {
+      int g = pair + n * npairs;
+      if (RING) {
+        int r_ok = 1;
+        if (lane == 0) r_ok = read_tile(n, g, 256);
+        g = __shfl_sync(0xffffffffu, g, 0);
+        if (!__shfl_sync(0xffffffffu, r_ok, 0)) break;
+      }
+      if (g < 0 || g >= total) break;
       int mb, rr_unused;
       const NarrowTile t = decode(g, mb, rr_unused);
       int w_ok = 1;

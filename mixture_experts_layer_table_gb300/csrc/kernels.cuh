@@ -93,10 +93,14 @@ struct RingArgs {
   const int32_t* mb_start;
   int32_t* gathered;
   int32_t* consumed;
+  int32_t* ticket;  // the narrow ring GEMM1's tile counter (zero at launch)
 };
 // variant GEMM_NARROW: the narrow-segment CTA-pair kernel (minibatch tables in chunks of
 // ring_chunk_rows() rows); else the row-tile kernel (128-row tiles)
 int ring_chunk_rows(int variant);
+// weight tiles per row chunk of the ring GEMM1 (its form follows the plain GEMM1's: paired SwiGLU
+// tiles of 256 intermediate indices from 384 rows per expert, else 128)
+int ring_tiles_per_chunk(int variant, int R, int E, int I);
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, int variant, cudaStream_t st);
 // MXFP8 weights (mx.cu)

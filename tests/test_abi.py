@@ -127,7 +127,7 @@ def _region_sizes(shp, ring_slots=0, minibatch=0):
         n_mb = -(-R // minibatch)
         ws.update({"ring": n_mb * minibatch * H * 2,
                    "mb_tables": (2 * n_mb * (E + 1) + n_mb + (n_mb + 1)) * 4,
-                   "mb_counters": ((2 * n_mb * 4 + 15) // 16) * 16 + 16})
+                   "mb_counters": (((2 * n_mb + 1) * 4 + 15) // 16) * 16 + 16})
     if shp.mxfp8:
         ws.update({"mx_dhu_r": R * 2 * I * 2, "mx_xg_r": R * H * 2,
                    "mx_do_r": R * H * 2, "mx_a_r": R * I * 2, "mx_blk_off": (E + 1) * 4})

@@ -246,6 +246,27 @@ def test_weight_gradients_pair_and_single_bitwise_with_a_hot_expert():
         assert torch.equal(g[name], g1[name]), name
 
 
+@pytest.mark.parametrize("T", [1200, 1199])
+def test_weight_gradients_of_long_experts_on_odd_strips(T):
+    """Every token takes all four experts, so each expert has T rows: far more than the pair
+    kernel's three stationary K blocks, so its tiles are dealt two at a time.  With H = 768 a dW13
+    strip has three tiles (its last item one tile); T = 1200 has no K block ending inside an MMA
+    K step, T = 1199 has one per expert.  The pair kernel is bitwise the single-CTA kernel and
+    both meet the bar against the oracle."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    shape = W.MoEShape(f"odd_strip_T{T}_H768_E4_I512_top4", T=T, H=768, E=4, I=512, k=4,
+                       router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.03)
+    inp = W.make_inputs(shape, seed=6, device="cpu")
+    f64 = inputs_f64(inp)
+    given = np.tile(np.arange(4, dtype=np.int32), (T, 1))
+    _, bwd = oracle_layer(shape, f64, topk_idx=given)
+    _, _, g = _run(shape, inp, given=given)
+    _, _, g1 = _run(shape, inp, given=given, flags=N.FLAG_GEMM_SINGLE)
+    for name in ("dw13", "dw2"):
+        assert torch.equal(g[name], g1[name]), name
+        assert_bf16_close(to_f64(g[name]), bwd[name], name)
+
+
 def test_empty_experts_get_zero_weight_gradient():
     shape = MID
     inp = W.make_inputs(shape, seed=1, device="cpu")
@@ -358,6 +379,8 @@ def test_stuck_wait_times_out_and_context_survives():
     (MID_SKEW, 700, 3, 2, 0),   # skewed experts cut at minibatch edges
     (TINY, 96, 2, 2, 0),        # tiny layer, softmax router
     (LONG, 3000, 2, 6, 0),      # 750 rows per expert: chunks of up to 256 rows cut at minibatch edges
+    (LONG, 700, 3, 4, 0),       # the paired SwiGLU GEMM1 (>= 384 rows per expert) on ragged cuts
+    (LONG_SKEW, 1000, 2, 2, 0),  # paired GEMM1, hot and cold experts cut at minibatch edges
     (MID, 300, 2, 3, "single"),  # the row-tile ring kernel (one CTA per 128-row tile), odd comm count
     (MID_SKEW, 700, 2, 4, "pair"),  # the row-tile ring kernel under the CTA-pair flag
     (ODD, 500, 2, 4, 0),        # H and I odd multiples of 128
@@ -409,7 +432,7 @@ def test_ring_backward_reuses_the_resident_minibatches():
     n_mb = -(-R // minibatch)
     head = (n_mb - slots) * minibatch
     stamp_ws = ring.ws[ring.layout["mb_counters"]:].view(torch.int32)
-    off = ((2 * n_mb * 4 + 15) // 16) * 4  # the u64 stamp after the counters, in int32 units
+    off = (((2 * n_mb + 1) * 4 + 15) // 16) * 4  # the u64 stamp after the counters, in int32 units
     stamp = stamp_ws[off:off + 4].view(torch.int64).cpu().tolist()
     assert stamp == [ring.ctx.data_ptr(), int(ring.view("ring_stamp")[0])]
     src = ring.view("src_of").cpu().numpy().astype(np.int64) // shape.k
