@@ -396,10 +396,11 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
                      CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     }
-    static_assert(wgrad_pair_smem_bytes(1024) <= 232448, "shared memory budget");
+    // the largest shared memory of any E: six stages up to WGP_E_SIX experts, five up to 1024
+    constexpr size_t smem_max = std::max(wgrad_pair_smem_bytes(WGP_E_SIX), wgrad_pair_smem_bytes(1024));
+    static_assert(smem_max <= 232448, "shared memory budget");
     auto run_pair = [&](auto kern) {
-      cudaError_t err =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wgrad_pair_smem_bytes(1024));
+      cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
       if (err != cudaSuccess) return err;
       cudaLaunchConfig_t cfg{};
       cudaLaunchAttribute attr[1];

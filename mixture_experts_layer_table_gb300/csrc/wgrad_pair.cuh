@@ -43,14 +43,21 @@
 namespace mok {
 
 constexpr int WGP_THREADS = 320;
-constexpr int WGP_STAGES = 5;
+// Streaming stages: six while the expert tables leave room (E <= WGP_E_SIX), else five.  A long
+// expert's item needs two stages per K block (one per tile), so six keep three K blocks in
+// flight, as many as the stationary ring holds.
+constexpr int WGP_STAGES = 6;  // barriers are laid out for this many
+constexpr int WGP_E_SIX = 297;
+__host__ __device__ constexpr int wgp_stages(int E) { return E <= WGP_E_SIX ? 6 : 5; }
 constexpr int WGP_STG = 4096;  // one epilogue warp's staging block (32 x 32 fp32)
 // the barriers, the TMEM address and the abort flag share 256 bytes
 static_assert((2 * WGP_STAGES + 5 + 4 * WG_KSTAT) * 8 + 8 <= 256, "wgrad pair barriers");
 
+// stationary slots, streaming stages, epilogue staging, alignment, barriers, the row offsets
+// (i32 [E + 1]) and the expert list (u16 [E + 1])
 __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
-  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(WGP_STAGES) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + 256 +
-         size_t(E + 1) * 4 * 2;
+  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(wgp_stages(E)) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + 256 +
+         size_t(E + 1) * 4 + size_t(E + 1) * 2;
 }
 
 template <bool STAT_A, bool OUT_F32, bool STAT_SPLIT = true>
@@ -61,15 +68,17 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stat = smem;                                   // WG_KSTAT slots
-  uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // WGP_STAGES stages
-  uint8_t* stg_all = ring + WGP_STAGES * WG_STAGE;        // 8 epilogue warps x WGP_STG
+  const int nst = wgp_stages(args.E);
+  uint8_t* ring = stat + WG_KSTAT * WG_STAT_SLOT;         // nst stages
+  uint8_t* stg_all = ring + nst * WG_STAGE;               // 8 epilogue warps x WGP_STG
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 8 * WGP_STG);
   // bars: full[S], empty[S], tfull[2], tempty[2], stat_full[K], stat_ready[K], stat_empty[K], drain,
   // stat_pfull[K] (K = WG_KSTAT)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 4 * WG_KSTAT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_off = reinterpret_cast<int*>(stg_all + 8 * WGP_STG + 256);
-  int* s_list = s_off + args.E + 1;  // experts with more than WG_KSTAT K blocks, then the others
+  // experts with more than WG_KSTAT K blocks, then the others; [E] = how many are first
+  uint16_t* s_list = reinterpret_cast<uint16_t*>(s_off + args.E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -88,7 +97,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   auto stat_pfull = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 5 + 3 * WG_KSTAT + j]); };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < WGP_STAGES; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -118,12 +127,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         const bool is_long = e < args.E && args.offsets[e + 1] - args.offsets[e] > WG_KSTAT * WG_BK;
         const bool take = e < args.E && (pass == 0 ? is_long : !is_long);
         const uint32_t m = __ballot_sync(0xffffffffu, take);
-        if (take) s_list[at + __popc(m & ((1u << lane) - 1u))] = e;
+        if (take) s_list[at + __popc(m & ((1u << lane) - 1u))] = (uint16_t)e;
         at += __popc(m);
       }
       if (pass == 0) n_long = at;
     }
-    if (lane == 0) s_list[args.E] = n_long;
+    if (lane == 0) s_list[args.E] = (uint16_t)n_long;
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), 512);
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         for (int q = 0; q < 2; ++q)
           tma_load_2d_pair(sa + q * 8192, st_map, fb, i * 256 + half0 + q * 64, row0 + kb * WG_BK, pol);
         ++issued;
-        if (++stage == WGP_STAGES) {
+        if (++stage == nst) {
           stage = 0;
           phase ^= 1;
         }
@@ -294,12 +303,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
           else if (rank == 0) mbar_wait(stat_pfull(j), lp, &no_abort, args.status, SITE_GEMM_DRAIN);
         }
         if (rank == 0) {
-          const int outstanding = min(issued, WGP_STAGES);
+          const int outstanding = min(issued, nst);
           int st = stage;
           uint32_t ph = phase;
           for (int n = 0; n < outstanding; ++n) {
             if (--st < 0) {
-              st = WGP_STAGES - 1;
+              st = nst - 1;
               ph ^= 1;
             }
             mbar_wait(full_bar(st), ph, &no_abort, args.status, SITE_GEMM_DRAIN);
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       }
       __syncwarp();
       any = true;
-      if (++stage == WGP_STAGES) {
+      if (++stage == nst) {
         stage = 0;
         phase ^= 1;
       }
