@@ -605,6 +605,12 @@ def run_mok(args, rank, world, local_rank):
                 "expert_rows_min_max": [int(sc.min()), int(sc.max())],
                 "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in skew_trace.items()}}
 
+    # ---- the tiny layer (T=256, H=256, 8 experts, I=512, top-2 softmax): launch-bound, so timed
+    #      eager and as one CUDA graph of the whole forward + backward, replayed
+    tiny = None
+    if not args.no_tiny:
+        tiny = tiny_layer_step(args.steps, args.warmup, dev, stream, max_over_ranks, barrier)
+
     # ---- end to end through the public API with host buffers (pinned), copies timed.  Every
     #      step copies its own x and dY in and its y and dX out; a copy stream moves step i+1's
     #      inputs and step i-1's outputs while step i computes (two device buffer sets).
@@ -816,6 +822,7 @@ def run_mok(args, rank, world, local_rank):
                         "the copies of neighbouring steps overlap the compute on a second stream"},
         "wgrad_bf16": wgrad_bf16 if wgrad_bf16_ms is not None else None,
         "skew_fwd_bwd": skew,
+        "tiny_fwd_bwd": tiny,
         "fwd_bwd_ms_wgrad_bf16": round(wgrad_bf16_ms, 4) if wgrad_bf16_ms is not None else None,
         "mxfp8_fwd": mx,
         "tensor_bound_fwd": tb,
@@ -827,6 +834,63 @@ def run_mok(args, rank, world, local_rank):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def tiny_layer_step(steps, warmup, dev, stream, max_over_ranks, barrier):
+    """The tiny layer's forward + backward: ms per step eager and as a replayed CUDA graph (the
+    captured step is checked bitwise against the eager one)."""
+    import torch
+
+    import mixture_experts_layer_table_gb300 as mok
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    shp = W.TINY
+    T, H, E, I, k = shp.T, shp.H, shp.E, shp.I, shp.k
+    inp = W.make_inputs(shp, seed=0, device=str(dev))
+    layer = mok.MoELayer(mok.desc_from_shape(shp), device=dev)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    g = {"dx": torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+         "dw_router": torch.empty((E, H), dtype=torch.float32, device=dev),
+         "dw13": torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev),
+         "dw2": torch.empty((E, H, I), dtype=torch.float32, device=dev),
+         "dgates": torch.empty((T, k), dtype=torch.float32, device=dev)}
+
+    def step():
+        layer.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"], y=y)
+        layer.backward(inp["dy"], inp["x"], inp["w_router"], inp["w13"], inp["w2"], out=g)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(steps, 100)  # each step is tens of microseconds
+
+    def timed(run):
+        for _ in range(warmup):
+            run()
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1) / n)
+
+    eager_ms = timed(step)
+    y0, g0 = y.clone(), {name: t.clone() for name, t in g.items()}
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph_ms = timed(graph.replay)
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set in the tiny layer")
+    same = bool(torch.equal(y, y0) and all(torch.equal(g[name], g0[name]) for name in g))
+    return {"workload": shp.name, "steps": n, "eager_ms": round(eager_ms, 4), "graph_ms": round(graph_ms, 4),
+            "tokens_per_s_eager": round(T / (eager_ms * 1e-3), 1), "tokens_per_s_graph": round(T / (graph_ms * 1e-3), 1),
+            "graph_bitwise_equal_to_eager": same}
 
 
 def tensor_bound_forward(shp, x, w_router, w13, w2, steps, warmup, flags=0):
@@ -1025,6 +1089,7 @@ def main():
                     help="skip the ring-forward minibatch sweep at T=16384 in the default line")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 forward and forward+backward timing")
     ap.add_argument("--no-skew", action="store_true", help="skip the skewed-routing forward+backward timing")
+    ap.add_argument("--no-tiny", action="store_true", help="skip the tiny layer (eager and CUDA-graph) timing")
     ap.add_argument("--no-tensor-bound", action="store_true",
                     help="skip the forward at T=16384 (tensor-bound grouped GEMMs)")
     ap.add_argument("--ring-sweep", action="store_true",
