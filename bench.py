@@ -706,10 +706,37 @@ def run_mok(args, rank, world, local_rank):
         mxb_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
         if mx_layer.status() != (0, 0):
             raise RuntimeError("device status set in the MXFP8 backward")
+        # the same step with bf16 weight gradients (MOK_FLAG_WGRAD_BF16: the fp32 ones rounded once;
+        # the MXFP8 tolerance is a relative Frobenius error, which that rounding barely moves)
+        mx_desc16 = mok.desc_from_shape(shp.scaled(mxfp8=True), flags=N.FLAG_WGRAD_BF16)
+        mx_layer16 = mok.MoELayer(mx_desc16, device=dev)
+        g16 = dict(grads)
+        g16["dw13"] = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
+        g16["dw2"] = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+
+        def mx_step16():
+            mok.moe_forward_mxfp8(mx_desc16, x, wr, None, None, wq, y, mx_layer16.ctx, mx_layer16.ws)
+            mx_layer16.backward_mxfp8(dy, x, wr, wb, out=g16)
+
+        for _ in range(2):
+            mx_step16()
+        barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            mx_step16()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        mxb16_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
+        if mx_layer16.status() != (0, 0):
+            raise RuntimeError("device status set in the MXFP8 backward with bf16 weight gradients")
+        del mx_layer16, g16
         mx = {"fwd_ms": round(mx_ms, 4), "tokens_per_s": round(whole_job_rate(T, world, mx_ms), 1),
               "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mx_trace.items()},
               "fwd_bwd_ms": round(mxb_ms, 4), "fwd_bwd_tokens_per_s": round(whole_job_rate(T, world, mxb_ms), 1),
               "fwd_bwd_kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in mxb_trace.items()},
+              "fwd_bwd_ms_wgrad_bf16": round(mxb16_ms, 4),
+              "fwd_bwd_tokens_per_s_wgrad_bf16": round(whole_job_rate(T, world, mxb16_ms), 1),
               "weights": "forward: E4M3 + E8M0 per 32 along K (11.3 GB + 0.35 GB of scales); backward: W2 "
                          "and W13 transposed, E4M3 + E8M0 along H and 2I (11.3 GB + 0.35 GB); GEMM1, GEMM2, dA' "
                          "and dX_g on the FP8 tensor path (block-scaled MMAs), the weight gradients on the "

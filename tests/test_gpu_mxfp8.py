@@ -206,10 +206,10 @@ def test_backward_weights_bit_exact(shape):
             assert np.array_equal(X_got[e], X.T), (name, e)
 
 
-def _mx_fwd_bwd(shape, seed=0, given=None):
+def _mx_fwd_bwd(shape, seed=0, given=None, flags=0):
     inp = W.make_inputs(shape, seed=seed, device="cpu")
     dev = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
-    desc = mok.desc_from_shape(shape)
+    desc = mok.desc_from_shape(shape, flags=flags)
     wq = mok.quantize_weights(desc, dev["w13"], dev["w2"])
     wb = mok.quantize_weights_backward(desc, dev["w13"], dev["w2"])
     layer = mok.MoELayer(desc)
@@ -243,6 +243,20 @@ def test_mx_backward_matches_mx_oracle(shape):
         _, _, fro_ref = err_stats(to_f64(g[name]), ref[name])
         print("%s: vs MX oracle %.3e, vs unquantised %.3e" % (name, fro, fro_ref))
         assert fro <= MX_FRO, (name, fro)
+
+
+def test_mx_backward_bf16_weight_gradients_are_rounded_fp32_ones():
+    """With bf16 weight gradients the MXFP8 backward gives the fp32 ones rounded to nearest even
+    (the same kernels, one rounding at the store); the other gradients do not change."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    shape = MID.scaled(name="mid_mx_skew", skew=True)
+    _, _, _, g32 = _mx_fwd_bwd(shape, seed=5)
+    _, _, _, g16 = _mx_fwd_bwd(shape, seed=5, flags=N.FLAG_WGRAD_BF16)
+    for name in ("dw13", "dw2"):
+        assert g16[name].dtype == torch.bfloat16
+        assert torch.equal(g16[name], g32[name].to(torch.bfloat16)), name
+    for name in ("dx", "dw_router", "dgates"):
+        assert torch.equal(g16[name], g32[name]), name
 
 
 def test_mx_backward_deterministic():
