@@ -127,12 +127,13 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& a2, const CUten
 // the narrow kernel's row chunks).
 int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
 
-// Split-operand narrow GEMMs (GEMM2, dX_g): when experts average at most 160 rows, chunks of at
-// most 192 rows and two 256-row weight tiles per pair tile sharing the row stages (EPI_F32_PAIRED:
-// 57% of each stage is weights instead of 40%, which these fill-bound GEMMs turn into weight
-// bandwidth; measured at 128 rows per expert dX_g 3.02 -> 2.76 ms, GEMM2 1.58 -> 1.57 ms); else
-// chunks of 256 rows, one weight tile (192-row chunks cut 512-row experts into 3 and were 10%
-// slower there, and at that shape GEMM2 is near its MMA rate, where pairing gained nothing).
+// Split-operand narrow GEMMs (GEMM2, dX_g): when experts average at most 160 rows, two 256-row
+// weight tiles per pair tile sharing the row stages (EPI_F32_PAIRED: about 57% of each stage's
+// bytes are weights instead of 40%, which these fill-bound GEMMs turn into weight bandwidth;
+// measured at 128 rows per expert dX_g 3.02 -> 2.76 ms, GEMM2 1.58 -> 1.57 ms), in chunks of at
+// most 256 rows (three stages either way; 192-row chunks cut the long experts of a skewed layer
+// into more chunks, each of which streams the weight tiles again); else one weight tile (at 512
+// rows per expert GEMM2 is near its MMA rate, where pairing gained nothing).
 bool narrow_short_rows(int R, int E) { return (long long)R <= 160LL * E; }
 
 // Narrow-segment GEMM on CTA pairs: W (K-major [E][N][K] or, WMN, MN-major [E][K][N]) against
@@ -270,11 +271,11 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
       // (the TMA copies are bitwise: the bf16 maps serve any 16-bit element)
       g.f16 = 1;
       if (narrow_short_rows(R, E))
-        return launch_narrow<false, false, 192, EPI_F32_PAIRED>(tw, act_hi, nullptr, I, g, R, n_sm, st);
+        return launch_narrow<false, false, 256, EPI_F32_PAIRED>(tw, act_hi, nullptr, I, g, R, n_sm, st);
       return launch_narrow<false, false, 256>(tw, act_hi, nullptr, I, g, R, n_sm, st);
     }
     if (narrow_short_rows(R, E))
-      return launch_narrow<false, true, 192, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
+      return launch_narrow<false, true, 256, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
     return launch_narrow<false, true, 256>(tw, act_hi, act_lo, I, g, R, n_sm, st);
   }
   CUtensorMap ta, ta2, tb;
@@ -334,7 +335,7 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
     g.ld0 = H;
     if (dhu_lo == nullptr) return launch_narrow<true, false, 256>(tw, dhu_hi, nullptr, 2 * I, g, R, n_sm, st);
     if (narrow_short_rows(R, E))
-      return launch_narrow<true, true, 192, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
+      return launch_narrow<true, true, 256, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
     return launch_narrow<true, true, 256>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
   }
   CUtensorMap ta, ta2, tb;
