@@ -489,6 +489,9 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     uint8_t* stg = stg_all + (warp - 2) * WGP_STG;
     const uint32_t stg_u = smem_u32(stg);
     if (lane == 0) tma_prefetch_desc(&tmO);
+    // the output is written once and not read back here: its lines go first when L2 needs room,
+    // before the operand rows that the other strips of the expert read again
+    const uint64_t pol_out = l2_policy_evict_first();
     uint32_t acc_phase = 0;
     int tcount = 0;  // tiles with MMAs seen so far (both groups count all of them)
     bool ok = true;
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO, stg_u, out_m, out_r + c * 32);
+            tma_store_2d_hint(&tmO, stg_u, out_m, out_r + c * 32, pol_out);
             bulk_commit_group();
           }
         }
