@@ -297,8 +297,22 @@ def fwd_gemm_hbm(trace, kb, peaks):
 
 
 def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
-    """The ring forward at `shp` (a fixed 512 MiB token ring) for each minibatch of the sweep:
-    ms per forward over K forwards after W warm-ups, and whether y is bitwise the plain forward's."""
+    """The ring forward at `shp` (a fixed 512 MiB token ring) for each minibatch of the sweep, with
+    GEMM2 and the merge as separate launches and in the persistent launch (`persistent`): ms per
+    forward over K forwards after W warm-ups, and whether y is bitwise the plain forward's."""
+    from mixture_experts_layer_table_gb300 import _native as N
+    from mixture_experts_layer_table_gb300 import workloads as W
+
+    sweep = {}
+    for m in W.RING_MINIBATCHES:
+        sweep[str(m)] = ring_point(shp, x, w_router, w13, w2, y_plain, steps, warmup, m, 0)
+        sweep[str(m)]["persistent"] = ring_point(shp, x, w_router, w13, w2, y_plain, steps, warmup, m,
+                                                 N.FLAG_RING_PERSISTENT)
+    return sweep
+
+
+def ring_point(shp, x, w_router, w13, w2, y_plain, steps, warmup, m, flags):
+    """One point of the ring sweep: minibatch m with the given descriptor flags."""
     import torch
 
     import mixture_experts_layer_table_gb300 as mok
@@ -307,31 +321,27 @@ def ring_sweep(shp, x, w_router, w13, w2, y_plain, steps, warmup):
 
     stream = torch.cuda.current_stream()
     y = torch.empty_like(y_plain)
-    sweep = {}
-    for m in W.RING_MINIBATCHES:
-        layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES), device=x.device)
-        for _ in range(warmup):
-            layer.forward(x, w_router, w13, w2, y=y)
-        torch.cuda.synchronize()
-        if layer.status() != (0, 0):
-            raise RuntimeError("device status set during the ring warm-up")
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        N.trace_start(16 * steps + 16)
-        e0.record(stream)
-        for _ in range(steps):
-            layer.forward(x, w_router, w13, w2, y=y)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        trace = N.trace_stop()
-        if layer.status() != (0, 0):
-            raise RuntimeError("device status set in the ring forward")
-        ms = e0.elapsed_time(e1) / steps
-        sweep[str(m)] = {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
-                         "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
-                         "bitwise_equal_to_plain": bool(torch.equal(y, y_plain)),
-                         "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in trace.items()}}
-        del layer
-    return sweep
+    layer = mok.MoELayer(mok.desc_from_shape(shp, minibatch=m, ring_bytes=W.RING_BYTES, flags=flags), device=x.device)
+    for _ in range(warmup):
+        layer.forward(x, w_router, w13, w2, y=y)
+    torch.cuda.synchronize()
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set during the ring warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    N.trace_start(16 * steps + 16)
+    e0.record(stream)
+    for _ in range(steps):
+        layer.forward(x, w_router, w13, w2, y=y)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    trace = N.trace_stop()
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set in the ring forward")
+    ms = e0.elapsed_time(e1) / steps
+    return {"fwd_ms": round(ms, 4), "tokens_per_s": round(shp.T / (ms * 1e-3), 1),
+            "ring_slots": min(W.RING_BYTES // (m * shp.H * 2), -(-shp.R // m)),
+            "bitwise_equal_to_plain": bool(torch.equal(y, y_plain)),
+            "kernels": {n: round(t["total_ms"] / t["launches"], 4) for n, t in trace.items()}}
 
 
 def ring_fwd_bwd(shp, x, w_router, w13, w2, steps, warmup, minibatch=2368):

@@ -44,6 +44,7 @@ FLAG_WGRAD_BF16 = 1
 FLAG_GEMM_PAIR = 2     # GEMM1 / GEMM2 on CTA pairs with 256-row tiles (dX_g: single CTAs)
 FLAG_GEMM_SINGLE = 4   # GEMM1 / GEMM2 / dX_g on single CTAs with 128-row tiles
 FLAG_W2_F16 = 8        # forward: w2 is fp16 (convert_f16), a kept as fp16, GEMM2 on fp16 operands
+FLAG_RING_PERSISTENT = 16  # ring forward: gather, GEMM1, GEMM2 and the merge in one persistent launch
 # neither: GEMM1, GEMM2 and dX_g on the narrow-segment pair kernel (expert rows as the MMA's N)
 CTX_FIELDS = LAYOUT_FIELDS[:LAYOUT_FIELDS.index("ctx_bytes")]
 WS_FIELDS = LAYOUT_FIELDS[LAYOUT_FIELDS.index("ctx_bytes") + 1:LAYOUT_FIELDS.index("ws_bytes")]

@@ -77,8 +77,9 @@ struct RingGeom {
 };
 
 // Byte offset of the ring stamp (u64 [2]) after the [2][n_mb] i32 counters.
-// counters: gathered [n_mb], consumed [n_mb], the tile ticket; then the stamp, 16-byte aligned
-int64_t ring_counter_ints(int n_mb) { return int64_t(2) * n_mb + 1; }
+// counters: gathered [n_mb], consumed [n_mb], the GEMM1 tile ticket, the GEMM2 tile ticket and the
+// GEMM2 epilogue count of the persistent ring forward; then the stamp, 16-byte aligned
+int64_t ring_counter_ints(int n_mb) { return int64_t(2) * n_mb + 3; }
 int64_t ring_stamp_offset(int n_mb) { return (ring_counter_ints(n_mb) * 4 + 15) & ~int64_t(15); }
 
 mok_status ring_geometry(const mok_layer_desc* d, RingGeom* g) {
@@ -305,6 +306,9 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
   // fp16 W2 (MOK_FLAG_W2_F16): the narrow-segment GEMMs without the ring only
   const bool w2_f16 = (d->flags & MOK_FLAG_W2_F16) != 0;
   if (w2_f16 && (d->ring_bytes > 0 || gemm_variant(d, GEMM2) != mok::GEMM_NARROW)) return MOK_ERR_UNSUPPORTED;
+  // the ring forward in one persistent launch (narrow GEMMs, top-k of at most 8)
+  const bool ring_persistent = d->ring_bytes > 0 && (d->flags & MOK_FLAG_RING_PERSISTENT) != 0 &&
+                               gemm_variant(d, GEMM1) == mok::GEMM_NARROW && d->k <= 8;
   RingGeom rg;
   const int comm = d->comm_sms > 0 ? d->comm_sms : 12;
   if (d->ring_bytes > 0) {
@@ -383,8 +387,16 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
     ra.gathered = counters;
     ra.consumed = counters + rg.n_mb;
     ra.ticket = counters + 2 * rg.n_mb;
-    MOK_LAUNCH("ring_gemm1_swiglu", st,
-               mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, ring_variant, st));
+    ra.ticket2 = counters + 2 * rg.n_mb + 1;
+    ra.done = counters + 2 * rg.n_mb + 2;
+    if (ring_persistent) {
+      // one launch for the rest of the forward: gather, GEMM1 + SwiGLU, GEMM2, weighted merge
+      MOK_LAUNCH("ring_forward", st,
+                 mok::launch_ring_forward(ra, w13, w2, hu, act, act_lo, o, gates, row_of, T, y, status, n_sm, st));
+    } else {
+      MOK_LAUNCH("ring_gemm1_swiglu", st,
+                 mok::launch_ring_gemm1(ra, w13, hu, act, act_lo, status, n_sm, ring_variant, st));
+    }
     // the ring rows are this forward's (the backward reuses them when it is given this ws)
     MOK_LAUNCH("ring_stamp", st,
                mok::launch_ring_stamp(at<unsigned long long>(ctx, L.ring_stamp),
@@ -392,6 +404,7 @@ mok_status mok_moe_forward(const mok_layer_desc* d, const void* x, const void* w
                                                                             ring_stamp_offset(rg.n_mb)),
                                       (unsigned long long)reinterpret_cast<uintptr_t>(ctx), st));
   }
+  if (ring_persistent) return MOK_OK;
   // 6. grouped GEMM2 (a as hi + lo, or as fp16 against the fp16 W2), fp32 expert outputs
   MOK_LAUNCH("gemm2", st,
              mok::launch_gemm2(act, act_lo, w2, R, H, I, E, offsets, tile_off, o, status, n_sm,

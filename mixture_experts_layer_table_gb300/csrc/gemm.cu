@@ -16,42 +16,6 @@ namespace mok {
 
 namespace {
 
-// Store map of a row-major output [rows][cols]: 32 x 32 boxes, fp32 with 128B swizzle (128-byte
-// box rows) or bf16 with 64B swizzle (64-byte box rows), as the epilogue stages them.
-bool tmap_out(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, bool f32) {
-  const uint64_t es = f32 ? 4 : 2;
-  const uint64_t dims[2] = {cols, rows};
-  const uint64_t strides[1] = {cols * es};
-  const uint32_t box[2] = {32, 32};
-  return make_tmap(m, base, 2, dims, strides, box,
-                   f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
-bool tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-             uint32_t box_outer) {
-  const uint64_t dims[2] = {inner, outer};
-  const uint64_t strides[1] = {inner * 2};
-  const uint32_t box[2] = {box_inner, box_outer};
-  return make_tmap(m, base, 2, dims, strides, box);
-}
-
-bool tmap_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
-  const uint64_t dims[3] = {d0, d1, d2};
-  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-  const uint32_t box[3] = {b0, b1, 1};
-  return make_tmap(m, base, 3, dims, strides, box);
-}
-
-// W13 [E][2I][H] seen as [E][2][I][H]: one box of 64 K x 64 rows x both halves brings 64 gate
-// rows followed by the 64 up rows of the same intermediate indices.
-bool tmap_w13_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t E, uint32_t rows = 64) {
-  const uint64_t dims[4] = {H, I, 2, E};
-  const uint64_t strides[3] = {H * 2, I * H * 2, 2 * I * H * 2};
-  const uint32_t box[4] = {64, rows, 2, 1};
-  return make_tmap(m, w13, 4, dims, strides, box);
-}
-
 // out_map / out1 / out2: store maps of the outputs for epilogues that use TMA stores.
 template <int MODE, int EPI, int SPLIT, int BN>
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMap& b, const CUtensorMap& b2,
@@ -70,15 +34,6 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& a2, const CUtensorMa
   return cudaGetLastError();
 }
 
-GemmArgs base_args(int E, const int32_t* offsets, const int32_t* tile_off, int* status) {
-  GemmArgs g{};
-  g.E = E;
-  g.offsets = offsets;
-  g.tile_off = tile_off;
-  g.total_tiles = -1;
-  g.status = status;
-  return g;
-}
 
 // Upper bound of the 128-row tiles of R expert-sorted rows split into E segments.
 int row_tiles_bound(int R, int E) { return (R + BM - 1) / BM + E; }
@@ -134,7 +89,6 @@ int pair_tiles_bound(int R, int E) { return (R + 255) / 256 + E; }
 // most 256 rows (three stages either way; 192-row chunks cut the long experts of a skewed layer
 // into more chunks, each of which streams the weight tiles again); else one weight tile (at 512
 // rows per expert GEMM2 is near its MMA rate, where pairing gained nothing).
-bool narrow_short_rows(int R, int E) { return (long long)R <= 160LL * E; }
 
 // Narrow-segment GEMM on CTA pairs: W (K-major [E][N][K] or, WMN, MN-major [E][K][N]) against
 // expert-sorted rows X [R][K] (hi, and lo when SPLIT; x_lo is ignored otherwise); fp32 out

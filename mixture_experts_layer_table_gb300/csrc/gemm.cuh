@@ -108,11 +108,25 @@ struct GemmArgs {
   int* gathered;            // [n_mb] rows gathered
   int* consumed;            // [n_mb] epilogue warps finished (consume_per_tile per tile)
   int consume_per_tile;     // epilogue warps counting out one tile (4, or 8 for a CTA pair)
-  int* ticket;              // narrow ring GEMM1: next tile to take (one counter for all pairs)
+  int* ticket;              // narrow ring GEMM1 / GEMM2: next tile to take (one counter for all pairs)
+  int fence_out;            // ring GEMM1: make each tile's outputs visible before counting it consumed
+  int mb_tiles1;            // ring GEMM2: GEMM1 tiles per row chunk (the minibatch tables count those)
+  int* done;                // ring GEMM2: epilogue warps finished, for the combine
   const __nv_bfloat16* x;   // [T][H] tokens
   const int* src_of;        // [R]
   __nv_bfloat16* ring;      // [ring_slots * mb_rows][H]
 };
+
+// GemmArgs with the fields every launch sets (the rest zero).
+inline GemmArgs base_args(int E, const int32_t* offsets, const int32_t* tile_off, int* status) {
+  GemmArgs g{};
+  g.E = E;
+  g.offsets = offsets;
+  g.tile_off = tile_off;
+  g.total_tiles = -1;
+  g.status = status;
+  return g;
+}
 
 struct TileInfo {
   int e, m, n;
@@ -588,7 +602,7 @@ __device__ __forceinline__ void copy_row_warp(const uint4* __restrict__ src, uin
 // gathering CTAs alone to fill the first slot: at T = 16384 with 2368-token minibatches the first
 // slot holds 271 MB, about half a millisecond for 12 gathering SMs.  The gathering CTAs go on from
 // minibatch 1.
-__device__ void ring_gather_first(const GemmArgs& a) {
+__device__ inline void ring_gather_first(const GemmArgs& a) {
   const int warps = (int)(blockDim.x >> 5);
   const int gw = (int)blockIdx.x * warps + (int)(threadIdx.x >> 5);
   const int nw = (int)gridDim.x * warps;
@@ -613,15 +627,15 @@ __device__ __forceinline__ int ring_gather_slots(const GemmArgs& a, int buf_byte
 
 // After ring_gather: its staging barriers are invalidated so that the CTA can set up other
 // barriers in the same shared memory (every copy that completes on them has landed).
-__device__ void ring_gather_retire(const GemmArgs& a, int buf_bytes, uint64_t* bars) {
+__device__ inline void ring_gather_retire(const GemmArgs& a, int buf_bytes, uint64_t* bars) {
   __syncthreads();
   if (threadIdx.x == 0)
     for (int j = 0; j < ring_gather_slots(a, buf_bytes); ++j)
-      asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(&bars[j])) : "memory");
+      mbar_inval(smem_u32(&bars[j]));
   __syncthreads();
 }
 
-__device__ void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint64_t* bars) {
+__device__ inline void ring_gather(const GemmArgs& a, uint8_t* buf, int buf_bytes, uint64_t* bars) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int copy_warps = (int)(blockDim.x >> 5) - 1;  // warps 1.. copy through registers
   const uint32_t row_bytes = (uint32_t)a.H * 2;

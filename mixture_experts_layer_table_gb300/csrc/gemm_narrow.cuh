@@ -31,10 +31,17 @@
 // weight tile in L2) are dealt to the pairs round-robin in a fixed order; every output element
 // is one tile's accumulator, reduced over K in a fixed order.
 #pragma once
+#include "combine.cuh"
 #include "gemm.cuh"
 #include "narrow_tiles.h"
 
 namespace mok {
+
+// Shared memory after the stages and the SwiGLU exchange buffer: barriers, TMEM address, abort
+// flag and (ring forward) the tile queue: NARROW_TQ entries of NARROW_QE ints.
+constexpr int NARROW_BAR_BYTES = 1024;
+constexpr int NARROW_TQ = 8;
+constexpr int NARROW_QE = 12;
 
 template <bool WMN, bool SPLIT, int NMAX_, int EPI = EPI_F32>
 struct NarrowCfg {
@@ -78,7 +85,7 @@ struct NarrowCfg {
                                    : (a.N + PM - 1) / PM;
   }
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
-    return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + 256 /*barriers*/ + size_t(2) * (E + 1) * 4;
+    return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + NARROW_BAR_BYTES + size_t(2) * (E + 1) * 4;
   }
 };
 
@@ -98,32 +105,37 @@ struct NarrowCfg {
 // barrier in both CTAs and an empty barrier in the even CTA); -1 ends the queue.  Which pair
 // computes a tile does not change its result: each output element is still one tile's
 // accumulator over K in a fixed order.
-template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
-__global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
-    gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
-                       const __grid_constant__ CUtensorMap tmX2s, const GemmArgs args) {
+// MODE of narrow_body: the fixed deal over the whole layer, the ring forward's GEMM1 (tiles from
+// a ticket, each minibatch's rows awaited in the token ring) or, in the persistent ring forward,
+// its GEMM2 (tiles from a second ticket, each minibatch's rows of a awaited from GEMM1).
+constexpr int NARROW_PLAIN = 0, NARROW_RING_GEMM1 = 1, NARROW_RING_GEMM2 = 2;
+constexpr uint32_t kTmemOwn = 0xffffffffu;  // narrow_body allocates (and frees) its own TMEM
+
+// One narrow-segment grouped GEMM on the CTA pairs of the launch.  `smem` is the CTA's 1024-byte
+// aligned dynamic shared memory; tmem_given is a TMEM base allocated by the caller for both CTAs
+// of the pair (at least C::TMEM_COLS columns), or kTmemOwn.  With a caller's TMEM the shared memory
+// is left for another phase: the barriers are invalidated before returning.
+template <bool WMN, bool SPLIT, int NMAX, int EPI, int MODE>
+__device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmX2,
+                                            const CUtensorMap& tmXs, const CUtensorMap& tmX2s,
+                                            const GemmArgs& args, uint8_t* smem, uint32_t tmem_given) {
   using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
+  constexpr bool RING = MODE != NARROW_PLAIN;
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // C::XBUF_BYTES
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES);
-  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, tq_full[TQ], tq_empty[TQ]
-  constexpr int TQ = 4;  // RING: depth of the tile queue
-  static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= 256, "barriers, TMEM address and abort flag");
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, tq_full[TQ], tq_empty[TQ], then
+  // the TMEM address and the abort flag; at +512 the tile queue's entries (RING)
+  constexpr int TQ = NARROW_TQ;
+  static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= 512 && 512 + TQ * NARROW_QE * 4 <= NARROW_BAR_BYTES,
+                "barriers, TMEM address, abort flag and tile queue");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + 256);
+  volatile int* tq = reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(bars) + 512);
+  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + NARROW_BAR_BYTES);
   int* s_coff = s_off + (args.E + 1);
-  volatile int* tq = s_off;  // RING: the tile queue (the segment tables are not used there)
 
-  if (RING) ring_gather_first(args);
-  if (RING && (int)blockIdx.x < args.comm_ctas) {
-    ring_gather(args, smem, STAGES * STAGE_BYTES, bars);
-    ring_gather_retire(args, STAGES * STAGE_BYTES, bars);  // then this pair runs tiles as well
-  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     }
     s_coff[args.E] = acc;
   }
-  if (warp == 1) {
+  if (warp == 1 && tmem_given == kTmemOwn) {
     tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish_pair();
   }
@@ -176,10 +188,15 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
   __syncthreads();
   cluster_sync();  // both CTAs' barriers are initialised before either signals the other's
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_base = tmem_given == kTmemOwn ? *tmem_slot : tmem_given;
 
   const int MT = C::m_tiles(args);
-  const int total = RING ? args.mb_start[args.n_mb] : s_coff[args.E] * MT;
+  // GEMM2 of the ring forward: the minibatch tables count GEMM1 tiles (args.mb_tiles1 per row
+  // chunk); the same row chunks give MT GEMM2 tiles each
+  auto tiles_before = [&](int mb) {
+    return MODE == NARROW_RING_GEMM2 ? args.mb_start[mb] / args.mb_tiles1 * MT : args.mb_start[mb];
+  };
+  const int total = RING ? tiles_before(args.n_mb) : s_coff[args.E] * MT;
   const int nkb = args.K / BK;
   // Tile g.  RING: the minibatch mb holding it, the tile decoded inside it, its rows' position in the
   // ring (ring_row0) and its rows' position in the outputs (t.row0, all rows of the layer).
@@ -193,41 +210,71 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     int lo = 0, hi = args.n_mb;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (args.mb_start[mid] <= g) lo = mid; else hi = mid;
+      if (tiles_before(mid) <= g) lo = mid; else hi = mid;
     }
     mb = lo;
-    NarrowTile t = decode_narrow_tile(g - args.mb_start[lo], MT, args.E, C::NMAX,
+    NarrowTile t = decode_narrow_tile(g - tiles_before(lo), MT, args.E, C::NMAX,
                                       args.mb_off + (size_t)lo * (args.E + 1), args.mb_toff + (size_t)lo * (args.E + 1));
     ring_row0 = ((lo + args.ring_shift) % args.ring_slots) * args.mb_rows + t.row0;
     t.row0 += lo * args.mb_rows;
+    if (MODE == NARROW_RING_GEMM2) ring_row0 = t.row0;  // a is read from the layer's rows
     return t;
   };
 
-  // RING: the n-th tile of this pair from the tile queue (-1: no more).  The even CTA's producer
-  // (one thread) waits until entry n % TQ has been read by everyone, takes the next ticket and
-  // writes it into both CTAs' queues; every other reader (one thread of a warp) waits for the
-  // entry, reads it and counts itself out on the even CTA's empty barrier.
-  auto publish_tile = [&](int n, int& g) -> bool {
+  // RING: the n-th tile of this pair, from the tile queue (g = -1: no more).  The even CTA's
+  // producer (one thread) takes each tile from the ticket counter, decodes it once (the minibatch
+  // tables are in global memory: a binary search over the minibatches and one over the experts)
+  // and writes the decoded tile into entry n % TQ of both CTAs' queues, one tile ahead of its own
+  // loads; every other reader waits for the entry, reads it and counts itself out on the even
+  // CTA's empty barrier of the entry.
+  auto publish_tile = [&](int n, int& g, NarrowTile& t, int& mb, int& rr) -> bool {
     const int q = n % TQ;
     const uint32_t u = (uint32_t)(n / TQ) & 1u;
     if (!mbar_wait<true>(tq_empty(q), u ^ 1, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, 32))
       return false;
     g = atomicAdd(args.ticket, 1);
     if (g >= total) g = -1;
-    tq[q] = g;
-    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&tq[q])), 1), (uint32_t)g);
+    if (g >= 0) t = decode(g, mb, rr);
+    const int v[10] = {g, t.e, t.c, t.m, t.nc, t.row0, t.rows, t.n, mb, rr};
+    volatile int* dst = tq + q * NARROW_QE;
+    const uint32_t peer = mapa_shared(smem_u32(const_cast<int*>(dst)), 1);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      dst[i] = v[i];
+      st_shared_cluster_u32(peer + 4u * i, (uint32_t)v[i]);
+    }
     mbar_arrive(tq_full(q));
     mbar_arrive_cluster(mapa_shared(tq_full(q), 1));  // release: the peer's copy is written
     return true;
   };
-  auto read_tile = [&](int n, int& g, uint32_t sleep_ns) -> bool {
+  // by all lanes of a warp (lane 0 waits and counts out) or by a single thread (warp_wide false)
+  auto read_tile = [&](int n, int& g, NarrowTile& t, int& mb, int& rr, uint32_t sleep_ns, bool warp_wide) -> bool {
     const int q = n % TQ;
     const uint32_t u = (uint32_t)(n / TQ) & 1u;
-    if (!mbar_wait<true>(tq_full(q), u, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, sleep_ns))
-      return false;
-    g = tq[q];
-    if (rank == 0) mbar_arrive(tq_empty(q));
-    else mbar_arrive_cluster(mapa_shared(tq_empty(q), 0));
+    int w_ok = 1;
+    if (lane == 0 || !warp_wide)
+      w_ok = mbar_wait<true>(tq_full(q), u, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, sleep_ns);
+    if (warp_wide) {
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      __syncwarp();
+    }
+    if (!w_ok) return false;
+    const volatile int* src = tq + q * NARROW_QE;
+    g = src[0];
+    t.e = src[1];
+    t.c = src[2];
+    t.m = src[3];
+    t.nc = src[4];
+    t.row0 = src[5];
+    t.rows = src[6];
+    t.n = src[7];
+    mb = src[8];
+    rr = src[9];
+    if (warp_wide) __syncwarp();  // every lane has read the entry
+    if (lane == 0 || !warp_wide) {
+      if (rank == 0) mbar_arrive(tq_empty(q));
+      else mbar_arrive_cluster(mapa_shared(tq_empty(q), 0));
+    }
     return true;
   };
 
@@ -249,20 +296,43 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      int ring_ready = -1;  // RING: last minibatch known to be gathered
+      int ring_ready = -1;  // RING: last minibatch known to be ready (gathered, or through GEMM1)
+      // RING, even CTA: the tile after the current one is taken during the current one's loads
+      int g_nx = 0, mb_nx = 0, rr_nx = 0;
+      NarrowTile t_nx{};
+      bool have_nx = false;
+      if (RING && rank == 0) {
+        ok = publish_tile(0, g_nx, t_nx, mb_nx, rr_nx);
+        have_nx = true;
+      }
       for (int n = 0; ok; ++n) {
-        int g = pair + n * npairs;
-        if (RING && !(rank == 0 ? publish_tile(n, g) : read_tile(n, g, 32))) {
+        int g, mb = 0, ring_row0 = 0;
+        NarrowTile t{};
+        if (!RING) {
+          g = pair + n * npairs;
+          if (g >= total) break;
+          t = decode(g, mb, ring_row0);
+        } else if (rank == 0) {
+          g = g_nx;
+          t = t_nx;
+          mb = mb_nx;
+          ring_row0 = rr_nx;
+          have_nx = false;
+        } else if (!read_tile(n, g, t, mb, ring_row0, 32, false)) {
           ok = false;
           break;
         }
-        if (g < 0 || g >= total) break;
-        int mb, ring_row0;
-        const NarrowTile t = decode(g, mb, ring_row0);
+        if (g < 0) break;
         if (RING && mb > ring_ready) {
-          // the minibatch's rows must be in the ring before the first load of its tiles
-          const int rows_mb = min(args.mb_rows, args.R - mb * args.mb_rows);
-          if (!wait_counter(&args.gathered[mb], rows_mb, args.status, SITE_RING_WAIT)) {
+          // GEMM1: the minibatch's rows must be in the ring before the first load of its tiles;
+          // GEMM2: every GEMM1 tile of the minibatch must have stored its rows of a
+          const bool ready =
+              MODE == NARROW_RING_GEMM1
+                  ? wait_counter(&args.gathered[mb], min(args.mb_rows, args.R - mb * args.mb_rows), args.status,
+                                 SITE_RING_WAIT)
+                  : wait_counter(&args.consumed[mb], args.consume_per_tile * (args.mb_start[mb + 1] - args.mb_start[mb]),
+                                 args.status, SITE_RING_WAIT);
+          if (!ready) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -278,7 +348,15 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
         const int w_row = t.m * C::PM + 128 * (int)rank;
         const uint32_t pair_tx = 2u * (C::A_BYTES + C::X_OPS * xrows * 128);
         const uint64_t pol_w = t.nc > 1 ? pol_shared : pol_once;
+        const int kb_pub = nkb - 1 < STAGES ? nkb - 1 : STAGES;  // the stage ring is full by then
         for (int kb = 0; kb < nkb; ++kb) {
+          if (RING && rank == 0 && !have_nx && kb == kb_pub) {
+            if (!publish_tile(n + 1, g_nx, t_nx, mb_nx, rr_nx)) {
+              ok = false;
+              break;
+            }
+            have_nx = true;
+          }
           if (!mbar_wait<true>(empty_bar(stage), phase ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY,
                                kWaitLimitNs, 32)) {
             ok = false;
@@ -364,19 +442,19 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       bool any_mma = false;
       const uint32_t a_lbo = WMN ? MOK_MN_LBO : 16, a_sbo = WMN ? MOK_MN_SBO : 1024;
       for (int n = 0; ok; ++n) {
-        int g = pair + n * npairs;
+        int g, mb_unused = 0, rr_unused = 0;
+        NarrowTile t{};
         if (RING) {
-          int r_ok = 1;
-          if (lane == 0) r_ok = read_tile(n, g, 32);
-          g = __shfl_sync(0xffffffffu, g, 0);
-          if (!__shfl_sync(0xffffffffu, r_ok, 0)) {
+          if (!read_tile(n, g, t, mb_unused, rr_unused, 32, true)) {
             ok = false;
             break;
           }
+        } else {
+          g = pair + n * npairs;
+          if (g >= total) break;
+          t = decode(g, mb_unused, rr_unused);
         }
-        if (g < 0 || g >= total) break;
-        int mb_unused, rr_unused;
-        const NarrowTile t = decode(g, mb_unused, rr_unused);
+        if (g < 0) break;
         uint32_t idesc = idesc_bf16_f32(C::PM, t.n, WMN, false);
         if (args.f16) idesc &= ~((1u << 7) | (1u << 10));  // A and B formats: fp16 instead of bf16
         int w_ok = 1;
@@ -439,7 +517,7 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
         __syncwarp();
       }
     }
-  } else {
+  } else if (warp < 2 + C::EPI_WARPS) {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are reachable by this warp
     const uint32_t tempty0_cl = mapa_shared(tempty_bar(0), 0);
@@ -447,16 +525,16 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int n = 0;; ++n) {
-      int g = pair + n * npairs;
+      int g, mb = 0, rr_unused = 0;
+      NarrowTile t{};
       if (RING) {
-        int r_ok = 1;
-        if (lane == 0) r_ok = read_tile(n, g, 256);
-        g = __shfl_sync(0xffffffffu, g, 0);
-        if (!__shfl_sync(0xffffffffu, r_ok, 0)) break;
+        if (!read_tile(n, g, t, mb, rr_unused, 256, true)) break;
+      } else {
+        g = pair + n * npairs;
+        if (g >= total) break;
+        t = decode(g, mb, rr_unused);
       }
-      if (g < 0 || g >= total) break;
-      int mb, rr_unused;
-      const NarrowTile t = decode(g, mb, rr_unused);
+      if (g < 0) break;
       int w_ok = 1;
       if (lane == 0)
         w_ok = mbar_wait<true>(tfull_bar(acc), acc_phase, abort_flag, args.status, SITE_GEMM_EPI_TMEM_FULL,
@@ -591,9 +669,17 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty0_cl + 8u * acc);
-      // RING: this warp is done with the tile (its MMAs have read the rows): once every epilogue
-      // warp of every tile of the minibatch has counted in, its ring slot may be refilled
-      if (RING && lane == 0) atomicAdd(&args.consumed[mb], 1);
+      // GEMM1 of the ring: this warp is done with the tile (its MMAs have read the rows): once
+      // every epilogue warp of every tile of the minibatch has counted in, its ring slot may be
+      // refilled (and, with args.fence_out, GEMM2 may read the minibatch's rows of a).  GEMM2 of
+      // the persistent ring forward: the warp's rows of o are stored (args.done, for the combine).
+      if (RING) {
+        if (MODE == NARROW_RING_GEMM2 || args.fence_out) {
+          __threadfence();  // this lane's stores, before the count (release, with the warp sync)
+          __syncwarp();
+        }
+        if (lane == 0) atomicAdd(MODE == NARROW_RING_GEMM2 ? args.done : &args.consumed[mb], 1);
+      }
       acc = (acc + 1) % C::ACCS;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -602,9 +688,195 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may still touch it
+  if (tmem_given == kTmemOwn) {
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+  } else {
+    // another phase sets up its barriers in this shared memory next
+    if (threadIdx.x == 0)
+      for (int i = 0; i < 2 * STAGES + 5 + 2 * TQ; ++i)
+        mbar_inval(smem_u32(&bars[i]));
+    __syncthreads();
+  }
+}
+
+template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
+__global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
+    gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
+                       const __grid_constant__ CUtensorMap tmX2s, const GemmArgs args) {
+  using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (RING) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XBUF_BYTES);
+    ring_gather_first(args);
+    if ((int)blockIdx.x < args.comm_ctas) {
+      ring_gather(args, smem, C::STAGES * C::STAGE_BYTES, bars);
+      ring_gather_retire(args, C::STAGES * C::STAGE_BYTES, bars);  // then this pair runs tiles as well
+    }
+  }
+  narrow_body<WMN, SPLIT, NMAX, EPI, RING ? NARROW_RING_GEMM1 : NARROW_PLAIN>(tmW, tmX, tmX2, tmXs, tmX2s, args, smem,
+                                                                              kTmemOwn);
+}
+
+// ------------------------------------------------------------------ persistent ring forward
+//
+// The whole ring forward after the schedule table in one cooperative launch, as the pages' two SM
+// groups ("把 MoE 通信延迟从 103μs 压到 18μs：Cursor 开源 GPU 内核 MoK", aientropygate.com, §03 ②:
+// one group runs dispatch, combine and state, the other the expert FFN, signalling through
+// counters): every CTA copies minibatch 0; args1.comm_ctas CTAs gather the later minibatches into
+// the token ring; the CTA pairs run GEMM1 + SwiGLU on each gathered minibatch (tiles from one
+// ticket); then GEMM2 on each minibatch whose GEMM1 tiles have all stored their rows of a (tiles
+// from a second ticket, so a pair takes GEMM2 tiles while others still finish GEMM1); then, once
+// every GEMM2 tile has stored its rows of o, every warp of the launch takes tokens of the weighted
+// merge.  The gathering CTAs join each stage once their gathering is done.  Each output element is
+// computed as by the separate launches (same tiles, K order, epilogues and merge), so y is bitwise
+// the same.
+struct RingCombineArgs {
+  const float* o;          // fp32 [R][H] expert outputs (written by this launch's GEMM2)
+  const float* gates;      // f32 [T][k]
+  const int32_t* row_of;   // i32 [T*k]
+  int T, k, vec_per_row;   // vec_per_row = H / 8
+  __nv_bfloat16* y;        // bf16 [T][H]
+};
+
+template <int EPI1, int EPI2>
+struct RingFwdCfg {
+  using C1 = NarrowCfg<false, false, 256, EPI1>;
+  using C2 = NarrowCfg<false, true, 256, EPI2>;
+  static constexpr int THREADS = C1::THREADS > C2::THREADS ? C1::THREADS : C2::THREADS;
+  // bytes each phase uses past the 1024-byte aligned base (stages, exchange buffer, barriers,
+  // segment tables); the TMEM address follows the larger
+  static __host__ __device__ constexpr int phase_end(int stages, int stage_bytes, int xbuf, int E) {
+    return stages * stage_bytes + xbuf + NARROW_BAR_BYTES + 2 * (E + 1) * 4;
+  }
+  static __host__ __device__ constexpr int tmem_slot_offset(int E) {
+    return phase_end(C1::STAGES, C1::STAGE_BYTES, C1::XBUF_BYTES, E) >
+                   phase_end(C2::STAGES, C2::STAGE_BYTES, C2::XBUF_BYTES, E)
+               ? phase_end(C1::STAGES, C1::STAGE_BYTES, C1::XBUF_BYTES, E)
+               : phase_end(C2::STAGES, C2::STAGE_BYTES, C2::XBUF_BYTES, E);
+  }
+  // TMEM address (16 bytes), then the merge's two barriers (16 bytes)
+  static __host__ __device__ constexpr size_t smem_bytes(int E) { return 1024 + size_t(tmem_slot_offset(E)) + 32; }
+  // the merge: a token's k <= 8 rows of o in parts of at most MERGE_VEC 8-column groups, two
+  // buffers of 8 row parts each (96 KB), refilled by bulk copies
+  static constexpr int MERGE_VEC = 192;
+  static_assert(2 * 8 * MERGE_VEC * 32 <= C1::STAGES * C1::STAGE_BYTES, "merge buffers in the stage memory");
+  static_assert(C1::TMEM_COLS <= 512 && C2::TMEM_COLS <= 512, "both GEMMs fit one TMEM allocation");
+};
+
+template <int EPI1, int EPI2>
+__global__ void __launch_bounds__(RingFwdCfg<EPI1, EPI2>::THREADS, 1)
+    ring_forward_kernel(const __grid_constant__ CUtensorMap tm1W, const __grid_constant__ CUtensorMap tm1X,
+                        const __grid_constant__ CUtensorMap tm1Xs, const __grid_constant__ CUtensorMap tm2W,
+                        const __grid_constant__ CUtensorMap tm2X, const __grid_constant__ CUtensorMap tm2X2,
+                        const __grid_constant__ CUtensorMap tm2Xs, const __grid_constant__ CUtensorMap tm2X2s,
+                        const GemmArgs a1, const GemmArgs a2, const RingCombineArgs cb) {
+  using R = RingFwdCfg<EPI1, EPI2>;
+  using C1 = typename R::C1;
+  using C2 = typename R::C2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + R::tmem_slot_offset(a1.E));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  ring_gather_first(a1);
+  if ((int)blockIdx.x < a1.comm_ctas) {
+    uint64_t* gbars = reinterpret_cast<uint64_t*>(smem + C1::STAGES * C1::STAGE_BYTES + C1::XBUF_BYTES);
+    ring_gather(a1, smem, C1::STAGES * C1::STAGE_BYTES, gbars);
+    ring_gather_retire(a1, C1::STAGES * C1::STAGE_BYTES, gbars);  // then this pair runs tiles as well
+  }
+  // one TMEM allocation of both CTAs of the pair for the two GEMMs
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  narrow_body<false, false, 256, EPI1, NARROW_RING_GEMM1>(tm1W, tm1X, tm1X, tm1Xs, tm1Xs, a1, smem, tmem_base);
+  narrow_body<false, true, 256, EPI2, NARROW_RING_GEMM2>(tm2W, tm2X, tm2X2, tm2Xs, tm2X2s, a2, smem, tmem_base);
+
+  // The weighted merge, once every GEMM2 epilogue warp of every tile has counted out.  Items are
+  // (token, part of its columns); the CTA's warp 0 bulk-copies an item's k row parts of o into
+  // one of two shared-memory buffers while every thread merges the other, so that each SM keeps
+  // up to 96 KB of o in flight (a warp per token, as the merge kernel, kept too little in flight
+  // with one CTA per SM here).  Per output the same fp32 sum over j = 0..k-1 and one rounding.
+  const int total2 = a2.mb_start[a2.n_mb] / a2.mb_tiles1 * C2::m_tiles(a2);
+  uint64_t* mbars = reinterpret_cast<uint64_t*>(smem + R::tmem_slot_offset(a1.E) + 16);
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    ok = wait_counter(a2.done, 2 * C2::EPI_WARPS * total2, a2.status, SITE_RING_WAIT);
+    mbar_init(smem_u32(&mbars[0]), 1);
+    mbar_init(smem_u32(&mbars[1]), 1);
+    fence_mbar_init();
+    fence_proxy_async_global();  // o, stored by other CTAs, is read by bulk copies
+  }
+  if (!__syncthreads_or(!ok)) {
+    constexpr int MV = R::MERGE_VEC;
+    const int parts = (cb.vec_per_row + MV - 1) / MV;
+    const int items = cb.T * parts;
+    auto part_vec = [&](int part) { return min(MV, cb.vec_per_row - part * MV); };
+    auto buf = [&](int b, int j) { return smem + (size_t)(b * 8 + j) * MV * 32; };
+    auto issue = [&](int item, int b) {  // warp 0: lane j copies row part j
+      const int t = item / parts, part = item - t * parts;
+      const uint32_t bytes = (uint32_t)part_vec(part) * 32;
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&mbars[b]), bytes * cb.k);
+      __syncwarp();
+      if (lane < cb.k) {
+        const int row = cb.row_of[(size_t)t * cb.k + lane];
+        bulk_load_g2s(smem_u32(buf(b, lane)), cb.o + (size_t)row * cb.vec_per_row * 8 + (size_t)part * MV * 8,
+                      bytes, smem_u32(&mbars[b]));
+      }
+    };
+    if (warp == 0 && (int)blockIdx.x < items) issue(blockIdx.x, 0);
+    bool live = true;
+    for (int i = 0; live; ++i) {
+      const int item = (int)blockIdx.x + i * (int)gridDim.x;
+      if (item >= items) break;
+      const int b = i & 1;
+      // the other buffer was merged in the previous iteration (all threads passed its barrier)
+      if (warp == 0 && item + (int)gridDim.x < items) issue(item + (int)gridDim.x, b ^ 1);
+      const int t = item / parts, part = item - t * parts;
+      float wj[8];  // loaded while the row parts land
+#pragma unroll
+      for (int j = 0; j < 8; ++j) wj[j] = j < cb.k ? cb.gates[(size_t)t * cb.k + j] : 0.0f;
+      volatile int no_abort = 0;
+      live = mbar_wait(smem_u32(&mbars[b]), (uint32_t)(i >> 1) & 1u, &no_abort, a2.status, SITE_RING_WAIT);
+      if (live) {
+        const int pv = part_vec(part);
+        for (int v = threadIdx.x; v < pv; v += blockDim.x) {
+          float acc[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < cb.k) {
+              const uint4* p = reinterpret_cast<const uint4*>(buf(b, j)) + 2 * v;
+              acc_f32x8(acc, p[0], p[1], wj[j]);
+            }
+          reinterpret_cast<uint4*>(cb.y)[(size_t)t * cb.vec_per_row + (size_t)part * MV + v] = pack_bf16x8(acc);
+        }
+      }
+      live = !__syncthreads_or(!live);
+    }
+    if (threadIdx.x == 0) {
+      mbar_inval(smem_u32(&mbars[0]));
+      mbar_inval(smem_u32(&mbars[1]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, 512);
   }
 }
 

@@ -94,6 +94,8 @@ struct RingArgs {
   int32_t* gathered;
   int32_t* consumed;
   int32_t* ticket;  // the narrow ring GEMM1's tile counter (zero at launch)
+  int32_t* ticket2;  // the persistent ring forward's GEMM2 tile counter (zero at launch)
+  int32_t* done;     // its GEMM2 epilogue warps finished (zero at launch)
 };
 // variant GEMM_NARROW: the narrow-segment CTA-pair kernel (minibatch tables in chunks of
 // ring_chunk_rows() rows); else the row-tile kernel (128-row tiles)
@@ -101,6 +103,18 @@ int ring_chunk_rows(int variant);
 // weight tiles per row chunk of the ring GEMM1 (its form follows the plain GEMM1's: paired SwiGLU
 // tiles of 256 intermediate indices from 384 rows per expert, else 128)
 int ring_tiles_per_chunk(int variant, int R, int E, int I);
+// the ring GEMM1 takes the paired SwiGLU form (as the plain GEMM1: >= 384 rows per expert, I a
+// multiple of 256)
+bool ring_gemm1_paired(int variant, int R, int E, int I);
+// The narrow split-operand GEMMs (GEMM2, dX_g) take two weight tiles per pair tile when the
+// experts average at most 160 rows.
+inline bool narrow_short_rows(int R, int E) { return (long long)R <= 160LL * E; }
+// The persistent ring forward (narrow kernels, k <= 8): after the schedule and the minibatch
+// tables, one cooperative launch gathers the minibatches into the ring and runs GEMM1 + SwiGLU,
+// GEMM2 and the weighted merge (hu, act hi / lo, o and y as the separate launches write them).
+cudaError_t launch_ring_forward(const RingArgs& ra, const void* w13, const void* w2, float* hu, void* act_hi,
+                                void* act_lo, float* o, const float* gates, const int32_t* row_of, int T, void* y,
+                                int* status, int n_sm, cudaStream_t st);
 cudaError_t launch_ring_gemm1(const RingArgs& ra, const void* w13, float* hu, void* act_hi, void* act_lo,
                               int* status, int n_sm, int variant, cudaStream_t st);
 // MXFP8 weights (mx.cu)

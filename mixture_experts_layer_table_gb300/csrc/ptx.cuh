@@ -29,6 +29,11 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The barrier's memory may then serve another purpose (or another barrier).
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");

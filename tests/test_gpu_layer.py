@@ -384,13 +384,21 @@ def test_stuck_wait_times_out_and_context_survives():
     (MID, 300, 2, 3, "single"),  # the row-tile ring kernel (one CTA per 128-row tile), odd comm count
     (MID_SKEW, 700, 2, 4, "pair"),  # the row-tile ring kernel under the CTA-pair flag
     (ODD, 500, 2, 4, 0),        # H and I odd multiples of 128
+    # GEMM2 and the merge in the persistent launch too (every GEMM1 / GEMM2 form pairing)
+    (MID, 300, 2, 4, "persistent"),        # unpaired GEMM1, paired GEMM2 (short rows)
+    (MID_SKEW, 700, 3, 2, "persistent"),   # skewed experts cut at minibatch edges
+    (LONG, 700, 3, 4, "persistent"),       # paired SwiGLU GEMM1, unpaired GEMM2
+    (LONG_SKEW, 1000, 2, 6, "persistent"),
+    (TINY, 96, 2, 2, "persistent"),        # tiny layer, softmax router, top-2
+    (ODD, 500, 2, 4, "persistent"),        # ragged last weight tiles
 ], ids=lambda v: getattr(v, "name", str(v)))
 def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm, flags):
     """The ring forward (persistent launch: gathering CTAs fill ring slots while GEMM CTAs run
     GEMM1 on earlier minibatches; GEMM1 on the narrow-segment CTA-pair kernel by default, on the
     row-tile kernel under the row-tile flags) computes every row exactly as the plain forward does,
     so y, h|u and a must be bitwise equal; the backward after a ring forward must match too."""
-    flags = {0: 0, "single": mok.FLAG_GEMM_SINGLE, "pair": mok.FLAG_GEMM_PAIR}[flags]
+    flags = {0: 0, "single": mok.FLAG_GEMM_SINGLE, "pair": mok.FLAG_GEMM_PAIR,
+             "persistent": mok.FLAG_RING_PERSISTENT}[flags]
     inp = W.make_inputs(shape, seed=0, device="cpu")
     dev = _gpu_inputs(inp)
     plain = mok.MoELayer(mok.desc_from_shape(shape, flags=flags))
@@ -407,6 +415,7 @@ def test_ring_forward_is_bitwise_the_plain_forward(shape, minibatch, slots, comm
         assert torch.equal(y1, y0)
         assert torch.equal(ring.view("hu"), plain.view("hu"))
         assert torch.equal(ring.view("act"), plain.view("act"))
+        assert torch.equal(ring.view("expert_out"), plain.view("expert_out"))
     g1 = ring.backward(dev["dy"], dev["x"], dev["w_router"], dev["w13"], dev["w2"])
     torch.cuda.synchronize()
     assert ring.status() == (0, 0)

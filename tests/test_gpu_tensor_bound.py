@@ -48,17 +48,31 @@ def run(cuda_ok):
     idx_ring = ring.view("topk_idx").cpu().numpy()
     del ring
     torch.cuda.empty_cache()
-    return inp, idx, y_plain, idx_ring, y_ring, table
+    # GEMM2 and the weighted merge in the persistent launch too
+    one = mok.MoELayer(mok.desc_from_shape(SHAPE, minibatch=MINIBATCH, ring_bytes=W.RING_BYTES,
+                                           flags=mok.FLAG_RING_PERSISTENT))
+    y_one = one.forward(inp["x"], inp["w_router"], inp["w13"], inp["w2"])
+    torch.cuda.synchronize()
+    assert one.status() == (0, 0)
+    del one
+    torch.cuda.empty_cache()
+    return inp, idx, y_plain, idx_ring, y_ring, table, y_one
 
 
 def test_ring_forward_is_bitwise_the_plain_forward(run):
-    _, idx, y_plain, idx_ring, y_ring, _ = run
+    _, idx, y_plain, idx_ring, y_ring, _, _ = run
     assert np.array_equal(idx, idx_ring)
     assert torch.equal(y_plain, y_ring)
 
 
+def test_persistent_ring_forward_is_bitwise_the_plain_forward(run):
+    """GEMM2 and the weighted merge in the ring's persistent launch as well."""
+    y_plain, y_persistent = run[2], run[6]
+    assert torch.equal(y_plain, y_persistent)
+
+
 def test_sampled_tokens_against_the_oracle(run):
-    inp, idx, y_plain, _, _, _ = run
+    inp, idx, y_plain, _, _, _, _ = run
     rng = np.random.default_rng(1)
     cand = np.sort(rng.choice(SHAPE.T, size=N_CANDIDATES, replace=False))
     w_r = to_f64(inp["w_router"])
@@ -84,7 +98,7 @@ def test_sampled_tokens_against_the_oracle(run):
 def test_schedule_table_bit_exact(run):
     """The whole schedule table at T=16384 (131,072 assignments), bit-exact against the oracle's
     stable counting sort of the same selection."""
-    _, idx, _, _, _, table = run
+    _, idx, _, _, _, table, _ = run
     ref = O.schedule(idx, SHAPE.E)
     for name in ("counts", "offsets", "row_of", "src_of"):
         assert np.array_equal(table[name], ref[name]), name
@@ -94,7 +108,7 @@ def test_fp16_w2_forward_sampled_tokens(run):
     """The same T=16384 forward with MOK_FLAG_W2_F16 (fp16 copy of W2, a as one fp16 value, one GEMM2
     MMA per K step): the same selection, and the sampled tokens against the oracle on the bf16
     weights at the bf16 bar."""
-    inp, idx, y_plain, _, _, _ = run
+    inp, idx, y_plain, _, _, _, _ = run
     w2_f16 = mok.convert_f16(inp["w2"])
     layer = mok.MoELayer(mok.desc_from_shape(SHAPE, flags=mok.FLAG_W2_F16))
     y = layer.forward(inp["x"], inp["w_router"], inp["w13"], w2_f16)
