@@ -25,12 +25,14 @@ def _lib(cuda_ok):
     mok.load()
 
 
-@pytest.mark.parametrize("shape,ring", [(W.TINY, False), (MID.scaled(name="mid_skew", skew=True), False),
-                                        (MID, True)], ids=lambda v: getattr(v, "name", str(v)))
+@pytest.mark.parametrize("shape,ring", [(W.TINY, None), (MID.scaled(name="mid_skew", skew=True), None),
+                                        (MID, "ring"), (MID, "persistent")],
+                         ids=lambda v: getattr(v, "name", str(v)))
 def test_graph_replay_is_bitwise_the_eager_step(shape, ring):
     inp = W.make_inputs(shape, seed=0, device="cuda")
-    desc = mok.desc_from_shape(shape, minibatch=300, ring_bytes=2 * 300 * shape.H * 2, comm_sms=4) if ring \
-        else mok.desc_from_shape(shape)
+    flags = mok.FLAG_RING_PERSISTENT if ring == "persistent" else 0
+    desc = mok.desc_from_shape(shape, minibatch=300, ring_bytes=2 * 300 * shape.H * 2, comm_sms=4, flags=flags) \
+        if ring else mok.desc_from_shape(shape)
     layer = mok.MoELayer(desc)
     T, H, E, I, k = shape.T, shape.H, shape.E, shape.I, shape.k
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
