@@ -23,10 +23,10 @@
 // 1.34 ms without it).  An expert of at most WG_KSTAT K blocks keeps its stationary
 // blocks for the whole strip; a longer one streams them again for each tile, one block per slot,
 // up to WG_KSTAT blocks ahead of the MMAs.
-// Work items (single tiles of the long experts, then strips of the others; see the item list
-// below) are dealt to the pairs in a fixed order; each output element is one tile's accumulator,
-// reduced over the expert's rows in a fixed order, so results are bitwise those of the single-CTA
-// kernel.
+// Work items (tile pairs of the long experts, then strips of the others; see the item list
+// below) go to whichever pair asks next; each output element is one tile's accumulator, reduced
+// over the expert's rows in a fixed order, so results are bitwise those of the single-CTA kernel
+// whichever pair computes them.
 //
 // The output leaves through TMA stores: an epilogue warp reads 32 columns of its 32 accumulator
 // rows from TMEM, parks them in its 4 KB shared-memory block as 32 output rows of 32 elements
@@ -47,16 +47,20 @@ constexpr int WGP_THREADS = 320;
 // expert's item needs two stages per K block (one per tile), so six keep three K blocks in
 // flight, as many as the stationary ring holds.
 constexpr int WGP_STAGES = 6;  // barriers are laid out for this many
-constexpr int WGP_E_SIX = 297;
+constexpr int WGP_E_SIX = 284;
 __host__ __device__ constexpr int wgp_stages(int E) { return E <= WGP_E_SIX ? 6 : 5; }
 constexpr int WGP_STG = 4096;  // one epilogue warp's staging block (32 x 32 fp32)
-// the barriers, the TMEM address and the abort flag share 256 bytes
-static_assert((2 * WGP_STAGES + 5 + 4 * WG_KSTAT) * 8 + 8 <= 256, "wgrad pair barriers");
+// the barriers, the TMEM address, the abort flag and the item queue (WGP_TQ entries) share
+// WGP_BAR_BYTES
+constexpr int WGP_TQ = 4;
+constexpr int WGP_BAR_BYTES = 336;
+static_assert((2 * WGP_STAGES + 5 + 4 * WG_KSTAT + 2 * WGP_TQ) * 8 + 8 + WGP_TQ * 4 <= WGP_BAR_BYTES,
+              "wgrad pair barriers");
 
 // stationary slots, streaming stages, epilogue staging, alignment, barriers, the row offsets
 // (i32 [E + 1]) and the expert list (u16 [E + 1])
 __host__ __device__ constexpr size_t wgrad_pair_smem_bytes(int E) {
-  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(wgp_stages(E)) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + 256 +
+  return size_t(WG_KSTAT) * WG_STAT_SLOT + size_t(wgp_stages(E)) * WG_STAGE + 8 * size_t(WGP_STG) + 1024 + WGP_BAR_BYTES +
          size_t(E + 1) * 4 + size_t(E + 1) * 2;
 }
 
@@ -73,18 +77,17 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   uint8_t* stg_all = ring + nst * WG_STAGE;               // 8 epilogue warps x WGP_STG
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 8 * WGP_STG);
   // bars: full[S], empty[S], tfull[2], tempty[2], stat_full[K], stat_ready[K], stat_empty[K], drain,
-  // stat_pfull[K] (K = WG_KSTAT)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 4 * WG_KSTAT);
+  // stat_pfull[K] (K = WG_KSTAT), iq_full[Q], iq_empty[Q] (Q = WGP_TQ)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * WGP_STAGES + 5 + 4 * WG_KSTAT + 2 * WGP_TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_off = reinterpret_cast<int*>(stg_all + 8 * WGP_STG + 256);
+  volatile int* iq = reinterpret_cast<volatile int*>(tmem_slot + 2);  // the item queue
+  int* s_off = reinterpret_cast<int*>(stg_all + 8 * WGP_STG + WGP_BAR_BYTES);
   // experts with more than WG_KSTAT K blocks, then the others; [E] = how many are first
   uint16_t* s_list = reinterpret_cast<uint16_t*>(s_off + args.E + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
-  const int pair = (int)blockIdx.x >> 1;
-  const int npairs = (int)gridDim.x >> 1;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[WGP_STAGES + s]); };
   auto tfull_bar = [&](int a) { return smem_u32(&bars[2 * WGP_STAGES + a]); };
@@ -95,6 +98,9 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   const uint32_t drain_bar = smem_u32(&bars[2 * WGP_STAGES + 4 + 3 * WG_KSTAT]);
   // a stationary block loaded by both CTAs onto the even CTA's barrier (no rows to zero)
   auto stat_pfull = [&](int j) { return smem_u32(&bars[2 * WGP_STAGES + 5 + 3 * WG_KSTAT + j]); };
+  // the item queue: full in both CTAs, empty in the even CTA
+  auto iq_full = [&](int q) { return smem_u32(&bars[2 * WGP_STAGES + 5 + 4 * WG_KSTAT + q]); };
+  auto iq_empty = [&](int q) { return smem_u32(&bars[2 * WGP_STAGES + 5 + 4 * WG_KSTAT + WGP_TQ + q]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -110,6 +116,12 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       mbar_init(stat_ready(j), 2);  // warp 1 of both CTAs
       mbar_init(stat_empty(j), 1);
       mbar_init(stat_pfull(j), 1);
+    }
+    for (int q = 0; q < WGP_TQ; ++q) {
+      mbar_init(iq_full(q), 1);
+      // readers: the even CTA's MMA warp and epilogue warps, the odd CTA's producer, warp 1 and
+      // epilogue warps
+      mbar_init(iq_empty(q), 1 + 8 + 1 + 1 + 8);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -162,10 +174,11 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   //  * then one item per strip (expert, 256-wide stationary tile f, all strip_len tiles) of the
   //    other experts, whose stationary blocks stay in shared memory for the whole strip (each
   //    expert's strips in a row, so neighbouring pairs share its streaming rows in L2).
-  // Pair p takes item round * npairs + p in even rounds and round * npairs + npairs - 1 - p in odd
-  // ones: dealt back and forth, so that a pair that drew a costly item in one round draws from the
-  // other end in the next and the pairs' totals even out.  Every role of both CTAs walks the same
-  // list.
+  // The pairs take items in list order from one counter (args.strip_counter): a pair that draws
+  // costly items, or runs on slower SMs, simply takes fewer (a fixed back-and-forth deal held the
+  // whole launch to the slowest pair's share).  The even CTA's producer takes each item and passes
+  // its index to every role of both CTAs through a WGP_TQ-deep queue in shared memory; -1 ends it.
+  // Which pair computes an output tile does not change it.
   const int n_long = s_list[args.E];
   const int pairs_f = (strip_len + 1) / 2;  // two-tile items per strip
   const int tiles_e = per_e * pairs_f;       // two-tile items per long expert
@@ -199,7 +212,39 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     const int kvalid = rows - kb * WG_BK;
     return kvalid < WG_BK && (kvalid & 15) != 0;
   };
-  auto item_at = [&](int round) { return round * npairs + ((round & 1) ? npairs - 1 - pair : pair); };
+  // the q-th item of this pair (-1: no more): taken by the even CTA's producer (one thread) ...
+  auto publish_item = [&](int q, int& n) -> bool {
+    const int qs = q % WGP_TQ;
+    const uint32_t u = (uint32_t)(q / WGP_TQ) & 1u;
+    if (!mbar_wait<true>(iq_empty(qs), u ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs, 32))
+      return false;
+    n = atomicAdd(args.strip_counter, 1);
+    if (n >= total) n = -1;
+    iq[qs] = n;
+    st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&iq[qs])), 1), (uint32_t)n);
+    mbar_arrive(iq_full(qs));
+    mbar_arrive_cluster(mapa_shared(iq_full(qs), 1));  // release: the peer's copy is written
+    return true;
+  };
+  // ... and read by every other role (lane 0 of a warp, or one thread), which counts itself out
+  auto read_item = [&](int q, int& n, uint32_t sleep_ns, bool warp_wide) -> bool {
+    const int qs = q % WGP_TQ;
+    const uint32_t u = (uint32_t)(q / WGP_TQ) & 1u;
+    int w_ok = 1;
+    if (lane == 0 || !warp_wide) {
+      w_ok = mbar_wait<true>(iq_full(qs), u, abort_flag, args.status, SITE_GEMM_MMA_FULL, kWaitLimitNs, sleep_ns);
+      if (w_ok) {
+        n = iq[qs];
+        if (rank == 0) mbar_arrive(iq_empty(qs));
+        else mbar_arrive_cluster(mapa_shared(iq_empty(qs), 0));
+      }
+    }
+    if (warp_wide) {
+      w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+      n = __shfl_sync(0xffffffffu, n, 0);
+    }
+    return w_ok != 0;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
@@ -275,7 +320,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
         }
         return true;
       };
-      for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+      for (int q = 0; ok; ++q) {
+        int n = -1;
+        ok = rank == 0 ? publish_item(q, n) : read_item(q, n, 32, false);
+        if (!ok || n < 0) break;
         int e, f, i0, i1, row0, rows, nkb;
         item(n, e, f, i0, i1, row0, rows, nkb);
         if (nkb == 0) continue;
@@ -434,7 +482,10 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
       if (lane == 0) umma_commit_pair(stat_empty(j), 0x3);  // both CTAs' slots are free once these MMAs end
       __syncwarp();
     };
-    for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+    for (int q = 0; ok; ++q) {
+      int n = -1;
+      ok = read_item(q, n, 32, true);
+      if (!ok || n < 0) break;
       int e, f, i0, i1, row0, rows, nkb;
       item(n, e, f, i0, i1, row0, rows, nkb);
       if (nkb == 0) continue;
@@ -495,7 +546,9 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     uint32_t acc_phase = 0;
     int tcount = 0;  // tiles with MMAs seen so far (both groups count all of them)
     bool ok = true;
-    for (int round = 0, n = pair; n < total && ok; n = item_at(++round)) {
+    for (int q = 0; ok; ++q) {
+      int n = -1;
+      if (!read_item(q, n, 256, true) || n < 0) break;
       int e, f, i0, i1, row0, rows, nkb;
       item(n, e, f, i0, i1, row0, rows, nkb);
       for (int i = i0; i < i1; ++i) {
