@@ -107,7 +107,9 @@ cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_
     return cudaErrorInvalidValue;
   const int bound = ((R + NMAX - 1) / NMAX + args.E) * C::m_tiles(args);
   if (R <= 0 || bound <= 0) return cudaSuccess;
-  auto kern = gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI>;
+  // tiles from a counter when the launch has one (args.ticket, zero at launch), else a fixed deal
+  auto kern = args.ticket != nullptr ? gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI, NARROW_PLAIN_TICKET>
+                                     : gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI, NARROW_PLAIN>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
@@ -121,17 +123,18 @@ cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_pairs[64] = {0};  // co-resident pairs of this kernel, per device
+  static int max_pairs[2][64] = {};  // co-resident pairs of each kernel, per device
   int dev = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_pairs[dev] == 0) {
+  int& mp = max_pairs[args.ticket != nullptr][dev];
+  if (mp == 0) {
     cfg.gridDim = dim3(2 * std::max(1, n_sm / 2), 1, 1);
     int clusters = 0;
     if ((err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return err;
-    max_pairs[dev] = std::max(1, clusters);
+    mp = std::max(1, clusters);
   }
-  cfg.gridDim = dim3(2 * std::min(bound, max_pairs[dev]), 1, 1);
+  cfg.gridDim = dim3(2 * std::min(bound, mp), 1, 1);
   err = cudaLaunchKernelEx(&cfg, kern, w, tx, tx2, txs, tx2s, args);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
@@ -174,6 +177,7 @@ cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, 
     g.out2 = act_lo;
     g.ld1 = I;
     g.a_f16 = a_f16 ? 1 : 0;
+    g.ticket = work_counter(status, CNT_GEMM1);
     if (paired) return launch_narrow<false, false, 256, EPI_SWIGLU_PAIRED>(tw, x_g, nullptr, H, g, R, n_sm, st);
     // at most 160 rows per expert on average: 192-row chunks (7 stages instead of 6; 1% faster at
     // 128 rows per expert)
@@ -220,6 +224,7 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
     g.K = I;
     g.out0 = out;
     g.ld0 = H;
+    g.ticket = work_counter(status, CNT_GEMM2);
     if (f16) {
       // fp16 a (one value, 11 significant bits) against an fp16 copy of W2: one MMA per K step
       // (the TMA copies are bitwise: the bf16 maps serve any 16-bit element)
@@ -287,6 +292,7 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
     g.K = 2 * I;
     g.out0 = dx_g;
     g.ld0 = H;
+    g.ticket = work_counter(status, CNT_DGRAD_X);
     if (dhu_lo == nullptr) return launch_narrow<true, false, 256>(tw, dhu_hi, nullptr, 2 * I, g, R, n_sm, st);
     if (narrow_short_rows(R, E))
       return launch_narrow<true, true, 256, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
@@ -452,7 +458,7 @@ cudaError_t launch_ring_gemm1_narrow(const RingArgs& ra, const void* w13, float*
   g.x = reinterpret_cast<const __nv_bfloat16*>(ra.x);
   g.src_of = ra.src_of;
   g.ring = reinterpret_cast<__nv_bfloat16*>(ra.ring);
-  auto kern = gemm_narrow_kernel<false, false, RING_NARROW_NMAX, EPI, true>;
+  auto kern = gemm_narrow_kernel<false, false, RING_NARROW_NMAX, EPI, NARROW_RING_GEMM1>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
   if (err != cudaSuccess) return err;
   // gathering and GEMM CTAs wait on each other: the launch is cooperative (all CTAs resident at

@@ -105,10 +105,12 @@ struct NarrowCfg {
 // barrier in both CTAs and an empty barrier in the even CTA); -1 ends the queue.  Which pair
 // computes a tile does not change its result: each output element is still one tile's
 // accumulator over K in a fixed order.
-// MODE of narrow_body: the fixed deal over the whole layer, the ring forward's GEMM1 (tiles from
-// a ticket, each minibatch's rows awaited in the token ring) or, in the persistent ring forward,
+// MODE of narrow_body: the fixed deal over the whole layer (pair p takes tiles p, p + npairs, ...),
+// the same tiles taken from a counter through the tile queue (NARROW_PLAIN_TICKET: a pair whose
+// SMs run slower, or whose tiles cost more, takes fewer), the ring forward's GEMM1 (tiles from a
+// ticket, each minibatch's rows awaited in the token ring) or, in the persistent ring forward,
 // its GEMM2 (tiles from a second ticket, each minibatch's rows of a awaited from GEMM1).
-constexpr int NARROW_PLAIN = 0, NARROW_RING_GEMM1 = 1, NARROW_RING_GEMM2 = 2;
+constexpr int NARROW_PLAIN = 0, NARROW_RING_GEMM1 = 1, NARROW_RING_GEMM2 = 2, NARROW_PLAIN_TICKET = 3;
 constexpr uint32_t kTmemOwn = 0xffffffffu;  // narrow_body allocates (and frees) its own TMEM
 
 // One narrow-segment grouped GEMM on the CTA pairs of the launch.  `smem` is the CTA's 1024-byte
@@ -120,13 +122,14 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
                                             const CUtensorMap& tmXs, const CUtensorMap& tmX2s,
                                             const GemmArgs& args, uint8_t* smem, uint32_t tmem_given) {
   using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
-  constexpr bool RING = MODE != NARROW_PLAIN;
+  constexpr bool RING = MODE == NARROW_RING_GEMM1 || MODE == NARROW_RING_GEMM2;
+  constexpr bool QUEUE = MODE != NARROW_PLAIN;  // tiles from args.ticket through the tile queue
   constexpr int STAGES = C::STAGES;
   constexpr int STAGE_BYTES = C::STAGE_BYTES;
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // C::XBUF_BYTES
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, tq_full[TQ], tq_empty[TQ], then
-  // the TMEM address and the abort flag; at +512 the tile queue's entries (RING)
+  // the TMEM address and the abort flag; at +512 the tile queue's entries (QUEUE)
   constexpr int TQ = NARROW_TQ;
   static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= 512 && 512 + TQ * NARROW_QE * 4 <= NARROW_BAR_BYTES,
                 "barriers, TMEM address, abort flag and tile queue");
@@ -139,7 +142,7 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
-  const int pair = (int)blockIdx.x >> 1;  // the fixed deal (not RING)
+  const int pair = (int)blockIdx.x >> 1;  // the fixed deal (not QUEUE)
   const int npairs = (int)gridDim.x >> 1;
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
@@ -221,19 +224,19 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
     return t;
   };
 
-  // RING: the n-th tile of this pair, from the tile queue (g = -1: no more).  The even CTA's
-  // producer (one thread) takes each tile from the ticket counter, decodes it once (the minibatch
-  // tables are in global memory: a binary search over the minibatches and one over the experts)
-  // and writes the decoded tile into entry n % TQ of both CTAs' queues, one tile ahead of its own
-  // loads; every other reader waits for the entry, reads it and counts itself out on the even
-  // CTA's empty barrier of the entry.
-  auto publish_tile = [&](int n, int& g, NarrowTile& t, int& mb, int& rr) -> bool {
+  // QUEUE: the n-th tile of this pair, from the tile queue (g = -1: no more).  The even CTA's
+  // producer (one thread) takes each tile from the ticket counter (g_taken: the atomic is issued a
+  // few K blocks before the tile is published, so that its round trip overlaps the loads), decodes
+  // it once (the minibatch tables are in global memory: a binary search over the minibatches and
+  // one over the experts) and writes the decoded tile into entry n % TQ of both CTAs' queues, one
+  // tile ahead of its own loads; every other reader waits for the entry, reads it and counts
+  // itself out on the even CTA's empty barrier of the entry.
+  auto publish_tile = [&](int n, int g_taken, int& g, NarrowTile& t, int& mb, int& rr) -> bool {
     const int q = n % TQ;
     const uint32_t u = (uint32_t)(n / TQ) & 1u;
     if (!mbar_wait<true>(tq_empty(q), u ^ 1, abort_flag, args.status, SITE_RING_WAIT, kWaitLimitNs, 32))
       return false;
-    g = atomicAdd(args.ticket, 1);
-    if (g >= total) g = -1;
+    g = g_taken < total ? g_taken : -1;
     if (g >= 0) t = decode(g, mb, rr);
     const int v[10] = {g, t.e, t.c, t.m, t.nc, t.row0, t.rows, t.n, mb, rr};
     volatile int* dst = tq + q * NARROW_QE;
@@ -297,18 +300,18 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
       int issued = 0;
       bool ok = true;
       int ring_ready = -1;  // RING: last minibatch known to be ready (gathered, or through GEMM1)
-      // RING, even CTA: the tile after the current one is taken during the current one's loads
+      // QUEUE, even CTA: the tile after the current one is taken during the current one's loads
       int g_nx = 0, mb_nx = 0, rr_nx = 0;
       NarrowTile t_nx{};
       bool have_nx = false;
-      if (RING && rank == 0) {
-        ok = publish_tile(0, g_nx, t_nx, mb_nx, rr_nx);
+      if (QUEUE && rank == 0) {
+        ok = publish_tile(0, atomicAdd(args.ticket, 1), g_nx, t_nx, mb_nx, rr_nx);
         have_nx = true;
       }
       for (int n = 0; ok; ++n) {
         int g, mb = 0, ring_row0 = 0;
         NarrowTile t{};
-        if (!RING) {
+        if (!QUEUE) {
           g = pair + n * npairs;
           if (g >= total) break;
           t = decode(g, mb, ring_row0);
@@ -349,9 +352,11 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
         const uint32_t pair_tx = 2u * (C::A_BYTES + C::X_OPS * xrows * 128);
         const uint64_t pol_w = t.nc > 1 ? pol_shared : pol_once;
         const int kb_pub = nkb - 1 < STAGES ? nkb - 1 : STAGES;  // the stage ring is full by then
+        int g_taken = 0;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (RING && rank == 0 && !have_nx && kb == kb_pub) {
-            if (!publish_tile(n + 1, g_nx, t_nx, mb_nx, rr_nx)) {
+          if (QUEUE && rank == 0 && !have_nx && kb == 0) g_taken = atomicAdd(args.ticket, 1);
+          if (QUEUE && rank == 0 && !have_nx && kb == kb_pub) {
+            if (!publish_tile(n + 1, g_taken, g_nx, t_nx, mb_nx, rr_nx)) {
               ok = false;
               break;
             }
@@ -444,7 +449,7 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
       for (int n = 0; ok; ++n) {
         int g, mb_unused = 0, rr_unused = 0;
         NarrowTile t{};
-        if (RING) {
+        if (QUEUE) {
           if (!read_tile(n, g, t, mb_unused, rr_unused, 32, true)) {
             ok = false;
             break;
@@ -527,7 +532,7 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
     for (int n = 0;; ++n) {
       int g, mb = 0, rr_unused = 0;
       NarrowTile t{};
-      if (RING) {
+      if (QUEUE) {
         if (!read_tile(n, g, t, mb, rr_unused, 256, true)) break;
       } else {
         g = pair + n * npairs;
@@ -702,7 +707,7 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
   }
 }
 
-template <bool WMN, bool SPLIT, int NMAX, int EPI, bool RING = false>
+template <bool WMN, bool SPLIT, int NMAX, int EPI, int KMODE = NARROW_PLAIN>
 __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
     gemm_narrow_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmXs,
@@ -710,7 +715,7 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
   using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if (RING) {
+  if (KMODE == NARROW_RING_GEMM1) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XBUF_BYTES);
     ring_gather_first(args);
     if ((int)blockIdx.x < args.comm_ctas) {
@@ -718,8 +723,7 @@ __global__ void __launch_bounds__(NarrowCfg<WMN, SPLIT, NMAX, EPI>::THREADS, 1)
       ring_gather_retire(args, C::STAGES * C::STAGE_BYTES, bars);  // then this pair runs tiles as well
     }
   }
-  narrow_body<WMN, SPLIT, NMAX, EPI, RING ? NARROW_RING_GEMM1 : NARROW_PLAIN>(tmW, tmX, tmX2, tmXs, tmX2s, args, smem,
-                                                                              kTmemOwn);
+  narrow_body<WMN, SPLIT, NMAX, EPI, KMODE>(tmW, tmX, tmX2, tmXs, tmX2s, args, smem, kTmemOwn);
 }
 
 // ------------------------------------------------------------------ persistent ring forward

@@ -78,7 +78,10 @@ cudaError_t launch_wgrad(const void* a_hi, const void* a_lo, int M, const void* 
 // int STATUS_COUNTERS on.
 constexpr int STATUS_BYTES = 256;
 constexpr int STATUS_COUNTERS = 16;
-enum WorkCounter { CNT_WGRAD_W2 = 0, CNT_WGRAD_W13 = 1 };
+enum WorkCounter { CNT_WGRAD_W2 = 0, CNT_WGRAD_W13 = 1, CNT_GEMM1 = 2, CNT_GEMM2 = 3, CNT_DGRAD_X = 4 };
+// The narrow-segment GEMMs (variant GEMM_NARROW of GEMM1, GEMM2 and dX_g) take their tiles from the
+// work counter of their kind in the status region that `status` points to.
+inline int* work_counter(int* status, WorkCounter c) { return status + STATUS_COUNTERS + (int)c; }
 // Ring forward GEMM1: comm_ctas CTAs gather minibatches into the ring, the rest run GEMM1
 // (SwiGLU epilogue, rows written at their global position).  Cooperative launch, grid = n_sm.
 struct RingArgs {
