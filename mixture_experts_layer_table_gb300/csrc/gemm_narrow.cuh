@@ -28,8 +28,9 @@
 // the bytes of both CTAs), empty[s] and tfull[a] in both CTAs (multicast commits), tempty[a] in
 // the even CTA (8 arrivals).  Tiles (expert e, weight tile m of 256 columns, row chunk c; c
 // fastest, then m, so the pairs running one expert at the same time share its rows and each
-// weight tile in L2) are dealt to the pairs round-robin in a fixed order; every output element
-// is one tile's accumulator, reduced over K in a fixed order.
+// weight tile in L2) are taken by the pairs in that order from one counter (or, without a
+// counter, dealt round-robin); every output element is one tile's accumulator, reduced over K in
+// a fixed order, whichever pair computes it.
 #pragma once
 #include "combine.cuh"
 #include "gemm.cuh"
