@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   const int MT = args.M / 256, NT = args.N / 256;
   const int per_e = STAT_A ? MT : NT;   // strips per expert
   const int strip_len = STAT_A ? NT : MT;
-  // Work items, dealt to the pairs in one fixed order:
-  //  * first, one item per two neighbouring output tiles (i, i + 1) of one stationary strip f of
+  // Work items, in two lists:
+  //  * one item per two neighbouring output tiles (i, i + 1) of one stationary strip f of
   //    each expert with more than WG_KSTAT K blocks of rows (expert by expert, in s_list order).
   //    Their stationary blocks are streamed again for every item, so the pairs spread over the
   //    items of one expert at a time and share its rows in L2 (one pair per strip of 28 tiles, as
@@ -171,14 +171,18 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   //    accumulate at once, one in each TMEM accumulator, so each stationary block that arrives
   //    feeds twice the MMAs (the epilogue of an item then no longer overlaps its MMAs; at 16
   //    experts of 1024 rows dW13 2.59 -> 2.02 ms, 1.34 us per K block of a pair tile);
-  //  * then one item per strip (expert, 256-wide stationary tile f, all strip_len tiles) of the
+  //  * one item per strip (expert, 256-wide stationary tile f, all strip_len tiles) of the
   //    other experts, whose stationary blocks stay in shared memory for the whole strip (each
   //    expert's strips in a row, so neighbouring pairs share its streaming rows in L2).
-  // The pairs take items in list order from one counter (args.strip_counter): a pair that draws
-  // costly items, or runs on slower SMs, simply takes fewer (a fixed back-and-forth deal held the
-  // whole launch to the slowest pair's share).  The even CTA's producer takes each item and passes
-  // its index to every role of both CTAs through a WGP_TQ-deep queue in shared memory; -1 ends it.
-  // Which pair computes an output tile does not change it.
+  // The two lists are merged with the long experts' items spread evenly among the strips, each
+  // list in its own order: the long experts' items are bound by their MMAs, the strips by their
+  // output stores, so pairs running both kinds at once keep the tensor cores and HBM busy together
+  // (the long items all first: skewed DSV3 layer dW13 5.99 ms, merged 5.74).  The pairs take
+  // positions of the merged list in order from one counter (args.strip_counter): a pair that
+  // draws costly items, or runs on slower SMs, simply takes fewer (a fixed back-and-forth deal
+  // held the whole launch to the slowest pair's share).  The even CTA's producer takes each item
+  // and passes its index to every role of both CTAs through a WGP_TQ-deep queue in shared memory;
+  // -1 ends it.  Which pair computes an output tile does not change it.
   const int n_long = s_list[args.E];
   const int pairs_f = (strip_len + 1) / 2;  // two-tile items per strip
   const int tiles_e = per_e * pairs_f;       // two-tile items per long expert
@@ -218,8 +222,15 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     const uint32_t u = (uint32_t)(q / WGP_TQ) & 1u;
     if (!mbar_wait<true>(iq_empty(qs), u ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs, 32))
       return false;
-    n = atomicAdd(args.strip_counter, 1);
-    if (n >= total) n = -1;
+    const int pos = atomicAdd(args.strip_counter, 1);
+    if (pos >= total) {
+      n = -1;
+    } else {
+      // position pos of the merged list: the long experts' items spread evenly among the strips
+      const long long nl0 = (long long)pos * n_tile_items / total;
+      const long long nl1 = (long long)(pos + 1) * n_tile_items / total;
+      n = nl1 > nl0 ? (int)nl0 : n_tile_items + (pos - (int)nl0);
+    }
     iq[qs] = n;
     st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&iq[qs])), 1), (uint32_t)n);
     mbar_arrive(iq_full(qs));
