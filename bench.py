@@ -988,6 +988,28 @@ def tensor_bound_forward(shp, x, w_router, w13, w2, steps, warmup, flags=0):
         # at the maximum clock): how close the kernels come at the clock the power cap allowed
         scale = clocks["sm_mhz"] / peaks["sm_max_mhz"]
         grouped["frac_bf16_peak_clock_normalised"] = round(g_tf / (peaks["bf16_tflops"] * scale), 4)
+    # Timed alone, as the burst peak was (the best of 10 single GEMMs): the best of 5 single
+    # forwards, each after half a second of idle (the power cap lets the clocks recover), GEMM1 +
+    # GEMM2 of that forward from the per-kernel trace, against the burst peak.
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    best = None
+    for _ in range(5):
+        time.sleep(0.5)
+        N.trace_start(32)
+        layer.forward(x, w_router, w13, w2, y=y)
+        torch.cuda.synchronize()
+        tr = N.trace_stop()
+        g = sum(tr[n]["total_ms"] / tr[n]["launches"] for n in fwd_gemm)
+        best = g if best is None else min(best, g)
+    bclocks = sampler.stop()
+    if layer.status() != (0, 0):
+        raise RuntimeError("device status set")
+    b_tf = sum(kf[n] for n in fwd_gemm) / (best * 1e-3) / 1e12
+    grouped["burst"] = {"ms": round(best, 4), "tflops": round(b_tf, 1),
+                        "frac_bf16_peak": round(b_tf / peaks["bf16_tflops"], 4), "peak": peaks["bf16_tflops"],
+                        "what": "best of 5 single forwards, each after 0.5 s idle (the burst peak is the best "
+                                "of 10 single GEMMs)", "clocks": bclocks}
     return ms, kernels, grouped, layer, y
 
 
