@@ -97,7 +97,8 @@ template <bool WMN, bool SPLIT, int NMAX, int EPI = EPI_F32>
 cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_lo, int K, GemmArgs args, int R,
                           int n_sm, cudaStream_t st) {
   using C = NarrowCfg<WMN, SPLIT, NMAX, EPI>;
-  static_assert(C::smem_bytes(1024) <= 232448, "shared memory budget");
+  static_assert(C::smem_bytes(C::kDeep ? NARROW_DEEP_MAX_E : 1024) <= 232448, "shared memory budget");
+  if (C::kDeep && args.E > NARROW_DEEP_MAX_E) return cudaErrorInvalidValue;
   CUtensorMap tx, tx2, txs, tx2s;
   if (!tmap_2d(&tx, x_hi, K, R, BK, NARROW_XBOX) || !tmap_2d(&txs, x_hi, K, R, BK, NARROW_XBOX_S))
     return cudaErrorInvalidValue;
@@ -110,7 +111,8 @@ cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_
   // tiles from a counter when the launch has one (args.ticket, zero at launch), else a fixed deal
   auto kern = args.ticket != nullptr ? gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI, NARROW_PLAIN_TICKET>
                                      : gemm_narrow_kernel<WMN, SPLIT, NMAX, EPI, NARROW_PLAIN>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem_bytes(1024));
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::smem_bytes(C::kDeep ? NARROW_DEEP_MAX_E : 1024));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[1];
@@ -233,6 +235,8 @@ cudaError_t launch_gemm2(const void* act_hi, const void* act_lo, const void* w2,
         return launch_narrow<false, false, 256, EPI_F32_PAIRED>(tw, act_hi, nullptr, I, g, R, n_sm, st);
       return launch_narrow<false, false, 256>(tw, act_hi, nullptr, I, g, R, n_sm, st);
     }
+    if (narrow_deep(R, E))
+      return launch_narrow<false, true, 192, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
     if (narrow_short_rows(R, E))
       return launch_narrow<false, true, 256, EPI_F32_PAIRED>(tw, act_hi, act_lo, I, g, R, n_sm, st);
     return launch_narrow<false, true, 256>(tw, act_hi, act_lo, I, g, R, n_sm, st);
@@ -294,6 +298,8 @@ cudaError_t launch_dgrad_x(const void* dhu_hi, const void* dhu_lo, const void* w
     g.ld0 = H;
     g.ticket = work_counter(status, CNT_DGRAD_X);
     if (dhu_lo == nullptr) return launch_narrow<true, false, 256>(tw, dhu_hi, nullptr, 2 * I, g, R, n_sm, st);
+    if (narrow_deep(R, E))
+      return launch_narrow<true, true, 192, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
     if (narrow_short_rows(R, E))
       return launch_narrow<true, true, 256, EPI_F32_PAIRED>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);
     return launch_narrow<true, true, 256>(tw, dhu_hi, dhu_lo, 2 * I, g, R, n_sm, st);

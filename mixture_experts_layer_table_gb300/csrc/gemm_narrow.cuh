@@ -32,6 +32,8 @@
 // counter, dealt round-robin); every output element is one tile's accumulator, reduced over K in
 // a fixed order, whichever pair computes it.
 #pragma once
+#include <type_traits>
+
 #include "combine.cuh"
 #include "gemm.cuh"
 #include "narrow_tiles.h"
@@ -39,10 +41,14 @@
 namespace mok {
 
 // Shared memory after the stages and the SwiGLU exchange buffer: barriers, TMEM address, abort
-// flag and (ring forward) the tile queue: NARROW_TQ entries of NARROW_QE ints.
+// flag and the tile queue: NARROW_TQ entries of NARROW_QE ints at byte NARROW_QOFF (the deep
+// form below packs them tighter).
 constexpr int NARROW_BAR_BYTES = 1024;
 constexpr int NARROW_TQ = 8;
 constexpr int NARROW_QE = 12;
+constexpr int NARROW_QOFF = 512;
+// Experts the deep form's 16-bit chunk prefixes and smem budget allow.
+constexpr int NARROW_DEEP_MAX_E = 256;
 
 template <bool WMN, bool SPLIT, int NMAX_, int EPI = EPI_F32>
 struct NarrowCfg {
@@ -64,7 +70,16 @@ struct NarrowCfg {
   static constexpr int A_BYTES = (kPaired ? 2 : 1) * 128 * BK * 2;
   static constexpr int X_OPS = SPLIT ? 2 : 1;
   static constexpr int STAGE_BYTES = A_BYTES + X_OPS * X_OP;
-  static constexpr int STAGES = (208 * 1024 / STAGE_BYTES) < 8 ? (208 * 1024 / STAGE_BYTES) : 8;
+  // The deep form: the paired split-operand GEMMs (GEMM2, dX_g) in 192-row chunks take a fourth
+  // 56 KB stage (measured at the DSV3 layer, 128 rows per expert: GEMM2 1.556 -> 1.473 ms, dX_g
+  // 2.749 -> 2.717 ms), which fits beside the alignment pad only with a 4-entry tile queue packed
+  // after the barriers and 16-bit chunk prefixes, for at most NARROW_DEEP_MAX_E experts.
+  static constexpr bool kDeep = EPI == EPI_F32_PAIRED && SPLIT && NMAX == 192;
+  static constexpr int STAGES = kDeep ? 4 : (208 * 1024 / STAGE_BYTES) < 8 ? (208 * 1024 / STAGE_BYTES) : 8;
+  static constexpr int TQ = kDeep ? 4 : NARROW_TQ;
+  static constexpr int QOFF = kDeep ? 192 : NARROW_QOFF;
+  static constexpr int BAR_BYTES = kDeep ? 384 : NARROW_BAR_BYTES;
+  using coff_t = typename std::conditional<kDeep, uint16_t, int>::type;
   // two accumulators of NMAX columns (paired: one of 256 + NMAX); tcgen05.alloc takes a power of
   // two from 32 to 512
   static constexpr int TMEM_COLS = (kPaired || 2 * NMAX > 256) ? 512 : 256;
@@ -85,8 +100,10 @@ struct NarrowCfg {
            : EPI == EPI_F32_PAIRED ? (a.N + 2 * PM - 1) / (2 * PM)
                                    : (a.N + PM - 1) / PM;
   }
+  // stages, exchange buffer, alignment pad, barriers, row offsets (i32 [E + 1]), chunk prefixes
   static __host__ __device__ constexpr size_t smem_bytes(int E) {
-    return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + NARROW_BAR_BYTES + size_t(2) * (E + 1) * 4;
+    return size_t(STAGES) * STAGE_BYTES + XBUF_BYTES + 1024 /*align*/ + BAR_BYTES + size_t(E + 1) * 4 +
+           ((size_t(E + 1) * sizeof(coff_t) + 3) & ~size_t(3));
   }
 };
 
@@ -130,15 +147,15 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
   float* xbuf = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);  // C::XBUF_BYTES
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES);
   // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, tq_full[TQ], tq_empty[TQ], then
-  // the TMEM address and the abort flag; at +512 the tile queue's entries (QUEUE)
-  constexpr int TQ = NARROW_TQ;
-  static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= 512 && 512 + TQ * NARROW_QE * 4 <= NARROW_BAR_BYTES,
+  // the TMEM address and the abort flag; at +C::QOFF the tile queue's entries (QUEUE)
+  constexpr int TQ = C::TQ;
+  static_assert((2 * STAGES + 5 + 2 * TQ) * 8 + 8 <= C::QOFF && C::QOFF + TQ * NARROW_QE * 4 <= C::BAR_BYTES,
                 "barriers, TMEM address, abort flag and tile queue");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * TQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* tq = reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(bars) + 512);
-  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + NARROW_BAR_BYTES);
-  int* s_coff = s_off + (args.E + 1);
+  volatile int* tq = reinterpret_cast<volatile int*>(reinterpret_cast<uint8_t*>(bars) + C::QOFF);
+  int* s_off = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + C::XBUF_BYTES + C::BAR_BYTES);
+  typename C::coff_t* s_coff = reinterpret_cast<typename C::coff_t*>(s_off + (args.E + 1));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -179,10 +196,10 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
   if (!RING && threadIdx.x == 0) {
     int acc = 0;
     for (int e = 0; e < args.E; ++e) {
-      s_coff[e] = acc;
+      s_coff[e] = (typename C::coff_t)acc;
       acc += (s_off[e + 1] - s_off[e] + C::NMAX - 1) / C::NMAX;
     }
-    s_coff[args.E] = acc;
+    s_coff[args.E] = (typename C::coff_t)acc;
   }
   if (warp == 1 && tmem_given == kTmemOwn) {
     tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -200,7 +217,7 @@ __device__ __forceinline__ void narrow_body(const CUtensorMap& tmW, const CUtens
   auto tiles_before = [&](int mb) {
     return MODE == NARROW_RING_GEMM2 ? args.mb_start[mb] / args.mb_tiles1 * MT : args.mb_start[mb];
   };
-  const int total = RING ? tiles_before(args.n_mb) : s_coff[args.E] * MT;
+  const int total = RING ? tiles_before(args.n_mb) : (int)s_coff[args.E] * MT;
   const int nkb = args.K / BK;
   // Tile g.  RING: the minibatch mb holding it, the tile decoded inside it, its rows' position in the
   // ring (ring_row0) and its rows' position in the outputs (t.row0, all rows of the layer).
@@ -752,11 +769,12 @@ template <int EPI1, int EPI2>
 struct RingFwdCfg {
   using C1 = NarrowCfg<false, false, 256, EPI1>;
   using C2 = NarrowCfg<false, true, 256, EPI2>;
+  static_assert(!C1::kDeep && !C2::kDeep, "the phases share the standard barrier layout");
   static constexpr int THREADS = C1::THREADS > C2::THREADS ? C1::THREADS : C2::THREADS;
   // bytes each phase uses past the 1024-byte aligned base (stages, exchange buffer, barriers,
   // segment tables); the TMEM address follows the larger
   static __host__ __device__ constexpr int phase_end(int stages, int stage_bytes, int xbuf, int E) {
-    return stages * stage_bytes + xbuf + NARROW_BAR_BYTES + 2 * (E + 1) * 4;
+    return stages * stage_bytes + xbuf + NARROW_BAR_BYTES + 2 * (E + 1) * 4;  // C1, C2: not the deep form
   }
   static __host__ __device__ constexpr int tmem_slot_offset(int E) {
     return phase_end(C1::STAGES, C1::STAGE_BYTES, C1::XBUF_BYTES, E) >

@@ -112,6 +112,11 @@ bool ring_gemm1_paired(int variant, int R, int E, int I);
 // The narrow split-operand GEMMs (GEMM2, dX_g) take two weight tiles per pair tile when the
 // experts average at most 160 rows.
 inline bool narrow_short_rows(int R, int E) { return (long long)R <= 160LL * E; }
+// Of those, the paired GEMM2 / dX_g take the deep form (192-row chunks, four stages) when the
+// 16-bit chunk prefixes and the shared-memory budget allow it: at most 256 experts.
+inline bool narrow_deep(int R, int E) {
+  return narrow_short_rows(R, E) && E <= 256 && (long long)R / 192 + E < 65535;
+}
 // The persistent ring forward (narrow kernels, k <= 8): after the schedule and the minibatch
 // tables, one cooperative launch gathers the minibatches into the ring and runs GEMM1 + SwiGLU,
 // GEMM2 and the weighted merge (hu, act hi / lo, o and y as the separate launches write them).

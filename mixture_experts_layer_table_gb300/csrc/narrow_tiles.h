@@ -52,17 +52,18 @@ MOK_HD int narrow_chunk(int cnt, int nc, int nmax) {
 // Expert e owns tiles [s_coff[e]*MT, s_coff[e+1]*MT) with s_coff the prefix of ceil(rows/nmax);
 // inside an expert the chunks of one weight tile are neighbours, so the pairs that run them at
 // the same time read that weight tile from HBM once.
-MOK_HD NarrowTile decode_narrow_tile(int g, int MT, int E, int nmax, const int* s_off, const int* s_coff) {
+template <typename CoffT>
+MOK_HD NarrowTile decode_narrow_tile(int g, int MT, int E, int nmax, const int* s_off, const CoffT* s_coff) {
   int lo = 0, hi = E;  // largest e with s_coff[e]*MT <= g (the last of equal starts owns tiles)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (s_coff[mid] * MT <= g) lo = mid; else hi = mid;
+    if ((int)s_coff[mid] * MT <= g) lo = mid; else hi = mid;
   }
   NarrowTile t;
   t.e = lo;
-  const int nc = s_coff[lo + 1] - s_coff[lo];
+  const int nc = (int)s_coff[lo + 1] - (int)s_coff[lo];
   const int cnt = s_off[lo + 1] - s_off[lo];
-  const int local = g - s_coff[lo] * MT;
+  const int local = g - (int)s_coff[lo] * MT;
   t.nc = nc;
   t.m = local / nc;
   t.c = local - t.m * nc;
