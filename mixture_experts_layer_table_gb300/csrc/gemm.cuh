@@ -157,7 +157,11 @@ struct GemmCfg {
                                    : (kTmaEpi || EPI == EPI_SWIGLU_BWD) ? 4 * 4096
                                                                         : 0;
   static constexpr int RING = (MODE == MODE_WGRAD) ? 3 * STAGE_BYTES : SMEM_RING;
-  static constexpr int STAGES = (RING / STAGE_BYTES) < 4 ? (RING / STAGE_BYTES) : 4;
+  // the router GEMM (MODE_DENSE, 64-column tiles of 24 KB stages) walks its whole K = H per tile:
+  // more stages in flight keep its loads' latency covered (at most 8: the barriers' 256 bytes)
+  static constexpr int MAX_STAGES = MODE == MODE_DENSE ? 8 : 4;
+  static constexpr int STAGES = (RING / STAGE_BYTES) < MAX_STAGES ? (RING / STAGE_BYTES) : MAX_STAGES;
+  static_assert((2 * STAGES + 5) * 8 + 8 <= 256, "barriers, TMEM address and abort flag");
   static constexpr int RINGS_BYTES = STAGES * STAGE_BYTES;
   static constexpr int ACC_COLS = BN;
   static constexpr int TMEM_COLS = 2 * BN;

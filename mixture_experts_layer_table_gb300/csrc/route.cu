@@ -20,16 +20,18 @@ constexpr int kMaxK = 16;
 // Selection score = score + bias (bias nullable); the k best are taken best-first, ties
 // to the lower expert index.  Gates = scores at the selected experts, renormalised over
 // the k when requested, times route_scale.
+// C: experts per lane (32 * C >= E), so that the scans run over the chunks that exist.
+template <int C>
 __global__ void topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias,
                             const int32_t* __restrict__ given, int T, int E, int k, int router,
                             int renorm, float route_scale, int32_t* __restrict__ topk_idx,
                             float* __restrict__ gates, float* __restrict__ scores_out,
                             int* status) {
+  static_assert(C >= 1 && 32 * C <= kMaxE, "experts per lane");
   const int warps = blockDim.x >> 5;
   const int t = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
-  constexpr int C = kMaxE / 32;
   float s[C];
   // logits == nullptr: the selection must be given; gates are then not produced
   const float* lrow = logits != nullptr ? logits + (size_t)t * E : nullptr;
@@ -619,8 +621,17 @@ cudaError_t launch_topk(const float* logits, const float* bias, const int32_t* g
                         int k, int router, int renorm, float route_scale, int32_t* topk_idx,
                         float* gates, float* scores, int* status, cudaStream_t st) {
   const int warps = 8;
-  topk_kernel<<<(T + warps - 1) / warps, warps * 32, 0, st>>>(logits, bias, given, T, E, k, router, renorm,
-                                                              route_scale, topk_idx, gates, scores, status);
+  const dim3 grid((T + warps - 1) / warps), block(warps * 32);
+#define MOK_TOPK(CC)                                                                                          \
+  topk_kernel<CC><<<grid, block, 0, st>>>(logits, bias, given, T, E, k, router, renorm, route_scale, topk_idx, \
+                                          gates, scores, status)
+  if (E <= 32) MOK_TOPK(1);
+  else if (E <= 64) MOK_TOPK(2);
+  else if (E <= 128) MOK_TOPK(4);
+  else if (E <= 256) MOK_TOPK(8);
+  else if (E <= 512) MOK_TOPK(16);
+  else MOK_TOPK(32);
+#undef MOK_TOPK
   return cudaGetLastError();
 }
 
