@@ -39,6 +39,7 @@
 // make room for the eight 4 KB blocks.
 #pragma once
 #include "wgrad.cuh"
+#include "wgrad_items.h"
 
 namespace mok {
 
@@ -183,28 +184,13 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
   // held the whole launch to the slowest pair's share).  The even CTA's producer takes each item
   // and passes its index to every role of both CTAs through a WGP_TQ-deep queue in shared memory;
   // -1 ends it.  Which pair computes an output tile does not change it.
-  const int n_long = s_list[args.E];
-  const int pairs_f = (strip_len + 1) / 2;  // two-tile items per strip
-  const int tiles_e = per_e * pairs_f;       // two-tile items per long expert
-  const int n_tile_items = n_long * tiles_e;
-  const int total = n_tile_items + (args.E - n_long) * per_e;
+  const WgpItems wi = wgp_items(per_e, strip_len, s_list[args.E], args.E);
+  const int total = wi.total;
   // item -> expert e, stationary strip f, tiles [i0, i1) along the strip, its rows
   auto item = [&](int n, int& e, int& f, int& i0, int& i1, int& row0, int& rows, int& nkb) {
-    if (n < n_tile_items) {
-      const int le = n / tiles_e;
-      const int local = n - le * tiles_e;
-      e = s_list[le];
-      f = local / pairs_f;
-      i0 = 2 * (local - f * pairs_f);
-      i1 = min(i0 + 2, strip_len);
-    } else {
-      const int b = n - n_tile_items;
-      const int se = b / per_e;
-      e = s_list[n_long + se];
-      f = b - se * per_e;
-      i0 = 0;
-      i1 = strip_len;
-    }
+    int le;
+    wgp_item(wi, n, le, f, i0, i1);
+    e = s_list[le];
     row0 = s_off[e];
     rows = s_off[e + 1] - row0;
     nkb = (rows + WG_BK - 1) / WG_BK;
@@ -223,14 +209,7 @@ __global__ void __launch_bounds__(WGP_THREADS, 1)
     if (!mbar_wait<true>(iq_empty(qs), u ^ 1, abort_flag, args.status, SITE_GEMM_PRODUCER_EMPTY, kWaitLimitNs, 32))
       return false;
     const int pos = atomicAdd(args.strip_counter, 1);
-    if (pos >= total) {
-      n = -1;
-    } else {
-      // position pos of the merged list: the long experts' items spread evenly among the strips
-      const long long nl0 = (long long)pos * n_tile_items / total;
-      const long long nl1 = (long long)(pos + 1) * n_tile_items / total;
-      n = nl1 > nl0 ? (int)nl0 : n_tile_items + (pos - (int)nl0);
-    }
+    n = pos < total ? wgp_item_at(wi, pos) : -1;  // the long experts' items spread among the strips
     iq[qs] = n;
     st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&iq[qs])), 1), (uint32_t)n);
     mbar_arrive(iq_full(qs));
