@@ -146,21 +146,25 @@ cudaError_t launch_narrow(const CUtensorMap& w, const void* x_hi, const void* x_
 
 cudaError_t launch_router_gemm(const void* x, const void* w_router, int T, int H, int E, float* logits,
                                int* status, int n_sm, cudaStream_t st) {
-  // 128 x 64 tiles: a skinny GEMM (E = 256 columns, K = H) whose 128 x 256 tiles occupied one SM in
-  // five at T = 4096 and ran at the fill rate of those (56 us); 64-column tiles spread it over four
-  // times the SMs, each A tile then read four times (from L2)
-  constexpr int RBN = 64;
-  CUtensorMap ta, tb;
-  if (!tmap_2d(&ta, x, H, T, BK, BM) || !tmap_2d(&tb, w_router, H, E, BK, RBN)) return cudaErrorInvalidValue;
+  // A skinny GEMM (E columns, K = H).  With few token tiles (T = 4096: 32 tiles of 128 x 256 on
+  // one SM in five, 56 us) 128 x 64 tiles spread it over four times the SMs, each A tile then read
+  // four times (from L2: 47 us); with enough tiles for half the SMs the 128 x 256 tiles stay (at
+  // T = 16384 the four reads of 235 MB of x no longer fit L2: 0.07 -> 0.18 ms)
   GemmArgs g = base_args(1, nullptr, nullptr, status);
   g.M = T;
   g.N = E;
   g.K = H;
   g.out0 = logits;
   g.ld0 = E;
-  const int tiles = ((T + BM - 1) / BM) * ((E + RBN - 1) / RBN);
+  const int mt = (T + BM - 1) / BM;
+  const bool narrow = mt * ((E + 255) / 256) < n_sm / 2;
+  const int bn = narrow ? 64 : 256;
+  CUtensorMap ta, tb;
+  if (!tmap_2d(&ta, x, H, T, BK, BM) || !tmap_2d(&tb, w_router, H, E, BK, bn)) return cudaErrorInvalidValue;
+  const int tiles = mt * ((E + bn - 1) / bn);
   g.total_tiles = tiles;
-  return launch<MODE_DENSE, EPI_F32, SPLIT_NONE, RBN>(ta, ta, tb, tb, g, std::min(tiles, n_sm), st);
+  if (narrow) return launch<MODE_DENSE, EPI_F32, SPLIT_NONE, 64>(ta, ta, tb, tb, g, std::min(tiles, n_sm), st);
+  return launch<MODE_DENSE, EPI_F32, SPLIT_NONE, 256>(ta, ta, tb, tb, g, std::min(tiles, n_sm), st);
 }
 
 cudaError_t launch_gemm1_swiglu(const void* x_g, const void* w13, int R, int H, int I, int E,
