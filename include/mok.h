@@ -29,6 +29,11 @@
  *   - Outputs are overwritten, never accumulated.  Results are bitwise reproducible for
  *     the same inputs, descriptor and device: every reduction runs in a fixed order and
  *     no floating-point atomics are used.
+ *   - One call at a time per `ws`: calls that may overlap on the GPU (different streams)
+ *     need a `ws` each.  Besides the temporaries, `ws` holds the status word and the work
+ *     counters from which the expert GEMMs and weight-gradient kernels take their tiles
+ *     (cleared by each call); two overlapping calls on one `ws` would share them and skip
+ *     tiles.
  *   - No C++ exception crosses this boundary.  No global mutable state besides per-device
  *     caches of the SM count and of how many CTA pairs of each pair kernel fit at once, the
  *     driver entry point used to encode TMA descriptors, the optional per-kernel trace
