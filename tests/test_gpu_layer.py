@@ -115,6 +115,33 @@ def test_router_topk_and_gates(shape):
     assert np.allclose(layer.view("scores").cpu().numpy(), scores, rtol=2e-5, atol=1e-7)
 
 
+# expert counts that take the top-k kernel's other per-lane widths (2, 4 and 16 experts per lane)
+ROUTER_WIDTHS = [
+    W.MoEShape("router_T200_H256_E48_I256_top6_softmax", T=200, H=256, E=48, I=256, k=6,
+               router=W.ROUTER_SOFTMAX, renorm=False, x_std=1.0, w_std=0.05),
+    W.MoEShape("router_T200_H256_E96_I256_top8_sigmoid", T=200, H=256, E=96, I=256, k=8,
+               router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.05),
+    W.MoEShape("router_T200_H256_E300_I256_top8_sigmoid", T=200, H=256, E=300, I=256, k=8,
+               router=W.ROUTER_SIGMOID, renorm=True, x_std=1.0, w_std=0.05),
+]
+
+
+@pytest.mark.parametrize("shape", ROUTER_WIDTHS, ids=lambda s: s.name)
+def test_router_topk_at_other_expert_counts(shape):
+    """The selection is a valid top-k of the oracle's scores (near-ties within the margin may
+    break either way), and the gates, scores and logits match the oracle on it."""
+    inp = W.make_inputs(shape, seed=0, device="cpu")
+    f64 = inputs_f64(inp)
+    logits, scores = O.router_scores(f64["x"], f64["w_router"], shape.router)
+    layer, _, _ = _run(shape, inp)
+    gidx = layer.view("topk_idx").cpu().numpy()
+    selection_is_valid(scores, gidx, shape.k)
+    ref_g = O.gate_values(scores, gidx, shape.renorm)
+    assert np.allclose(layer.view("gates").cpu().numpy(), ref_g, rtol=2e-5, atol=1e-7)
+    assert np.allclose(layer.view("logits").cpu().numpy(), logits, rtol=1e-4, atol=1e-5)
+    assert np.allclose(layer.view("scores").cpu().numpy(), scores, rtol=2e-5, atol=1e-7)
+
+
 # ----------------------------------------------------------------------------- forward / backward
 
 LONG = W.MoEShape("long_T1500_H512_E8_I768_top4_sigmoid", T=1500, H=512, E=8, I=768, k=4,
